@@ -1,0 +1,129 @@
+"""ctypes binding of libmoe.so: argument marshalling only.
+
+Every function here hands raw device pointers (from torch tensors) and sizes to
+the C entry points declared in include/moe.h; all arithmetic of the layer runs
+in the library's CUDA kernels.  There is no fallback: if libmoe.so is missing or
+cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK = 0
+ERRORS = {-1: "MOE_ERR_INVALID", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA"}
+STATUS_CAPACITY, STATUS_TIMEOUT, STATUS_BAD_INDEX = 1, 2, 4
+GEMM_GATEUP_SWIGLU, GEMM_DOWN = 0, 1
+FMT_FP8, FMT_BF16 = 0, 1
+
+_c_int, _c_i64, _c_sz, _vp, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+
+
+class RouteCfg(ctypes.Structure):
+    _fields_ = [("B", _c_int), ("H", _c_int), ("N", _c_int), ("K", _c_int),
+                ("n_group", _c_int), ("topk_group", _c_int), ("score_fn", _c_int),
+                ("renorm", _c_int), ("route_scale", _f)]
+
+
+class DispatchCfg(ctypes.Structure):
+    _fields_ = [("B", _c_int), ("H", _c_int), ("K", _c_int), ("N_log", _c_int),
+                ("N_phys", _c_int), ("layout", _c_int), ("cap", _c_int), ("fmt", _c_int)]
+
+
+class GemmArgs(ctypes.Structure):
+    _fields_ = [("op", _c_int), ("n", _c_int), ("k", _c_int), ("rows", _c_i64),
+                ("max_tiles", _c_i64), ("num_experts", _c_int), ("A", _vp), ("A_sf", _vp),
+                ("W", _vp), ("W_sf", _vp), ("phys2log", _vp), ("tiles", _vp), ("out", _vp),
+                ("out_sf", _vp), ("signal", _vp), ("block_m_signal", _c_int),
+                ("num_sms", _c_int), ("status", _vp)]
+
+
+class CombineCfg(ctypes.Structure):
+    _fields_ = [("B", _c_int), ("H", _c_int), ("K", _c_int), ("signal", _vp),
+                ("threshold", _c_int), ("block_m_signal", _c_int), ("timeout_ns", _c_i64),
+                ("num_ctas", _c_int)]
+
+
+class Layer(ctypes.Structure):
+    _fields_ = [("route", RouteCfg), ("N_phys", _c_int), ("layout", _c_int), ("cap", _c_int),
+                ("I", _c_int), ("has_shared", _c_int), ("sbo", _c_int),
+                ("block_m_signal", _c_int), ("rows", _c_i64), ("max_tiles", _c_i64),
+                ("timeout_ns", _c_i64), ("num_sms", _c_int), ("combine_ctas", _c_int)] + [
+        (n, _vp) for n in (
+            "x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
+            "W2_sf", "W13s", "W13s_sf", "W2s", "W2s_sf", "topk_idx", "topk_w",
+            "expert_counts", "counts", "row_of", "tiles", "shared_tiles", "signal", "A",
+            "A_sf", "H1", "H1_sf", "Y", "As", "As_sf", "Hs", "Hs_sf", "S", "out", "route_ws",
+            "dispatch_ws")] + [("route_ws_bytes", _c_sz), ("dispatch_ws_bytes", _c_sz),
+                               ("status", _vp), ("stream2", _vp)]
+
+
+#: Every symbol include/moe.h declares, with (restype, argtypes).
+SIGNATURES = {
+    "moe_route_workspace_size": (_c_sz, [ctypes.POINTER(RouteCfg)]),
+    "moe_route": (_c_int, [ctypes.POINTER(RouteCfg), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_sz, _vp]),
+    "eplb_build_map": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_dispatch_rows": (_c_i64, [ctypes.POINTER(DispatchCfg)]),
+    "moe_dispatch_max_tiles": (_c_i64, [ctypes.POINTER(DispatchCfg)]),
+    "moe_dispatch_workspace_size": (_c_sz, [ctypes.POINTER(DispatchCfg)]),
+    "moe_dispatch": (_c_int, [ctypes.POINTER(DispatchCfg)] + [_vp] * 13 + [_c_sz, _vp, _vp]),
+    "moe_grouped_gemm_fp8": (_c_int, [ctypes.POINTER(GemmArgs), _vp]),
+    "moe_packed_scale_bytes": (_c_sz, [_c_int, _c_int, _c_int]),
+    "moe_pack_weight_scales": (_c_int, [_c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_combine": (_c_int, [ctypes.POINTER(CombineCfg), _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_read_status": (_c_int, [_vp, _vp]),
+    "moe_last_cuda_error": (_c_int, []),
+    "moe_num_sms": (_c_int, []),
+    "moe_layer_forward": (_c_int, [ctypes.POINTER(Layer), _vp]),
+    "moe_layer_forward_host": (_c_int, [ctypes.POINTER(Layer), _vp, _vp, _vp]),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so (built by ``combine_moe_route_03_gb300.build``); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libmoe.so not found at {path}: build it with "
+                               "`python -m combine_moe_route_03_gb300.build` (no fallback path)")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+class MoEError(RuntimeError):
+    pass
+
+
+def check(rc: int, what: str) -> None:
+    if rc != MOE_OK:
+        extra = ""
+        if rc == -3:
+            extra = f" (cudaError {load().moe_last_cuda_error()})"
+        raise MoEError(f"{what} failed: {ERRORS.get(rc, rc)}{extra}")
+
+
+def ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        if t.is_cuda and not t.is_contiguous():
+            raise ValueError("tensors passed to libmoe must be contiguous")
+        return t.data_ptr()
+    return int(t)
+
+
+def stream_ptr(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream

@@ -1,0 +1,267 @@
+"""Python face of libmoe: same names as the C entry points, torch tensors in and out.
+
+Only marshalling happens here (shape checks, output allocation through torch,
+pointer passing); each step of the layer runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import (FMT_BF16, FMT_FP8, GEMM_DOWN, GEMM_GATEUP_SWIGLU, CombineCfg, DispatchCfg,
+                   GemmArgs, Layer, RouteCfg, check, load, ptr, stream_ptr)
+from .configs import MASKED, MoEConfig
+
+__all__ = ["route", "eplb_build_map", "dispatch", "dispatch_sizes", "pack_weight_scales",
+           "grouped_gemm_fp8", "combine", "read_status", "new_status", "MoELayer",
+           "FMT_FP8", "FMT_BF16", "GEMM_GATEUP_SWIGLU", "GEMM_DOWN", "num_sms"]
+
+
+def num_sms() -> int:
+    return load().moe_num_sms()
+
+
+def new_status(device="cuda") -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def read_status(status: torch.Tensor) -> int:
+    v = ctypes.c_int32(0)
+    check(load().moe_read_status(ptr(status), ctypes.addressof(v)), "moe_read_status")
+    return int(v.value)
+
+
+def _route_cfg(cfg: MoEConfig, B: int | None = None) -> RouteCfg:
+    return RouteCfg(cfg.B if B is None else B, cfg.H, cfg.N, cfg.K, cfg.n_group, cfg.topk_group,
+                    cfg.score_fn, cfg.renorm, cfg.route_scale)
+
+
+def route(cfg: MoEConfig, x: torch.Tensor, W: torch.Tensor, bias: torch.Tensor | None,
+          stream=None, counts: bool = True) -> dict:
+    """moe_route: x bf16 [B][H], W fp32 [N][H], bias fp32 [N] -> topk_idx, topk_w, counts."""
+    B = x.shape[0]
+    rc = _route_cfg(cfg, B)
+    dev = x.device
+    idx = torch.empty((B, cfg.K), dtype=torch.int32, device=dev)
+    w = torch.empty((B, cfg.K), dtype=torch.float32, device=dev)
+    cnt = torch.empty(cfg.N, dtype=torch.int32, device=dev) if counts else None
+    L = load()
+    ws = torch.empty(max(1, L.moe_route_workspace_size(ctypes.byref(rc))), dtype=torch.uint8,
+                     device=dev)
+    check(L.moe_route(ctypes.byref(rc), ptr(x), ptr(W), ptr(bias), ptr(idx), ptr(w), ptr(cnt),
+                      ptr(ws), ws.numel(), stream_ptr(stream)), "moe_route")
+    return dict(topk_idx=idx, topk_w=w, counts=cnt, logits=ws)
+
+
+def eplb_build_map(counts: np.ndarray, N_log: int, N_phys: int):
+    """Host EPLB map -> (log2phys [N_log][2], rep [N_log], phys2log [N_phys]) int32 numpy."""
+    c = np.ascontiguousarray(counts, dtype=np.int64)
+    l2p = np.empty((N_log, 2), np.int32)
+    rep = np.empty(N_log, np.int32)
+    p2l = np.empty(N_phys, np.int32)
+    check(load().eplb_build_map(c.ctypes.data, N_log, N_phys, l2p.ctypes.data, rep.ctypes.data,
+                                p2l.ctypes.data), "eplb_build_map")
+    return l2p, rep, p2l
+
+
+def _dispatch_cfg(cfg: MoEConfig, B: int, fmt: int, cap: int | None = None) -> DispatchCfg:
+    return DispatchCfg(B, cfg.H, cfg.K, cfg.N, cfg.N_phys, cfg.layout,
+                       cfg.cap if cap is None else cap, fmt)
+
+
+def dispatch_sizes(cfg: MoEConfig, B: int | None = None, fmt: int = FMT_FP8,
+                   cap: int | None = None) -> dict:
+    dc = _dispatch_cfg(cfg, cfg.B if B is None else B, fmt, cap)
+    L = load()
+    return dict(rows=L.moe_dispatch_rows(ctypes.byref(dc)),
+                max_tiles=L.moe_dispatch_max_tiles(ctypes.byref(dc)),
+                ws=L.moe_dispatch_workspace_size(ctypes.byref(dc)))
+
+
+def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=None, rep=None,
+             fmt: int = FMT_FP8, shared: bool = False, status: torch.Tensor | None = None,
+             cap: int | None = None, stream=None, out: dict | None = None) -> dict:
+    """moe_dispatch -> A, A_sf, counts, row_of, src_of, tiles (+ shared copy)."""
+    B, H = x.shape
+    dev = x.device
+    dc = _dispatch_cfg(cfg, B, fmt, cap)
+    sz = dispatch_sizes(cfg, B, fmt, cap)
+    rows, mt = sz["rows"], sz["max_tiles"]
+    if rows <= 0:
+        raise ValueError("unsupported dispatch configuration")
+    o = out if out is not None else {}
+    if "A" not in o:
+        o["A"] = torch.empty((rows, H * (2 if fmt == FMT_BF16 else 1)), dtype=torch.uint8, device=dev)
+        o["A_sf"] = torch.empty(rows * (H // 128) * 4, dtype=torch.uint8, device=dev)
+        o["counts"] = torch.empty(cfg.N_phys, dtype=torch.int32, device=dev)
+        o["row_of"] = torch.empty((B, cfg.K), dtype=torch.int32, device=dev)
+        o["src_of"] = torch.empty(rows, dtype=torch.int32, device=dev)
+        o["tiles"] = torch.empty(8 + 8 * mt, dtype=torch.int32, device=dev)
+        o["ws"] = torch.empty(max(1, sz["ws"]), dtype=torch.uint8, device=dev)
+        if shared:
+            srows = (B + 127) // 128 * 128
+            o["As"] = torch.empty((srows, H), dtype=torch.uint8, device=dev)
+            o["As_sf"] = torch.empty(srows * (H // 128) * 4, dtype=torch.uint8, device=dev)
+            o["shared_tiles"] = torch.empty(8 + 8 * (srows // 128), dtype=torch.int32, device=dev)
+    st = status if status is not None else new_status(dev)
+    check(load().moe_dispatch(ctypes.byref(dc), ptr(x), ptr(topk_idx), ptr(log2phys), ptr(rep),
+                              ptr(o["A"]), ptr(o["A_sf"]), ptr(o["counts"]), ptr(o["row_of"]),
+                              ptr(o.get("src_of")), ptr(o["tiles"]), ptr(o.get("As")),
+                              ptr(o.get("As_sf")), ptr(o.get("shared_tiles")), ptr(o["ws"]),
+                              o["ws"].numel(), ptr(st), stream_ptr(stream)), "moe_dispatch")
+    o.update(rows=rows, max_tiles=mt, status=st)
+    return o
+
+
+def pack_weight_scales(W_sf: torch.Tensor, stream=None) -> torch.Tensor:
+    """UE8M0 bytes [E][n/128][k/128] (device) -> SF atoms [E][n/128][k/128][512]."""
+    E, nb, kb = W_sf.shape
+    L = load()
+    nbytes = L.moe_packed_scale_bytes(E, nb * 128, kb * 128)
+    out = torch.empty(nbytes, dtype=torch.uint8, device=W_sf.device)
+    check(L.moe_pack_weight_scales(E, nb * 128, kb * 128, ptr(W_sf), ptr(out),
+                                   stream_ptr(stream)), "moe_pack_weight_scales")
+    return out
+
+
+def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tensor,
+                     W_sf_atoms: torch.Tensor, tiles: torch.Tensor, max_tiles: int,
+                     out: torch.Tensor | None = None, out_sf: torch.Tensor | None = None,
+                     phys2log: torch.Tensor | None = None, signal: torch.Tensor | None = None,
+                     block_m_signal: int = 64, num_sms_: int = 0,
+                     status: torch.Tensor | None = None, stream=None):
+    """moe_grouped_gemm_fp8.  W e4m3 [E][n][k]; A e4m3 [rows][k]."""
+    E, n, k = W.shape
+    rows = A.shape[0]
+    dev = A.device
+    if op == GEMM_GATEUP_SWIGLU:
+        I = n // 2
+        if out is None:
+            out = torch.empty((rows, I), dtype=torch.uint8, device=dev)
+            out_sf = torch.empty(rows * (I // 128) * 4, dtype=torch.uint8, device=dev)
+    elif out is None:
+        out = torch.empty((rows, n), dtype=torch.bfloat16, device=dev)
+    st = status if status is not None else new_status(dev)
+    g = GemmArgs(op, n, k, rows, max_tiles, E, ptr(A), ptr(A_sf), ptr(W), ptr(W_sf_atoms),
+                 ptr(phys2log), ptr(tiles), ptr(out), ptr(out_sf), ptr(signal), block_m_signal,
+                 num_sms_, ptr(st))
+    check(load().moe_grouped_gemm_fp8(ctypes.byref(g), stream_ptr(stream)), "moe_grouped_gemm_fp8")
+    return (out, out_sf) if op == GEMM_GATEUP_SWIGLU else out
+
+
+def combine(Y: torch.Tensor, row_of: torch.Tensor, topk_w: torch.Tensor,
+            shared: torch.Tensor | None = None, out: torch.Tensor | None = None,
+            signal: torch.Tensor | None = None, threshold: int = 0, block_m_signal: int = 64,
+            timeout_ns: int = 1_000_000_000, num_ctas: int = 0,
+            status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """moe_combine: Y bf16 [rows][H] -> out bf16 [B][H]."""
+    B, K = row_of.shape
+    H = Y.shape[1] if Y.dtype == torch.bfloat16 else Y.shape[1] // 2
+    if out is None:
+        out = torch.empty((B, H), dtype=torch.bfloat16, device=Y.device)
+    cc = CombineCfg(B, H, K, ptr(signal), threshold, block_m_signal, timeout_ns, num_ctas)
+    st = status if status is not None else new_status(Y.device)
+    check(load().moe_combine(ctypes.byref(cc), ptr(Y), ptr(row_of), ptr(topk_w), ptr(shared),
+                             ptr(out), ptr(st), stream_ptr(stream)), "moe_combine")
+    return out
+
+
+class MoELayer:
+    """All device buffers of one MoE layer plus the moe_layer_forward chain.
+
+    ``weights``: dict of device uint8 tensors W13 [N][2I][H], W13_sf [N][2I/128][H/128],
+    W2 [N][H][I], W2_sf [N][H/128][I/128] (raw UE8M0 bytes; packed here once), and
+    for a shared expert W13s/W13s_sf/W2s/W2s_sf ([1][...] or unbatched).
+    """
+
+    def __init__(self, cfg: MoEConfig, W_router: torch.Tensor, bias: torch.Tensor | None,
+                 weights: dict, eplb_map=None, num_sms_: int = 0, combine_ctas: int = 16,
+                 timeout_ns: int = 1_000_000_000, device="cuda"):
+        self.cfg = cfg
+        dev = torch.device(device)
+        B, H, I, K = cfg.B, cfg.H, cfg.I, cfg.K
+        L = load()
+        self.keep = []
+        t = lambda *s, dtype=torch.uint8: torch.empty(s, dtype=dtype, device=dev)  # noqa: E731
+        self.x = t(B, H, dtype=torch.bfloat16)
+        self.W_router, self.bias = W_router, bias
+        self.W13, self.W2 = weights["W13"], weights["W2"]
+        self.W13_sf = pack_weight_scales(weights["W13_sf"])
+        self.W2_sf = pack_weight_scales(weights["W2_sf"])
+        self.has_shared = cfg.shared
+        if cfg.shared:
+            self.W13s = weights["W13s"].reshape(1, 2 * I, H)
+            self.W2s = weights["W2s"].reshape(1, H, I)
+            self.W13s_sf = pack_weight_scales(weights["W13s_sf"].reshape(1, 2 * I // 128, H // 128))
+            self.W2s_sf = pack_weight_scales(weights["W2s_sf"].reshape(1, H // 128, I // 128))
+        self.log2phys = self.rep = self.phys2log = None
+        if eplb_map is not None:
+            l2p, rep, p2l = eplb_map
+            self.log2phys = torch.from_numpy(np.ascontiguousarray(l2p)).to(dev)
+            self.rep = torch.from_numpy(np.ascontiguousarray(rep)).to(dev)
+            self.phys2log = torch.from_numpy(np.ascontiguousarray(p2l)).to(dev)
+        sz = dispatch_sizes(cfg)
+        self.rows, self.max_tiles = sz["rows"], sz["max_tiles"]
+        rows = self.rows
+        self.topk_idx = t(B, K, dtype=torch.int32)
+        self.topk_w = t(B, K, dtype=torch.float32)
+        self.expert_counts = t(cfg.N, dtype=torch.int32)
+        self.counts = t(cfg.N_phys, dtype=torch.int32)
+        self.row_of = t(B, K, dtype=torch.int32)
+        self.tiles = t(8 + 8 * self.max_tiles, dtype=torch.int32)
+        self.A = t(rows, H)
+        self.A_sf = t(rows * (H // 128) * 4)
+        self.H1 = t(rows, I)
+        self.H1_sf = t(rows * (I // 128) * 4)
+        self.Y = t(rows, H, dtype=torch.bfloat16)
+        srows = (B + 127) // 128 * 128
+        if cfg.shared:
+            self.As, self.As_sf = t(srows, H), t(srows * (H // 128) * 4)
+            self.Hs, self.Hs_sf = t(srows, I), t(srows * (I // 128) * 4)
+            self.S = t(srows, H, dtype=torch.bfloat16)
+            self.shared_tiles = t(8 + 8 * (srows // 128), dtype=torch.int32)
+        self.signal = t(rows // cfg.block_m_signal, dtype=torch.int32) if cfg.sbo else None
+        self.out = t(B, H, dtype=torch.bfloat16)
+        rcfg = _route_cfg(cfg)
+        self.route_ws = t(max(1, L.moe_route_workspace_size(ctypes.byref(rcfg))))
+        self.dispatch_ws = t(max(1, sz["ws"]))
+        self.status = new_status(dev)
+        self.stream2 = torch.cuda.Stream(device=dev) if cfg.sbo else None
+        lay = Layer()
+        lay.route = rcfg
+        lay.N_phys, lay.layout, lay.cap, lay.I = cfg.N_phys, cfg.layout, cfg.cap, I
+        lay.has_shared, lay.sbo, lay.block_m_signal = int(cfg.shared), int(cfg.sbo), cfg.block_m_signal
+        lay.rows, lay.max_tiles, lay.timeout_ns = rows, self.max_tiles, timeout_ns
+        sms = num_sms_ or num_sms()
+        lay.num_sms = sms - combine_ctas if cfg.sbo else sms
+        lay.combine_ctas = combine_ctas
+        names = ["x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
+                 "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",
+                 "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws", "dispatch_ws",
+                 "status"]
+        if cfg.shared:
+            names += ["W13s", "W13s_sf", "W2s", "W2s_sf", "As", "As_sf", "Hs", "Hs_sf", "S",
+                      "shared_tiles"]
+        for n in names:
+            setattr(lay, n, ptr(getattr(self, n)))
+        lay.route_ws_bytes = self.route_ws.numel()
+        lay.dispatch_ws_bytes = self.dispatch_ws.numel()
+        lay.stream2 = self.stream2.cuda_stream if self.stream2 is not None else None
+        self.layer = lay
+
+    def forward(self, x: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Runs the layer on self.x (copied from ``x`` first when given)."""
+        if x is not None:
+            self.x.copy_(x)
+        check(load().moe_layer_forward(ctypes.byref(self.layer), stream_ptr(stream)),
+              "moe_layer_forward")
+        return self.out
+
+    def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> None:
+        """x from (pinned) host memory, out back to host memory, through the C ABI."""
+        check(load().moe_layer_forward_host(ctypes.byref(self.layer), ptr(x_host),
+                                            ptr(out_host), stream_ptr(stream)),
+              "moe_layer_forward_host")

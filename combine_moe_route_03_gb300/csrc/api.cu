@@ -1,0 +1,199 @@
+// Host-side entry points of libmoe: error and status reporting, the EPLB map
+// builder, and the whole-layer chain.
+#include <algorithm>
+#include <atomic>
+#include <vector>
+
+#include "common.cuh"
+
+namespace moe {
+
+static std::atomic<int> g_last_cuda_error{0};
+
+int set_cuda_error(cudaError_t e) {
+  g_last_cuda_error.store((int)e);
+  return MOE_ERR_CUDA;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+extern "C" int moe_num_sms(void) { return device_sm_count(); }
+
+extern "C" int moe_read_status(const int32_t *status, int32_t *host_status) {
+  if (!status || !host_status) return MOE_ERR_INVALID;
+  cudaError_t e = cudaMemcpy(host_status, status, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+}
+
+// Redundant-expert placement: one replica for each of the N_phys - N_log most
+// loaded logical experts ("Large-scale EP ...", §EPLB: 256 logical experts in 288
+// physical slots, popular experts in several places, each copy taking a share).
+extern "C" int eplb_build_map(const int64_t *counts_host, int N_log, int N_phys,
+                              int32_t *log2phys, int32_t *rep, int32_t *phys2log) {
+  if (!counts_host || !log2phys || !rep || !phys2log || N_log <= 0) return MOE_ERR_INVALID;
+  const int extra = N_phys - N_log;
+  if (extra < 0 || extra > N_log) return MOE_ERR_INVALID;
+  std::vector<int> order(N_log);
+  for (int e = 0; e < N_log; ++e) order[e] = e;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return counts_host[a] > counts_host[b]; });
+  for (int e = 0; e < N_log; ++e) {
+    log2phys[2 * e] = e;
+    log2phys[2 * e + 1] = e;
+    rep[e] = 1;
+    phys2log[e] = e;
+  }
+  for (int i = 0; i < extra; ++i) {
+    const int e = order[i];
+    log2phys[2 * e + 1] = N_log + i;
+    rep[e] = 2;
+    phys2log[N_log + i] = e;
+  }
+  return MOE_OK;
+}
+
+namespace {
+
+cudaEvent_t layer_event(int i) {
+  static cudaEvent_t ev[2] = {nullptr, nullptr};
+  if (!ev[i]) cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+  return ev[i];
+}
+
+}  // namespace
+
+extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
+  if (!L) return MOE_ERR_INVALID;
+  const moe_route_cfg &rc = L->route;
+  int rc_ = moe_route(&rc, L->x, L->W_router, L->bias, L->topk_idx, L->topk_w, L->expert_counts,
+                      L->route_ws, L->route_ws_bytes, stream);
+  if (rc_) return rc_;
+  moe_dispatch_cfg dc;
+  dc.B = rc.B;
+  dc.H = rc.H;
+  dc.K = rc.K;
+  dc.N_log = rc.N;
+  dc.N_phys = L->N_phys;
+  dc.layout = L->layout;
+  dc.cap = L->cap;
+  dc.fmt = MOE_FMT_FP8;
+  rc_ = moe_dispatch(&dc, L->x, L->topk_idx, L->log2phys, L->rep, L->A, L->A_sf, L->counts,
+                     L->row_of, nullptr, L->tiles, L->has_shared ? L->As : nullptr,
+                     L->has_shared ? L->As_sf : nullptr,
+                     L->has_shared ? L->shared_tiles : nullptr, L->dispatch_ws,
+                     L->dispatch_ws_bytes, L->status, stream);
+  if (rc_) return rc_;
+  const int64_t srows = ((int64_t)rc.B + 127) / 128 * 128;
+  if (L->has_shared) {
+    moe_gemm_args g{};
+    g.op = MOE_GEMM_GATEUP_SWIGLU;
+    g.n = 2 * L->I;
+    g.k = rc.H;
+    g.rows = srows;
+    g.max_tiles = srows / 128;
+    g.num_experts = 1;
+    g.A = L->As;
+    g.A_sf = L->As_sf;
+    g.W = L->W13s;
+    g.W_sf = L->W13s_sf;
+    g.tiles = L->shared_tiles;
+    g.out = L->Hs;
+    g.out_sf = L->Hs_sf;
+    g.num_sms = L->num_sms;
+    g.status = L->status;
+    if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+    g.op = MOE_GEMM_DOWN;
+    g.n = rc.H;
+    g.k = L->I;
+    g.A = L->Hs;
+    g.A_sf = L->Hs_sf;
+    g.W = L->W2s;
+    g.W_sf = L->W2s_sf;
+    g.out = L->S;
+    g.out_sf = nullptr;
+    if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+  }
+  moe_gemm_args g{};
+  g.op = MOE_GEMM_GATEUP_SWIGLU;
+  g.n = 2 * L->I;
+  g.k = rc.H;
+  g.rows = L->rows;
+  g.max_tiles = L->max_tiles;
+  g.num_experts = rc.N;
+  g.A = L->A;
+  g.A_sf = L->A_sf;
+  g.W = L->W13;
+  g.W_sf = L->W13_sf;
+  g.phys2log = L->phys2log;
+  g.tiles = L->tiles;
+  g.out = L->H1;
+  g.out_sf = L->H1_sf;
+  g.num_sms = L->num_sms;
+  g.status = L->status;
+  if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+  g.op = MOE_GEMM_DOWN;
+  g.n = rc.H;
+  g.k = L->I;
+  g.A = L->H1;
+  g.A_sf = L->H1_sf;
+  g.W = L->W2;
+  g.W_sf = L->W2_sf;
+  g.out = L->Y;
+  g.out_sf = nullptr;
+  moe_combine_cfg cc{};
+  cc.B = rc.B;
+  cc.H = rc.H;
+  cc.K = rc.K;
+  cudaStream_t st = as_stream(stream);
+  if (L->sbo) {
+    if (!L->signal || !L->stream2 || L->stream2 == stream || L->block_m_signal <= 0)
+      return MOE_ERR_INVALID;
+    const size_t nsig = (size_t)(L->rows / L->block_m_signal);
+    cudaError_t e = cudaMemsetAsync(L->signal, 0, nsig * sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaEventRecord(layer_event(0), st);
+    cudaStream_t st2 = as_stream(L->stream2);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st2, layer_event(0), 0);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    g.signal = L->signal;
+    g.block_m_signal = L->block_m_signal;
+    if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+    cc.signal = L->signal;
+    cc.threshold = rc.H / 256;
+    cc.block_m_signal = L->block_m_signal;
+    cc.timeout_ns = L->timeout_ns > 0 ? L->timeout_ns : 1000000000ll;
+    cc.num_ctas = L->combine_ctas;
+    if ((rc_ = moe_combine(&cc, L->Y, L->row_of, L->topk_w, L->has_shared ? L->S : nullptr,
+                           L->out, L->status, L->stream2)))
+      return rc_;
+    e = cudaEventRecord(layer_event(1), st2);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, layer_event(1), 0);
+    return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+  }
+  if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+  return moe_combine(&cc, L->Y, L->row_of, L->topk_w, L->has_shared ? L->S : nullptr, L->out,
+                     L->status, stream);
+}
+
+extern "C" int moe_layer_forward_host(const moe_layer *L, const void *x_host, void *out_host,
+                                      void *stream) {
+  if (!L || !x_host || !out_host) return MOE_ERR_INVALID;
+  const size_t bytes = (size_t)L->route.B * L->route.H * 2;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = cudaMemcpyAsync(L->x, x_host, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  int rc = moe_layer_forward(L, stream);
+  if (rc) return rc;
+  e = cudaMemcpyAsync(out_host, L->out, bytes, cudaMemcpyDeviceToHost, st);
+  return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+}

@@ -1,0 +1,116 @@
+// moe_combine: weighted gather-reduce of the expert outputs back to token order.
+//
+// Combine moves every expert output back to its token and reduces the K of them
+// with the routing weights ("DeepEP 完全拆解", §专家并行 and §为什么 combine 比
+// dispatch 慢).  Here it is a gather: one warp owns one token, reads its K rows
+// of Y and sums them in fp32 in the fixed rank order k = 0..K-1, so the result is
+// deterministic (the page lists DeepEP's non-deterministic BF16 pre-reduction as
+// a limitation, §局限).
+//
+// Single-batch overlap ("Single Batch Overlap (SBO)" PR, §2): with a signal
+// array, a row is read only after the down GEMM has published all of its output
+// tiles (acquire load of the row block's counter reaching the threshold).  Polls
+// are bounded by a wall-clock limit; a row that never becomes ready is skipped
+// and MOE_STATUS_TIMEOUT is raised.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
+    const uint16_t *__restrict__ Y, const int32_t *__restrict__ row_of,
+    const float *__restrict__ topk_w, const uint16_t *__restrict__ S, uint16_t *__restrict__ out,
+    int B, int H, int K, const int32_t *signal, int threshold, int bm, int64_t timeout_ns,
+    int32_t *status) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = gridDim.x * kCombineWarps;
+  for (int t = blockIdx.x * kCombineWarps + warp; t < B; t += nwarps) {
+    int my_r = -1;
+    float my_w = 0.0f;
+    if (lane < K) {
+      my_r = row_of[(size_t)t * K + lane];
+      my_w = topk_w[(size_t)t * K + lane];
+      if (signal && my_r >= 0) {
+        const int32_t *sp = signal + my_r / bm;
+        if (ld_acquire_gpu(sp) < threshold) {
+          const uint64_t t0 = globaltimer();
+          while (ld_acquire_gpu(sp) < threshold) {
+            if (globaltimer() - t0 > (uint64_t)timeout_ns) {
+              status_or(status, MOE_STATUS_TIMEOUT);
+              my_r = -1;
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    int r[16];
+    float w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      r[k] = __shfl_sync(0xffffffffu, my_r, k);
+      w[k] = __shfl_sync(0xffffffffu, my_w, k);
+    }
+    for (int h0 = 0; h0 < H; h0 += 256) {
+      const int h = h0 + 8 * lane;
+      if (h >= H) continue;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (k >= K || r[k] < 0) continue;
+        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(Y + (size_t)r[k] * H + h));
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = __fmaf_rn(w[k], __uint_as_float(u[i] << 16), acc[2 * i]);
+          acc[2 * i + 1] = __fmaf_rn(w[k], __uint_as_float(u[i] & 0xffff0000u), acc[2 * i + 1]);
+        }
+      }
+      if (S) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(S + (size_t)t * H + h));
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = __fadd_rn(acc[2 * i], __uint_as_float(u[i] << 16));
+          acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __uint_as_float(u[i] & 0xffff0000u));
+        }
+      }
+      uint4 o;
+      o.x = f32_to_bf16_bits(acc[0]) | (f32_to_bf16_bits(acc[1]) << 16);
+      o.y = f32_to_bf16_bits(acc[2]) | (f32_to_bf16_bits(acc[3]) << 16);
+      o.z = f32_to_bf16_bits(acc[4]) | (f32_to_bf16_bits(acc[5]) << 16);
+      o.w = f32_to_bf16_bits(acc[6]) | (f32_to_bf16_bits(acc[7]) << 16);
+      __stcs(reinterpret_cast<uint4 *>(out + (size_t)t * H + h), o);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_combine(const moe_combine_cfg *c, const void *Y, const int32_t *row_of,
+                           const float *topk_w, const void *shared, void *out, int32_t *status,
+                           void *stream) {
+  if (!c || c->B < 0 || c->H <= 0 || c->K <= 0) return MOE_ERR_INVALID;
+  if (c->H % 128 || c->K > 16) return MOE_ERR_UNSUPPORTED;
+  if (c->B == 0) return MOE_OK;
+  if (!Y || !row_of || !topk_w || !out) return MOE_ERR_INVALID;
+  if ((uintptr_t)Y % 16 || (uintptr_t)out % 16 || (shared && (uintptr_t)shared % 16))
+    return MOE_ERR_INVALID;
+  if (c->signal && (c->block_m_signal <= 0 || c->timeout_ns <= 0)) return MOE_ERR_INVALID;
+  int grid = (c->B + kCombineWarps - 1) / kCombineWarps;
+  if (c->num_ctas > 0 && c->num_ctas < grid) grid = c->num_ctas;
+  combine_kernel<<<grid, kCombineWarps * 32, 0, as_stream(stream)>>>(
+      static_cast<const uint16_t *>(Y), row_of, topk_w, static_cast<const uint16_t *>(shared),
+      static_cast<uint16_t *>(out), c->B, c->H, c->K, c->signal, c->threshold,
+      c->block_m_signal > 0 ? c->block_m_signal : 1, c->timeout_ns, status);
+  return check_launch();
+}

@@ -1,0 +1,375 @@
+// moe_dispatch: the EP all-to-all of one GPU — a stable expert-major permutation
+// of the routed (token, k) rows inside HBM, fused with 1x128 FP8 quantisation.
+//
+// The two layouts are the ones DeepEP's two dispatch modes hand to DeepGEMM
+// ("Large-scale EP: DeepEP, EPLB and two-batch overlap", §DeepEP: each mode where
+// it belongs): contiguous per-expert segments (normal mode, prefill) and a
+// fixed-capacity masked buffer (low-latency mode, decode; fixed shapes that a CUDA
+// graph can replay).  DeepEP's normal mode has the CPU wait for a GPU count before
+// it can size buffers ("DeepEP 完全拆解", §隐式的 CPU 等待); here the counts, the
+// prefix sums and the tile list stay on the device, so no call waits.
+//
+// Three kernels, no atomics whose order could change a result:
+//   dispatch_count_kernel   per chunk of 128 tokens: physical expert of every
+//                           (t,k) (EPLB map applied), its rank among the chunk's
+//                           rows of that expert in (t,k) order, chunk histogram.
+//   dispatch_scan_kernel    one CTA: chunk bases per expert, expert counts,
+//                           segment starts, capacity check, M-tile list.
+//   dispatch_scatter_kernel one warp per token: quantise the row once, write its K
+//                           copies and their scales, row_of / src_of.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 128;  // tokens per count chunk
+constexpr int kCountWarps = 8;
+constexpr int kScanThreads = 1024;
+constexpr int kScatterWarps = 8;
+
+struct DispatchWs {
+  int32_t *phys, *rank, *hist, *seg;
+};
+
+__host__ __device__ inline size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+__host__ __device__ inline DispatchWs carve(void *ws, int B, int K, int N_phys) {
+  char *p = static_cast<char *>(ws);
+  const int nchunks = (B + kChunk - 1) / kChunk;
+  DispatchWs w;
+  w.phys = reinterpret_cast<int32_t *>(p);
+  p += align256(sizeof(int32_t) * B * K);
+  w.rank = reinterpret_cast<int32_t *>(p);
+  p += align256(sizeof(int32_t) * B * K);
+  w.hist = reinterpret_cast<int32_t *>(p);
+  p += align256(sizeof(int32_t) * (size_t)nchunks * N_phys);
+  w.seg = reinterpret_cast<int32_t *>(p);
+  return w;
+}
+
+__global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
+    const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ log2phys,
+    const int32_t *__restrict__ rep, int B, int K, int N_log, int N_phys, DispatchWs ws,
+    int32_t *status) {
+  extern __shared__ int32_t sm[];
+  int32_t *whist = sm;                              // [kCountWarps][N_phys]
+  int32_t *pp = whist + kCountWarps * N_phys;       // [kChunk*K]
+  int32_t *lr = pp + kChunk * K;                    // [kChunk*K]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t_begin = blockIdx.x * kChunk;
+  const int ntok = min(kChunk, B - t_begin);
+  const int npairs = ntok * K;
+  for (int i = tid; i < kCountWarps * N_phys; i += blockDim.x) whist[i] = 0;
+  __syncthreads();
+
+  const int per = (npairs + kCountWarps - 1) / kCountWarps;
+  const int w_begin = warp * per, w_end = min(npairs, w_begin + per);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int base = w_begin; base < w_end; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < w_end;
+    int p = -1;
+    if (valid) {
+      const int t = t_begin + i / K;
+      const int e = topk_idx[(size_t)t_begin * K + i];
+      if (e < 0 || e >= N_log) {
+        status_or(status, MOE_STATUS_BAD_INDEX);
+      } else if (log2phys) {
+        const int re = rep[e];
+        p = (re == 1 || re == 2) ? log2phys[2 * e + (t % re)] : -1;
+        if (p < 0 || p >= N_phys) {
+          status_or(status, MOE_STATUS_BAD_INDEX);
+          p = -1;
+        }
+      } else {
+        p = e < N_phys ? e : -1;
+      }
+    }
+    const int key = valid ? p : -2;
+    const uint32_t mask = __match_any_sync(0xffffffffu, key);
+    const int leader = __ffs(mask) - 1;
+    const int old = (p >= 0) ? whist[warp * N_phys + p] : 0;
+    const int r = old + __popc(mask & lt_mask);
+    __syncwarp();
+    if (p >= 0 && lane == leader) whist[warp * N_phys + p] = old + __popc(mask);
+    __syncwarp();
+    if (valid) {
+      pp[i] = p;
+      lr[i] = r;
+    }
+  }
+  __syncthreads();
+  for (int p = tid; p < N_phys; p += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kCountWarps; ++w) {
+      const int v = whist[w * N_phys + p];
+      whist[w * N_phys + p] = run;
+      run += v;
+    }
+    ws.hist[(size_t)blockIdx.x * N_phys + p] = run;
+  }
+  __syncthreads();
+  for (int i = tid; i < npairs; i += blockDim.x) {
+    const int p = pp[i];
+    const int w = i / per;
+    ws.phys[(size_t)t_begin * K + i] = p;
+    ws.rank[(size_t)t_begin * K + i] = p >= 0 ? whist[w * N_phys + p] + lr[i] : -1;
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
+    int B, int N_phys, int nchunks, int layout, int cap, int64_t rows_alloc, DispatchWs ws,
+    int32_t *__restrict__ counts, int32_t *__restrict__ tiles, int32_t *__restrict__ src_of,
+    int32_t *__restrict__ shared_tiles, int32_t *status) {
+  __shared__ int32_t scan[kScanThreads];
+  __shared__ int32_t total_tiles;
+  const int p = threadIdx.x;
+  int cnt = 0, valid = 0, nt = 0;
+  if (p < N_phys) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = ws.hist[(size_t)c * N_phys + p];
+      ws.hist[(size_t)c * N_phys + p] = cnt;
+      cnt += v;
+    }
+    counts[p] = cnt;
+    valid = cnt;
+    if (layout == MOE_LAYOUT_MASKED && cnt > cap) {
+      valid = cap;
+      status_or(status, MOE_STATUS_CAPACITY);
+    }
+    nt = (valid + 127) / 128;
+  }
+  // block-wide inclusive scan of nt (Hillis-Steele)
+  scan[p] = nt;
+  __syncthreads();
+  for (int off = 1; off < kScanThreads; off <<= 1) {
+    const int v = p >= off ? scan[p - off] : 0;
+    __syncthreads();
+    scan[p] += v;
+    __syncthreads();
+  }
+  const int first = scan[p] - nt;
+  if (p == kScanThreads - 1) total_tiles = scan[p];
+  __syncthreads();
+  if (p < N_phys) {
+    const int seg = layout == MOE_LAYOUT_CONTIG ? first * 128 : p * cap;
+    ws.seg[p] = seg;
+    for (int i = 0; i < nt; ++i) {
+      int32_t *tl = tiles + 8 + 8 * (size_t)(first + i);
+      tl[0] = seg + 128 * i;
+      tl[1] = p;
+      tl[2] = min(128, valid - 128 * i);
+      tl[3] = first;
+      tl[4] = nt;
+      tl[5] = tl[6] = tl[7] = 0;
+    }
+    if (src_of) {  // rows of this expert that no token fills
+      const int end = layout == MOE_LAYOUT_CONTIG ? nt * 128 : cap;
+      for (int j = valid; j < end; ++j) src_of[seg + j] = -1;
+    }
+  }
+  const int64_t used = layout == MOE_LAYOUT_CONTIG ? (int64_t)total_tiles * 128
+                                                   : (int64_t)N_phys * cap;
+  if (p == 0) {
+    tiles[0] = total_tiles;
+    tiles[1] = (int32_t)used;
+    for (int i = 2; i < 8; ++i) tiles[i] = 0;
+  }
+  if (src_of)
+    for (int64_t r = used + p; r < rows_alloc; r += kScanThreads) src_of[r] = -1;
+  if (shared_tiles) {
+    const int snt = (B + 127) / 128;
+    if (p == 0) {
+      shared_tiles[0] = snt;
+      shared_tiles[1] = snt * 128;
+      for (int i = 2; i < 8; ++i) shared_tiles[i] = 0;
+    }
+    for (int i = p; i < snt; i += kScanThreads) {
+      int32_t *tl = shared_tiles + 8 + 8 * (size_t)i;
+      tl[0] = 128 * i;
+      tl[1] = 0;
+      tl[2] = min(128, B - 128 * i);
+      tl[3] = 0;
+      tl[4] = snt;
+      tl[5] = tl[6] = tl[7] = 0;
+    }
+  }
+}
+
+// Byte offset of row r's scale word for 128-column block kb in an SF-atom array
+// of Kb blocks per row.
+__device__ __forceinline__ size_t sf_atom_offset(int64_t r, int kb, int Kb) {
+  return ((size_t)(r >> 7) * Kb + kb) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5);
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
+    const uint16_t *__restrict__ x, int B, int H, int K, int N_phys, int layout, int cap,
+    DispatchWs ws, uint8_t *__restrict__ A, uint8_t *__restrict__ A_sf,
+    int32_t *__restrict__ row_of, int32_t *__restrict__ src_of, uint8_t *__restrict__ As,
+    uint8_t *__restrict__ As_sf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * kScatterWarps + warp;
+  if (t >= B) return;
+  const int chunk = t / kChunk;
+  int64_t my_row = -1;
+  if (lane < K) {
+    const int p = ws.phys[(size_t)t * K + lane];
+    if (p >= 0) {
+      const int slot = ws.hist[(size_t)chunk * N_phys + p] + ws.rank[(size_t)t * K + lane];
+      if (layout == MOE_LAYOUT_CONTIG)
+        my_row = (int64_t)ws.seg[p] + slot;
+      else if (slot < cap)
+        my_row = (int64_t)p * cap + slot;
+    }
+    row_of[(size_t)t * K + lane] = (int32_t)my_row;
+    if (src_of && my_row >= 0) src_of[my_row] = t;
+  }
+  int64_t rows[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) rows[k] = __shfl_sync(0xffffffffu, my_row, k);
+
+  const uint16_t *xr = x + (size_t)t * H;
+  const int Hb = H / 128;
+  for (int h0 = 0; h0 < H; h0 += 256) {
+    const int h = h0 + 8 * lane;
+    const bool act = h < H;
+    const uint4 v = act ? __ldg(reinterpret_cast<const uint4 *>(xr + h)) : make_uint4(0, 0, 0, 0);
+    if (!kFp8) {
+      if (act) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if (k < K && rows[k] >= 0)
+            *reinterpret_cast<uint4 *>(A + ((size_t)rows[k] * H + h) * 2) = v;
+      }
+      continue;
+    }
+    float f[8];
+    f[0] = __uint_as_float(v.x << 16);
+    f[1] = __uint_as_float(v.x & 0xffff0000u);
+    f[2] = __uint_as_float(v.y << 16);
+    f[3] = __uint_as_float(v.y & 0xffff0000u);
+    f[4] = __uint_as_float(v.z << 16);
+    f[5] = __uint_as_float(v.z & 0xffff0000u);
+    f[6] = __uint_as_float(v.w << 16);
+    f[7] = __uint_as_float(v.w & 0xffff0000u);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1)  // the 16 lanes of one 128-column block
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const int e = ue8m0_exp(amax);
+    const float inv = pow2i(-e);
+    uint2 q;
+    q.x = e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
+          (e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
+    q.y = e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
+          (e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
+    const uint32_t sfw = (uint32_t)(e + 127) * 0x01010101u;
+    const int kb = h >> 7;
+    if (act) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (k >= K || rows[k] < 0) continue;
+        *reinterpret_cast<uint2 *>(A + (size_t)rows[k] * H + h) = q;
+        if ((lane & 15) == 0)
+          *reinterpret_cast<uint32_t *>(A_sf + sf_atom_offset(rows[k], kb, Hb)) = sfw;
+      }
+      if (As) {
+        *reinterpret_cast<uint2 *>(As + (size_t)t * H + h) = q;
+        if ((lane & 15) == 0)
+          *reinterpret_cast<uint32_t *>(As_sf + sf_atom_offset(t, kb, Hb)) = sfw;
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+static int dispatch_check(const moe_dispatch_cfg *c) {
+  if (!c) return MOE_ERR_INVALID;
+  if (c->B < 0 || c->H <= 0 || c->K <= 0 || c->N_log <= 0 || c->N_phys <= 0)
+    return MOE_ERR_INVALID;
+  if (c->H % 128 || c->K > 16 || c->N_phys > kScanThreads) return MOE_ERR_UNSUPPORTED;
+  if (c->layout != MOE_LAYOUT_CONTIG && c->layout != MOE_LAYOUT_MASKED) return MOE_ERR_INVALID;
+  if (c->fmt != MOE_FMT_FP8 && c->fmt != MOE_FMT_BF16) return MOE_ERR_INVALID;
+  if (c->layout == MOE_LAYOUT_MASKED && (c->cap <= 0 || c->cap % 128)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+extern "C" int64_t moe_dispatch_rows(const moe_dispatch_cfg *c) {
+  if (dispatch_check(c)) return 0;
+  if (c->layout == MOE_LAYOUT_MASKED) return (int64_t)c->N_phys * c->cap;
+  return ((int64_t)c->B * c->K + (int64_t)c->N_phys * 127 + 127) / 128 * 128;
+}
+
+extern "C" int64_t moe_dispatch_max_tiles(const moe_dispatch_cfg *c) {
+  return moe_dispatch_rows(c) / 128;
+}
+
+extern "C" size_t moe_dispatch_workspace_size(const moe_dispatch_cfg *c) {
+  if (dispatch_check(c)) return 0;
+  const size_t nchunks = (c->B + kChunk - 1) / kChunk;
+  return 2 * align256(sizeof(int32_t) * (size_t)c->B * c->K) +
+         align256(sizeof(int32_t) * nchunks * c->N_phys) +
+         align256(sizeof(int32_t) * (c->N_phys + 1));
+}
+
+extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int32_t *topk_idx,
+                            const int32_t *log2phys, const int32_t *rep, void *A, void *A_sf,
+                            int32_t *counts, int32_t *row_of, int32_t *src_of, int32_t *tiles,
+                            void *A_shared, void *A_shared_sf, int32_t *shared_tiles,
+                            void *workspace, size_t workspace_bytes, int32_t *status,
+                            void *stream) {
+  int rc = dispatch_check(c);
+  if (rc) return rc;
+  if (!x || !topk_idx || !A || !counts || !row_of || !tiles || !workspace)
+    return MOE_ERR_INVALID;
+  if (c->fmt == MOE_FMT_FP8 && !A_sf) return MOE_ERR_INVALID;
+  if ((log2phys == nullptr) != (rep == nullptr)) return MOE_ERR_INVALID;
+  if (A_shared && (c->fmt != MOE_FMT_FP8 || !A_shared_sf)) return MOE_ERR_INVALID;
+  if (workspace_bytes < moe_dispatch_workspace_size(c)) return MOE_ERR_INVALID;
+  if ((uintptr_t)x % 16 || (uintptr_t)A % 16 || (A_sf && (uintptr_t)A_sf % 16) ||
+      (A_shared && (uintptr_t)A_shared % 16))
+    return MOE_ERR_INVALID;
+  cudaStream_t st = as_stream(stream);
+  const int B = c->B, K = c->K, Np = c->N_phys;
+  if (B == 0) {
+    cudaError_t e = cudaMemsetAsync(tiles, 0, 8 * sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * Np, st);
+    if (e == cudaSuccess && shared_tiles)
+      e = cudaMemsetAsync(shared_tiles, 0, 8 * sizeof(int32_t), st);
+    return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+  }
+  const int nchunks = (B + kChunk - 1) / kChunk;
+  DispatchWs ws = carve(workspace, B, K, Np);
+  const size_t smem = sizeof(int32_t) * ((size_t)kCountWarps * Np + 2 * kChunk * K);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(dispatch_count_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  dispatch_count_kernel<<<nchunks, kCountWarps * 32, smem, st>>>(topk_idx, log2phys, rep, B, K,
+                                                                c->N_log, Np, ws, status);
+  if ((rc = check_launch())) return rc;
+  dispatch_scan_kernel<<<1, kScanThreads, 0, st>>>(B, Np, nchunks, c->layout, c->cap,
+                                                   moe_dispatch_rows(c), ws, counts, tiles,
+                                                   src_of, shared_tiles, status);
+  if ((rc = check_launch())) return rc;
+  const int grid = (B + kScatterWarps - 1) / kScatterWarps;
+  const uint16_t *xb = static_cast<const uint16_t *>(x);
+  if (c->fmt == MOE_FMT_FP8)
+    dispatch_scatter_kernel<true><<<grid, kScatterWarps * 32, 0, st>>>(
+        xb, B, c->H, K, Np, c->layout, c->cap, ws, static_cast<uint8_t *>(A),
+        static_cast<uint8_t *>(A_sf), row_of, src_of, static_cast<uint8_t *>(A_shared),
+        static_cast<uint8_t *>(A_shared_sf));
+  else
+    dispatch_scatter_kernel<false><<<grid, kScatterWarps * 32, 0, st>>>(
+        xb, B, c->H, K, Np, c->layout, c->cap, ws, static_cast<uint8_t *>(A), nullptr, row_of,
+        src_of, nullptr, nullptr);
+  return check_launch();
+}

@@ -1,0 +1,445 @@
+// moe_grouped_gemm_fp8: grouped FP8 GEMMs of the expert FFN on tcgen05 tensor
+// cores (sm_100-class), persistent over the M-tile list written by moe_dispatch.
+//
+// What it computes follows DeepGEMM's grouped GEMMs for the two dispatch layouts
+// ("Large-scale EP: DeepEP, EPLB and two-batch overlap", §DeepEP: each mode where
+// it belongs) with 1x128 activation and 128x128 weight scaling ("Single Batch
+// Overlap (SBO)" PR, §3 "1d2d"), and the SBO producer side: per (expert, block_m)
+// completion counters bumped with release atomics (same PR, §2).  How it computes
+// is Blackwell-specific: the scales are powers of two (UE8M0), so the tensor core
+// applies them itself (kind::mxf8f6f4 block scaling, one scale per 32 K values,
+// each 1x128 / 128x128 scale repeated over its four 32-wide sub-blocks) and the
+// fp32 accumulator stays in tensor memory for the whole K loop.
+//
+// CTA = 6 warps, one CTA per SM, persistent:
+//   warp 0  TMA producer: A tile 128x128 e4m3, B tile 256x128 e4m3 (two 128-row
+//           boxes: gate and up halves for GATEUP, two output blocks for DOWN),
+//           and the matching scale atoms (cp.async.bulk), STAGES-deep ring.
+//   warp 1  TMEM owner and MMA issuer: scale atoms -> TMEM (tcgen05.cp), four
+//           128x256x32 block-scaled MMAs per stage, commits free the stage.
+//   warps 2-5 epilogue: TMEM -> registers (one accumulator row per thread),
+//           SwiGLU + 1x128 requantisation (GATEUP) or bf16 rounding (DOWN),
+//           global stores, optional release signals.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int kGemmThreads = 192;
+constexpr uint32_t A_BYTES = BM * BK;   // 16 KB
+constexpr uint32_t B_BYTES = BN * BK;   // 32 KB
+constexpr uint32_t SFA_BYTES = 512;     // one SF atom
+constexpr uint32_t SFB_BYTES = 1024;    // two SF atoms
+constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
+constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+constexpr uint32_t OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_SF = 256;  // scale columns start here, 16 per stage
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+struct GemmParams {
+  int op, n, k, Kb, n_tiles, I;
+  const uint8_t *A_sf, *W_sf;
+  const int32_t *phys2log, *tiles;
+  uint8_t *out, *out_sf;
+  int32_t *signal;
+  int bm_signal;
+  int32_t *status;
+};
+
+__device__ __forceinline__ void decode_unit(const int32_t *tiles, int unit, int n_tiles,
+                                            int &mi, int &ni) {
+  const int g = unit / n_tiles;  // some M tile of the right expert band
+  const int f = tiles[8 + 8 * g + 3], c = tiles[8 + 8 * g + 4];
+  const int local = unit - n_tiles * f;
+  ni = local / c;
+  mi = f + local % c;
+}
+
+__device__ __forceinline__ size_t sf_atom_off(int64_t r, int kb, int Kb) {
+  return ((size_t)(r >> 7) * Kb + kb) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5);
+}
+
+__device__ __forceinline__ void fail(int32_t *status, volatile int *abort) {
+  *abort = 1;
+  status_or(status, MOE_STATUS_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmW, const GemmParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t bar_full = s_base + OFF_BAR;                 // [STAGES]
+  const uint32_t bar_empty = bar_full + 8 * STAGES;           // [STAGES]
+  const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
+  const uint32_t bar_acc_empty = bar_acc_full + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+  volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, 128);
+    *abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int num_m = P.tiles[0];
+  const int total = num_m * P.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) {
+        int mi, ni;
+        decode_unit(P.tiles, unit, P.n_tiles, mi, ni);
+        const int32_t *tl = P.tiles + 8 + 8 * mi;
+        const int row0 = tl[0];
+        const int pe = tl[1];
+        const int we = P.phys2log ? P.phys2log[pe] : pe;
+        int wrow0, wrow1, nb0, nb1;
+        if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
+          wrow0 = we * P.n + ni * 128;
+          wrow1 = we * P.n + P.I + ni * 128;
+          nb0 = ni;
+          nb1 = P.I / 128 + ni;
+        } else {
+          wrow0 = we * P.n + ni * 256;
+          wrow1 = wrow0 + 128;
+          nb0 = 2 * ni;
+          nb1 = 2 * ni + 1;
+        }
+        const uint8_t *sfa = P.A_sf + (size_t)(row0 >> 7) * P.Kb * 512;
+        const uint8_t *sfb0 = P.W_sf + ((size_t)we * (P.n / 128) + nb0) * P.Kb * 512;
+        const uint8_t *sfb1 = P.W_sf + ((size_t)we * (P.n / 128) + nb1) * P.Kb * 512;
+        for (int kb = 0; kb < P.Kb; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort, kWaitLimitNs)) {
+            fail(P.status, abort);
+            ok = false;
+            break;
+          }
+          const uint32_t full = bar_full + 8 * stage;
+          mbar_arrive_expect_tx(full, STAGE_TX);
+          const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
+          const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
+          tma_load_2d(sa, &tmA, full, kb * BK, row0, pol_a);
+          tma_load_2d(sb, &tmW, full, kb * BK, wrow0, pol_w);
+          tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
+          const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
+          const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
+          bulk_load(ssfa, sfa + (size_t)kb * 512, 512, full);
+          bulk_load(ssfb, sfb0 + (size_t)kb * 512, 512, full);
+          bulk_load(ssfb + 512, sfb1 + (size_t)kb * 512, 512, full);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already in flight land before the CTA can exit.
+        for (int i = 0; i < STAGES && i < issued; ++i) {
+          if (--stage < 0) {
+            stage = STAGES - 1;
+            phase ^= 1;
+          }
+          volatile int never = 0;
+          mbar_wait(bar_full + 8 * stage, phase, &never, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // kind::mxf8f6f4 instruction descriptor: E4M3 x E4M3, K-major A and B,
+      // N = 256, UE8M0 scales, M = 128; bits 4-5 / 29-30 select the scale byte.
+      const uint32_t idesc_base = ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+                                  ((uint32_t)(BM >> 4) << 24);
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) {
+        if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
+          fail(P.status, abort);
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < P.Kb; ++kb) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort, kWaitLimitNs)) {
+            fail(P.status, abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
+          const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
+          const uint32_t t_sfa = tmem + TMEM_SF + 16 * stage;
+          const uint32_t t_sfb = t_sfa + 4;
+          const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
+          const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
+          tc_cp_32x128b_x4(t_sfa, smem_desc(ssfa, 16, 128, 0));
+          tc_cp_32x128b_x4(t_sfb, smem_desc(ssfb, 16, 128, 0));
+          tc_cp_32x128b_x4(t_sfb + 4, smem_desc(ssfb + 512, 16, 128, 0));
+#pragma unroll
+          for (int j = 0; j < BK / 32; ++j) {
+            const uint64_t ad = smem_desc(sa + 32 * j, 16, 1024, 2);
+            const uint64_t bd = smem_desc(sb + 32 * j, 16, 1024, 2);
+            const uint32_t idesc = idesc_base | ((uint32_t)j << 29) | ((uint32_t)j << 4);
+            tc_mma_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | j) != 0);
+          }
+          tc_commit(bar_empty + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(bar_acc_full);
+        acc_phase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_local = 32 * q + lane;
+    const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
+    uint32_t acc_phase = 0;
+    for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
+      int mi, ni;
+      decode_unit(P.tiles, unit, P.n_tiles, mi, ni);
+      const int32_t *tl = P.tiles + 8 + 8 * mi;
+      const int row0 = tl[0], valid = tl[2];
+      const int64_t r = (int64_t)row0 + row_local;
+      const bool store = row_local < valid;
+      if (!mbar_wait(bar_acc_full, acc_phase, abort, kWaitLimitNs)) {
+        fail(P.status, abort);
+        break;
+      }
+      tc_fence_after();
+      if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
+        float h[128];
+        float amax = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          MOE_TMEM_LD_32x32b_X32(t_row + 32 * c, g);
+          MOE_TMEM_LD_32x32b_X32(t_row + 128 + 32 * c, u);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float gf = __uint_as_float(g[i]), uf = __uint_as_float(u[i]);
+            const float v = gf / (1.0f + expf(-gf)) * uf;
+            h[32 * c + i] = v;
+            amax = fmaxf(amax, fabsf(v));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_acc_empty);
+        if (store) {
+          const int e = ue8m0_exp(amax);
+          const float inv = pow2i(-e);
+          uint8_t *dst = P.out + (size_t)r * P.I + (size_t)ni * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 w;
+            uint32_t *wp = &w.x;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int b = 16 * c + 4 * j;
+              wp[j] = e4m3x2(__fmul_rn(h[b], inv), __fmul_rn(h[b + 1], inv)) |
+                      (e4m3x2(__fmul_rn(h[b + 2], inv), __fmul_rn(h[b + 3], inv)) << 16);
+            }
+            *reinterpret_cast<uint4 *>(dst + 16 * c) = w;
+          }
+          *reinterpret_cast<uint32_t *>(P.out_sf + sf_atom_off(r, ni, P.I / 128)) =
+              (uint32_t)(e + 127) * 0x01010101u;
+        }
+      } else {
+        uint8_t *dst = P.out + ((size_t)r * P.n + (size_t)ni * 256) * 2;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          MOE_TMEM_LD_32x32b_X32(t_row + 32 * c, v);
+          tc_wait_ld();
+          if (c == 7) {
+            tc_fence_before();
+            mbar_arrive(bar_acc_empty);
+          }
+          if (store) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4 w;
+              w.x = f32_to_bf16_bits(__uint_as_float(v[8 * j + 0])) |
+                    (f32_to_bf16_bits(__uint_as_float(v[8 * j + 1])) << 16);
+              w.y = f32_to_bf16_bits(__uint_as_float(v[8 * j + 2])) |
+                    (f32_to_bf16_bits(__uint_as_float(v[8 * j + 3])) << 16);
+              w.z = f32_to_bf16_bits(__uint_as_float(v[8 * j + 4])) |
+                    (f32_to_bf16_bits(__uint_as_float(v[8 * j + 5])) << 16);
+              w.w = f32_to_bf16_bits(__uint_as_float(v[8 * j + 6])) |
+                    (f32_to_bf16_bits(__uint_as_float(v[8 * j + 7])) << 16);
+              *reinterpret_cast<uint4 *>(dst + 64 * c + 16 * j) = w;
+            }
+          }
+        }
+        if (P.signal) {
+          __threadfence();
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (warp == 2 && lane == 0) {
+            for (int j = 0; j * P.bm_signal < BM; ++j)
+              if (j * P.bm_signal < valid)
+                red_release_gpu_add(P.signal + (row0 + j * P.bm_signal) / P.bm_signal, 1);
+          }
+        }
+      }
+      acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+__global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ atoms,
+                                   size_t n_atoms) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // one 16-byte piece
+  if (i >= n_atoms * 32) return;
+  const uint32_t b = (uint32_t)sf[i >> 5] * 0x01010101u;
+  reinterpret_cast<uint4 *>(atoms)[i] = make_uint4(b, b, b, b);
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows][cols] (cols contiguous), 128 x 128 boxes, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_packed_scale_bytes(int E, int n, int k) {
+  if (E <= 0 || n <= 0 || k <= 0 || n % 128 || k % 128) return 0;
+  return (size_t)E * (n / 128) * (k / 128) * 512;
+}
+
+extern "C" int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf,
+                                      void *W_sf_packed, void *stream) {
+  const size_t bytes = moe_packed_scale_bytes(E, n, k);
+  if (!bytes || !W_sf || !W_sf_packed || (uintptr_t)W_sf_packed % 16) return MOE_ERR_INVALID;
+  const size_t n_atoms = bytes / 512;
+  const size_t pieces = n_atoms * 32;
+  pack_scales_kernel<<<(unsigned)((pieces + 255) / 256), 256, 0, as_stream(stream)>>>(
+      W_sf, static_cast<uint8_t *>(W_sf_packed), n_atoms);
+  return check_launch();
+}
+
+extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
+  if (!a) return MOE_ERR_INVALID;
+  if (a->op != MOE_GEMM_GATEUP_SWIGLU && a->op != MOE_GEMM_DOWN) return MOE_ERR_INVALID;
+  if (a->n <= 0 || a->k <= 0 || a->rows <= 0 || a->max_tiles <= 0 || a->num_experts <= 0)
+    return MOE_ERR_INVALID;
+  if (a->n % 256 || a->k % 128 || a->rows % 128) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)a->num_experts * a->n > INT32_MAX || a->rows > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if (!a->A || !a->A_sf || !a->W || !a->W_sf || !a->tiles || !a->out) return MOE_ERR_INVALID;
+  if (a->op == MOE_GEMM_GATEUP_SWIGLU && (!a->out_sf || a->signal)) return MOE_ERR_INVALID;
+  if (a->signal && (a->block_m_signal <= 0 || BM % a->block_m_signal)) return MOE_ERR_INVALID;
+  const void *ptrs[] = {a->A, a->A_sf, a->W, a->W_sf, a->out, a->out_sf};
+  for (const void *p : ptrs)
+    if ((uintptr_t)p % 16) return MOE_ERR_INVALID;
+  CUtensorMap mA, mW;
+  if (!make_map(&mA, a->A, (uint64_t)a->rows, (uint64_t)a->k) ||
+      !make_map(&mW, a->W, (uint64_t)a->num_experts * a->n, (uint64_t)a->k))
+    return MOE_ERR_CUDA;
+  GemmParams P;
+  P.op = a->op;
+  P.n = a->n;
+  P.k = a->k;
+  P.Kb = a->k / BK;
+  P.n_tiles = a->n / BN;
+  P.I = a->n / 2;
+  P.A_sf = static_cast<const uint8_t *>(a->A_sf);
+  P.W_sf = static_cast<const uint8_t *>(a->W_sf);
+  P.phys2log = a->phys2log;
+  P.tiles = a->tiles;
+  P.out = static_cast<uint8_t *>(a->out);
+  P.out_sf = static_cast<uint8_t *>(a->out_sf);
+  P.signal = a->signal;
+  P.bm_signal = a->block_m_signal > 0 ? a->block_m_signal : BM;
+  P.status = a->status;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    attr_set = true;
+  }
+  const int sms = a->num_sms > 0 ? a->num_sms : device_sm_count();
+  const int64_t max_units = a->max_tiles * (a->n / BN);
+  const int grid = (int)(max_units < sms ? max_units : sms);
+  grouped_gemm_kernel<<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mW, P);
+  return check_launch();
+}

@@ -1,0 +1,370 @@
+// moe_route: router logits, scores, group-limited top-K and routing weights.
+//
+// The layer's router ("DeepEP 完全拆解", §专家并行) scores each token against N
+// experts and keeps K; DeepSeek-V3's group-limited gating (same page, §group-limited
+// gating) first keeps the best groups, then the best experts inside them.
+//
+// Two kernels:
+//   route_logits_kernel  z = x . W^T in fp32, each logit one fused multiply-add per
+//                        k in order k = 0..H-1 (register-tiled SIMT: the ordering
+//                        rule keeps this off the tensor cores, which round inputs
+//                        and reorder partial sums).
+//   route_select_kernel  one warp per token: scores, group scores, top-K with the
+//                        (score desc, index asc) order, weights, expert counts.
+#include <cfloat>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteBK = 32;        // k values staged per step
+constexpr int kRouteThreads = 128;  // 4 warps: 2 (tokens) x 2 (experts)
+
+// Warp tile: lanes as 4 (tokens) x 8 (experts); thread tile TT tokens x TE experts,
+// strided by 4 and 8 so the shared-memory reads of one warp hit 4 and 8 distinct
+// rows whose 36-float pitch puts them in distinct banks.
+template <int TT, int TE>
+__global__ void __launch_bounds__(kRouteThreads) route_logits_kernel(const uint16_t *__restrict__ x,
+                                                                     const float *__restrict__ W,
+                                                                     float *__restrict__ logits,
+                                                                     int B, int H, int N) {
+  constexpr int BT = 2 * 4 * TT;  // tokens per CTA
+  constexpr int BE = 2 * 8 * TE;  // experts per CTA
+  constexpr int LD = kRouteBK + 4;
+  __shared__ __align__(16) float xs[2][BT][LD];
+  __shared__ __align__(16) float ws[2][BE][LD];
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int tl = lane >> 3, el = lane & 7;
+  const int wt = warp >> 1, we = warp & 1;
+  const int t0 = blockIdx.y * BT, e0 = blockIdx.x * BE;
+
+  // Staging maps: x chunk BT x 32 bf16 = BT*4 16-byte pieces; W chunk BE x 32 fp32
+  // = BE*8 16-byte pieces.
+  auto load_x = [&](int kc, uint4 *reg) {
+#pragma unroll
+    for (int it = 0; it < (BT * 4 + kRouteThreads - 1) / kRouteThreads; ++it) {
+      const int i = tid + it * kRouteThreads;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (i < BT * 4) {
+        const int t = i >> 2, k = kc + (i & 3) * 8;
+        if (t0 + t < B) v = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + t) * H + k));
+      }
+      reg[it] = v;
+    }
+  };
+  auto store_x = [&](int buf, const uint4 *reg) {
+#pragma unroll
+    for (int it = 0; it < (BT * 4 + kRouteThreads - 1) / kRouteThreads; ++it) {
+      const int i = tid + it * kRouteThreads;
+      if (i < BT * 4) {
+        const int t = i >> 2, k = (i & 3) * 8;
+        const uint4 v = reg[it];
+        float4 a, b;
+        a.x = __uint_as_float(v.x << 16);
+        a.y = __uint_as_float(v.x & 0xffff0000u);
+        a.z = __uint_as_float(v.y << 16);
+        a.w = __uint_as_float(v.y & 0xffff0000u);
+        b.x = __uint_as_float(v.z << 16);
+        b.y = __uint_as_float(v.z & 0xffff0000u);
+        b.z = __uint_as_float(v.w << 16);
+        b.w = __uint_as_float(v.w & 0xffff0000u);
+        *reinterpret_cast<float4 *>(&xs[buf][t][k]) = a;
+        *reinterpret_cast<float4 *>(&xs[buf][t][k + 4]) = b;
+      }
+    }
+  };
+  auto load_w = [&](int kc, int buf) {
+#pragma unroll
+    for (int it = 0; it < (BE * 8 + kRouteThreads - 1) / kRouteThreads; ++it) {
+      const int i = tid + it * kRouteThreads;
+      if (i < BE * 8) {
+        const int e = i >> 3, k = (i & 7) * 4;
+        const uint32_t dst = smem_u32(&ws[buf][e][k]);
+        const bool ok = e0 + e < N;
+        const float *src = W + (size_t)(ok ? e0 + e : 0) * H + kc + k;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                     "r"(ok ? 16 : 0)
+                     : "memory");
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
+  float acc[TT][TE];
+#pragma unroll
+  for (int i = 0; i < TT; ++i)
+#pragma unroll
+    for (int j = 0; j < TE; ++j) acc[i][j] = 0.0f;
+
+  constexpr int XR = (BT * 4 + kRouteThreads - 1) / kRouteThreads;
+  uint4 xreg[XR];
+  load_x(0, xreg);
+  load_w(0, 0);
+  store_x(0, xreg);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+
+  const int nchunks = H / kRouteBK;
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c & 1;
+    const bool more = c + 1 < nchunks;
+    if (more) {
+      load_x((c + 1) * kRouteBK, xreg);
+      load_w((c + 1) * kRouteBK, buf ^ 1);
+    }
+#pragma unroll
+    for (int k4 = 0; k4 < kRouteBK; k4 += 4) {
+      float4 xv[TT], wv[TE];
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+        xv[i] = *reinterpret_cast<const float4 *>(&xs[buf][wt * 4 * TT + tl + 4 * i][k4]);
+#pragma unroll
+      for (int j = 0; j < TE; ++j)
+        wv[j] = *reinterpret_cast<const float4 *>(&ws[buf][we * 8 * TE + el + 8 * j][k4]);
+      // k order is strictly sequential for every output
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+#pragma unroll
+        for (int j = 0; j < TE; ++j) {
+          acc[i][j] = __fmaf_rn(xv[i].x, wv[j].x, acc[i][j]);
+          acc[i][j] = __fmaf_rn(xv[i].y, wv[j].y, acc[i][j]);
+          acc[i][j] = __fmaf_rn(xv[i].z, wv[j].z, acc[i][j]);
+          acc[i][j] = __fmaf_rn(xv[i].w, wv[j].w, acc[i][j]);
+        }
+    }
+    if (more) {
+      store_x(buf ^ 1, xreg);
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < TT; ++i) {
+    const int t = t0 + wt * 4 * TT + tl + 4 * i;
+    if (t >= B) continue;
+#pragma unroll
+    for (int j = 0; j < TE; ++j) {
+      const int e = e0 + we * 8 * TE + el + 8 * j;
+      if (e < N) logits[(size_t)t * N + e] = acc[i][j];
+    }
+  }
+}
+
+struct Cand {
+  float v;  // choice score
+  int i;    // expert index (INT_MAX = none)
+  float s;  // weight score of that expert
+};
+
+// a ranks before b: larger score first, equal scores -> lower index first.
+__device__ __forceinline__ bool before(const Cand &a, const Cand &b) {
+  if (a.i == INT_MAX) return false;
+  if (b.i == INT_MAX) return true;
+  return a.v > b.v || (a.v == b.v && a.i < b.i);
+}
+
+__device__ __forceinline__ Cand warp_best(Cand c) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Cand o;
+    o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
+    o.i = __shfl_xor_sync(0xffffffffu, c.i, off);
+    o.s = __shfl_xor_sync(0xffffffffu, c.s, off);
+    if (before(o, c)) c = o;
+  }
+  return c;
+}
+
+constexpr int kMaxNI = 16;  // N <= 512
+constexpr int kSelWarps = 8;
+
+__global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
+    const float *__restrict__ logits, const float *__restrict__ bias, int B, int N, int K,
+    int n_group, int topk_group, int score_fn, int renorm, float route_scale,
+    int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int32_t *__restrict__ counts) {
+  __shared__ float sd[kSelWarps][kMaxNI * 32];
+  __shared__ float sg[kSelWarps][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * kSelWarps + warp;
+  if (t >= B) return;
+  const int NI = (N + 31) >> 5;
+
+  float c[kMaxNI], s[kMaxNI];
+  bool elig[kMaxNI];
+#pragma unroll
+  for (int i = 0; i < kMaxNI; ++i) {
+    const int e = lane + 32 * i;
+    elig[i] = (i < NI) && (e < N);
+    c[i] = elig[i] ? logits[(size_t)t * N + e] : 0.0f;
+  }
+  if (score_fn == MOE_SCORE_SOFTMAX) {
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < kMaxNI; ++i)
+      if (elig[i]) m = fmaxf(m, c[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+#pragma unroll
+    for (int i = 0; i < kMaxNI; ++i)
+      if (elig[i]) {
+        s[i] = route_exp(__fsub_rn(c[i], m));
+        sd[warp][lane + 32 * i] = s[i];
+      }
+    __syncwarp();
+    float S = 0.0f;
+    if (lane == 0)
+      for (int e = 0; e < N; ++e) S = __fadd_rn(S, sd[warp][e]);  // expert order
+    S = __shfl_sync(0xffffffffu, S, 0);
+#pragma unroll
+    for (int i = 0; i < kMaxNI; ++i)
+      if (elig[i]) s[i] = __fdiv_rn(s[i], S);  // choice score stays z
+  } else {
+#pragma unroll
+    for (int i = 0; i < kMaxNI; ++i)
+      if (elig[i]) {
+        const int e = lane + 32 * i;
+        s[i] = route_sigmoid(c[i]);
+        c[i] = bias ? __fadd_rn(s[i], __ldg(bias + e)) : s[i];
+      }
+  }
+
+  if (n_group > 1) {
+    const int gs = N / n_group;
+    for (int j = 0; j < n_group; ++j) {
+      Cand b1{0.0f, INT_MAX, 0.0f};
+#pragma unroll
+      for (int i = 0; i < kMaxNI; ++i) {
+        const int e = lane + 32 * i;
+        Cand x{c[i], e, 0.0f};
+        if (elig[i] && e / gs == j && before(x, b1)) b1 = x;
+      }
+      b1 = warp_best(b1);
+      Cand b2{0.0f, INT_MAX, 0.0f};
+#pragma unroll
+      for (int i = 0; i < kMaxNI; ++i) {
+        const int e = lane + 32 * i;
+        Cand x{c[i], e, 0.0f};
+        if (elig[i] && e / gs == j && e != b1.i && before(x, b2)) b2 = x;
+      }
+      b2 = warp_best(b2);
+      if (lane == 0) sg[warp][j] = __fadd_rn(b1.v, b2.v);
+    }
+    __syncwarp();
+    uint32_t keep = 0;
+    for (int r = 0; r < topk_group; ++r) {
+      int best = -1;
+      for (int j = 0; j < n_group; ++j) {
+        if (keep >> j & 1) continue;
+        if (best < 0 || sg[warp][j] > sg[warp][best]) best = j;  // ties keep the lower j
+      }
+      keep |= 1u << best;
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxNI; ++i) {
+      const int e = lane + 32 * i;
+      if (elig[i]) elig[i] = (keep >> (e / gs)) & 1;
+    }
+  }
+
+  int my_idx = -1;
+  float my_s = 0.0f;
+  for (int r = 0; r < K; ++r) {
+    Cand b{0.0f, INT_MAX, 0.0f};
+#pragma unroll
+    for (int i = 0; i < kMaxNI; ++i) {
+      Cand x{c[i], lane + 32 * i, s[i]};
+      if (elig[i] && before(x, b)) b = x;
+    }
+    b = warp_best(b);
+#pragma unroll
+    for (int i = 0; i < kMaxNI; ++i)
+      if (lane + 32 * i == b.i) elig[i] = false;
+    if (lane == r) {  // no candidate only if scores are NaN: report index -1
+      my_idx = b.i == INT_MAX ? -1 : b.i;
+      my_s = b.s;
+    }
+  }
+  // weights: the normaliser sums the selected scores in rank order
+  float sum = 0.0f;
+  for (int r = 0; r < K; ++r) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_s, r));
+  if (lane < K) {
+    const float w = renorm ? __fmul_rn(__fdiv_rn(my_s, sum), route_scale)
+                           : __fmul_rn(my_s, route_scale);
+    topk_idx[(size_t)t * K + lane] = my_idx;
+    topk_w[(size_t)t * K + lane] = w;
+    if (counts && my_idx >= 0) atomicAdd(counts + my_idx, 1);
+  }
+}
+
+template <int TT, int TE>
+void launch_logits(const uint16_t *x, const float *W, float *lg, int B, int H, int N,
+                   cudaStream_t st) {
+  constexpr int BT = 8 * TT, BE = 16 * TE;
+  dim3 grid((N + BE - 1) / BE, (B + BT - 1) / BT);
+  route_logits_kernel<TT, TE><<<grid, kRouteThreads, 0, st>>>(x, W, lg, B, H, N);
+}
+
+int route_check(const moe_route_cfg *c) {
+  if (!c) return MOE_ERR_INVALID;
+  if (c->B < 0 || c->H <= 0 || c->N <= 0 || c->K <= 0) return MOE_ERR_INVALID;
+  if (c->H % kRouteBK || c->N > 32 * kMaxNI || c->K > 16 || c->K > c->N)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->score_fn != MOE_SCORE_SOFTMAX && c->score_fn != MOE_SCORE_SIGMOID)
+    return MOE_ERR_INVALID;
+  if (c->n_group > 1) {
+    if (c->n_group > 32 || c->N % c->n_group || c->N / c->n_group < 2 || c->topk_group < 1 ||
+        c->topk_group > c->n_group || c->K > c->topk_group * (c->N / c->n_group))
+      return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_route_workspace_size(const moe_route_cfg *cfg) {
+  if (!cfg || cfg->B < 0 || cfg->N <= 0) return 0;
+  return ((size_t)cfg->B * cfg->N * sizeof(float) + 255) / 256 * 256;
+}
+
+extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W,
+                         const float *bias, int32_t *topk_idx, float *topk_w,
+                         int32_t *expert_counts, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+  int rc = route_check(cfg);
+  if (rc) return rc;
+  if (cfg->B == 0) return MOE_OK;
+  if (!x || !W || !topk_idx || !topk_w || !workspace) return MOE_ERR_INVALID;
+  if (workspace_bytes < moe_route_workspace_size(cfg)) return MOE_ERR_INVALID;
+  if ((uintptr_t)x % 16 || (uintptr_t)W % 16) return MOE_ERR_INVALID;
+  cudaStream_t st = as_stream(stream);
+  float *lg = static_cast<float *>(workspace);
+  const int B = cfg->B, H = cfg->H, N = cfg->N;
+  if (expert_counts) {
+    cudaError_t e = cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * N, st);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  // Pick the largest per-thread tile that still gives every SM several CTAs.
+  const long sms = device_sm_count();
+  auto ctas = [&](int tt, int te) {
+    return (long)((N + 16 * te - 1) / (16 * te)) * ((B + 8 * tt - 1) / (8 * tt));
+  };
+  const uint16_t *xb = static_cast<const uint16_t *>(x);
+  if (ctas(4, 4) >= 4 * sms)
+    launch_logits<4, 4>(xb, W, lg, B, H, N, st);
+  else if (ctas(2, 2) >= 4 * sms)
+    launch_logits<2, 2>(xb, W, lg, B, H, N, st);
+  else
+    launch_logits<1, 1>(xb, W, lg, B, H, N, st);
+  rc = check_launch();
+  if (rc) return rc;
+  route_select_kernel<<<(B + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, st>>>(
+      lg, bias, B, N, cfg->K, cfg->n_group, cfg->topk_group, cfg->score_fn, cfg->renorm,
+      cfg->route_scale, topk_idx, topk_w, expert_counts);
+  return check_launch();
+}

@@ -1,0 +1,302 @@
+/*
+ * libmoe — single-GPU MoE layer hot path for GB300 (sm_103a).
+ *
+ * route -> (EPLB map) -> dispatch -> grouped FP8 gate/up + SwiGLU -> grouped FP8
+ * down -> combine, each a C entry point over caller-owned device memory.
+ *
+ * The layer ("DeepEP 完全拆解", §专家并行): a router scores each of N experts for
+ * every one of B tokens of hidden size H, keeps the top K, sends the token through
+ * those K expert FFNs and sums the outputs weighted by the routing weights.  On
+ * one GPU the EP all-to-all "dispatch" becomes a permutation of token rows inside
+ * HBM, and the "combine" becomes a gather + weighted reduce back to token order.
+ *
+ * Conventions shared by every call
+ *   - All pointers are device pointers unless a parameter says "host".  The
+ *     caller allocates and owns all memory; no entry point allocates device
+ *     memory.  Sizes of work buffers come from the *_workspace_size queries.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call only enqueues work; none synchronises the host, so sequences of
+ *     calls can be captured into a CUDA graph.
+ *   - Return value: MOE_OK, or a negative MOE_ERR_* detected on the host before
+ *     anything is launched (MOE_ERR_INVALID: null pointer, bad size or
+ *     alignment; MOE_ERR_UNSUPPORTED: a shape outside the supported range;
+ *     MOE_ERR_CUDA: a CUDA launch or API error, the CUDA error is then available
+ *     from moe_last_cuda_error()).
+ *   - Errors found on the device are OR-ed into the caller's int32 `status` word
+ *     (MOE_STATUS_* bits; sticky until the caller clears it).  moe_read_status()
+ *     is the only call that waits for the device.
+ *   - bf16 tensors are passed as void* and hold IEEE bfloat16 bit patterns.
+ *   - e4m3 tensors hold OCP FP8 E4M3 ("e4m3fn") codes.  Scales are UE8M0
+ *     bytes: value = 2^(byte - 127).
+ *
+ * Packed scale layout ("SF atoms").  Every FP8 operand of the grouped GEMM
+ * carries its 1x128 (activation) or 128x128 (weight) block scales as 512-byte
+ * atoms, one per (128-row block, 128-column block).  Inside an atom, the scale of
+ * row r (0..127 within the block) sits at bytes 16*(r%32) + 4*(r/32) + {0,1,2,3}
+ * (the byte repeated four times, once per 32-column sub-block).  An activation
+ * tensor of `rows` rows and `k` columns has atoms
+ * [rows/128][k/128][512]; a weight tensor of E experts x n rows x k columns has
+ * atoms [E][n/128][k/128][512] (all 512 bytes of a weight atom are equal).
+ *
+ * Tile list.  moe_dispatch describes the rows it wrote as 128-row "M tiles" in
+ * an int32 array `tiles` of 8 + 8*max_tiles entries:
+ *   tiles[0] = number of M tiles, tiles[1] = rows in use (contiguous layout);
+ *   tile i at tiles[8 + 8*i ...]: {first row, physical expert, valid rows (1..128),
+ *   first tile of this expert, number of tiles of this expert, 0, 0, 0}.
+ * Tiles of one expert are consecutive.  The grouped GEMM reads this list on the
+ * device, so the host never needs the routing result.
+ */
+#ifndef LIBMOE_MOE_H
+#define LIBMOE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID (-1)
+#define MOE_ERR_UNSUPPORTED (-2)
+#define MOE_ERR_CUDA (-3)
+
+#define MOE_STATUS_CAPACITY 1  /* a masked-layout expert received more rows than cap */
+#define MOE_STATUS_TIMEOUT 2   /* a bounded device-side wait gave up */
+#define MOE_STATUS_BAD_INDEX 4 /* an expert index outside [0, N) reached dispatch */
+
+#define MOE_SCORE_SOFTMAX 0
+#define MOE_SCORE_SIGMOID 1
+#define MOE_LAYOUT_CONTIG 0
+#define MOE_LAYOUT_MASKED 1
+#define MOE_FMT_FP8 0
+#define MOE_FMT_BF16 1
+#define MOE_GEMM_GATEUP_SWIGLU 0
+#define MOE_GEMM_DOWN 1
+
+/* ------------------------------------------------------------------ route */
+/*
+ * Router ("DeepEP 完全拆解", §专家并行 and §group-limited gating).
+ *   logits z[t][e] = sum_k x[t][k] * W[e][k], accumulated in fp32 by one fused
+ *     multiply-add per k in order k = 0..H-1 (so results are reproducible bit
+ *     for bit);
+ *   score_fn SOFTMAX: choice score z; s = softmax(z) over all N (max-shifted,
+ *     denominator summed in expert order);
+ *   score_fn SIGMOID: s = 1/(1+exp(-z)); choice score c = s + bias (bias may be
+ *     NULL = 0);  exp is the library's own Cody-Waite + degree-7 polynomial;
+ *   n_group > 1: experts form n_group equal groups; a group scores the sum of
+ *     its two best choice scores; the topk_group best groups stay eligible;
+ *   top-K eligible experts by (choice score desc, index asc), stored in that
+ *     order in topk_idx[t][0..K-1];
+ *   topk_w = renorm ? s_k / (s_0+...+s_{K-1}) * route_scale : s_k * route_scale.
+ *   expert_counts[e] (nullable) = number of (t,k) routed to e (overwritten).
+ * Shapes: x bf16 [B][H], W fp32 [N][H], bias fp32 [N], topk_idx int32 [B][K],
+ * topk_w fp32 [B][K].  Limits: H % 32 == 0, N <= 512, K <= 16, n_group <= 32,
+ * N % n_group == 0 with at least 2 experts per group.
+ */
+typedef struct moe_route_cfg {
+  int B, H, N, K;
+  int n_group, topk_group;
+  int score_fn;
+  int renorm;
+  float route_scale;
+} moe_route_cfg;
+
+size_t moe_route_workspace_size(const moe_route_cfg *cfg);
+int moe_route(const moe_route_cfg *cfg, const void *x, const float *W, const float *bias,
+              int32_t *topk_idx, float *topk_w, int32_t *expert_counts, void *workspace,
+              size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------- EPLB */
+/*
+ * Redundant experts ("Large-scale EP: DeepEP, EPLB and two-batch overlap", §EPLB:
+ * 256 logical experts in 288 physical slots, the popular ones copied).  HOST
+ * function, deterministic: the N_phys - N_log hottest logical experts by
+ * counts_host (ties -> lower index) get one replica each; the i-th hottest gets
+ * physical id N_log + i.  Outputs (host arrays): log2phys [N_log][2] (column 0 =
+ * e itself, column 1 = its replica or e), rep [N_log] (1 or 2), phys2log
+ * [N_phys].  moe_dispatch then sends token t of logical expert e to
+ * log2phys[e][t % rep[e]].  Returns MOE_ERR_INVALID unless 0 <= N_phys - N_log <= N_log.
+ */
+int eplb_build_map(const int64_t *counts_host, int N_log, int N_phys, int32_t *log2phys,
+                   int32_t *rep, int32_t *phys2log);
+
+/* --------------------------------------------------------------- dispatch */
+/*
+ * Dispatch ("Large-scale EP ...", §DeepEP: each mode where it belongs — the
+ * contiguous layout after normal dispatch, the masked fixed-shape layout after
+ * low-latency dispatch; "DeepEP 完全拆解", §通信量: each token sent once per
+ * chosen expert, FP8 with s = 1 byte).
+ *   Rows of one physical expert are taken in ascending (t, k) order.
+ *   CONTIG: expert p's segment starts at sum_{q<p} roundup128(count_q); rows
+ *     past a segment's count are padding and are never written or read back.
+ *   MASKED: expert p's slot j is row p*cap + j; rows with j >= cap are dropped
+ *     (row_of = -1, MOE_STATUS_CAPACITY set); cap is a multiple of 128.
+ *   FP8: each token row is quantised once in 1x128 blocks — block exponent
+ *     e = smallest integer with amax <= 448*2^e (amax == 0 -> 0, clamped to
+ *     [-127,127]), code = e4m3_rne_satfinite(x * 2^-e) — and copied to its K
+ *     rows of A [rows][H]; the exponents go to A_sf as SF atoms.
+ *   BF16: rows are copied unchanged (A is bf16 [rows][H], A_sf unused).
+ *   log2phys/rep (nullable, EPLB) map logical to physical experts.
+ *   counts [N_phys]: rows routed to each physical expert (before capacity).
+ *   row_of [B][K]: A row of (t,k); src_of [rows] (nullable): token of each row,
+ *     -1 for padding / empty slots.  tiles: see the tile list above.
+ *   A_shared (nullable, FP8 only): the same quantised rows in token order,
+ *     [roundup128(B)][H] + SF atoms A_shared_sf, and its tile list shared_tiles
+ *     (one expert, id 0) for a shared expert.
+ *   status: device int32, MOE_STATUS_* bits OR-ed in.
+ * Limits: H % 128 == 0, K <= 16, N_phys <= 1024, rows as returned by
+ * moe_dispatch_rows().
+ */
+typedef struct moe_dispatch_cfg {
+  int B, H, K;
+  int N_log, N_phys;
+  int layout;
+  int cap;
+  int fmt;
+} moe_dispatch_cfg;
+
+int64_t moe_dispatch_rows(const moe_dispatch_cfg *cfg);      /* rows of A to allocate */
+int64_t moe_dispatch_max_tiles(const moe_dispatch_cfg *cfg); /* M tiles in `tiles` */
+size_t moe_dispatch_workspace_size(const moe_dispatch_cfg *cfg);
+int moe_dispatch(const moe_dispatch_cfg *cfg, const void *x, const int32_t *topk_idx,
+                 const int32_t *log2phys, const int32_t *rep, void *A, void *A_sf,
+                 int32_t *counts, int32_t *row_of, int32_t *src_of, int32_t *tiles,
+                 void *A_shared, void *A_shared_sf, int32_t *shared_tiles, void *workspace,
+                 size_t workspace_bytes, int32_t *status, void *stream);
+
+/* ------------------------------------------------------------ grouped GEMM */
+/*
+ * Grouped FP8 GEMM over the M tiles of a tile list (DeepGEMM's contiguous and
+ * masked grouped GEMMs, "Large-scale EP ...", §DeepEP; FP8 1x128 x 128x128
+ * "1d2d" scaling, "Single Batch Overlap (SBO)" PR, §3), on tcgen05 tensor
+ * cores with TMEM accumulators, operands fed by TMA.
+ *   acc[r][j] = sum_k a[r][k] * w[j][k] with a = e4m3(A)*2^(sfA-127) per 1x128
+ *   block and w = e4m3(W)*2^(sfW-127) per 128x128 block, fp32 accumulation.
+ *   GATEUP_SWIGLU: W [E][n][k] with n = 2I, rows [0,I) gate and [I,2I) up;
+ *     h = silu(g) * u in fp32, quantised per 1x128 block exactly as dispatch
+ *     quantises x; out = e4m3 [rows][I], out_sf = SF atoms [rows/128][I/128].
+ *   DOWN: W [E][n][k] with n = H, k = I; out = bf16 [rows][n] (round to nearest
+ *     even).  signal (nullable): after the tile (rows R..R+127, any 256 output
+ *     columns) is stored, signal[(R + j) / block_m_signal] += 1 (release, gpu
+ *     scope) for every block j*block_m_signal of the tile; a row block is
+ *     complete when its count reaches n / 256.
+ *   The weight expert of physical expert p is phys2log[p] (nullable = p), so
+ *   EPLB replicas read the same weights.  Rows past a tile's valid count are
+ *   computed but never stored.
+ *   W_sf: SF atoms from moe_pack_weight_scales.
+ *   num_sms: CTAs of the persistent grid (0 = every SM).
+ * Limits: k % 128 == 0, n % 256 == 0, 16-byte aligned pointers.
+ */
+typedef struct moe_gemm_args {
+  int op;
+  int n, k;
+  int64_t rows;      /* rows of A and out */
+  int64_t max_tiles; /* capacity of the tile list */
+  int num_experts;   /* experts in W */
+  const void *A;
+  const void *A_sf;
+  const void *W;
+  const void *W_sf;
+  const int32_t *phys2log;
+  const int32_t *tiles;
+  void *out;
+  void *out_sf;
+  int32_t *signal;
+  int block_m_signal;
+  int num_sms;
+  int32_t *status;
+} moe_gemm_args;
+
+int moe_grouped_gemm_fp8(const moe_gemm_args *args, void *stream);
+
+/*
+ * Weight scales (UE8M0 bytes W_sf [E][n/128][k/128]) -> SF atoms
+ * [E][n/128][k/128][512] (moe_packed_scale_bytes bytes).  One-time setup, off the
+ * hot path.
+ */
+size_t moe_packed_scale_bytes(int E, int n, int k);
+int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf, void *W_sf_packed,
+                           void *stream);
+
+/* ----------------------------------------------------------------- combine */
+/*
+ * Combine ("DeepEP 完全拆解", §专家并行 and §为什么 combine 比 dispatch 慢: move
+ * the expert outputs back and reduce them with the routing weights):
+ *   acc = 0; for k = 0..K-1: if row_of[t][k] >= 0: acc = fma(topk_w[t][k],
+ *   Y[row_of[t][k]], acc); if shared: acc += shared[t]; out[t] = bf16(acc)
+ * in fp32, fixed k order (deterministic).  Y bf16 [rows][H], shared bf16 [B][H]
+ * (nullable), out bf16 [B][H].
+ * Single-batch overlap ("Single Batch Overlap (SBO)" PR, §2): with signal
+ * non-NULL, the row r of (t,k) is read only after signal[r / block_m_signal]
+ * reaches threshold (acquire load, polled); a poll that lasts longer than
+ * timeout_ns gives up, sets MOE_STATUS_TIMEOUT and skips the row.  num_ctas
+ * bounds the grid (0 = one warp per token); a small grid on its own stream runs
+ * beside the producing GEMM.
+ * Limits: H % 256 == 0, K <= 16.
+ */
+typedef struct moe_combine_cfg {
+  int B, H, K;
+  const int32_t *signal;
+  int threshold;
+  int block_m_signal;
+  int64_t timeout_ns;
+  int num_ctas;
+} moe_combine_cfg;
+
+int moe_combine(const moe_combine_cfg *cfg, const void *Y, const int32_t *row_of,
+                const float *topk_w, const void *shared, void *out, int32_t *status,
+                void *stream);
+
+/* ------------------------------------------------------------------ status */
+/* Copies the device status word to *host_status (synchronous). */
+int moe_read_status(const int32_t *status, int32_t *host_status);
+/* The last CUDA error an entry point saw (cudaError_t as int). */
+int moe_last_cuda_error(void);
+/* SM count of the current device. */
+int moe_num_sms(void);
+
+/* ------------------------------------------------------------------- layer */
+/*
+ * The whole layer as one call: route -> dispatch -> gate/up -> down -> [shared
+ * expert gate/up -> down] -> combine, every buffer caller-owned (see the fields).
+ * With sbo != 0 (masked layout) the down GEMM publishes per-block signals and
+ * the combine runs on stream2 beside it, polling them; stream2 must be a stream
+ * other than `stream` (the call orders it after the work before the down GEMM
+ * and makes `stream` wait for the combine).
+ * moe_layer_forward_host additionally copies x from host memory (pinned for
+ * asynchronous copies) to layer->x before, and out to host memory after, all on
+ * `stream`; it returns once the work is enqueued.
+ */
+typedef struct moe_layer {
+  moe_route_cfg route;
+  int N_phys, layout, cap, I, has_shared, sbo, block_m_signal;
+  int64_t rows, max_tiles, timeout_ns;
+  int num_sms, combine_ctas;
+  /* inputs and weights */
+  void *x;                                         /* bf16 [B][H] */
+  const float *W_router, *bias;                    /* [N][H], [N] or NULL */
+  const int32_t *log2phys, *rep, *phys2log;        /* EPLB map or NULL */
+  const void *W13, *W13_sf, *W2, *W2_sf;           /* e4m3 + SF atoms */
+  const void *W13s, *W13s_sf, *W2s, *W2s_sf;       /* shared expert or NULL */
+  /* outputs and intermediates */
+  int32_t *topk_idx;
+  float *topk_w;
+  int32_t *expert_counts, *counts, *row_of, *tiles, *shared_tiles, *signal;
+  void *A, *A_sf, *H1, *H1_sf, *Y;
+  void *As, *As_sf, *Hs, *Hs_sf, *S;
+  void *out;
+  void *route_ws, *dispatch_ws;
+  size_t route_ws_bytes, dispatch_ws_bytes;
+  int32_t *status;
+  void *stream2;
+} moe_layer;
+
+int moe_layer_forward(const moe_layer *layer, void *stream);
+int moe_layer_forward_host(const moe_layer *layer, const void *x_host, void *out_host,
+                           void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LIBMOE_MOE_H */

@@ -1,0 +1,85 @@
+"""Test helpers: seeded workloads on host and device, SF-atom unpacking, tolerances."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+from combine_moe_route_03_gb300 import configs, inputs
+
+# Layer output tolerance: max |gpu - oracle| <= REL * max |oracle| + ABS (bf16 outputs).
+REL, ABS = 2e-2, 1e-3
+
+
+def unpack_sf_atoms(atoms: np.ndarray, rows: int, kb: int) -> np.ndarray:
+    """SF atoms [rows/128][kb][512] -> UE8M0 bytes [rows][kb] (checks the 4 copies agree)."""
+    a = np.asarray(atoms, dtype=np.uint8).reshape(rows // 128, kb, 32, 4, 4)  # r%32, r/32, copy
+    assert np.all(a == a[..., :1]), "scale byte not repeated over its four 32-column sub-blocks"
+    # a[mb, b, r%32, r/32, 0] -> row = mb*128 + (r/32)*32 + r%32
+    return a[..., 0].transpose(0, 3, 2, 1).reshape(rows, kb)
+
+
+def within_tol(got: np.ndarray, ref: np.ndarray, rel=REL, abs_=ABS) -> tuple[bool, float, float]:
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    bound = rel * float(np.max(np.abs(ref))) + abs_ if ref.size else abs_
+    return err <= bound, err, bound
+
+
+@functools.lru_cache(maxsize=None)
+def host_workload(name: str):
+    cfg = configs.ALL[name]
+    x = inputs.make_x(cfg)
+    W, bias = inputs.make_router(cfg)
+    return cfg, x, W, bias
+
+
+def host_experts(name: str) -> dict:
+    """All routed experts (+ shared expert) of a workload, host numpy, stored form.
+    Workloads of the same model (shapes and seed) share one copy."""
+    c = configs.ALL[name]
+    return _experts(c.N, c.H, c.I, c.shared, c.seed)
+
+
+@functools.lru_cache(maxsize=2)
+def _experts(N, H, I, shared, seed) -> dict:
+    cfg = configs.MoEConfig("model", B=1, H=H, N=N, K=1, I=I, shared=shared, seed=seed)
+    ex = inputs.make_all_experts(cfg)
+    if cfg.shared:
+        s = inputs.make_shared_expert(cfg)
+        ex.update(W13s=s[0], W13s_sf=s[1], W2s=s[2], W2s_sf=s[3])
+    return ex
+
+
+def getter(ex: dict):
+    return lambda e: (ex["W13"][e], ex["W13_sf"][e], ex["W2"][e], ex["W2_sf"][e])
+
+
+def shared_of(ex: dict):
+    if "W13s" not in ex:
+        return None
+    return ex["W13s"], ex["W13s_sf"], ex["W2s"], ex["W2s_sf"]
+
+
+def to_dev(a, dev="cuda", dtype=None):
+    if a is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(dev)
+
+
+def device_weights(ex: dict, dev="cuda") -> dict:
+    return {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in ex.items()}
+
+
+def bf16_dev(x_bits: np.ndarray, dev="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x_bits)).view(torch.bfloat16).to(dev)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 device tensor -> uint16 numpy bits."""
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

@@ -1,0 +1,103 @@
+"""Grouped FP8 GEMM (tcgen05) against the oracle's dequantised fp64 products."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_route_03_gb300 import api, inputs
+from support import bits, within_tol
+
+pytestmark = pytest.mark.gpu
+
+
+def pack_sf_atoms(sf: np.ndarray) -> np.ndarray:
+    """UE8M0 bytes [rows][kb] -> SF atoms [rows/128][kb][512] (layout of include/moe.h)."""
+    rows, kb = sf.shape
+    a = sf.reshape(rows // 128, 4, 32, kb).transpose(0, 3, 2, 1)       # mb, kb, r%32, r/32
+    return np.repeat(a[..., None], 4, axis=-1).reshape(-1).copy()
+
+
+def dense_tiles(rows: int, experts_of_tiles=None) -> np.ndarray:
+    mt = rows // 128
+    t = np.zeros(8 + 8 * mt, np.int32)
+    t[0], t[1] = mt, rows
+    ex = np.zeros(mt, np.int32) if experts_of_tiles is None else np.asarray(experts_of_tiles)
+    for i in range(mt):
+        first = int(np.flatnonzero(ex == ex[i])[0])
+        t[8 + 8 * i: 8 + 8 * i + 5] = [128 * i, ex[i], 128, first, int((ex == ex[i]).sum())]
+    return t
+
+
+def activations(rows, k, seed, spread=True):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((rows, k)).astype(np.float32)
+    if spread:   # per-row and per-block magnitudes differ, so every scale byte matters
+        v *= (2.0 ** rng.integers(-6, 7, (rows, k // 128))).repeat(128, axis=1).astype(np.float32)
+    return oracle.quantize_rows(v)
+
+
+@pytest.mark.parametrize("rows,n,k,E", [(128, 256, 128, 1), (256, 512, 512, 1), (384, 256, 1024, 3)])
+def test_down_gemm_matches_fp64(dev, rows, n, k, E):
+    q, sf = activations(rows, k, 1)
+    W, Wsf = zip(*[inputs.make_fp8_matrix(n, k, (5, 77, e)) for e in range(E)])
+    W, Wsf = np.stack(W), np.stack(Wsf)
+    ex = np.arange(rows // 128) % E
+    tiles = dense_tiles(rows, ex)
+    # tiles of one expert must be consecutive: reorder rows by expert
+    order = np.argsort(ex, kind="stable")
+    tiles = dense_tiles(rows, ex[order])
+    qo = q.reshape(-1, 128, k)[order].reshape(rows, k)
+    sfo = sf.reshape(-1, 128, k // 128)[order].reshape(rows, k // 128)
+    A = torch.from_numpy(qo).to(dev)
+    A_sf = torch.from_numpy(pack_sf_atoms(sfo)).to(dev)
+    Wd = torch.from_numpy(W).to(dev)
+    Wsf_atoms = api.pack_weight_scales(torch.from_numpy(Wsf).to(dev))
+    st = api.new_status(dev)
+    out = api.grouped_gemm_fp8(api.GEMM_DOWN, A, A_sf, Wd, Wsf_atoms,
+                               torch.from_numpy(tiles).to(dev), rows // 128, status=st)
+    torch.cuda.synchronize()
+    assert api.read_status(st) == 0
+    got = oracle.bf16_to_f32(bits(out)).astype(np.float64)
+    a = oracle.dequant_rows(qo, sfo)
+    exs = ex[order].repeat(128)
+    for e in range(E):
+        m = exs == e
+        ref = a[m] @ oracle.dequant_blocks(W[e], Wsf[e]).T
+        refb = oracle.bf16_to_f32(oracle.f32_to_bf16(ref.astype(np.float32))).astype(np.float64)
+        # fp32 accumulation vs fp64: at most a bf16 rounding step apart
+        assert np.all(np.abs(got[m] - refb) <= np.abs(refb) * 2.0 ** -7 + 1e-30 + 1e-6 * np.abs(ref).max()), e
+
+
+def test_gateup_swiglu_matches_oracle(dev):
+    rows, I, H = 256, 256, 512
+    q, sf = activations(rows, H, 2, spread=False)
+    W13, W13sf = inputs.make_fp8_matrix(2 * I, H, (6, 1, 0))
+    tiles = dense_tiles(rows)
+    A = torch.from_numpy(q).to(dev)
+    A_sf = torch.from_numpy(pack_sf_atoms(sf)).to(dev)
+    st = api.new_status(dev)
+    H1, H1_sf = api.grouped_gemm_fp8(api.GEMM_GATEUP_SWIGLU, A, A_sf,
+                                     torch.from_numpy(W13[None]).to(dev),
+                                     api.pack_weight_scales(torch.from_numpy(W13sf[None]).to(dev)),
+                                     torch.from_numpy(tiles).to(dev), rows // 128, status=st)
+    torch.cuda.synchronize()
+    assert api.read_status(st) == 0
+    hq = H1.cpu().numpy()
+    hsf = support_unpack(H1_sf.cpu().numpy(), rows, I // 128)
+    a = oracle.dequant_rows(q, sf)
+    gu = a @ oracle.dequant_blocks(W13, W13sf).T
+    g, u = gu[:, :I], gu[:, I:]
+    h = g / (1 + np.exp(-g)) * u
+    hq_ref, hsf_ref = oracle.quantize_rows(h.astype(np.float32))
+    # scale exponents: equal except where amax sits on a power-of-two boundary
+    assert np.mean(hsf == hsf_ref) > 0.99 and np.all(np.abs(hsf.astype(int) - hsf_ref) <= 1)
+    got = oracle.dequant_rows(hq, hsf)
+    ok, err, bound = within_tol(got, h, rel=2 ** -4, abs_=0)
+    assert ok, (err, bound)
+    # most codes identical (fp32 vs fp64 h only moves values across rounding ties)
+    assert np.mean(hq == hq_ref) > 0.98
+
+
+def support_unpack(atoms, rows, kb):
+    from support import unpack_sf_atoms
+    return unpack_sf_atoms(atoms, rows, kb)

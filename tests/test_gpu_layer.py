@@ -1,0 +1,226 @@
+"""Parity of route / dispatch / combine / whole layer with the CPU oracle (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_route_03_gb300 import api, configs, inputs
+from support import (bf16_dev, bits, device_weights, getter, host_experts, host_workload,
+                     shared_of, to_dev, unpack_sf_atoms, within_tol)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny", "small_contig", "small_masked", "small_eplb", "small_sbo"]
+
+
+def eplb_for(cfg, idx_host):
+    if cfg.N_phys == cfg.N:
+        return None
+    return oracle.eplb_build_map(oracle.expert_counts(idx_host, cfg.N), cfg.N, cfg.N_phys)
+
+
+# ------------------------------------------------------------------- route
+@pytest.mark.parametrize("name", SMALL + ["decode", "sbo"])
+def test_route_bit_exact(dev, name):
+    cfg, x, W, bias = host_workload(name)
+    r = api.route(cfg, bf16_dev(x), to_dev(W), to_dev(bias))
+    torch.cuda.synchronize()
+    idx, w, lg = oracle.route(x, W, bias, cfg, want_logits=True)
+    got_lg = r["logits"][: cfg.B * cfg.N * 4].view(torch.float32).cpu().numpy().reshape(cfg.B, cfg.N)
+    assert np.array_equal(got_lg.view(np.uint32), lg.view(np.uint32))
+    assert np.array_equal(r["topk_idx"].cpu().numpy(), idx)
+    assert np.array_equal(r["topk_w"].cpu().numpy().view(np.uint32), w.view(np.uint32))
+    assert np.array_equal(r["counts"].cpu().numpy(), oracle.expert_counts(idx, cfg.N))
+
+
+@pytest.mark.parametrize("name", ["prefill", "skew"])
+def test_route_full_size_sampled(dev, name):
+    """Full B: routing of a sample of tokens bit-exact, counts consistent at any size."""
+    cfg, x, W, bias = host_workload(name)
+    r = api.route(cfg, bf16_dev(x), to_dev(W), to_dev(bias))
+    torch.cuda.synchronize()
+    gi = r["topk_idx"].cpu().numpy()
+    tok = np.random.default_rng(0).choice(cfg.B, 384, replace=False)
+    tok = np.concatenate([tok, [0, cfg.B - 1]]).astype(np.int32)
+    idx, w = oracle.route(x, W, bias, cfg, tokens=tok)
+    assert np.array_equal(gi[tok], idx)
+    assert np.array_equal(r["topk_w"].cpu().numpy()[tok].view(np.uint32), w.view(np.uint32))
+    assert np.array_equal(r["counts"].cpu().numpy(), np.bincount(gi.reshape(-1), minlength=cfg.N))
+    assert all(len(set(row)) == cfg.K for row in gi)   # K distinct experts per token
+
+
+# ---------------------------------------------------------------- dispatch
+def check_dispatch(cfg, x, idx, d, ref, fmt=api.FMT_FP8):
+    rows = d["rows"]
+    assert np.array_equal(d["counts"].cpu().numpy(), ref["cnt"])
+    ro = d["row_of"].cpu().numpy()
+    assert np.array_equal(ro, ref["row_of"])
+    assert np.array_equal(d["src_of"].cpu().numpy(), ref["src_of"][:rows])
+    valid = ro[ro >= 0]
+    A = d["A"].cpu().numpy()
+    if fmt == api.FMT_FP8:
+        assert np.array_equal(A[valid], ref["A"][valid])
+        sf = unpack_sf_atoms(d["A_sf"].cpu().numpy(), rows, cfg.H // 128)
+        assert np.array_equal(sf[valid], ref["sf"][valid])
+    else:
+        assert np.array_equal(A[valid], ref["A"][valid])
+    t = d["tiles"].cpu().numpy()
+    nt = t[0]
+    cnt = np.minimum(ref["cnt"], cfg.cap) if cfg.layout == configs.MASKED else ref["cnt"]
+    assert nt == int(((cnt + 127) // 128).sum())
+    tl = t[8: 8 + 8 * nt].reshape(nt, 8)
+    i = 0
+    for p in range(cfg.N_phys):
+        base = ref["seg_start"][p] if cfg.layout == configs.CONTIG else p * cfg.cap
+        for j in range((cnt[p] + 127) // 128):
+            assert list(tl[i, :5]) == [base + 128 * j, p, min(128, cnt[p] - 128 * j),
+                                       i - j, (cnt[p] + 127) // 128]
+            i += 1
+
+
+@pytest.mark.parametrize("name", SMALL + ["decode", "sbo"])
+def test_dispatch_bit_exact(dev, name):
+    cfg, x, W, bias = host_workload(name)
+    idx, _ = oracle.route(x, W, bias, cfg)
+    emap = eplb_for(cfg, idx)
+    ref = oracle.dispatch(x, idx, cfg, *(emap[:2] if emap else (None, None)))
+    d = api.dispatch(cfg, bf16_dev(x), to_dev(idx), *(map(to_dev, emap[:2]) if emap else (None, None)),
+                     shared=cfg.shared)
+    torch.cuda.synchronize()
+    assert api.read_status(d["status"]) == 0
+    check_dispatch(cfg, x, idx, d, ref)
+    if cfg.shared:
+        q, sf = oracle.quantize_rows(oracle.bf16_to_f32(x))
+        assert np.array_equal(d["As"].cpu().numpy()[: cfg.B], q)
+        srows = d["As"].shape[0]
+        assert np.array_equal(unpack_sf_atoms(d["As_sf"].cpu().numpy(), srows, cfg.H // 128)[: cfg.B], sf)
+
+
+@pytest.mark.parametrize("name", ["prefill", "skew"])
+def test_dispatch_full_size(dev, name):
+    """Full-size dispatch on the oracle's full routing (the oracle routes all B tokens)."""
+    cfg, x, W, bias = host_workload(name)
+    idx, _ = oracle.route(x, W, bias, cfg)
+    ref = oracle.dispatch(x, idx, cfg)
+    d = api.dispatch(cfg, bf16_dev(x), to_dev(idx))
+    torch.cuda.synchronize()
+    check_dispatch(cfg, x, idx, d, ref)
+
+
+def test_dispatch_capacity_overflow_sets_status(dev):
+    cfg = configs.SMALL_MASKED
+    x = inputs.make_x(cfg)
+    idx = np.tile(np.arange(cfg.K, dtype=np.int32), (cfg.B, 1))      # all tokens -> experts 0..K-1
+    ref = oracle.dispatch(x, idx, cfg)
+    assert ref["dropped"]
+    d = api.dispatch(cfg, bf16_dev(x), to_dev(idx))
+    torch.cuda.synchronize()
+    assert api.read_status(d["status"]) & 1
+    check_dispatch(cfg, x, idx, d, ref)
+
+
+def test_dispatch_bad_index_sets_status(dev):
+    cfg = configs.SMALL_CONTIG
+    x = inputs.make_x(cfg)
+    idx = np.tile(np.arange(cfg.K, dtype=np.int32), (cfg.B, 1))
+    idx[5, 1] = cfg.N + 3
+    d = api.dispatch(cfg, bf16_dev(x), to_dev(idx))
+    torch.cuda.synchronize()
+    assert api.read_status(d["status"]) & 4
+    assert d["row_of"].cpu().numpy()[5, 1] == -1
+
+
+def test_empty_batch(dev):
+    cfg = configs.SMALL_CONTIG.with_(B=0)
+    x = torch.empty((0, cfg.H), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((0, cfg.K), dtype=torch.int32, device=dev)
+    d = api.dispatch(cfg, x, idx)
+    torch.cuda.synchronize()
+    assert d["tiles"][0].item() == 0 and int(d["counts"].sum()) == 0
+
+
+# ----------------------------------------------------------------- combine
+@pytest.mark.parametrize("name", ["small_contig", "small_masked", "decode"])
+def test_combine_bit_exact(dev, name):
+    cfg, x, W, bias = host_workload(name)
+    idx, w = oracle.route(x, W, bias, cfg)
+    ref = oracle.dispatch(x, idx, cfg)
+    rng = np.random.default_rng(3)
+    Y = inputs.bf16_bits(rng.standard_normal((ref["rows"], cfg.H)).astype(np.float32))
+    S = inputs.bf16_bits(rng.standard_normal((cfg.B, cfg.H)).astype(np.float32))
+    out_ref = oracle.combine(Y, ref["row_of"], w, S)
+    out = api.combine(bf16_dev(Y), to_dev(ref["row_of"]), to_dev(w), shared=bf16_dev(S))
+    assert np.array_equal(bits(out), out_ref)
+    out_ref = oracle.combine(Y, ref["row_of"], w)
+    out = api.combine(bf16_dev(Y), to_dev(ref["row_of"]), to_dev(w))
+    assert np.array_equal(bits(out), out_ref)
+
+
+def test_bf16_round_trip_is_exact(dev):
+    cfg = configs.SMALL_CONTIG.with_(K=1)
+    x = inputs.make_x(cfg)
+    idx = (np.arange(cfg.B) % cfg.N).astype(np.int32).reshape(-1, 1)
+    d = api.dispatch(cfg, bf16_dev(x), to_dev(idx), fmt=api.FMT_BF16)
+    Y = d["A"].view(torch.bfloat16)
+    out = api.combine(Y, d["row_of"], torch.ones((cfg.B, 1), dtype=torch.float32, device=dev))
+    assert np.array_equal(bits(out), x)
+
+
+def test_combine_poll_times_out_without_hanging(dev):
+    cfg = configs.SMALL_MASKED
+    x = inputs.make_x(cfg)
+    idx = np.tile(np.arange(cfg.K, dtype=np.int32), (cfg.B, 1))
+    rows = cfg.N * 256
+    sig = torch.zeros(rows // 64, dtype=torch.int32, device=dev)        # nothing sets it
+    row_of = to_dev(oracle.dispatch(x, idx, cfg, cap=256)["row_of"][:16])
+    Y = torch.zeros((rows, cfg.H), dtype=torch.bfloat16, device=dev)
+    st = api.new_status(dev)
+    w = torch.ones((16, cfg.K), dtype=torch.float32, device=dev)
+    api.combine(Y, row_of, w, signal=sig, threshold=4, timeout_ns=2_000_000, status=st)
+    torch.cuda.synchronize()
+    assert api.read_status(st) & 2
+
+
+# ------------------------------------------------------------------- layer
+def run_layer(cfg, x, W, bias, ex, emap=None, **kw):
+    lay = api.MoELayer(cfg, to_dev(W), to_dev(bias), device_weights(ex), eplb_map=emap, **kw)
+    out = lay.forward(bf16_dev(x))
+    torch.cuda.synchronize()
+    assert api.read_status(lay.status) == 0
+    return lay, bits(out)
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_layer_matches_oracle(dev, name):
+    cfg, x, W, bias = host_workload(name)
+    ex = host_experts(name)
+    idx, _ = oracle.route(x, W, bias, cfg)
+    emap = eplb_for(cfg, idx)
+    lay, out = run_layer(cfg, x, W, bias, ex, emap)
+    ref = oracle.layer_tokens(cfg, x, W, bias, getter(ex), shared_of(ex))
+    ok, err, bound = within_tol(oracle.bf16_to_f32(out), oracle.bf16_to_f32(ref["out"]))
+    assert ok, (err, bound)
+    # determinism: a second run gives the same bytes
+    out2 = bits(lay.forward())
+    assert np.array_equal(out, out2)
+
+
+def test_layouts_and_eplb_agree_bitwise(dev):
+    """Masked = contiguous, EPLB on = off: same rows, same weights -> same bytes."""
+    base = configs.SMALL_EPLB
+    cfg, x, W, bias = host_workload("small_eplb")
+    ex = host_experts("small_eplb")
+    idx, _ = oracle.route(x, W, bias, cfg)
+    outs = []
+    for c, em in ((base, eplb_for(base, idx)), (base.with_(n_phys=0), None),
+                  (base.with_(n_phys=0, layout=configs.MASKED, cap=384), None)):
+        outs.append(run_layer(c, x, W, bias, ex, em)[1])
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
+def test_sbo_equals_sequential(dev):
+    cfg, x, W, bias = host_workload("small_sbo")
+    ex = host_experts("small_sbo")
+    _, a = run_layer(cfg, x, W, bias, ex)
+    _, b = run_layer(cfg.with_(sbo=False), x, W, bias, ex)
+    assert np.array_equal(a, b)

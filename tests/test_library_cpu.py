@@ -1,0 +1,92 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every declared symbol,
+and its host-only entry points (EPLB map, size queries, argument checks) behave."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from combine_moe_route_03_gb300 import _lib, api, configs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from combine_moe_route_03_gb300 import build
+    build.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    hdr = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return set(re.findall(r"^(?:int|size_t|int64_t)\s+\**(\w+)\(", hdr, re.M))
+
+
+def test_exports_every_declared_symbol(L):
+    decl = declared_symbols()
+    assert decl == set(_lib.SIGNATURES)
+    for name in decl:
+        assert getattr(L, name) is not None
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "moe.h"\nint main(void){moe_route_cfg c; (void)c; return 0;}\n')
+    import subprocess
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           str(src), "-o", str(tmp_path / "t")])
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_eplb_map_matches_oracle(L, seed):
+    rng = np.random.default_rng(seed)
+    N = [8, 32, 256][seed % 3]
+    counts = rng.integers(0, 6, N) * rng.integers(1, 4)        # many ties
+    for extra in (0, 1, N // 8, N):
+        got = api.eplb_build_map(counts, N, N + extra)
+        ref = oracle.eplb_build_map(counts, N, N + extra)
+        for g, r in zip(got, ref):
+            assert np.array_equal(g, r)
+
+
+def test_eplb_map_rejects_bad_sizes(L):
+    with pytest.raises(_lib.MoEError):
+        api.eplb_build_map(np.zeros(8), 8, 7)
+    with pytest.raises(_lib.MoEError):
+        api.eplb_build_map(np.zeros(8), 8, 17)
+
+
+@pytest.mark.parametrize("name", list(configs.ALL))
+def test_dispatch_size_queries(L, name):
+    cfg = configs.ALL[name]
+    sz = api.dispatch_sizes(cfg)
+    if cfg.layout == configs.CONTIG:
+        assert sz["rows"] == oracle.contig_rows_alloc(cfg.B, cfg.K, cfg.N_phys)
+    else:
+        assert sz["rows"] == cfg.N_phys * cfg.cap
+    assert sz["max_tiles"] * 128 == sz["rows"] and sz["ws"] > 0
+
+
+def test_host_argument_checks_return_before_launch(L):
+    bad = _lib.RouteCfg(4, 100, 8, 2, 1, 1, 0, 0, 1.0)           # H % 32 != 0
+    assert L.moe_route(ctypes.byref(bad), None, None, None, None, None, None, None, 0, None) == -2
+    bad = _lib.RouteCfg(4, 128, 8, 9, 1, 1, 0, 0, 1.0)            # K > N
+    assert L.moe_route(ctypes.byref(bad), None, None, None, None, None, None, None, 0, None) == -2
+    bad = _lib.RouteCfg(4, 128, 16, 8, 4, 1, 1, 1, 1.0)           # K > experts in kept groups
+    assert L.moe_route(ctypes.byref(bad), None, None, None, None, None, None, None, 0, None) == -2
+    ok = _lib.RouteCfg(4, 128, 8, 2, 1, 1, 0, 0, 1.0)
+    assert L.moe_route(ctypes.byref(ok), None, None, None, None, None, None, None, 0, None) == -1
+    dc = _lib.DispatchCfg(4, 100, 2, 8, 8, 0, 0, 0)               # H % 128 != 0
+    assert L.moe_dispatch_rows(ctypes.byref(dc)) == 0
+    dc = _lib.DispatchCfg(4, 128, 2, 8, 8, 1, 100, 0)             # cap % 128 != 0
+    assert L.moe_dispatch(ctypes.byref(dc), *([None] * 13), 0, None, None) == -2
+    g = _lib.GemmArgs(0, 300, 128, 128, 1, 1, *([None] * 9), 64, 0, None)   # n % 256 != 0
+    assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -2
+    g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *([None] * 9), 64, 0, None)   # null operands
+    assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
+    cc = _lib.CombineCfg(4, 100, 2, None, 0, 64, 0, 0)             # H % 128 != 0
+    assert L.moe_combine(ctypes.byref(cc), *([None] * 7)) == -2
+    assert L.moe_packed_scale_bytes(2, 256, 384) == 2 * 2 * 3 * 512
