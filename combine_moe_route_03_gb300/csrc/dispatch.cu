@@ -327,8 +327,17 @@ extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int3
                             void *stream) {
   int rc = dispatch_check(c);
   if (rc) return rc;
-  if (!x || !topk_idx || !A || !counts || !row_of || !tiles || !workspace)
-    return MOE_ERR_INVALID;
+  cudaStream_t st = as_stream(stream);
+  const int B = c->B, K = c->K, Np = c->N_phys;
+  if (!counts || !tiles) return MOE_ERR_INVALID;
+  if (B == 0) {  // empty batch: no rows, no tiles, zero counts
+    cudaError_t e = cudaMemsetAsync(tiles, 0, 8 * sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * Np, st);
+    if (e == cudaSuccess && shared_tiles)
+      e = cudaMemsetAsync(shared_tiles, 0, 8 * sizeof(int32_t), st);
+    return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+  }
+  if (!x || !topk_idx || !A || !row_of || !workspace) return MOE_ERR_INVALID;
   if (c->fmt == MOE_FMT_FP8 && !A_sf) return MOE_ERR_INVALID;
   if ((log2phys == nullptr) != (rep == nullptr)) return MOE_ERR_INVALID;
   if (A_shared && (c->fmt != MOE_FMT_FP8 || !A_shared_sf)) return MOE_ERR_INVALID;
@@ -336,15 +345,6 @@ extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int3
   if ((uintptr_t)x % 16 || (uintptr_t)A % 16 || (A_sf && (uintptr_t)A_sf % 16) ||
       (A_shared && (uintptr_t)A_shared % 16))
     return MOE_ERR_INVALID;
-  cudaStream_t st = as_stream(stream);
-  const int B = c->B, K = c->K, Np = c->N_phys;
-  if (B == 0) {
-    cudaError_t e = cudaMemsetAsync(tiles, 0, 8 * sizeof(int32_t), st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * Np, st);
-    if (e == cudaSuccess && shared_tiles)
-      e = cudaMemsetAsync(shared_tiles, 0, 8 * sizeof(int32_t), st);
-    return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
-  }
   const int nchunks = (B + kChunk - 1) / kChunk;
   DispatchWs ws = carve(workspace, B, K, Np);
   const size_t smem = sizeof(int32_t) * ((size_t)kCountWarps * Np + 2 * kChunk * K);

@@ -12,12 +12,17 @@ from combine_moe_route_03_gb300 import configs, inputs
 REL, ABS = 2e-2, 1e-3
 
 
-def unpack_sf_atoms(atoms: np.ndarray, rows: int, kb: int) -> np.ndarray:
-    """SF atoms [rows/128][kb][512] -> UE8M0 bytes [rows][kb] (checks the 4 copies agree)."""
+def unpack_sf_atoms(atoms: np.ndarray, rows: int, kb: int, check_rows=None) -> np.ndarray:
+    """SF atoms [rows/128][kb][512] -> UE8M0 bytes [rows][kb].
+
+    For the rows listed in ``check_rows`` (default: all) it also checks that each
+    scale byte is repeated over its four 32-column sub-blocks."""
     a = np.asarray(atoms, dtype=np.uint8).reshape(rows // 128, kb, 32, 4, 4)  # r%32, r/32, copy
-    assert np.all(a == a[..., :1]), "scale byte not repeated over its four 32-column sub-blocks"
-    # a[mb, b, r%32, r/32, 0] -> row = mb*128 + (r/32)*32 + r%32
-    return a[..., 0].transpose(0, 3, 2, 1).reshape(rows, kb)
+    # a[mb, b, r%32, r/32, c] -> row = mb*128 + (r/32)*32 + r%32
+    full = a.transpose(0, 3, 2, 1, 4).reshape(rows, kb, 4)
+    chk = full if check_rows is None else full[check_rows]
+    assert np.all(chk == chk[..., :1]), "scale byte not repeated over its four 32-column sub-blocks"
+    return full[..., 0].copy()
 
 
 def within_tol(got: np.ndarray, ref: np.ndarray, rel=REL, abs_=ABS) -> tuple[bool, float, float]:

@@ -101,3 +101,8 @@ def test_gateup_swiglu_matches_oracle(dev):
 def support_unpack(atoms, rows, kb):
     from support import unpack_sf_atoms
     return unpack_sf_atoms(atoms, rows, kb)
+
+
+def test_pack_unpack_sf_atoms_inverse():
+    sf = np.random.default_rng(0).integers(0, 255, (384, 5)).astype(np.uint8)
+    assert np.array_equal(support_unpack(pack_sf_atoms(sf), 384, 5), sf)
