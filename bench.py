@@ -1,0 +1,366 @@
+"""MoE-layer throughput on GB300: route -> dispatch -> grouped FP8 FFN -> combine.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|...]
+    python bench.py --impl reference ...     # the CPU oracle, timed on the host cores
+
+One step = one pass of the whole layer (moe_layer_forward: route, dispatch, shared
+expert, gate/up + SwiGLU, down, combine) over one batch of seeded synthetic input,
+inputs resident in HBM.  Prints one JSON line (rank 0).  Under torchrun each rank
+runs its own independent batch (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_moe_route_03_gb300 import _lib, api, configs, inputs  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 GB300; GEMM % FP8 peak; dispatch/combine % HBM BW"
+UNIT = "tokens/s"
+STAGES = _lib.STAGES
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def describe(cfg) -> str:
+    lay = "masked cap %d" % cfg.cap if cfg.layout == configs.MASKED else "contiguous"
+    s = (f"{cfg.name}: B={cfg.B} H={cfg.H} N={cfg.N} K={cfg.K} I={cfg.I} "
+         f"groups={cfg.n_group}/top{cfg.topk_group} {'sigmoid+bias' if cfg.score_fn else 'softmax'} "
+         f"{lay}")
+    if cfg.shared:
+        s += " +1 shared expert"
+    if cfg.N_phys != cfg.N:
+        s += f" EPLB {cfg.N}->{cfg.N_phys}"
+    if cfg.sbo:
+        s += " SBO signals"
+    return s
+
+
+def stage_work(cfg, counts: np.ndarray) -> dict:
+    """Algorithmic bytes and flops per launch of each stage (the minimum a stage must
+    move: padding rows, unused capacity and scale replication not counted)."""
+    B, H, N, K, I = cfg.B, cfg.H, cfg.N, cfg.K, cfg.I
+    R = int(np.minimum(counts, cfg.cap).sum()) if cfg.layout == configs.MASKED else B * K
+    Hb, Ib = H // 128, I // 128
+    touched = counts > 0
+    nt = int(touched.sum())
+    w13 = 2 * I * H + (2 * I // 128) * Hb          # codes + one UE8M0 byte per block
+    w2 = H * I + Hb * Ib
+    sh = 1 if cfg.shared else 0
+    return {
+        "route": dict(bytes=B * H * 2 + N * H * 4 + B * K * 8, flops=2 * B * H * N, bound="alu"),
+        "dispatch": dict(bytes=B * H * 2 + R * (H + Hb * 4 + 8) + sh * B * (H + Hb * 4), flops=0,
+                         bound="hbm"),
+        "shared_gateup": dict(bytes=sh * (w13 + B * (H + Hb) + B * (I + Ib)),
+                              flops=sh * 2 * B * H * 2 * I, bound="hbm"),
+        "shared_down": dict(bytes=sh * (w2 + B * (I + Ib) + B * H * 2), flops=sh * 2 * B * I * H,
+                            bound="hbm"),
+        "gateup": dict(bytes=nt * w13 + R * (H + Hb) + R * (I + Ib), flops=2 * R * H * 2 * I,
+                       bound="hbm"),
+        "down": dict(bytes=nt * w2 + R * (I + Ib) + R * H * 2, flops=2 * R * I * H, bound="hbm"),
+        "combine": dict(bytes=R * H * 2 + sh * B * H * 2 + R * 8 + B * H * 2, flops=0, bound="hbm"),
+    }
+
+
+def physical_work(cfg, counts_phys, phys2log) -> dict:
+    """stage_work for an EPLB layout: replicas read their logical expert's weights."""
+    logical = np.zeros(cfg.N, np.int64)
+    np.add.at(logical, phys2log, counts_phys)
+    return stage_work(cfg.with_(n_phys=0), logical)
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.p = gpu, None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def load_workload(cfg, dev):
+    x = inputs.make_x(cfg)
+    W, bias = inputs.make_router(cfg)
+    host = inputs.fill_expert_weights(cfg, inputs.alloc_expert_weights(cfg))
+    wdev = {k: v.to(dev) for k, v in host.items()}
+    shared = None
+    if cfg.shared:
+        s = inputs.make_shared_expert(cfg)
+        shared = s
+        for k, v in zip(("W13s", "W13s_sf", "W2s", "W2s_sf"), s):
+            wdev[k] = torch.from_numpy(v).to(dev)
+    return x, W, bias, host, shared, wdev
+
+
+def cpu_oracle_rate(cfg, x, W, bias, host, shared, ntok: int, seed: int = 0):
+    """The oracle as it stands, full layer for `ntok` sampled tokens -> tokens/s."""
+    import oracle
+    oracle.build()
+    ex = {k: v.numpy() for k, v in host.items()}
+    get = lambda e: (ex["W13"][e], ex["W13_sf"][e], ex["W2"][e], ex["W2_sf"][e])  # noqa: E731
+    tok = np.sort(np.random.default_rng(seed).choice(cfg.B, ntok, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.layer_tokens(cfg, x, W, bias, get, shared, tokens=tok)
+    dt = time.perf_counter() - t0
+    return ntok / dt, dt, tok
+
+
+def run_reference(args, cfg):
+    """--impl reference: the CPU oracle on the host cores, one sampled token per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg_run = cfg
+    x = inputs.make_x(cfg_run)
+    W, bias = inputs.make_router(cfg_run)
+    # only the experts the sampled tokens need are generated
+    import oracle
+    oracle.build()
+    ntot = args.warmup + args.steps
+    tok = np.random.default_rng(7).choice(cfg.B, ntot, replace=ntot > cfg.B).astype(np.int32)
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            cache[e] = inputs.make_expert(cfg, e)
+        return cache[e]
+    shared = inputs.make_shared_expert(cfg) if cfg.shared else None
+    idx, _ = oracle.route(x, W, bias, cfg, tokens=tok)
+    for e in np.unique(idx):
+        get(int(e))
+    times = []
+    for i in range(ntot):
+        t0 = time.perf_counter()
+        oracle.layer_tokens(cfg, x, W, bias, get, shared, tokens=tok[i:i + 1])
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = args.steps / total
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": describe(cfg), "global_batch": 1,
+                       "step": "one sampled token of the workload through the whole layer"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} tokens of {cfg.name}, one per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(configs.NAMED))
+    ap.add_argument("--cpu-tokens", type=int, default=4,
+                    help="tokens of the CPU-oracle baseline sample (0 = skip)")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    cfg = configs.NAMED[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    cfg = cfg.with_(seed=cfg.seed + rank)           # independent batch per rank
+
+    x, W, bias, host, shared, wdev = load_workload(cfg, dev)
+    emap = None
+    if cfg.N_phys != cfg.N:                          # EPLB map from an unreplicated pass
+        r = api.route(cfg, torch.from_numpy(x).view(torch.bfloat16).to(dev),
+                      torch.from_numpy(W).to(dev), torch.from_numpy(bias).to(dev))
+        emap = api.eplb_build_map(r["counts"].cpu().numpy(), cfg.N, cfg.N_phys)
+    lay = api.MoELayer(cfg, torch.from_numpy(W).to(dev),
+                       None if bias is None else torch.from_numpy(bias).to(dev), wdev,
+                       eplb_map=emap, device=dev)
+    lay.x.copy_(torch.from_numpy(x).view(torch.bfloat16).to(dev))
+    for _ in range(args.warmup):
+        lay.forward()
+    torch.cuda.synchronize()
+    if api.read_status(lay.status) != 0:
+        raise RuntimeError(f"device status {api.read_status(lay.status)}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(_lib.LAYER_EVENTS)]
+           for _ in range(K)]
+    for row in evs:                      # torch creates the CUDA event on first record
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(K):
+        lay.forward(events=evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / K
+    value = world * cfg.B / (ms_step * 1e-3)
+    stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]))
+                for j, s in enumerate(STAGES)}
+
+    # end to end through the host-buffer C entry point
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(x).view(torch.bfloat16).pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        for _ in range(2):
+            lay.forward_host(xh, oh)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(K):
+            lay.forward_host(xh, oh)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        if dist:
+            tt = torch.tensor([ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms = float(tt.item())
+        e2e = {"value": world * cfg.B / (ms / K * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2}
+    st = api.read_status(lay.status)
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+
+    counts = lay.counts.cpu().numpy()
+    work = (stage_work(cfg, counts) if emap is None
+            else physical_work(cfg, counts, emap[2]))
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16_sus"]          # e4m3 = 2x bf16 (nominal dense ratio 4.5 / 2.25)
+    dom = max((s for s in STAGES if work[s]["bytes"]), key=lambda s: stage_ms[s])
+    w = work[dom]
+    dur = stage_ms[dom] * 1e-3
+    t_hbm = w["bytes"] / (pk["hbm"] * 1e9)
+    t_tc = w["flops"] / (fp8_peak * 1e12) if dom not in ("route",) else 0.0
+    if dom == "route":
+        roof = {"bound": "alu", "achieved": w["flops"] / dur / 1e12, "unit": "TFLOP/s"}
+    elif t_tc > t_hbm:
+        roof = {"bound": "tensor", "achieved": w["flops"] / dur / 1e12, "peak": fp8_peak,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": w["bytes"] / dur / 1e9, "peak": pk["hbm"],
+                "unit": "GB/s"}
+    if roof["bound"] == "alu":
+        # fp32 FFMA: 152 SMs x 128 lanes x 2 flop x median SM clock under load
+        mhz = clocks.get("sm_mhz") or 1900.0
+        roof["peak"] = 152 * 128 * 2 * mhz * 1e6 / 1e12
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{pk['src']} ({'sustained bf16 x2 for e4m3' if roof['bound'] == 'tensor' else 'hbm_gbs' if roof['bound'] == 'hbm' else 'FFMA units x clock'})"
+    per_stage = {}
+    for s in STAGES:
+        d = stage_ms[s] * 1e-3
+        if d <= 0 or not work[s]["bytes"]:
+            continue
+        per_stage[s] = {"ms": round(stage_ms[s], 4),
+                        "GBps": round(work[s]["bytes"] / d / 1e9, 1),
+                        "hbm_frac": round(work[s]["bytes"] / d / 1e9 / pk["hbm"], 3),
+                        "TFLOPs": round(work[s]["flops"] / d / 1e12, 1)}
+
+    launches_per_step = 2 + 3 + (2 if cfg.shared else 0) + 2 + 1
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic (seeded; random-init weights stored as e4m3 + UE8M0 128x128 scales)",
+            "config": {"workload": describe(cfg), "global_batch": world * cfg.B,
+                       "parallelism": f"dp{world} (independent batch per GPU)",
+                       "l2": "inputs larger than L2: every step streams the touched experts' "
+                             "e4m3 weights (about 11 GB) from HBM"},
+            "clocks": clocks, "gpu_launches": launches_per_step * K, "roofline": roof,
+            "stages": per_stage, "e2e": e2e}
+    if rank == 0 and world == 1 and args.cpu_tokens > 0:
+        rate, dt, tok = cpu_oracle_rate(cfg, x, W, bias, host, shared, args.cpu_tokens)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{len(tok)} sampled tokens of {cfg.name} through the "
+                                          f"whole layer ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

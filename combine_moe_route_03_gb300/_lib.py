@@ -60,7 +60,10 @@ class Layer(ctypes.Structure):
             "expert_counts", "counts", "row_of", "tiles", "shared_tiles", "signal", "A",
             "A_sf", "H1", "H1_sf", "Y", "As", "As_sf", "Hs", "Hs_sf", "S", "out", "route_ws",
             "dispatch_ws")] + [("route_ws_bytes", _c_sz), ("dispatch_ws_bytes", _c_sz),
-                               ("status", _vp), ("stream2", _vp)]
+                               ("status", _vp), ("stream2", _vp), ("events", _vp)]
+
+LAYER_EVENTS = 8
+STAGES = ("route", "dispatch", "shared_gateup", "shared_down", "gateup", "down", "combine")
 
 
 #: Every symbol include/moe.h declares, with (restype, argtypes).

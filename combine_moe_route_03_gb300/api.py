@@ -252,12 +252,22 @@ class MoELayer:
         lay.stream2 = self.stream2.cuda_stream if self.stream2 is not None else None
         self.layer = lay
 
-    def forward(self, x: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-        """Runs the layer on self.x (copied from ``x`` first when given)."""
+    def forward(self, x: torch.Tensor | None = None, stream=None, events=None) -> torch.Tensor:
+        """Runs the layer on self.x (copied from ``x`` first when given).
+
+        ``events``: optional list of 8 torch.cuda.Event recorded at the stage
+        boundaries (see moe_layer.events)."""
         if x is not None:
             self.x.copy_(x)
-        check(load().moe_layer_forward(ctypes.byref(self.layer), stream_ptr(stream)),
-              "moe_layer_forward")
+        keep = None
+        if events is not None:
+            keep = (ctypes.c_void_p * _lib.LAYER_EVENTS)(*[e.cuda_event for e in events])
+            self.layer.events = ctypes.cast(keep, ctypes.c_void_p)
+        try:
+            check(load().moe_layer_forward(ctypes.byref(self.layer), stream_ptr(stream)),
+                  "moe_layer_forward")
+        finally:
+            self.layer.events = None
         return self.out
 
     def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> None:

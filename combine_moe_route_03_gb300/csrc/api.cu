@@ -76,9 +76,14 @@ cudaEvent_t layer_event(int i) {
 extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   if (!L) return MOE_ERR_INVALID;
   const moe_route_cfg &rc = L->route;
+  auto mark = [&](int i) {
+    if (L->events) cudaEventRecord(static_cast<cudaEvent_t>(L->events[i]), as_stream(stream));
+  };
+  mark(0);
   int rc_ = moe_route(&rc, L->x, L->W_router, L->bias, L->topk_idx, L->topk_w, L->expert_counts,
                       L->route_ws, L->route_ws_bytes, stream);
   if (rc_) return rc_;
+  mark(1);
   moe_dispatch_cfg dc;
   dc.B = rc.B;
   dc.H = rc.H;
@@ -94,6 +99,7 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
                      L->has_shared ? L->shared_tiles : nullptr, L->dispatch_ws,
                      L->dispatch_ws_bytes, L->status, stream);
   if (rc_) return rc_;
+  mark(2);
   const int64_t srows = ((int64_t)rc.B + 127) / 128 * 128;
   if (L->has_shared) {
     moe_gemm_args g{};
@@ -113,6 +119,7 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
     g.num_sms = L->num_sms;
     g.status = L->status;
     if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+    mark(3);
     g.op = MOE_GEMM_DOWN;
     g.n = rc.H;
     g.k = L->I;
@@ -123,6 +130,10 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
     g.out = L->S;
     g.out_sf = nullptr;
     if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+    mark(4);
+  } else {
+    mark(3);
+    mark(4);
   }
   moe_gemm_args g{};
   g.op = MOE_GEMM_GATEUP_SWIGLU;
@@ -142,6 +153,7 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   g.num_sms = L->num_sms;
   g.status = L->status;
   if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+  mark(5);
   g.op = MOE_GEMM_DOWN;
   g.n = rc.H;
   g.k = L->I;
@@ -168,6 +180,7 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
     g.signal = L->signal;
     g.block_m_signal = L->block_m_signal;
     if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+    mark(6);
     cc.signal = L->signal;
     cc.threshold = rc.H / 256;
     cc.block_m_signal = L->block_m_signal;
@@ -178,11 +191,17 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
       return rc_;
     e = cudaEventRecord(layer_event(1), st2);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, layer_event(1), 0);
-    return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    mark(7);
+    return MOE_OK;
   }
   if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
-  return moe_combine(&cc, L->Y, L->row_of, L->topk_w, L->has_shared ? L->S : nullptr, L->out,
-                     L->status, stream);
+  mark(6);
+  rc_ = moe_combine(&cc, L->Y, L->row_of, L->topk_w, L->has_shared ? L->S : nullptr, L->out,
+                    L->status, stream);
+  if (rc_) return rc_;
+  mark(7);
+  return MOE_OK;
 }
 
 extern "C" int moe_layer_forward_host(const moe_layer *L, const void *x_host, void *out_host,

@@ -290,7 +290,13 @@ typedef struct moe_layer {
   size_t route_ws_bytes, dispatch_ws_bytes;
   int32_t *status;
   void *stream2;
+  /* nullable: MOE_LAYER_EVENTS cudaEvent_t handles, recorded on `stream` at the
+     stage boundaries (start, after route, dispatch, shared gate/up, shared down,
+     gate/up, down, combine) so a caller can time each stage of the chain. */
+  void *const *events;
 } moe_layer;
+
+#define MOE_LAYER_EVENTS 8
 
 int moe_layer_forward(const moe_layer *layer, void *stream);
 int moe_layer_forward_host(const moe_layer *layer, const void *x_host, void *out_host,
