@@ -17,6 +17,8 @@
 //                           segment starts, capacity check, M-tile list.
 //   dispatch_scatter_kernel one warp per token: quantise the row once, write its K
 //                           copies and their scales, row_of / src_of.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -347,6 +349,96 @@ extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int3
     return MOE_ERR_INVALID;
   const int nchunks = (B + kChunk - 1) / kChunk;
   DispatchWs ws = carve(workspace, B, K, Np);
+  const size_t smem = sizeof(int32_t) * ((size_t)kCountWarps * Np + 2 * kChunk * K);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(dispatch_count_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  dispatch_count_kernel<<<nchunks, kCountWarps * 32, smem, st>>>(topk_idx, log2phys, rep, B, K,
+                                                                c->N_log, Np, ws, status);
+  if ((rc = check_launch())) return rc;
+  dispatch_scan_kernel<<<1, kScanThreads, 0, st>>>(B, Np, nchunks, c->layout, c->cap,
+                                                   moe_dispatch_rows(c), ws, counts, tiles,
+                                                   src_of, shared_tiles, status);
+  if ((rc = check_launch())) return rc;
+  const int grid = (B + kScatterWarps - 1) / kScatterWarps;
+  const uint16_t *xb = static_cast<const uint16_t *>(x);
+  if (c->fmt == MOE_FMT_FP8)
+    dispatch_scatter_kernel<true><<<grid, kScatterWarps * 32, 0, st>>>(
+        xb, B, c->H, K, Np, c->layout, c->cap, ws, static_cast<uint8_t *>(A),
+        static_cast<uint8_t *>(A_sf), row_of, src_of, static_cast<uint8_t *>(A_shared),
+        static_cast<uint8_t *>(A_shared_sf));
+  else
+    dispatch_scatter_kernel<false><<<grid, kScatterWarps * 32, 0, st>>>(
+        xb, B, c->H, K, Np, c->layout, c->cap, ws, static_cast<uint8_t *>(A), nullptr, row_of,
+        src_of, nullptr, nullptr);
+  return check_launch();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the scratch of the three dispatch kernels lives in this
+// file-scope device array instead of a caller-provided workspace.  Host code must
+// not pass the symbol itself to a kernel (on the host it only names a stand-in);
+// the device address is looked up once per device and cached.
+static __device__ __align__(256) uint8_t g_dispatch_scratch[MOE_DISPATCH_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_dispatch_scratch on the current device (set up on first use).
+int scratch_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+    if (e != cudaSuccess || !p) return set_cuda_error(e != cudaSuccess ? e : cudaErrorUnknown);
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_dispatch_noalloc(const moe_dispatch_cfg *c, const void *x,
+                                    const int32_t *topk_idx, const int32_t *log2phys,
+                                    const int32_t *rep, void *A, void *A_sf, int32_t *counts,
+                                    int32_t *row_of, int32_t *src_of, int32_t *tiles,
+                                    void *A_shared, void *A_shared_sf, int32_t *shared_tiles,
+                                    int32_t *status, void *stream) {
+  int rc = dispatch_check(c);
+  if (rc) return rc;
+  const size_t need = moe_dispatch_workspace_size(c);
+  if (need > MOE_DISPATCH_STATIC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t st = as_stream(stream);
+  const int B = c->B, K = c->K, Np = c->N_phys;
+  if (!counts || !tiles) return MOE_ERR_INVALID;
+  if (B == 0) {
+    cudaError_t e = cudaMemsetAsync(tiles, 0, 8 * sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * Np, st);
+    if (e == cudaSuccess && shared_tiles)
+      e = cudaMemsetAsync(shared_tiles, 0, 8 * sizeof(int32_t), st);
+    return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+  }
+  if (!x || !topk_idx || !A || !row_of) return MOE_ERR_INVALID;
+  if (c->fmt == MOE_FMT_FP8 && !A_sf) return MOE_ERR_INVALID;
+  if ((log2phys == nullptr) != (rep == nullptr)) return MOE_ERR_INVALID;
+  if (A_shared && (c->fmt != MOE_FMT_FP8 || !A_shared_sf)) return MOE_ERR_INVALID;
+  if ((uintptr_t)x % 16 || (uintptr_t)A % 16 || (A_sf && (uintptr_t)A_sf % 16) ||
+      (A_shared && (uintptr_t)A_shared % 16))
+    return MOE_ERR_INVALID;
+  void *scratch = nullptr;
+  if ((rc = scratch_address(&scratch))) return rc;
+  const int nchunks = (B + kChunk - 1) / kChunk;
+  DispatchWs ws = carve(scratch, B, K, Np);
   const size_t smem = sizeof(int32_t) * ((size_t)kCountWarps * Np + 2 * kChunk * K);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(dispatch_count_kernel,

@@ -165,6 +165,36 @@ int moe_dispatch(const moe_dispatch_cfg *cfg, const void *x, const int32_t *topk
                  void *A_shared, void *A_shared_sf, int32_t *shared_tiles, void *workspace,
                  size_t workspace_bytes, int32_t *status, void *stream);
 
+/*
+ * moe_dispatch for callers that cannot allocate device memory.  (The pages have
+ * no counterpart of this entry point; it exists for library users.)
+ *
+ * Some callers cannot call cudaMalloc at all or at the point where they dispatch:
+ * a host framework that owns every byte of device memory through its own
+ * pre-reserved pool, a code path that must never make the device synchronise
+ * (cudaMalloc and cudaFree may), or a plugin host that forbids allocation while
+ * it runs.  This variant takes the same arguments as moe_dispatch except the
+ * workspace: its scratch lives in a fixed device array inside this library,
+ * MOE_DISPATCH_STATIC_SCRATCH_BYTES (4 MiB) large, which every GPU that loads
+ * the library keeps until the process exits.  It allocates nothing.
+ *   - A configuration whose workspace (moe_dispatch_workspace_size) exceeds that
+ *     size is rejected with MOE_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on each device looks up the array's device address (a
+ *     one-time set-up on the then-current device); make that first call before
+ *     any stream capture on the device.
+ *   - All calls share the one array, and it keeps whatever the last call left:
+ *     nothing in it needs to start at zero (every scratch word is written before
+ *     it is read within a call), but two calls whose work overlaps on the GPU (on
+ *     different streams without ordering between them) race on it and give wrong
+ *     results.  Order such calls on one stream or with events.
+ */
+#define MOE_DISPATCH_STATIC_SCRATCH_BYTES (4u << 20)
+int moe_dispatch_noalloc(const moe_dispatch_cfg *cfg, const void *x, const int32_t *topk_idx,
+                         const int32_t *log2phys, const int32_t *rep, void *A, void *A_sf,
+                         int32_t *counts, int32_t *row_of, int32_t *src_of, int32_t *tiles,
+                         void *A_shared, void *A_shared_sf, int32_t *shared_tiles,
+                         int32_t *status, void *stream);
+
 /* ------------------------------------------------------------ grouped GEMM */
 /*
  * Grouped FP8 GEMM over the M tiles of a tile list (DeepGEMM's contiguous and
