@@ -69,13 +69,11 @@ def stage_work(cfg, counts: np.ndarray) -> dict:
         "route": dict(bytes=B * H * 2 + N * H * 4 + B * K * 8, flops=2 * B * H * N, bound="alu"),
         "dispatch": dict(bytes=B * H * 2 + R * (H + Hb * 4 + 8) + sh * B * (H + Hb * 4), flops=0,
                          bound="hbm"),
-        "shared_gateup": dict(bytes=sh * (w13 + B * (H + Hb) + B * (I + Ib)),
-                              flops=sh * 2 * B * H * 2 * I, bound="hbm"),
-        "shared_down": dict(bytes=sh * (w2 + B * (I + Ib) + B * H * 2), flops=sh * 2 * B * I * H,
-                            bound="hbm"),
-        "gateup": dict(bytes=nt * w13 + R * (H + Hb) + R * (I + Ib), flops=2 * R * H * 2 * I,
-                       bound="hbm"),
-        "down": dict(bytes=nt * w2 + R * (I + Ib) + R * H * 2, flops=2 * R * I * H, bound="hbm"),
+        # the shared expert's B rows run inside the routed GEMM launches
+        "gateup": dict(bytes=(nt + sh) * w13 + (R + sh * B) * (H + Hb + I + Ib),
+                       flops=2 * (R + sh * B) * H * 2 * I, bound="hbm"),
+        "down": dict(bytes=(nt + sh) * w2 + (R + sh * B) * (I + Ib + H * 2),
+                     flops=2 * (R + sh * B) * I * H, bound="hbm"),
         "combine": dict(bytes=R * H * 2 + sh * B * H * 2 + R * 8 + B * H * 2, flops=0, bound="hbm"),
     }
 
@@ -206,13 +204,14 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=sorted(configs.NAMED))
+    ap.add_argument("--workload", default="decode",
+                    choices=sorted(configs.NAMED) + sorted(configs.PROFILE))
     ap.add_argument("--cpu-tokens", type=int, default=4,
                     help="tokens of the CPU-oracle baseline sample (0 = skip)")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    cfg = configs.NAMED[args.workload]
+    cfg = {**configs.NAMED, **configs.PROFILE}[args.workload]
     if args.impl == "reference":
         return run_reference(args, cfg)
 
@@ -339,7 +338,7 @@ def main():
                         "hbm_frac": round(work[s]["bytes"] / d / 1e9 / pk["hbm"], 3),
                         "TFLOPs": round(work[s]["flops"] / d / 1e12, 1)}
 
-    launches_per_step = 2 + 3 + (2 if cfg.shared else 0) + 2 + 1
+    launches_per_step = 2 + 3 + 2 + 1
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",

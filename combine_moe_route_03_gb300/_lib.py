@@ -38,7 +38,8 @@ class DispatchCfg(ctypes.Structure):
 class GemmArgs(ctypes.Structure):
     _fields_ = [("op", _c_int), ("n", _c_int), ("k", _c_int), ("rows", _c_i64),
                 ("max_tiles", _c_i64), ("num_experts", _c_int), ("A", _vp), ("A_sf", _vp),
-                ("W", _vp), ("W_sf", _vp), ("phys2log", _vp), ("tiles", _vp), ("out", _vp),
+                ("W", _vp), ("W_sf", _vp), ("phys2log", _vp), ("tiles", _vp), ("tiles2", _vp),
+                ("row_offset2", _c_i64), ("expert2", _c_int), ("out", _vp),
                 ("out_sf", _vp), ("signal", _vp), ("block_m_signal", _c_int),
                 ("num_sms", _c_int), ("status", _vp)]
 
@@ -46,7 +47,7 @@ class GemmArgs(ctypes.Structure):
 class CombineCfg(ctypes.Structure):
     _fields_ = [("B", _c_int), ("H", _c_int), ("K", _c_int), ("signal", _vp),
                 ("threshold", _c_int), ("block_m_signal", _c_int), ("timeout_ns", _c_i64),
-                ("num_ctas", _c_int)]
+                ("num_ctas", _c_int), ("shared_row0", _c_i64)]
 
 
 class Layer(ctypes.Structure):
@@ -56,14 +57,13 @@ class Layer(ctypes.Structure):
                 ("timeout_ns", _c_i64), ("num_sms", _c_int), ("combine_ctas", _c_int)] + [
         (n, _vp) for n in (
             "x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
-            "W2_sf", "W13s", "W13s_sf", "W2s", "W2s_sf", "topk_idx", "topk_w",
-            "expert_counts", "counts", "row_of", "tiles", "shared_tiles", "signal", "A",
-            "A_sf", "H1", "H1_sf", "Y", "As", "As_sf", "Hs", "Hs_sf", "S", "out", "route_ws",
+            "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",
+            "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",
             "dispatch_ws")] + [("route_ws_bytes", _c_sz), ("dispatch_ws_bytes", _c_sz),
                                ("status", _vp), ("stream2", _vp), ("events", _vp)]
 
-LAYER_EVENTS = 8
-STAGES = ("route", "dispatch", "shared_gateup", "shared_down", "gateup", "down", "combine")
+LAYER_EVENTS = 6
+STAGES = ("route", "dispatch", "gateup", "down", "combine")
 
 
 #: Every symbol include/moe.h declares, with (restype, argtypes).

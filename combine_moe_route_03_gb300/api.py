@@ -132,7 +132,8 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
                      out: torch.Tensor | None = None, out_sf: torch.Tensor | None = None,
                      phys2log: torch.Tensor | None = None, signal: torch.Tensor | None = None,
                      block_m_signal: int = 64, num_sms_: int = 0,
-                     status: torch.Tensor | None = None, stream=None):
+                     status: torch.Tensor | None = None, stream=None,
+                     tiles2: torch.Tensor | None = None, row_offset2: int = 0, expert2: int = 0):
     """moe_grouped_gemm_fp8.  W e4m3 [E][n][k]; A e4m3 [rows][k]."""
     E, n, k = W.shape
     rows = A.shape[0]
@@ -146,8 +147,8 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
         out = torch.empty((rows, n), dtype=torch.bfloat16, device=dev)
     st = status if status is not None else new_status(dev)
     g = GemmArgs(op, n, k, rows, max_tiles, E, ptr(A), ptr(A_sf), ptr(W), ptr(W_sf_atoms),
-                 ptr(phys2log), ptr(tiles), ptr(out), ptr(out_sf), ptr(signal), block_m_signal,
-                 num_sms_, ptr(st))
+                 ptr(phys2log), ptr(tiles), ptr(tiles2), row_offset2, expert2, ptr(out),
+                 ptr(out_sf), ptr(signal), block_m_signal, num_sms_, ptr(st))
     check(load().moe_grouped_gemm_fp8(ctypes.byref(g), stream_ptr(stream)), "moe_grouped_gemm_fp8")
     return (out, out_sf) if op == GEMM_GATEUP_SWIGLU else out
 
@@ -155,14 +156,15 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
 def combine(Y: torch.Tensor, row_of: torch.Tensor, topk_w: torch.Tensor,
             shared: torch.Tensor | None = None, out: torch.Tensor | None = None,
             signal: torch.Tensor | None = None, threshold: int = 0, block_m_signal: int = 64,
-            timeout_ns: int = 1_000_000_000, num_ctas: int = 0,
+            timeout_ns: int = 1_000_000_000, num_ctas: int = 0, shared_row0: int = 0,
             status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """moe_combine: Y bf16 [rows][H] -> out bf16 [B][H]."""
     B, K = row_of.shape
     H = Y.shape[1] if Y.dtype == torch.bfloat16 else Y.shape[1] // 2
     if out is None:
         out = torch.empty((B, H), dtype=torch.bfloat16, device=Y.device)
-    cc = CombineCfg(B, H, K, ptr(signal), threshold, block_m_signal, timeout_ns, num_ctas)
+    cc = CombineCfg(B, H, K, ptr(signal), threshold, block_m_signal, timeout_ns, num_ctas,
+                    shared_row0)
     st = status if status is not None else new_status(Y.device)
     check(load().moe_combine(ctypes.byref(cc), ptr(Y), ptr(row_of), ptr(topk_w), ptr(shared),
                              ptr(out), ptr(st), stream_ptr(stream)), "moe_combine")
@@ -174,7 +176,9 @@ class MoELayer:
 
     ``weights``: dict of device uint8 tensors W13 [N][2I][H], W13_sf [N][2I/128][H/128],
     W2 [N][H][I], W2_sf [N][H/128][I/128] (raw UE8M0 bytes; packed here once), and
-    for a shared expert W13s/W13s_sf/W2s/W2s_sf ([1][...] or unbatched).
+    for a shared expert W13s/W13s_sf/W2s/W2s_sf (one expert, batched or not).  The
+    shared expert is stored as expert N of the layer's weight tensors, and its rows
+    follow the routed rows in the row buffers (see moe_layer in include/moe.h).
     """
 
     def __init__(self, cfg: MoEConfig, W_router: torch.Tensor, bias: torch.Tensor | None,
@@ -184,19 +188,26 @@ class MoELayer:
         dev = torch.device(device)
         B, H, I, K = cfg.B, cfg.H, cfg.I, cfg.K
         L = load()
-        self.keep = []
         t = lambda *s, dtype=torch.uint8: torch.empty(s, dtype=dtype, device=dev)  # noqa: E731
         self.x = t(B, H, dtype=torch.bfloat16)
         self.W_router, self.bias = W_router, bias
-        self.W13, self.W2 = weights["W13"], weights["W2"]
-        self.W13_sf = pack_weight_scales(weights["W13_sf"])
-        self.W2_sf = pack_weight_scales(weights["W2_sf"])
         self.has_shared = cfg.shared
+        ne = cfg.N + (1 if cfg.shared else 0)
         if cfg.shared:
-            self.W13s = weights["W13s"].reshape(1, 2 * I, H)
-            self.W2s = weights["W2s"].reshape(1, H, I)
-            self.W13s_sf = pack_weight_scales(weights["W13s_sf"].reshape(1, 2 * I // 128, H // 128))
-            self.W2s_sf = pack_weight_scales(weights["W2s_sf"].reshape(1, H // 128, I // 128))
+            def cat(a, b, *shape):
+                out = t(ne, *shape)
+                out[: cfg.N].copy_(a.reshape(cfg.N, *shape))
+                out[cfg.N].copy_(b.reshape(*shape))
+                return out
+            self.W13 = cat(weights["W13"], weights["W13s"], 2 * I, H)
+            self.W2 = cat(weights["W2"], weights["W2s"], H, I)
+            W13_sf = cat(weights["W13_sf"], weights["W13s_sf"], 2 * I // 128, H // 128)
+            W2_sf = cat(weights["W2_sf"], weights["W2s_sf"], H // 128, I // 128)
+        else:
+            self.W13, self.W2 = weights["W13"], weights["W2"]
+            W13_sf, W2_sf = weights["W13_sf"], weights["W2_sf"]
+        self.W13_sf = pack_weight_scales(W13_sf)
+        self.W2_sf = pack_weight_scales(W2_sf)
         self.log2phys = self.rep = self.phys2log = None
         if eplb_map is not None:
             l2p, rep, p2l = eplb_map
@@ -205,24 +216,21 @@ class MoELayer:
             self.phys2log = torch.from_numpy(np.ascontiguousarray(p2l)).to(dev)
         sz = dispatch_sizes(cfg)
         self.rows, self.max_tiles = sz["rows"], sz["max_tiles"]
-        rows = self.rows
+        self.srows = (B + 127) // 128 * 128 if cfg.shared else 0
+        rows = self.rows + self.srows
         self.topk_idx = t(B, K, dtype=torch.int32)
         self.topk_w = t(B, K, dtype=torch.float32)
         self.expert_counts = t(cfg.N, dtype=torch.int32)
         self.counts = t(cfg.N_phys, dtype=torch.int32)
         self.row_of = t(B, K, dtype=torch.int32)
         self.tiles = t(8 + 8 * self.max_tiles, dtype=torch.int32)
+        self.shared_tiles = t(8 + 8 * (self.srows // 128), dtype=torch.int32) if cfg.shared else None
         self.A = t(rows, H)
         self.A_sf = t(rows * (H // 128) * 4)
         self.H1 = t(rows, I)
         self.H1_sf = t(rows * (I // 128) * 4)
         self.Y = t(rows, H, dtype=torch.bfloat16)
-        srows = (B + 127) // 128 * 128
-        if cfg.shared:
-            self.As, self.As_sf = t(srows, H), t(srows * (H // 128) * 4)
-            self.Hs, self.Hs_sf = t(srows, I), t(srows * (I // 128) * 4)
-            self.S = t(srows, H, dtype=torch.bfloat16)
-            self.shared_tiles = t(8 + 8 * (srows // 128), dtype=torch.int32)
+        self.S = self.Y[self.rows:] if cfg.shared else None
         self.signal = t(rows // cfg.block_m_signal, dtype=torch.int32) if cfg.sbo else None
         self.out = t(B, H, dtype=torch.bfloat16)
         rcfg = _route_cfg(cfg)
@@ -234,17 +242,14 @@ class MoELayer:
         lay.route = rcfg
         lay.N_phys, lay.layout, lay.cap, lay.I = cfg.N_phys, cfg.layout, cfg.cap, I
         lay.has_shared, lay.sbo, lay.block_m_signal = int(cfg.shared), int(cfg.sbo), cfg.block_m_signal
-        lay.rows, lay.max_tiles, lay.timeout_ns = rows, self.max_tiles, timeout_ns
+        lay.rows, lay.max_tiles, lay.timeout_ns = self.rows, self.max_tiles, timeout_ns
         sms = num_sms_ or num_sms()
         lay.num_sms = sms - combine_ctas if cfg.sbo else sms
         lay.combine_ctas = combine_ctas
         names = ["x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
                  "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",
-                 "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws", "dispatch_ws",
-                 "status"]
-        if cfg.shared:
-            names += ["W13s", "W13s_sf", "W2s", "W2s_sf", "As", "As_sf", "Hs", "Hs_sf", "S",
-                      "shared_tiles"]
+                 "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",
+                 "dispatch_ws", "status"]
         for n in names:
             setattr(lay, n, ptr(getattr(self, n)))
         lay.route_ws_bytes = self.route_ws.numel()
@@ -255,8 +260,8 @@ class MoELayer:
     def forward(self, x: torch.Tensor | None = None, stream=None, events=None) -> torch.Tensor:
         """Runs the layer on self.x (copied from ``x`` first when given).
 
-        ``events``: optional list of 8 torch.cuda.Event recorded at the stage
-        boundaries (see moe_layer.events)."""
+        ``events``: optional list of moe_layer.events torch.cuda.Event recorded at the
+        stage boundaries."""
         if x is not None:
             self.x.copy_(x)
         keep = None

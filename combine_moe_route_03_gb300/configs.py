@@ -94,3 +94,13 @@ SMALL_SBO = MoEConfig("small_sbo", B=160, layout=MASKED, cap=256, sbo=True, **_S
 
 SMALL = {c.name: c for c in (SMALL_CONTIG, SMALL_MASKED, SMALL_EPLB, SMALL_SBO)}
 ALL = {**NAMED, **SMALL}
+
+# Profiling shapes: the decode and prefill layers with 64 experts (8 groups of 8),
+# so a profiler capture holds about 3 GB of weights instead of 11 GB while each
+# expert keeps the full-size per-expert row counts (prefill: B*K/N = 256 rows).
+_DSV3_64 = {**_DSV3, "N": 64}
+DECODE_N64 = MoEConfig("decode_n64", B=128, layout=MASKED, cap=128, bias_init="normal",
+                       **_DSV3_64)
+PREFILL_N64 = MoEConfig("prefill_n64", B=2048, layout=CONTIG, router_init="uniform", **_DSV3_64)
+PROFILE = {c.name: c for c in (DECODE_N64, PREFILL_N64)}
+ALL.update(PROFILE)

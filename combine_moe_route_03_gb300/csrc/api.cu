@@ -76,9 +76,14 @@ cudaEvent_t layer_event(int i) {
 extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   if (!L) return MOE_ERR_INVALID;
   const moe_route_cfg &rc = L->route;
+  cudaStream_t st = as_stream(stream);
   auto mark = [&](int i) {
-    if (L->events) cudaEventRecord(static_cast<cudaEvent_t>(L->events[i]), as_stream(stream));
+    if (L->events) cudaEventRecord(static_cast<cudaEvent_t>(L->events[i]), st);
   };
+  if (L->has_shared && !L->shared_tiles) return MOE_ERR_INVALID;
+  const int64_t srows = L->has_shared ? ((int64_t)rc.B + 127) / 128 * 128 : 0;
+  const int64_t rows_all = L->rows + srows;
+  const size_t Hb = rc.H / 128, Ib = L->I / 128;
   mark(0);
   int rc_ = moe_route(&rc, L->x, L->W_router, L->bias, L->topk_idx, L->topk_w, L->expert_counts,
                       L->route_ws, L->route_ws_bytes, stream);
@@ -93,67 +98,38 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   dc.layout = L->layout;
   dc.cap = L->cap;
   dc.fmt = MOE_FMT_FP8;
-  rc_ = moe_dispatch(&dc, L->x, L->topk_idx, L->log2phys, L->rep, L->A, L->A_sf, L->counts,
-                     L->row_of, nullptr, L->tiles, L->has_shared ? L->As : nullptr,
-                     L->has_shared ? L->As_sf : nullptr,
+  uint8_t *A = static_cast<uint8_t *>(L->A), *A_sf = static_cast<uint8_t *>(L->A_sf);
+  rc_ = moe_dispatch(&dc, L->x, L->topk_idx, L->log2phys, L->rep, A, A_sf, L->counts, L->row_of,
+                     nullptr, L->tiles, L->has_shared ? A + L->rows * rc.H : nullptr,
+                     L->has_shared ? A_sf + L->rows * Hb * 4 : nullptr,
                      L->has_shared ? L->shared_tiles : nullptr, L->dispatch_ws,
                      L->dispatch_ws_bytes, L->status, stream);
   if (rc_) return rc_;
   mark(2);
-  const int64_t srows = ((int64_t)rc.B + 127) / 128 * 128;
-  if (L->has_shared) {
-    moe_gemm_args g{};
-    g.op = MOE_GEMM_GATEUP_SWIGLU;
-    g.n = 2 * L->I;
-    g.k = rc.H;
-    g.rows = srows;
-    g.max_tiles = srows / 128;
-    g.num_experts = 1;
-    g.A = L->As;
-    g.A_sf = L->As_sf;
-    g.W = L->W13s;
-    g.W_sf = L->W13s_sf;
-    g.tiles = L->shared_tiles;
-    g.out = L->Hs;
-    g.out_sf = L->Hs_sf;
-    g.num_sms = L->num_sms;
-    g.status = L->status;
-    if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
-    mark(3);
-    g.op = MOE_GEMM_DOWN;
-    g.n = rc.H;
-    g.k = L->I;
-    g.A = L->Hs;
-    g.A_sf = L->Hs_sf;
-    g.W = L->W2s;
-    g.W_sf = L->W2s_sf;
-    g.out = L->S;
-    g.out_sf = nullptr;
-    if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
-    mark(4);
-  } else {
-    mark(3);
-    mark(4);
-  }
   moe_gemm_args g{};
   g.op = MOE_GEMM_GATEUP_SWIGLU;
   g.n = 2 * L->I;
   g.k = rc.H;
-  g.rows = L->rows;
-  g.max_tiles = L->max_tiles;
-  g.num_experts = rc.N;
+  g.rows = rows_all;
+  g.max_tiles = rows_all / 128;
+  g.num_experts = rc.N + (L->has_shared ? 1 : 0);
   g.A = L->A;
   g.A_sf = L->A_sf;
   g.W = L->W13;
   g.W_sf = L->W13_sf;
   g.phys2log = L->phys2log;
   g.tiles = L->tiles;
+  if (L->has_shared) {
+    g.tiles2 = L->shared_tiles;
+    g.row_offset2 = L->rows;
+    g.expert2 = rc.N;
+  }
   g.out = L->H1;
   g.out_sf = L->H1_sf;
   g.num_sms = L->num_sms;
   g.status = L->status;
   if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
-  mark(5);
+  mark(3);
   g.op = MOE_GEMM_DOWN;
   g.n = rc.H;
   g.k = L->I;
@@ -167,11 +143,14 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   cc.B = rc.B;
   cc.H = rc.H;
   cc.K = rc.K;
-  cudaStream_t st = as_stream(stream);
+  const void *S = L->has_shared ? static_cast<uint8_t *>(L->Y) + (size_t)L->rows * rc.H * 2
+                                : nullptr;
+  (void)Ib;
   if (L->sbo) {
-    if (!L->signal || !L->stream2 || L->stream2 == stream || L->block_m_signal <= 0)
+    if (!L->signal || !L->stream2 || L->stream2 == stream || L->block_m_signal <= 0 ||
+        128 % L->block_m_signal)
       return MOE_ERR_INVALID;
-    const size_t nsig = (size_t)(L->rows / L->block_m_signal);
+    const size_t nsig = (size_t)(rows_all / L->block_m_signal);
     cudaError_t e = cudaMemsetAsync(L->signal, 0, nsig * sizeof(int32_t), st);
     if (e == cudaSuccess) e = cudaEventRecord(layer_event(0), st);
     cudaStream_t st2 = as_stream(L->stream2);
@@ -180,27 +159,26 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
     g.signal = L->signal;
     g.block_m_signal = L->block_m_signal;
     if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
-    mark(6);
+    mark(4);
     cc.signal = L->signal;
     cc.threshold = rc.H / 256;
     cc.block_m_signal = L->block_m_signal;
     cc.timeout_ns = L->timeout_ns > 0 ? L->timeout_ns : 1000000000ll;
     cc.num_ctas = L->combine_ctas;
-    if ((rc_ = moe_combine(&cc, L->Y, L->row_of, L->topk_w, L->has_shared ? L->S : nullptr,
-                           L->out, L->status, L->stream2)))
+    cc.shared_row0 = L->rows;
+    if ((rc_ = moe_combine(&cc, L->Y, L->row_of, L->topk_w, S, L->out, L->status, L->stream2)))
       return rc_;
     e = cudaEventRecord(layer_event(1), st2);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, layer_event(1), 0);
     if (e != cudaSuccess) return set_cuda_error(e);
-    mark(7);
+    mark(5);
     return MOE_OK;
   }
   if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
-  mark(6);
-  rc_ = moe_combine(&cc, L->Y, L->row_of, L->topk_w, L->has_shared ? L->S : nullptr, L->out,
-                    L->status, stream);
+  mark(4);
+  rc_ = moe_combine(&cc, L->Y, L->row_of, L->topk_w, S, L->out, L->status, stream);
   if (rc_) return rc_;
-  mark(7);
+  mark(5);
   return MOE_OK;
 }
 

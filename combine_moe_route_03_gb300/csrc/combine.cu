@@ -2,10 +2,10 @@
 //
 // Combine moves every expert output back to its token and reduces the K of them
 // with the routing weights ("DeepEP 完全拆解", §专家并行 and §为什么 combine 比
-// dispatch 慢).  Here it is a gather: one warp owns one token, reads its K rows
-// of Y and sums them in fp32 in the fixed rank order k = 0..K-1, so the result is
-// deterministic (the page lists DeepEP's non-deterministic BF16 pre-reduction as
-// a limitation, §局限).
+// dispatch 慢).  Here it is a gather: for each token, the K rows of Y are summed in
+// fp32 in the fixed rank order k = 0..K-1, so the result is deterministic (the
+// page lists DeepEP's non-deterministic BF16 pre-reduction as a limitation,
+// §局限).
 //
 // Single-batch overlap ("Single Batch Overlap (SBO)" PR, §2): with a signal
 // array, a row is read only after the down GEMM has published all of its output
@@ -19,21 +19,35 @@ namespace {
 
 constexpr int kCombineWarps = 8;
 
+// One warp owns a task = (token, run of `cpt` consecutive 256-column chunks), so a
+// small batch still spreads over many warps and every lane keeps K independent
+// 16-byte loads in flight.
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     const uint16_t *__restrict__ Y, const int32_t *__restrict__ row_of,
     const float *__restrict__ topk_w, const uint16_t *__restrict__ S, uint16_t *__restrict__ out,
-    int B, int H, int K, const int32_t *signal, int threshold, int bm, int64_t timeout_ns,
-    int32_t *status) {
+    int B, int H, int K, int cpt, const int32_t *signal, int threshold, int bm,
+    int64_t timeout_ns, int64_t shared_row0, int32_t *status) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = gridDim.x * kCombineWarps;
-  for (int t = blockIdx.x * kCombineWarps + warp; t < B; t += nwarps) {
+  const int nch = (H + 255) / 256;
+  const int tpt = (nch + cpt - 1) / cpt;  // tasks per token
+  const long ntasks = (long)B * tpt;
+  for (long task = (long)blockIdx.x * kCombineWarps + warp; task < ntasks; task += nwarps) {
+    const int t = (int)(task / tpt);
+    const int c0 = (int)(task % tpt) * cpt;
+    const int c1 = min(nch, c0 + cpt);
     int my_r = -1;
     float my_w = 0.0f;
     if (lane < K) {
       my_r = row_of[(size_t)t * K + lane];
       my_w = topk_w[(size_t)t * K + lane];
-      if (signal && my_r >= 0) {
-        const int32_t *sp = signal + my_r / bm;
+    } else if (lane == K && S) {
+      my_r = 0;  // this lane waits for the shared expert's row of token t
+    }
+    if (signal && my_r >= 0 && lane <= K) {
+      {
+        const int64_t sr = lane < K ? (int64_t)my_r : shared_row0 + t;
+        const int32_t *sp = signal + sr / bm;
         if (ld_acquire_gpu(sp) < threshold) {
           const uint64_t t0 = globaltimer();
           while (ld_acquire_gpu(sp) < threshold) {
@@ -48,6 +62,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
       }
     }
     __syncwarp();
+    const bool use_s = S && (K >= 32 || __shfl_sync(0xffffffffu, my_r, K) >= 0);
     int r[16];
     float w[16];
 #pragma unroll
@@ -55,8 +70,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
       r[k] = __shfl_sync(0xffffffffu, my_r, k);
       w[k] = __shfl_sync(0xffffffffu, my_w, k);
     }
-    for (int h0 = 0; h0 < H; h0 += 256) {
-      const int h = h0 + 8 * lane;
+    for (int c = c0; c < c1; ++c) {
+      const int h = c * 256 + 8 * lane;
       if (h >= H) continue;
       float acc[8];
 #pragma unroll
@@ -72,7 +87,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
           acc[2 * i + 1] = __fmaf_rn(w[k], __uint_as_float(u[i] & 0xffff0000u), acc[2 * i + 1]);
         }
       }
-      if (S) {
+      if (use_s) {
         const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(S + (size_t)t * H + h));
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -106,11 +121,17 @@ extern "C" int moe_combine(const moe_combine_cfg *c, const void *Y, const int32_
   if ((uintptr_t)Y % 16 || (uintptr_t)out % 16 || (shared && (uintptr_t)shared % 16))
     return MOE_ERR_INVALID;
   if (c->signal && (c->block_m_signal <= 0 || c->timeout_ns <= 0)) return MOE_ERR_INVALID;
-  int grid = (c->B + kCombineWarps - 1) / kCombineWarps;
+  // chunks per task: enough tasks for ~4 resident warps per SM sub-partition
+  const long nch = (c->H + 255) / 256;
+  const long want = (long)device_sm_count() * 128;
+  long cpt = ((long)c->B * nch) / want;
+  cpt = cpt < 1 ? 1 : (cpt > nch ? nch : cpt);
+  const long tasks = (long)c->B * ((nch + cpt - 1) / cpt);
+  long grid = (tasks + kCombineWarps - 1) / kCombineWarps;
   if (c->num_ctas > 0 && c->num_ctas < grid) grid = c->num_ctas;
-  combine_kernel<<<grid, kCombineWarps * 32, 0, as_stream(stream)>>>(
+  combine_kernel<<<(unsigned)grid, kCombineWarps * 32, 0, as_stream(stream)>>>(
       static_cast<const uint16_t *>(Y), row_of, topk_w, static_cast<const uint16_t *>(shared),
-      static_cast<uint16_t *>(out), c->B, c->H, c->K, c->signal, c->threshold,
-      c->block_m_signal > 0 ? c->block_m_signal : 1, c->timeout_ns, status);
+      static_cast<uint16_t *>(out), c->B, c->H, c->K, (int)cpt, c->signal, c->threshold,
+      c->block_m_signal > 0 ? c->block_m_signal : 1, c->timeout_ns, c->shared_row0, status);
   return check_launch();
 }

@@ -15,8 +15,9 @@
 //                           rows of that expert in (t,k) order, chunk histogram.
 //   dispatch_scan_kernel    one CTA: chunk bases per expert, expert counts,
 //                           segment starts, capacity check, M-tile list.
-//   dispatch_scatter_kernel one warp per token: quantise the row once, write its K
-//                           copies and their scales, row_of / src_of.
+//   dispatch_scatter_kernel warps over (token, column chunk): quantise each piece of
+//                           a row once, write its K copies and their scales,
+//                           row_of / src_of.
 #include <mutex>
 
 #include "common.cuh"
@@ -204,15 +205,23 @@ __device__ __forceinline__ size_t sf_atom_offset(int64_t r, int kb, int Kb) {
   return ((size_t)(r >> 7) * Kb + kb) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5);
 }
 
+// One warp per task = (token, run of `cpt` 256-column chunks): each lane quantises
+// 8 values, 16 lanes share one 128-column block's amax.  The task holding a token's
+// first chunk also writes row_of / src_of.
 template <bool kFp8>
 __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
     const uint16_t *__restrict__ x, int B, int H, int K, int N_phys, int layout, int cap,
-    DispatchWs ws, uint8_t *__restrict__ A, uint8_t *__restrict__ A_sf,
+    int cpt, DispatchWs ws, uint8_t *__restrict__ A, uint8_t *__restrict__ A_sf,
     int32_t *__restrict__ row_of, int32_t *__restrict__ src_of, uint8_t *__restrict__ As,
     uint8_t *__restrict__ As_sf) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t = blockIdx.x * kScatterWarps + warp;
-  if (t >= B) return;
+  const int nch = (H + 255) / 256;
+  const int tpt = (nch + cpt - 1) / cpt;
+  const long ntasks = (long)B * tpt;
+  const long task = (long)blockIdx.x * kScatterWarps + warp;
+  if (task >= ntasks) return;
+  const int t = (int)(task / tpt);
+  const int c0 = (int)(task % tpt) * cpt, c1 = min(nch, c0 + cpt);
   const int chunk = t / kChunk;
   int64_t my_row = -1;
   if (lane < K) {
@@ -224,8 +233,10 @@ __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
       else if (slot < cap)
         my_row = (int64_t)p * cap + slot;
     }
-    row_of[(size_t)t * K + lane] = (int32_t)my_row;
-    if (src_of && my_row >= 0) src_of[my_row] = t;
+    if (c0 == 0) {
+      row_of[(size_t)t * K + lane] = (int32_t)my_row;
+      if (src_of && my_row >= 0) src_of[my_row] = t;
+    }
   }
   int64_t rows[16];
 #pragma unroll
@@ -233,8 +244,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
 
   const uint16_t *xr = x + (size_t)t * H;
   const int Hb = H / 128;
-  for (int h0 = 0; h0 < H; h0 += 256) {
-    const int h = h0 + 8 * lane;
+  for (int c = c0; c < c1; ++c) {
+    const int h = c * 256 + 8 * lane;
     const bool act = h < H;
     const uint4 v = act ? __ldg(reinterpret_cast<const uint4 *>(xr + h)) : make_uint4(0, 0, 0, 0);
     if (!kFp8) {
@@ -285,6 +296,13 @@ __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
       }
     }
   }
+}
+
+// Chunks per scatter task: enough warps for the whole GPU, at most a full row.
+inline int scatter_cpt(int B, int H) {
+  const long nch = (H + 255) / 256;
+  long cpt = ((long)B * nch) / ((long)device_sm_count() * 128);
+  return (int)(cpt < 1 ? 1 : (cpt > nch ? nch : cpt));
 }
 
 }  // namespace
@@ -362,17 +380,19 @@ extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int3
                                                    moe_dispatch_rows(c), ws, counts, tiles,
                                                    src_of, shared_tiles, status);
   if ((rc = check_launch())) return rc;
-  const int grid = (B + kScatterWarps - 1) / kScatterWarps;
+  const int cpt = scatter_cpt(B, c->H);
+  const long tasks = (long)B * (((c->H + 255) / 256 + cpt - 1) / cpt);
+  const unsigned grid = (unsigned)((tasks + kScatterWarps - 1) / kScatterWarps);
   const uint16_t *xb = static_cast<const uint16_t *>(x);
   if (c->fmt == MOE_FMT_FP8)
     dispatch_scatter_kernel<true><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, ws, static_cast<uint8_t *>(A),
+        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, static_cast<uint8_t *>(A),
         static_cast<uint8_t *>(A_sf), row_of, src_of, static_cast<uint8_t *>(A_shared),
         static_cast<uint8_t *>(A_shared_sf));
   else
     dispatch_scatter_kernel<false><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, ws, static_cast<uint8_t *>(A), nullptr, row_of,
-        src_of, nullptr, nullptr);
+        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, static_cast<uint8_t *>(A), nullptr,
+        row_of, src_of, nullptr, nullptr);
   return check_launch();
 }
 
@@ -452,16 +472,18 @@ extern "C" int moe_dispatch_noalloc(const moe_dispatch_cfg *c, const void *x,
                                                    moe_dispatch_rows(c), ws, counts, tiles,
                                                    src_of, shared_tiles, status);
   if ((rc = check_launch())) return rc;
-  const int grid = (B + kScatterWarps - 1) / kScatterWarps;
+  const int cpt = scatter_cpt(B, c->H);
+  const long tasks = (long)B * (((c->H + 255) / 256 + cpt - 1) / cpt);
+  const unsigned grid = (unsigned)((tasks + kScatterWarps - 1) / kScatterWarps);
   const uint16_t *xb = static_cast<const uint16_t *>(x);
   if (c->fmt == MOE_FMT_FP8)
     dispatch_scatter_kernel<true><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, ws, static_cast<uint8_t *>(A),
+        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, static_cast<uint8_t *>(A),
         static_cast<uint8_t *>(A_sf), row_of, src_of, static_cast<uint8_t *>(A_shared),
         static_cast<uint8_t *>(A_shared_sf));
   else
     dispatch_scatter_kernel<false><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, ws, static_cast<uint8_t *>(A), nullptr, row_of,
-        src_of, nullptr, nullptr);
+        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, static_cast<uint8_t *>(A), nullptr,
+        row_of, src_of, nullptr, nullptr);
   return check_launch();
 }

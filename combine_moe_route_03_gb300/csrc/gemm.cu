@@ -47,21 +47,49 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct GemmParams {
   int op, n, k, Kb, n_tiles, I;
+  int64_t rows;
   const uint8_t *A_sf, *W_sf;
-  const int32_t *phys2log, *tiles;
+  const int32_t *phys2log, *tiles, *tiles2;
+  int row_offset2, expert2, num_experts;
   uint8_t *out, *out_sf;
   int32_t *signal;
   int bm_signal;
   int32_t *status;
 };
 
-__device__ __forceinline__ void decode_unit(const int32_t *tiles, int unit, int n_tiles,
-                                            int &mi, int &ni) {
-  const int g = unit / n_tiles;  // some M tile of the right expert band
-  const int f = tiles[8 + 8 * g + 3], c = tiles[8 + 8 * g + 4];
-  const int local = unit - n_tiles * f;
-  ni = local / c;
-  mi = f + local % c;
+struct Unit {
+  int row0;   // first A / out row of the tile
+  int valid;  // rows of the tile that hold data (0: unit skipped, bad tile entry)
+  int we;     // weight expert
+  int ni;     // output column tile
+};
+
+// Work unit -> (M tile, N tile).  Units of one expert band (its consecutive M
+// tiles) are ordered N-tile-major, M fastest, so CTAs running side by side share
+// the same weight tile through L2.  Units of tiles2 come first.
+__device__ __forceinline__ Unit get_unit(const GemmParams &P, int unit, int units2) {
+  const int32_t *tl = P.tiles;
+  int u = unit;
+  const bool second = unit < units2;
+  if (second)
+    tl = P.tiles2;
+  else
+    u -= units2;
+  const int g = u / P.n_tiles;  // some M tile of the right expert band
+  const int f = tl[8 + 8 * g + 3], c = tl[8 + 8 * g + 4];
+  const int local = u - P.n_tiles * f;
+  const int mi = f + local % c;
+  const int32_t *t = tl + 8 + 8 * mi;
+  Unit r;
+  r.ni = local / c;
+  r.row0 = t[0] + (second ? P.row_offset2 : 0);
+  r.valid = t[2];
+  r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[t[1]] : t[1]);
+  // every role skips a tile entry that would address memory outside the operands
+  if (r.row0 < 0 || (int64_t)r.row0 + 128 > P.rows || r.row0 % 128 || r.we < 0 ||
+      r.we >= P.num_experts || r.valid <= 0 || r.valid > 128 || r.ni >= P.n_tiles)
+    r.valid = 0;
+  return r;
 }
 
 __device__ __forceinline__ size_t sf_atom_off(int64_t r, int kb, int Kb) {
@@ -73,8 +101,12 @@ __device__ __forceinline__ void fail(int32_t *status, volatile int *abort) {
   status_or(status, MOE_STATUS_TIMEOUT);
 }
 
+// tmA loads full 128-row A tiles; tmA32 loads 32-row slices, used for tiles with
+// fewer valid rows so rows that hold no data are never fetched (the MMA then reads
+// stale shared memory for them, which only feeds accumulator rows never stored).
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmA32,
                         const __grid_constant__ CUtensorMap tmW, const GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -98,6 +130,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     *abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmA32);
     tma_prefetch_desc(&tmW);
   }
   if (warp == 1) {
@@ -109,8 +142,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int num_m = P.tiles[0];
-  const int total = num_m * P.n_tiles;
+  const int units2 = P.tiles2 ? P.tiles2[0] * P.n_tiles : 0;
+  const int total = P.tiles[0] * P.n_tiles + units2;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -121,12 +154,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) {
-        int mi, ni;
-        decode_unit(P.tiles, unit, P.n_tiles, mi, ni);
-        const int32_t *tl = P.tiles + 8 + 8 * mi;
-        const int row0 = tl[0];
-        const int pe = tl[1];
-        const int we = P.phys2log ? P.phys2log[pe] : pe;
+        const Unit U = get_unit(P, unit, units2);
+        if (U.valid == 0) {
+          status_or(P.status, MOE_STATUS_BAD_INDEX);
+          continue;
+        }
+        const int row0 = U.row0, we = U.we, ni = U.ni;
+        const int a_slices = U.valid == BM ? 0 : (U.valid + 31) / 32;  // 0: one full box
+        const uint32_t tx = STAGE_TX - (a_slices ? A_BYTES - a_slices * (A_BYTES / 4) : 0);
         int wrow0, wrow1, nb0, nb1;
         if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
           wrow0 = we * P.n + ni * 128;
@@ -149,10 +184,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           const uint32_t full = bar_full + 8 * stage;
-          mbar_arrive_expect_tx(full, STAGE_TX);
+          mbar_arrive_expect_tx(full, tx);
           const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
           const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
-          tma_load_2d(sa, &tmA, full, kb * BK, row0, pol_a);
+          if (a_slices == 0)
+            tma_load_2d(sa, &tmA, full, kb * BK, row0, pol_a);
+          else
+            for (int j = 0; j < a_slices; ++j)
+              tma_load_2d(sa + j * (A_BYTES / 4), &tmA32, full, kb * BK, row0 + 32 * j, pol_a);
           tma_load_2d(sb, &tmW, full, kb * BK, wrow0, pol_w);
           tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
           const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
@@ -190,6 +229,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) {
+        if (get_unit(P, unit, units2).valid == 0) continue;
         if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
           fail(P.status, abort);
           break;
@@ -236,12 +276,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
     uint32_t acc_phase = 0;
     for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
-      int mi, ni;
-      decode_unit(P.tiles, unit, P.n_tiles, mi, ni);
-      const int32_t *tl = P.tiles + 8 + 8 * mi;
-      const int row0 = tl[0], valid = tl[2];
+      const Unit U = get_unit(P, unit, units2);
+      if (U.valid == 0) continue;
+      const int row0 = U.row0, valid = U.valid, ni = U.ni;
       const int64_t r = (int64_t)row0 + row_local;
-      const bool store = row_local < valid;
+      const bool store = row_local < valid && r < P.rows;
       if (!mbar_wait(bar_acc_full, acc_phase, abort, kWaitLimitNs)) {
         fail(P.status, abort);
         break;
@@ -259,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float gf = __uint_as_float(g[i]), uf = __uint_as_float(u[i]);
-            const float v = gf / (1.0f + expf(-gf)) * uf;
+            const float v = __fdividef(gf, 1.0f + __expf(-gf)) * uf;  // silu(g) * u
             h[32 * c + i] = v;
             amax = fmaxf(amax, fabsf(v));
           }
@@ -317,7 +356,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           asm volatile("bar.sync 1, 128;" ::: "memory");
           if (warp == 2 && lane == 0) {
             for (int j = 0; j * P.bm_signal < BM; ++j)
-              if (j * P.bm_signal < valid)
+              if (j * P.bm_signal < valid && row0 + j * P.bm_signal < P.rows)
                 red_release_gpu_add(P.signal + (row0 + j * P.bm_signal) / P.bm_signal, 1);
           }
         }
@@ -361,13 +400,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D byte tensor [rows][cols] (cols contiguous), 128 x 128 boxes, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+// 2-D byte tensor [rows][cols] (cols contiguous), boxes of box_rows x 128 bytes,
+// 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
+              uint32_t box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {128, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -409,12 +450,21 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   const void *ptrs[] = {a->A, a->A_sf, a->W, a->W_sf, a->out, a->out_sf};
   for (const void *p : ptrs)
     if ((uintptr_t)p % 16) return MOE_ERR_INVALID;
-  CUtensorMap mA, mW;
+  CUtensorMap mA, mA32, mW;
   if (!make_map(&mA, a->A, (uint64_t)a->rows, (uint64_t)a->k) ||
+      !make_map(&mA32, a->A, (uint64_t)a->rows, (uint64_t)a->k, 32) ||
       !make_map(&mW, a->W, (uint64_t)a->num_experts * a->n, (uint64_t)a->k))
     return MOE_ERR_CUDA;
+  if (a->tiles2 && (a->expert2 < 0 || a->expert2 >= a->num_experts || a->row_offset2 < 0 ||
+                    a->row_offset2 % 128 || a->row_offset2 >= a->rows))
+    return MOE_ERR_INVALID;
   GemmParams P;
   P.op = a->op;
+  P.rows = a->rows;
+  P.tiles2 = a->tiles2;
+  P.row_offset2 = (int)a->row_offset2;
+  P.expert2 = a->expert2;
+  P.num_experts = a->num_experts;
   P.n = a->n;
   P.k = a->k;
   P.Kb = a->k / BK;
@@ -438,8 +488,8 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
     attr_set = true;
   }
   const int sms = a->num_sms > 0 ? a->num_sms : device_sm_count();
-  const int64_t max_units = a->max_tiles * (a->n / BN);
+  const int64_t max_units = a->tiles2 ? sms : a->max_tiles * (a->n / BN);
   const int grid = (int)(max_units < sms ? max_units : sms);
-  grouped_gemm_kernel<<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mW, P);
+  grouped_gemm_kernel<<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW, P);
   return check_launch();
 }

@@ -18,79 +18,56 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteBK = 32;        // k values staged per step
 constexpr int kRouteThreads = 128;  // 4 warps: 2 (tokens) x 2 (experts)
 
 // Warp tile: lanes as 4 (tokens) x 8 (experts); thread tile TT tokens x TE experts,
 // strided by 4 and 8 so the shared-memory reads of one warp hit 4 and 8 distinct
-// rows whose 36-float pitch puts them in distinct banks.
-template <int TT, int TE>
+// rows whose pitches (80 B for x, 144 B for W) put them in distinct banks.
+// Operands stream through an S-stage cp.async ring of 32-wide k chunks (x stays
+// bf16 in shared memory and is widened when read), so even the small decode grids
+// keep enough loads in flight to cover the memory latency of each chunk.
+template <int TT, int TE, int S, int kRouteBK>
 __global__ void __launch_bounds__(kRouteThreads) route_logits_kernel(const uint16_t *__restrict__ x,
                                                                      const float *__restrict__ W,
                                                                      float *__restrict__ logits,
                                                                      int B, int H, int N) {
   constexpr int BT = 2 * 4 * TT;  // tokens per CTA
   constexpr int BE = 2 * 8 * TE;  // experts per CTA
-  constexpr int LD = kRouteBK + 4;
-  __shared__ __align__(16) float xs[2][BT][LD];
-  __shared__ __align__(16) float ws[2][BE][LD];
+  constexpr int LDX = kRouteBK + 8;  // bf16 per staged x row
+  constexpr int LDW = kRouteBK + 4;  // fp32 per staged W row
+  constexpr int XST = BT * LDX, WST = BE * LDW;
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  uint16_t *xs = reinterpret_cast<uint16_t *>(route_smem);                // [S][BT][LDX]
+  float *ws = reinterpret_cast<float *>(route_smem + S * XST * 2);        // [S][BE][LDW]
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int tl = lane >> 3, el = lane & 7;
   const int wt = warp >> 1, we = warp & 1;
   const int t0 = blockIdx.y * BT, e0 = blockIdx.x * BE;
+  const int nchunks = H / kRouteBK;
 
-  // Staging maps: x chunk BT x 32 bf16 = BT*4 16-byte pieces; W chunk BE x 32 fp32
-  // = BE*8 16-byte pieces.
-  auto load_x = [&](int kc, uint4 *reg) {
-#pragma unroll
-    for (int it = 0; it < (BT * 4 + kRouteThreads - 1) / kRouteThreads; ++it) {
-      const int i = tid + it * kRouteThreads;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (i < BT * 4) {
-        const int t = i >> 2, k = kc + (i & 3) * 8;
-        if (t0 + t < B) v = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + t) * H + k));
-      }
-      reg[it] = v;
+  auto load = [&](int c, int buf) {
+    const int kc = c * kRouteBK;
+    constexpr int XP = kRouteBK / 8, WP = kRouteBK / 4;  // 16-byte pieces per row
+    for (int i = tid; i < BT * XP; i += kRouteThreads) {
+      const int t = i / XP, k = (i % XP) * 8;
+      const bool ok = t0 + t < B;
+      const uint16_t *src = x + (size_t)(ok ? t0 + t : 0) * H + kc + k;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                       smem_u32(xs + buf * XST + t * LDX + k)),
+                   "l"(src), "r"(ok ? 16 : 0)
+                   : "memory");
     }
-  };
-  auto store_x = [&](int buf, const uint4 *reg) {
-#pragma unroll
-    for (int it = 0; it < (BT * 4 + kRouteThreads - 1) / kRouteThreads; ++it) {
-      const int i = tid + it * kRouteThreads;
-      if (i < BT * 4) {
-        const int t = i >> 2, k = (i & 3) * 8;
-        const uint4 v = reg[it];
-        float4 a, b;
-        a.x = __uint_as_float(v.x << 16);
-        a.y = __uint_as_float(v.x & 0xffff0000u);
-        a.z = __uint_as_float(v.y << 16);
-        a.w = __uint_as_float(v.y & 0xffff0000u);
-        b.x = __uint_as_float(v.z << 16);
-        b.y = __uint_as_float(v.z & 0xffff0000u);
-        b.z = __uint_as_float(v.w << 16);
-        b.w = __uint_as_float(v.w & 0xffff0000u);
-        *reinterpret_cast<float4 *>(&xs[buf][t][k]) = a;
-        *reinterpret_cast<float4 *>(&xs[buf][t][k + 4]) = b;
-      }
+    for (int i = tid; i < BE * WP; i += kRouteThreads) {
+      const int e = i / WP, k = (i % WP) * 4;
+      const bool ok = e0 + e < N;
+      const float *src = W + (size_t)(ok ? e0 + e : 0) * H + kc + k;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                       smem_u32(ws + buf * WST + e * LDW + k)),
+                   "l"(src), "r"(ok ? 16 : 0)
+                   : "memory");
     }
-  };
-  auto load_w = [&](int kc, int buf) {
-#pragma unroll
-    for (int it = 0; it < (BE * 8 + kRouteThreads - 1) / kRouteThreads; ++it) {
-      const int i = tid + it * kRouteThreads;
-      if (i < BE * 8) {
-        const int e = i >> 3, k = (i & 7) * 4;
-        const uint32_t dst = smem_u32(&ws[buf][e][k]);
-        const bool ok = e0 + e < N;
-        const float *src = W + (size_t)(ok ? e0 + e : 0) * H + kc + k;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                     "r"(ok ? 16 : 0)
-                     : "memory");
-      }
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
   };
 
   float acc[TT][TE];
@@ -99,31 +76,30 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_kernel(const uint1
 #pragma unroll
     for (int j = 0; j < TE; ++j) acc[i][j] = 0.0f;
 
-  constexpr int XR = (BT * 4 + kRouteThreads - 1) / kRouteThreads;
-  uint4 xreg[XR];
-  load_x(0, xreg);
-  load_w(0, 0);
-  store_x(0, xreg);
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-
-  const int nchunks = H / kRouteBK;
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    if (s < nchunks) load(s, s);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
-    const bool more = c + 1 < nchunks;
-    if (more) {
-      load_x((c + 1) * kRouteBK, xreg);
-      load_w((c + 1) * kRouteBK, buf ^ 1);
-    }
+    asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");
+    __syncthreads();  // chunk c visible to all; chunk c-1's buffer no longer read
+    if (c + S - 1 < nchunks) load(c + S - 1, (c + S - 1) % S);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const uint16_t *xb = xs + (c % S) * XST;
+    const float *wb = ws + (c % S) * WST;
 #pragma unroll
     for (int k4 = 0; k4 < kRouteBK; k4 += 4) {
       float4 xv[TT], wv[TE];
 #pragma unroll
-      for (int i = 0; i < TT; ++i)
-        xv[i] = *reinterpret_cast<const float4 *>(&xs[buf][wt * 4 * TT + tl + 4 * i][k4]);
+      for (int i = 0; i < TT; ++i) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(xb + (wt * 4 * TT + tl + 4 * i) * LDX + k4);
+        xv[i] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                            __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+      }
 #pragma unroll
       for (int j = 0; j < TE; ++j)
-        wv[j] = *reinterpret_cast<const float4 *>(&ws[buf][we * 8 * TE + el + 8 * j][k4]);
+        wv[j] = *reinterpret_cast<const float4 *>(wb + (we * 8 * TE + el + 8 * j) * LDW + k4);
       // k order is strictly sequential for every output
 #pragma unroll
       for (int i = 0; i < TT; ++i)
@@ -135,11 +111,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_kernel(const uint1
           acc[i][j] = __fmaf_rn(xv[i].w, wv[j].w, acc[i][j]);
         }
     }
-    if (more) {
-      store_x(buf ^ 1, xreg);
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
-    __syncthreads();
   }
 #pragma unroll
   for (int i = 0; i < TT; ++i) {
@@ -299,18 +270,27 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
   }
 }
 
-template <int TT, int TE>
-void launch_logits(const uint16_t *x, const float *W, float *lg, int B, int H, int N,
-                   cudaStream_t st) {
+template <int TT, int TE, int S, int kRouteBK>
+int launch_logits(const uint16_t *x, const float *W, float *lg, int B, int H, int N,
+                  cudaStream_t st) {
   constexpr int BT = 8 * TT, BE = 16 * TE;
+  constexpr size_t smem = (size_t)S * (BT * (kRouteBK + 8) * 2 + BE * (kRouteBK + 4) * 4);
+  static bool attr = false;
+  if (!attr && smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(route_logits_kernel<TT, TE, S, kRouteBK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  attr = true;
   dim3 grid((N + BE - 1) / BE, (B + BT - 1) / BT);
-  route_logits_kernel<TT, TE><<<grid, kRouteThreads, 0, st>>>(x, W, lg, B, H, N);
+  route_logits_kernel<TT, TE, S, kRouteBK><<<grid, kRouteThreads, smem, st>>>(x, W, lg, B, H, N);
+  return check_launch();
 }
 
 int route_check(const moe_route_cfg *c) {
   if (!c) return MOE_ERR_INVALID;
   if (c->B < 0 || c->H <= 0 || c->N <= 0 || c->K <= 0) return MOE_ERR_INVALID;
-  if (c->H % kRouteBK || c->N > 32 * kMaxNI || c->K > 16 || c->K > c->N)
+  if (c->H % 32 || c->N > 32 * kMaxNI || c->K > 16 || c->K > c->N)
     return MOE_ERR_UNSUPPORTED;
   if (c->score_fn != MOE_SCORE_SOFTMAX && c->score_fn != MOE_SCORE_SIGMOID)
     return MOE_ERR_INVALID;
@@ -356,12 +336,13 @@ extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W
   };
   const uint16_t *xb = static_cast<const uint16_t *>(x);
   if (ctas(4, 4) >= 4 * sms)
-    launch_logits<4, 4>(xb, W, lg, B, H, N, st);
+    rc = launch_logits<4, 4, 4, 32>(xb, W, lg, B, H, N, st);
   else if (ctas(2, 2) >= 4 * sms)
-    launch_logits<2, 2>(xb, W, lg, B, H, N, st);
+    rc = launch_logits<2, 2, 4, 64>(xb, W, lg, B, H, N, st);
+  else if (H % 128 == 0)
+    rc = launch_logits<1, 1, 4, 128>(xb, W, lg, B, H, N, st);
   else
-    launch_logits<1, 1>(xb, W, lg, B, H, N, st);
-  rc = check_launch();
+    rc = launch_logits<1, 1, 8, 32>(xb, W, lg, B, H, N, st);
   if (rc) return rc;
   route_select_kernel<<<(B + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, st>>>(
       lg, bias, B, N, cfg->K, cfg->n_group, cfg->topk_group, cfg->score_fn, cfg->renorm,

@@ -215,6 +215,9 @@ int moe_dispatch_noalloc(const moe_dispatch_cfg *cfg, const void *x, const int32
  *   EPLB replicas read the same weights.  Rows past a tile's valid count are
  *   computed but never stored.
  *   W_sf: SF atoms from moe_pack_weight_scales.
+ *   tiles2 (nullable): tiles of a second group, e.g. a shared expert whose rows
+ *     sit at row_offset2 in A/out and whose weights are expert expert2 of W; its
+ *     tiles join the same persistent grid (scheduled before those of `tiles`).
  *   num_sms: CTAs of the persistent grid (0 = every SM).
  * Limits: k % 128 == 0, n % 256 == 0, 16-byte aligned pointers.
  */
@@ -230,6 +233,9 @@ typedef struct moe_gemm_args {
   const void *W_sf;
   const int32_t *phys2log;
   const int32_t *tiles;
+  const int32_t *tiles2; /* nullable: a second tile list computed in the same launch */
+  int64_t row_offset2;   /* added to every row of tiles2 (A and out rows) */
+  int expert2;           /* weight expert of every tile of tiles2 (phys2log unused) */
   void *out;
   void *out_sf;
   int32_t *signal;
@@ -260,9 +266,9 @@ int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf, void *W_sf_
  * Single-batch overlap ("Single Batch Overlap (SBO)" PR, §2): with signal
  * non-NULL, the row r of (t,k) is read only after signal[r / block_m_signal]
  * reaches threshold (acquire load, polled); a poll that lasts longer than
- * timeout_ns gives up, sets MOE_STATUS_TIMEOUT and skips the row.  num_ctas
- * bounds the grid (0 = one warp per token); a small grid on its own stream runs
- * beside the producing GEMM.
+ * timeout_ns gives up, sets MOE_STATUS_TIMEOUT and skips the row (the shared row
+ * likewise, see shared_row0).  num_ctas bounds the grid (0 = as many warps as the
+ * work splits into); a small grid on its own stream runs beside the producing GEMM.
  * Limits: H % 256 == 0, K <= 16.
  */
 typedef struct moe_combine_cfg {
@@ -272,6 +278,9 @@ typedef struct moe_combine_cfg {
   int block_m_signal;
   int64_t timeout_ns;
   int num_ctas;
+  int64_t shared_row0; /* with signal and shared: row (in the signal's row space) of
+                          shared[0]; shared[t] is read after signal[(shared_row0 + t) /
+                          block_m_signal] reaches threshold */
 } moe_combine_cfg;
 
 int moe_combine(const moe_combine_cfg *cfg, const void *Y, const int32_t *row_of,
@@ -288,8 +297,12 @@ int moe_num_sms(void);
 
 /* ------------------------------------------------------------------- layer */
 /*
- * The whole layer as one call: route -> dispatch -> gate/up -> down -> [shared
- * expert gate/up -> down] -> combine, every buffer caller-owned (see the fields).
+ * The whole layer as one call: route -> dispatch -> gate/up -> down -> combine,
+ * every buffer caller-owned (see the fields).
+ * Shared expert (has_shared != 0): its weights are the last expert (index N) of
+ * W13 / W13_sf / W2 / W2_sf, which then hold N + 1 experts; its rows (the batch in
+ * token order, roundup128(B) rows) follow the `rows` routed rows in A, A_sf, H1,
+ * H1_sf and Y, and its tiles (shared_tiles) run inside the routed GEMM launches.
  * With sbo != 0 (masked layout) the down GEMM publishes per-block signals and
  * the combine runs on stream2 beside it, polling them; stream2 must be a stream
  * other than `stream` (the call orders it after the work before the down GEMM
@@ -307,26 +320,25 @@ typedef struct moe_layer {
   void *x;                                         /* bf16 [B][H] */
   const float *W_router, *bias;                    /* [N][H], [N] or NULL */
   const int32_t *log2phys, *rep, *phys2log;        /* EPLB map or NULL */
-  const void *W13, *W13_sf, *W2, *W2_sf;           /* e4m3 + SF atoms */
-  const void *W13s, *W13s_sf, *W2s, *W2s_sf;       /* shared expert or NULL */
-  /* outputs and intermediates */
+  const void *W13, *W13_sf, *W2, *W2_sf;           /* e4m3 + SF atoms, N (+1) experts */
+  /* outputs and intermediates; row buffers hold rows (+ roundup128(B)) rows */
   int32_t *topk_idx;
   float *topk_w;
-  int32_t *expert_counts, *counts, *row_of, *tiles, *shared_tiles, *signal;
+  int32_t *expert_counts, *counts, *row_of, *tiles, *shared_tiles;
+  int32_t *signal; /* sbo: (rows + shared rows) / block_m_signal counters */
   void *A, *A_sf, *H1, *H1_sf, *Y;
-  void *As, *As_sf, *Hs, *Hs_sf, *S;
   void *out;
   void *route_ws, *dispatch_ws;
   size_t route_ws_bytes, dispatch_ws_bytes;
   int32_t *status;
   void *stream2;
   /* nullable: MOE_LAYER_EVENTS cudaEvent_t handles, recorded on `stream` at the
-     stage boundaries (start, after route, dispatch, shared gate/up, shared down,
-     gate/up, down, combine) so a caller can time each stage of the chain. */
+     stage boundaries (start, after route, dispatch, gate/up, down, combine) so a
+     caller can time each stage of the chain. */
   void *const *events;
 } moe_layer;
 
-#define MOE_LAYER_EVENTS 8
+#define MOE_LAYER_EVENTS 6
 
 int moe_layer_forward(const moe_layer *layer, void *stream);
 int moe_layer_forward_host(const moe_layer *layer, const void *x_host, void *out_host,
