@@ -62,6 +62,7 @@ struct Unit {
   int valid;  // rows of the tile that hold data (0: unit skipped, bad tile entry)
   int we;     // weight expert
   int ni;     // output column tile
+  int band;   // M tiles sharing this unit's weight tile
 };
 
 // Work unit -> (M tile, N tile).  Units of one expert band (its consecutive M
@@ -82,6 +83,7 @@ __device__ __forceinline__ Unit get_unit(const GemmParams &P, int unit, int unit
   const int32_t *t = tl + 8 + 8 * mi;
   Unit r;
   r.ni = local / c;
+  r.band = c;
   r.row0 = t[0] + (second ? P.row_offset2 : 0);
   r.valid = t[2];
   r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[t[1]] : t[1]);
@@ -148,7 +150,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+      // A tiles are re-read by every N tile of their expert: keep them in L2.  A
+      // weight tile read by one M tile only is streamed (evict first); one shared by
+      // several M tiles (read by neighbouring CTAs at about the same time) is kept.
+      const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_normal();
+      const uint64_t pol_a = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -160,6 +166,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           continue;
         }
         const int row0 = U.row0, we = U.we, ni = U.ni;
+        const uint64_t pol_w = U.band > 1 ? pol_keep : pol_stream;
         const int a_slices = U.valid == BM ? 0 : (U.valid + 31) / 32;  // 0: one full box
         const uint32_t tx = STAGE_TX - (a_slices ? A_BYTES - a_slices * (A_BYTES / 4) : 0);
         int wrow0, wrow1, nb0, nb1;

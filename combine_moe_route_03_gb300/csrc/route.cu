@@ -88,18 +88,28 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_kernel(const uint1
     asm volatile("cp.async.commit_group;" ::: "memory");
     const uint16_t *xb = xs + (c % S) * XST;
     const float *wb = ws + (c % S) * WST;
+    // operands of step k4 + 4 are fetched while step k4's FMAs run
+    uint2 xr[TT];
+    float4 wr[TE];
+    auto fetch = [&](int k4) {
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+        xr[i] = *reinterpret_cast<const uint2 *>(xb + (wt * 4 * TT + tl + 4 * i) * LDX + k4);
+#pragma unroll
+      for (int j = 0; j < TE; ++j)
+        wr[j] = *reinterpret_cast<const float4 *>(wb + (we * 8 * TE + el + 8 * j) * LDW + k4);
+    };
+    fetch(0);
 #pragma unroll
     for (int k4 = 0; k4 < kRouteBK; k4 += 4) {
       float4 xv[TT], wv[TE];
 #pragma unroll
-      for (int i = 0; i < TT; ++i) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(xb + (wt * 4 * TT + tl + 4 * i) * LDX + k4);
-        xv[i] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
-                            __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-      }
+      for (int i = 0; i < TT; ++i)
+        xv[i] = make_float4(__uint_as_float(xr[i].x << 16), __uint_as_float(xr[i].x & 0xffff0000u),
+                            __uint_as_float(xr[i].y << 16), __uint_as_float(xr[i].y & 0xffff0000u));
 #pragma unroll
-      for (int j = 0; j < TE; ++j)
-        wv[j] = *reinterpret_cast<const float4 *>(wb + (we * 8 * TE + el + 8 * j) * LDW + k4);
+      for (int j = 0; j < TE; ++j) wv[j] = wr[j];
+      if (k4 + 4 < kRouteBK) fetch(k4 + 4);
       // k order is strictly sequential for every output
 #pragma unroll
       for (int i = 0; i < TT; ++i)
@@ -270,6 +280,135 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
   }
 }
 
+// Top-2 of two ranked pairs: (a1, a2) <- best two of {a1, a2, b1, b2}.
+__device__ __forceinline__ void merge_top2(Cand &a1, Cand &a2, const Cand &b1, const Cand &b2) {
+  if (before(b1, a1)) {
+    a2 = before(a1, b2) ? a1 : b2;
+    a1 = b1;
+  } else if (before(b1, a2)) {
+    a2 = b1;
+  }
+}
+
+// Selection with contiguous ownership: lane l holds experts [l*NPL, (l+1)*NPL).
+// When a group's experts fill whole lanes (group size a multiple of NPL, a power
+// of two of lanes per group), a group's top two are a scan of the lane's own
+// values plus log2(lanes per group) butterfly merges, and each top-K round is a
+// scan of NPL values plus one warp argmax.  Same results as route_select_kernel.
+template <int NPL>
+__global__ void __launch_bounds__(kSelWarps * 32) route_select_lanes_kernel(
+    const float *__restrict__ logits, const float *__restrict__ bias, int B, int N, int K,
+    int n_group, int topk_group, int score_fn, int renorm, float route_scale,
+    int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int32_t *__restrict__ counts) {
+  __shared__ float sd[kSelWarps][kMaxNI * 32];
+  __shared__ float sg[kSelWarps][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * kSelWarps + warp;
+  if (t >= B) return;
+  const int base = lane * NPL;
+  float c[NPL], s[NPL];
+  bool elig[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    elig[i] = base + i < N;
+    c[i] = elig[i] ? logits[(size_t)t * N + base + i] : 0.0f;
+  }
+  if (score_fn == MOE_SCORE_SOFTMAX) {
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (elig[i]) m = fmaxf(m, c[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (elig[i]) {
+        s[i] = route_exp(__fsub_rn(c[i], m));
+        sd[warp][base + i] = s[i];
+      }
+    __syncwarp();
+    float S = 0.0f;
+    if (lane == 0)
+      for (int e = 0; e < N; ++e) S = __fadd_rn(S, sd[warp][e]);  // expert order
+    S = __shfl_sync(0xffffffffu, S, 0);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (elig[i]) s[i] = __fdiv_rn(s[i], S);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (elig[i]) {
+        s[i] = route_sigmoid(c[i]);
+        c[i] = bias ? __fadd_rn(s[i], __ldg(bias + base + i)) : s[i];
+      }
+  }
+  if (n_group > 1) {
+    const int gs = N / n_group, L = gs / NPL;
+    Cand b1{0.0f, INT_MAX, 0.0f}, b2{0.0f, INT_MAX, 0.0f};
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const Cand x{c[i], base + i, 0.0f};
+      if (!elig[i]) continue;
+      if (before(x, b1)) {
+        b2 = b1;
+        b1 = x;
+      } else if (before(x, b2)) {
+        b2 = x;
+      }
+    }
+    for (int off = 1; off < L; off <<= 1) {
+      Cand o1, o2;
+      o1.v = __shfl_xor_sync(0xffffffffu, b1.v, off);
+      o1.i = __shfl_xor_sync(0xffffffffu, b1.i, off);
+      o2.v = __shfl_xor_sync(0xffffffffu, b2.v, off);
+      o2.i = __shfl_xor_sync(0xffffffffu, b2.i, off);
+      o1.s = o2.s = 0.0f;
+      merge_top2(b1, b2, o1, o2);
+    }
+    if (lane % L == 0 && lane / L < n_group) sg[warp][lane / L] = __fadd_rn(b1.v, b2.v);
+    __syncwarp();
+    uint32_t keep = 0;
+    for (int r = 0; r < topk_group; ++r) {
+      int best = -1;
+      for (int j = 0; j < n_group; ++j) {
+        if (keep >> j & 1) continue;
+        if (best < 0 || sg[warp][j] > sg[warp][best]) best = j;  // ties keep the lower j
+      }
+      keep |= 1u << best;
+    }
+    const bool mine = base < N && ((keep >> (base / gs)) & 1);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) elig[i] = elig[i] && mine;
+  }
+  int my_idx = -1;
+  float my_s = 0.0f;
+  for (int r = 0; r < K; ++r) {
+    Cand b{0.0f, INT_MAX, 0.0f};
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const Cand x{c[i], base + i, s[i]};
+      if (elig[i] && before(x, b)) b = x;
+    }
+    b = warp_best(b);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (base + i == b.i) elig[i] = false;
+    if (lane == r) {
+      my_idx = b.i == INT_MAX ? -1 : b.i;
+      my_s = b.s;
+    }
+  }
+  float sum = 0.0f;
+  for (int r = 0; r < K; ++r) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_s, r));
+  if (lane < K) {
+    const float w = renorm ? __fmul_rn(__fdiv_rn(my_s, sum), route_scale)
+                           : __fmul_rn(my_s, route_scale);
+    topk_idx[(size_t)t * K + lane] = my_idx;
+    topk_w[(size_t)t * K + lane] = w;
+    if (counts && my_idx >= 0) atomicAdd(counts + my_idx, 1);
+  }
+}
+
 template <int TT, int TE, int S, int kRouteBK>
 int launch_logits(const uint16_t *x, const float *W, float *lg, int B, int H, int N,
                   cudaStream_t st) {
@@ -337,15 +476,36 @@ extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W
   const uint16_t *xb = static_cast<const uint16_t *>(x);
   if (ctas(4, 4) >= 4 * sms)
     rc = launch_logits<4, 4, 4, 32>(xb, W, lg, B, H, N, st);
-  else if (ctas(2, 2) >= 4 * sms)
+  else if (ctas(2, 2) >= 4 * sms && H % 64 == 0)
     rc = launch_logits<2, 2, 4, 64>(xb, W, lg, B, H, N, st);
-  else if (H % 128 == 0)
-    rc = launch_logits<1, 1, 4, 128>(xb, W, lg, B, H, N, st);
+  else if (H % 128 == 0)  // small grid: only the in-flight chunks hide the load latency
+    rc = launch_logits<1, 1, 8, 128>(xb, W, lg, B, H, N, st);
   else
     rc = launch_logits<1, 1, 8, 32>(xb, W, lg, B, H, N, st);
   if (rc) return rc;
-  route_select_kernel<<<(B + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, st>>>(
-      lg, bias, B, N, cfg->K, cfg->n_group, cfg->topk_group, cfg->score_fn, cfg->renorm,
-      cfg->route_scale, topk_idx, topk_w, expert_counts);
+  // lanes-own-experts selection when every group fills whole lanes, else generic
+  int npl = 1;
+  while (npl * 32 < N) npl *= 2;
+  const int gs = cfg->n_group > 1 ? N / cfg->n_group : 0;
+  const int L = gs ? gs / npl : 0;
+  const bool lanes_ok = cfg->n_group <= 1 || (gs % npl == 0 && L >= 1 && (L & (L - 1)) == 0 &&
+                                             L * cfg->n_group <= 32);
+  const dim3 grid((B + kSelWarps - 1) / kSelWarps), block(kSelWarps * 32);
+#define MOE_SEL_ARGS                                                                         \
+  lg, bias, B, N, cfg->K, cfg->n_group, cfg->topk_group, cfg->score_fn, cfg->renorm,      \
+      cfg->route_scale, topk_idx, topk_w, expert_counts
+  if (!lanes_ok)
+    route_select_kernel<<<grid, block, 0, st>>>(MOE_SEL_ARGS);
+  else if (npl == 1)
+    route_select_lanes_kernel<1><<<grid, block, 0, st>>>(MOE_SEL_ARGS);
+  else if (npl == 2)
+    route_select_lanes_kernel<2><<<grid, block, 0, st>>>(MOE_SEL_ARGS);
+  else if (npl == 4)
+    route_select_lanes_kernel<4><<<grid, block, 0, st>>>(MOE_SEL_ARGS);
+  else if (npl == 8)
+    route_select_lanes_kernel<8><<<grid, block, 0, st>>>(MOE_SEL_ARGS);
+  else
+    route_select_lanes_kernel<16><<<grid, block, 0, st>>>(MOE_SEL_ARGS);
+#undef MOE_SEL_ARGS
   return check_launch();
 }

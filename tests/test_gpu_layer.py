@@ -33,6 +33,21 @@ def test_route_bit_exact(dev, name):
     assert np.array_equal(r["counts"].cpu().numpy(), oracle.expert_counts(idx, cfg.N))
 
 
+@pytest.mark.parametrize("N,G,TG,K", [(24, 8, 3, 4), (48, 6, 2, 5), (64, 1, 1, 6)])
+def test_route_bit_exact_other_group_shapes(dev, N, G, TG, K):
+    """Group shapes that do not fill whole lanes (the generic selection path)."""
+    cfg = configs.MoEConfig("odd", B=77, H=256, N=N, K=K, I=128, n_group=G, topk_group=TG,
+                            score_fn=configs.SIGMOID, renorm=1, route_scale=2.5,
+                            bias_init="normal", seed=3)
+    x = inputs.make_x(cfg)
+    W, bias = inputs.make_router(cfg)
+    r = api.route(cfg, bf16_dev(x), to_dev(W), to_dev(bias))
+    torch.cuda.synchronize()
+    idx, w = oracle.route(x, W, bias, cfg)
+    assert np.array_equal(r["topk_idx"].cpu().numpy(), idx)
+    assert np.array_equal(r["topk_w"].cpu().numpy().view(np.uint32), w.view(np.uint32))
+
+
 @pytest.mark.parametrize("name", ["prefill", "skew"])
 def test_route_full_size_sampled(dev, name):
     """Full B: routing of a sample of tokens bit-exact, counts consistent at any size."""
