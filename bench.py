@@ -235,6 +235,8 @@ def main():
     lay = api.MoELayer(cfg, torch.from_numpy(W).to(dev),
                        None if bias is None else torch.from_numpy(bias).to(dev), wdev,
                        eplb_map=emap, device=dev)
+    del wdev                                          # the layer holds its own copy
+    torch.cuda.empty_cache()
     lay.x.copy_(torch.from_numpy(x).view(torch.bfloat16).to(dev))
     for _ in range(args.warmup):
         lay.forward()

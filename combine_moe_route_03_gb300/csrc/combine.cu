@@ -17,7 +17,7 @@
 namespace moe {
 namespace {
 
-constexpr int kCombineWarps = 8;
+constexpr int kCombineWarps = 4;  // small CTAs: an SBO consumer fits beside a GEMM CTA
 
 // One warp owns a task = (token, run of `cpt` consecutive 256-column chunks), so a
 // small batch still spreads over many warps and every lane keeps K independent

@@ -11,15 +11,16 @@
 // each 1x128 / 128x128 scale repeated over its four 32-wide sub-blocks) and the
 // fp32 accumulator stays in tensor memory for the whole K loop.
 //
-// CTA = 6 warps, one CTA per SM, persistent:
+// CTA = 10 warps, one CTA per SM, persistent:
 //   warp 0  TMA producer: A tile 128x128 e4m3, B tile 256x128 e4m3 (two 128-row
 //           boxes: gate and up halves for GATEUP, two output blocks for DOWN),
 //           and the matching scale atoms (cp.async.bulk), STAGES-deep ring.
 //   warp 1  TMEM owner and MMA issuer: scale atoms -> TMEM (tcgen05.cp), four
 //           128x256x32 block-scaled MMAs per stage, commits free the stage.
-//   warps 2-5 epilogue: TMEM -> registers (one accumulator row per thread),
-//           SwiGLU + 1x128 requantisation (GATEUP) or bf16 rounding (DOWN),
-//           global stores, optional release signals.
+//   warps 2-9 epilogue: TMEM -> registers (two warps per accumulator row group,
+//           half the columns each; TMEM is released before any math), SwiGLU +
+//           1x128 requantisation (GATEUP) or bf16 rounding (DOWN), global
+//           stores, optional release signals.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -28,7 +29,8 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 320;  // producer, MMA, 8 epilogue warps
+constexpr int kEpiThreads = 256;
 constexpr uint32_t A_BYTES = BM * BK;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK;   // 32 KB
 constexpr uint32_t SFA_BYTES = 512;     // one SF atom
@@ -40,7 +42,8 @@ constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+constexpr uint32_t OFF_AMAX = OFF_MISC + 16;  // [2][128] partial row amax of the epilogue
+constexpr uint32_t SMEM_BYTES = OFF_AMAX + 2 * 128 * 4 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF = 256;  // scale columns start here, 16 per stage
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, 128);
+    mbar_init(bar_acc_empty, kEpiThreads);
     *abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -278,9 +281,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // Eight warps: a warp may read TMEM lanes 32*(warp%4)..+31 (its rows); the two
+    // warps of a lane quarter split the columns.  Each thread moves its half-row of
+    // the accumulator into registers and releases TMEM at once, so the next tile's
+    // MMAs run while these warps finish SwiGLU / quantisation / stores.
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_local = 32 * q + lane;
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
+    float *amax_x = reinterpret_cast<float *>(smem + OFF_AMAX);  // [half][row]
     uint32_t acc_phase = 0;
     for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
       const Unit U = get_unit(P, unit, units2);
@@ -294,73 +303,78 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_after();
       if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
-        float h[128];
-        float amax = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t g[32], u[32];
-          MOE_TMEM_LD_32x32b_X32(t_row + 32 * c, g);
-          MOE_TMEM_LD_32x32b_X32(t_row + 128 + 32 * c, u);
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float gf = __uint_as_float(g[i]), uf = __uint_as_float(u[i]);
-            const float v = __fdividef(gf, 1.0f + __expf(-gf)) * uf;  // silu(g) * u
-            h[32 * c + i] = v;
-            amax = fmaxf(amax, fabsf(v));
-          }
-        }
+        // gate columns [64*half, +64) and the matching up columns [128 + 64*half, +64)
+        uint32_t g[64], u[64];
+        MOE_TMEM_LD_32x32b_X32(t_row + 64 * half, g);
+        MOE_TMEM_LD_32x32b_X32(t_row + 64 * half + 32, (g + 32));
+        MOE_TMEM_LD_32x32b_X32(t_row + 128 + 64 * half, u);
+        MOE_TMEM_LD_32x32b_X32(t_row + 128 + 64 * half + 32, (u + 32));
+        tc_wait_ld();
         tc_fence_before();
         mbar_arrive(bar_acc_empty);
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float gf = __uint_as_float(g[i]), uf = __uint_as_float(u[i]);
+          const float v = __fdividef(gf, 1.0f + __expf(-gf)) * uf;  // silu(g) * u
+          g[i] = __float_as_uint(v);
+          amax = fmaxf(amax, fabsf(v));
+        }
+        // the 1x128 block of h spans both halves of the row
+        amax_x[half * 128 + row_local] = amax;
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+        amax = fmaxf(amax, amax_x[(half ^ 1) * 128 + row_local]);
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
         if (store) {
           const int e = ue8m0_exp(amax);
           const float inv = pow2i(-e);
-          uint8_t *dst = P.out + (size_t)r * P.I + (size_t)ni * 128;
+          uint8_t *dst = P.out + (size_t)r * P.I + (size_t)ni * 128 + 64 * half;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint4 w;
             uint32_t *wp = &w.x;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int b = 16 * c + 4 * j;
-              wp[j] = e4m3x2(__fmul_rn(h[b], inv), __fmul_rn(h[b + 1], inv)) |
-                      (e4m3x2(__fmul_rn(h[b + 2], inv), __fmul_rn(h[b + 3], inv)) << 16);
+              wp[j] = e4m3x2(__fmul_rn(__uint_as_float(g[b]), inv),
+                             __fmul_rn(__uint_as_float(g[b + 1]), inv)) |
+                      (e4m3x2(__fmul_rn(__uint_as_float(g[b + 2]), inv),
+                              __fmul_rn(__uint_as_float(g[b + 3]), inv))
+                       << 16);
             }
             *reinterpret_cast<uint4 *>(dst + 16 * c) = w;
           }
-          *reinterpret_cast<uint32_t *>(P.out_sf + sf_atom_off(r, ni, P.I / 128)) =
-              (uint32_t)(e + 127) * 0x01010101u;
+          if (half == 0)
+            *reinterpret_cast<uint32_t *>(P.out_sf + sf_atom_off(r, ni, P.I / 128)) =
+                (uint32_t)(e + 127) * 0x01010101u;
         }
       } else {
-        uint8_t *dst = P.out + ((size_t)r * P.n + (size_t)ni * 256) * 2;
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[32];
-          MOE_TMEM_LD_32x32b_X32(t_row + 32 * c, v);
-          tc_wait_ld();
-          if (c == 7) {
-            tc_fence_before();
-            mbar_arrive(bar_acc_empty);
-          }
-          if (store) {
+        // output columns [128*half, +128)
+        uint32_t v[128];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 w;
-              w.x = f32_to_bf16_bits(__uint_as_float(v[8 * j + 0])) |
-                    (f32_to_bf16_bits(__uint_as_float(v[8 * j + 1])) << 16);
-              w.y = f32_to_bf16_bits(__uint_as_float(v[8 * j + 2])) |
-                    (f32_to_bf16_bits(__uint_as_float(v[8 * j + 3])) << 16);
-              w.z = f32_to_bf16_bits(__uint_as_float(v[8 * j + 4])) |
-                    (f32_to_bf16_bits(__uint_as_float(v[8 * j + 5])) << 16);
-              w.w = f32_to_bf16_bits(__uint_as_float(v[8 * j + 6])) |
-                    (f32_to_bf16_bits(__uint_as_float(v[8 * j + 7])) << 16);
-              *reinterpret_cast<uint4 *>(dst + 64 * c + 16 * j) = w;
-            }
+        for (int c = 0; c < 4; ++c) MOE_TMEM_LD_32x32b_X32(t_row + 128 * half + 32 * c, (v + 32 * c));
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_acc_empty);
+        if (store) {
+          uint8_t *dst = P.out + ((size_t)r * P.n + (size_t)ni * 256 + 128 * half) * 2;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            uint4 w;
+            w.x = f32_to_bf16_bits(__uint_as_float(v[8 * j + 0])) |
+                  (f32_to_bf16_bits(__uint_as_float(v[8 * j + 1])) << 16);
+            w.y = f32_to_bf16_bits(__uint_as_float(v[8 * j + 2])) |
+                  (f32_to_bf16_bits(__uint_as_float(v[8 * j + 3])) << 16);
+            w.z = f32_to_bf16_bits(__uint_as_float(v[8 * j + 4])) |
+                  (f32_to_bf16_bits(__uint_as_float(v[8 * j + 5])) << 16);
+            w.w = f32_to_bf16_bits(__uint_as_float(v[8 * j + 6])) |
+                  (f32_to_bf16_bits(__uint_as_float(v[8 * j + 7])) << 16);
+            *reinterpret_cast<uint4 *>(dst + 16 * j) = w;
           }
         }
         if (P.signal) {
           __threadfence();
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
           if (warp == 2 && lane == 0) {
             for (int j = 0; j * P.bm_signal < BM; ++j)
               if (j * P.bm_signal < valid && row0 + j * P.bm_signal < P.rows)
