@@ -41,7 +41,7 @@ class GemmArgs(ctypes.Structure):
                 ("W", _vp), ("W_sf", _vp), ("phys2log", _vp), ("tiles", _vp), ("tiles2", _vp),
                 ("row_offset2", _c_i64), ("expert2", _c_int), ("out", _vp),
                 ("out_sf", _vp), ("signal", _vp), ("block_m_signal", _c_int),
-                ("num_sms", _c_int), ("status", _vp)]
+                ("num_sms", _c_int), ("pair_tiles", _c_int), ("status", _vp)]
 
 
 class CombineCfg(ctypes.Structure):
@@ -54,7 +54,8 @@ class Layer(ctypes.Structure):
     _fields_ = [("route", RouteCfg), ("N_phys", _c_int), ("layout", _c_int), ("cap", _c_int),
                 ("I", _c_int), ("has_shared", _c_int), ("sbo", _c_int),
                 ("block_m_signal", _c_int), ("rows", _c_i64), ("max_tiles", _c_i64),
-                ("timeout_ns", _c_i64), ("num_sms", _c_int), ("combine_ctas", _c_int)] + [
+                ("timeout_ns", _c_i64), ("num_sms", _c_int), ("combine_ctas", _c_int),
+                ("gemm_pairs", _c_int)] + [
         (n, _vp) for n in (
             "x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
             "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",

@@ -133,7 +133,8 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
                      phys2log: torch.Tensor | None = None, signal: torch.Tensor | None = None,
                      block_m_signal: int = 64, num_sms_: int = 0,
                      status: torch.Tensor | None = None, stream=None,
-                     tiles2: torch.Tensor | None = None, row_offset2: int = 0, expert2: int = 0):
+                     tiles2: torch.Tensor | None = None, row_offset2: int = 0, expert2: int = 0,
+                     pair_tiles: int = 0):
     """moe_grouped_gemm_fp8.  W e4m3 [E][n][k]; A e4m3 [rows][k]."""
     E, n, k = W.shape
     rows = A.shape[0]
@@ -148,7 +149,7 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
     st = status if status is not None else new_status(dev)
     g = GemmArgs(op, n, k, rows, max_tiles, E, ptr(A), ptr(A_sf), ptr(W), ptr(W_sf_atoms),
                  ptr(phys2log), ptr(tiles), ptr(tiles2), row_offset2, expert2, ptr(out),
-                 ptr(out_sf), ptr(signal), block_m_signal, num_sms_, ptr(st))
+                 ptr(out_sf), ptr(signal), block_m_signal, num_sms_, pair_tiles, ptr(st))
     check(load().moe_grouped_gemm_fp8(ctypes.byref(g), stream_ptr(stream)), "moe_grouped_gemm_fp8")
     return (out, out_sf) if op == GEMM_GATEUP_SWIGLU else out
 
@@ -183,7 +184,7 @@ class MoELayer:
 
     def __init__(self, cfg: MoEConfig, W_router: torch.Tensor, bias: torch.Tensor | None,
                  weights: dict, eplb_map=None, num_sms_: int = 0, combine_ctas: int = 16,
-                 timeout_ns: int = 1_000_000_000, device="cuda"):
+                 timeout_ns: int = 1_000_000_000, device="cuda", gemm_pairs: int = 0):
         self.cfg = cfg
         dev = torch.device(device)
         B, H, I, K = cfg.B, cfg.H, cfg.I, cfg.K
@@ -246,6 +247,7 @@ class MoELayer:
         sms = num_sms_ or num_sms()
         lay.num_sms = sms - combine_ctas if cfg.sbo else sms
         lay.combine_ctas = combine_ctas
+        lay.gemm_pairs = gemm_pairs
         names = ["x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
                  "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",
                  "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",

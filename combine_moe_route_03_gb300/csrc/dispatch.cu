@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     int32_t *__restrict__ counts, int32_t *__restrict__ tiles, int32_t *__restrict__ src_of,
     int32_t *__restrict__ shared_tiles, int32_t *status) {
   __shared__ int32_t scan[kScanThreads];
-  __shared__ int32_t total_tiles;
+  __shared__ int32_t total_tiles, total_pairs;
   const int p = threadIdx.x;
   int cnt = 0, valid = 0, nt = 0;
   if (p < N_phys) {
@@ -154,6 +154,19 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
   const int first = scan[p] - nt;
   if (p == kScanThreads - 1) total_tiles = scan[p];
   __syncthreads();
+  // second scan: pairs of consecutive M tiles of one expert (ceil(nt / 2) per expert)
+  const int np = (nt + 1) / 2;
+  scan[p] = np;
+  __syncthreads();
+  for (int off = 1; off < kScanThreads; off <<= 1) {
+    const int v = p >= off ? scan[p - off] : 0;
+    __syncthreads();
+    scan[p] += v;
+    __syncthreads();
+  }
+  const int pfirst = scan[p] - np;
+  if (p == kScanThreads - 1) total_pairs = scan[p];
+  __syncthreads();
   if (p < N_phys) {
     const int seg = layout == MOE_LAYOUT_CONTIG ? first * 128 : p * cap;
     ws.seg[p] = seg;
@@ -164,8 +177,11 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
       tl[2] = min(128, valid - 128 * i);
       tl[3] = first;
       tl[4] = nt;
-      tl[5] = tl[6] = tl[7] = 0;
+      tl[5] = pfirst;
+      tl[6] = np;
     }
+    // field 7 of entry q: first M tile of pair q (pairs never outnumber tiles)
+    for (int j = 0; j < np; ++j) tiles[8 + 8 * (size_t)(pfirst + j) + 7] = first + 2 * j;
     if (src_of) {  // rows of this expert that no token fills
       const int end = layout == MOE_LAYOUT_CONTIG ? nt * 128 : cap;
       for (int j = valid; j < end; ++j) src_of[seg + j] = -1;
@@ -176,16 +192,19 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
   if (p == 0) {
     tiles[0] = total_tiles;
     tiles[1] = (int32_t)used;
-    for (int i = 2; i < 8; ++i) tiles[i] = 0;
+    tiles[2] = total_pairs;
+    for (int i = 3; i < 8; ++i) tiles[i] = 0;
   }
   if (src_of)
     for (int64_t r = used + p; r < rows_alloc; r += kScanThreads) src_of[r] = -1;
   if (shared_tiles) {
     const int snt = (B + 127) / 128;
+    const int snp = (snt + 1) / 2;
     if (p == 0) {
       shared_tiles[0] = snt;
       shared_tiles[1] = snt * 128;
-      for (int i = 2; i < 8; ++i) shared_tiles[i] = 0;
+      shared_tiles[2] = snp;
+      for (int i = 3; i < 8; ++i) shared_tiles[i] = 0;
     }
     for (int i = p; i < snt; i += kScanThreads) {
       int32_t *tl = shared_tiles + 8 + 8 * (size_t)i;
@@ -194,7 +213,9 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
       tl[2] = min(128, B - 128 * i);
       tl[3] = 0;
       tl[4] = snt;
-      tl[5] = tl[6] = tl[7] = 0;
+      tl[5] = 0;
+      tl[6] = snp;
+      tl[7] = i < snp ? 2 * i : 0;
     }
   }
 }

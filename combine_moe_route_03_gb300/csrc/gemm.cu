@@ -35,7 +35,6 @@ constexpr uint32_t A_BYTES = BM * BK;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK;   // 32 KB
 constexpr uint32_t SFA_BYTES = 512;     // one SF atom
 constexpr uint32_t SFB_BYTES = 1024;    // two SF atoms
-constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -53,7 +52,7 @@ struct GemmParams {
   int64_t rows;
   const uint8_t *A_sf, *W_sf;
   const int32_t *phys2log, *tiles, *tiles2;
-  int row_offset2, expert2, num_experts;
+  int row_offset2, expert2, num_experts, max_tiles;
   uint8_t *out, *out_sf;
   int32_t *signal;
   int bm_signal;
@@ -61,12 +60,19 @@ struct GemmParams {
 };
 
 struct Unit {
-  int row0;   // first A / out row of the tile
-  int valid;  // rows of the tile that hold data (0: unit skipped, bad tile entry)
-  int we;     // weight expert
-  int ni;     // output column tile
-  int band;   // M tiles sharing this unit's weight tile
+  int row0;    // first A / out row of this CTA's tile
+  int nvalid;  // rows of that tile that hold data
+  int we;      // weight expert
+  int ni;      // output column tile
+  int band;    // M tiles sharing this unit's weight tile
+  bool ok;     // the unit runs (its tile-list entries address memory inside the operands)
+  bool active; // this CTA has a tile (a cluster pair's second CTA may have none)
 };
+
+__device__ __forceinline__ bool tile_ok(const GemmParams &P, int row0, int nvalid) {
+  return row0 >= 0 && (int64_t)row0 + 128 <= P.rows && row0 % 128 == 0 && nvalid > 0 &&
+         nvalid <= 128;
+}
 
 // Work unit -> (M tile, N tile).  Units of one expert band (its consecutive M
 // tiles) are ordered N-tile-major, M fastest, so CTAs running side by side share
@@ -88,12 +94,49 @@ __device__ __forceinline__ Unit get_unit(const GemmParams &P, int unit, int unit
   r.ni = local / c;
   r.band = c;
   r.row0 = t[0] + (second ? P.row_offset2 : 0);
-  r.valid = t[2];
+  r.nvalid = t[2];
   r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[t[1]] : t[1]);
   // every role skips a tile entry that would address memory outside the operands
-  if (r.row0 < 0 || (int64_t)r.row0 + 128 > P.rows || r.row0 % 128 || r.we < 0 ||
-      r.we >= P.num_experts || r.valid <= 0 || r.valid > 128 || r.ni >= P.n_tiles)
-    r.valid = 0;
+  r.ok = tile_ok(P, r.row0, r.nvalid) && r.we >= 0 && r.we < P.num_experts && r.ni < P.n_tiles;
+  r.active = r.ok;
+  return r;
+}
+
+// Cluster-pair variant: unit -> (pair of M tiles of one expert, N tile); CTA
+// `rank` of the cluster takes the pair's tile `rank` (none if the expert's tile
+// count is odd and this is its last pair).  Units of one band are N-tile-major,
+// pair fastest.
+__device__ __forceinline__ Unit get_pair_unit(const GemmParams &P, int unit, int units2,
+                                              int rank) {
+  const int32_t *tl = P.tiles;
+  int u = unit;
+  const bool second = unit < units2;
+  if (second)
+    tl = P.tiles2;
+  else
+    u -= units2;
+  const int g = u / P.n_tiles;           // some pair of the right band
+  const int m0 = tl[8 + 8 * g + 7];      // first tile of pair g
+  Unit r;
+  r.ok = false;
+  r.active = false;
+  r.row0 = r.nvalid = r.we = r.ni = r.band = 0;
+  if (m0 < 0 || m0 >= P.max_tiles) return r;
+  const int32_t *b = tl + 8 + 8 * m0;
+  const int f = b[3], c = b[4], pf = b[5], pc = b[6];
+  if (pc <= 0 || c <= 0 || f < 0 || f + c > P.max_tiles) return r;
+  const int local = u - P.n_tiles * pf;
+  r.ni = local / pc;
+  const int mi = f + 2 * (local % pc) + rank;
+  r.band = c;
+  r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[b[1]] : b[1]);
+  r.ok = r.we >= 0 && r.we < P.num_experts && r.ni >= 0 && r.ni < P.n_tiles;
+  if (r.ok && mi < f + c) {
+    const int32_t *t = tl + 8 + 8 * mi;
+    r.row0 = t[0] + (second ? P.row_offset2 : 0);
+    r.nvalid = t[2];
+    r.active = tile_ok(P, r.row0, r.nvalid);
+  }
   return r;
 }
 
@@ -109,6 +152,12 @@ __device__ __forceinline__ void fail(int32_t *status, volatile int *abort) {
 // tmA loads full 128-row A tiles; tmA32 loads 32-row slices, used for tiles with
 // fewer valid rows so rows that hold no data are never fetched (the MMA then reads
 // stale shared memory for them, which only feeds accumulator rows never stored).
+// kPair: launched as 2-CTA clusters; the two CTAs take the two M tiles of a pair
+// and each loads half of the shared weight tile (and one weight scale atom),
+// multicast into both CTAs' shared memory, so the weight tile leaves L2 once per
+// pair and both tiles consume it in lockstep.  A stage is refilled only after both
+// CTAs' MMAs released it (commits multicast to both CTAs' empty barriers).
+template <bool kPair>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA32,
@@ -125,10 +174,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
+  constexpr uint16_t kBoth = 3;  // cluster CTA mask of a pair
+  const int rank = kPair ? (int)cluster_ctarank() : 0;
+  const int first_unit = kPair ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int ustride = kPair ? (int)cluster_count_x() : (int)gridDim.x;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kPair ? 2 : 1);
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, kEpiThreads);
@@ -144,11 +197,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();  // the peer's barriers exist before anything targets them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int units2 = P.tiles2 ? P.tiles2[0] * P.n_tiles : 0;
-  const int total = P.tiles[0] * P.n_tiles + units2;
+  const int units2 = P.tiles2 ? P.tiles2[kPair ? 2 : 0] * P.n_tiles : 0;
+  const int total = P.tiles[kPair ? 2 : 0] * P.n_tiles + units2;
+  auto unit_at = [&](int u) {
+    return kPair ? get_pair_unit(P, u, units2, rank) : get_unit(P, u, units2);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -162,16 +219,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) {
-        const Unit U = get_unit(P, unit, units2);
-        if (U.valid == 0) {
+      for (int unit = first_unit; ok && unit < total; unit += ustride) {
+        const Unit U = unit_at(unit);
+        if (!U.ok) {
           status_or(P.status, MOE_STATUS_BAD_INDEX);
           continue;
         }
         const int row0 = U.row0, we = U.we, ni = U.ni;
-        const uint64_t pol_w = U.band > 1 ? pol_keep : pol_stream;
-        const int a_slices = U.valid == BM ? 0 : (U.valid + 31) / 32;  // 0: one full box
-        const uint32_t tx = STAGE_TX - (a_slices ? A_BYTES - a_slices * (A_BYTES / 4) : 0);
+        const uint64_t pol_w = U.band > (kPair ? 2 : 1) ? pol_keep : pol_stream;
+        const int a_slices = U.nvalid == BM ? 0 : (U.nvalid + 31) / 32;  // 0: one full box
+        const uint32_t a_bytes = a_slices ? a_slices * (A_BYTES / 4) : A_BYTES;
+        const uint32_t tx = (U.active ? a_bytes + SFA_BYTES : 0) + B_BYTES + SFB_BYTES;
         int wrow0, wrow1, nb0, nb1;
         if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
           wrow0 = we * P.n + ni * 128;
@@ -197,19 +255,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(full, tx);
           const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
           const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
-          if (a_slices == 0)
-            tma_load_2d(sa, &tmA, full, kb * BK, row0, pol_a);
-          else
-            for (int j = 0; j < a_slices; ++j)
-              tma_load_2d(sa + j * (A_BYTES / 4), &tmA32, full, kb * BK, row0 + 32 * j, pol_a);
-          tma_load_2d(sb, &tmW, full, kb * BK, wrow0, pol_w);
-          tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
           const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
           const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
-          bulk_load(ssfa, sfa + (size_t)kb * 512, 512, full);
-          bulk_load(ssfb, sfb0 + (size_t)kb * 512, 512, full);
-          bulk_load(ssfb + 512, sfb1 + (size_t)kb * 512, 512, full);
+          if (U.active) {
+            if (a_slices == 0)
+              tma_load_2d(sa, &tmA, full, kb * BK, row0, pol_a);
+            else
+              for (int j = 0; j < a_slices; ++j)
+                tma_load_2d(sa + j * (A_BYTES / 4), &tmA32, full, kb * BK, row0 + 32 * j,
+                            pol_a);
+            bulk_load(ssfa, sfa + (size_t)kb * 512, 512, full);
+          }
+          if (kPair) {  // my half of the weight tile, into both CTAs
+            tma_load_2d_mc(sb + rank * (B_BYTES / 2), &tmW, full, kb * BK, rank ? wrow1 : wrow0,
+                           kBoth, pol_w);
+            bulk_load_mc(ssfb + rank * 512, (rank ? sfb1 : sfb0) + (size_t)kb * 512, 512, full,
+                         kBoth);
+          } else {
+            tma_load_2d(sb, &tmW, full, kb * BK, wrow0, pol_w);
+            tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
+            bulk_load(ssfb, sfb0 + (size_t)kb * 512, 512, full);
+            bulk_load(ssfb + 512, sfb1 + (size_t)kb * 512, 512, full);
+          }
           ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (kPair && ok) {
+        // Wait until both CTAs released every stage: after this no arrival from the
+        // peer is still on its way to this CTA's barriers.
+        for (int i = 0; i < STAGES; ++i) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort, kWaitLimitNs)) {
+            fail(P.status, abort);
+            break;
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -238,13 +320,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) {
-        if (get_unit(P, unit, units2).valid == 0) continue;
-        if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
-          fail(P.status, abort);
-          break;
+      for (int unit = first_unit; ok && unit < total; unit += ustride) {
+        const Unit U = unit_at(unit);
+        if (!U.ok) continue;
+        if (U.active) {
+          if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
+            fail(P.status, abort);
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
         for (int kb = 0; kb < P.Kb; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort, kWaitLimitNs)) {
             fail(P.status, abort);
@@ -252,31 +337,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
-          const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
-          const uint32_t t_sfa = tmem + TMEM_SF + 16 * stage;
-          const uint32_t t_sfb = t_sfa + 4;
-          const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
-          const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
-          tc_cp_32x128b_x4(t_sfa, smem_desc(ssfa, 16, 128, 0));
-          tc_cp_32x128b_x4(t_sfb, smem_desc(ssfb, 16, 128, 0));
-          tc_cp_32x128b_x4(t_sfb + 4, smem_desc(ssfb + 512, 16, 128, 0));
+          if (U.active) {
+            const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
+            const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
+            const uint32_t t_sfa = tmem + TMEM_SF + 16 * stage;
+            const uint32_t t_sfb = t_sfa + 4;
+            const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
+            const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
+            tc_cp_32x128b_x4(t_sfa, smem_desc(ssfa, 16, 128, 0));
+            tc_cp_32x128b_x4(t_sfb, smem_desc(ssfb, 16, 128, 0));
+            tc_cp_32x128b_x4(t_sfb + 4, smem_desc(ssfb + 512, 16, 128, 0));
 #pragma unroll
-          for (int j = 0; j < BK / 32; ++j) {
-            const uint64_t ad = smem_desc(sa + 32 * j, 16, 1024, 2);
-            const uint64_t bd = smem_desc(sb + 32 * j, 16, 1024, 2);
-            const uint32_t idesc = idesc_base | ((uint32_t)j << 29) | ((uint32_t)j << 4);
-            tc_mma_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | j) != 0);
+            for (int j = 0; j < BK / 32; ++j) {
+              const uint64_t ad = smem_desc(sa + 32 * j, 16, 1024, 2);
+              const uint64_t bd = smem_desc(sb + 32 * j, 16, 1024, 2);
+              const uint32_t idesc = idesc_base | ((uint32_t)j << 29) | ((uint32_t)j << 4);
+              tc_mma_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | j) != 0);
+            }
           }
-          tc_commit(bar_empty + 8 * stage);
+          if (kPair)
+            tc_commit_mc(bar_empty + 8 * stage, kBoth);
+          else
+            tc_commit(bar_empty + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc_commit(bar_acc_full);
-        acc_phase ^= 1;
+        if (U.active) {
+          tc_commit(bar_acc_full);
+          acc_phase ^= 1;
+        }
       }
     }
   } else {
@@ -291,10 +383,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
     float *amax_x = reinterpret_cast<float *>(smem + OFF_AMAX);  // [half][row]
     uint32_t acc_phase = 0;
-    for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
-      const Unit U = get_unit(P, unit, units2);
-      if (U.valid == 0) continue;
-      const int row0 = U.row0, valid = U.valid, ni = U.ni;
+    for (int unit = first_unit; unit < total; unit += ustride) {
+      const Unit U = unit_at(unit);
+      if (!U.ok || !U.active) continue;
+      const int row0 = U.row0, valid = U.nvalid, ni = U.ni;
       const int64_t r = (int64_t)row0 + row_local;
       const bool store = row_local < valid && r < P.rows;
       if (!mbar_wait(bar_acc_full, acc_phase, abort, kWaitLimitNs)) {
@@ -392,6 +484,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+  if (kPair) cluster_sync();  // neither CTA leaves while the other may still target it
 }
 
 __global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ atoms,
@@ -479,6 +572,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   if (a->tiles2 && (a->expert2 < 0 || a->expert2 >= a->num_experts || a->row_offset2 < 0 ||
                     a->row_offset2 % 128 || a->row_offset2 >= a->rows))
     return MOE_ERR_INVALID;
+  if (a->max_tiles > INT32_MAX) return MOE_ERR_UNSUPPORTED;
   GemmParams P;
   P.op = a->op;
   P.rows = a->rows;
@@ -486,6 +580,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.row_offset2 = (int)a->row_offset2;
   P.expert2 = a->expert2;
   P.num_experts = a->num_experts;
+  P.max_tiles = (int)a->max_tiles;
   P.n = a->n;
   P.k = a->k;
   P.Kb = a->k / BK;
@@ -502,15 +597,44 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.status = a->status;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return set_cuda_error(e);
     attr_set = true;
   }
   const int sms = a->num_sms > 0 ? a->num_sms : device_sm_count();
+  if (a->pair_tiles) {
+    // one 2-CTA cluster per pair of SMs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sms / 2 * 2 > 0 ? sms / 2 * 2 : 2));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = as_stream(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a persistent grid must be resident all at once: no more clusters than fit
+    static int max_clusters = 0;
+    if (max_clusters == 0) {
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_kernel<true>, &cfg);
+      if (e != cudaSuccess || max_clusters <= 0) return set_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidConfiguration);
+    }
+    if ((int)cfg.gridDim.x / 2 > max_clusters) cfg.gridDim = dim3((unsigned)(2 * max_clusters));
+    cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<true>, mA, mA32, mW, P);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return check_launch();
+  }
   const int64_t max_units = a->tiles2 ? sms : a->max_tiles * (a->n / BN);
   const int grid = (int)(max_units < sms ? max_units : sms);
-  grouped_gemm_kernel<<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW, P);
+  grouped_gemm_kernel<false><<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW,
+                                                                                    P);
   return check_launch();
 }

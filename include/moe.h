@@ -40,9 +40,12 @@
  *
  * Tile list.  moe_dispatch describes the rows it wrote as 128-row "M tiles" in
  * an int32 array `tiles` of 8 + 8*max_tiles entries:
- *   tiles[0] = number of M tiles, tiles[1] = rows in use (contiguous layout);
+ *   tiles[0] = number of M tiles, tiles[1] = rows in use (contiguous layout),
+ *   tiles[2] = number of tile pairs (an expert's tiles grouped two by two);
  *   tile i at tiles[8 + 8*i ...]: {first row, physical expert, valid rows (1..128),
- *   first tile of this expert, number of tiles of this expert, 0, 0, 0}.
+ *   first tile of this expert, number of tiles of this expert, first pair of this
+ *   expert, number of pairs of this expert, P} where P (in entry q < tiles[2]) is
+ *   the first tile of pair q.
  * Tiles of one expert are consecutive.  The grouped GEMM reads this list on the
  * device, so the host never needs the routing result.
  */
@@ -241,6 +244,8 @@ typedef struct moe_gemm_args {
   int32_t *signal;
   int block_m_signal;
   int num_sms;
+  int pair_tiles; /* 1: 2-CTA clusters take an expert's M tiles two by two and share
+                     each weight tile (multicast), for experts with several M tiles */
   int32_t *status;
 } moe_gemm_args;
 
@@ -316,6 +321,7 @@ typedef struct moe_layer {
   int N_phys, layout, cap, I, has_shared, sbo, block_m_signal;
   int64_t rows, max_tiles, timeout_ns;
   int num_sms, combine_ctas;
+  int gemm_pairs; /* 0: pair_tiles GEMMs when B*K/N_phys >= 128; 1: always; -1: never */
   /* inputs and weights */
   void *x;                                         /* bf16 [B][H] */
   const float *W_router, *bias;                    /* [N][H], [N] or NULL */

@@ -106,3 +106,48 @@ def support_unpack(atoms, rows, kb):
 def test_pack_unpack_sf_atoms_inverse():
     sf = np.random.default_rng(0).integers(0, 255, (384, 5)).astype(np.uint8)
     assert np.array_equal(support_unpack(pack_sf_atoms(sf), 384, 5), sf)
+
+
+@pytest.mark.parametrize("op", [0, 1])
+def test_cluster_pair_gemm_equals_single_cta(dev, op):
+    """Two-CTA clusters sharing weight tiles give the same bytes as one CTA per tile,
+    for experts with 1, 2, 3 and 5 M tiles (odd counts leave a cluster CTA idle)."""
+    tiles_per_expert = [1, 2, 3, 5, 2]
+    E = len(tiles_per_expert)
+    k, n = (512, 512) if op == 0 else (256, 768)
+    mt = sum(tiles_per_expert)
+    rows = 128 * mt
+    q, sf = activations(rows, k, 7)
+    W, Wsf = zip(*[inputs.make_fp8_matrix(n, k, (9, 55, e)) for e in range(E)])
+    W, Wsf = np.stack(W), np.stack(Wsf)
+    t = np.zeros(8 + 8 * mt, np.int32)
+    t[0], t[1] = mt, rows
+    i = pq = 0
+    for e, c in enumerate(tiles_per_expert):
+        npair = (c + 1) // 2
+        for j in range(c):
+            t[8 + 8 * (i + j): 8 + 8 * (i + j) + 7] = [128 * (i + j), e, 128 - 5 * j, i, c, pq, npair]
+        for j in range(npair):
+            t[8 + 8 * (pq + j) + 7] = i + 2 * j
+        i += c
+        pq += npair
+    t[2] = pq
+    A = torch.from_numpy(q).to(dev)
+    A_sf = torch.from_numpy(pack_sf_atoms(sf)).to(dev)
+    Wd = torch.from_numpy(W).to(dev)
+    Wa = api.pack_weight_scales(torch.from_numpy(Wsf).to(dev))
+    tl = torch.from_numpy(t).to(dev)
+    outs = []
+    for pairs in (0, 1):
+        st = api.new_status(dev)
+        o = api.grouped_gemm_fp8(op, A, A_sf, Wd, Wa, tl, mt, status=st, pair_tiles=pairs)
+        torch.cuda.synchronize()
+        assert api.read_status(st) == 0
+        outs.append(o)
+    if op == 1:
+        a, b = outs[0].view(torch.int16), outs[1].view(torch.int16)
+    else:
+        a, b = outs[0][0], outs[1][0]
+    for i0 in range(mt):                      # rows each tile stores
+        nvalid = t[8 + 8 * i0 + 2]
+        assert torch.equal(a[128 * i0: 128 * i0 + nvalid], b[128 * i0: 128 * i0 + nvalid]), i0

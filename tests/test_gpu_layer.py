@@ -83,14 +83,20 @@ def check_dispatch(cfg, x, idx, d, ref, fmt=api.FMT_FP8):
     nt = t[0]
     cnt = np.minimum(ref["cnt"], cfg.cap) if cfg.layout == configs.MASKED else ref["cnt"]
     assert nt == int(((cnt + 127) // 128).sum())
+    ntp = (cnt + 127) // 128
+    assert t[2] == int(((ntp + 1) // 2).sum())
     tl = t[8: 8 + 8 * nt].reshape(nt, 8)
-    i = 0
+    i = q = 0
     for p in range(cfg.N_phys):
         base = ref["seg_start"][p] if cfg.layout == configs.CONTIG else p * cfg.cap
-        for j in range((cnt[p] + 127) // 128):
-            assert list(tl[i, :5]) == [base + 128 * j, p, min(128, cnt[p] - 128 * j),
-                                       i - j, (cnt[p] + 127) // 128]
+        npairs = (ntp[p] + 1) // 2
+        for j in range(ntp[p]):
+            assert list(tl[i, :7]) == [base + 128 * j, p, min(128, cnt[p] - 128 * j),
+                                       i - j, ntp[p], q, npairs]
             i += 1
+        for j in range(npairs):
+            assert tl[q + j, 7] == i - ntp[p] + 2 * j
+        q += npairs
 
 
 @pytest.mark.parametrize("name", SMALL + ["decode", "sbo"])
@@ -233,6 +239,21 @@ def test_layouts_and_eplb_agree_bitwise(dev):
                   (base.with_(n_phys=0, layout=configs.MASKED, cap=384), None)):
         outs.append(run_layer(c, x, W, bias, ex, em)[1])
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("name", ["small_contig", "small_eplb", "small_sbo"])
+def test_layer_with_cluster_pairs_matches_single_cta(dev, name):
+    cfg, x, W, bias = host_workload(name)
+    ex = host_experts(name)
+    idx, _ = oracle.route(x, W, bias, cfg)
+    emap = eplb_for(cfg, idx)
+    lay = api.MoELayer(cfg, to_dev(W), to_dev(bias), device_weights(ex), eplb_map=emap,
+                       gemm_pairs=1)
+    a = bits(lay.forward(bf16_dev(x)))
+    torch.cuda.synchronize()
+    assert api.read_status(lay.status) == 0
+    _, b = run_layer(cfg, x, W, bias, ex, emap, gemm_pairs=-1)
+    assert np.array_equal(a, b)
 
 
 def test_sbo_equals_sequential(dev):

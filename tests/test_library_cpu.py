@@ -83,9 +83,9 @@ def test_host_argument_checks_return_before_launch(L):
     assert L.moe_dispatch_rows(ctypes.byref(dc)) == 0
     dc = _lib.DispatchCfg(4, 128, 2, 8, 8, 1, 100, 0)             # cap % 128 != 0
     assert L.moe_dispatch(ctypes.byref(dc), *([None] * 13), 0, None, None) == -2
-    g = _lib.GemmArgs(0, 300, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, None)
+    g = _lib.GemmArgs(0, 300, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, None)
     assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -2
-    g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, None)
+    g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, None)
     assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
     cc = _lib.CombineCfg(4, 100, 2, None, 0, 64, 0, 0, 0)          # H % 128 != 0
     assert L.moe_combine(ctypes.byref(cc), *([None] * 7)) == -2
