@@ -40,6 +40,25 @@ def peaks() -> dict:
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch recorded by an ncu capture (profiles/traffic.txt), or None
+    when none exists or the GEMM sources changed since it was taken."""
+    import hashlib
+    csrc = os.path.join(ROOT, "combine_moe_route_03_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    sha = h.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split("#")[0].split()
+        if len(f) == 4 and f[0] == workload and f[1] == kernel and f[2] == sha:
+            return int(f[3])
+    return None
+
+
 def describe(cfg) -> str:
     lay = "masked cap %d" % cfg.cap if cfg.layout == configs.MASKED else "contiguous"
     s = (f"{cfg.name}: B={cfg.B} H={cfg.H} N={cfg.N} K={cfg.K} I={cfg.I} "
@@ -206,7 +225,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode",
                     choices=sorted(configs.NAMED) + sorted(configs.PROFILE))
-    ap.add_argument("--cpu-tokens", type=int, default=4,
+    ap.add_argument("--cpu-tokens", type=int, default=12,
                     help="tokens of the CPU-oracle baseline sample (0 = skip)")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -327,7 +346,8 @@ def main():
         mhz = clocks.get("sm_mhz") or 1900.0
         roof["peak"] = 152 * 128 * 2 * mhz * 1e6 / 1e12
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    tr = recorded_traffic(cfg.name, dom) if dom in ("gateup", "down") else None
+    roof["traffic"] = tr
     roof["kernel"] = dom
     roof["peak_source"] = f"{pk['src']} ({'sustained bf16 x2 for e4m3' if roof['bound'] == 'tensor' else 'hbm_gbs' if roof['bound'] == 'hbm' else 'FFMA units x clock'})"
     per_stage = {}
