@@ -40,6 +40,20 @@ def peaks() -> dict:
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
+def max_over_ranks(ms: float, dist, device) -> float:
+    """Wall time of the slowest rank (every rank gets it)."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Tokens/s of the whole job: every rank processes its own batch each step."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch recorded by an ncu capture (profiles/traffic.txt), or None
     when none exists or the GEMM sources changed since it was taken."""
@@ -286,13 +300,9 @@ def main():
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    ms_total = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     ms_step = ms_total / K
-    value = world * cfg.B / (ms_step * 1e-3)
+    value = whole_job_rate(world, cfg.B, ms_step)
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]))
                 for j, s in enumerate(STAGES)}
 
@@ -312,12 +322,8 @@ def main():
             lay.forward_host(xh, oh)
         b.record()
         torch.cuda.synchronize()
-        ms = a.elapsed_time(b)
-        if dist:
-            tt = torch.tensor([ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms = float(tt.item())
-        e2e = {"value": world * cfg.B / (ms / K * 1e-3), "unit": UNIT,
+        ms = max_over_ranks(a.elapsed_time(b), dist, dev)
+        e2e = {"value": whole_job_rate(world, cfg.B, ms / K), "unit": UNIT,
                "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2}
     st = api.read_status(lay.status)
     if st != 0:
