@@ -99,13 +99,13 @@ def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=N
         o["counts"] = torch.empty(cfg.N_phys, dtype=torch.int32, device=dev)
         o["row_of"] = torch.empty((B, cfg.K), dtype=torch.int32, device=dev)
         o["src_of"] = torch.empty(rows, dtype=torch.int32, device=dev)
-        o["tiles"] = torch.empty(8 + 8 * mt, dtype=torch.int32, device=dev)
+        o["tiles"] = torch.empty(8 + 16 * mt, dtype=torch.int32, device=dev)
         o["ws"] = torch.empty(max(1, sz["ws"]), dtype=torch.uint8, device=dev)
         if shared:
             srows = (B + 127) // 128 * 128
             o["As"] = torch.empty((srows, H), dtype=torch.uint8, device=dev)
             o["As_sf"] = torch.empty(srows * (H // 128) * 4, dtype=torch.uint8, device=dev)
-            o["shared_tiles"] = torch.empty(8 + 8 * (srows // 128), dtype=torch.int32, device=dev)
+            o["shared_tiles"] = torch.empty(8 + 16 * (srows // 128), dtype=torch.int32, device=dev)
     st = status if status is not None else new_status(dev)
     check(load().moe_dispatch(ctypes.byref(dc), ptr(x), ptr(topk_idx), ptr(log2phys), ptr(rep),
                               ptr(o["A"]), ptr(o["A_sf"]), ptr(o["counts"]), ptr(o["row_of"]),
@@ -224,8 +224,8 @@ class MoELayer:
         self.expert_counts = t(cfg.N, dtype=torch.int32)
         self.counts = t(cfg.N_phys, dtype=torch.int32)
         self.row_of = t(B, K, dtype=torch.int32)
-        self.tiles = t(8 + 8 * self.max_tiles, dtype=torch.int32)
-        self.shared_tiles = t(8 + 8 * (self.srows // 128), dtype=torch.int32) if cfg.shared else None
+        self.tiles = t(8 + 16 * self.max_tiles, dtype=torch.int32)
+        self.shared_tiles = t(8 + 16 * (self.srows // 128), dtype=torch.int32) if cfg.shared else None
         self.A = t(rows, H)
         self.A_sf = t(rows * (H // 128) * 4)
         self.H1 = t(rows, I)

@@ -110,8 +110,8 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   g.op = MOE_GEMM_GATEUP_SWIGLU;
   g.n = 2 * L->I;
   g.k = rc.H;
-  g.rows = rows_all;
-  g.max_tiles = rows_all / 128;
+  g.rows = rows_all;            // A / H1 / Y hold the routed rows, then the shared rows
+  g.max_tiles = L->max_tiles;   // capacity of the routed tile list (as dispatch wrote it)
   g.num_experts = rc.N + (L->has_shared ? 1 : 0);
   g.A = L->A;
   g.A_sf = L->A_sf;

@@ -120,12 +120,60 @@ __global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
   }
 }
 
+// Inclusive block-wide scan (Hillis-Steele) of one value per thread.
+__device__ __forceinline__ int block_scan(int32_t *buf, int v) {
+  const int p = threadIdx.x;
+  buf[p] = v;
+  __syncthreads();
+  for (int off = 1; off < kScanThreads; off <<= 1) {
+    const int o = p >= off ? buf[p - off] : 0;
+    __syncthreads();
+    buf[p] += o;
+    __syncthreads();
+  }
+  const int r = buf[p];
+  __syncthreads();
+  return r;
+}
+
+// Work items for the cluster-mode GEMM, in schedule order: an expert's tile pairs
+// (shared weight tile), then — when this expert's odd last tile completes a couple
+// of singles — that couple (the earlier expert's single and this one's), so a
+// single runs soon after the pairs that read the same weight tile.  Item k =
+// {tile 0, tile 1 or -1, first item of its group, items in its group, shared
+// weight tile, 0, 0, 0}; a group's units are N-tile-major.
+__device__ __forceinline__ void write_items(int32_t *items, int first, int nt, int item_first,
+                                            int s_index, int prev_single, bool emit_single) {
+  const int np = nt / 2;
+  for (int j = 0; j < np; ++j) {
+    int32_t *it = items + 8 * (size_t)(item_first + j);
+    it[0] = first + 2 * j;
+    it[1] = first + 2 * j + 1;
+    it[2] = item_first;
+    it[3] = np;
+    it[4] = 1;
+    it[5] = it[6] = it[7] = 0;
+  }
+  if (emit_single) {
+    const int k = item_first + np;
+    int32_t *it = items + 8 * (size_t)k;
+    const int mine = first + nt - 1;
+    it[0] = (s_index & 1) ? prev_single : mine;
+    it[1] = (s_index & 1) ? mine : -1;
+    it[2] = k;
+    it[3] = 1;
+    it[4] = 0;
+    it[5] = it[6] = it[7] = 0;
+  }
+}
+
 __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     int B, int N_phys, int nchunks, int layout, int cap, int64_t rows_alloc, DispatchWs ws,
     int32_t *__restrict__ counts, int32_t *__restrict__ tiles, int32_t *__restrict__ src_of,
     int32_t *__restrict__ shared_tiles, int32_t *status) {
   __shared__ int32_t scan[kScanThreads];
-  __shared__ int32_t total_tiles, total_pairs;
+  __shared__ int32_t single_tile[kScanThreads];
+  __shared__ int32_t totals[4];  // tiles, pairs, singles, items
   const int p = threadIdx.x;
   int cnt = 0, valid = 0, nt = 0;
   if (p < N_phys) {
@@ -142,31 +190,32 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     }
     nt = (valid + 127) / 128;
   }
-  // block-wide inclusive scan of nt (Hillis-Steele)
-  scan[p] = nt;
-  __syncthreads();
-  for (int off = 1; off < kScanThreads; off <<= 1) {
-    const int v = p >= off ? scan[p - off] : 0;
-    __syncthreads();
-    scan[p] += v;
-    __syncthreads();
+  const int first = block_scan(scan, nt) - nt;
+  const int np = nt / 2, ns = nt % 2;
+  const int pairs_incl = block_scan(scan, np);
+  const int sfirst = block_scan(scan, ns) - ns;
+  if (p == kScanThreads - 1) {
+    totals[0] = first + nt;
+    totals[1] = pairs_incl;
+    totals[2] = sfirst + ns;
   }
-  const int first = scan[p] - nt;
-  if (p == kScanThreads - 1) total_tiles = scan[p];
+  single_tile[p] = ns ? first + nt - 1 : -1;
   __syncthreads();
-  // second scan: pairs of consecutive M tiles of one expert (ceil(nt / 2) per expert)
-  const int np = (nt + 1) / 2;
-  scan[p] = np;
+  const int n_singles = totals[2];
+  const bool emit = ns && ((sfirst & 1) || sfirst == n_singles - 1);
+  const int n_items = np + (emit ? 1 : 0);
+  const int item_first = block_scan(scan, n_items) - n_items;
+  if (p == kScanThreads - 1) totals[3] = item_first + n_items;
+  // the earlier single of a couple belongs to the previous expert with a single
+  int prev_single = -1;
+  if (emit && (sfirst & 1))
+    for (int q = p - 1; q >= 0; --q)
+      if (single_tile[q] >= 0) {
+        prev_single = single_tile[q];
+        break;
+      }
   __syncthreads();
-  for (int off = 1; off < kScanThreads; off <<= 1) {
-    const int v = p >= off ? scan[p - off] : 0;
-    __syncthreads();
-    scan[p] += v;
-    __syncthreads();
-  }
-  const int pfirst = scan[p] - np;
-  if (p == kScanThreads - 1) total_pairs = scan[p];
-  __syncthreads();
+  const int64_t max_tiles = rows_alloc / 128;
   if (p < N_phys) {
     const int seg = layout == MOE_LAYOUT_CONTIG ? first * 128 : p * cap;
     ws.seg[p] = seg;
@@ -177,34 +226,37 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
       tl[2] = min(128, valid - 128 * i);
       tl[3] = first;
       tl[4] = nt;
-      tl[5] = pfirst;
-      tl[6] = np;
+      tl[5] = tl[6] = tl[7] = 0;
     }
-    // field 7 of entry q: first M tile of pair q (pairs never outnumber tiles)
-    for (int j = 0; j < np; ++j) tiles[8 + 8 * (size_t)(pfirst + j) + 7] = first + 2 * j;
+    write_items(tiles + 8 + 8 * max_tiles, first, nt, item_first, sfirst, prev_single, emit);
     if (src_of) {  // rows of this expert that no token fills
       const int end = layout == MOE_LAYOUT_CONTIG ? nt * 128 : cap;
       for (int j = valid; j < end; ++j) src_of[seg + j] = -1;
     }
   }
+  const int total_tiles = totals[0];
   const int64_t used = layout == MOE_LAYOUT_CONTIG ? (int64_t)total_tiles * 128
                                                    : (int64_t)N_phys * cap;
   if (p == 0) {
     tiles[0] = total_tiles;
     tiles[1] = (int32_t)used;
-    tiles[2] = total_pairs;
-    for (int i = 3; i < 8; ++i) tiles[i] = 0;
+    tiles[2] = totals[1];
+    tiles[3] = totals[2];
+    tiles[4] = totals[3];
+    for (int i = 5; i < 8; ++i) tiles[i] = 0;
   }
   if (src_of)
     for (int64_t r = used + p; r < rows_alloc; r += kScanThreads) src_of[r] = -1;
-  if (shared_tiles) {
+  if (shared_tiles) {  // one expert, the batch in token order; capacity = its tiles
     const int snt = (B + 127) / 128;
-    const int snp = (snt + 1) / 2;
     if (p == 0) {
       shared_tiles[0] = snt;
       shared_tiles[1] = snt * 128;
-      shared_tiles[2] = snp;
-      for (int i = 3; i < 8; ++i) shared_tiles[i] = 0;
+      shared_tiles[2] = snt / 2;
+      shared_tiles[3] = snt % 2;
+      shared_tiles[4] = snt / 2 + snt % 2;
+      for (int i = 5; i < 8; ++i) shared_tiles[i] = 0;
+      write_items(shared_tiles + 8 + 8 * (size_t)snt, 0, snt, 0, 0, -1, snt % 2);
     }
     for (int i = p; i < snt; i += kScanThreads) {
       int32_t *tl = shared_tiles + 8 + 8 * (size_t)i;
@@ -213,9 +265,7 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
       tl[2] = min(128, B - 128 * i);
       tl[3] = 0;
       tl[4] = snt;
-      tl[5] = 0;
-      tl[6] = snp;
-      tl[7] = i < snp ? 2 * i : 0;
+      tl[5] = tl[6] = tl[7] = 0;
     }
   }
 }

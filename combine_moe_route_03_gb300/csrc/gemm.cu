@@ -66,7 +66,9 @@ struct Unit {
   int ni;      // output column tile
   int band;    // M tiles sharing this unit's weight tile
   bool ok;     // the unit runs (its tile-list entries address memory inside the operands)
-  bool active; // this CTA has a tile (a cluster pair's second CTA may have none)
+  bool active; // this CTA has a tile (a cluster's second CTA may have none)
+  bool mcast;  // pair mode: the two CTAs share one weight tile, half loaded by each
+  bool load_b; // this CTA loads a weight tile (its half, or its own whole one)
 };
 
 __device__ __forceinline__ bool tile_ok(const GemmParams &P, int row0, int nvalid) {
@@ -87,10 +89,17 @@ __device__ __forceinline__ Unit get_unit(const GemmParams &P, int unit, int unit
     u -= units2;
   const int g = u / P.n_tiles;  // some M tile of the right expert band
   const int f = tl[8 + 8 * g + 3], c = tl[8 + 8 * g + 4];
+  const int cap = second ? tl[0] : P.max_tiles;
+  Unit r;
+  // the entry must describe its own band, inside the list
+  if (f < 0 || c < 1 || g < f || g >= f + c || f + c > cap) {
+    r.ok = r.active = r.mcast = r.load_b = false;
+    r.row0 = r.nvalid = r.we = r.ni = r.band = 0;
+    return r;
+  }
   const int local = u - P.n_tiles * f;
   const int mi = f + local % c;
   const int32_t *t = tl + 8 + 8 * mi;
-  Unit r;
   r.ni = local / c;
   r.band = c;
   r.row0 = t[0] + (second ? P.row_offset2 : 0);
@@ -99,13 +108,17 @@ __device__ __forceinline__ Unit get_unit(const GemmParams &P, int unit, int unit
   // every role skips a tile entry that would address memory outside the operands
   r.ok = tile_ok(P, r.row0, r.nvalid) && r.we >= 0 && r.we < P.num_experts && r.ni < P.n_tiles;
   r.active = r.ok;
+  r.mcast = false;
+  r.load_b = r.ok;
   return r;
 }
 
-// Cluster-pair variant: unit -> (pair of M tiles of one expert, N tile); CTA
-// `rank` of the cluster takes the pair's tile `rank` (none if the expert's tile
-// count is odd and this is its last pair).  Units of one band are N-tile-major,
-// pair fastest.
+// Cluster variant: unit -> (work item, N tile) from the item table that follows
+// the tile entries (capacity max_tiles; for tiles2 its own tile count).  CTA `rank`
+// takes the item's tile `rank`.  A shared-weight item (a pair of one expert's
+// tiles) has each CTA load half of the weight tile for both; otherwise each CTA
+// loads its own tile's weights (the second CTA may have no tile).  Units of one
+// item group are N-tile-major, item fastest.
 __device__ __forceinline__ Unit get_pair_unit(const GemmParams &P, int unit, int units2,
                                               int rank) {
   const int32_t *tl = P.tiles;
@@ -115,28 +128,42 @@ __device__ __forceinline__ Unit get_pair_unit(const GemmParams &P, int unit, int
     tl = P.tiles2;
   else
     u -= units2;
-  const int g = u / P.n_tiles;           // some pair of the right band
-  const int m0 = tl[8 + 8 * g + 7];      // first tile of pair g
   Unit r;
-  r.ok = false;
-  r.active = false;
+  r.ok = r.active = r.mcast = r.load_b = false;
   r.row0 = r.nvalid = r.we = r.ni = r.band = 0;
-  if (m0 < 0 || m0 >= P.max_tiles) return r;
-  const int32_t *b = tl + 8 + 8 * m0;
-  const int f = b[3], c = b[4], pf = b[5], pc = b[6];
-  if (pc <= 0 || c <= 0 || f < 0 || f + c > P.max_tiles) return r;
-  const int local = u - P.n_tiles * pf;
-  r.ni = local / pc;
-  const int mi = f + 2 * (local % pc) + rank;
-  r.band = c;
-  r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[b[1]] : b[1]);
-  r.ok = r.we >= 0 && r.we < P.num_experts && r.ni >= 0 && r.ni < P.n_tiles;
-  if (r.ok && mi < f + c) {
+  const int cap = second ? tl[0] : P.max_tiles;
+  const int nitems = tl[4];
+  const int32_t *items = tl + 8 + 8 * (size_t)cap;
+  const int g = u / P.n_tiles;  // some item of the right group
+  if (g >= nitems) return r;
+  const int gf = items[8 * g + 2], gc = items[8 * g + 3];
+  // the item must lie inside the group it names (so local >= 0 below)
+  if (gf < 0 || gc < 1 || g < gf || g >= gf + gc || gf + gc > nitems) return r;
+  const int local = u - P.n_tiles * gf;
+  r.ni = local / gc;
+  const int32_t *it = items + 8 * (gf + local % gc);
+  const int t0 = it[0], mi = rank ? it[1] : it[0];
+  r.mcast = it[4] != 0;
+  if (r.mcast) {  // both CTAs decide alike from tile 0's expert
+    if (t0 < 0 || t0 >= cap || mi < 0 || mi >= cap) return r;
+    const int32_t *e0 = tl + 8 + 8 * t0;
+    r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[e0[1]] : e0[1]);
+    r.band = e0[4];
+    r.ok = r.load_b = r.we >= 0 && r.we < P.num_experts && r.ni < P.n_tiles;
     const int32_t *t = tl + 8 + 8 * mi;
     r.row0 = t[0] + (second ? P.row_offset2 : 0);
     r.nvalid = t[2];
-    r.active = tile_ok(P, r.row0, r.nvalid);
+    r.active = r.ok && tile_ok(P, r.row0, r.nvalid);
+    return r;
   }
+  r.ok = r.ni < P.n_tiles;  // runs even when this CTA has no tile
+  if (!r.ok || mi < 0 || mi >= cap) return r;
+  const int32_t *t = tl + 8 + 8 * mi;
+  r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[t[1]] : t[1]);
+  r.band = t[4];
+  r.row0 = t[0] + (second ? P.row_offset2 : 0);
+  r.nvalid = t[2];
+  r.active = r.load_b = r.we >= 0 && r.we < P.num_experts && tile_ok(P, r.row0, r.nvalid);
   return r;
 }
 
@@ -201,8 +228,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int units2 = P.tiles2 ? P.tiles2[kPair ? 2 : 0] * P.n_tiles : 0;
-  const int total = P.tiles[kPair ? 2 : 0] * P.n_tiles + units2;
+  // work items of a list: its M tiles, or (cluster mode) its pairs + singles two by two
+  auto items = [&](const int32_t *t) { return kPair ? t[4] : t[0]; };
+  const int units2 = P.tiles2 ? items(P.tiles2) * P.n_tiles : 0;
+  const int total = items(P.tiles) * P.n_tiles + units2;
   auto unit_at = [&](int u) {
     return kPair ? get_pair_unit(P, u, units2, rank) : get_unit(P, u, units2);
   };
@@ -226,10 +255,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           continue;
         }
         const int row0 = U.row0, we = U.we, ni = U.ni;
-        const uint64_t pol_w = U.band > (kPair ? 2 : 1) ? pol_keep : pol_stream;
+        // a weight tile that another work item will read again stays in L2
+        const uint64_t pol_w = U.band > (U.mcast ? 2 : 1) ? pol_keep : pol_stream;
         const int a_slices = U.nvalid == BM ? 0 : (U.nvalid + 31) / 32;  // 0: one full box
         const uint32_t a_bytes = a_slices ? a_slices * (A_BYTES / 4) : A_BYTES;
-        const uint32_t tx = (U.active ? a_bytes + SFA_BYTES : 0) + B_BYTES + SFB_BYTES;
+        const uint32_t tx =
+            (U.active ? a_bytes + SFA_BYTES : 0) + (U.load_b ? B_BYTES + SFB_BYTES : 0);
         int wrow0, wrow1, nb0, nb1;
         if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
           wrow0 = we * P.n + ni * 128;
@@ -266,12 +297,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             pol_a);
             bulk_load(ssfa, sfa + (size_t)kb * 512, 512, full);
           }
-          if (kPair) {  // my half of the weight tile, into both CTAs
+          if (U.mcast) {  // my half of the shared weight tile, into both CTAs
             tma_load_2d_mc(sb + rank * (B_BYTES / 2), &tmW, full, kb * BK, rank ? wrow1 : wrow0,
                            kBoth, pol_w);
             bulk_load_mc(ssfb + rank * 512, (rank ? sfb1 : sfb0) + (size_t)kb * 512, 512, full,
                          kBoth);
-          } else {
+          } else if (U.load_b) {
             tma_load_2d(sb, &tmW, full, kb * BK, wrow0, pol_w);
             tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
             bulk_load(ssfb, sfb0 + (size_t)kb * 512, 512, full);

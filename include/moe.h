@@ -39,13 +39,16 @@
  * atoms [E][n/128][k/128][512] (all 512 bytes of a weight atom are equal).
  *
  * Tile list.  moe_dispatch describes the rows it wrote as 128-row "M tiles" in
- * an int32 array `tiles` of 8 + 8*max_tiles entries:
- *   tiles[0] = number of M tiles, tiles[1] = rows in use (contiguous layout),
- *   tiles[2] = number of tile pairs (an expert's tiles grouped two by two);
+ * an int32 array `tiles` of 8 + 16*max_tiles entries:
+ *   header tiles[0..7] = {M tiles, rows in use (contiguous layout), tile pairs,
+ *   singles, work items, 0, 0, 0};
  *   tile i at tiles[8 + 8*i ...]: {first row, physical expert, valid rows (1..128),
- *   first tile of this expert, number of tiles of this expert, first pair of this
- *   expert, number of pairs of this expert, P} where P (in entry q < tiles[2]) is
- *   the first tile of pair q.
+ *   first tile of this expert, number of tiles of this expert, 0, 0, 0};
+ *   work item k at tiles[8 + 8*max_tiles + 8*k ...]: {tile 0, tile 1 or -1, first
+ *   item of its group, items in its group, 1 if both tiles share one expert's
+ *   weights, 0, 0, 0}.  An expert's tiles form pairs two by two; an odd last tile
+ *   is a single, and singles form items two by two; items are listed so that a
+ *   couple of singles follows the pairs of the expert that completes it.
  * Tiles of one expert are consecutive.  The grouped GEMM reads this list on the
  * device, so the host never needs the routing result.
  */
@@ -168,6 +171,9 @@ int moe_dispatch(const moe_dispatch_cfg *cfg, const void *x, const int32_t *topk
                  void *A_shared, void *A_shared_sf, int32_t *shared_tiles, void *workspace,
                  size_t workspace_bytes, int32_t *status, void *stream);
 
+/* Int32 entries of a tile list with room for max_tiles M tiles. */
+#define MOE_TILE_LIST_INTS(max_tiles) (8 + 16 * (max_tiles))
+
 /*
  * moe_dispatch for callers that cannot allocate device memory.  (The pages have
  * no counterpart of this entry point; it exists for library users.)
@@ -220,7 +226,8 @@ int moe_dispatch_noalloc(const moe_dispatch_cfg *cfg, const void *x, const int32
  *   W_sf: SF atoms from moe_pack_weight_scales.
  *   tiles2 (nullable): tiles of a second group, e.g. a shared expert whose rows
  *     sit at row_offset2 in A/out and whose weights are expert expert2 of W; its
- *     tiles join the same persistent grid (scheduled before those of `tiles`).
+ *     tiles join the same persistent grid (scheduled before those of `tiles`); its
+ *     capacity is its own tile count (as moe_dispatch writes a shared tile list).
  *   num_sms: CTAs of the persistent grid (0 = every SM).
  * Limits: k % 128 == 0, n % 256 == 0, 16-byte aligned pointers.
  */

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from combine_moe_route_03_gb300 import api, inputs
-from support import bits, within_tol
+from support import bits, cluster_items, within_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -110,8 +110,9 @@ def test_pack_unpack_sf_atoms_inverse():
 
 @pytest.mark.parametrize("op", [0, 1])
 def test_cluster_pair_gemm_equals_single_cta(dev, op):
-    """Two-CTA clusters sharing weight tiles give the same bytes as one CTA per tile,
-    for experts with 1, 2, 3 and 5 M tiles (odd counts leave a cluster CTA idle)."""
+    """Two-CTA clusters (pairs sharing a weight tile, singles two by two) give the same
+    bytes as one CTA per tile, for experts with 1, 2, 3 and 5 M tiles (three singles:
+    the last cluster item has one idle CTA)."""
     tiles_per_expert = [1, 2, 3, 5, 2]
     E = len(tiles_per_expert)
     k, n = (512, 512) if op == 0 else (256, 768)
@@ -120,18 +121,17 @@ def test_cluster_pair_gemm_equals_single_cta(dev, op):
     q, sf = activations(rows, k, 7)
     W, Wsf = zip(*[inputs.make_fp8_matrix(n, k, (9, 55, e)) for e in range(E)])
     W, Wsf = np.stack(W), np.stack(Wsf)
-    t = np.zeros(8 + 8 * mt, np.int32)
-    t[0], t[1] = mt, rows
-    i = pq = 0
+    t = np.zeros(8 + 16 * mt, np.int32)
+    i = 0
     for e, c in enumerate(tiles_per_expert):
-        npair = (c + 1) // 2
         for j in range(c):
-            t[8 + 8 * (i + j): 8 + 8 * (i + j) + 7] = [128 * (i + j), e, 128 - 5 * j, i, c, pq, npair]
-        for j in range(npair):
-            t[8 + 8 * (pq + j) + 7] = i + 2 * j
+            t[8 + 8 * (i + j): 8 + 8 * (i + j) + 5] = [128 * (i + j), e, 128 - 5 * j, i, c]
         i += c
-        pq += npair
-    t[2] = pq
+    items = cluster_items(tiles_per_expert)
+    t[0:5] = [mt, rows, sum(c // 2 for c in tiles_per_expert),
+              sum(c % 2 for c in tiles_per_expert), len(items)]
+    for k, it in enumerate(items):
+        t[8 + 8 * mt + 8 * k: 8 + 8 * mt + 8 * k + 5] = it
     A = torch.from_numpy(q).to(dev)
     A_sf = torch.from_numpy(pack_sf_atoms(sf)).to(dev)
     Wd = torch.from_numpy(W).to(dev)

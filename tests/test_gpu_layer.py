@@ -5,8 +5,8 @@ import torch
 
 import oracle
 from combine_moe_route_03_gb300 import api, configs, inputs
-from support import (bf16_dev, bits, device_weights, getter, host_experts, host_workload,
-                     shared_of, to_dev, unpack_sf_atoms, within_tol)
+from support import (bf16_dev, bits, cluster_items, device_weights, getter, host_experts,
+                     host_workload, shared_of, to_dev, unpack_sf_atoms, within_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -84,19 +84,20 @@ def check_dispatch(cfg, x, idx, d, ref, fmt=api.FMT_FP8):
     cnt = np.minimum(ref["cnt"], cfg.cap) if cfg.layout == configs.MASKED else ref["cnt"]
     assert nt == int(((cnt + 127) // 128).sum())
     ntp = (cnt + 127) // 128
-    assert t[2] == int(((ntp + 1) // 2).sum())
+    assert list(t[2:5]) == [int((ntp // 2).sum()), int((ntp % 2).sum()),
+                            len(cluster_items(list(ntp)))]
     tl = t[8: 8 + 8 * nt].reshape(nt, 8)
-    i = q = 0
+    i = 0
     for p in range(cfg.N_phys):
         base = ref["seg_start"][p] if cfg.layout == configs.CONTIG else p * cfg.cap
-        npairs = (ntp[p] + 1) // 2
         for j in range(ntp[p]):
-            assert list(tl[i, :7]) == [base + 128 * j, p, min(128, cnt[p] - 128 * j),
-                                       i - j, ntp[p], q, npairs]
+            assert list(tl[i]) == [base + 128 * j, p, min(128, cnt[p] - 128 * j),
+                                   i - j, ntp[p], 0, 0, 0]
             i += 1
-        for j in range(npairs):
-            assert tl[q + j, 7] == i - ntp[p] + 2 * j
-        q += npairs
+    items = cluster_items(list(ntp))
+    mt = d["max_tiles"]
+    got = t[8 + 8 * mt: 8 + 8 * mt + 8 * len(items)].reshape(-1, 8)
+    assert [list(r[:5]) for r in got] == items
 
 
 @pytest.mark.parametrize("name", SMALL + ["decode", "sbo"])

@@ -24,9 +24,9 @@ def _outputs(cfg, B, dev):
         else torch.full(s, -7, dtype=dt, device=dev)  # noqa: E731
     return dict(A=e(rows, cfg.H), A_sf=e(rows * (cfg.H // 128) * 4),
                 counts=e(cfg.N_phys, dt=torch.int32), row_of=e(B, cfg.K, dt=torch.int32),
-                src_of=e(rows, dt=torch.int32), tiles=e(8 + 8 * mt, dt=torch.int32),
+                src_of=e(rows, dt=torch.int32), tiles=e(8 + 16 * mt, dt=torch.int32),
                 As=e(srows, cfg.H), As_sf=e(srows * (cfg.H // 128) * 4),
-                shared_tiles=e(8 + 8 * (srows // 128), dt=torch.int32),
+                shared_tiles=e(8 + 16 * (srows // 128), dt=torch.int32),
                 status=torch.zeros(1, dtype=torch.int32, device=dev))
 
 
