@@ -11,7 +11,7 @@
 // each 1x128 / 128x128 scale repeated over its four 32-wide sub-blocks) and the
 // fp32 accumulator stays in tensor memory for the whole K loop.
 //
-// CTA = 10 warps, one CTA per SM, persistent:
+// CTA = 11 warps, one CTA per SM, persistent:
 //   warp 0  TMA producer: A tile 128x128 e4m3, B tile 256x128 e4m3 (two 128-row
 //           boxes: gate and up halves for GATEUP, two output blocks for DOWN),
 //           and the matching scale atoms (cp.async.bulk), STAGES-deep ring.
@@ -21,6 +21,9 @@
 //           half the columns each; TMEM is released before any math), SwiGLU +
 //           1x128 requantisation (GATEUP) or bf16 rounding (DOWN), global
 //           stores, optional release signals.
+//   warp 10 scheduler: decodes the CTA's work units from the tile list (a few
+//           dependent global loads each) into a shared-memory ring, kUnitQ units
+//           ahead, so no role waits on that latency at a tile boundary.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -29,7 +32,8 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
-constexpr int kGemmThreads = 320;  // producer, MMA, 8 epilogue warps
+constexpr int kGemmThreads = 352;  // producer, MMA, 8 epilogue warps, scheduler
+constexpr int kUnitQ = 8;          // decoded units in flight
 constexpr int kEpiThreads = 256;
 constexpr uint32_t A_BYTES = BM * BK;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK;   // 32 KB
@@ -42,7 +46,9 @@ constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
 constexpr uint32_t OFF_AMAX = OFF_MISC + 16;  // [2][128] partial row amax of the epilogue
-constexpr uint32_t SMEM_BYTES = OFF_AMAX + 2 * 128 * 4 + 1024;  // + alignment slack
+constexpr uint32_t OFF_UNITQ = OFF_AMAX + 2 * 128 * 4;  // [kUnitQ] decoded units
+constexpr uint32_t OFF_UBAR = OFF_UNITQ + kUnitQ * 32;  // [kUnitQ] full, [kUnitQ] empty
+constexpr uint32_t SMEM_BYTES = OFF_UBAR + 2 * kUnitQ * 8 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF = 256;  // scale columns start here, 16 per stage
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -70,6 +76,8 @@ struct Unit {
   bool mcast;  // pair mode: the two CTAs share one weight tile, half loaded by each
   bool load_b; // this CTA loads a weight tile (its half, or its own whole one)
 };
+
+static_assert(sizeof(Unit) <= 32, "unit ring slot");
 
 __device__ __forceinline__ bool tile_ok(const GemmParams &P, int row0, int nvalid) {
   return row0 >= 0 && (int64_t)row0 + 128 <= P.rows && row0 % 128 == 0 && nvalid > 0 &&
@@ -198,6 +206,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t bar_empty = bar_full + 8 * STAGES;           // [STAGES]
   const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
+  const uint32_t bar_unit_full = s_base + OFF_UBAR;          // [kUnitQ]
+  const uint32_t bar_unit_empty = bar_unit_full + 8 * kUnitQ; // [kUnitQ]
+  Unit *unit_q = reinterpret_cast<Unit *>(smem + OFF_UNITQ);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
@@ -212,6 +223,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, kEpiThreads);
+    for (int q = 0; q < kUnitQ; ++q) {
+      mbar_init(bar_unit_full + 8 * q, 1);
+      mbar_init(bar_unit_empty + 8 * q, 2 + kEpiThreads / 32);  // producer, MMA, epilogue warps
+    }
     *abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -235,6 +250,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   auto unit_at = [&](int u) {
     return kPair ? get_pair_unit(P, u, units2, rank) : get_unit(P, u, units2);
   };
+  // The seq-th unit of this CTA from the scheduler's ring (false: timed out / aborted).
+  // The caller releases the slot with release_unit once it has copied the unit.
+  auto take_unit = [&](int seq, Unit &U) {
+    const int slot = seq % kUnitQ;
+    if (!mbar_wait(bar_unit_full + 8 * slot, (uint32_t)(seq / kUnitQ) & 1u, abort, kWaitLimitNs))
+      return false;
+    U = unit_q[slot];
+    return true;
+  };
+  auto release_unit = [&](int seq) { mbar_arrive(bar_unit_empty + 8 * (seq % kUnitQ)); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -248,8 +273,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int unit = first_unit; ok && unit < total; unit += ustride) {
-        const Unit U = unit_at(unit);
+      int seq = 0;
+      for (int unit = first_unit; ok && unit < total; unit += ustride, ++seq) {
+        Unit U;
+        if (!take_unit(seq, U)) {
+          fail(P.status, abort);
+          ok = false;
+          break;
+        }
+        release_unit(seq);
         if (!U.ok) {
           status_or(P.status, MOE_STATUS_BAD_INDEX);
           continue;
@@ -351,8 +383,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int unit = first_unit; ok && unit < total; unit += ustride) {
-        const Unit U = unit_at(unit);
+      int seq = 0;
+      for (int unit = first_unit; ok && unit < total; unit += ustride, ++seq) {
+        Unit U;
+        if (!take_unit(seq, U)) {
+          fail(P.status, abort);
+          break;
+        }
+        release_unit(seq);
         if (!U.ok) continue;
         if (U.active) {
           if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
@@ -402,7 +440,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp < 2 + kEpiThreads / 32) {
     // ------------------------------------------------------------ epilogue
     // Eight warps: a warp may read TMEM lanes 32*(warp%4)..+31 (its rows); the two
     // warps of a lane quarter split the columns.  Each thread moves its half-row of
@@ -414,8 +452,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
     float *amax_x = reinterpret_cast<float *>(smem + OFF_AMAX);  // [half][row]
     uint32_t acc_phase = 0;
-    for (int unit = first_unit; unit < total; unit += ustride) {
-      const Unit U = unit_at(unit);
+    int seq = 0;
+    for (int unit = first_unit; unit < total; unit += ustride, ++seq) {
+      Unit U;
+      if (!take_unit(seq, U)) {
+        fail(P.status, abort);
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) release_unit(seq);
       if (!U.ok || !U.active) continue;
       const int row0 = U.row0, valid = U.nvalid, ni = U.ni;
       const int64_t r = (int64_t)row0 + row_local;
@@ -506,6 +551,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       acc_phase ^= 1;
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ scheduler
+    int seq = 0;
+    for (int unit = first_unit; unit < total; unit += ustride, ++seq) {
+      const int slot = seq % kUnitQ;
+      if (!mbar_wait(bar_unit_empty + 8 * slot, ((uint32_t)(seq / kUnitQ) & 1u) ^ 1u, abort,
+                     kWaitLimitNs)) {
+        fail(P.status, abort);
+        break;
+      }
+      unit_q[slot] = unit_at(unit);
+      mbar_arrive(bar_unit_full + 8 * slot);  // release: the unit is visible to the waiters
     }
   }
 
