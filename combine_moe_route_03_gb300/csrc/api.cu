@@ -128,8 +128,9 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   g.out_sf = L->H1_sf;
   g.num_sms = L->num_sms;
   g.status = L->status;
-  g.pair_tiles = L->gemm_pairs > 0 ||
-                 (L->gemm_pairs == 0 && (int64_t)rc.B * rc.K >= 128LL * L->N_phys);
+  g.pair_tiles = L->gemm_pairs == 2 ? 2
+                 : (L->gemm_pairs > 0 ||
+                    (L->gemm_pairs == 0 && (int64_t)rc.B * rc.K >= 128LL * L->N_phys));
   if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
   mark(3);
   g.op = MOE_GEMM_DOWN;

@@ -63,6 +63,7 @@ struct GemmParams {
   int32_t *signal;
   int bm_signal;
   int32_t *status;
+  int singles;  // one-CTA kernel: only the single tiles of the item table (see get_single_unit)
 };
 
 struct Unit {
@@ -75,6 +76,8 @@ struct Unit {
   bool active; // this CTA has a tile (a cluster's second CTA may have none)
   bool mcast;  // pair mode: the two CTAs share one weight tile, half loaded by each
   bool load_b; // this CTA loads a weight tile (its half, or its own whole one)
+  bool skip;   // not this launch's work (the scheduler drops it)
+  bool end;    // end of the CTA's unit stream
 };
 
 static_assert(sizeof(Unit) <= 32, "unit ring slot");
@@ -101,10 +104,11 @@ __device__ __forceinline__ Unit get_unit(const GemmParams &P, int unit, int unit
   Unit r;
   // the entry must describe its own band, inside the list
   if (f < 0 || c < 1 || g < f || g >= f + c || f + c > cap) {
-    r.ok = r.active = r.mcast = r.load_b = false;
+    r.ok = r.active = r.mcast = r.load_b = r.skip = r.end = false;
     r.row0 = r.nvalid = r.we = r.ni = r.band = 0;
     return r;
   }
+  r.skip = r.end = false;
   const int local = u - P.n_tiles * f;
   const int mi = f + local % c;
   const int32_t *t = tl + 8 + 8 * mi;
@@ -137,7 +141,7 @@ __device__ __forceinline__ Unit get_pair_unit(const GemmParams &P, int unit, int
   else
     u -= units2;
   Unit r;
-  r.ok = r.active = r.mcast = r.load_b = false;
+  r.ok = r.active = r.mcast = r.load_b = r.skip = r.end = false;
   r.row0 = r.nvalid = r.we = r.ni = r.band = 0;
   const int cap = second ? tl[0] : P.max_tiles;
   const int nitems = tl[4];
@@ -175,6 +179,43 @@ __device__ __forceinline__ Unit get_pair_unit(const GemmParams &P, int unit, int
   return r;
 }
 
+// Singles variant (one-CTA kernel after the 2-SM kernel took the pairs): unit ->
+// (item, N tile, slot); the tile in that slot of an item without a shared weight tile,
+// or `skip` (a pair item, or an empty slot).  Two units per item and N tile.
+__device__ __forceinline__ Unit get_single_unit(const GemmParams &P, int unit, int units2) {
+  const int32_t *tl = P.tiles;
+  int u = unit;
+  const bool second = unit < units2;
+  if (second)
+    tl = P.tiles2;
+  else
+    u -= units2;
+  Unit r;
+  r.ok = r.active = r.mcast = r.load_b = r.skip = r.end = false;
+  r.row0 = r.nvalid = r.we = r.ni = r.band = 0;
+  const int cap = second ? tl[0] : P.max_tiles;
+  const int nitems = tl[4];
+  const int32_t *items = tl + 8 + 8 * (size_t)cap;
+  const int g = u / (2 * P.n_tiles), rem = u % (2 * P.n_tiles);
+  if (g >= nitems) return r;
+  const int32_t *it = items + 8 * g;
+  const int mi = it[rem & 1];
+  if (it[4] != 0 || mi < 0) {
+    r.skip = true;
+    return r;
+  }
+  r.ni = rem >> 1;
+  if (mi >= cap) return r;
+  const int32_t *t = tl + 8 + 8 * mi;
+  r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[t[1]] : t[1]);
+  r.band = t[4];
+  r.row0 = t[0] + (second ? P.row_offset2 : 0);
+  r.nvalid = t[2];
+  r.ok = r.active = r.load_b = tile_ok(P, r.row0, r.nvalid) && r.we >= 0 &&
+                               r.we < P.num_experts;
+  return r;
+}
+
 __device__ __forceinline__ size_t sf_atom_off(int64_t r, int kb, int Kb) {
   return ((size_t)(r >> 7) * Kb + kb) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5);
 }
@@ -182,6 +223,98 @@ __device__ __forceinline__ size_t sf_atom_off(int64_t r, int kb, int Kb) {
 __device__ __forceinline__ void fail(int32_t *status, volatile int *abort) {
   *abort = 1;
   status_or(status, MOE_STATUS_TIMEOUT);
+}
+
+// Epilogue of one 128-row accumulator for this thread's half-row: TMEM ->
+// registers, release() (the MMAs may overwrite the accumulator from then on), then
+// SwiGLU + 1x128 requantisation (GATEUP) or bf16 rounding (DOWN), global stores and
+// the optional per-block_m release signals.  All kEpiThreads epilogue threads call it.
+template <class Release>
+__device__ __forceinline__ void epilogue_tile(const GemmParams &P, int row0, int valid, int ni,
+                                              uint32_t t_row, int half, int row_local, int warp,
+                                              int lane, float *amax_x, Release release) {
+  const int64_t r = (int64_t)row0 + row_local;
+  const bool store = row_local < valid && r < P.rows;
+  if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
+    // gate columns [64*half, +64) and the matching up columns [128 + 64*half, +64)
+    uint32_t g[64], u[64];
+    MOE_TMEM_LD_32x32b_X32(t_row + 64 * half, g);
+    MOE_TMEM_LD_32x32b_X32(t_row + 64 * half + 32, (g + 32));
+    MOE_TMEM_LD_32x32b_X32(t_row + 128 + 64 * half, u);
+    MOE_TMEM_LD_32x32b_X32(t_row + 128 + 64 * half + 32, (u + 32));
+    tc_wait_ld();
+    tc_fence_before();
+    release();
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float gf = __uint_as_float(g[i]), uf = __uint_as_float(u[i]);
+      const float v = __fdividef(gf, 1.0f + __expf(-gf)) * uf;  // silu(g) * u
+      g[i] = __float_as_uint(v);
+      amax = fmaxf(amax, fabsf(v));
+    }
+    // the 1x128 block of h spans both halves of the row
+    amax_x[half * 128 + row_local] = amax;
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+    amax = fmaxf(amax, amax_x[(half ^ 1) * 128 + row_local]);
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+    if (store) {
+      const int e = ue8m0_exp(amax);
+      const float inv = pow2i(-e);
+      uint8_t *dst = P.out + (size_t)r * P.I + (size_t)ni * 128 + 64 * half;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 w;
+        uint32_t *wp = &w.x;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int b = 16 * c + 4 * j;
+          wp[j] = e4m3x2(__fmul_rn(__uint_as_float(g[b]), inv),
+                         __fmul_rn(__uint_as_float(g[b + 1]), inv)) |
+                  (e4m3x2(__fmul_rn(__uint_as_float(g[b + 2]), inv),
+                          __fmul_rn(__uint_as_float(g[b + 3]), inv))
+                   << 16);
+        }
+        *reinterpret_cast<uint4 *>(dst + 16 * c) = w;
+      }
+      if (half == 0)
+        *reinterpret_cast<uint32_t *>(P.out_sf + sf_atom_off(r, ni, P.I / 128)) =
+            (uint32_t)(e + 127) * 0x01010101u;
+    }
+  } else {
+    // output columns [128*half, +128)
+    uint32_t v[128];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) MOE_TMEM_LD_32x32b_X32(t_row + 128 * half + 32 * c, (v + 32 * c));
+    tc_wait_ld();
+    tc_fence_before();
+    release();
+    if (store) {
+      uint8_t *dst = P.out + ((size_t)r * P.n + (size_t)ni * 256 + 128 * half) * 2;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        uint4 w;
+        w.x = f32_to_bf16_bits(__uint_as_float(v[8 * j + 0])) |
+              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 1])) << 16);
+        w.y = f32_to_bf16_bits(__uint_as_float(v[8 * j + 2])) |
+              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 3])) << 16);
+        w.z = f32_to_bf16_bits(__uint_as_float(v[8 * j + 4])) |
+              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 5])) << 16);
+        w.w = f32_to_bf16_bits(__uint_as_float(v[8 * j + 6])) |
+              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 7])) << 16);
+        *reinterpret_cast<uint4 *>(dst + 16 * j) = w;
+      }
+    }
+    if (P.signal) {
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      if (warp == 2 && lane == 0) {
+        for (int j = 0; j * P.bm_signal < BM; ++j)
+          if (j * P.bm_signal < valid && row0 + j * P.bm_signal < P.rows)
+            red_release_gpu_add(P.signal + (row0 + j * P.bm_signal) / P.bm_signal, 1);
+      }
+    }
+  }
 }
 
 // tmA loads full 128-row A tiles; tmA32 loads 32-row slices, used for tiles with
@@ -244,11 +377,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // work items of a list: its M tiles, or (cluster mode) its pairs + singles two by two
-  auto items = [&](const int32_t *t) { return kPair ? t[4] : t[0]; };
+  auto items = [&](const int32_t *t) { return kPair ? t[4] : (P.singles ? 2 * t[4] : t[0]); };
   const int units2 = P.tiles2 ? items(P.tiles2) * P.n_tiles : 0;
   const int total = items(P.tiles) * P.n_tiles + units2;
   auto unit_at = [&](int u) {
-    return kPair ? get_pair_unit(P, u, units2, rank) : get_unit(P, u, units2);
+    return kPair ? get_pair_unit(P, u, units2, rank)
+                 : (P.singles ? get_single_unit(P, u, units2) : get_unit(P, u, units2));
   };
   // The seq-th unit of this CTA from the scheduler's ring (false: timed out / aborted).
   // The caller releases the slot with release_unit once it has copied the unit.
@@ -273,8 +407,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      int seq = 0;
-      for (int unit = first_unit; ok && unit < total; unit += ustride, ++seq) {
+      for (int seq = 0; ok; ++seq) {
         Unit U;
         if (!take_unit(seq, U)) {
           fail(P.status, abort);
@@ -282,6 +415,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         release_unit(seq);
+        if (U.end) break;
         if (!U.ok) {
           status_or(P.status, MOE_STATUS_BAD_INDEX);
           continue;
@@ -383,14 +517,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      int seq = 0;
-      for (int unit = first_unit; ok && unit < total; unit += ustride, ++seq) {
+      for (int seq = 0; ok; ++seq) {
         Unit U;
         if (!take_unit(seq, U)) {
           fail(P.status, abort);
           break;
         }
         release_unit(seq);
+        if (U.end) break;
         if (!U.ok) continue;
         if (U.active) {
           if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
@@ -452,8 +586,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
     float *amax_x = reinterpret_cast<float *>(smem + OFF_AMAX);  // [half][row]
     uint32_t acc_phase = 0;
-    int seq = 0;
-    for (int unit = first_unit; unit < total; unit += ustride, ++seq) {
+    for (int seq = 0;; ++seq) {
       Unit U;
       if (!take_unit(seq, U)) {
         fail(P.status, abort);
@@ -461,109 +594,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       __syncwarp();
       if (lane == 0) release_unit(seq);
+      if (U.end) break;
       if (!U.ok || !U.active) continue;
       const int row0 = U.row0, valid = U.nvalid, ni = U.ni;
-      const int64_t r = (int64_t)row0 + row_local;
-      const bool store = row_local < valid && r < P.rows;
       if (!mbar_wait(bar_acc_full, acc_phase, abort, kWaitLimitNs)) {
         fail(P.status, abort);
         break;
       }
       tc_fence_after();
-      if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
-        // gate columns [64*half, +64) and the matching up columns [128 + 64*half, +64)
-        uint32_t g[64], u[64];
-        MOE_TMEM_LD_32x32b_X32(t_row + 64 * half, g);
-        MOE_TMEM_LD_32x32b_X32(t_row + 64 * half + 32, (g + 32));
-        MOE_TMEM_LD_32x32b_X32(t_row + 128 + 64 * half, u);
-        MOE_TMEM_LD_32x32b_X32(t_row + 128 + 64 * half + 32, (u + 32));
-        tc_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar_acc_empty);
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float gf = __uint_as_float(g[i]), uf = __uint_as_float(u[i]);
-          const float v = __fdividef(gf, 1.0f + __expf(-gf)) * uf;  // silu(g) * u
-          g[i] = __float_as_uint(v);
-          amax = fmaxf(amax, fabsf(v));
-        }
-        // the 1x128 block of h spans both halves of the row
-        amax_x[half * 128 + row_local] = amax;
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-        amax = fmaxf(amax, amax_x[(half ^ 1) * 128 + row_local]);
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-        if (store) {
-          const int e = ue8m0_exp(amax);
-          const float inv = pow2i(-e);
-          uint8_t *dst = P.out + (size_t)r * P.I + (size_t)ni * 128 + 64 * half;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint4 w;
-            uint32_t *wp = &w.x;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int b = 16 * c + 4 * j;
-              wp[j] = e4m3x2(__fmul_rn(__uint_as_float(g[b]), inv),
-                             __fmul_rn(__uint_as_float(g[b + 1]), inv)) |
-                      (e4m3x2(__fmul_rn(__uint_as_float(g[b + 2]), inv),
-                              __fmul_rn(__uint_as_float(g[b + 3]), inv))
-                       << 16);
-            }
-            *reinterpret_cast<uint4 *>(dst + 16 * c) = w;
-          }
-          if (half == 0)
-            *reinterpret_cast<uint32_t *>(P.out_sf + sf_atom_off(r, ni, P.I / 128)) =
-                (uint32_t)(e + 127) * 0x01010101u;
-        }
-      } else {
-        // output columns [128*half, +128)
-        uint32_t v[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) MOE_TMEM_LD_32x32b_X32(t_row + 128 * half + 32 * c, (v + 32 * c));
-        tc_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar_acc_empty);
-        if (store) {
-          uint8_t *dst = P.out + ((size_t)r * P.n + (size_t)ni * 256 + 128 * half) * 2;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            uint4 w;
-            w.x = f32_to_bf16_bits(__uint_as_float(v[8 * j + 0])) |
-                  (f32_to_bf16_bits(__uint_as_float(v[8 * j + 1])) << 16);
-            w.y = f32_to_bf16_bits(__uint_as_float(v[8 * j + 2])) |
-                  (f32_to_bf16_bits(__uint_as_float(v[8 * j + 3])) << 16);
-            w.z = f32_to_bf16_bits(__uint_as_float(v[8 * j + 4])) |
-                  (f32_to_bf16_bits(__uint_as_float(v[8 * j + 5])) << 16);
-            w.w = f32_to_bf16_bits(__uint_as_float(v[8 * j + 6])) |
-                  (f32_to_bf16_bits(__uint_as_float(v[8 * j + 7])) << 16);
-            *reinterpret_cast<uint4 *>(dst + 16 * j) = w;
-          }
-        }
-        if (P.signal) {
-          __threadfence();
-          asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-          if (warp == 2 && lane == 0) {
-            for (int j = 0; j * P.bm_signal < BM; ++j)
-              if (j * P.bm_signal < valid && row0 + j * P.bm_signal < P.rows)
-                red_release_gpu_add(P.signal + (row0 + j * P.bm_signal) / P.bm_signal, 1);
-          }
-        }
-      }
+      epilogue_tile(P, row0, valid, ni, t_row, half, row_local, warp, lane, amax_x,
+                    [&] { mbar_arrive(bar_acc_empty); });
       acc_phase ^= 1;
     }
   } else if (lane == 0) {
     // ------------------------------------------------------------ scheduler
     int seq = 0;
-    for (int unit = first_unit; unit < total; unit += ustride, ++seq) {
+    auto push = [&](const Unit &U) {
       const int slot = seq % kUnitQ;
       if (!mbar_wait(bar_unit_empty + 8 * slot, ((uint32_t)(seq / kUnitQ) & 1u) ^ 1u, abort,
                      kWaitLimitNs)) {
         fail(P.status, abort);
-        break;
+        return false;
       }
-      unit_q[slot] = unit_at(unit);
+      unit_q[slot] = U;
       mbar_arrive(bar_unit_full + 8 * slot);  // release: the unit is visible to the waiters
+      ++seq;
+      return true;
+    };
+    bool ok = true;
+    for (int unit = first_unit; ok && unit < total; unit += ustride) {
+      const Unit U = unit_at(unit);
+      if (!U.skip) ok = push(U);
+    }
+    if (ok) {
+      Unit end = {};
+      end.end = true;
+      push(end);
     }
   }
 
@@ -574,6 +640,399 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_dealloc(tmem, TMEM_COLS);
   }
   if (kPair) cluster_sync();  // neither CTA leaves while the other may still target it
+}
+
+// ------------------------------------------------------------ 2-SM variant
+// The two CTAs of a cluster (the two SMs of a TPC) run one M=256 x N=256 block-
+// scaled MMA per 32-K step (tcgen05 cta_group::2).  Each CTA holds its own 128
+// activation rows, half of the 256-row weight tile and both weight scale atoms; in
+// TMEM it holds its rows' accumulator and scales.  The even CTA issues the MMAs and
+// scale copies for both.  Both CTAs' TMA loads complete on the even CTA's stage
+// barrier, and the MMA commits free the stage in both.  Per SM, a 128-deep k-block
+// moves 16 KB of weights instead of 32 KB, and that operand traffic is what bounds
+// the one-CTA kernel near the ridge.  A pair item (two M tiles of one expert) is one
+// sub-unit.  A couple of singles of different experts is two: one tile each, the
+// other CTA's rows idle.
+// A stage holds KB2 k-blocks (256 K): the issuing thread waits, fences and commits
+// once per eight MMAs, which keeps the pair's tensor pipe fed.
+constexpr int KB2 = 2, S2 = 3;              // k-blocks per stage, stages
+constexpr uint32_t BH_BYTES = B_BYTES / 2;  // a CTA's half of a k-block's weight tile
+constexpr uint32_t O2_A = 0;
+constexpr uint32_t O2_B = O2_A + S2 * KB2 * A_BYTES;
+constexpr uint32_t O2_SFA = O2_B + S2 * KB2 * BH_BYTES;
+constexpr uint32_t O2_SFB = O2_SFA + S2 * KB2 * SFA_BYTES;
+constexpr uint32_t O2_BAR = O2_SFB + S2 * KB2 * SFB_BYTES;  // full, empty [S2]; acc full, empty
+constexpr uint32_t O2_MISC = O2_BAR + (2 * S2 + 2) * 8;
+constexpr uint32_t O2_AMAX = O2_MISC + 16;
+constexpr uint32_t O2_UNITQ = O2_AMAX + 2 * 128 * 4;
+constexpr uint32_t O2_UBAR = O2_UNITQ + kUnitQ * 32;
+constexpr uint32_t SMEM2_BYTES = O2_UBAR + 2 * kUnitQ * 8 + 1024;
+constexpr uint32_t TMEM_SF2 = 256;  // scale columns of stage s, k-block h: +32 s + 16 h
+static_assert(TMEM_SF2 + 32 * S2 <= TMEM_COLS, "TMEM columns");
+
+struct Unit2 {
+  int row0, nvalid;  // this CTA's tile, when active
+  int we, ni, band;
+  uint32_t tx;       // bytes one stage brings into both CTAs (expected on the even CTA)
+  bool ok, active, end;
+};
+static_assert(sizeof(Unit2) <= 32, "unit ring slot");
+
+// Work unit -> its 2-SM sub-unit (1), 0 for a unit of a single (not this launch's
+// work), -1 when the unit's entries do not describe tiles inside the operands.  Both CTAs compute the same list (rank only selects
+// which tile fills row0/nvalid/active).
+__device__ __forceinline__ int get_pair2_units(const GemmParams &P, int unit, int units2,
+                                               int rank, Unit2 *out) {
+  const int32_t *tl = P.tiles;
+  int u = unit;
+  const bool second = unit < units2;
+  if (second)
+    tl = P.tiles2;
+  else
+    u -= units2;
+  const int cap = second ? tl[0] : P.max_tiles;
+  const int nitems = tl[4];
+  const int32_t *items = tl + 8 + 8 * (size_t)cap;
+  const int g = u / P.n_tiles;
+  if (g >= nitems) return -1;
+  const int gf = items[8 * g + 2], gc = items[8 * g + 3];
+  if (gf < 0 || gc < 1 || g < gf || g >= gf + gc || gf + gc > nitems) return -1;
+  const int local = u - P.n_tiles * gf;
+  const int ni = local / gc;
+  if (ni >= P.n_tiles) return -1;
+  const int32_t *it = items + 8 * (gf + local % gc);
+  if (it[4] == 0) return 0;  // singles: the one-CTA launch that follows takes them
+  int sub[2][2];
+  int ns = 1;
+  sub[0][0] = it[0];  // one expert's pair: one sub-unit, both CTAs
+  sub[0][1] = it[1];
+  for (int s = 0; s < ns; ++s) {
+    Unit2 &U = out[s];
+    U.ok = U.active = U.end = false;
+    U.row0 = U.nvalid = 0;
+    U.ni = ni;
+    const int lead = sub[s][0] >= 0 ? sub[s][0] : sub[s][1];  // the tile naming the weights
+    if (lead < 0 || lead >= cap) return -1;
+    const int32_t *e = tl + 8 + 8 * lead;
+    U.we = second ? P.expert2 : (P.phys2log ? P.phys2log[e[1]] : e[1]);
+    U.band = e[4];
+    if (U.we < 0 || U.we >= P.num_experts) return -1;
+    uint32_t tx = 0;
+    for (int c = 0; c < 2; ++c) {
+      tx += KB2 * BH_BYTES;
+      const int mi = sub[s][c];
+      if (mi < 0) continue;
+      if (mi >= cap) return -1;
+      const int32_t *t = tl + 8 + 8 * mi;
+      const int row0 = t[0] + (second ? P.row_offset2 : 0), nv = t[2];
+      if (!tile_ok(P, row0, nv)) return -1;
+      const int slices = nv == BM ? 0 : (nv + 31) / 32;
+      tx += KB2 * ((slices ? slices * (A_BYTES / 4) : A_BYTES) + SFA_BYTES + SFB_BYTES);
+      if (c == rank) {
+        U.row0 = row0;
+        U.nvalid = nv;
+        U.active = true;
+      }
+    }
+    U.tx = tx;
+    U.ok = true;
+  }
+  return ns;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmA32,
+                              const __grid_constant__ CUtensorMap tmW,
+                              const __grid_constant__ CUtensorMap tmSFA,
+                              const __grid_constant__ CUtensorMap tmSFW, const GemmParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t bar_full = s_base + O2_BAR;          // [S2], used in the even CTA
+  const uint32_t bar_empty = bar_full + 8 * S2;       // [S2]
+  const uint32_t bar_acc_full = bar_empty + 8 * S2;
+  const uint32_t bar_acc_empty = bar_acc_full + 8;    // used in the even CTA
+  const uint32_t bar_unit_full = s_base + O2_UBAR;
+  const uint32_t bar_unit_empty = bar_unit_full + 8 * kUnitQ;
+  Unit2 *unit_q = reinterpret_cast<Unit2 *>(smem + O2_UNITQ);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + O2_MISC);
+  volatile int *abort = reinterpret_cast<volatile int *>(smem + O2_MISC + 4);
+  constexpr uint16_t kBoth = 3;
+  const int rank = (int)cluster_ctarank();
+  const int first_unit = (int)cluster_id_x();
+  const int ustride = (int)cluster_count_x();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S2; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, 2 * (kEpiThreads / 32));  // epilogue warps of both CTAs
+    for (int q = 0; q < kUnitQ; ++q) {
+      mbar_init(bar_unit_full + 8 * q, 1);
+      mbar_init(bar_unit_empty + 8 * q, 2 + kEpiThreads / 32);
+    }
+    *abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmA32);
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmSFA);
+    tma_prefetch_desc(&tmSFW);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before anything targets them
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int units2 = P.tiles2 ? P.tiles2[4] * P.n_tiles : 0;
+  const int total = P.tiles[4] * P.n_tiles + units2;
+  auto take = [&](int seq, Unit2 &U) {
+    const int slot = seq % kUnitQ;
+    if (!mbar_wait(bar_unit_full + 8 * slot, (uint32_t)(seq / kUnitQ) & 1u, abort, kWaitLimitNs))
+      return false;
+    U = unit_q[slot];
+    return true;
+  };
+  auto release_unit = [&](int seq) { mbar_arrive(bar_unit_empty + 8 * (seq % kUnitQ)); };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_normal();
+      const uint64_t pol_a = policy_evict_last();
+      const uint32_t lead_full = mapa_shared(bar_full, 0);  // the even CTA's stage barriers
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int seq = 0; ok; ++seq) {
+        Unit2 U;
+        if (!take(seq, U)) {
+          fail(P.status, abort);
+          ok = false;
+          break;
+        }
+        release_unit(seq);
+        if (U.end) break;
+        if (!U.ok) {
+          status_or(P.status, MOE_STATUS_BAD_INDEX);
+          continue;
+        }
+        const int we = U.we, ni = U.ni;
+        const uint64_t pol_w = U.band > 2 ? pol_keep : pol_stream;
+        const int a_slices = U.nvalid == BM ? 0 : (U.nvalid + 31) / 32;
+        int wrow, nb0, nb1;
+        if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
+          wrow = we * P.n + (rank ? P.I : 0) + ni * 128;  // gate half / up half
+          nb0 = ni;
+          nb1 = P.I / 128 + ni;
+        } else {
+          wrow = we * P.n + ni * 256 + 128 * rank;
+          nb0 = 2 * ni;
+          nb1 = 2 * ni + 1;
+        }
+        const int sfa_atom = (U.row0 >> 7) * P.Kb;
+        const int sfb_atom0 = (we * (P.n / 128) + nb0) * P.Kb;
+        const int sfb_atom1 = (we * (P.n / 128) + nb1) * P.Kb;
+        for (int kb = 0; kb < P.Kb; kb += KB2) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort, kWaitLimitNs)) {
+            fail(P.status, abort);
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, U.tx);
+          const uint32_t fb = lead_full + 8 * stage;
+          const uint32_t sb = s_base + O2_B + stage * KB2 * BH_BYTES;
+#pragma unroll
+          for (int h = 0; h < KB2; ++h)
+            tma_load_2d_pair(sb + h * BH_BYTES, &tmW, fb, (kb + h) * BK, wrow, pol_w);
+          if (U.active) {
+            const uint32_t sa = s_base + O2_A + stage * KB2 * A_BYTES;
+#pragma unroll
+            for (int h = 0; h < KB2; ++h) {
+              if (a_slices == 0)
+                tma_load_2d_pair(sa + h * A_BYTES, &tmA, fb, (kb + h) * BK, U.row0, pol_a);
+              else
+                for (int j = 0; j < a_slices; ++j)
+                  tma_load_2d_pair(sa + h * A_BYTES + j * (A_BYTES / 4), &tmA32, fb, (kb + h) * BK,
+                                   U.row0 + 32 * j, pol_a);
+            }
+            // scale atoms of consecutive k-blocks are adjacent: one box per stage each
+            tma_load_2d_pair(s_base + O2_SFA + stage * KB2 * SFA_BYTES, &tmSFA, fb, 0,
+                             sfa_atom + kb, pol_a);
+            const uint32_t ssfb = s_base + O2_SFB + stage * KB2 * SFB_BYTES;
+            tma_load_2d_pair(ssfb, &tmSFW, fb, 0, sfb_atom0 + kb, pol_w);
+            tma_load_2d_pair(ssfb + KB2 * 512, &tmSFW, fb, 0, sfb_atom1 + kb, pol_w);
+          }
+          ++issued;
+          if (++stage == S2) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already in flight land before the CTA can exit: the even CTA
+        // sees them on its stage barriers, the odd CTA waits a fixed grace period.
+        if (rank == 0) {
+          volatile int never = 0;
+          for (int i = 0; i < S2 && i < issued; ++i) {
+            if (--stage < 0) {
+              stage = S2 - 1;
+              phase ^= 1;
+            }
+            mbar_wait(bar_full + 8 * stage, phase, &never, 100000000ull);
+          }
+        } else {
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 1000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // N = 256, UE8M0 scales, M = 256 over the pair; bits 4-5 / 29-30 pick the scale byte
+      const uint32_t idesc_base = ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+                                  ((uint32_t)((2 * BM) >> 4) << 24);
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int seq = 0; ok; ++seq) {
+        Unit2 U;
+        if (!take(seq, U)) {
+          fail(P.status, abort);
+          break;
+        }
+        release_unit(seq);
+        if (U.end) break;
+        if (!U.ok || rank != 0) continue;  // the odd CTA only follows the unit stream
+        if (!mbar_wait_cluster(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
+          fail(P.status, abort);
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < P.Kb; kb += KB2) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort, kWaitLimitNs)) {
+            fail(P.status, abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // a stage's scale columns are rewritten S2 stages later, after its refill
+          const uint32_t ssfa = s_base + O2_SFA + stage * KB2 * SFA_BYTES;
+          const uint32_t ssfb = s_base + O2_SFB + stage * KB2 * SFB_BYTES;
+          const uint32_t sa = s_base + O2_A + stage * KB2 * A_BYTES;
+          const uint32_t sb = s_base + O2_B + stage * KB2 * BH_BYTES;
+#pragma unroll
+          for (int h = 0; h < KB2; ++h) {
+            const uint32_t t_sfa = tmem + TMEM_SF2 + 32 * stage + 16 * h;
+            const uint32_t t_sfb = t_sfa + 4;
+            tc_cp_pair_32x128b_x4(t_sfa, smem_desc(ssfa + 512 * h, 16, 128, 0));
+            tc_cp_pair_32x128b_x4(t_sfb, smem_desc(ssfb + 512 * h, 16, 128, 0));
+            tc_cp_pair_32x128b_x4(t_sfb + 4, smem_desc(ssfb + KB2 * 512 + 512 * h, 16, 128, 0));
+#pragma unroll
+            for (int j = 0; j < BK / 32; ++j) {
+              const uint64_t ad = smem_desc(sa + h * A_BYTES + 32 * j, 16, 1024, 2);
+              const uint64_t bd = smem_desc(sb + h * BH_BYTES + 32 * j, 16, 1024, 2);
+              const uint32_t idesc = idesc_base | ((uint32_t)j << 29) | ((uint32_t)j << 4);
+              tc_mma_pair_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | h | j) != 0);
+            }
+          }
+          tc_commit_pair_mc(bar_empty + 8 * stage, kBoth);
+          if (++stage == S2) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(bar_acc_full, kBoth);
+        acc_phase ^= 1;
+      }
+    }
+  } else if (warp < 2 + kEpiThreads / 32) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row_local = 32 * q + lane;
+    const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
+    float *amax_x = reinterpret_cast<float *>(smem + O2_AMAX);
+    const uint32_t lead_acc_empty = mapa_shared(bar_acc_empty, 0);
+    auto release_acc = [&] {
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(lead_acc_empty);
+    };
+    uint32_t acc_phase = 0;
+    for (int seq = 0;; ++seq) {
+      Unit2 U;
+      if (!take(seq, U)) {
+        fail(P.status, abort);
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) release_unit(seq);
+      if (U.end) break;
+      if (!U.ok) continue;
+      if (!mbar_wait(bar_acc_full, acc_phase, abort, kWaitLimitNs)) {
+        fail(P.status, abort);
+        break;
+      }
+      tc_fence_after();
+      if (U.active) {
+        epilogue_tile(P, U.row0, U.nvalid, U.ni, t_row, half, row_local, warp, lane, amax_x,
+                      release_acc);
+      } else {  // this CTA's rows of the pair MMA carry no tile
+        tc_fence_before();
+        release_acc();
+      }
+      acc_phase ^= 1;
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ scheduler
+    int seq = 0;
+    auto push = [&](const Unit2 &U) {
+      const int slot = seq % kUnitQ;
+      if (!mbar_wait(bar_unit_empty + 8 * slot, ((uint32_t)(seq / kUnitQ) & 1u) ^ 1u, abort,
+                     kWaitLimitNs)) {
+        fail(P.status, abort);
+        return false;
+      }
+      unit_q[slot] = U;
+      mbar_arrive(bar_unit_full + 8 * slot);
+      ++seq;
+      return true;
+    };
+    bool ok = true;
+    for (int unit = first_unit; ok && unit < total; unit += ustride) {
+      Unit2 sub[2];
+      const int n = get_pair2_units(P, unit, units2, rank, sub);
+      if (n < 0) {
+        Unit2 bad = {};
+        ok = push(bad);
+      }
+      for (int i = 0; ok && i < n; ++i) ok = push(sub[i]);
+    }
+    if (ok) {
+      Unit2 end = {};
+      end.end = true;
+      push(end);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the even CTA's MMAs read the odd CTA's shared memory to the end
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
 __global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ atoms,
@@ -617,6 +1076,48 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Scale atoms [n_atoms][512 bytes] as a 2-D uint32 tensor [n_atoms][128], box_atoms
+// atoms per box, so TMA (which can signal the other CTA of a pair) moves them.
+bool make_sf_map(CUtensorMap *m, const void *base, uint64_t n_atoms, uint32_t box_atoms) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || n_atoms == 0 || n_atoms > 0x7fffffffull) return false;
+  cuuint64_t dims[2] = {128, n_atoms};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, box_atoms};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-CTA cluster launch of `kernel` on at most one cluster per SM pair, no more
+// clusters than can be resident at once (the grid is persistent).
+template <class Kernel, class... Args>
+int launch_pairs(Kernel kernel, uint32_t smem, int sms, int &max_clusters, cudaStream_t st,
+                 Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sms / 2 * 2 > 0 ? sms / 2 * 2 : 2));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg);
+    if (e != cudaSuccess || max_clusters <= 0)
+      return set_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidConfiguration);
+  }
+  if ((int)cfg.gridDim.x / 2 > max_clusters) cfg.gridDim = dim3((unsigned)(2 * max_clusters));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return check_launch();
 }
 
 }  // namespace
@@ -684,6 +1185,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.signal = a->signal;
   P.bm_signal = a->block_m_signal > 0 ? a->block_m_signal : BM;
   P.status = a->status;
+  P.singles = 0;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
@@ -692,34 +1194,33 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_pair2_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
     if (e != cudaSuccess) return set_cuda_error(e);
     attr_set = true;
   }
   const int sms = a->num_sms > 0 ? a->num_sms : device_sm_count();
-  if (a->pair_tiles) {
-    // one 2-CTA cluster per pair of SMs
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(sms / 2 * 2 > 0 ? sms / 2 * 2 : 2));
-    cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = as_stream(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // a persistent grid must be resident all at once: no more clusters than fit
-    static int max_clusters = 0;
-    if (max_clusters == 0) {
-      cudaError_t e = cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_kernel<true>, &cfg);
-      if (e != cudaSuccess || max_clusters <= 0) return set_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidConfiguration);
-    }
-    if ((int)cfg.gridDim.x / 2 > max_clusters) cfg.gridDim = dim3((unsigned)(2 * max_clusters));
-    cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<true>, mA, mA32, mW, P);
-    if (e != cudaSuccess) return set_cuda_error(e);
+  if (a->pair_tiles == 2) {
+    if (a->k % (KB2 * BK)) return MOE_ERR_UNSUPPORTED;
+    CUtensorMap mSFA, mSFW;
+    if (!make_sf_map(&mSFA, a->A_sf, (uint64_t)(a->rows / 128) * (a->k / BK), KB2) ||
+        !make_sf_map(&mSFW, a->W_sf, (uint64_t)a->num_experts * (a->n / 128) * (a->k / BK), KB2))
+      return MOE_ERR_CUDA;
+    // the pairs on 2-SM MMAs, then the single tiles on one CTA each
+    static int max_clusters2 = 0;
+    int rc = launch_pairs(grouped_gemm_pair2_kernel, SMEM2_BYTES, sms, max_clusters2,
+                          as_stream(stream), mA, mA32, mW, mSFA, mSFW, P);
+    if (rc) return rc;
+    P.singles = 1;
+    grouped_gemm_kernel<false><<<sms, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32,
+                                                                                    mW, P);
     return check_launch();
+  }
+  if (a->pair_tiles) {
+    static int max_clusters = 0;
+    return launch_pairs(grouped_gemm_kernel<true>, SMEM_BYTES, sms, max_clusters,
+                        as_stream(stream), mA, mA32, mW, P);
   }
   const int64_t max_units = a->tiles2 ? sms : a->max_tiles * (a->n / BN);
   const int grid = (int)(max_units < sms ? max_units : sms);

@@ -251,8 +251,14 @@ typedef struct moe_gemm_args {
   int32_t *signal;
   int block_m_signal;
   int num_sms;
-  int pair_tiles; /* 1: 2-CTA clusters take an expert's M tiles two by two and share
-                     each weight tile (multicast), for experts with several M tiles */
+  int pair_tiles; /* 0: one CTA per M tile.
+                     1: 2-CTA clusters take an expert's M tiles two by two and share
+                        each weight tile (multicast), for experts with several M tiles.
+                     2: an expert's tile pairs run as 2-SM MMAs (M = 256 over the
+                        CTA pair, each SM holding half of the weight tile), then the
+                        single tiles run one per CTA in a second launch; needs
+                        k % 256 == 0 (else MOE_ERR_UNSUPPORTED).  Faster than 1 for
+                        experts with many M tiles and long K, slower for short K. */
   int32_t *status;
 } moe_gemm_args;
 
@@ -328,7 +334,8 @@ typedef struct moe_layer {
   int N_phys, layout, cap, I, has_shared, sbo, block_m_signal;
   int64_t rows, max_tiles, timeout_ns;
   int num_sms, combine_ctas;
-  int gemm_pairs; /* 0: pair_tiles GEMMs when B*K/N_phys >= 128; 1: always; -1: never */
+  int gemm_pairs; /* pair_tiles of both GEMMs.  0: 1 when B*K/N_phys >= 128, else 0;
+                     1: always 1; 2: always 2 (H and I multiples of 256); -1: always 0 */
   /* inputs and weights */
   void *x;                                         /* bf16 [B][H] */
   const float *W_router, *bias;                    /* [N][H], [N] or NULL */

@@ -138,16 +138,15 @@ def test_cluster_pair_gemm_equals_single_cta(dev, op):
     Wa = api.pack_weight_scales(torch.from_numpy(Wsf).to(dev))
     tl = torch.from_numpy(t).to(dev)
     outs = []
-    for pairs in (0, 1):
+    for pairs in (0, 1, 2):
         st = api.new_status(dev)
         o = api.grouped_gemm_fp8(op, A, A_sf, Wd, Wa, tl, mt, status=st, pair_tiles=pairs)
         torch.cuda.synchronize()
         assert api.read_status(st) == 0
         outs.append(o)
-    if op == 1:
-        a, b = outs[0].view(torch.int16), outs[1].view(torch.int16)
-    else:
-        a, b = outs[0][0], outs[1][0]
-    for i0 in range(mt):                      # rows each tile stores
-        nvalid = t[8 + 8 * i0 + 2]
-        assert torch.equal(a[128 * i0: 128 * i0 + nvalid], b[128 * i0: 128 * i0 + nvalid]), i0
+    res = [o.view(torch.int16) if op == 1 else o[0] for o in outs]
+    for b in res[1:]:
+        for i0 in range(mt):                  # rows each tile stores
+            nvalid = t[8 + 8 * i0 + 2]
+            assert torch.equal(res[0][128 * i0: 128 * i0 + nvalid],
+                               b[128 * i0: 128 * i0 + nvalid]), i0

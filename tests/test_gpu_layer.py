@@ -242,14 +242,15 @@ def test_layouts_and_eplb_agree_bitwise(dev):
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
 
 
+@pytest.mark.parametrize("pairs", [1, 2])
 @pytest.mark.parametrize("name", ["small_contig", "small_eplb", "small_sbo"])
-def test_layer_with_cluster_pairs_matches_single_cta(dev, name):
+def test_layer_with_cluster_pairs_matches_single_cta(dev, name, pairs):
     cfg, x, W, bias = host_workload(name)
     ex = host_experts(name)
     idx, _ = oracle.route(x, W, bias, cfg)
     emap = eplb_for(cfg, idx)
     lay = api.MoELayer(cfg, to_dev(W), to_dev(bias), device_weights(ex), eplb_map=emap,
-                       gemm_pairs=1)
+                       gemm_pairs=pairs)
     a = bits(lay.forward(bf16_dev(x)))
     torch.cuda.synchronize()
     assert api.read_status(lay.status) == 0
