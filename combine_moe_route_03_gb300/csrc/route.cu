@@ -4,11 +4,13 @@
 // experts and keeps K; DeepSeek-V3's group-limited gating (same page, §group-limited
 // gating) first keeps the best groups, then the best experts inside them.
 //
-// Two kernels:
+// Kernels:
 //   route_logits_kernel  z = x . W^T in fp32, each logit one fused multiply-add per
 //                        k in order k = 0..H-1 (register-tiled SIMT: the ordering
 //                        rule keeps this off the tensor cores, which round inputs
-//                        and reorder partial sums).
+//                        and reorder partial sums).  Small grids.
+//   route_logits_wide_kernel  the same arithmetic for wide grids: x widened to fp32
+//                        once per CTA, larger per-thread tiles.
 //   route_select_kernel  one warp per token: scores, group scores, top-K with the
 //                        (score desc, index asc) order, weights, expert counts.
 #include <cfloat>
@@ -110,6 +112,121 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_kernel(const uint1
 #pragma unroll
       for (int j = 0; j < TE; ++j) wv[j] = wr[j];
       if (k4 + 4 < kRouteBK) fetch(k4 + 4);
+      // k order is strictly sequential for every output
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+#pragma unroll
+        for (int j = 0; j < TE; ++j) {
+          acc[i][j] = __fmaf_rn(xv[i].x, wv[j].x, acc[i][j]);
+          acc[i][j] = __fmaf_rn(xv[i].y, wv[j].y, acc[i][j]);
+          acc[i][j] = __fmaf_rn(xv[i].z, wv[j].z, acc[i][j]);
+          acc[i][j] = __fmaf_rn(xv[i].w, wv[j].w, acc[i][j]);
+        }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < TT; ++i) {
+    const int t = t0 + wt * 4 * TT + tl + 4 * i;
+    if (t >= B) continue;
+#pragma unroll
+    for (int j = 0; j < TE; ++j) {
+      const int e = e0 + we * 8 * TE + el + 8 * j;
+      if (e < N) logits[(size_t)t * N + e] = acc[i][j];
+    }
+  }
+}
+
+// Wide-grid variant: the same thread and warp tiling and the same k order, but each
+// chunk's x is widened from bf16 to fp32 once, into a buffer the whole CTA reads, so
+// the inner loop is 128-bit shared loads and fused multiply-adds only (every thread
+// that shares a token would otherwise widen the same values again).  Chunk loop of
+// one CTA: wait for chunk c | barrier | widen x(c) | refill the ring slot chunk c-1
+// used | barrier | FMAs of chunk c.  The first barrier also ends every read of the
+// widened buffer by chunk c-1, so one buffer is enough.  Large tiles (up to 8 x 8 per
+// thread) pay off once the grid has CTAs to spare; small grids keep the bf16 kernel.
+template <int TT, int TE, int S, int BK>
+__global__ void __launch_bounds__(kRouteThreads) route_logits_wide_kernel(
+    const uint16_t *__restrict__ x, const float *__restrict__ W, float *__restrict__ logits,
+    int B, int H, int N) {
+  constexpr int BT = 2 * 4 * TT;  // tokens per CTA
+  constexpr int BE = 2 * 8 * TE;  // experts per CTA
+  constexpr int LDH = BK + 8;     // bf16 per staged x row
+  constexpr int LDF = BK + 4;     // fp32 per widened x row and staged W row
+  constexpr int XST = BT * LDH, WST = BE * LDF;
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  float *ws = reinterpret_cast<float *>(route_smem);           // [S][BE][LDF]
+  float *xf = ws + S * WST;                                    // [BT][LDF]
+  uint16_t *xs = reinterpret_cast<uint16_t *>(xf + BT * LDF);  // [S][BT][LDH]
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int tl = lane >> 3, el = lane & 7;
+  const int wt = warp >> 1, we = warp & 1;
+  const int t0 = blockIdx.y * BT, e0 = blockIdx.x * BE;
+  const int nchunks = H / BK;
+
+  auto load = [&](int c, int buf) {
+    const int kc = c * BK;
+    constexpr int XP = BK / 8, WP = BK / 4;  // 16-byte pieces per row
+    for (int i = tid; i < BT * XP; i += kRouteThreads) {
+      const int t = i / XP, k = (i % XP) * 8;
+      const bool ok = t0 + t < B;
+      const uint16_t *src = x + (size_t)(ok ? t0 + t : 0) * H + kc + k;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                       smem_u32(xs + buf * XST + t * LDH + k)),
+                   "l"(src), "r"(ok ? 16 : 0)
+                   : "memory");
+    }
+    for (int i = tid; i < BE * WP; i += kRouteThreads) {
+      const int e = i / WP, k = (i % WP) * 4;
+      const bool ok = e0 + e < N;
+      const float *src = W + (size_t)(ok ? e0 + e : 0) * H + kc + k;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                       smem_u32(ws + buf * WST + e * LDF + k)),
+                   "l"(src), "r"(ok ? 16 : 0)
+                   : "memory");
+    }
+  };
+
+  float acc[TT][TE];
+#pragma unroll
+  for (int i = 0; i < TT; ++i)
+#pragma unroll
+    for (int j = 0; j < TE; ++j) acc[i][j] = 0.0f;
+
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    if (s < nchunks) load(s, s);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int c = 0; c < nchunks; ++c) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");
+    __syncthreads();
+    {  // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 word
+      const uint16_t *xb = xs + (c % S) * XST;
+      for (int i = tid; i < BT * BK / 8; i += kRouteThreads) {
+        const int t = i / (BK / 8), k = (i % (BK / 8)) * 8;
+        const uint4 v = *reinterpret_cast<const uint4 *>(xb + t * LDH + k);
+        float4 *d = reinterpret_cast<float4 *>(xf + t * LDF + k);
+        d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+        d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
+                           __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+      }
+    }
+    if (c + S - 1 < nchunks) load(c + S - 1, (c + S - 1) % S);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    __syncthreads();
+    const float *wb = ws + (c % S) * WST;
+#pragma unroll
+    for (int k4 = 0; k4 < BK; k4 += 4) {
+      float4 xv[TT], wv[TE];
+#pragma unroll
+      for (int i = 0; i < TT; ++i)
+        xv[i] = *reinterpret_cast<const float4 *>(xf + (wt * 4 * TT + tl + 4 * i) * LDF + k4);
+#pragma unroll
+      for (int j = 0; j < TE; ++j)
+        wv[j] = *reinterpret_cast<const float4 *>(wb + (we * 8 * TE + el + 8 * j) * LDF + k4);
       // k order is strictly sequential for every output
 #pragma unroll
       for (int i = 0; i < TT; ++i)
@@ -426,6 +543,24 @@ int launch_logits(const uint16_t *x, const float *W, float *lg, int B, int H, in
   return check_launch();
 }
 
+template <int TT, int TE, int S, int BK>
+int launch_logits_wide(const uint16_t *x, const float *W, float *lg, int B, int H, int N,
+                       cudaStream_t st) {
+  constexpr int BT = 8 * TT, BE = 16 * TE;
+  constexpr size_t smem =
+      (size_t)S * (BT * (BK + 8) * 2 + BE * (BK + 4) * 4) + (size_t)BT * (BK + 4) * 4;
+  static bool attr = false;
+  if (!attr && smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(route_logits_wide_kernel<TT, TE, S, BK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  attr = true;
+  dim3 grid((N + BE - 1) / BE, (B + BT - 1) / BT);
+  route_logits_wide_kernel<TT, TE, S, BK><<<grid, kRouteThreads, smem, st>>>(x, W, lg, B, H, N);
+  return check_launch();
+}
+
 int route_check(const moe_route_cfg *c) {
   if (!c) return MOE_ERR_INVALID;
   if (c->B < 0 || c->H <= 0 || c->N <= 0 || c->K <= 0) return MOE_ERR_INVALID;
@@ -474,7 +609,15 @@ extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W
     return (long)((N + 16 * te - 1) / (16 * te)) * ((B + 8 * tt - 1) / (8 * tt));
   };
   const uint16_t *xb = static_cast<const uint16_t *>(x);
-  if (ctas(4, 4) >= 4 * sms)
+  // Wide grids: fp32-widened x and the largest per-thread tile that still leaves
+  // every SM one and a half CTAs; small grids: the bf16 kernel below.
+  if (2 * ctas(8, 8) >= 3 * sms)
+    rc = launch_logits_wide<8, 8, 3, 32>(xb, W, lg, B, H, N, st);
+  else if (2 * ctas(4, 8) >= 3 * sms)
+    rc = launch_logits_wide<4, 8, 3, 32>(xb, W, lg, B, H, N, st);
+  else if (B >= 256 && H % 64 == 0)
+    rc = launch_logits_wide<2, 2, 4, 64>(xb, W, lg, B, H, N, st);
+  else if (ctas(4, 4) >= 4 * sms)
     rc = launch_logits<4, 4, 4, 32>(xb, W, lg, B, H, N, st);
   else if (ctas(2, 2) >= 4 * sms && H % 64 == 0)
     rc = launch_logits<2, 2, 4, 64>(xb, W, lg, B, H, N, st);
