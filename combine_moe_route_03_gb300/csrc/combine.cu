@@ -22,6 +22,7 @@ constexpr int kCombineWarps = 4;  // small CTAs: an SBO consumer fits beside a G
 // One warp owns a task = (token, run of `cpt` consecutive 256-column chunks), so a
 // small batch still spreads over many warps and every lane keeps K independent
 // 16-byte loads in flight.
+template <int KM>  // K <= KM
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     const uint16_t *__restrict__ Y, const int32_t *__restrict__ row_of,
     const float *__restrict__ topk_w, const uint16_t *__restrict__ S, uint16_t *__restrict__ out,
@@ -63,10 +64,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     }
     __syncwarp();
     const bool use_s = S && (K >= 32 || __shfl_sync(0xffffffffu, my_r, K) >= 0);
-    int r[16];
-    float w[16];
+    int r[KM];
+    float w[KM];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < KM; ++k) {
       r[k] = __shfl_sync(0xffffffffu, my_r, k);
       w[k] = __shfl_sync(0xffffffffu, my_w, k);
     }
@@ -76,10 +77,19 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      // all K loads of the chunk first, then the sum in rank order
+      uint4 y[KM];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < KM; ++k)
+        y[k] = (k < K && r[k] >= 0)
+                   ? __ldcg(reinterpret_cast<const uint4 *>(Y + (size_t)r[k] * H + h))
+                   : make_uint4(0, 0, 0, 0);
+      uint4 sv = make_uint4(0, 0, 0, 0);
+      if (use_s) sv = __ldcs(reinterpret_cast<const uint4 *>(S + (size_t)t * H + h));
+#pragma unroll
+      for (int k = 0; k < KM; ++k) {
         if (k >= K || r[k] < 0) continue;
-        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(Y + (size_t)r[k] * H + h));
+        const uint4 v = y[k];
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -88,7 +98,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
         }
       }
       if (use_s) {
-        const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(S + (size_t)t * H + h));
+        const uint4 v = sv;
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -129,9 +139,14 @@ extern "C" int moe_combine(const moe_combine_cfg *c, const void *Y, const int32_
   const long tasks = (long)c->B * ((nch + cpt - 1) / cpt);
   long grid = (tasks + kCombineWarps - 1) / kCombineWarps;
   if (c->num_ctas > 0 && c->num_ctas < grid) grid = c->num_ctas;
-  combine_kernel<<<(unsigned)grid, kCombineWarps * 32, 0, as_stream(stream)>>>(
-      static_cast<const uint16_t *>(Y), row_of, topk_w, static_cast<const uint16_t *>(shared),
-      static_cast<uint16_t *>(out), c->B, c->H, c->K, (int)cpt, c->signal, c->threshold,
-      c->block_m_signal > 0 ? c->block_m_signal : 1, c->timeout_ns, c->shared_row0, status);
+#define MOE_COMBINE_ARGS                                                                   \
+  static_cast<const uint16_t *>(Y), row_of, topk_w, static_cast<const uint16_t *>(shared),   \
+      static_cast<uint16_t *>(out), c->B, c->H, c->K, (int)cpt, c->signal, c->threshold,     \
+      c->block_m_signal > 0 ? c->block_m_signal : 1, c->timeout_ns, c->shared_row0, status
+  if (c->K <= 8)
+    combine_kernel<8><<<(unsigned)grid, kCombineWarps * 32, 0, as_stream(stream)>>>(MOE_COMBINE_ARGS);
+  else
+    combine_kernel<16><<<(unsigned)grid, kCombineWarps * 32, 0, as_stream(stream)>>>(MOE_COMBINE_ARGS);
+#undef MOE_COMBINE_ARGS
   return check_launch();
 }

@@ -18,6 +18,7 @@
 //   dispatch_scatter_kernel warps over (token, column chunk): quantise each piece of
 //                           a row once, write its K copies and their scales,
 //                           row_of / src_of.
+#include <climits>
 #include <mutex>
 
 #include "common.cuh"
@@ -121,19 +122,37 @@ __global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
 }
 
 // Inclusive block-wide scan (Hillis-Steele) of one value per thread.
-__device__ __forceinline__ int block_scan(int32_t *buf, int v) {
-  const int p = threadIdx.x;
-  buf[p] = v;
-  __syncthreads();
-  for (int off = 1; off < kScanThreads; off <<= 1) {
-    const int o = p >= off ? buf[p - off] : 0;
-    __syncthreads();
-    buf[p] += o;
-    __syncthreads();
+// Scan over the CTA's kScanThreads threads (op: sum, or max when kMax): shuffles
+// inside each warp, then one warp scans the warp totals.  Returns the inclusive
+// scan; *excl (if given) gets the exclusive one (identity: 0, or -1 for max of
+// non-negative values).  `buf` holds one int per warp.
+template <bool kMax = false>
+__device__ __forceinline__ int block_scan(int32_t *buf, int v, int *excl = nullptr) {
+  const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
+  const int id = kMax ? -1 : 0;
+  auto op = [](int a, int b) { return kMax ? max(a, b) : a + b; };
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v = op(v, o);
   }
-  const int r = buf[p];
+  const int e = __shfl_up_sync(0xffffffffu, v, 1);
+  if (lane == 31) buf[warp] = v;
   __syncthreads();
-  return r;
+  if (warp == 0) {
+    int w = lane < kScanThreads / 32 ? buf[lane] : id;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w = op(w, o);
+    }
+    if (lane < kScanThreads / 32) buf[lane] = w;
+  }
+  __syncthreads();
+  const int prefix = warp > 0 ? buf[warp - 1] : id;
+  if (excl) *excl = lane > 0 ? op(e, prefix) : prefix;
+  __syncthreads();  // buf is reused by the next scan
+  return op(v, prefix);
 }
 
 // Work items for the cluster-mode GEMM, in schedule order: an expert's tile pairs
@@ -171,16 +190,25 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     int B, int N_phys, int nchunks, int layout, int cap, int64_t rows_alloc, DispatchWs ws,
     int32_t *__restrict__ counts, int32_t *__restrict__ tiles, int32_t *__restrict__ src_of,
     int32_t *__restrict__ shared_tiles, int32_t *status) {
-  __shared__ int32_t scan[kScanThreads];
+  __shared__ int32_t scan[kScanThreads / 32];
   __shared__ int32_t single_tile[kScanThreads];
+  __shared__ int32_t pad_seg[kScanThreads], pad_from[kScanThreads], pad_to[kScanThreads];
   __shared__ int32_t totals[4];  // tiles, pairs, singles, items
   const int p = threadIdx.x;
   int cnt = 0, valid = 0, nt = 0;
   if (p < N_phys) {
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = ws.hist[(size_t)c * N_phys + p];
-      ws.hist[(size_t)c * N_phys + p] = cnt;
-      cnt += v;
+    // exclusive prefix over the chunks, 16 loads in flight before their stores
+    constexpr int kBatch = 16;
+    for (int c0 = 0; c0 < nchunks; c0 += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        v[i] = c0 + i < nchunks ? ws.hist[(size_t)(c0 + i) * N_phys + p] : 0;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (c0 + i < nchunks) ws.hist[(size_t)(c0 + i) * N_phys + p] = cnt;
+        cnt += v[i];
+      }
     }
     counts[p] = cnt;
     valid = cnt;
@@ -206,14 +234,11 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
   const int n_items = np + (emit ? 1 : 0);
   const int item_first = block_scan(scan, n_items) - n_items;
   if (p == kScanThreads - 1) totals[3] = item_first + n_items;
-  // the earlier single of a couple belongs to the previous expert with a single
-  int prev_single = -1;
-  if (emit && (sfirst & 1))
-    for (int q = p - 1; q >= 0; --q)
-      if (single_tile[q] >= 0) {
-        prev_single = single_tile[q];
-        break;
-      }
+  // the earlier single of a couple belongs to the previous expert with a single:
+  // the largest q < p with one (exclusive max-scan of such indices)
+  int before = -1;
+  block_scan<true>(scan, ns ? p : -1, &before);
+  const int prev_single = (emit && (sfirst & 1) && before >= 0) ? single_tile[before] : -1;
   __syncthreads();
   const int64_t max_tiles = rows_alloc / 128;
   if (p < N_phys) {
@@ -229,10 +254,15 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
       tl[5] = tl[6] = tl[7] = 0;
     }
     write_items(tiles + 8 + 8 * max_tiles, first, nt, item_first, sfirst, prev_single, emit);
-    if (src_of) {  // rows of this expert that no token fills
-      const int end = layout == MOE_LAYOUT_CONTIG ? nt * 128 : cap;
-      for (int j = valid; j < end; ++j) src_of[seg + j] = -1;
-    }
+    pad_seg[p] = seg;  // rows [valid, end) of this expert's segment that no token fills
+    pad_from[p] = valid;
+    pad_to[p] = layout == MOE_LAYOUT_CONTIG ? nt * 128 : cap;
+  }
+  __syncthreads();
+  if (src_of) {  // one warp per expert, coalesced
+    const int lane = p & 31;
+    for (int e = p >> 5; e < N_phys; e += kScanThreads / 32)
+      for (int j = pad_from[e] + lane; j < pad_to[e]; j += 32) src_of[pad_seg[e] + j] = -1;
   }
   const int total_tiles = totals[0];
   const int64_t used = layout == MOE_LAYOUT_CONTIG ? (int64_t)total_tiles * 128
@@ -256,7 +286,18 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
       shared_tiles[3] = snt % 2;
       shared_tiles[4] = snt / 2 + snt % 2;
       for (int i = 5; i < 8; ++i) shared_tiles[i] = 0;
-      write_items(shared_tiles + 8 + 8 * (size_t)snt, 0, snt, 0, 0, -1, snt % 2);
+    }
+    // items: snt / 2 pairs of one group, then the odd last tile alone
+    const int snp = snt / 2;
+    for (int j = p; j < snp + snt % 2; j += kScanThreads) {
+      int32_t *it = shared_tiles + 8 + 8 * (size_t)snt + 8 * (size_t)j;
+      const bool pair = j < snp;
+      it[0] = 2 * j;
+      it[1] = pair ? 2 * j + 1 : -1;
+      it[2] = pair ? 0 : j;
+      it[3] = pair ? snp : 1;
+      it[4] = pair ? 1 : 0;
+      it[5] = it[6] = it[7] = 0;
     }
     for (int i = p; i < snt; i += kScanThreads) {
       int32_t *tl = shared_tiles + 8 + 8 * (size_t)i;
@@ -276,17 +317,21 @@ __device__ __forceinline__ size_t sf_atom_offset(int64_t r, int kb, int Kb) {
   return ((size_t)(r >> 7) * Kb + kb) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5);
 }
 
-// One warp per task = (token, run of `cpt` 256-column chunks): each lane quantises
-// 8 values, 16 lanes share one 128-column block's amax.  The task holding a token's
-// first chunk also writes row_of / src_of.
-template <bool kFp8>
+// One warp per task = (token, run of `cpt` chunks of kCols columns): each lane
+// quantises kCols/32 values (8 or 16), 128/(kCols/32) lanes share one 128-column
+// block's amax, and each lane stores 8 or 16 bytes into each of the K copies.  The
+// task holding a token's first chunk also writes row_of / src_of.
+template <bool kFp8, int kCols>
 __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
     const uint16_t *__restrict__ x, int B, int H, int K, int N_phys, int layout, int cap,
     int cpt, DispatchWs ws, uint8_t *__restrict__ A, uint8_t *__restrict__ A_sf,
     int32_t *__restrict__ row_of, int32_t *__restrict__ src_of, uint8_t *__restrict__ As,
     uint8_t *__restrict__ As_sf) {
+  static_assert(kCols == 256 || (kFp8 && kCols == 512), "chunk width");
+  constexpr int kPer = kCols / 32;    // columns per lane
+  constexpr int kBlk = 128 / kPer;    // lanes per 128-column scale block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nch = (H + 255) / 256;
+  const int nch = (H + kCols - 1) / kCols;
   const int tpt = (nch + cpt - 1) / cpt;
   const long ntasks = (long)B * tpt;
   const long task = (long)blockIdx.x * kScatterWarps + warp;
@@ -316,64 +361,102 @@ __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
   const uint16_t *xr = x + (size_t)t * H;
   const int Hb = H / 128;
   for (int c = c0; c < c1; ++c) {
-    const int h = c * 256 + 8 * lane;
+    const int h = c * kCols + kPer * lane;
     const bool act = h < H;
-    const uint4 v = act ? __ldg(reinterpret_cast<const uint4 *>(xr + h)) : make_uint4(0, 0, 0, 0);
-    if (!kFp8) {
+    uint4 v[kPer / 8];
+#pragma unroll
+    for (int i = 0; i < kPer / 8; ++i)
+      v[i] = act ? __ldg(reinterpret_cast<const uint4 *>(xr + h + 8 * i)) : make_uint4(0, 0, 0, 0);
+    if constexpr (!kFp8) {
       if (act) {
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           if (k < K && rows[k] >= 0)
-            *reinterpret_cast<uint4 *>(A + ((size_t)rows[k] * H + h) * 2) = v;
+            *reinterpret_cast<uint4 *>(A + ((size_t)rows[k] * H + h) * 2) = v[0];
       }
       continue;
-    }
-    float f[8];
-    f[0] = __uint_as_float(v.x << 16);
-    f[1] = __uint_as_float(v.x & 0xffff0000u);
-    f[2] = __uint_as_float(v.y << 16);
-    f[3] = __uint_as_float(v.y & 0xffff0000u);
-    f[4] = __uint_as_float(v.z << 16);
-    f[5] = __uint_as_float(v.z & 0xffff0000u);
-    f[6] = __uint_as_float(v.w << 16);
-    f[7] = __uint_as_float(v.w & 0xffff0000u);
-    float amax = 0.0f;
+    } else {
+      float f[kPer];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      for (int i = 0; i < kPer / 8; ++i) {
+        const uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1)  // the 16 lanes of one 128-column block
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const int e = ue8m0_exp(amax);
-    const float inv = pow2i(-e);
-    uint2 q;
-    q.x = e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
-          (e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
-    q.y = e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
-          (e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
-    const uint32_t sfw = (uint32_t)(e + 127) * 0x01010101u;
-    const int kb = h >> 7;
-    if (act) {
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if (k >= K || rows[k] < 0) continue;
-        *reinterpret_cast<uint2 *>(A + (size_t)rows[k] * H + h) = q;
-        if ((lane & 15) == 0)
-          *reinterpret_cast<uint32_t *>(A_sf + sf_atom_offset(rows[k], kb, Hb)) = sfw;
+        for (int j = 0; j < 4; ++j) {
+          f[8 * i + 2 * j] = __uint_as_float(u[j] << 16);
+          f[8 * i + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
+        }
       }
-      if (As) {
-        *reinterpret_cast<uint2 *>(As + (size_t)t * H + h) = q;
-        if ((lane & 15) == 0)
-          *reinterpret_cast<uint32_t *>(As_sf + sf_atom_offset(t, kb, Hb)) = sfw;
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+      for (int off = kBlk / 2; off > 0; off >>= 1)  // the lanes of one 128-column block
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const int e = ue8m0_exp(amax);
+      const float inv = pow2i(-e);
+      uint32_t q[kPer / 4];
+#pragma unroll
+      for (int i = 0; i < kPer / 4; ++i)
+        q[i] = e4m3x2(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv)) |
+               (e4m3x2(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv)) << 16);
+      const uint32_t sfw = (uint32_t)(e + 127) * 0x01010101u;
+      const int kb = h >> 7;
+      auto put = [&](uint8_t *dst) {
+        if constexpr (kPer == 8)
+          *reinterpret_cast<uint2 *>(dst) = make_uint2(q[0], q[1]);
+        else
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
+      };
+      if (act) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          if (k >= K || rows[k] < 0) continue;
+          put(A + (size_t)rows[k] * H + h);
+          if ((lane & (kBlk - 1)) == 0)
+            *reinterpret_cast<uint32_t *>(A_sf + sf_atom_offset(rows[k], kb, Hb)) = sfw;
+        }
+        if (As) {
+          put(As + (size_t)t * H + h);
+          if ((lane & (kBlk - 1)) == 0)
+            *reinterpret_cast<uint32_t *>(As_sf + sf_atom_offset(t, kb, Hb)) = sfw;
+        }
       }
     }
   }
 }
 
 // Chunks per scatter task: enough warps for the whole GPU, at most a full row.
-inline int scatter_cpt(int B, int H) {
-  const long nch = (H + 255) / 256;
+inline int scatter_cpt(int B, int H, int cols) {
+  const long nch = (H + cols - 1) / cols;
   long cpt = ((long)B * nch) / ((long)device_sm_count() * 128);
   return (int)(cpt < 1 ? 1 : (cpt > nch ? nch : cpt));
+}
+
+// The scatter launch of both dispatch entry points: fp8 rows in 512-column chunks
+// (16-byte stores per lane and copy) when H allows, else 256.
+int launch_scatter(const moe_dispatch_cfg *c, int B, int K, int Np, const void *x,
+                   const DispatchWs &ws, void *A, void *A_sf, int32_t *row_of, int32_t *src_of,
+                   void *As, void *As_sf, cudaStream_t st) {
+  const uint16_t *xb = static_cast<const uint16_t *>(x);
+  const bool fp8 = c->fmt == MOE_FMT_FP8;
+  const int cols = fp8 && c->H % 512 == 0 ? 512 : 256;
+  const int cpt = scatter_cpt(B, c->H, cols);
+  const long tasks = (long)B * (((c->H + cols - 1) / cols + cpt - 1) / cpt);
+  const unsigned grid = (unsigned)((tasks + kScatterWarps - 1) / kScatterWarps);
+  uint8_t *a = static_cast<uint8_t *>(A);
+  if (!fp8)
+    dispatch_scatter_kernel<false, 256><<<grid, kScatterWarps * 32, 0, st>>>(
+        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, a, nullptr, row_of, src_of, nullptr,
+        nullptr);
+  else if (cols == 512)
+    dispatch_scatter_kernel<true, 512><<<grid, kScatterWarps * 32, 0, st>>>(
+        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, a, static_cast<uint8_t *>(A_sf), row_of,
+        src_of, static_cast<uint8_t *>(As), static_cast<uint8_t *>(As_sf));
+  else
+    dispatch_scatter_kernel<true, 256><<<grid, kScatterWarps * 32, 0, st>>>(
+        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, a, static_cast<uint8_t *>(A_sf), row_of,
+        src_of, static_cast<uint8_t *>(As), static_cast<uint8_t *>(As_sf));
+  return check_launch();
 }
 
 }  // namespace
@@ -451,20 +534,7 @@ extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int3
                                                    moe_dispatch_rows(c), ws, counts, tiles,
                                                    src_of, shared_tiles, status);
   if ((rc = check_launch())) return rc;
-  const int cpt = scatter_cpt(B, c->H);
-  const long tasks = (long)B * (((c->H + 255) / 256 + cpt - 1) / cpt);
-  const unsigned grid = (unsigned)((tasks + kScatterWarps - 1) / kScatterWarps);
-  const uint16_t *xb = static_cast<const uint16_t *>(x);
-  if (c->fmt == MOE_FMT_FP8)
-    dispatch_scatter_kernel<true><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, static_cast<uint8_t *>(A),
-        static_cast<uint8_t *>(A_sf), row_of, src_of, static_cast<uint8_t *>(A_shared),
-        static_cast<uint8_t *>(A_shared_sf));
-  else
-    dispatch_scatter_kernel<false><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, static_cast<uint8_t *>(A), nullptr,
-        row_of, src_of, nullptr, nullptr);
-  return check_launch();
+  return launch_scatter(c, B, K, Np, x, ws, A, A_sf, row_of, src_of, A_shared, A_shared_sf, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -543,18 +613,5 @@ extern "C" int moe_dispatch_noalloc(const moe_dispatch_cfg *c, const void *x,
                                                    moe_dispatch_rows(c), ws, counts, tiles,
                                                    src_of, shared_tiles, status);
   if ((rc = check_launch())) return rc;
-  const int cpt = scatter_cpt(B, c->H);
-  const long tasks = (long)B * (((c->H + 255) / 256 + cpt - 1) / cpt);
-  const unsigned grid = (unsigned)((tasks + kScatterWarps - 1) / kScatterWarps);
-  const uint16_t *xb = static_cast<const uint16_t *>(x);
-  if (c->fmt == MOE_FMT_FP8)
-    dispatch_scatter_kernel<true><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, static_cast<uint8_t *>(A),
-        static_cast<uint8_t *>(A_sf), row_of, src_of, static_cast<uint8_t *>(A_shared),
-        static_cast<uint8_t *>(A_shared_sf));
-  else
-    dispatch_scatter_kernel<false><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, static_cast<uint8_t *>(A), nullptr,
-        row_of, src_of, nullptr, nullptr);
-  return check_launch();
+  return launch_scatter(c, B, K, Np, x, ws, A, A_sf, row_of, src_of, A_shared, A_shared_sf, st);
 }
