@@ -11,6 +11,8 @@
 //                        and reorder partial sums).  Small grids.
 //   route_logits_wide_kernel  the same arithmetic for wide grids: x widened to fp32
 //                        once per CTA, larger per-thread tiles.
+//   route_logits_slice_kernel  256 experts, large batches: a warp owns a slice of
+//                        tokens against all experts, one CTA per SM.
 //   route_select_kernel  one warp per token: scores, group scores, top-K with the
 //                        (score desc, index asc) order, weights, expert counts.
 #include <cfloat>
@@ -248,6 +250,108 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_wide_kernel(
       const int e = e0 + we * 8 * TE + el + 8 * j;
       if (e < N) logits[(size_t)t * N + e] = acc[i][j];
     }
+  }
+}
+
+// Token-sliced variant for wide batches: one CTA of NW warps per SM, and each warp owns
+// TT consecutive tokens (TT = B / (NW * SMs), rounded up) against all 32 * TE experts:
+// lane l takes experts l, l + 32, ...  Per 4-deep k step a lane loads its TE rows of W
+// (distinct addresses) and each token row of fp32-widened x as a warp-wide broadcast
+// (half the shared-memory cost of a distinct load), then does 4 * TT * TE fused
+// multiply-adds; the token slicing keeps every SM equally loaded (a fixed 2-D tiling of
+// 2^21 logits over 152 SMs leaves a sixth of them idle).  Same sequential k order per
+// logit.
+template <int TT, int TE, int S, int BK, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) route_logits_slice_kernel(
+    const uint16_t *__restrict__ x, const float *__restrict__ W, float *__restrict__ logits,
+    int B, int H) {
+  constexpr int BT = NW * TT, NE = 32 * TE, NT = NW * 32;
+  constexpr int LDH = BK + 8, LDF = BK + 4;
+  constexpr int XST = BT * LDH, WST = NE * LDF;
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  float *ws = reinterpret_cast<float *>(route_smem);           // [S][NE][LDF]
+  float *xf = ws + S * WST;                                    // [BT][LDF]
+  uint16_t *xs = reinterpret_cast<uint16_t *>(xf + BT * LDF);  // [S][BT][LDH]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * BT;
+  const int nchunks = H / BK;
+
+  auto load = [&](int c, int buf) {
+    const int kc = c * BK;
+    constexpr int XP = BK / 8, WP = BK / 4;
+    for (int i = tid; i < BT * XP; i += NT) {
+      const int t = i / XP, k = (i % XP) * 8;
+      const bool ok = t0 + t < B;
+      const uint16_t *src = x + (size_t)(ok ? t0 + t : 0) * H + kc + k;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                       smem_u32(xs + buf * XST + t * LDH + k)),
+                   "l"(src), "r"(ok ? 16 : 0)
+                   : "memory");
+    }
+    for (int i = tid; i < NE * WP; i += NT) {
+      const int e = i / WP, k = (i % WP) * 4;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                       smem_u32(ws + buf * WST + e * LDF + k)),
+                   "l"(W + (size_t)e * H + kc + k)
+                   : "memory");
+    }
+  };
+
+  float acc[TT][TE];
+#pragma unroll
+  for (int i = 0; i < TT; ++i)
+#pragma unroll
+    for (int j = 0; j < TE; ++j) acc[i][j] = 0.0f;
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    if (s < nchunks) load(s, s);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int c = 0; c < nchunks; ++c) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");
+    __syncthreads();
+    {  // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 word
+      const uint16_t *xb = xs + (c % S) * XST;
+      for (int i = tid; i < BT * BK / 8; i += NT) {
+        const int t = i / (BK / 8), k = (i % (BK / 8)) * 8;
+        const uint4 v = *reinterpret_cast<const uint4 *>(xb + t * LDH + k);
+        float4 *d = reinterpret_cast<float4 *>(xf + t * LDF + k);
+        d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+        d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
+                           __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+      }
+    }
+    if (c + S - 1 < nchunks) load(c + S - 1, (c + S - 1) % S);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    __syncthreads();
+    const float *wb = ws + (c % S) * WST + lane * LDF;
+    const float *xw = xf + warp * TT * LDF;
+#pragma unroll 2
+    for (int k4 = 0; k4 < BK; k4 += 4) {
+      float4 wv[TE];
+#pragma unroll
+      for (int j = 0; j < TE; ++j) wv[j] = *reinterpret_cast<const float4 *>(wb + 32 * j * LDF + k4);
+#pragma unroll
+      for (int i = 0; i < TT; ++i) {
+        const float4 xv = *reinterpret_cast<const float4 *>(xw + i * LDF + k4);  // broadcast
+        // k order is strictly sequential for every output
+#pragma unroll
+        for (int j = 0; j < TE; ++j) {
+          acc[i][j] = __fmaf_rn(xv.x, wv[j].x, acc[i][j]);
+          acc[i][j] = __fmaf_rn(xv.y, wv[j].y, acc[i][j]);
+          acc[i][j] = __fmaf_rn(xv.z, wv[j].z, acc[i][j]);
+          acc[i][j] = __fmaf_rn(xv.w, wv[j].w, acc[i][j]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < TT; ++i) {
+    const int t = t0 + warp * TT + i;
+    if (t >= B) continue;
+#pragma unroll
+    for (int j = 0; j < TE; ++j) logits[(size_t)t * NE + 32 * j + lane] = acc[i][j];
   }
 }
 
@@ -561,6 +665,24 @@ int launch_logits_wide(const uint16_t *x, const float *W, float *lg, int B, int 
   return check_launch();
 }
 
+template <int TT, int TE, int S, int BK, int NW>
+int launch_logits_slice(const uint16_t *x, const float *W, float *lg, int B, int H,
+                        cudaStream_t st) {
+  constexpr int BT = NW * TT;
+  constexpr size_t smem = (size_t)S * (BT * (BK + 8) * 2 + 32 * TE * (BK + 4) * 4) +
+                          (size_t)BT * (BK + 4) * 4;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(route_logits_slice_kernel<TT, TE, S, BK, NW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  attr = true;
+  route_logits_slice_kernel<TT, TE, S, BK, NW><<<(B + BT - 1) / BT, NW * 32, smem, st>>>(x, W, lg,
+                                                                                    B, H);
+  return check_launch();
+}
+
 int route_check(const moe_route_cfg *c) {
   if (!c) return MOE_ERR_INVALID;
   if (c->B < 0 || c->H <= 0 || c->N <= 0 || c->K <= 0) return MOE_ERR_INVALID;
@@ -609,9 +731,17 @@ extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W
     return (long)((N + 16 * te - 1) / (16 * te)) * ((B + 8 * tt - 1) / (8 * tt));
   };
   const uint16_t *xb = static_cast<const uint16_t *>(x);
-  // Wide grids: fp32-widened x and the largest per-thread tile that still leaves
+  // 256 experts and 6-8 tokens per warp at 8 warps per SM: the token-sliced kernel.
+  // Other wide grids: fp32-widened x and the largest per-thread tile that still leaves
   // every SM one and a half CTAs; small grids: the bf16 kernel below.
-  if (2 * ctas(8, 8) >= 3 * sms)
+  const long tt8 = (B + 8 * sms - 1) / (8 * sms);
+  if (N == 256 && tt8 == 6)
+    rc = launch_logits_slice<6, 8, 3, 32, 8>(xb, W, lg, B, H, st);
+  else if (N == 256 && tt8 == 7)
+    rc = launch_logits_slice<7, 8, 3, 32, 8>(xb, W, lg, B, H, st);
+  else if (N == 256 && tt8 == 8)
+    rc = launch_logits_slice<8, 8, 3, 32, 8>(xb, W, lg, B, H, st);
+  else if (2 * ctas(8, 8) >= 3 * sms)
     rc = launch_logits_wide<8, 8, 3, 32>(xb, W, lg, B, H, N, st);
   else if (2 * ctas(4, 8) >= 3 * sms)
     rc = launch_logits_wide<4, 8, 3, 32>(xb, W, lg, B, H, N, st);

@@ -48,10 +48,16 @@ def test_route_bit_exact_other_group_shapes(dev, N, G, TG, K):
     assert np.array_equal(r["topk_w"].cpu().numpy().view(np.uint32), w.view(np.uint32))
 
 
-@pytest.mark.parametrize("name", ["prefill", "skew"])
-def test_route_full_size_sampled(dev, name):
-    """Full B: routing of a sample of tokens bit-exact, counts consistent at any size."""
+@pytest.mark.parametrize("name,B", [("prefill", 0), ("skew", 0), ("prefill", 6100),
+                                    ("prefill", 9700)])
+def test_route_full_size_sampled(dev, name, B):
+    """Full B: routing of a sample of tokens bit-exact, counts consistent at any size.
+    The prefill batch sizes 6100 and 9700 take the token-sliced logits kernel with
+    6 and 8 tokens per warp (8192 takes 7), with ragged last slices."""
     cfg, x, W, bias = host_workload(name)
+    if B:
+        cfg = cfg.with_(B=B)
+        x = inputs.make_x(cfg)
     r = api.route(cfg, bf16_dev(x), to_dev(W), to_dev(bias))
     torch.cuda.synchronize()
     gi = r["topk_idx"].cpu().numpy()
