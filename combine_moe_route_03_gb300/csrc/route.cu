@@ -514,15 +514,15 @@ __device__ __forceinline__ void merge_top2(Cand &a1, Cand &a2, const Cand &b1, c
 // Selection with contiguous ownership: lane l holds experts [l*NPL, (l+1)*NPL).
 // When a group's experts fill whole lanes (group size a multiple of NPL, a power
 // of two of lanes per group), a group's top two are a scan of the lane's own
-// values plus log2(lanes per group) butterfly merges, and each top-K round is a
-// scan of NPL values plus one warp argmax.  Same results as route_select_kernel.
+// values plus log2(lanes per group) butterfly merges, the kept groups follow from
+// each group's rank, and each top-K round is a scan of NPL values plus two warp
+// reductions (redux).  Same results as route_select_kernel.
 template <int NPL>
 __global__ void __launch_bounds__(kSelWarps * 32) route_select_lanes_kernel(
     const float *__restrict__ logits, const float *__restrict__ bias, int B, int N, int K,
     int n_group, int topk_group, int score_fn, int renorm, float route_scale,
     int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int32_t *__restrict__ counts) {
   __shared__ float sd[kSelWarps][kMaxNI * 32];
-  __shared__ float sg[kSelWarps][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x * kSelWarps + warp;
   if (t >= B) return;
@@ -586,37 +586,54 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_lanes_kernel(
       o1.s = o2.s = 0.0f;
       merge_top2(b1, b2, o1, o2);
     }
-    if (lane % L == 0 && lane / L < n_group) sg[warp][lane / L] = __fadd_rn(b1.v, b2.v);
-    __syncwarp();
-    uint32_t keep = 0;
-    for (int r = 0; r < topk_group; ++r) {
-      int best = -1;
-      for (int j = 0; j < n_group; ++j) {
-        if (keep >> j & 1) continue;
-        if (best < 0 || sg[warp][j] > sg[warp][best]) best = j;  // ties keep the lower j
-      }
-      keep |= 1u << best;
+    // Every lane of a group holds its score now.  A group is kept when fewer than
+    // topk_group groups rank before it (higher score; equal scores: lower index).
+    const float gsc = __fadd_rn(b1.v, b2.v);
+    const int gme = lane / L;
+    int ahead = 0;
+    for (int j = 0; j < n_group; ++j) {
+      const float o = __shfl_sync(0xffffffffu, gsc, j * L);
+      ahead += (o > gsc || (o == gsc && j < gme)) ? 1 : 0;
     }
-    const bool mine = base < N && ((keep >> (base / gs)) & 1);
+    const bool mine = base < N && gme < n_group && ahead < topk_group;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) elig[i] = elig[i] && mine;
+  }
+  // Top-K rounds as warp reductions on an order-preserving key of the score (+0 for
+  // -0, so equal scores tie), ties to the smallest expert index; 0 = not a candidate.
+  uint32_t key[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const uint32_t u = __float_as_uint(__fadd_rn(c[i], 0.0f));
+    key[i] = elig[i] ? (u & 0x80000000u ? ~u : u | 0x80000000u) : 0u;
   }
   int my_idx = -1;
   float my_s = 0.0f;
   for (int r = 0; r < K; ++r) {
-    Cand b{0.0f, INT_MAX, 0.0f};
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const Cand x{c[i], base + i, s[i]};
-      if (elig[i] && before(x, b)) b = x;
-    }
-    b = warp_best(b);
+    uint32_t kb = 0;
+    int ib = 0;
 #pragma unroll
     for (int i = 0; i < NPL; ++i)
-      if (base + i == b.i) elig[i] = false;
+      if (key[i] > kb) {  // strict: the lower index keeps a tie
+        kb = key[i];
+        ib = i;
+      }
+    const uint32_t km = __reduce_max_sync(0xffffffffu, kb);
+    const uint32_t win =
+        __reduce_min_sync(0xffffffffu, (km != 0 && kb == km) ? (uint32_t)(base + ib) : 0xffffffffu);
+    float sb = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (i == ib) sb = s[i];
+    const int owner = win == 0xffffffffu ? 0 : (int)win / NPL;
+    const float sw = __shfl_sync(0xffffffffu, sb, owner);
+    if (lane == owner && win != 0xffffffffu)
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (i == ib) key[i] = 0u;
     if (lane == r) {
-      my_idx = b.i == INT_MAX ? -1 : b.i;
-      my_s = b.s;
+      my_idx = win == 0xffffffffu ? -1 : (int)win;
+      my_s = win == 0xffffffffu ? 0.0f : sw;
     }
   }
   float sum = 0.0f;
