@@ -5,8 +5,11 @@
 
 One step = one pass of the whole layer (moe_layer_forward: route, dispatch, shared
 expert, gate/up + SwiGLU, down, combine) over one batch of seeded synthetic input,
-inputs resident in HBM.  Prints one JSON line (rank 0).  Under torchrun each rank
-runs its own independent batch (weak scaling, no collective on the data path).
+inputs resident in HBM; the K timed steps run as one CUDA graph of K passes, each
+recording its stage events.  `e2e` replays the library's host-buffer graph (x copied
+in, the layer, out copied back) once per step.  Prints one JSON line (rank 0).  Under
+torchrun each rank runs its own independent batch (weak scaling, no collective on the
+data path).
 """
 from __future__ import annotations
 
@@ -271,31 +274,46 @@ def main():
     del wdev                                          # the layer holds its own copy
     torch.cuda.empty_cache()
     lay.x.copy_(torch.from_numpy(x).view(torch.bfloat16).to(dev))
+    st = torch.cuda.Stream(device=dev)              # graphs capture on a created stream
+    st.wait_stream(torch.cuda.current_stream())
     for _ in range(args.warmup):
-        lay.forward()
+        lay.forward(stream=st)
     torch.cuda.synchronize()
     if api.read_status(lay.status) != 0:
         raise RuntimeError(f"device status {api.read_status(lay.status)}")
 
+    # The timed region is one CUDA graph of K layer passes (the decode serving form:
+    # launches replayed, no host work per step).  Every EVERY-th pass records its
+    # stage events as graph nodes; their averages give the per-kernel durations of the
+    # roofline (an event node costs a few microseconds, so not every pass has them).
     K = args.steps
+    EVERY = 8
+    sampled = list(range(0, K, EVERY))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(_lib.LAYER_EVENTS)]
-           for _ in range(K)]
+           for _ in sampled]
     for row in evs:                      # torch creates the CUDA event on first record
         for e in row:
-            e.record()
+            e.record(st)
+    torch.cuda.synchronize()
+    steps_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(steps_graph, stream=st):
+        for i in range(K):
+            lay.forward(stream=st, events=evs[i // EVERY] if i % EVERY == 0 else None)
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.2)
+    for _ in range(args.warmup):                    # the GPU idled while the sampler started
+        lay.forward(stream=st)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for i in range(K):
-        lay.forward(events=evs[i])
-    t1.record()
+    with torch.cuda.stream(st):                     # replay() launches on the current stream
+        t0.record(st)
+        steps_graph.replay()
+        t1.record(st)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -303,25 +321,29 @@ def main():
     ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     ms_step = ms_total / K
     value = whole_job_rate(world, cfg.B, ms_step)
-    stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]))
+    stage_ms = {s: float(np.mean([row[j].elapsed_time(row[j + 1]) for row in evs]))
                 for j, s in enumerate(STAGES)}
 
-    # end to end through the host-buffer C entry point
+    # end to end through the library's host-buffer graph: each step is one launch of
+    # (x host->device, the layer, out device->host)
     e2e = None
     if not args.no_e2e:
         xh = torch.from_numpy(x).view(torch.bfloat16).pin_memory()
         oh = torch.empty_like(xh).pin_memory()
+        lay.forward_host(xh, oh, stream=st)
+        host_graph = api.LayerGraph(lay, st, xh, oh)
         for _ in range(2):
-            lay.forward_host(xh, oh)
+            host_graph.launch(st)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
+        a.record(st)
         for _ in range(K):
-            lay.forward_host(xh, oh)
-        b.record()
+            host_graph.launch(st)
+        b.record(st)
         torch.cuda.synchronize()
+        host_graph.close()
         ms = max_over_ranks(a.elapsed_time(b), dist, dev)
         e2e = {"value": whole_job_rate(world, cfg.B, ms / K), "unit": UNIT,
                "h2d_bytes_per_step": xh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2}

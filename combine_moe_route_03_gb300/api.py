@@ -282,3 +282,34 @@ class MoELayer:
         check(load().moe_layer_forward_host(ctypes.byref(self.layer), ptr(x_host),
                                             ptr(out_host), stream_ptr(stream)),
               "moe_layer_forward_host")
+
+
+class LayerGraph:
+    """One captured layer call (moe_layer_graph_create), replayed by launch().
+
+    The graph keeps the layer's buffers and, for a host graph, the pinned host buffers
+    it was captured with; keep them alive and unchanged while the graph is used."""
+
+    def __init__(self, layer: "MoELayer", stream: torch.cuda.Stream,
+                 x_host: torch.Tensor | None = None, out_host: torch.Tensor | None = None):
+        self._keep = (layer, x_host, out_host)
+        h = ctypes.c_void_p()
+        check(load().moe_layer_graph_create(ctypes.byref(layer.layer), ptr(x_host), ptr(out_host),
+                                            stream_ptr(stream), ctypes.byref(h)),
+              "moe_layer_graph_create")
+        self.handle = h
+
+    def launch(self, stream) -> None:
+        check(load().moe_layer_graph_launch(self.handle, stream_ptr(stream)),
+              "moe_layer_graph_launch")
+
+    def close(self) -> None:
+        if self.handle:
+            check(load().moe_layer_graph_destroy(self.handle), "moe_layer_graph_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -77,8 +77,16 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   if (!L) return MOE_ERR_INVALID;
   const moe_route_cfg &rc = L->route;
   cudaStream_t st = as_stream(stream);
+  // Under stream capture a stage event becomes an event-record node of the graph, so
+  // it records at every replay (a plain record would only order the capture).
+  unsigned ev_flags = cudaEventRecordDefault;
+  if (L->events) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+      ev_flags = cudaEventRecordExternal;
+  }
   auto mark = [&](int i) {
-    if (L->events) cudaEventRecord(static_cast<cudaEvent_t>(L->events[i]), st);
+    if (L->events) cudaEventRecordWithFlags(static_cast<cudaEvent_t>(L->events[i]), st, ev_flags);
   };
   if (L->has_shared && !L->shared_tiles) return MOE_ERR_INVALID;
   const int64_t srows = L->has_shared ? ((int64_t)rc.B + 127) / 128 * 128 : 0;
@@ -195,5 +203,45 @@ extern "C" int moe_layer_forward_host(const moe_layer *L, const void *x_host, vo
   int rc = moe_layer_forward(L, stream);
   if (rc) return rc;
   e = cudaMemcpyAsync(out_host, L->out, bytes, cudaMemcpyDeviceToHost, st);
+  return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+}
+
+// Whole-layer CUDA graph ("Large-scale EP ...", §DeepEP: fixed shapes make decode
+// replayable as a graph, which keeps launch overhead off each step).  Every call of
+// the layer is stream work with no host synchronisation, so it captures as is.
+extern "C" int moe_layer_graph_create(const moe_layer *L, const void *x_host, void *out_host,
+                                      void *stream, void **graph) {
+  if (!L || !graph || !stream) return MOE_ERR_INVALID;  // no capture on the legacy stream
+  if ((x_host == nullptr) != (out_host == nullptr)) return MOE_ERR_INVALID;
+  *graph = nullptr;
+  moe_layer Lc = *L;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  const int rc = x_host ? moe_layer_forward_host(&Lc, x_host, out_host, stream)
+                        : moe_layer_forward(&Lc, stream);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(st, &g);
+  if (rc || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    return rc ? rc : set_cuda_error(e);
+  }
+  cudaGraphExec_t ex = nullptr;
+  e = cudaGraphInstantiate(&ex, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  *graph = ex;
+  return MOE_OK;
+}
+
+extern "C" int moe_layer_graph_launch(void *graph, void *stream) {
+  if (!graph) return MOE_ERR_INVALID;
+  cudaError_t e = cudaGraphLaunch(static_cast<cudaGraphExec_t>(graph), as_stream(stream));
+  return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+}
+
+extern "C" int moe_layer_graph_destroy(void *graph) {
+  if (!graph) return MOE_OK;
+  cudaError_t e = cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(graph));
   return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
 }

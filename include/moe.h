@@ -364,6 +364,28 @@ int moe_layer_forward(const moe_layer *layer, void *stream);
 int moe_layer_forward_host(const moe_layer *layer, const void *x_host, void *out_host,
                            void *stream);
 
+/*
+ * Whole-layer CUDA graph ("Large-scale EP: DeepEP, EPLB and two-batch overlap",
+ * §DeepEP: each mode where it belongs -- the fixed-shape low-latency path is the
+ * one decode replays as a CUDA graph to keep launch overhead off each step).
+ *
+ * moe_layer_graph_create captures one moe_layer_forward of L (or, with x_host and
+ * out_host both non-NULL, one moe_layer_forward_host: the copies are part of the
+ * graph, so the host buffers must be pinned) on `stream` and instantiates it into
+ * *graph.  `stream` must be a created stream, not the legacy default stream.  The
+ * graph keeps every pointer of L and of the host buffers as they were at capture:
+ * launch it only while they stay valid and unchanged; the stage events of L, if any,
+ * are recorded at every replay.  Run the layer once eagerly before capturing (first calls
+ * set kernel attributes).  moe_layer_graph_launch replays it on `stream` (no host
+ * synchronisation); moe_layer_graph_destroy frees it (NULL is a no-op).
+ * Errors: MOE_ERR_INVALID for NULL L / graph / stream or only one host buffer; a
+ * failing layer call or capture returns its code and leaves *graph NULL.
+ */
+int moe_layer_graph_create(const moe_layer *L, const void *x_host, void *out_host, void *stream,
+                           void **graph);
+int moe_layer_graph_launch(void *graph, void *stream);
+int moe_layer_graph_destroy(void *graph);
+
 #ifdef __cplusplus
 }
 #endif

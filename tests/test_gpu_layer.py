@@ -235,6 +235,51 @@ def test_layer_matches_oracle(dev, name):
     assert np.array_equal(out, out2)
 
 
+@pytest.mark.parametrize("name", ["small_masked", "small_contig", "small_sbo"])
+def test_layer_graph_replay_matches_eager(dev, name):
+    """A captured layer graph replays the same bytes as eager calls, on new inputs too
+    (the graph reads the layer's x buffer at every launch)."""
+    cfg, x, W, bias = host_workload(name)
+    ex = host_experts(name)
+    idx, _ = oracle.route(x, W, bias, cfg)
+    lay, out_a = run_layer(cfg, x, W, bias, ex, eplb_for(cfg, idx))
+    x2 = inputs.make_x(cfg.with_(seed=cfg.seed + 11))
+    lay.forward(bf16_dev(x2))
+    out_b = bits(lay.out)
+    st = torch.cuda.Stream(device=dev)
+    st.wait_stream(torch.cuda.current_stream())
+    g = api.LayerGraph(lay, st)
+    for xi, want in ((x, out_a), (x2, out_b), (x, out_a)):
+        lay.x.copy_(bf16_dev(xi))
+        st.wait_stream(torch.cuda.current_stream())
+        lay.out.zero_()
+        st.wait_stream(torch.cuda.current_stream())
+        g.launch(st)
+        torch.cuda.current_stream().wait_stream(st)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(lay.out), want)
+    assert api.read_status(lay.status) == 0
+    g.close()
+
+
+def test_layer_host_graph_matches_forward_host(dev):
+    """A graph that includes the pinned host copies gives forward_host's bytes."""
+    cfg, x, W, bias = host_workload("small_masked")
+    ex = host_experts("small_masked")
+    lay, out_a = run_layer(cfg, x, W, bias, ex)
+    xh = torch.from_numpy(x).view(torch.bfloat16).pin_memory()
+    oh = torch.zeros(cfg.B, cfg.H, dtype=torch.bfloat16).pin_memory()
+    st = torch.cuda.Stream(device=dev)
+    st.wait_stream(torch.cuda.current_stream())
+    g = api.LayerGraph(lay, st, xh, oh)
+    for _ in range(2):
+        oh.zero_()
+        g.launch(st)
+        st.synchronize()
+        assert np.array_equal(oh.view(torch.int16).numpy().view(np.uint16), out_a)
+    g.close()
+
+
 def test_layouts_and_eplb_agree_bitwise(dev):
     """Masked = contiguous, EPLB on = off: same rows, same weights -> same bytes."""
     base = configs.SMALL_EPLB

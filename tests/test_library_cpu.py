@@ -90,3 +90,11 @@ def test_host_argument_checks_return_before_launch(L):
     cc = _lib.CombineCfg(4, 100, 2, None, 0, 64, 0, 0, 0)          # H % 128 != 0
     assert L.moe_combine(ctypes.byref(cc), *([None] * 7)) == -2
     assert L.moe_packed_scale_bytes(2, 256, 384) == 2 * 2 * 3 * 512
+    h = ctypes.c_void_p()
+    lay = _lib.Layer()
+    assert L.moe_layer_graph_create(None, None, None, None, ctypes.byref(h)) == -1
+    assert L.moe_layer_graph_create(ctypes.byref(lay), None, None, None, ctypes.byref(h)) == -1
+    assert L.moe_layer_graph_create(ctypes.byref(lay), ctypes.c_void_p(16), None,
+                                    ctypes.c_void_p(16), ctypes.byref(h)) == -1  # one host buffer
+    assert L.moe_layer_graph_launch(None, None) == -1
+    assert L.moe_layer_graph_destroy(None) == 0
