@@ -648,11 +648,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // activation rows, half of the 256-row weight tile and both weight scale atoms; in
 // TMEM it holds its rows' accumulator and scales.  The even CTA issues the MMAs and
 // scale copies for both.  Both CTAs' TMA loads complete on the even CTA's stage
-// barrier, and the MMA commits free the stage in both.  Per SM, a 128-deep k-block
-// moves 16 KB of weights instead of 32 KB, and that operand traffic is what bounds
-// the one-CTA kernel near the ridge.  A pair item (two M tiles of one expert) is one
-// sub-unit.  A couple of singles of different experts is two: one tile each, the
-// other CTA's rows idle.
+// barrier, and the MMA commits free the stage in both.  The pair instruction issues
+// about 1.5x the FLOPs per SM-cycle of the one-CTA M=128 form, which bounds the
+// one-CTA kernel at full tiles, and each SM moves 16 KB of weights per 128-deep
+// k-block instead of 32 KB.  A pair item (two M tiles of one expert) is one unit; the
+// single tiles run in a second, one-CTA launch.
 // A stage holds KB2 k-blocks (256 K): the issuing thread waits, fences and commits
 // once per eight MMAs, which keeps the pair's tensor pipe fed.
 constexpr int KB2 = 2, S2 = 3;              // k-blocks per stage, stages
@@ -678,11 +678,12 @@ struct Unit2 {
 };
 static_assert(sizeof(Unit2) <= 32, "unit ring slot");
 
-// Work unit -> its 2-SM sub-unit (1), 0 for a unit of a single (not this launch's
-// work), -1 when the unit's entries do not describe tiles inside the operands.  Both CTAs compute the same list (rank only selects
-// which tile fills row0/nvalid/active).
-__device__ __forceinline__ int get_pair2_units(const GemmParams &P, int unit, int units2,
-                                               int rank, Unit2 *out) {
+// Work unit -> the pair item's 2-SM unit in *out: returns 1; 0 for a unit of a single
+// tile (the one-CTA launch that follows takes those); -1 when the unit's entries do not
+// describe tiles inside the operands.  Both CTAs decode alike: `rank` only selects which
+// of the two tiles fills row0 / nvalid / active.
+__device__ __forceinline__ int get_pair2_unit(const GemmParams &P, int unit, int units2,
+                                              int rank, Unit2 *out) {
   const int32_t *tl = P.tiles;
   int u = unit;
   const bool second = unit < units2;
@@ -701,43 +702,37 @@ __device__ __forceinline__ int get_pair2_units(const GemmParams &P, int unit, in
   const int ni = local / gc;
   if (ni >= P.n_tiles) return -1;
   const int32_t *it = items + 8 * (gf + local % gc);
-  if (it[4] == 0) return 0;  // singles: the one-CTA launch that follows takes them
-  int sub[2][2];
-  int ns = 1;
-  sub[0][0] = it[0];  // one expert's pair: one sub-unit, both CTAs
-  sub[0][1] = it[1];
-  for (int s = 0; s < ns; ++s) {
-    Unit2 &U = out[s];
-    U.ok = U.active = U.end = false;
-    U.row0 = U.nvalid = 0;
-    U.ni = ni;
-    const int lead = sub[s][0] >= 0 ? sub[s][0] : sub[s][1];  // the tile naming the weights
-    if (lead < 0 || lead >= cap) return -1;
-    const int32_t *e = tl + 8 + 8 * lead;
-    U.we = second ? P.expert2 : (P.phys2log ? P.phys2log[e[1]] : e[1]);
-    U.band = e[4];
-    if (U.we < 0 || U.we >= P.num_experts) return -1;
-    uint32_t tx = 0;
-    for (int c = 0; c < 2; ++c) {
-      tx += KB2 * BH_BYTES;
-      const int mi = sub[s][c];
-      if (mi < 0) continue;
-      if (mi >= cap) return -1;
-      const int32_t *t = tl + 8 + 8 * mi;
-      const int row0 = t[0] + (second ? P.row_offset2 : 0), nv = t[2];
-      if (!tile_ok(P, row0, nv)) return -1;
-      const int slices = nv == BM ? 0 : (nv + 31) / 32;
-      tx += KB2 * ((slices ? slices * (A_BYTES / 4) : A_BYTES) + SFA_BYTES + SFB_BYTES);
-      if (c == rank) {
-        U.row0 = row0;
-        U.nvalid = nv;
-        U.active = true;
-      }
+  if (it[4] == 0) return 0;
+  const int tile[2] = {it[0], it[1]};  // one expert's two tiles, one per CTA
+  Unit2 &U = *out;
+  U.ok = U.active = U.end = false;
+  U.row0 = U.nvalid = 0;
+  U.ni = ni;
+  if (tile[0] < 0 || tile[0] >= cap) return -1;
+  const int32_t *e = tl + 8 + 8 * tile[0];
+  U.we = second ? P.expert2 : (P.phys2log ? P.phys2log[e[1]] : e[1]);
+  U.band = e[4];
+  if (U.we < 0 || U.we >= P.num_experts) return -1;
+  uint32_t tx = 0;
+  for (int c = 0; c < 2; ++c) {
+    tx += KB2 * BH_BYTES;
+    const int mi = tile[c];
+    if (mi < 0) continue;
+    if (mi >= cap) return -1;
+    const int32_t *t = tl + 8 + 8 * mi;
+    const int row0 = t[0] + (second ? P.row_offset2 : 0), nv = t[2];
+    if (!tile_ok(P, row0, nv)) return -1;
+    const int slices = nv == BM ? 0 : (nv + 31) / 32;
+    tx += KB2 * ((slices ? slices * (A_BYTES / 4) : A_BYTES) + SFA_BYTES + SFB_BYTES);
+    if (c == rank) {
+      U.row0 = row0;
+      U.nvalid = nv;
+      U.active = true;
     }
-    U.tx = tx;
-    U.ok = true;
   }
-  return ns;
+  U.tx = tx;
+  U.ok = true;
+  return 1;
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -1013,13 +1008,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     };
     bool ok = true;
     for (int unit = first_unit; ok && unit < total; unit += ustride) {
-      Unit2 sub[2];
-      const int n = get_pair2_units(P, unit, units2, rank, sub);
-      if (n < 0) {
-        Unit2 bad = {};
-        ok = push(bad);
-      }
-      for (int i = 0; ok && i < n; ++i) ok = push(sub[i]);
+      Unit2 U = {};
+      const int n = get_pair2_unit(P, unit, units2, rank, &U);
+      if (n != 0) ok = push(U);  // -1: U.ok is false, and the producer records it
     }
     if (ok) {
       Unit2 end = {};
