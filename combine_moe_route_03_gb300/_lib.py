@@ -32,7 +32,13 @@ class RouteCfg(ctypes.Structure):
 
 class DispatchCfg(ctypes.Structure):
     _fields_ = [("B", _c_int), ("H", _c_int), ("K", _c_int), ("N_log", _c_int),
-                ("N_phys", _c_int), ("layout", _c_int), ("cap", _c_int), ("fmt", _c_int)]
+                ("N_phys", _c_int), ("layout", _c_int), ("cap", _c_int), ("fmt", _c_int),
+                ("max_rep", _c_int)]
+
+
+class EplbCfg(ctypes.Structure):
+    _fields_ = [("N_log", _c_int), ("n_group", _c_int), ("N_phys", _c_int),
+                ("n_nodes", _c_int), ("n_gpus", _c_int), ("max_rep", _c_int)]
 
 
 class GemmArgs(ctypes.Structure):
@@ -61,7 +67,8 @@ class Layer(ctypes.Structure):
             "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",
             "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",
             "dispatch_ws")] + [("route_ws_bytes", _c_sz), ("dispatch_ws_bytes", _c_sz),
-                               ("status", _vp), ("stream2", _vp), ("events", _vp)]
+                               ("status", _vp), ("stream2", _vp), ("events", _vp),
+                               ("eplb_max_rep", _c_int)]
 
 LAYER_EVENTS = 6
 STAGES = ("route", "dispatch", "gateup", "down", "combine")
@@ -72,6 +79,7 @@ SIGNATURES = {
     "moe_route_workspace_size": (_c_sz, [ctypes.POINTER(RouteCfg)]),
     "moe_route": (_c_int, [ctypes.POINTER(RouteCfg), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_sz, _vp]),
     "eplb_build_map": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_eplb_plan": (_c_int, [ctypes.POINTER(EplbCfg), _vp, _vp, _vp, _vp, _vp]),
     "moe_dispatch_rows": (_c_i64, [ctypes.POINTER(DispatchCfg)]),
     "moe_dispatch_max_tiles": (_c_i64, [ctypes.POINTER(DispatchCfg)]),
     "moe_dispatch_workspace_size": (_c_sz, [ctypes.POINTER(DispatchCfg)]),

@@ -12,10 +12,10 @@ import torch
 
 from . import _lib
 from ._lib import (FMT_BF16, FMT_FP8, GEMM_DOWN, GEMM_GATEUP_SWIGLU, CombineCfg, DispatchCfg,
-                   GemmArgs, Layer, RouteCfg, check, load, ptr, stream_ptr)
+                   EplbCfg, GemmArgs, Layer, RouteCfg, check, load, ptr, stream_ptr)
 from .configs import MASKED, MoEConfig
 
-__all__ = ["route", "eplb_build_map", "dispatch", "dispatch_sizes", "pack_weight_scales",
+__all__ = ["route", "eplb_build_map", "eplb_plan", "EplbRecorder", "dispatch", "dispatch_sizes", "pack_weight_scales",
            "grouped_gemm_fp8", "combine", "read_status", "new_status", "MoELayer",
            "FMT_FP8", "FMT_BF16", "GEMM_GATEUP_SWIGLU", "GEMM_DOWN", "num_sms"]
 
@@ -67,9 +67,60 @@ def eplb_build_map(counts: np.ndarray, N_log: int, N_phys: int):
     return l2p, rep, p2l
 
 
-def _dispatch_cfg(cfg: MoEConfig, B: int, fmt: int, cap: int | None = None) -> DispatchCfg:
+def eplb_plan(load_counts: np.ndarray, N_log: int, N_phys: int, n_group: int = 1,
+              n_nodes: int = 1, n_gpus: int = 1, max_rep: int = 2):
+    """moe_eplb_plan (host): recorded loads -> (log2phys [N_log][max_rep], rep [N_log],
+    phys2log [N_phys]) int32 numpy, and the plan's balance (mean / max GPU load)."""
+    c = np.ascontiguousarray(load_counts, dtype=np.int64)
+    if c.shape != (N_log,):
+        raise ValueError("one load per logical expert")
+    cfg = EplbCfg(N_log, n_group, N_phys, n_nodes, n_gpus, max_rep)
+    l2p = np.empty((N_log, max_rep), np.int32)
+    rep = np.empty(N_log, np.int32)
+    p2l = np.empty(N_phys, np.int32)
+    bal = ctypes.c_double()
+    check(load().moe_eplb_plan(ctypes.byref(cfg), c.ctypes.data, p2l.ctypes.data,
+                               l2p.ctypes.data, rep.ctypes.data, ctypes.byref(bal)),
+          "moe_eplb_plan")
+    return (l2p, rep, p2l), bal.value
+
+
+class EplbRecorder:
+    """Periodic rebalancing from measured loads: adds each step's per-expert token
+    counts (the route's expert_counts) and, every ``period`` steps, plans a new map
+    from the loads recorded since the last plan ("Large-scale EP ...", §EPLB: the
+    dynamic mode re-measures and rebalances while running)."""
+
+    def __init__(self, N_log: int, N_phys: int, period: int, **plan_kw):
+        if period < 1:
+            raise ValueError("period >= 1")
+        self.N_log, self.N_phys, self.period, self.plan_kw = N_log, N_phys, period, plan_kw
+        self.load = np.zeros(N_log, np.int64)
+        self.steps = 0
+
+    def observe(self, expert_counts) -> None:
+        c = expert_counts.cpu().numpy() if isinstance(expert_counts, torch.Tensor) else expert_counts
+        c = np.asarray(c, np.int64)
+        if c.shape != (self.N_log,) or np.any(c < 0):
+            raise ValueError("expert counts: one non-negative count per logical expert")
+        self.load += c
+        self.steps += 1
+
+    def due(self) -> bool:
+        return self.steps >= self.period
+
+    def plan(self):
+        """The map for the loads recorded so far; the recorder then starts afresh."""
+        m, bal = eplb_plan(self.load, self.N_log, self.N_phys, **self.plan_kw)
+        self.load[:] = 0
+        self.steps = 0
+        return m, bal
+
+
+def _dispatch_cfg(cfg: MoEConfig, B: int, fmt: int, cap: int | None = None,
+                  max_rep: int = 0) -> DispatchCfg:
     return DispatchCfg(B, cfg.H, cfg.K, cfg.N, cfg.N_phys, cfg.layout,
-                       cfg.cap if cap is None else cap, fmt)
+                       cfg.cap if cap is None else cap, fmt, max_rep)
 
 
 def dispatch_sizes(cfg: MoEConfig, B: int | None = None, fmt: int = FMT_FP8,
@@ -84,10 +135,11 @@ def dispatch_sizes(cfg: MoEConfig, B: int | None = None, fmt: int = FMT_FP8,
 def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=None, rep=None,
              fmt: int = FMT_FP8, shared: bool = False, status: torch.Tensor | None = None,
              cap: int | None = None, stream=None, out: dict | None = None) -> dict:
-    """moe_dispatch -> A, A_sf, counts, row_of, src_of, tiles (+ shared copy)."""
+    """moe_dispatch -> A, A_sf, counts, row_of, src_of, tiles (+ shared copy).
+    log2phys [N][max_rep] / rep [N]: an EPLB map (max_rep = its column count)."""
     B, H = x.shape
     dev = x.device
-    dc = _dispatch_cfg(cfg, B, fmt, cap)
+    dc = _dispatch_cfg(cfg, B, fmt, cap, 0 if log2phys is None else log2phys.shape[1])
     sz = dispatch_sizes(cfg, B, fmt, cap)
     rows, mt = sz["rows"], sz["max_tiles"]
     if rows <= 0:
@@ -212,9 +264,9 @@ class MoELayer:
         self.log2phys = self.rep = self.phys2log = None
         if eplb_map is not None:
             l2p, rep, p2l = eplb_map
-            self.log2phys = torch.from_numpy(np.ascontiguousarray(l2p)).to(dev)
-            self.rep = torch.from_numpy(np.ascontiguousarray(rep)).to(dev)
-            self.phys2log = torch.from_numpy(np.ascontiguousarray(p2l)).to(dev)
+            self.log2phys = torch.from_numpy(np.ascontiguousarray(l2p, np.int32)).to(dev)
+            self.rep = torch.from_numpy(np.ascontiguousarray(rep, np.int32)).to(dev)
+            self.phys2log = torch.from_numpy(np.ascontiguousarray(p2l, np.int32)).to(dev)
         sz = dispatch_sizes(cfg)
         self.rows, self.max_tiles = sz["rows"], sz["max_tiles"]
         self.srows = (B + 127) // 128 * 128 if cfg.shared else 0
@@ -248,6 +300,7 @@ class MoELayer:
         lay.num_sms = sms - combine_ctas if cfg.sbo else sms
         lay.combine_ctas = combine_ctas
         lay.gemm_pairs = gemm_pairs
+        lay.eplb_max_rep = 0 if self.log2phys is None else self.log2phys.shape[1]
         names = ["x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
                  "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",
                  "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",
@@ -258,6 +311,21 @@ class MoELayer:
         lay.dispatch_ws_bytes = self.dispatch_ws.numel()
         lay.stream2 = self.stream2.cuda_stream if self.stream2 is not None else None
         self.layer = lay
+
+    def set_eplb_map(self, eplb_map) -> None:
+        """Installs a new EPLB map of the same physical expert count (a replica reads
+        its logical expert's weights through phys2log, so no weight moves on one GPU).
+        Call between steps: a captured graph keeps the map buffers, not their values,
+        so it uses the new map from its next replay when the column count is kept."""
+        if self.log2phys is None:
+            raise ValueError("the layer was built without an EPLB map")
+        l2p, rep, p2l = (np.ascontiguousarray(a, np.int32) for a in eplb_map)
+        if l2p.shape != tuple(self.log2phys.shape) or p2l.shape != tuple(self.phys2log.shape) \
+                or rep.shape != tuple(self.rep.shape):
+            raise ValueError("the new map must keep the layer's shapes")
+        self.log2phys.copy_(torch.from_numpy(l2p))
+        self.rep.copy_(torch.from_numpy(rep))
+        self.phys2log.copy_(torch.from_numpy(p2l))
 
     def forward(self, x: torch.Tensor | None = None, stream=None, events=None) -> torch.Tensor:
         """Runs the layer on self.x (copied from ``x`` first when given).

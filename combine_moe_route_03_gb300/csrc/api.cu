@@ -106,6 +106,7 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   dc.layout = L->layout;
   dc.cap = L->cap;
   dc.fmt = MOE_FMT_FP8;
+  dc.max_rep = L->eplb_max_rep;
   uint8_t *A = static_cast<uint8_t *>(L->A), *A_sf = static_cast<uint8_t *>(L->A_sf);
   rc_ = moe_dispatch(&dc, L->x, L->topk_idx, L->log2phys, L->rep, A, A_sf, L->counts, L->row_of,
                      nullptr, L->tiles, L->has_shared ? A + L->rows * rc.H : nullptr,

@@ -53,8 +53,8 @@ __host__ __device__ inline DispatchWs carve(void *ws, int B, int K, int N_phys) 
 
 __global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
     const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ log2phys,
-    const int32_t *__restrict__ rep, int B, int K, int N_log, int N_phys, DispatchWs ws,
-    int32_t *status) {
+    const int32_t *__restrict__ rep, int max_rep, int B, int K, int N_log, int N_phys,
+    DispatchWs ws, int32_t *status) {
   extern __shared__ int32_t sm[];
   int32_t *whist = sm;                              // [kCountWarps][N_phys]
   int32_t *pp = whist + kCountWarps * N_phys;       // [kChunk*K]
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
         status_or(status, MOE_STATUS_BAD_INDEX);
       } else if (log2phys) {
         const int re = rep[e];
-        p = (re == 1 || re == 2) ? log2phys[2 * e + (t % re)] : -1;
+        p = (re >= 1 && re <= max_rep) ? log2phys[(size_t)max_rep * e + (t % re)] : -1;
         if (p < 0 || p >= N_phys) {
           status_or(status, MOE_STATUS_BAD_INDEX);
           p = -1;
@@ -472,6 +472,7 @@ static int dispatch_check(const moe_dispatch_cfg *c) {
   if (c->layout != MOE_LAYOUT_CONTIG && c->layout != MOE_LAYOUT_MASKED) return MOE_ERR_INVALID;
   if (c->fmt != MOE_FMT_FP8 && c->fmt != MOE_FMT_BF16) return MOE_ERR_INVALID;
   if (c->layout == MOE_LAYOUT_MASKED && (c->cap <= 0 || c->cap % 128)) return MOE_ERR_UNSUPPORTED;
+  if (c->max_rep < 0 || c->max_rep > 64) return MOE_ERR_INVALID;
   return MOE_OK;
 }
 
@@ -527,8 +528,8 @@ extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int3
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return set_cuda_error(e);
   }
-  dispatch_count_kernel<<<nchunks, kCountWarps * 32, smem, st>>>(topk_idx, log2phys, rep, B, K,
-                                                                c->N_log, Np, ws, status);
+  dispatch_count_kernel<<<nchunks, kCountWarps * 32, smem, st>>>(
+      topk_idx, log2phys, rep, c->max_rep ? c->max_rep : 2, B, K, c->N_log, Np, ws, status);
   if ((rc = check_launch())) return rc;
   dispatch_scan_kernel<<<1, kScanThreads, 0, st>>>(B, Np, nchunks, c->layout, c->cap,
                                                    moe_dispatch_rows(c), ws, counts, tiles,
@@ -606,8 +607,8 @@ extern "C" int moe_dispatch_noalloc(const moe_dispatch_cfg *c, const void *x,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return set_cuda_error(e);
   }
-  dispatch_count_kernel<<<nchunks, kCountWarps * 32, smem, st>>>(topk_idx, log2phys, rep, B, K,
-                                                                c->N_log, Np, ws, status);
+  dispatch_count_kernel<<<nchunks, kCountWarps * 32, smem, st>>>(
+      topk_idx, log2phys, rep, c->max_rep ? c->max_rep : 2, B, K, c->N_log, Np, ws, status);
   if ((rc = check_launch())) return rc;
   dispatch_scan_kernel<<<1, kScanThreads, 0, st>>>(B, Np, nchunks, c->layout, c->cap,
                                                    moe_dispatch_rows(c), ws, counts, tiles,

@@ -127,6 +127,50 @@ int moe_route(const moe_route_cfg *cfg, const void *x, const float *W, const flo
 int eplb_build_map(const int64_t *counts_host, int N_log, int N_phys, int32_t *log2phys,
                    int32_t *rep, int32_t *phys2log);
 
+/*
+ * EPLB placement from recorded loads: DeepSeek's algorithm as the pages describe it
+ * ("Large-scale EP: DeepEP, EPLB and two-batch overlap", §EPLB: hierarchical — the
+ * expert groups are packed onto nodes first and the experts placed within each node,
+ * so that one node's experts come from the same groups; rebalanced from measured
+ * counts; "SGLang开源首个对标官方性能的DeepSeek-V3/R1 H100部署方案", §专家并行负载均衡器:
+ * redundant slots hold extra copies of the most used experts, and cold experts
+ * share a GPU with medium ones; balance = mean / max of the per-GPU load).  HOST
+ * function, deterministic.
+ *   load [N_log]: recorded tokens per logical expert, 0 <= load < 2^40.
+ *   Groups: expert e belongs to group e / (N_log / n_group).  When n_nodes > 1 and
+ *   n_group % n_nodes == 0 the plan is hierarchical: (1) the groups, heaviest
+ *   first (ties -> lower group), each go to the lightest node that holds fewer than
+ *   n_group / n_nodes groups (ties -> lower node); a node's experts are those of its
+ *   groups in ascending order.  Otherwise all experts and GPUs form one node.
+ *   (2) Within a node, every expert gets one slot and each remaining slot of the
+ *   node (N_phys / nodes in all) goes, one at a time, to the expert with the largest
+ *   load per replica, load[e] / rep[e], that has fewer than max_rep replicas (ties
+ *   -> lower e).  (3) The node's replicas, each carrying load[e] / rep[e], are taken
+ *   heaviest first (ties -> lower e) and each put on the lightest GPU of the node
+ *   that has a free slot (ties -> lower GPU), N_phys / n_gpus slots per GPU.
+ *   Outputs (host arrays): phys2log [N_phys] — slot j of GPU g is physical expert
+ *   g * (N_phys / n_gpus) + j, filled in placement order; log2phys [N_log][max_rep]
+ *   — e's physical experts ascending, the unused tail repeating the first; rep
+ *   [N_log]; balance (nullable) — mean / max of the per-GPU loads (1 when all are 0).
+ *   moe_dispatch sends token t of e to log2phys[e][t % rep[e]] (cfg->max_rep =
+ *   max_rep).
+ * Returns MOE_ERR_INVALID unless N_log >= 1, n_group >= 1, N_log % n_group == 0,
+ * N_phys >= N_log, N_phys <= 8192, n_gpus % n_nodes == 0, N_phys % n_gpus == 0,
+ * 1 <= max_rep <= 8, and each node's slots lie between its expert count and max_rep
+ * times it.
+ */
+typedef struct moe_eplb_cfg {
+  int N_log;    /* logical experts */
+  int n_group;  /* expert groups (1: none) */
+  int N_phys;   /* physical expert slots */
+  int n_nodes;  /* nodes */
+  int n_gpus;   /* GPUs in all */
+  int max_rep;  /* replicas of one logical expert at most, 1..8 */
+} moe_eplb_cfg;
+
+int moe_eplb_plan(const moe_eplb_cfg *cfg, const int64_t *load, int32_t *phys2log,
+                  int32_t *log2phys, int32_t *rep, double *balance);
+
 /* --------------------------------------------------------------- dispatch */
 /*
  * Dispatch ("Large-scale EP ...", §DeepEP: each mode where it belongs — the
@@ -143,7 +187,10 @@ int eplb_build_map(const int64_t *counts_host, int N_log, int N_phys, int32_t *l
  *     [-127,127]), code = e4m3_rne_satfinite(x * 2^-e) — and copied to its K
  *     rows of A [rows][H]; the exponents go to A_sf as SF atoms.
  *   BF16: rows are copied unchanged (A is bf16 [rows][H], A_sf unused).
- *   log2phys/rep (nullable, EPLB) map logical to physical experts.
+ *   log2phys [N_log][max_rep] / rep [N_log] (nullable, EPLB) map logical to
+ *     physical experts: token t of e goes to log2phys[e][t % rep[e]], and a
+ *     rep[e] outside [1, max_rep] or a physical id outside [0, N_phys) sets
+ *     MOE_STATUS_BAD_INDEX and drops the pair.
  *   counts [N_phys]: rows routed to each physical expert (before capacity).
  *   row_of [B][K]: A row of (t,k); src_of [rows] (nullable): token of each row,
  *     -1 for padding / empty slots.  tiles: see the tile list above.
@@ -160,6 +207,7 @@ typedef struct moe_dispatch_cfg {
   int layout;
   int cap;
   int fmt;
+  int max_rep; /* columns of log2phys (0: 2, the eplb_build_map layout), at most 64 */
 } moe_dispatch_cfg;
 
 int64_t moe_dispatch_rows(const moe_dispatch_cfg *cfg);      /* rows of A to allocate */
@@ -356,6 +404,7 @@ typedef struct moe_layer {
      stage boundaries (start, after route, dispatch, gate/up, down, combine) so a
      caller can time each stage of the chain. */
   void *const *events;
+  int eplb_max_rep; /* columns of log2phys (0: 2) */
 } moe_layer;
 
 #define MOE_LAYER_EVENTS 6

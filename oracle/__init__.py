@@ -64,7 +64,7 @@ def lib():
         L.oracle_eplb_build_map.argtypes = [_i64p, ctypes.c_int, ctypes.c_int, _i32p, _i32p, _i32p]
         L.oracle_eplb_build_map.restype = ctypes.c_int
         L.oracle_dispatch.argtypes = [_u16p, _i32p, ctypes.c_void_p, ctypes.c_void_p] + [
-            ctypes.c_int] * 7 + [_i32p, _i32p, _i32p, _i32p, _i32p, ctypes.c_int64, _u8p, _u8p]
+            ctypes.c_int] * 8 + [_i32p, _i32p, _i32p, _i32p, _i32p, ctypes.c_int64, _u8p, _u8p]
         L.oracle_dispatch.restype = ctypes.c_int
         L.oracle_combine.argtypes = [_u16p, _i32p, _f32p, ctypes.c_void_p] + [ctypes.c_int] * 3 + [_u16p]
         L.oracle_combine.restype = None
@@ -195,7 +195,8 @@ def contig_rows_alloc(B: int, K: int, N_phys: int) -> int:
 
 def dispatch(x: np.ndarray, topk_idx: np.ndarray, cfg, log2phys=None, rep=None,
              fmt: int = 0, cap: int | None = None) -> dict:
-    """Expert-major permutation + 1x128 e4m3 quantisation (see moe_oracle.c)."""
+    """Expert-major permutation + 1x128 e4m3 quantisation (see moe_oracle.c).
+    log2phys [N_log][R] / rep: an EPLB map of R columns (eplb_build_map: R = 2)."""
     B, K, H = x.shape[0], topk_idx.shape[1], x.shape[1]
     Np = cfg.N_phys
     layout = cfg.layout
@@ -212,6 +213,7 @@ def dispatch(x: np.ndarray, topk_idx: np.ndarray, cfg, log2phys=None, rep=None,
                                np.ascontiguousarray(topk_idx, dtype=np.int32),
                                _ptr(None if log2phys is None else np.ascontiguousarray(log2phys, np.int32)),
                                _ptr(None if rep is None else np.ascontiguousarray(rep, np.int32)),
+                               0 if log2phys is None else np.shape(log2phys)[1],
                                B, H, K, Np, layout, cap, fmt, phys, cnt, seg, row_of, src_of,
                                rows, A, sf)
     return dict(phys=phys, cnt=cnt, seg_start=seg, row_of=row_of, src_of=src_of, A=A, sf=sf,

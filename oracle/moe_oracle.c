@@ -403,7 +403,8 @@ int oracle_eplb_build_map(const int64_t *counts, int N_log, int N_phys, int32_t 
 /*
  * Expert-major permutation of the routed rows, the single-GPU counterpart of the
  * EP all-to-all (each token copied to its K experts).
- *   phys(t,k) = log2phys[e][t mod rep[e]] (or e without a map).
+ *   phys(t,k) = log2phys[e][t mod rep[e]] (or e without a map); log2phys has
+ *   max_rep columns.
  *   Within a physical expert, rows are taken in ascending (t, k) order.
  *   layout 0 (contiguous): expert p's segment starts at
  *       sum_{q<p} ceil(cnt_q / 128) * 128; rows_used = that sum over all experts.
@@ -416,7 +417,8 @@ int oracle_eplb_build_map(const int64_t *counts, int N_log, int N_phys, int32_t 
  * Returns 0, or 2 if any row was dropped for capacity.
  */
 int oracle_dispatch(const uint16_t *x, const int32_t *topk_idx, const int32_t *log2phys,
-                    const int32_t *rep, int B, int H, int K, int N_phys, int layout, int cap,
+                    const int32_t *rep, int max_rep, int B, int H, int K, int N_phys,
+                    int layout, int cap,
                     int fmt, int32_t *phys, int32_t *cnt, int32_t *seg_start, int32_t *row_of,
                     int32_t *src_of, int64_t rows_alloc, uint8_t *A, uint8_t *sf)
 {
@@ -428,7 +430,7 @@ int oracle_dispatch(const uint16_t *x, const int32_t *topk_idx, const int32_t *l
     for (int t = 0; t < B; ++t)
         for (int k = 0; k < K; ++k) {
             int e = topk_idx[t * K + k];
-            int p = log2phys ? log2phys[2 * e + (t % rep[e])] : e;
+            int p = log2phys ? log2phys[max_rep * e + (t % rep[e])] : e;
             phys[t * K + k] = p;
             cnt[p] += 1;
         }

@@ -108,6 +108,24 @@ def test_pack_unpack_sf_atoms_inverse():
     assert np.array_equal(support_unpack(pack_sf_atoms(sf), 384, 5), sf)
 
 
+def cluster_tile_list(tiles_per_expert, nvalid_of) -> np.ndarray:
+    """Tile list (entries + cluster item table) for consecutive experts with the given
+    M-tile counts; tile j of an expert holds nvalid_of(j) rows."""
+    mt = sum(tiles_per_expert)
+    t = np.zeros(8 + 16 * mt, np.int32)
+    i = 0
+    for e, c in enumerate(tiles_per_expert):
+        for j in range(c):
+            t[8 + 8 * (i + j): 8 + 8 * (i + j) + 5] = [128 * (i + j), e, nvalid_of(j), i, c]
+        i += c
+    items = cluster_items(tiles_per_expert)
+    t[0:5] = [mt, 128 * mt, sum(c // 2 for c in tiles_per_expert),
+              sum(c % 2 for c in tiles_per_expert), len(items)]
+    for k, it in enumerate(items):
+        t[8 + 8 * mt + 8 * k: 8 + 8 * mt + 8 * k + 5] = it
+    return t
+
+
 @pytest.mark.parametrize("op", [0, 1])
 def test_cluster_pair_gemm_equals_single_cta(dev, op):
     """Two-CTA clusters (pairs sharing a weight tile, singles two by two) give the same
@@ -121,17 +139,7 @@ def test_cluster_pair_gemm_equals_single_cta(dev, op):
     q, sf = activations(rows, k, 7)
     W, Wsf = zip(*[inputs.make_fp8_matrix(n, k, (9, 55, e)) for e in range(E)])
     W, Wsf = np.stack(W), np.stack(Wsf)
-    t = np.zeros(8 + 16 * mt, np.int32)
-    i = 0
-    for e, c in enumerate(tiles_per_expert):
-        for j in range(c):
-            t[8 + 8 * (i + j): 8 + 8 * (i + j) + 5] = [128 * (i + j), e, 128 - 5 * j, i, c]
-        i += c
-    items = cluster_items(tiles_per_expert)
-    t[0:5] = [mt, rows, sum(c // 2 for c in tiles_per_expert),
-              sum(c % 2 for c in tiles_per_expert), len(items)]
-    for k, it in enumerate(items):
-        t[8 + 8 * mt + 8 * k: 8 + 8 * mt + 8 * k + 5] = it
+    t = cluster_tile_list(tiles_per_expert, lambda j: 128 - 5 * j)
     A = torch.from_numpy(q).to(dev)
     A_sf = torch.from_numpy(pack_sf_atoms(sf)).to(dev)
     Wd = torch.from_numpy(W).to(dev)
@@ -150,3 +158,39 @@ def test_cluster_pair_gemm_equals_single_cta(dev, op):
             nvalid = t[8 + 8 * i0 + 2]
             assert torch.equal(res[0][128 * i0: 128 * i0 + nvalid],
                                b[128 * i0: 128 * i0 + nvalid]), i0
+
+
+@pytest.mark.parametrize("k", [768, 4352])
+@pytest.mark.parametrize("pairs", [0, 1, 2])
+def test_weight_scale_bytes_per_block(dev, pairs, k):
+    """Weight scale bytes drawn per 128x128 block over 21 binades, K of 6 and 34
+    k-blocks: the down GEMM still equals the fp64 product of the dequantised operands
+    in every scheduling mode (a scale atom read for the wrong block, k-block or row
+    half moves an output by a power of two)."""
+    tiles_per_expert = [2, 3, 1]
+    E, n = len(tiles_per_expert), 512
+    mt = sum(tiles_per_expert)
+    rows = 128 * mt
+    q, sf = activations(rows, k, 11)
+    W = np.stack([inputs.make_fp8_matrix(n, k, (12, 3, e))[0] for e in range(E)])
+    Wsf = np.random.default_rng(13).integers(117, 138, (E, n // 128, k // 128)).astype(np.uint8)
+    t = cluster_tile_list(tiles_per_expert, lambda j: 128)
+    st = api.new_status(dev)
+    out = api.grouped_gemm_fp8(api.GEMM_DOWN, torch.from_numpy(q).to(dev),
+                               torch.from_numpy(pack_sf_atoms(sf)).to(dev),
+                               torch.from_numpy(W).to(dev),
+                               api.pack_weight_scales(torch.from_numpy(Wsf).to(dev)),
+                               torch.from_numpy(t).to(dev), mt, status=st, pair_tiles=pairs)
+    torch.cuda.synchronize()
+    assert api.read_status(st) == 0
+    got = oracle.bf16_to_f32(bits(out)).astype(np.float64)
+    a = oracle.dequant_rows(q, sf)
+    r0 = 0
+    for e, c in enumerate(tiles_per_expert):
+        m = slice(r0, r0 + 128 * c)
+        ref = a[m] @ oracle.dequant_blocks(W[e], Wsf[e]).T
+        refb = oracle.bf16_to_f32(oracle.f32_to_bf16(ref.astype(np.float32))).astype(np.float64)
+        # bf16 rounding of the fp32 sum, plus fp32 accumulation error growing ~ sqrt(k)
+        tol = np.abs(refb) * 2.0 ** -7 + 2e-6 * np.sqrt(k / 768) * np.abs(ref).max()
+        assert np.all(np.abs(got[m] - refb) <= tol), e
+        r0 += 128 * c

@@ -293,6 +293,47 @@ def test_layouts_and_eplb_agree_bitwise(dev):
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
 
 
+def planned_map(cfg, idx_host, seed_shift=0, max_rep=4):
+    """An EPLB map from the planner (the reduced EPLB workload on 2 nodes x 2 GPUs) for
+    the recorded loads with the hottest expert's load x50, so it gets max_rep copies."""
+    load = oracle.expert_counts(idx_host, cfg.N).astype(np.int64)
+    load[np.argmax(load)] *= 50
+    if seed_shift:
+        load = np.roll(load, seed_shift)
+    return api.eplb_plan(load, cfg.N, cfg.N_phys, cfg.n_group, 2, 4, max_rep)[0]
+
+
+def test_dispatch_with_planned_replicas_bit_exact(dev):
+    """Up to four replicas per expert (log2phys of four columns): the same rows,
+    slots, counts and bytes as the oracle's dispatch with that map."""
+    cfg, x, W, bias = host_workload("small_eplb")
+    idx, _ = oracle.route(x, W, bias, cfg)
+    emap = planned_map(cfg, idx)
+    assert emap[1].max() == 4
+    ref = oracle.dispatch(x, idx, cfg, emap[0], emap[1])
+    d = api.dispatch(cfg, bf16_dev(x), to_dev(idx), to_dev(emap[0]), to_dev(emap[1]))
+    torch.cuda.synchronize()
+    assert api.read_status(d["status"]) == 0
+    check_dispatch(cfg, x, idx, d, ref)
+
+
+def test_layer_with_planned_eplb_and_map_swap_matches_no_eplb(dev):
+    """Planned replicas read their logical expert's weights, so the layer output is
+    the same bytes as without EPLB, before and after installing a new map."""
+    base = configs.SMALL_EPLB
+    cfg, x, W, bias = host_workload("small_eplb")
+    ex = host_experts("small_eplb")
+    idx, _ = oracle.route(x, W, bias, cfg)
+    ref = run_layer(base.with_(n_phys=0), x, W, bias, ex, None)[1]
+    lay, out = run_layer(base, x, W, bias, ex, planned_map(base, idx))
+    assert np.array_equal(out, ref)
+    lay.set_eplb_map(planned_map(base, idx, seed_shift=5))
+    out2 = bits(lay.forward())
+    torch.cuda.synchronize()
+    assert api.read_status(lay.status) == 0
+    assert np.array_equal(out2, ref)
+
+
 @pytest.mark.parametrize("pairs", [1, 2])
 @pytest.mark.parametrize("name", ["small_contig", "small_eplb", "small_sbo"])
 def test_layer_with_cluster_pairs_matches_single_cta(dev, name, pairs):
