@@ -94,6 +94,8 @@ SIGNATURES = {
     "moe_num_sms": (_c_int, []),
     "moe_layer_forward": (_c_int, [ctypes.POINTER(Layer), _vp]),
     "moe_layer_forward_host": (_c_int, [ctypes.POINTER(Layer), _vp, _vp, _vp]),
+    "moe_layer_forward_host_pipelined": (_c_int, [ctypes.POINTER(Layer), _vp, _vp, _vp, _vp,
+                                                  _c_int, _vp, _vp]),
     "moe_layer_graph_create": (_c_int, [ctypes.POINTER(Layer), _vp, _vp, _vp,
                                         ctypes.POINTER(ctypes.c_void_p)]),
     "moe_layer_graph_launch": (_c_int, [_vp, _vp]),

@@ -351,6 +351,27 @@ class MoELayer:
                                             ptr(out_host), stream_ptr(stream)),
               "moe_layer_forward_host")
 
+    def forward_host_pipelined(self, x_hosts, out_hosts, stream=None, copy_stream=None) -> None:
+        """moe_layer_forward_host_pipelined: len(x_hosts) steps, each copying x_hosts[i]
+        (pinned bf16 [B][H]) in and the output to out_hosts[i] (pinned), the copies of
+        neighbouring steps on ``copy_stream`` overlapping the layer on ``stream``.  The
+        second pair of device buffers is allocated on first use."""
+        n = len(x_hosts)
+        if n != len(out_hosts) or n < 1:
+            raise ValueError("one output buffer per input batch")
+        if getattr(self, "_x2", None) is None:
+            self._x2 = torch.empty_like(self.x)
+            self._out2 = torch.empty_like(self.out)
+        if copy_stream is None:
+            if getattr(self, "_copy_stream", None) is None:
+                self._copy_stream = torch.cuda.Stream(device=self.x.device)
+            copy_stream = self._copy_stream
+        xs = (ctypes.c_void_p * n)(*[ptr(t) for t in x_hosts])
+        outs = (ctypes.c_void_p * n)(*[ptr(t) for t in out_hosts])
+        check(load().moe_layer_forward_host_pipelined(
+            ctypes.byref(self.layer), ptr(self._x2), ptr(self._out2), xs, outs, n,
+            stream_ptr(stream), stream_ptr(copy_stream)), "moe_layer_forward_host_pipelined")
+
 
 class LayerGraph:
     """One captured layer call (moe_layer_graph_create), replayed by launch().

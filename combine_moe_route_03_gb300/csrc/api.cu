@@ -207,6 +207,78 @@ extern "C" int moe_layer_forward_host(const moe_layer *L, const void *x_host, vo
   return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
 }
 
+// Copies of neighbouring steps overlapped with the layer ("Large-scale EP ...", §TBO:
+// data movement hidden behind the other batch's computation).  Per step i (buffer
+// b = i % 2): stream waits for x(i) and for out(i-2)'s copy, runs the layer, records
+// done(i); copy_stream then copies x(i+1) in (after done(i-1): the last reader of
+// that input buffer) and out(i) back (after done(i)).
+extern "C" int moe_layer_forward_host_pipelined(const moe_layer *L, void *x2, void *out2,
+                                                const void *const *x_host,
+                                                void *const *out_host, int n_steps,
+                                                void *stream, void *copy_stream) {
+  if (!L || !x2 || !out2 || !x_host || !out_host || n_steps < 1 || !copy_stream ||
+      copy_stream == stream)
+    return MOE_ERR_INVALID;
+  for (int i = 0; i < n_steps; ++i)
+    if (!x_host[i] || !out_host[i]) return MOE_ERR_INVALID;
+  const size_t bytes = (size_t)L->route.B * L->route.H * 2;
+  cudaStream_t st = as_stream(stream), cs = as_stream(copy_stream);
+  void *xd[2] = {L->x, x2}, *od[2] = {L->out, out2};
+  cudaEvent_t in_ready[2], done[2], out_copied[2];
+  bool made[3][2] = {};
+  cudaError_t e = cudaSuccess;
+  int rc = MOE_OK;
+  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+    if ((e = cudaEventCreateWithFlags(&in_ready[b], cudaEventDisableTiming)) == cudaSuccess)
+      made[0][b] = true;
+    if (e == cudaSuccess &&
+        (e = cudaEventCreateWithFlags(&done[b], cudaEventDisableTiming)) == cudaSuccess)
+      made[1][b] = true;
+    if (e == cudaSuccess &&
+        (e = cudaEventCreateWithFlags(&out_copied[b], cudaEventDisableTiming)) == cudaSuccess)
+      made[2][b] = true;
+  }
+  // copy_stream starts after the work already on stream (the caller's inputs may
+  // have been prepared there)
+  if (e == cudaSuccess) e = cudaEventRecord(done[1], st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, done[1], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(xd[0], x_host[0], bytes, cudaMemcpyHostToDevice, cs);
+  if (e == cudaSuccess) e = cudaEventRecord(in_ready[0], cs);
+  for (int i = 0; e == cudaSuccess && i < n_steps; ++i) {
+    const int b = i & 1;
+    if ((e = cudaStreamWaitEvent(st, in_ready[b], 0)) != cudaSuccess) break;
+    if (i >= 2 && (e = cudaStreamWaitEvent(st, out_copied[b], 0)) != cudaSuccess) break;
+    moe_layer Lc = *L;
+    Lc.x = xd[b];
+    Lc.out = od[b];
+    if ((rc = moe_layer_forward(&Lc, stream))) break;
+    if ((e = cudaEventRecord(done[b], st)) != cudaSuccess) break;
+    if (i + 1 < n_steps) {  // the next input, into the buffer step i-1 read
+      if (i >= 1 && (e = cudaStreamWaitEvent(cs, done[b ^ 1], 0)) != cudaSuccess) break;
+      if ((e = cudaMemcpyAsync(xd[b ^ 1], x_host[i + 1], bytes, cudaMemcpyHostToDevice, cs)) !=
+          cudaSuccess)
+        break;
+      if ((e = cudaEventRecord(in_ready[b ^ 1], cs)) != cudaSuccess) break;
+    }
+    if ((e = cudaStreamWaitEvent(cs, done[b], 0)) != cudaSuccess) break;
+    if ((e = cudaMemcpyAsync(out_host[i], od[b], bytes, cudaMemcpyDeviceToHost, cs)) !=
+        cudaSuccess)
+      break;
+    if ((e = cudaEventRecord(out_copied[b], cs)) != cudaSuccess) break;
+  }
+  // stream follows the last copy (whatever was enqueued)
+  if (made[2][0]) {
+    cudaError_t e2 = cudaEventRecord(out_copied[0], cs);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, out_copied[0], 0);
+    if (e == cudaSuccess) e = e2;
+  }
+  for (int k = 0; k < 3; ++k)
+    for (int b = 0; b < 2; ++b)
+      if (made[k][b]) cudaEventDestroy(k == 0 ? in_ready[b] : k == 1 ? done[b] : out_copied[b]);
+  if (rc) return rc;
+  return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
+}
+
 // Whole-layer CUDA graph ("Large-scale EP ...", §DeepEP: fixed shapes make decode
 // replayable as a graph, which keeps launch overhead off each step).  Every call of
 // the layer is stream work with no host synchronisation, so it captures as is.

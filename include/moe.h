@@ -414,6 +414,26 @@ int moe_layer_forward_host(const moe_layer *layer, const void *x_host, void *out
                            void *stream);
 
 /*
+ * n_steps layer passes over host batches, the copies overlapped with the kernels
+ * ("Large-scale EP ...", §TBO: hide data movement behind the other batch's
+ * computation, here the host<->device copies of neighbouring steps): step i copies
+ * x_host[i] (pinned, bf16 [B][H]) in, runs the layer and copies out to out_host[i]
+ * (pinned).  Device input and output buffers alternate between layer->x / layer->out
+ * (even steps) and x2 / out2 (odd steps; same sizes, caller-owned).  The copies run on
+ * copy_stream (a created stream other than `stream`): step i+1's input is copied
+ * while step i computes, step i's output while step i+1 computes; events order a
+ * buffer's reuse after its last reader.  On return everything is enqueued and
+ * `stream` waits for the last copy, so work or an event recorded on `stream`
+ * afterwards follows all n steps.  x_host / out_host entries may repeat (copies to
+ * one host buffer are ordered on copy_stream).
+ * Errors: MOE_ERR_INVALID for NULL arguments, n_steps < 1, or copy_stream equal to
+ * stream; a failing layer call returns its code (work already enqueued stays).
+ */
+int moe_layer_forward_host_pipelined(const moe_layer *layer, void *x2, void *out2,
+                                     const void *const *x_host, void *const *out_host,
+                                     int n_steps, void *stream, void *copy_stream);
+
+/*
  * Whole-layer CUDA graph ("Large-scale EP: DeepEP, EPLB and two-batch overlap",
  * §DeepEP: each mode where it belongs -- the fixed-shape low-latency path is the
  * one decode replays as a CUDA graph to keep launch overhead off each step).

@@ -334,6 +334,33 @@ def test_layer_with_planned_eplb_and_map_swap_matches_no_eplb(dev):
     assert np.array_equal(out2, ref)
 
 
+@pytest.mark.parametrize("name", ["small_masked", "small_sbo"])
+def test_pipelined_host_steps_match_forward_host(dev, name):
+    """Five host batches through the pipelined entry point (copies of neighbouring
+    steps overlapping the layer, two device buffer pairs alternating) give each batch
+    the bytes of a plain host-buffer call; inputs and outputs never cross steps."""
+    cfg, x, W, bias = host_workload(name)
+    ex = host_experts(name)
+    lay = api.MoELayer(cfg, to_dev(W), to_dev(bias), device_weights(ex))
+    rng = np.random.default_rng(5)
+    batches = [x] + [np.ascontiguousarray(x[rng.permutation(cfg.B)]) for _ in range(4)]
+    xh = [torch.from_numpy(b).view(torch.bfloat16).pin_memory() for b in batches]
+    ref = []
+    for h in xh:
+        o = torch.empty_like(h).pin_memory()
+        lay.forward_host(h, o)
+        torch.cuda.synchronize()
+        ref.append(o.view(torch.int16).numpy().copy())
+    st = torch.cuda.Stream()
+    outs = [torch.zeros_like(h).pin_memory() for h in xh]
+    lay.forward_host_pipelined(xh, outs, stream=st)
+    torch.cuda.synchronize()
+    assert api.read_status(lay.status) == 0
+    for i in range(len(xh)):
+        assert np.array_equal(outs[i].view(torch.int16).numpy(), ref[i]), i
+    assert not np.array_equal(ref[0], ref[1])   # the batches differ
+
+
 @pytest.mark.parametrize("pairs", [1, 2])
 @pytest.mark.parametrize("name", ["small_contig", "small_eplb", "small_sbo"])
 def test_layer_with_cluster_pairs_matches_single_cta(dev, name, pairs):

@@ -98,3 +98,11 @@ def test_host_argument_checks_return_before_launch(L):
                                     ctypes.c_void_p(16), ctypes.byref(h)) == -1  # one host buffer
     assert L.moe_layer_graph_launch(None, None) == -1
     assert L.moe_layer_graph_destroy(None) == 0
+    hx = (ctypes.c_void_p * 2)(16, 16)
+    s1, s2 = ctypes.c_void_p(32), ctypes.c_void_p(48)
+    f = L.moe_layer_forward_host_pipelined
+    assert f(None, s1, s1, hx, hx, 2, s1, s2) == -1                          # no layer
+    assert f(ctypes.byref(lay), s1, s1, hx, hx, 0, s1, s2) == -1             # no steps
+    assert f(ctypes.byref(lay), s1, s1, hx, hx, 2, s1, s1) == -1             # one stream
+    assert f(ctypes.byref(lay), None, s1, hx, hx, 2, s1, s2) == -1           # no 2nd buffer
+    assert f(ctypes.byref(lay), s1, s1, (ctypes.c_void_p * 2)(16, None), hx, 2, s1, s2) == -1
