@@ -12,7 +12,10 @@
 //   route_logits_wide_kernel  the same arithmetic for wide grids: x widened to fp32
 //                        once per CTA, larger per-thread tiles.
 //   route_logits_slice_kernel  256 experts, large batches: a warp owns a slice of
-//                        tokens against all experts, one CTA per SM.
+//                        tokens against all experts, one CTA per SM; each step's W
+//                        and x operands are loaded into registers one step ahead
+//                        (the 8 warps of an SM leave register room, and a load
+//                        right before its FMAs stalled the warp).
 //   route_select_kernel  one warp per token: scores, group scores, top-K with the
 //                        (score desc, index asc) order, weights, expert counts.
 #include <cfloat>
@@ -327,14 +330,29 @@ __global__ void __launch_bounds__(NW * 32, 1) route_logits_slice_kernel(
     __syncthreads();
     const float *wb = ws + (c % S) * WST + lane * LDF;
     const float *xw = xf + warp * TT * LDF;
-#pragma unroll 2
-    for (int k4 = 0; k4 < BK; k4 += 4) {
-      float4 wv[TE];
+    // operands of step k4 + 4 are loaded while step k4's FMAs run
+    float4 wn[TE], xn[TT];
 #pragma unroll
-      for (int j = 0; j < TE; ++j) wv[j] = *reinterpret_cast<const float4 *>(wb + 32 * j * LDF + k4);
+    for (int j = 0; j < TE; ++j) wn[j] = *reinterpret_cast<const float4 *>(wb + 32 * j * LDF);
+#pragma unroll
+    for (int i = 0; i < TT; ++i) xn[i] = *reinterpret_cast<const float4 *>(xw + i * LDF);
+#pragma unroll
+    for (int k4 = 0; k4 < BK; k4 += 4) {
+      float4 wv[TE], xc[TT];
+#pragma unroll
+      for (int j = 0; j < TE; ++j) wv[j] = wn[j];
+#pragma unroll
+      for (int i = 0; i < TT; ++i) xc[i] = xn[i];
+      if (k4 + 4 < BK) {
+#pragma unroll
+        for (int j = 0; j < TE; ++j)
+          wn[j] = *reinterpret_cast<const float4 *>(wb + 32 * j * LDF + k4 + 4);
+#pragma unroll
+        for (int i = 0; i < TT; ++i) xn[i] = *reinterpret_cast<const float4 *>(xw + i * LDF + k4 + 4);
+      }
 #pragma unroll
       for (int i = 0; i < TT; ++i) {
-        const float4 xv = *reinterpret_cast<const float4 *>(xw + i * LDF + k4);  // broadcast
+        const float4 xv = xc[i];  // broadcast
         // k order is strictly sequential for every output
 #pragma unroll
         for (int j = 0; j < TE; ++j) {
