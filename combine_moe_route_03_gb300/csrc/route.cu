@@ -780,6 +780,8 @@ extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W
     rc = launch_logits_wide<8, 8, 3, 32>(xb, W, lg, B, H, N, st);
   else if (2 * ctas(4, 8) >= 3 * sms)
     rc = launch_logits_wide<4, 8, 3, 32>(xb, W, lg, B, H, N, st);
+  else if (B >= 128 && B <= 512 && H % 128 == 0)  // two tokens per thread: ILP for the FMA
+    rc = launch_logits<2, 1, 8, 128>(xb, W, lg, B, H, N, st);  // chains, half the W reads
   else if (B >= 256 && H % 64 == 0)
     rc = launch_logits_wide<2, 2, 4, 64>(xb, W, lg, B, H, N, st);
   else if (ctas(4, 4) >= 4 * sms)
