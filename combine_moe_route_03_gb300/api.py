@@ -109,9 +109,18 @@ class EplbRecorder:
     def due(self) -> bool:
         return self.steps >= self.period
 
-    def plan(self):
-        """The map for the loads recorded so far; the recorder then starts afresh."""
-        m, bal = eplb_plan(self.load, self.N_log, self.N_phys, **self.plan_kw)
+    def plan(self, group=None):
+        """The map for the loads recorded so far; the recorder then starts afresh.
+
+        With a torch.distributed process group, the ranks' recorded loads are summed
+        first (one all-reduce of N_log counts on the host side), so every rank of the
+        group plans the same map from the whole job's loads."""
+        load = self.load
+        if group is not None:
+            t = torch.from_numpy(self.load.copy())
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM, group=group)
+            load = t.numpy()
+        m, bal = eplb_plan(load, self.N_log, self.N_phys, **self.plan_kw)
         self.load[:] = 0
         self.steps = 0
         return m, bal

@@ -1,4 +1,5 @@
-"""The multi-rank bench path on CPU: two gloo ranks, weak scaling, max over ranks."""
+"""Multi-rank host paths on CPU (two gloo ranks): the bench's weak scaling and max over
+ranks, and EPLB planning from the loads of all ranks."""
 import os
 import socket
 
@@ -46,3 +47,44 @@ def test_single_rank_needs_no_collective():
     import bench
     assert bench.max_over_ranks(3.5, None, None) == 3.5
     assert bench.whole_job_rate(1, 128, 1.0) == 128_000
+
+
+def _eplb_rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import numpy as np
+    from combine_moe_route_03_gb300 import api
+    rec = api.EplbRecorder(32, 40, period=2, n_group=4, n_nodes=2, n_gpus=4, max_rep=4)
+    rng = np.random.default_rng(rank)
+    for _ in range(2):
+        rec.observe(rng.integers(0, 100 * (rank + 1), 32).astype(np.int32))
+    mine = rec.load.copy()
+    m, bal = rec.plan(group=dist.group.WORLD)
+    q.put((rank, mine, [a.tolist() for a in m], bal))
+    dist.destroy_process_group()
+
+
+def test_eplb_plan_from_all_ranks_loads():
+    """Each rank records its own loads; planning sums them across ranks, so both
+    ranks install the same map — the oracle's plan of the summed loads."""
+    import numpy as np
+    from combine_moe_route_03_gb300 import build
+    build.build()
+    from oracle import eplb as oeplb
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_eplb_rank, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted((q.get(timeout=120) for _ in range(world)), key=lambda r: r[0])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    total = res[0][1] + res[1][1]
+    ref, rbal = oeplb.plan(total, 32, 40, 4, 2, 4, 4)
+    for _, _, m, bal in res:
+        assert m[0] == ref[0] and m[1] == ref[1] and m[2] == ref[2]
+        assert abs(bal - rbal) < 1e-12
+    assert not np.array_equal(res[0][1], res[1][1])   # the ranks saw different loads
