@@ -169,6 +169,60 @@ def test_empty_batch(dev):
     assert d["tiles"][0].item() == 0 and int(d["counts"].sum()) == 0
 
 
+@pytest.mark.parametrize("B", [1, 37, 300])
+def test_route_at_the_largest_expert_count(dev, B):
+    """512 experts in 8 groups of 64, top-3 groups, K = 16 (the largest K), sigmoid +
+    bias: logits, ids, weights and counts bit-exact, for one token, a ragged batch and
+    a wider one."""
+    cfg = configs.MoEConfig("n512", B=B, H=512, N=512, K=16, I=128, n_group=8, topk_group=3,
+                            score_fn=configs.SIGMOID, renorm=1, route_scale=2.5,
+                            bias_init="normal", seed=9)
+    x = inputs.make_x(cfg)
+    W, bias = inputs.make_router(cfg)
+    r = api.route(cfg, bf16_dev(x), to_dev(W), to_dev(bias))
+    torch.cuda.synchronize()
+    idx, w, lg = oracle.route(x, W, bias, cfg, want_logits=True)
+    got_lg = r["logits"][: B * cfg.N * 4].view(torch.float32).cpu().numpy().reshape(B, cfg.N)
+    assert np.array_equal(got_lg.view(np.uint32), lg.view(np.uint32))
+    assert np.array_equal(r["topk_idx"].cpu().numpy(), idx)
+    assert np.array_equal(r["topk_w"].cpu().numpy().view(np.uint32), w.view(np.uint32))
+    assert np.array_equal(r["counts"].cpu().numpy(), oracle.expert_counts(idx, cfg.N))
+
+
+@pytest.mark.parametrize("layout", [configs.CONTIG, configs.MASKED])
+def test_dispatch_at_the_largest_physical_expert_count(dev, layout):
+    """1024 physical experts (the scan's limit) behind 512 logical ones with an EPLB
+    map of two columns, K = 16: rows, slots, tile list and bytes as the oracle's."""
+    cfg = configs.MoEConfig("p1024", B=300, H=256, N=512, K=16, I=128, n_phys=1024,
+                            layout=layout, cap=128, seed=3)
+    rng = np.random.default_rng(4)
+    x = inputs.make_x(cfg)
+    idx = np.stack([rng.choice(cfg.N, cfg.K, replace=False) for _ in range(cfg.B)]).astype(np.int32)
+    emap = oracle.eplb_build_map(oracle.expert_counts(idx, cfg.N), cfg.N, cfg.N_phys)
+    ref = oracle.dispatch(x, idx, cfg, emap[0], emap[1])
+    d = api.dispatch(cfg, bf16_dev(x), to_dev(idx), to_dev(emap[0]), to_dev(emap[1]))
+    torch.cuda.synchronize()
+    assert api.read_status(d["status"]) == 0
+    check_dispatch(cfg, x, idx, d, ref)
+
+
+def test_single_token_layer(dev):
+    """B = 1 through the whole layer (one row per chosen expert, the shared expert's
+    single row, a 128-row tile holding one valid row each)."""
+    name = "small_masked"
+    cfg, x, W, bias = host_workload(name)
+    cfg1 = cfg.with_(B=1, shared=True)
+    x1 = np.ascontiguousarray(x[:1])
+    ex = host_experts(name)
+    if "W13s" not in ex:
+        s = inputs.make_shared_expert(cfg1)
+        ex = dict(ex, W13s=s[0], W13s_sf=s[1], W2s=s[2], W2s_sf=s[3])
+    lay, out = run_layer(cfg1, x1, W, bias, ex, None)
+    ref = oracle.layer_tokens(cfg1, x1, W, bias, getter(ex), shared_of(ex))
+    ok, err, bound = within_tol(oracle.bf16_to_f32(out), oracle.bf16_to_f32(ref["out"]))
+    assert ok, (err, bound)
+
+
 # ----------------------------------------------------------------- combine
 @pytest.mark.parametrize("name", ["small_contig", "small_masked", "decode"])
 def test_combine_bit_exact(dev, name):
