@@ -389,7 +389,10 @@ def main():
                         "hbm_frac": round(work[s]["bytes"] / d / 1e9 / pk["hbm"], 3),
                         "TFLOPs": round(work[s]["flops"] / d / 1e12, 1)}
 
-    launches_per_step = 2 + 3 + 2 + 1
+    # route (logits, select), dispatch (count + scan fused into one launch for a
+    # batch of one 128-token chunk, then scatter), gate/up, down, combine
+    fused = cfg.B <= 128 and 4 * (8 * cfg.N_phys + 2 * 128 * cfg.K) <= 24 * 1024
+    launches_per_step = 2 + (2 if fused else 3) + 2 + 1
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",

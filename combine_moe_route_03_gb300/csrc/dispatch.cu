@@ -51,16 +51,22 @@ __host__ __device__ inline DispatchWs carve(void *ws, int B, int K, int N_phys) 
   return w;
 }
 
-__global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
-    const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ log2phys,
-    const int32_t *__restrict__ rep, int max_rep, int B, int K, int N_log, int N_phys,
-    DispatchWs ws, int32_t *status) {
-  extern __shared__ int32_t sm[];
+// Counts of one kChunk-token chunk: each (t, k) pair's physical expert and its rank
+// among the chunk's pairs of that expert (ascending (t, k)); the chunk's per-expert
+// totals go to ws.hist.  kCountWarps warps do the work; a larger block calls it too
+// (every thread reaches the barriers, warps past kCountWarps get no pairs).  sm:
+// kCountWarps * N_phys + 2 * kChunk * K ints of shared memory.
+__device__ __forceinline__ void count_chunk(int chunk, const int32_t *__restrict__ topk_idx,
+                                            const int32_t *__restrict__ log2phys,
+                                            const int32_t *__restrict__ rep, int max_rep,
+                                            int B, int K, int N_log, int N_phys,
+                                            const DispatchWs &ws, int32_t *status,
+                                            int32_t *sm) {
   int32_t *whist = sm;                              // [kCountWarps][N_phys]
   int32_t *pp = whist + kCountWarps * N_phys;       // [kChunk*K]
   int32_t *lr = pp + kChunk * K;                    // [kChunk*K]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t_begin = blockIdx.x * kChunk;
+  const int t_begin = chunk * kChunk;
   const int ntok = min(kChunk, B - t_begin);
   const int npairs = ntok * K;
   for (int i = tid; i < kCountWarps * N_phys; i += blockDim.x) whist[i] = 0;
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
       whist[w * N_phys + p] = run;
       run += v;
     }
-    ws.hist[(size_t)blockIdx.x * N_phys + p] = run;
+    ws.hist[(size_t)chunk * N_phys + p] = run;
   }
   __syncthreads();
   for (int i = tid; i < npairs; i += blockDim.x) {
@@ -119,6 +125,15 @@ __global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
     ws.phys[(size_t)t_begin * K + i] = p;
     ws.rank[(size_t)t_begin * K + i] = p >= 0 ? whist[w * N_phys + p] + lr[i] : -1;
   }
+}
+
+__global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
+    const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ log2phys,
+    const int32_t *__restrict__ rep, int max_rep, int B, int K, int N_log, int N_phys,
+    DispatchWs ws, int32_t *status) {
+  extern __shared__ int32_t sm[];
+  count_chunk(blockIdx.x, topk_idx, log2phys, rep, max_rep, B, K, N_log, N_phys, ws, status,
+              sm);
 }
 
 // Inclusive block-wide scan (Hillis-Steele) of one value per thread.
@@ -186,10 +201,20 @@ __device__ __forceinline__ void write_items(int32_t *items, int first, int nt, i
   }
 }
 
+// With a single chunk (small batches) the count runs here first, in this block
+// (fused = 1, count_chunk's shared memory as the launch's dynamic shared memory): one
+// launch and one round trip of the counts through global memory fewer.
 __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     int B, int N_phys, int nchunks, int layout, int cap, int64_t rows_alloc, DispatchWs ws,
     int32_t *__restrict__ counts, int32_t *__restrict__ tiles, int32_t *__restrict__ src_of,
-    int32_t *__restrict__ shared_tiles, int32_t *status) {
+    int32_t *__restrict__ shared_tiles, int32_t *status, int fused,
+    const int32_t *__restrict__ topk_idx, const int32_t *__restrict__ log2phys,
+    const int32_t *__restrict__ rep, int max_rep, int K, int N_log) {
+  if (fused) {
+    extern __shared__ int32_t sm[];
+    count_chunk(0, topk_idx, log2phys, rep, max_rep, B, K, N_log, N_phys, ws, status, sm);
+    __syncthreads();  // ws.hist / phys / rank of the chunk, written by this block
+  }
   __shared__ int32_t scan[kScanThreads / 32];
   __shared__ int32_t single_tile[kScanThreads];
   __shared__ int32_t pad_seg[kScanThreads], pad_from[kScanThreads], pad_to[kScanThreads];
@@ -432,6 +457,35 @@ inline int scatter_cpt(int B, int H, int cols) {
   return (int)(cpt < 1 ? 1 : (cpt > nch ? nch : cpt));
 }
 
+// The count and scan launches of both dispatch entry points: one fused launch when
+// the batch is a single chunk and the count's shared memory fits beside the scan's.
+int launch_count_scan(const moe_dispatch_cfg *c, int B, int K, int Np, int nchunks,
+                      const int32_t *topk_idx, const int32_t *log2phys, const int32_t *rep,
+                      const DispatchWs &ws, int32_t *counts, int32_t *tiles, int32_t *src_of,
+                      int32_t *shared_tiles, int32_t *status, cudaStream_t st) {
+  const int max_rep = c->max_rep ? c->max_rep : 2;
+  const size_t smem = sizeof(int32_t) * ((size_t)kCountWarps * Np + 2 * kChunk * K);
+  if (nchunks == 1 && smem <= 24 * 1024) {
+    dispatch_scan_kernel<<<1, kScanThreads, smem, st>>>(
+        B, Np, nchunks, c->layout, c->cap, moe_dispatch_rows(c), ws, counts, tiles, src_of,
+        shared_tiles, status, 1, topk_idx, log2phys, rep, max_rep, K, c->N_log);
+    return check_launch();
+  }
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(dispatch_count_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  dispatch_count_kernel<<<nchunks, kCountWarps * 32, smem, st>>>(
+      topk_idx, log2phys, rep, max_rep, B, K, c->N_log, Np, ws, status);
+  int rc = check_launch();
+  if (rc) return rc;
+  dispatch_scan_kernel<<<1, kScanThreads, 0, st>>>(
+      B, Np, nchunks, c->layout, c->cap, moe_dispatch_rows(c), ws, counts, tiles, src_of,
+      shared_tiles, status, 0, nullptr, nullptr, nullptr, 0, 0, 0);
+  return check_launch();
+}
+
 // The scatter launch of both dispatch entry points: fp8 rows in 512-column chunks
 // (16-byte stores per lane and copy) when H allows, else 256.
 int launch_scatter(const moe_dispatch_cfg *c, int B, int K, int Np, const void *x,
@@ -522,19 +576,9 @@ extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int3
     return MOE_ERR_INVALID;
   const int nchunks = (B + kChunk - 1) / kChunk;
   DispatchWs ws = carve(workspace, B, K, Np);
-  const size_t smem = sizeof(int32_t) * ((size_t)kCountWarps * Np + 2 * kChunk * K);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(dispatch_count_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return set_cuda_error(e);
-  }
-  dispatch_count_kernel<<<nchunks, kCountWarps * 32, smem, st>>>(
-      topk_idx, log2phys, rep, c->max_rep ? c->max_rep : 2, B, K, c->N_log, Np, ws, status);
-  if ((rc = check_launch())) return rc;
-  dispatch_scan_kernel<<<1, kScanThreads, 0, st>>>(B, Np, nchunks, c->layout, c->cap,
-                                                   moe_dispatch_rows(c), ws, counts, tiles,
-                                                   src_of, shared_tiles, status);
-  if ((rc = check_launch())) return rc;
+  if ((rc = launch_count_scan(c, B, K, Np, nchunks, topk_idx, log2phys, rep, ws, counts, tiles,
+                              src_of, shared_tiles, status, st)))
+    return rc;
   return launch_scatter(c, B, K, Np, x, ws, A, A_sf, row_of, src_of, A_shared, A_shared_sf, st);
 }
 
@@ -601,18 +645,8 @@ extern "C" int moe_dispatch_noalloc(const moe_dispatch_cfg *c, const void *x,
   if ((rc = scratch_address(&scratch))) return rc;
   const int nchunks = (B + kChunk - 1) / kChunk;
   DispatchWs ws = carve(scratch, B, K, Np);
-  const size_t smem = sizeof(int32_t) * ((size_t)kCountWarps * Np + 2 * kChunk * K);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(dispatch_count_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return set_cuda_error(e);
-  }
-  dispatch_count_kernel<<<nchunks, kCountWarps * 32, smem, st>>>(
-      topk_idx, log2phys, rep, c->max_rep ? c->max_rep : 2, B, K, c->N_log, Np, ws, status);
-  if ((rc = check_launch())) return rc;
-  dispatch_scan_kernel<<<1, kScanThreads, 0, st>>>(B, Np, nchunks, c->layout, c->cap,
-                                                   moe_dispatch_rows(c), ws, counts, tiles,
-                                                   src_of, shared_tiles, status);
-  if ((rc = check_launch())) return rc;
+  if ((rc = launch_count_scan(c, B, K, Np, nchunks, topk_idx, log2phys, rep, ws, counts, tiles,
+                              src_of, shared_tiles, status, st)))
+    return rc;
   return launch_scatter(c, B, K, Np, x, ws, A, A_sf, row_of, src_of, A_shared, A_shared_sf, st);
 }
