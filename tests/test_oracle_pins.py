@@ -312,6 +312,28 @@ def test_dispatch_invariants(name):
     l2p = rep = None
     if cfg.N_phys != cfg.N:
         l2p, rep, _ = oracle.eplb_build_map(oracle.expert_counts(idx, cfg.N), cfg.N, cfg.N_phys)
+    check_dispatch(cfg, x, idx, l2p, rep)
+
+
+@pytest.mark.parametrize("layout", [configs.CONTIG, configs.MASKED])
+def test_dispatch_invariants_with_planned_replicas(layout):
+    """A planned map with up to 4 replicas per expert (4 columns in log2phys): token t
+    of logical expert e lands on replica t mod rep[e] and every other invariant holds.
+    The skewed loads make the planner give the hottest experts 3 or 4 replicas."""
+    from oracle import eplb as oeplb
+    cfg = configs.SMALL_EPLB.with_(layout=layout, cap=512 if layout else 0, n_phys=56)
+    x = inputs.make_x(cfg)
+    W, bias = inputs.make_router(cfg)
+    idx, _ = oracle.route(x, W, bias, cfg)
+    load = oracle.expert_counts(idx, cfg.N).astype(np.int64)
+    load[int(np.argmax(load))] *= 50
+    (l2p, rep, _), _ = oeplb.plan(load, cfg.N, cfg.N_phys, n_group=cfg.n_group, max_rep=4)
+    l2p, rep = np.asarray(l2p, np.int32), np.asarray(rep, np.int32)
+    assert l2p.shape == (cfg.N, 4) and rep.max() >= 3
+    check_dispatch(cfg, x, idx, l2p, rep)
+
+
+def check_dispatch(cfg, x, idx, l2p, rep):
     d = oracle.dispatch(x, idx, cfg, l2p, rep)
     B, K = idx.shape
     assert d["cnt"].sum() == B * K
