@@ -392,6 +392,36 @@ def test_identity_expert_combine_is_weighted_sum():
     assert np.allclose(out, ref, rtol=2 ** -7, atol=1e-6)     # one bf16 rounding
 
 
+def test_combine_exact_sum_with_shared_and_dropped_rows():
+    """Integer rows, power-of-two weights and an integer shared-expert row make every fp32
+    partial sum exact, so out[t] must be bf16-RNE (torch) of the exact sum of w * Y over
+    the rows that token t's row_of names (scattered, some dropped), plus S[t] once."""
+    rng = np.random.default_rng(16)
+    B, K, H = 24, 3, 128
+    rows = B * K + 5
+    Yv = rng.integers(-600, 600, (rows, H)).astype(np.float32)      # beyond bf16's 8 bits
+    Sv = rng.integers(-600, 600, (B, H)).astype(np.float32)
+    Yv = torch.from_numpy(Yv).bfloat16().float().numpy()              # bf16-exact inputs
+    Sv = torch.from_numpy(Sv).bfloat16().float().numpy()
+    to_bits = lambda a: torch.from_numpy(a).bfloat16().view(torch.int16).numpy().view(np.uint16)
+    row_of = rng.permutation(rows)[: B * K].reshape(B, K).astype(np.int32)
+    row_of[rng.random((B, K)) < 0.15] = -1                            # dropped copies
+    w = (2.0 ** rng.integers(-3, 3, (B, K))).astype(np.float32)
+    for S in (None, Sv):
+        out = oracle.bf16_to_f32(oracle.combine(to_bits(Yv), row_of, w,
+                                                None if S is None else to_bits(S)))
+        ref = np.zeros((B, H))
+        for t in range(B):
+            for k in range(K):
+                if row_of[t, k] >= 0:
+                    ref[t] += float(w[t, k]) * Yv[row_of[t, k]].astype(np.float64)
+            if S is not None:
+                ref[t] += S[t]
+        assert np.all(np.abs(ref) < 2 ** 24)                          # exact in fp32
+        want = torch.from_numpy(ref.astype(np.float32)).bfloat16().float().numpy()
+        assert np.array_equal(out, want)
+
+
 # ----------------------------------------------------------------------------- FFN
 def _tiny_expert(rng, H=128, I=128):
     W13, W13_sf = inputs.make_fp8_matrix(2 * I, H, (int(rng.integers(1 << 30)), 99, 0))
