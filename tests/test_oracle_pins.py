@@ -471,6 +471,43 @@ def test_ffn_scaling_invariants():
     assert np.all(oracle.bf16_to_f32(oracle.expert_ffn(q, sf, W13z, W13_sf, W2, W2_sf)) == 0)
 
 
+def test_layer_composition_by_power_of_two_experts():
+    """Expert e is one base expert with its down scale raised by s[e], so its output for
+    token t is exactly 2^s[e] y_t, y_t the base output (power-of-two scales act exactly);
+    the shared expert is the base with scale +1, i.e. 2 y_t.  The whole layer must equal
+    the combine of rows y_t with weights w[t,k] 2^s[idx[t,k]] (also exact), token by
+    token: a wrong expert, token or weight pairing in the gather or scatter breaks it.
+    Dropped copies leave their term out."""
+    rng = np.random.default_rng(17)
+    cfg = _tiny_cfg(B=40, H=256, N=16, K=4, n_group=4, topk_group=2, score_fn=configs.SIGMOID,
+                    renorm=1, route_scale=2.5)
+    x = inputs.bf16_bits(rng.standard_normal((cfg.B, cfg.H)).astype(np.float32))
+    W = (rng.standard_normal((cfg.N, cfg.H)) * 0.1).astype(np.float32)
+    bias = (rng.standard_normal(cfg.N) * 0.1).astype(np.float32)
+    W13, W13_sf, W2, W2_sf = _tiny_expert(rng, H=256, I=128)
+    shift = rng.integers(0, 4, cfg.N)
+    up = lambda d: (W2_sf.astype(np.int64) + int(d)).astype(np.uint8)
+    get = lambda e: (W13, W13_sf, W2, up(shift[e]))
+    q, sf = oracle.quantize_rows(oracle.bf16_to_f32(x))
+    y = oracle.expert_ffn(q, sf, W13, W13_sf, W2, W2_sf)
+    two_y = oracle.expert_ffn(q, sf, W13, W13_sf, W2, up(1))
+    assert np.array_equal(oracle.bf16_to_f32(two_y), 2 * oracle.bf16_to_f32(y))
+    idx, w = oracle.route(x, W, bias, cfg)
+    assert len(np.unique(shift[idx])) > 1
+    w_scaled = (w * 2.0 ** shift[idx]).astype(np.float32)
+    tok_rows = np.repeat(np.arange(cfg.B, dtype=np.int32)[:, None], cfg.K, 1)
+    dropped = rng.random((cfg.B, cfg.K)) < 0.2
+    for drop in (None, dropped):
+        got = oracle.layer_tokens(cfg, x, W, bias, get, shared=(W13, W13_sf, W2, up(1)),
+                                  dropped=drop)
+        assert np.array_equal(got["topk_idx"], idx)
+        ro = tok_rows if drop is None else np.where(drop, -1, tok_rows).astype(np.int32)
+        assert np.array_equal(got["out"], oracle.combine(y, ro, w_scaled, two_y))
+    sub = [5, 0, 39, 17]                     # a token list gives those tokens' rows
+    got = oracle.layer_tokens(cfg, x, W, bias, get, shared=(W13, W13_sf, W2, up(1)), tokens=sub)
+    assert np.array_equal(got["out"], oracle.combine(y, tok_rows, w_scaled, two_y)[sub])
+
+
 # --------------------------------------------------------------------------- golden
 def test_golden_decode_dispatch_volume():
     """Per-rank decode dispatch volume b*K*H*s printed by the DeepEP page."""
