@@ -195,6 +195,15 @@ def cpu_oracle_rate(cfg, x, W, bias, host, shared, ntok: int, seed: int = 0):
 REF_BUDGET_S = 60.0  # timed oracle seconds the reference arm spends at most (about)
 
 
+def run_config(cfg, world):
+    """The JSON line's `config`, the same for both arms: the reference arm times a
+    sample of this workload (its cpu_baseline says which)."""
+    return {"workload": describe(cfg), "global_batch": world * cfg.B,
+            "parallelism": f"dp{world} (independent batch per GPU)",
+            "l2": "inputs larger than L2: every step streams the touched experts' "
+                  "e4m3 weights (about 11 GB) from HBM"}
+
+
 def run_reference(args, cfg):
     """--impl reference: the CPU oracle on the host cores, one sampled token per step.
 
@@ -242,11 +251,10 @@ def run_reference(args, cfg):
             "steps": n, "requested_steps": args.steps, "warmup": nwarm, "ms_per_step": 1e3 * total / n,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
-            "config": {"workload": describe(cfg), "global_batch": 1,
-                       "step": "one sampled token of the workload through the whole layer"},
+            "config": run_config(cfg, int(os.environ.get("WORLD_SIZE", args.gpus))),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{n} sampled tokens of {cfg.name}, one per step "
-                                       f"({total:.1f} s of oracle time)"},
+                             "sample": f"{n} sampled tokens of {cfg.name}, one per step through the "
+                                       f"whole layer ({total:.1f} s of oracle time)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -412,10 +420,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic (seeded; random-init weights stored as e4m3 + UE8M0 128x128 scales)",
-            "config": {"workload": describe(cfg), "global_batch": world * cfg.B,
-                       "parallelism": f"dp{world} (independent batch per GPU)",
-                       "l2": "inputs larger than L2: every step streams the touched experts' "
-                             "e4m3 weights (about 11 GB) from HBM"},
+            "config": run_config(cfg, world),
             "clocks": clocks, "gpu_launches": launches_per_step * K, "roofline": roof,
             "stages": per_stage, "e2e": e2e}
     if rank == 0 and world == 1 and args.cpu_tokens > 0:

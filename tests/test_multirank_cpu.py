@@ -88,3 +88,17 @@ def test_eplb_plan_from_all_ranks_loads():
         assert m[0] == ref[0] and m[1] == ref[1] and m[2] == ref[2]
         assert abs(bal - rbal) < 1e-12
     assert not np.array_equal(res[0][1], res[1][1])   # the ranks saw different loads
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    """Under torchrun the reference arm's other ranks exit at once, with no output and no
+    process group (rank 0 alone times the oracle and prints the line)."""
+    import argparse
+
+    import bench
+    from combine_moe_route_03_gb300 import configs
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.run_reference(argparse.Namespace(steps=1, warmup=1, gpus=2), configs.DECODE)
+    assert capsys.readouterr().out == ""
+    assert bench.run_config(configs.DECODE, 2)["global_batch"] == 2 * configs.DECODE.B
