@@ -784,8 +784,7 @@ extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W
     rc = launch_logits<2, 1, 8, 128>(xb, W, lg, B, H, N, st);  // chains, half the W reads
   else if (B >= 256 && H % 64 == 0)
     rc = launch_logits_wide<2, 2, 4, 64>(xb, W, lg, B, H, N, st);
-  else if (ctas(4, 4) >= 4 * sms)
-    rc = launch_logits<4, 4, 4, 32>(xb, W, lg, B, H, N, st);
+  // (a <4,4> tile is never reached here: ctas(4, 4) <= 2 * ctas(4, 8) < 3 * sms)
   else if (ctas(2, 2) >= 4 * sms && H % 64 == 0)
     rc = launch_logits<2, 2, 4, 64>(xb, W, lg, B, H, N, st);
   else if (H % 128 == 0)  // small grid: only the in-flight chunks hide the load latency

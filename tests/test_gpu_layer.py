@@ -48,6 +48,29 @@ def test_route_bit_exact_other_group_shapes(dev, N, G, TG, K):
     assert np.array_equal(r["topk_w"].cpu().numpy().view(np.uint32), w.view(np.uint32))
 
 
+@pytest.mark.parametrize("B,N,H", [(10000, 256, 256), (4000, 512, 256), (1000, 256, 256),
+                                   (700, 512, 192), (300, 256, 160), (77, 64, 160)])
+def test_route_logits_kernel_shapes(dev, B, N, H):
+    """The logits kernel is chosen from B, N and H.  On 152 SMs these shapes take, in
+    order: the fp32-widened 8x8 tile past the token-sliced range (256 experts) and at
+    512 experts, the 2x2 tile with 64-wide chunks (H a multiple of 128, and of 64 only),
+    and the 32-wide-chunk kernel (H a multiple of 32 only) for a wide and a ragged
+    batch.  All logits, ids and weights bit-exact."""
+    kw = (dict(n_group=8, topk_group=3, K=16) if N == 512 else
+          dict(n_group=8, topk_group=4, K=8) if N == 256 else dict(n_group=4, topk_group=2, K=6))
+    cfg = configs.MoEConfig("shape", B=B, H=H, N=N, I=128, score_fn=configs.SIGMOID, renorm=1,
+                            route_scale=2.5, bias_init="normal", seed=5, **kw)
+    x = inputs.make_x(cfg)
+    W, bias = inputs.make_router(cfg)
+    r = api.route(cfg, bf16_dev(x), to_dev(W), to_dev(bias))
+    torch.cuda.synchronize()
+    idx, w, lg = oracle.route(x, W, bias, cfg, want_logits=True)
+    got_lg = r["logits"][: B * N * 4].view(torch.float32).cpu().numpy().reshape(B, N)
+    assert np.array_equal(got_lg.view(np.uint32), lg.view(np.uint32))
+    assert np.array_equal(r["topk_idx"].cpu().numpy(), idx)
+    assert np.array_equal(r["topk_w"].cpu().numpy().view(np.uint32), w.view(np.uint32))
+    assert np.array_equal(r["counts"].cpu().numpy(), oracle.expert_counts(idx, N))
+
 @pytest.mark.parametrize("name,B", [("prefill", 0), ("skew", 0), ("prefill", 6100),
                                     ("prefill", 9700)])
 def test_route_full_size_sampled(dev, name, B):
@@ -370,6 +393,24 @@ def test_dispatch_with_planned_replicas_bit_exact(dev):
     assert api.read_status(d["status"]) == 0
     check_dispatch(cfg, x, idx, d, ref)
 
+
+@pytest.mark.parametrize("layout", [configs.CONTIG, configs.MASKED])
+@pytest.mark.parametrize("B", [1, 77, 128, 129])
+def test_single_chunk_dispatch_with_planned_map(dev, B, layout):
+    """Up to 128 tokens are counted inside the scan's block (one launch fewer); 129
+    tokens take the separate count launch.  Both, with a planned map of four columns
+    and in both layouts, give the oracle's rows, slots, tile list and bytes."""
+    cfg0, x, W, bias = host_workload("small_eplb")
+    cfg = cfg0.with_(B=B, layout=layout, cap=256 if layout == configs.MASKED else 0)
+    xb = np.ascontiguousarray(x[:B])
+    idx, _ = oracle.route(xb, W, bias, cfg)
+    emap = planned_map(cfg, idx)
+    assert emap[0].shape == (cfg.N, 4)
+    ref = oracle.dispatch(xb, idx, cfg, emap[0], emap[1])
+    d = api.dispatch(cfg, bf16_dev(xb), to_dev(idx), to_dev(emap[0]), to_dev(emap[1]))
+    torch.cuda.synchronize()
+    assert api.read_status(d["status"]) == 0
+    check_dispatch(cfg, xb, idx, d, ref)
 
 def test_layer_with_planned_eplb_and_map_swap_matches_no_eplb(dev):
     """Planned replicas read their logical expert's weights, so the layer output is
