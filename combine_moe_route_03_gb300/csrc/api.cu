@@ -15,6 +15,13 @@ int set_cuda_error(cudaError_t e) {
   return MOE_ERR_CUDA;
 }
 
+int device_slot() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return dev >= 0 && dev < kMaxDevices ? dev : MOE_ERR_UNSUPPORTED;
+}
+
 int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;

@@ -20,6 +20,10 @@ inline int check_launch() {
 }
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 int device_sm_count();
+// One-time setup (kernel shared-memory limits, cluster occupancy) is kept per device:
+// the current device's ordinal, or a negative MOE_ERR_* code.
+constexpr int kMaxDevices = 64;
+int device_slot();
 
 // ---------------------------------------------------------------- status word
 __device__ __forceinline__ void status_or(int32_t *st, int bits) {

@@ -1177,8 +1177,11 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.bm_signal = a->block_m_signal > 0 ? a->block_m_signal : BM;
   P.status = a->status;
   P.singles = 0;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[kMaxDevices] = {};
+  static int max_clusters[kMaxDevices] = {}, max_clusters2[kMaxDevices] = {};
+  const int dev = device_slot();
+  if (dev < 0) return dev;
+  if (!attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
@@ -1189,7 +1192,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
       e = cudaFuncSetAttribute(grouped_gemm_pair2_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
     if (e != cudaSuccess) return set_cuda_error(e);
-    attr_set = true;
+    attr_set[dev] = true;
   }
   const int sms = a->num_sms > 0 ? a->num_sms : device_sm_count();
   if (a->pair_tiles == 2) {
@@ -1199,8 +1202,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
         !make_sf_map(&mSFW, a->W_sf, (uint64_t)a->num_experts * (a->n / 128) * (a->k / BK), KB2))
       return MOE_ERR_CUDA;
     // the pairs on 2-SM MMAs, then the single tiles on one CTA each
-    static int max_clusters2 = 0;
-    int rc = launch_pairs(grouped_gemm_pair2_kernel, SMEM2_BYTES, sms, max_clusters2,
+    int rc = launch_pairs(grouped_gemm_pair2_kernel, SMEM2_BYTES, sms, max_clusters2[dev],
                           as_stream(stream), mA, mA32, mW, mSFA, mSFW, P);
     if (rc) return rc;
     P.singles = 1;
@@ -1209,8 +1211,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
     return check_launch();
   }
   if (a->pair_tiles) {
-    static int max_clusters = 0;
-    return launch_pairs(grouped_gemm_kernel<true>, SMEM_BYTES, sms, max_clusters,
+    return launch_pairs(grouped_gemm_kernel<true>, SMEM_BYTES, sms, max_clusters[dev],
                         as_stream(stream), mA, mA32, mW, P);
   }
   const int64_t max_units = a->tiles2 ? sms : a->max_tiles * (a->n / BN);

@@ -670,13 +670,15 @@ int launch_logits(const uint16_t *x, const float *W, float *lg, int B, int H, in
                   cudaStream_t st) {
   constexpr int BT = 8 * TT, BE = 16 * TE;
   constexpr size_t smem = (size_t)S * (BT * (kRouteBK + 8) * 2 + BE * (kRouteBK + 4) * 4);
-  static bool attr = false;
-  if (!attr && smem > 48 * 1024) {
+  static bool attr[kMaxDevices] = {};
+  const int dev = device_slot();
+  if (dev < 0) return dev;
+  if (!attr[dev] && smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(route_logits_kernel<TT, TE, S, kRouteBK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return set_cuda_error(e);
   }
-  attr = true;
+  attr[dev] = true;
   dim3 grid((N + BE - 1) / BE, (B + BT - 1) / BT);
   route_logits_kernel<TT, TE, S, kRouteBK><<<grid, kRouteThreads, smem, st>>>(x, W, lg, B, H, N);
   return check_launch();
@@ -688,13 +690,15 @@ int launch_logits_wide(const uint16_t *x, const float *W, float *lg, int B, int 
   constexpr int BT = 8 * TT, BE = 16 * TE;
   constexpr size_t smem =
       (size_t)S * (BT * (BK + 8) * 2 + BE * (BK + 4) * 4) + (size_t)BT * (BK + 4) * 4;
-  static bool attr = false;
-  if (!attr && smem > 48 * 1024) {
+  static bool attr[kMaxDevices] = {};
+  const int dev = device_slot();
+  if (dev < 0) return dev;
+  if (!attr[dev] && smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(route_logits_wide_kernel<TT, TE, S, BK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return set_cuda_error(e);
   }
-  attr = true;
+  attr[dev] = true;
   dim3 grid((N + BE - 1) / BE, (B + BT - 1) / BT);
   route_logits_wide_kernel<TT, TE, S, BK><<<grid, kRouteThreads, smem, st>>>(x, W, lg, B, H, N);
   return check_launch();
@@ -706,13 +710,15 @@ int launch_logits_slice(const uint16_t *x, const float *W, float *lg, int B, int
   constexpr int BT = NW * TT;
   constexpr size_t smem = (size_t)S * (BT * (BK + 8) * 2 + 32 * TE * (BK + 4) * 4) +
                           (size_t)BT * (BK + 4) * 4;
-  static bool attr = false;
-  if (!attr) {
+  static bool attr[kMaxDevices] = {};
+  const int dev = device_slot();
+  if (dev < 0) return dev;
+  if (!attr[dev]) {
     cudaError_t e = cudaFuncSetAttribute(route_logits_slice_kernel<TT, TE, S, BK, NW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return set_cuda_error(e);
   }
-  attr = true;
+  attr[dev] = true;
   route_logits_slice_kernel<TT, TE, S, BK, NW><<<(B + BT - 1) / BT, NW * 32, smem, st>>>(x, W, lg,
                                                                                     B, H);
   return check_launch();

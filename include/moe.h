@@ -25,6 +25,9 @@
  *   - Errors found on the device are OR-ed into the caller's int32 `status` word
  *     (MOE_STATUS_* bits; sticky until the caller clears it).  moe_read_status()
  *     is the only call that waits for the device.
+ *   - Calls run on the calling thread's current CUDA device.  The first call on a
+ *     device raises the kernels' shared-memory limits and caches cluster
+ *     occupancy for that device (up to 64 devices per process).
  *   - bf16 tensors are passed as void* and hold IEEE bfloat16 bit patterns.
  *   - e4m3 tensors hold OCP FP8 E4M3 ("e4m3fn") codes.  Scales are UE8M0
  *     bytes: value = 2^(byte - 127).
