@@ -83,7 +83,7 @@ SIGNATURES = {
     "moe_dispatch_rows": (_c_i64, [ctypes.POINTER(DispatchCfg)]),
     "moe_dispatch_max_tiles": (_c_i64, [ctypes.POINTER(DispatchCfg)]),
     "moe_dispatch_workspace_size": (_c_sz, [ctypes.POINTER(DispatchCfg)]),
-    "moe_dispatch": (_c_int, [ctypes.POINTER(DispatchCfg)] + [_vp] * 13 + [_c_sz, _vp, _vp]),
+    "moe_dispatch": (_c_int, [ctypes.POINTER(DispatchCfg)] + [_vp] * 14 + [_c_sz, _vp, _vp]),
     "moe_dispatch_noalloc": (_c_int, [ctypes.POINTER(DispatchCfg)] + [_vp] * 15),
     "moe_grouped_gemm_fp8": (_c_int, [ctypes.POINTER(GemmArgs), _vp]),
     "moe_packed_scale_bytes": (_c_sz, [_c_int, _c_int, _c_int]),

@@ -40,6 +40,70 @@ def test_header_compiles_as_plain_c(tmp_path):
                            str(src), "-o", str(tmp_path / "t")])
 
 
+STRUCTS = {"RouteCfg": "moe_route_cfg", "DispatchCfg": "moe_dispatch_cfg",
+           "EplbCfg": "moe_eplb_cfg", "GemmArgs": "moe_gemm_args",
+           "CombineCfg": "moe_combine_cfg", "Layer": "moe_layer"}
+
+
+def test_binding_structs_match_the_c_layout(tmp_path):
+    """Every ctypes structure of the binding has the C struct's size, and each of its
+    fields the C field's offset and size (gcc, printed by a program including moe.h)."""
+    import subprocess
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "moe.h"', 'int main(void){']
+    for py, c in STRUCTS.items():
+        lines.append(f'printf("{py} . %zu %zu\\n", sizeof({c}), (size_t)0);')
+        for f, _ in getattr(_lib, py)._fields_:
+            lines.append(f'printf("{py} {f} %zu %zu\\n", offsetof({c}, {f}), '
+                         f'sizeof((({c} *)0)->{f}));')
+    lines.append("return 0;}")
+    (tmp_path / "l.c").write_text("\n".join(lines) + "\n")
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           str(tmp_path / "l.c"), "-o", str(tmp_path / "l")])
+    out = subprocess.check_output([str(tmp_path / "l")], text=True).split("\n")
+    n = 0
+    for line in filter(None, out):
+        py, f, a, b = line.split()
+        cls = getattr(_lib, py)
+        if f == ".":
+            assert ctypes.sizeof(cls) == int(a), py
+        else:
+            fd = getattr(cls, f)
+            assert (fd.offset, fd.size) == (int(a), int(b)), (py, f)
+            n += 1
+    assert n == sum(len(getattr(_lib, py)._fields_) for py in STRUCTS)
+
+
+def _kind(c_type: str) -> str:
+    c_type = c_type.strip()
+    if "*" in c_type:
+        return "ptr"
+    base = c_type.replace("const", "").split()[0]
+    return {"int": "int", "size_t": "size", "int64_t": "i64", "float": "f32",
+            "double": "f64"}[base]
+
+
+def _ctypes_kind(t) -> str:
+    if t is ctypes.c_void_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "ptr"
+    return {ctypes.c_int: "int", ctypes.c_size_t: "size", ctypes.c_int64: "i64",
+            ctypes.c_float: "f32", ctypes.c_double: "f64"}[t]
+
+
+def test_binding_signatures_match_the_header():
+    """Each declared entry point's return type and parameter list (count, and pointer
+    or integer width of each) equals the binding's ctypes signature."""
+    hdr = open(os.path.join(ROOT, "include", "moe.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", " ", hdr, flags=re.S)
+    hdr = re.sub(r"//[^\n]*", " ", hdr)
+    decls = re.findall(r"^(int|size_t|int64_t)\s+(\w+)\s*\(([^;{]*?)\)\s*;", hdr, re.M | re.S)
+    assert {d[1] for d in decls} == set(_lib.SIGNATURES)
+    for ret, name, params in decls:
+        res, args = _lib.SIGNATURES[name]
+        assert _kind(ret) == _ctypes_kind(res), name
+        ps = [] if params.strip() in ("", "void") else params.split(",")
+        assert [_kind(" ".join(p.split()[:-1]) + (" *" if "*" in p else "")) for p in ps] == \
+            [_ctypes_kind(a) for a in args], name
+
 @pytest.mark.parametrize("seed", range(6))
 def test_eplb_map_matches_oracle(L, seed):
     rng = np.random.default_rng(seed)
@@ -82,7 +146,7 @@ def test_host_argument_checks_return_before_launch(L):
     dc = _lib.DispatchCfg(4, 100, 2, 8, 8, 0, 0, 0)               # H % 128 != 0
     assert L.moe_dispatch_rows(ctypes.byref(dc)) == 0
     dc = _lib.DispatchCfg(4, 128, 2, 8, 8, 1, 100, 0)             # cap % 128 != 0
-    assert L.moe_dispatch(ctypes.byref(dc), *([None] * 13), 0, None, None) == -2
+    assert L.moe_dispatch(ctypes.byref(dc), *([None] * 14), 0, None, None) == -2
     g = _lib.GemmArgs(0, 300, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, None)
     assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -2
     g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, None)
@@ -106,3 +170,25 @@ def test_host_argument_checks_return_before_launch(L):
     assert f(ctypes.byref(lay), s1, s1, hx, hx, 2, s1, s1) == -1             # one stream
     assert f(ctypes.byref(lay), None, s1, hx, hx, 2, s1, s2) == -1           # no 2nd buffer
     assert f(ctypes.byref(lay), s1, s1, (ctypes.c_void_p * 2)(16, None), hx, 2, s1, s2) == -1
+
+
+def test_binding_calls_pass_every_parameter():
+    """ctypes passes arguments beyond argtypes by default conversion (a pointer would go
+    as a C int), so every call of an entry point in the binding, whether through
+    load() or a local L = load(), passes exactly its declared parameters."""
+    import ast
+    src = open(os.path.join(ROOT, "combine_moe_route_03_gb300", "api.py")).read()
+    calls = 0
+    for node in ast.walk(ast.parse(src)):
+        if not (isinstance(node, ast.Call) and isinstance(node.func, ast.Attribute)
+                and node.func.attr in _lib.SIGNATURES):
+            continue
+        recv = node.func.value
+        if not ((isinstance(recv, ast.Name) and recv.id == "L") or
+                (isinstance(recv, ast.Call) and getattr(recv.func, "id", "") == "load")):
+            continue
+        assert not any(isinstance(a, ast.Starred) for a in node.args)
+        assert len(node.args) == len(_lib.SIGNATURES[node.func.attr][1]), \
+            (node.func.attr, node.lineno)
+        calls += 1
+    assert calls >= 18
