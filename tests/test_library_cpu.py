@@ -192,3 +192,35 @@ def test_binding_calls_pass_every_parameter():
             (node.func.attr, node.lineno)
         calls += 1
     assert calls >= 18
+
+
+def test_oracle_binding_matches_its_c_definitions():
+    """The oracle's ctypes table against the C definitions in oracle/moe_oracle.c:
+    return type and each parameter's kind (pointer, or integer / float width)."""
+    src = open(os.path.join(ROOT, "oracle", "moe_oracle.c")).read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    defs = re.findall(r"^(int|void|float|uint8_t|uint16_t)\s+(oracle_\w+)\s*\(([^;{]*?)\)\s*\{",
+                      src, re.M | re.S)
+    kinds = {"int": "int", "int64_t": "i64", "float": "f32", "uint8_t": "u8", "uint16_t": "u16",
+             "void": None}
+    ct = {ctypes.c_int: "int", ctypes.c_int64: "i64", ctypes.c_float: "f32",
+          ctypes.c_uint8: "u8", ctypes.c_uint16: "u16", None: None}
+
+    def ckind(t):
+        if t is ctypes.c_void_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+            return "ptr"
+        if getattr(t, "__name__", "").startswith("ndpointer_"):    # numpy array pointers
+            return "ptr"
+        return ct[t]
+    L = oracle.lib()
+    checked = 0
+    for ret, name, params in defs:
+        fn = getattr(L, name)
+        if fn.argtypes is None:          # helpers the binding never calls
+            continue
+        ps = [] if params.strip() in ("", "void") else params.split(",")
+        want = ["ptr" if "*" in p else kinds[p.replace("const", "").split()[0]] for p in ps]
+        assert [ckind(a) for a in fn.argtypes] == want, name
+        assert ckind(fn.restype) == kinds[ret], name
+        checked += 1
+    assert checked >= 12
