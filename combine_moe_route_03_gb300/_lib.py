@@ -133,12 +133,24 @@ def check(rc: int, what: str) -> None:
         raise MoEError(f"{what} failed: {ERRORS.get(rc, rc)}{extra}")
 
 
-def ptr(t) -> int | None:
+def ptr(t, host: bool = False) -> int | None:
+    """Address of a contiguous tensor (or a raw address) for a pointer parameter.
+
+    Device parameters take CUDA tensors on the current device (the library's kernels
+    would otherwise dereference host or another GPU's addresses); host parameters
+    (``host=True``: the pinned buffers of the host-copy entry points) take CPU
+    tensors."""
     if t is None:
         return None
     if isinstance(t, torch.Tensor):
-        if t.is_cuda and not t.is_contiguous():
+        if not t.is_contiguous():
             raise ValueError("tensors passed to libmoe must be contiguous")
+        if host:
+            if t.is_cuda:
+                raise ValueError("a host buffer parameter got a CUDA tensor")
+        elif not t.is_cuda or t.device.index != torch.cuda.current_device():
+            raise ValueError(f"a device parameter got a tensor on {t.device}; libmoe runs on "
+                             f"the current CUDA device")
         return t.data_ptr()
     return int(t)
 

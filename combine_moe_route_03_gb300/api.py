@@ -356,8 +356,8 @@ class MoELayer:
 
     def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> None:
         """x from (pinned) host memory, out back to host memory, through the C ABI."""
-        check(load().moe_layer_forward_host(ctypes.byref(self.layer), ptr(x_host),
-                                            ptr(out_host), stream_ptr(stream)),
+        check(load().moe_layer_forward_host(ctypes.byref(self.layer), ptr(x_host, host=True),
+                                            ptr(out_host, host=True), stream_ptr(stream)),
               "moe_layer_forward_host")
 
     def forward_host_pipelined(self, x_hosts, out_hosts, stream=None, copy_stream=None) -> None:
@@ -375,8 +375,8 @@ class MoELayer:
             if getattr(self, "_copy_stream", None) is None:
                 self._copy_stream = torch.cuda.Stream(device=self.x.device)
             copy_stream = self._copy_stream
-        xs = (ctypes.c_void_p * n)(*[ptr(t) for t in x_hosts])
-        outs = (ctypes.c_void_p * n)(*[ptr(t) for t in out_hosts])
+        xs = (ctypes.c_void_p * n)(*[ptr(t, host=True) for t in x_hosts])
+        outs = (ctypes.c_void_p * n)(*[ptr(t, host=True) for t in out_hosts])
         check(load().moe_layer_forward_host_pipelined(
             ctypes.byref(self.layer), ptr(self._x2), ptr(self._out2), xs, outs, n,
             stream_ptr(stream), stream_ptr(copy_stream)), "moe_layer_forward_host_pipelined")
@@ -392,7 +392,8 @@ class LayerGraph:
                  x_host: torch.Tensor | None = None, out_host: torch.Tensor | None = None):
         self._keep = (layer, x_host, out_host)
         h = ctypes.c_void_p()
-        check(load().moe_layer_graph_create(ctypes.byref(layer.layer), ptr(x_host), ptr(out_host),
+        check(load().moe_layer_graph_create(ctypes.byref(layer.layer), ptr(x_host, host=True),
+                                            ptr(out_host, host=True),
                                             stream_ptr(stream), ctypes.byref(h)),
               "moe_layer_graph_create")
         self.handle = h

@@ -224,3 +224,28 @@ def test_oracle_binding_matches_its_c_definitions():
         assert ckind(fn.restype) == kinds[ret], name
         checked += 1
     assert checked >= 12
+
+
+def test_binding_rejects_host_tensors_for_device_parameters(L):
+    """A CPU tensor where the library expects device memory is refused in the binding,
+    before any call: a kernel would otherwise dereference a host address."""
+    import torch
+    cfg = configs.TINY
+    x = torch.zeros((cfg.B, cfg.H), dtype=torch.bfloat16)
+    idx = torch.zeros((cfg.B, cfg.K), dtype=torch.int32)
+    u8 = torch.zeros((256, 128), dtype=torch.uint8)
+    calls = [
+        lambda: api.route(cfg, x, torch.zeros((cfg.N, cfg.H)), None),
+        lambda: api.dispatch(cfg, x, idx),
+        lambda: api.combine(torch.zeros((4, 128), dtype=torch.bfloat16),
+                            torch.zeros((2, 1), dtype=torch.int32), torch.ones((2, 1))),
+        lambda: api.pack_weight_scales(torch.zeros((1, 1, 1), dtype=torch.uint8)),
+        lambda: api.grouped_gemm_fp8(api.GEMM_DOWN, u8, u8, u8[None, :128], u8, idx, 1),
+        lambda: api.read_status(torch.zeros(1, dtype=torch.int32)),
+    ]
+    for c in calls:
+        with pytest.raises(ValueError, match="device parameter"):
+            c()
+    with pytest.raises(ValueError, match="contiguous"):
+        _lib.ptr(torch.zeros((4, 4)).t(), host=True)
+    assert _lib.ptr(torch.zeros(4), host=True) is not None and _lib.ptr(None) is None
