@@ -34,6 +34,20 @@ def read_status(status: torch.Tensor) -> int:
     return int(v.value)
 
 
+_BF16 = (torch.bfloat16, torch.int16)   # bf16 values, or their bits viewed as int16
+
+
+def _expect(t, what: str, dtypes, shape) -> None:
+    """Shape and dtype of a tensor argument against the configuration (None in
+    `shape`: any extent); a mismatch would make a kernel read past a buffer."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what}: a torch tensor is required")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{what}: dtype {t.dtype}, expected one of {dtypes}")
+    if t.dim() != len(shape) or any(w is not None and g != w for g, w in zip(t.shape, shape)):
+        raise ValueError(f"{what}: shape {tuple(t.shape)}, expected {shape}")
+
+
 def _route_cfg(cfg: MoEConfig, B: int | None = None) -> RouteCfg:
     return RouteCfg(cfg.B if B is None else B, cfg.H, cfg.N, cfg.K, cfg.n_group, cfg.topk_group,
                     cfg.score_fn, cfg.renorm, cfg.route_scale)
@@ -42,6 +56,10 @@ def _route_cfg(cfg: MoEConfig, B: int | None = None) -> RouteCfg:
 def route(cfg: MoEConfig, x: torch.Tensor, W: torch.Tensor, bias: torch.Tensor | None,
           stream=None, counts: bool = True) -> dict:
     """moe_route: x bf16 [B][H], W fp32 [N][H], bias fp32 [N] -> topk_idx, topk_w, counts."""
+    _expect(x, "x", _BF16, (None, cfg.H))
+    _expect(W, "W", (torch.float32,), (cfg.N, cfg.H))
+    if bias is not None:
+        _expect(bias, "bias", (torch.float32,), (cfg.N,))
     B = x.shape[0]
     rc = _route_cfg(cfg, B)
     dev = x.device
@@ -146,7 +164,14 @@ def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=N
              cap: int | None = None, stream=None, out: dict | None = None) -> dict:
     """moe_dispatch -> A, A_sf, counts, row_of, src_of, tiles (+ shared copy).
     log2phys [N][max_rep] / rep [N]: an EPLB map (max_rep = its column count)."""
+    _expect(x, "x", _BF16, (None, cfg.H))
     B, H = x.shape
+    _expect(topk_idx, "topk_idx", (torch.int32,), (B, cfg.K))
+    if (log2phys is None) != (rep is None):
+        raise ValueError("log2phys and rep go together")
+    if log2phys is not None:
+        _expect(log2phys, "log2phys", (torch.int32,), (cfg.N, None))
+        _expect(rep, "rep", (torch.int32,), (cfg.N,))
     dev = x.device
     dc = _dispatch_cfg(cfg, B, fmt, cap, 0 if log2phys is None else log2phys.shape[1])
     sz = dispatch_sizes(cfg, B, fmt, cap)
@@ -221,8 +246,15 @@ def combine(Y: torch.Tensor, row_of: torch.Tensor, topk_w: torch.Tensor,
             timeout_ns: int = 1_000_000_000, num_ctas: int = 0, shared_row0: int = 0,
             status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """moe_combine: Y bf16 [rows][H] -> out bf16 [B][H]."""
+    _expect(row_of, "row_of", (torch.int32,), (None, None))
     B, K = row_of.shape
-    H = Y.shape[1] if Y.dtype == torch.bfloat16 else Y.shape[1] // 2
+    _expect(topk_w, "topk_w", (torch.float32,), (B, K))
+    _expect(Y, "Y", _BF16 + (torch.uint8,), (None, None))
+    H = Y.shape[1] if Y.element_size() == 2 else Y.shape[1] // 2
+    if shared is not None:
+        _expect(shared, "shared", _BF16, (B, H))
+    if out is not None:
+        _expect(out, "out", _BF16, (B, H))
     if out is None:
         out = torch.empty((B, H), dtype=torch.bfloat16, device=Y.device)
     cc = CombineCfg(B, H, K, ptr(signal), threshold, block_m_signal, timeout_ns, num_ctas,

@@ -249,3 +249,33 @@ def test_binding_rejects_host_tensors_for_device_parameters(L):
     with pytest.raises(ValueError, match="contiguous"):
         _lib.ptr(torch.zeros((4, 4)).t(), host=True)
     assert _lib.ptr(torch.zeros(4), host=True) is not None and _lib.ptr(None) is None
+
+
+def test_binding_checks_shapes_and_dtypes_against_the_config(L):
+    """Arguments whose shape or dtype disagrees with the configuration are refused
+    before any pointer is taken (a kernel would read past the smaller buffer)."""
+    import torch
+    cfg = configs.SMALL_CONTIG
+    B, H, N, K = 10, cfg.H, cfg.N, cfg.K
+    x = torch.zeros((B, H), dtype=torch.bfloat16)
+    W = torch.zeros((N, H))
+    i32 = lambda *s: torch.zeros(s, dtype=torch.int32)  # noqa: E731
+    bad = [
+        lambda: api.route(cfg, x[:, :128].contiguous(), W, None),           # H
+        lambda: api.route(cfg, x, W[:-1].contiguous(), None),                # N rows of W
+        lambda: api.route(cfg, x, W.double(), None),                          # W dtype
+        lambda: api.route(cfg, x, W, torch.zeros(N + 1)),                     # bias length
+        lambda: api.route(cfg, x.float(), W, None),                           # x dtype
+        lambda: api.dispatch(cfg, x, i32(B, K + 1)),                          # K
+        lambda: api.dispatch(cfg, x, i32(B, K).long()),                       # index dtype
+        lambda: api.dispatch(cfg, x, i32(B, K), i32(N, 2), None),             # map half given
+        lambda: api.dispatch(cfg, x, i32(B, K), i32(N - 1, 2), i32(N)),       # map rows
+        lambda: api.combine(torch.zeros((40, H), dtype=torch.bfloat16), i32(B, K),
+                            torch.zeros((B, K + 1))),                         # weights shape
+        lambda: api.combine(torch.zeros((40, H), dtype=torch.bfloat16), i32(B, K),
+                            torch.zeros((B, K)), shared=torch.zeros((B, H + 128),
+                                                                    dtype=torch.bfloat16)),
+    ]
+    for i, c in enumerate(bad):
+        with pytest.raises(ValueError, match="expected|together"):
+            c()
