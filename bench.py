@@ -94,7 +94,8 @@ def describe(cfg) -> str:
 
 def stage_work(cfg, counts: np.ndarray) -> dict:
     """Algorithmic bytes and flops per launch of each stage (the minimum a stage must
-    move: padding rows, unused capacity and scale replication not counted)."""
+    move: padding rows, unused capacity and scale replication not counted; a 1x128 or
+    128x128 block's scale is one byte wherever it is written or read)."""
     B, H, N, K, I = cfg.B, cfg.H, cfg.N, cfg.K, cfg.I
     R = int(np.minimum(counts, cfg.cap).sum()) if cfg.layout == configs.MASKED else B * K
     Hb, Ib = H // 128, I // 128
@@ -105,7 +106,7 @@ def stage_work(cfg, counts: np.ndarray) -> dict:
     sh = 1 if cfg.shared else 0
     return {
         "route": dict(bytes=B * H * 2 + N * H * 4 + B * K * 8, flops=2 * B * H * N, bound="alu"),
-        "dispatch": dict(bytes=B * H * 2 + R * (H + Hb * 4 + 8) + sh * B * (H + Hb * 4), flops=0,
+        "dispatch": dict(bytes=B * H * 2 + R * (H + Hb + 8) + sh * B * (H + Hb), flops=0,
                          bound="hbm"),
         # the shared expert's B rows run inside the routed GEMM launches
         "gateup": dict(bytes=(nt + sh) * w13 + (R + sh * B) * (H + Hb + I + Ib),
