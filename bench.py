@@ -117,6 +117,42 @@ def stage_work(cfg, counts: np.ndarray) -> dict:
     }
 
 
+# Nominal GB300 figures, the secondary denominators (the measured ones are primary):
+# HBM3e about 8 TB/s; dense e4m3 tensor throughput 4.5 PFLOP/s.
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_FP8_TFLOPS = 4500.0
+
+
+def stage_summary(work: dict, stage_ms: dict, hbm_gbs: float, fp8_tflops: float) -> dict:
+    """Per-stage duration, GB/s and TFLOP/s from the algorithmic work, as fractions of
+    the measured HBM and e4m3 peaks and of the nominal ones."""
+    out = {}
+    for s in STAGES:
+        d = stage_ms[s] * 1e-3
+        if d <= 0 or not work[s]["bytes"]:
+            continue
+        gbs = work[s]["bytes"] / d / 1e9
+        tfs = work[s]["flops"] / d / 1e12
+        out[s] = {"ms": round(stage_ms[s], 4), "GBps": round(gbs, 1),
+                  "hbm_frac": round(gbs / hbm_gbs, 3),
+                  "hbm_frac_nominal": round(gbs / NOMINAL_HBM_GBS, 3),
+                  "TFLOPs": round(tfs, 1)}
+        if s in ("gateup", "down"):
+            out[s]["fp8_frac"] = round(tfs / fp8_tflops, 3)
+            out[s]["fp8_frac_nominal"] = round(tfs / NOMINAL_FP8_TFLOPS, 3)
+    return out
+
+
+def expert_balance(counts) -> dict:
+    """Rows per physical expert in the last step: mean / max (1 = perfectly even), the
+    balance measure the EPLB pages use, with the extremes."""
+    c = np.asarray(counts, np.float64)
+    top = float(c.max()) if c.size else 0.0
+    return {"mean_over_max": round(float(c.mean()) / top, 4) if top > 0 else None,
+            "max_rows": int(top), "min_rows": int(c.min()) if c.size else 0,
+            "experts": int(c.size)}
+
+
 def physical_work(cfg, counts_phys, phys2log) -> dict:
     """stage_work for an EPLB layout: replicas read their logical expert's weights."""
     logical = np.zeros(cfg.N, np.int64)
@@ -403,15 +439,7 @@ def main():
     roof["traffic"] = tr
     roof["kernel"] = dom
     roof["peak_source"] = f"{pk['src']} ({'sustained bf16 x2 for e4m3' if roof['bound'] == 'tensor' else 'hbm_gbs' if roof['bound'] == 'hbm' else 'FFMA units x clock'})"
-    per_stage = {}
-    for s in STAGES:
-        d = stage_ms[s] * 1e-3
-        if d <= 0 or not work[s]["bytes"]:
-            continue
-        per_stage[s] = {"ms": round(stage_ms[s], 4),
-                        "GBps": round(work[s]["bytes"] / d / 1e9, 1),
-                        "hbm_frac": round(work[s]["bytes"] / d / 1e9 / pk["hbm"], 3),
-                        "TFLOPs": round(work[s]["flops"] / d / 1e12, 1)}
+    per_stage = stage_summary(work, stage_ms, pk["hbm"], fp8_peak)
 
     # route (logits, select), dispatch (count + scan fused into one launch for a
     # batch of one 128-token chunk, then scatter), gate/up, down, combine
@@ -423,7 +451,7 @@ def main():
             "data": "synthetic (seeded; random-init weights stored as e4m3 + UE8M0 128x128 scales)",
             "config": run_config(cfg, world),
             "clocks": clocks, "gpu_launches": launches_per_step * K, "roofline": roof,
-            "stages": per_stage, "e2e": e2e}
+            "stages": per_stage, "expert_balance": expert_balance(counts), "e2e": e2e}
     if rank == 0 and world == 1 and args.cpu_tokens > 0:
         rate, dt, tok = cpu_oracle_rate(cfg, x, W, bias, host, shared, args.cpu_tokens)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),

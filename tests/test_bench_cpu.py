@@ -56,3 +56,26 @@ def test_replicas_read_their_logical_experts_weights_once():
     with_map = bench.physical_work(cfg, d["cnt"], p2l)
     without = bench.stage_work(cfg.with_(n_phys=0), counts)
     assert with_map == without
+
+
+def test_stage_summary_fractions():
+    work = {"route": dict(bytes=0, flops=10), "dispatch": dict(bytes=6_000_000, flops=0),
+            "gateup": dict(bytes=8_000_000, flops=4 * 10**12), "down": dict(bytes=1, flops=0),
+            "combine": dict(bytes=3_000_000, flops=0)}
+    ms = {"route": 1.0, "dispatch": 0.001, "gateup": 2.0, "down": 0.0, "combine": 0.001}
+    s = bench.stage_summary(work, ms, hbm_gbs=6000.0, fp8_tflops=4000.0)
+    assert set(s) == {"dispatch", "gateup", "combine"}     # no bytes, or no time: left out
+    assert s["dispatch"]["GBps"] == 6000.0 and s["dispatch"]["hbm_frac"] == 1.0
+    assert s["dispatch"]["hbm_frac_nominal"] == 0.75 and "fp8_frac" not in s["dispatch"]
+    assert s["gateup"]["TFLOPs"] == 2000.0 and s["gateup"]["fp8_frac"] == 0.5
+    assert s["gateup"]["fp8_frac_nominal"] == round(2000.0 / 4500.0, 3)
+    assert s["combine"]["GBps"] == 3000.0
+
+
+def test_expert_balance():
+    assert bench.expert_balance([7, 7, 7])["mean_over_max"] == 1.0
+    b = bench.expert_balance(np.array([4, 2, 0, 2], np.int32))
+    assert b == {"mean_over_max": 0.5, "max_rows": 4, "min_rows": 0, "experts": 4}
+    assert bench.expert_balance([0, 0])["mean_over_max"] is None
+    import json
+    json.dumps(b)
