@@ -102,3 +102,59 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     bench.run_reference(argparse.Namespace(steps=1, warmup=1, gpus=2), configs.DECODE)
     assert capsys.readouterr().out == ""
     assert bench.run_config(configs.DECODE, 2)["global_batch"] == 2 * configs.DECODE.B
+
+
+def _eplb_dead_peer_rank(rank, world, port, q):
+    import datetime
+    import time
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=5))
+    if rank == 1:
+        dist.barrier()
+        os._exit(0)                      # leaves between steps, never plans
+    import numpy as np
+    from combine_moe_route_03_gb300 import api
+    rec = api.EplbRecorder(32, 40, period=1, n_group=4, n_nodes=2, n_gpus=4, max_rep=4)
+    rec.observe(np.arange(32, dtype=np.int32))
+    dist.barrier()
+    time.sleep(1.0)
+    t0 = time.time()
+    try:
+        rec.plan(group=dist.group.WORLD)
+        q.put(("planned", 0.0, None, None))
+    except Exception:                    # the peer is gone: the collective fails
+        q.put(("error", time.time() - t0, rec.load.tolist(), rec.steps))
+        m, _ = rec.plan()                # the kept window still plans locally
+        q.put(("local", 0.0, [a.tolist() for a in m], None))
+    q.close()
+    q.join_thread()                      # flush before leaving without cleanup
+    os._exit(0)
+
+
+def test_cross_rank_plan_with_a_departed_rank_fails_and_keeps_the_window():
+    """A rank that left between steps makes the other rank's cross-rank plan raise
+    within the process group's timeout instead of waiting for ever; the recorder keeps
+    the loads it recorded, so the caller can re-plan (here: locally)."""
+    from combine_moe_route_03_gb300 import build
+    build.build()
+    from oracle import eplb as oeplb
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_eplb_dead_peer_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    try:
+        kind, dt, load, steps = q.get(timeout=90)
+        assert kind == "error" and dt < 30.0
+        assert load == list(range(32)) and steps == 1
+        kind, _, m, _ = q.get(timeout=60)
+        ref, _ = oeplb.plan(list(range(32)), 32, 40, 4, 2, 4, 4)
+        assert kind == "local" and m == [[list(map(int, r)) for r in ref[0]],
+                                         list(map(int, ref[1])), list(map(int, ref[2]))]
+    finally:
+        for p in procs:
+            p.join(timeout=30)
+            if p.is_alive():
+                p.kill()
