@@ -15,7 +15,7 @@ from ._lib import (FMT_BF16, FMT_FP8, GEMM_DOWN, GEMM_GATEUP_SWIGLU, CombineCfg,
                    EplbCfg, GemmArgs, Layer, RouteCfg, check, load, ptr, stream_ptr)
 from .configs import MASKED, MoEConfig
 
-__all__ = ["route", "eplb_build_map", "eplb_plan", "EplbRecorder", "dispatch", "dispatch_sizes", "pack_weight_scales",
+__all__ = ["route", "eplb_build_map", "eplb_plan", "check_eplb_map", "EplbRecorder", "dispatch", "dispatch_sizes", "pack_weight_scales",
            "grouped_gemm_fp8", "combine", "read_status", "new_status", "MoELayer",
            "FMT_FP8", "FMT_BF16", "GEMM_GATEUP_SWIGLU", "GEMM_DOWN", "num_sms"]
 
@@ -101,6 +101,25 @@ def eplb_plan(load_counts: np.ndarray, N_log: int, N_phys: int, n_group: int = 1
                                l2p.ctypes.data, rep.ctypes.data, ctypes.byref(bal)),
           "moe_eplb_plan")
     return (l2p, rep, p2l), bal.value
+
+
+def check_eplb_map(eplb_map, N_log: int, N_phys: int) -> None:
+    """Raises ValueError unless (log2phys [N_log][R], rep [N_log], phys2log [N_phys]) is
+    a map as eplb_build_map and eplb_plan make it: every logical expert has 1..R
+    replicas, the replica counts fill the physical slots, and every entry of a row of
+    log2phys (the tail repeats the first) is a slot that phys2log maps back to it."""
+    l2p, rep, p2l = (np.asarray(a) for a in eplb_map)
+    if l2p.ndim != 2 or l2p.shape[0] != N_log or not 1 <= l2p.shape[1] <= 64 \
+            or rep.shape != (N_log,) or p2l.shape != (N_phys,):
+        raise ValueError("EPLB map: shapes must be [N_log][R] (R <= 64), [N_log], [N_phys]")
+    if rep.min() < 1 or rep.max() > l2p.shape[1] or int(rep.sum()) != N_phys:
+        raise ValueError("EPLB map: replica counts must be 1..R and fill the physical slots")
+    if p2l.min() < 0 or p2l.max() >= N_log or l2p.min() < 0 or l2p.max() >= N_phys:
+        raise ValueError("EPLB map: expert index out of range")
+    if not np.array_equal(p2l[l2p], np.broadcast_to(np.arange(N_log)[:, None], l2p.shape)):
+        raise ValueError("EPLB map: log2phys and phys2log disagree")
+    if not np.array_equal(np.bincount(p2l, minlength=N_log), rep):
+        raise ValueError("EPLB map: a logical expert's replica count differs from its slots")
 
 
 class EplbRecorder:
@@ -304,6 +323,7 @@ class MoELayer:
         self.W2_sf = pack_weight_scales(W2_sf)
         self.log2phys = self.rep = self.phys2log = None
         if eplb_map is not None:
+            check_eplb_map(eplb_map, cfg.N, cfg.N_phys)
             l2p, rep, p2l = eplb_map
             self.log2phys = torch.from_numpy(np.ascontiguousarray(l2p, np.int32)).to(dev)
             self.rep = torch.from_numpy(np.ascontiguousarray(rep, np.int32)).to(dev)
@@ -360,6 +380,7 @@ class MoELayer:
         so it uses the new map from its next replay when the column count is kept."""
         if self.log2phys is None:
             raise ValueError("the layer was built without an EPLB map")
+        check_eplb_map(eplb_map, self.cfg.N, self.cfg.N_phys)
         l2p, rep, p2l = (np.ascontiguousarray(a, np.int32) for a in eplb_map)
         if l2p.shape != tuple(self.log2phys.shape) or p2l.shape != tuple(self.phys2log.shape) \
                 or rep.shape != tuple(self.rep.shape):

@@ -190,3 +190,41 @@ def test_recorder_plans_every_period_from_the_recorded_loads(L):
     assert not rec.due() and rec.load.sum() == 0          # a fresh window
     with pytest.raises(ValueError):
         rec.observe(np.zeros(31, np.int32))
+
+
+# -------------------------------------------------------------- map validation
+@pytest.mark.parametrize("seed", range(8))
+def test_maps_from_both_builders_pass_the_layer_check(L, seed):
+    """Every map the fixed builder and the planner make (library and oracle) is
+    accepted when a layer installs it."""
+    from combine_moe_route_03_gb300 import configs
+    import oracle
+    rng = np.random.default_rng(seed)
+    for N, P in ((32, 40), (256, 288), (256, 256), (8, 16), (512, 1024)):
+        counts = rng.integers(0, 5, N) * rng.integers(0, 3, N)
+        api.check_eplb_map(api.eplb_build_map(counts, N, P), N, P)
+        api.check_eplb_map(oracle.eplb_build_map(counts, N, P), N, P)
+    for shape in SHAPES:
+        N, P, G, nodes, gpus, R = shape
+        load = skewed_load(rng, N)
+        api.check_eplb_map(api.eplb_plan(load, N, P, G, nodes, gpus, R)[0], N, P)
+    cfg = configs.SMALL_EPLB
+    api.check_eplb_map(api.eplb_plan(skewed_load(rng, cfg.N) * 50, cfg.N, cfg.N_phys,
+                                     cfg.n_group, 2, 4, 4)[0], cfg.N, cfg.N_phys)
+
+
+def test_layer_check_rejects_broken_maps(L):
+    l2p, rep, p2l = api.eplb_plan(skewed_load(np.random.default_rng(1), 32), 32, 40, 4, 2, 4, 4)[0]
+    api.check_eplb_map((l2p, rep, p2l), 32, 40)
+    hot = int(np.argmax(rep))
+    broken = []
+    r = rep.copy(); r[hot] -= 1; broken.append((l2p, r, p2l))            # counts short of the slots
+    p = p2l.copy(); p[l2p[hot, 1]] = (hot + 1) % 32; broken.append((l2p, rep, p))   # disagree
+    m = l2p.copy(); m[0, 0] = 40; broken.append((m, rep, p2l))           # slot out of range
+    p = p2l.copy(); p[0] = -1; broken.append((l2p, rep, p))              # expert out of range
+    broken.append((l2p[:31], rep[:31], p2l))                              # shape
+    for b in broken:
+        with pytest.raises(ValueError):
+            api.check_eplb_map(b, 32, 40)
+    with pytest.raises(ValueError):
+        api.check_eplb_map((l2p, rep, p2l), 32, 48)                       # wrong slot count
