@@ -96,14 +96,6 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
     if (L->events) cudaEventRecordWithFlags(static_cast<cudaEvent_t>(L->events[i]), st, ev_flags);
   };
   if (L->has_shared && !L->shared_tiles) return MOE_ERR_INVALID;
-  const int64_t srows = L->has_shared ? ((int64_t)rc.B + 127) / 128 * 128 : 0;
-  const int64_t rows_all = L->rows + srows;
-  const size_t Hb = rc.H / 128, Ib = L->I / 128;
-  mark(0);
-  int rc_ = moe_route(&rc, L->x, L->W_router, L->bias, L->topk_idx, L->topk_w, L->expert_counts,
-                      L->route_ws, L->route_ws_bytes, stream);
-  if (rc_) return rc_;
-  mark(1);
   moe_dispatch_cfg dc;
   dc.B = rc.B;
   dc.H = rc.H;
@@ -114,6 +106,18 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   dc.cap = L->cap;
   dc.fmt = MOE_FMT_FP8;
   dc.max_rep = L->eplb_max_rep;
+  // the row buffers and the tile list must hold what dispatch writes (before any launch)
+  const int64_t need_rows = moe_dispatch_rows(&dc);
+  if (need_rows > 0 && (L->rows < need_rows || L->max_tiles < need_rows / 128))
+    return MOE_ERR_INVALID;
+  const int64_t srows = L->has_shared ? ((int64_t)rc.B + 127) / 128 * 128 : 0;
+  const int64_t rows_all = L->rows + srows;
+  const size_t Hb = rc.H / 128, Ib = L->I / 128;
+  mark(0);
+  int rc_ = moe_route(&rc, L->x, L->W_router, L->bias, L->topk_idx, L->topk_w, L->expert_counts,
+                      L->route_ws, L->route_ws_bytes, stream);
+  if (rc_) return rc_;
+  mark(1);
   uint8_t *A = static_cast<uint8_t *>(L->A), *A_sf = static_cast<uint8_t *>(L->A_sf);
   rc_ = moe_dispatch(&dc, L->x, L->topk_idx, L->log2phys, L->rep, A, A_sf, L->counts, L->row_of,
                      nullptr, L->tiles, L->has_shared ? A + L->rows * rc.H : nullptr,

@@ -383,7 +383,9 @@ int moe_num_sms(void);
 typedef struct moe_layer {
   moe_route_cfg route;
   int N_phys, layout, cap, I, has_shared, sbo, block_m_signal;
-  int64_t rows, max_tiles, timeout_ns;
+  int64_t rows, max_tiles, timeout_ns; /* rows, max_tiles: at least moe_dispatch_rows and
+                                           moe_dispatch_max_tiles of the layer's dispatch
+                                           (else MOE_ERR_INVALID before any launch) */
   int num_sms, combine_ctas;
   int gemm_pairs; /* pair_tiles of both GEMMs.  0: 1 when B*K/N_phys >= 128, else 0;
                      1: always 1; 2: always 2 (H and I multiples of 256); -1: always 0 */

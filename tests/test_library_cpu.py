@@ -279,3 +279,19 @@ def test_binding_checks_shapes_and_dtypes_against_the_config(L):
     for i, c in enumerate(bad):
         with pytest.raises(ValueError, match="expected|together"):
             c()
+
+
+def test_layer_rejects_row_buffers_smaller_than_dispatch_writes(L):
+    """moe_layer_forward checks, before anything is launched, that the layer's row count
+    and tile capacity hold what its dispatch writes."""
+    lay = _lib.Layer()
+    lay.route = _lib.RouteCfg(4, 128, 2, 4, 1, 1, 0, 0, 1.0)   # K > N: the router refuses (-2)
+    lay.N_phys, lay.layout = 2, 0
+    need = L.moe_dispatch_rows(ctypes.byref(_lib.DispatchCfg(4, 128, 4, 2, 2, 0, 0, 0)))
+    assert need == 384
+    lay.rows, lay.max_tiles = need, need // 128
+    assert L.moe_layer_forward(ctypes.byref(lay), None) == -2  # sizes fine: on to the router
+    lay.rows = need - 128
+    assert L.moe_layer_forward(ctypes.byref(lay), None) == -1  # too few rows
+    lay.rows, lay.max_tiles = need, need // 128 - 1
+    assert L.moe_layer_forward(ctypes.byref(lay), None) == -1  # too few tiles
