@@ -316,7 +316,8 @@ typedef struct moe_gemm_args {
 int moe_grouped_gemm_fp8(const moe_gemm_args *args, void *stream);
 
 /*
- * Weight scales (UE8M0 bytes W_sf [E][n/128][k/128]) -> SF atoms
+ * Weight scales (UE8M0 bytes W_sf [E][n/128][k/128], one per 128x128 block as in the
+ * "1d2d" scaling of the "Single Batch Overlap (SBO)" PR, §3) -> SF atoms
  * [E][n/128][k/128][512] (moe_packed_scale_bytes bytes).  One-time setup, off the
  * hot path.
  */
@@ -366,14 +367,15 @@ int moe_num_sms(void);
 
 /* ------------------------------------------------------------------- layer */
 /*
- * The whole layer as one call: route -> dispatch -> gate/up -> down -> combine,
- * every buffer caller-owned (see the fields).
+ * The whole layer as one call ("DeepEP 完全拆解", §专家并行: route, send each token
+ * to its K experts, run them, weighted sum back): route -> dispatch -> gate/up ->
+ * down -> combine, every buffer caller-owned (see the fields).
  * Shared expert (has_shared != 0): its weights are the last expert (index N) of
  * W13 / W13_sf / W2 / W2_sf, which then hold N + 1 experts; its rows (the batch in
  * token order, roundup128(B) rows) follow the `rows` routed rows in A, A_sf, H1,
  * H1_sf and Y, and its tiles (shared_tiles) run inside the routed GEMM launches.
- * With sbo != 0 (masked layout) the down GEMM publishes per-block signals and
- * the combine runs on stream2 beside it, polling them; stream2 must be a stream
+ * With sbo != 0 (masked layout; "Single Batch Overlap (SBO)" PR, §2) the down GEMM
+ * publishes per-block signals and the combine runs on stream2 beside it, polling them; stream2 must be a stream
  * other than `stream` (the call orders it after the work before the down GEMM
  * and makes `stream` wait for the combine).
  * moe_layer_forward_host additionally copies x from host memory (pinned for
