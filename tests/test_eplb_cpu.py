@@ -228,3 +228,22 @@ def test_layer_check_rejects_broken_maps(L):
             api.check_eplb_map(b, 32, 40)
     with pytest.raises(ValueError):
         api.check_eplb_map((l2p, rep, p2l), 32, 48)                       # wrong slot count
+
+
+@pytest.mark.parametrize("shape", [(32, 40, 4, 2, 4, 4), (16, 16, 1, 1, 1, 1), (8, 64, 2, 2, 8, 8),
+                                   (1, 1, 1, 1, 1, 1), (1, 8, 1, 1, 8, 8)])
+def test_degenerate_loads_and_shapes(L, shape):
+    """All-zero loads (a window with no tokens) and extreme shapes (one expert, one slot
+    per GPU, eight replicas each): the library equals the oracle, the map is valid, and
+    an idle window's balance is 1 (no GPU is the maximum)."""
+    N, P, G, nodes, gpus, R = shape
+    for load in (np.zeros(N, np.int64), np.arange(1, N + 1, dtype=np.int64)):
+        got, gbal = api.eplb_plan(load, N, P, G, nodes, gpus, R)
+        ref, rbal = oeplb.plan(list(load), N, P, G, nodes, gpus, R)
+        for g, r in zip(got, ref):
+            assert np.array_equal(g, np.asarray(r, np.int32))
+        assert abs(gbal - rbal) <= 1e-12
+        check_invariants(got, load, N, P, G, nodes, gpus, R)
+        api.check_eplb_map(got, N, P)
+        if not load.any():
+            assert gbal == 1.0
