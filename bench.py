@@ -5,11 +5,15 @@
 
 One step = one pass of the whole layer (moe_layer_forward: route, dispatch, shared
 expert, gate/up + SwiGLU, down, combine) over one batch of seeded synthetic input,
-inputs resident in HBM; the K timed steps run as one CUDA graph of K passes, each
-recording its stage events.  `e2e` runs K steps through the library's pipelined
+inputs resident in HBM; the K timed steps run as one CUDA graph of K passes, every
+8th recording its stage events (their averages give each stage's duration).  `e2e` runs
+K steps through the library's pipelined
 host-buffer call (each step's x copied in from pinned host memory and its output copied
 back, the copies of neighbouring steps overlapping the layer on a copy stream; all copies
-inside the timed region).  Prints one JSON line (rank 0).  Under
+inside the timed region).  Prints one JSON line (rank 0): the rates, the dominant
+kernel against its roofline (`roofline`), every stage against the measured and nominal
+peaks (`stages`), the step's expert balance, clocks, and the oracle's rate on a sample of
+the same workload (`cpu_baseline`).  Under
 torchrun each rank runs its own independent batch (weak scaling, no collective on the
 data path).
 """
