@@ -236,13 +236,28 @@ def cpu_oracle_rate(cfg, x, W, bias, host, shared, ntok: int, seed: int = 0):
 REF_BUDGET_S = 60.0  # timed oracle seconds the reference arm spends at most (about)
 
 
+def streamed_weight_bytes(cfg, counts=None) -> int:
+    """e4m3 weight bytes (+ one scale byte per block) the two GEMMs read per step: the
+    touched experts' W13 and W2, and the shared expert's.  Without counts, every
+    expert counts as touched (the bound for a large batch)."""
+    touched = cfg.N if counts is None else int((np.asarray(counts) > 0).sum())
+    per = 2 * cfg.I * cfg.H + cfg.H * cfg.I + 3 * (cfg.I // 128) * (cfg.H // 128)
+    return (touched + (1 if cfg.shared else 0)) * per
+
+
 def run_config(cfg, world):
     """The JSON line's `config`, the same for both arms: the reference arm times a
     sample of this workload (its cpu_baseline says which)."""
+    per_mb = streamed_weight_bytes(cfg.with_(N=1, shared=False), None) / 1e6
+    top_gb = streamed_weight_bytes(cfg, None) / 1e9
     return {"workload": describe(cfg), "global_batch": world * cfg.B,
             "parallelism": f"dp{world} (independent batch per GPU)",
-            "l2": "inputs larger than L2: every step streams the touched experts' "
-                  "e4m3 weights (about 11 GB) from HBM"}
+            "l2": (f"inputs larger than L2 (129 MB): each step streams from HBM the e4m3 "
+                   f"weights of the experts its batch touches ({per_mb:.1f} MB per expert, "
+                   f"at most {top_gb:.1f} GB; weights_streamed_gb gives the step's figure)"
+                   if top_gb > 0.129 else
+                   f"weights ({top_gb * 1e3:.1f} MB) fit in L2 and stay resident between "
+                   f"steps (no flush)")}
 
 
 def run_reference(args, cfg):
@@ -306,7 +321,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode",
+    ap.add_argument("--workload", default="prefill",
                     choices=sorted(configs.NAMED) + sorted(configs.PROFILE))
     ap.add_argument("--cpu-tokens", type=int, default=12,
                     help="tokens of the CPU-oracle baseline sample (0 = skip)")
@@ -420,29 +435,34 @@ def main():
     work = (stage_work(cfg, counts) if emap is None
             else physical_work(cfg, counts, emap[2]))
     pk = peaks()
-    fp8_peak = 2.0 * pk["bf16_sus"]          # e4m3 = 2x bf16 (nominal dense ratio 4.5 / 2.25)
+    # e4m3 = 2x bf16 (the nominal dense ratio 4.5 / 2.25 PFLOP/s); the burst figure, as
+    # each GEMM launch is timed alone (well under a second), the sustained one beside it
+    fp8_peak = 2.0 * pk["bf16"]
+    fp8_peak_sus = 2.0 * pk["bf16_sus"]
     dom = max((s for s in STAGES if work[s]["bytes"]), key=lambda s: stage_ms[s])
     w = work[dom]
     dur = stage_ms[dom] * 1e-3
     t_hbm = w["bytes"] / (pk["hbm"] * 1e9)
     t_tc = w["flops"] / (fp8_peak * 1e12) if dom not in ("route",) else 0.0
+    sms = _lib.load().moe_num_sms()
     if dom == "route":
         roof = {"bound": "alu", "achieved": w["flops"] / dur / 1e12, "unit": "TFLOP/s"}
-    elif t_tc > t_hbm:
+    elif t_tc >= 0.75 * t_hbm:
+        # at (or within a quarter of) the ridge, the GEMM is held to the tensor peak
         roof = {"bound": "tensor", "achieved": w["flops"] / dur / 1e12, "peak": fp8_peak,
-                "unit": "TFLOP/s"}
+                "unit": "TFLOP/s", "frac_of_sustained": w["flops"] / dur / 1e12 / fp8_peak_sus}
     else:
         roof = {"bound": "hbm", "achieved": w["bytes"] / dur / 1e9, "peak": pk["hbm"],
                 "unit": "GB/s"}
     if roof["bound"] == "alu":
-        # fp32 FFMA: 152 SMs x 128 lanes x 2 flop x median SM clock under load
+        # fp32 FFMA: SMs x 128 lanes x 2 flop x median SM clock under load
         mhz = clocks.get("sm_mhz") or 1900.0
-        roof["peak"] = 152 * 128 * 2 * mhz * 1e6 / 1e12
+        roof["peak"] = sms * 128 * 2 * mhz * 1e6 / 1e12
     roof["frac"] = roof["achieved"] / roof["peak"]
     tr = recorded_traffic(cfg.name, dom) if dom in ("gateup", "down") else None
     roof["traffic"] = tr
     roof["kernel"] = dom
-    roof["peak_source"] = f"{pk['src']} ({'sustained bf16 x2 for e4m3' if roof['bound'] == 'tensor' else 'hbm_gbs' if roof['bound'] == 'hbm' else 'FFMA units x clock'})"
+    roof["peak_source"] = f"{pk['src']} ({'burst bf16 x2 for e4m3' if roof['bound'] == 'tensor' else 'hbm_gbs' if roof['bound'] == 'hbm' else 'FFMA units x clock'})"
     per_stage = stage_summary(work, stage_ms, pk["hbm"], fp8_peak)
 
     # route (logits, select), dispatch (count + scan fused into one launch for a
@@ -454,6 +474,8 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic (seeded; random-init weights stored as e4m3 + UE8M0 128x128 scales)",
             "config": run_config(cfg, world),
+            "weights_streamed_gb": round(streamed_weight_bytes(
+                cfg, counts if emap is None else np.bincount(emap[2][counts > 0], minlength=cfg.N)) / 1e9, 3),
             "clocks": clocks, "gpu_launches": launches_per_step * K, "roofline": roof,
             "stages": per_stage, "expert_balance": expert_balance(counts), "e2e": e2e}
     if rank == 0 and world == 1 and args.cpu_tokens > 0:

@@ -96,6 +96,8 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
     if (L->events) cudaEventRecordWithFlags(static_cast<cudaEvent_t>(L->events[i]), st, ev_flags);
   };
   if (L->has_shared && !L->shared_tiles) return MOE_ERR_INVALID;
+  if (L->gemm_pairs < -1 || L->gemm_pairs > 1) return MOE_ERR_INVALID;
+  if (L->gemm_pairs == 1 && (rc.H % 256 || L->I % 256)) return MOE_ERR_UNSUPPORTED;
   moe_dispatch_cfg dc;
   dc.B = rc.B;
   dc.H = rc.H;
@@ -148,9 +150,11 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   g.out_sf = L->H1_sf;
   g.num_sms = L->num_sms;
   g.status = L->status;
-  g.pair_tiles = L->gemm_pairs == 2 ? 2
-                 : (L->gemm_pairs > 0 ||
-                    (L->gemm_pairs == 0 && (int64_t)rc.B * rc.K >= 128LL * L->N_phys));
+  // 2-SM GEMMs when experts average at least one full M tile (and both GEMMs' K allow
+  // 256-deep stages); one CTA per tile otherwise (decode: HBM-bound on the weights)
+  g.pair_tiles = L->gemm_pairs == 1 ||
+                 (L->gemm_pairs == 0 && (int64_t)rc.B * rc.K >= 128LL * L->N_phys &&
+                  rc.H % 256 == 0 && L->I % 256 == 0);
   if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
   mark(3);
   g.op = MOE_GEMM_DOWN;

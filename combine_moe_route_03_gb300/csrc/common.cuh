@@ -181,24 +181,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
-// Multicast forms: the data (and the complete_tx on the mbarrier at the same
-// shared-memory offset) go to every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *map, uint32_t bar, int x,
-                                               int y, uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-      "l"(map), "r"(bar), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void *src, uint32_t bytes,
-                                             uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -254,15 +236,8 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// Arrive on the mbarrier at this shared-memory offset in every CTA of cta_mask once
-// this thread's earlier tcgen05 operations are complete.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
-}
+// Arrive on this CTA's mbarrier once this thread's earlier tcgen05 operations are
+// complete.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -360,6 +335,11 @@ __device__ __forceinline__ void tc_cp_pair_32x128b_x4(uint32_t taddr, uint64_t s
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                : "memory");
 }
+// Scale copy issued by the even CTA without replication: 128 rows of 16 bytes in each
+// CTA's shared memory -> TMEM lanes 0-127 of its own TMEM (row r -> lane r).
+__device__ __forceinline__ void tc_cp_pair_128x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 // M = 256 block-scaled MMA over the pair: rows 0-127 from the even CTA's A tile,
 // 128-255 from the odd CTA's; B columns 0-127 from the even CTA's B half, 128-255
 // from the odd CTA's; each CTA's TMEM holds its rows' accumulator and scales.
@@ -374,6 +354,8 @@ __device__ __forceinline__ void tc_mma_pair_mxf8(uint32_t d_tmem, uint64_t adesc
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");
 }
+// Pair form of tc_commit: arrive on the mbarrier at this shared-memory offset in every
+// CTA of cta_mask (an arrival, not a data transfer).
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "

@@ -136,67 +136,48 @@ __global__ void __launch_bounds__(kCountWarps * 32) dispatch_count_kernel(
               sm);
 }
 
-// Inclusive block-wide scan (Hillis-Steele) of one value per thread.
-// Scan over the CTA's kScanThreads threads (op: sum, or max when kMax): shuffles
-// inside each warp, then one warp scans the warp totals.  Returns the inclusive
-// scan; *excl (if given) gets the exclusive one (identity: 0, or -1 for max of
-// non-negative values).  `buf` holds one int per warp.
-template <bool kMax = false>
-__device__ __forceinline__ int block_scan(int32_t *buf, int v, int *excl = nullptr) {
+// Inclusive block-wide sum (Hillis-Steele) of one value per thread over the CTA's
+// kScanThreads threads: shuffles inside each warp, then one warp scans the warp
+// totals.  `buf` holds one int per warp.
+__device__ __forceinline__ int block_scan(int32_t *buf, int v) {
   const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
-  const int id = kMax ? -1 : 0;
-  auto op = [](int a, int b) { return kMax ? max(a, b) : a + b; };
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int o = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v = op(v, o);
+    if (lane >= off) v += o;
   }
-  const int e = __shfl_up_sync(0xffffffffu, v, 1);
   if (lane == 31) buf[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < kScanThreads / 32 ? buf[lane] : id;
+    int w = lane < kScanThreads / 32 ? buf[lane] : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int o = __shfl_up_sync(0xffffffffu, w, off);
-      if (lane >= off) w = op(w, o);
+      if (lane >= off) w += o;
     }
     if (lane < kScanThreads / 32) buf[lane] = w;
   }
   __syncthreads();
-  const int prefix = warp > 0 ? buf[warp - 1] : id;
-  if (excl) *excl = lane > 0 ? op(e, prefix) : prefix;
+  const int prefix = warp > 0 ? buf[warp - 1] : 0;
   __syncthreads();  // buf is reused by the next scan
-  return op(v, prefix);
+  return v + prefix;
 }
 
-// Work items for the cluster-mode GEMM, in schedule order: an expert's tile pairs
-// (shared weight tile), then — when this expert's odd last tile completes a couple
-// of singles — that couple (the earlier expert's single and this one's), so a
-// single runs soon after the pairs that read the same weight tile.  Item k =
-// {tile 0, tile 1 or -1, first item of its group, items in its group, shared
-// weight tile, 0, 0, 0}; a group's units are N-tile-major.
-__device__ __forceinline__ void write_items(int32_t *items, int first, int nt, int item_first,
-                                            int s_index, int prev_single, bool emit_single) {
-  const int np = nt / 2;
-  for (int j = 0; j < np; ++j) {
+// Work items of the 2-SM GEMM, in schedule order: an expert's tile pairs (one weight
+// tile shared by both SMs of a pair), then its odd last tile alone, all in one group,
+// so the single runs beside the pairs that read the same weight tiles.  Item k =
+// {tile 0, tile 1 or -1, first item of its group, items in its group, 1 for a pair,
+// 0, 0, 0}; a group's units are N-tile-major.
+__device__ __forceinline__ void write_items(int32_t *items, int first, int nt, int item_first) {
+  const int np = nt / 2, gc = np + nt % 2;
+  for (int j = 0; j < gc; ++j) {
     int32_t *it = items + 8 * (size_t)(item_first + j);
+    const bool pair = j < np;
     it[0] = first + 2 * j;
-    it[1] = first + 2 * j + 1;
+    it[1] = pair ? first + 2 * j + 1 : -1;
     it[2] = item_first;
-    it[3] = np;
-    it[4] = 1;
-    it[5] = it[6] = it[7] = 0;
-  }
-  if (emit_single) {
-    const int k = item_first + np;
-    int32_t *it = items + 8 * (size_t)k;
-    const int mine = first + nt - 1;
-    it[0] = (s_index & 1) ? prev_single : mine;
-    it[1] = (s_index & 1) ? mine : -1;
-    it[2] = k;
-    it[3] = 1;
-    it[4] = 0;
+    it[3] = gc;
+    it[4] = pair ? 1 : 0;
     it[5] = it[6] = it[7] = 0;
   }
 }
@@ -216,7 +197,6 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     __syncthreads();  // ws.hist / phys / rank of the chunk, written by this block
   }
   __shared__ int32_t scan[kScanThreads / 32];
-  __shared__ int32_t single_tile[kScanThreads];
   __shared__ int32_t pad_seg[kScanThreads], pad_from[kScanThreads], pad_to[kScanThreads];
   __shared__ int32_t totals[4];  // tiles, pairs, singles, items
   const int p = threadIdx.x;
@@ -246,24 +226,14 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
   const int first = block_scan(scan, nt) - nt;
   const int np = nt / 2, ns = nt % 2;
   const int pairs_incl = block_scan(scan, np);
-  const int sfirst = block_scan(scan, ns) - ns;
+  const int singles_incl = block_scan(scan, ns);
+  const int item_first = block_scan(scan, np + ns) - (np + ns);
   if (p == kScanThreads - 1) {
     totals[0] = first + nt;
     totals[1] = pairs_incl;
-    totals[2] = sfirst + ns;
+    totals[2] = singles_incl;
+    totals[3] = item_first + np + ns;
   }
-  single_tile[p] = ns ? first + nt - 1 : -1;
-  __syncthreads();
-  const int n_singles = totals[2];
-  const bool emit = ns && ((sfirst & 1) || sfirst == n_singles - 1);
-  const int n_items = np + (emit ? 1 : 0);
-  const int item_first = block_scan(scan, n_items) - n_items;
-  if (p == kScanThreads - 1) totals[3] = item_first + n_items;
-  // the earlier single of a couple belongs to the previous expert with a single:
-  // the largest q < p with one (exclusive max-scan of such indices)
-  int before = -1;
-  block_scan<true>(scan, ns ? p : -1, &before);
-  const int prev_single = (emit && (sfirst & 1) && before >= 0) ? single_tile[before] : -1;
   __syncthreads();
   const int64_t max_tiles = rows_alloc / 128;
   if (p < N_phys) {
@@ -278,7 +248,7 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
       tl[4] = nt;
       tl[5] = tl[6] = tl[7] = 0;
     }
-    write_items(tiles + 8 + 8 * max_tiles, first, nt, item_first, sfirst, prev_single, emit);
+    write_items(tiles + 8 + 8 * max_tiles, first, nt, item_first);
     pad_seg[p] = seg;  // rows [valid, end) of this expert's segment that no token fills
     pad_from[p] = valid;
     pad_to[p] = layout == MOE_LAYOUT_CONTIG ? nt * 128 : cap;
@@ -312,15 +282,15 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
       shared_tiles[4] = snt / 2 + snt % 2;
       for (int i = 5; i < 8; ++i) shared_tiles[i] = 0;
     }
-    // items: snt / 2 pairs of one group, then the odd last tile alone
-    const int snp = snt / 2;
-    for (int j = p; j < snp + snt % 2; j += kScanThreads) {
+    // items: snt / 2 pairs, then the odd last tile alone, all in one group
+    const int snp = snt / 2, sgc = snp + snt % 2;
+    for (int j = p; j < sgc; j += kScanThreads) {
       int32_t *it = shared_tiles + 8 + 8 * (size_t)snt + 8 * (size_t)j;
       const bool pair = j < snp;
       it[0] = 2 * j;
       it[1] = pair ? 2 * j + 1 : -1;
-      it[2] = pair ? 0 : j;
-      it[3] = pair ? snp : 1;
+      it[2] = 0;
+      it[3] = sgc;
       it[4] = pair ? 1 : 0;
       it[5] = it[6] = it[7] = 0;
     }

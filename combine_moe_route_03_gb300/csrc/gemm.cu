@@ -11,12 +11,15 @@
 // each 1x128 / 128x128 scale repeated over its four 32-wide sub-blocks) and the
 // fp32 accumulator stays in tensor memory for the whole K loop.
 //
-// CTA = 11 warps, one CTA per SM, persistent:
+// Two kernels over the same tile list, both persistent with 11 warps per CTA:
+//   grouped_gemm_kernel (one CTA per M tile, 128x256 MMAs) and grouped_gemm_2sm_kernel
+//   (CTA pairs on one TPC: an expert's tile pairs as M=256 cta_group::2 MMAs, its odd
+//   last tile as an M=128 or M=256 pair MMA in the same launch).
 //   warp 0  TMA producer: A tile 128x128 e4m3, B tile 256x128 e4m3 (two 128-row
 //           boxes: gate and up halves for GATEUP, two output blocks for DOWN),
-//           and the matching scale atoms (cp.async.bulk), STAGES-deep ring.
+//           and the matching scale atoms, a ring of stages.
 //   warp 1  TMEM owner and MMA issuer: scale atoms -> TMEM (tcgen05.cp), four
-//           128x256x32 block-scaled MMAs per stage, commits free the stage.
+//           block-scaled MMAs per 128-deep k-block, commits free the stage.
 //   warps 2-9 epilogue: TMEM -> registers (two warps per accumulator row group,
 //           half the columns each; TMEM is released before any math), SwiGLU +
 //           1x128 requantisation (GATEUP) or bf16 rounding (DOWN), global
@@ -63,7 +66,6 @@ struct GemmParams {
   int32_t *signal;
   int bm_signal;
   int32_t *status;
-  int singles;  // one-CTA kernel: only the single tiles of the item table (see get_single_unit)
 };
 
 struct Unit {
@@ -73,10 +75,6 @@ struct Unit {
   int ni;      // output column tile
   int band;    // M tiles sharing this unit's weight tile
   bool ok;     // the unit runs (its tile-list entries address memory inside the operands)
-  bool active; // this CTA has a tile (a cluster's second CTA may have none)
-  bool mcast;  // pair mode: the two CTAs share one weight tile, half loaded by each
-  bool load_b; // this CTA loads a weight tile (its half, or its own whole one)
-  bool skip;   // not this launch's work (the scheduler drops it)
   bool end;    // end of the CTA's unit stream
 };
 
@@ -104,11 +102,11 @@ __device__ __forceinline__ Unit get_unit(const GemmParams &P, int unit, int unit
   Unit r;
   // the entry must describe its own band, inside the list
   if (f < 0 || c < 1 || g < f || g >= f + c || f + c > cap) {
-    r.ok = r.active = r.mcast = r.load_b = r.skip = r.end = false;
+    r.ok = r.end = false;
     r.row0 = r.nvalid = r.we = r.ni = r.band = 0;
     return r;
   }
-  r.skip = r.end = false;
+  r.end = false;
   const int local = u - P.n_tiles * f;
   const int mi = f + local % c;
   const int32_t *t = tl + 8 + 8 * mi;
@@ -119,100 +117,6 @@ __device__ __forceinline__ Unit get_unit(const GemmParams &P, int unit, int unit
   r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[t[1]] : t[1]);
   // every role skips a tile entry that would address memory outside the operands
   r.ok = tile_ok(P, r.row0, r.nvalid) && r.we >= 0 && r.we < P.num_experts && r.ni < P.n_tiles;
-  r.active = r.ok;
-  r.mcast = false;
-  r.load_b = r.ok;
-  return r;
-}
-
-// Cluster variant: unit -> (work item, N tile) from the item table that follows
-// the tile entries (capacity max_tiles; for tiles2 its own tile count).  CTA `rank`
-// takes the item's tile `rank`.  A shared-weight item (a pair of one expert's
-// tiles) has each CTA load half of the weight tile for both; otherwise each CTA
-// loads its own tile's weights (the second CTA may have no tile).  Units of one
-// item group are N-tile-major, item fastest.
-__device__ __forceinline__ Unit get_pair_unit(const GemmParams &P, int unit, int units2,
-                                              int rank) {
-  const int32_t *tl = P.tiles;
-  int u = unit;
-  const bool second = unit < units2;
-  if (second)
-    tl = P.tiles2;
-  else
-    u -= units2;
-  Unit r;
-  r.ok = r.active = r.mcast = r.load_b = r.skip = r.end = false;
-  r.row0 = r.nvalid = r.we = r.ni = r.band = 0;
-  const int cap = second ? tl[0] : P.max_tiles;
-  const int nitems = tl[4];
-  const int32_t *items = tl + 8 + 8 * (size_t)cap;
-  const int g = u / P.n_tiles;  // some item of the right group
-  if (g >= nitems) return r;
-  const int gf = items[8 * g + 2], gc = items[8 * g + 3];
-  // the item must lie inside the group it names (so local >= 0 below)
-  if (gf < 0 || gc < 1 || g < gf || g >= gf + gc || gf + gc > nitems) return r;
-  const int local = u - P.n_tiles * gf;
-  r.ni = local / gc;
-  const int32_t *it = items + 8 * (gf + local % gc);
-  const int t0 = it[0], mi = rank ? it[1] : it[0];
-  r.mcast = it[4] != 0;
-  if (r.mcast) {  // both CTAs decide alike from tile 0's expert
-    if (t0 < 0 || t0 >= cap || mi < 0 || mi >= cap) return r;
-    const int32_t *e0 = tl + 8 + 8 * t0;
-    r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[e0[1]] : e0[1]);
-    r.band = e0[4];
-    r.ok = r.load_b = r.we >= 0 && r.we < P.num_experts && r.ni < P.n_tiles;
-    const int32_t *t = tl + 8 + 8 * mi;
-    r.row0 = t[0] + (second ? P.row_offset2 : 0);
-    r.nvalid = t[2];
-    r.active = r.ok && tile_ok(P, r.row0, r.nvalid);
-    return r;
-  }
-  r.ok = r.ni < P.n_tiles;  // runs even when this CTA has no tile
-  if (!r.ok || mi < 0 || mi >= cap) return r;
-  const int32_t *t = tl + 8 + 8 * mi;
-  r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[t[1]] : t[1]);
-  r.band = t[4];
-  r.row0 = t[0] + (second ? P.row_offset2 : 0);
-  r.nvalid = t[2];
-  r.active = r.load_b = r.we >= 0 && r.we < P.num_experts && tile_ok(P, r.row0, r.nvalid);
-  return r;
-}
-
-// Singles variant (one-CTA kernel after the 2-SM kernel took the pairs): unit ->
-// (item, N tile, slot); the tile in that slot of an item without a shared weight tile,
-// or `skip` (a pair item, or an empty slot).  Two units per item and N tile.
-__device__ __forceinline__ Unit get_single_unit(const GemmParams &P, int unit, int units2) {
-  const int32_t *tl = P.tiles;
-  int u = unit;
-  const bool second = unit < units2;
-  if (second)
-    tl = P.tiles2;
-  else
-    u -= units2;
-  Unit r;
-  r.ok = r.active = r.mcast = r.load_b = r.skip = r.end = false;
-  r.row0 = r.nvalid = r.we = r.ni = r.band = 0;
-  const int cap = second ? tl[0] : P.max_tiles;
-  const int nitems = tl[4];
-  const int32_t *items = tl + 8 + 8 * (size_t)cap;
-  const int g = u / (2 * P.n_tiles), rem = u % (2 * P.n_tiles);
-  if (g >= nitems) return r;
-  const int32_t *it = items + 8 * g;
-  const int mi = it[rem & 1];
-  if (it[4] != 0 || mi < 0) {
-    r.skip = true;
-    return r;
-  }
-  r.ni = rem >> 1;
-  if (mi >= cap) return r;
-  const int32_t *t = tl + 8 + 8 * mi;
-  r.we = second ? P.expert2 : (P.phys2log ? P.phys2log[t[1]] : t[1]);
-  r.band = t[4];
-  r.row0 = t[0] + (second ? P.row_offset2 : 0);
-  r.nvalid = t[2];
-  r.ok = r.active = r.load_b = tile_ok(P, r.row0, r.nvalid) && r.we >= 0 &&
-                               r.we < P.num_experts;
   return r;
 }
 
@@ -320,12 +224,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &P, int row0, int
 // tmA loads full 128-row A tiles; tmA32 loads 32-row slices, used for tiles with
 // fewer valid rows so rows that hold no data are never fetched (the MMA then reads
 // stale shared memory for them, which only feeds accumulator rows never stored).
-// kPair: launched as 2-CTA clusters; the two CTAs take the two M tiles of a pair
-// and each loads half of the shared weight tile (and one weight scale atom),
-// multicast into both CTAs' shared memory, so the weight tile leaves L2 once per
-// pair and both tiles consume it in lockstep.  A stage is refilled only after both
-// CTAs' MMAs released it (commits multicast to both CTAs' empty barriers).
-template <bool kPair>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA32,
@@ -345,14 +243,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
-  constexpr uint16_t kBoth = 3;  // cluster CTA mask of a pair
-  const int rank = kPair ? (int)cluster_ctarank() : 0;
-  const int first_unit = kPair ? (int)cluster_id_x() : (int)blockIdx.x;
-  const int ustride = kPair ? (int)cluster_count_x() : (int)gridDim.x;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kPair ? 2 : 1);
+      mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, kEpiThreads);
@@ -372,18 +266,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (kPair) cluster_sync();  // the peer's barriers exist before anything targets them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // work items of a list: its M tiles, or (cluster mode) its pairs + singles two by two
-  auto items = [&](const int32_t *t) { return kPair ? t[4] : (P.singles ? 2 * t[4] : t[0]); };
-  const int units2 = P.tiles2 ? items(P.tiles2) * P.n_tiles : 0;
-  const int total = items(P.tiles) * P.n_tiles + units2;
-  auto unit_at = [&](int u) {
-    return kPair ? get_pair_unit(P, u, units2, rank)
-                 : (P.singles ? get_single_unit(P, u, units2) : get_unit(P, u, units2));
-  };
+  const int units2 = P.tiles2 ? P.tiles2[0] * P.n_tiles : 0;
+  const int total = P.tiles[0] * P.n_tiles + units2;
   // The seq-th unit of this CTA from the scheduler's ring (false: timed out / aborted).
   // The caller releases the slot with release_unit once it has copied the unit.
   auto take_unit = [&](int seq, Unit &U) {
@@ -421,12 +308,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           continue;
         }
         const int row0 = U.row0, we = U.we, ni = U.ni;
-        // a weight tile that another work item will read again stays in L2
-        const uint64_t pol_w = U.band > (U.mcast ? 2 : 1) ? pol_keep : pol_stream;
+        const uint64_t pol_w = U.band > 1 ? pol_keep : pol_stream;
         const int a_slices = U.nvalid == BM ? 0 : (U.nvalid + 31) / 32;  // 0: one full box
         const uint32_t a_bytes = a_slices ? a_slices * (A_BYTES / 4) : A_BYTES;
-        const uint32_t tx =
-            (U.active ? a_bytes + SFA_BYTES : 0) + (U.load_b ? B_BYTES + SFB_BYTES : 0);
+        const uint32_t tx = a_bytes + SFA_BYTES + B_BYTES + SFB_BYTES;
         int wrow0, wrow1, nb0, nb1;
         if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
           wrow0 = we * P.n + ni * 128;
@@ -454,41 +339,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
           const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
           const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
-          if (U.active) {
-            if (a_slices == 0)
-              tma_load_2d(sa, &tmA, full, kb * BK, row0, pol_a);
-            else
-              for (int j = 0; j < a_slices; ++j)
-                tma_load_2d(sa + j * (A_BYTES / 4), &tmA32, full, kb * BK, row0 + 32 * j,
-                            pol_a);
-            bulk_load(ssfa, sfa + (size_t)kb * 512, 512, full);
-          }
-          if (U.mcast) {  // my half of the shared weight tile, into both CTAs
-            tma_load_2d_mc(sb + rank * (B_BYTES / 2), &tmW, full, kb * BK, rank ? wrow1 : wrow0,
-                           kBoth, pol_w);
-            bulk_load_mc(ssfb + rank * 512, (rank ? sfb1 : sfb0) + (size_t)kb * 512, 512, full,
-                         kBoth);
-          } else if (U.load_b) {
-            tma_load_2d(sb, &tmW, full, kb * BK, wrow0, pol_w);
-            tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
-            bulk_load(ssfb, sfb0 + (size_t)kb * 512, 512, full);
-            bulk_load(ssfb + 512, sfb1 + (size_t)kb * 512, 512, full);
-          }
+          if (a_slices == 0)
+            tma_load_2d(sa, &tmA, full, kb * BK, row0, pol_a);
+          else
+            for (int j = 0; j < a_slices; ++j)
+              tma_load_2d(sa + j * (A_BYTES / 4), &tmA32, full, kb * BK, row0 + 32 * j, pol_a);
+          bulk_load(ssfa, sfa + (size_t)kb * 512, 512, full);
+          tma_load_2d(sb, &tmW, full, kb * BK, wrow0, pol_w);
+          tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
+          bulk_load(ssfb, sfb0 + (size_t)kb * 512, 512, full);
+          bulk_load(ssfb + 512, sfb1 + (size_t)kb * 512, 512, full);
           ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
-      if (kPair && ok) {
-        // Wait until both CTAs released every stage: after this no arrival from the
-        // peer is still on its way to this CTA's barriers.
-        for (int i = 0; i < STAGES; ++i) {
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort, kWaitLimitNs)) {
-            fail(P.status, abort);
-            break;
-          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -526,13 +387,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         release_unit(seq);
         if (U.end) break;
         if (!U.ok) continue;
-        if (U.active) {
-          if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
-            fail(P.status, abort);
-            break;
-          }
-          tc_fence_after();
+        if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
+          fail(P.status, abort);
+          break;
         }
+        tc_fence_after();
         for (int kb = 0; kb < P.Kb; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort, kWaitLimitNs)) {
             fail(P.status, abort);
@@ -540,38 +399,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          if (U.active) {
-            const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
-            const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
-            const uint32_t t_sfa = tmem + TMEM_SF + 16 * stage;
-            const uint32_t t_sfb = t_sfa + 4;
-            const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
-            const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
-            tc_cp_32x128b_x4(t_sfa, smem_desc(ssfa, 16, 128, 0));
-            tc_cp_32x128b_x4(t_sfb, smem_desc(ssfb, 16, 128, 0));
-            tc_cp_32x128b_x4(t_sfb + 4, smem_desc(ssfb + 512, 16, 128, 0));
+          const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
+          const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
+          const uint32_t t_sfa = tmem + TMEM_SF + 16 * stage;
+          const uint32_t t_sfb = t_sfa + 4;
+          const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
+          const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
+          tc_cp_32x128b_x4(t_sfa, smem_desc(ssfa, 16, 128, 0));
+          tc_cp_32x128b_x4(t_sfb, smem_desc(ssfb, 16, 128, 0));
+          tc_cp_32x128b_x4(t_sfb + 4, smem_desc(ssfb + 512, 16, 128, 0));
 #pragma unroll
-            for (int j = 0; j < BK / 32; ++j) {
-              const uint64_t ad = smem_desc(sa + 32 * j, 16, 1024, 2);
-              const uint64_t bd = smem_desc(sb + 32 * j, 16, 1024, 2);
-              const uint32_t idesc = idesc_base | ((uint32_t)j << 29) | ((uint32_t)j << 4);
-              tc_mma_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | j) != 0);
-            }
+          for (int j = 0; j < BK / 32; ++j) {
+            const uint64_t ad = smem_desc(sa + 32 * j, 16, 1024, 2);
+            const uint64_t bd = smem_desc(sb + 32 * j, 16, 1024, 2);
+            const uint32_t idesc = idesc_base | ((uint32_t)j << 29) | ((uint32_t)j << 4);
+            tc_mma_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | j) != 0);
           }
-          if (kPair)
-            tc_commit_mc(bar_empty + 8 * stage, kBoth);
-          else
-            tc_commit(bar_empty + 8 * stage);
+          tc_commit(bar_empty + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        if (U.active) {
-          tc_commit(bar_acc_full);
-          acc_phase ^= 1;
-        }
+        tc_commit(bar_acc_full);
+        acc_phase ^= 1;
       }
     }
   } else if (warp < 2 + kEpiThreads / 32) {
@@ -595,14 +447,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) release_unit(seq);
       if (U.end) break;
-      if (!U.ok || !U.active) continue;
-      const int row0 = U.row0, valid = U.nvalid, ni = U.ni;
+      if (!U.ok) continue;
       if (!mbar_wait(bar_acc_full, acc_phase, abort, kWaitLimitNs)) {
         fail(P.status, abort);
         break;
       }
       tc_fence_after();
-      epilogue_tile(P, row0, valid, ni, t_row, half, row_local, warp, lane, amax_x,
+      epilogue_tile(P, U.row0, U.nvalid, U.ni, t_row, half, row_local, warp, lane, amax_x,
                     [&] { mbar_arrive(bar_acc_empty); });
       acc_phase ^= 1;
     }
@@ -622,10 +473,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       return true;
     };
     bool ok = true;
-    for (int unit = first_unit; ok && unit < total; unit += ustride) {
-      const Unit U = unit_at(unit);
-      if (!U.skip) ok = push(U);
-    }
+    for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) ok = push(get_unit(P, unit, units2));
     if (ok) {
       Unit end = {};
       end.end = true;
@@ -639,22 +487,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
-  if (kPair) cluster_sync();  // neither CTA leaves while the other may still target it
 }
 
 // ------------------------------------------------------------ 2-SM variant
-// The two CTAs of a cluster (the two SMs of a TPC) run one M=256 x N=256 block-
-// scaled MMA per 32-K step (tcgen05 cta_group::2).  Each CTA holds its own 128
-// activation rows, half of the 256-row weight tile and both weight scale atoms; in
-// TMEM it holds its rows' accumulator and scales.  The even CTA issues the MMAs and
-// scale copies for both.  Both CTAs' TMA loads complete on the even CTA's stage
-// barrier, and the MMA commits free the stage in both.  The pair instruction issues
-// about 1.5x the FLOPs per SM-cycle of the one-CTA M=128 form, which bounds the
-// one-CTA kernel at full tiles, and each SM moves 16 KB of weights per 128-deep
-// k-block instead of 32 KB.  A pair item (two M tiles of one expert) is one unit; the
-// single tiles run in a second, one-CTA launch.
-// A stage holds KB2 k-blocks (256 K): the issuing thread waits, fences and commits
-// once per eight MMAs, which keeps the pair's tensor pipe fed.
+// The two CTAs of a cluster (the two SMs of a TPC) share one weight tile: each holds
+// half of it (128 of its 256 rows: the gate or up half for GATEUP, one output block
+// for DOWN) and both weight scale atoms, and the even CTA issues tcgen05 cta_group::2
+// MMAs that read both halves.  Work units (an item of the tile list's item table at
+// one N tile):
+//   pair   two M tiles of one expert, one per CTA: M=256 x N=256 block-scaled MMAs;
+//          each CTA's TMEM holds its 128 rows' accumulator (lanes = rows, columns = N).
+//   single an expert's odd last tile, in the even CTA; with at most 64 valid rows it
+//          runs M=128 MMAs (64 rows per CTA; the odd CTA's half is idle), whose
+//          accumulator sits in TMEM lanes 0-63 for columns [0,128) and lanes 64-127
+//          for columns [128,256) of the same 64 rows; with more rows, M=256 MMAs with
+//          the odd CTA's rows idle.
+// Scales in TMEM: each 32-lane quarter of the tensor core reads the scales of the
+// accumulator lanes it computes from its own TMEM lanes: a row's scale at its lane,
+// word (row % 64) / 32 of the A scale columns (M=128; row / 32 at M=256), and output
+// column c's weight scale at lane 32 * quarter + c % 32, word (c % 128) / 32 of the
+// B scale columns.  So the replicated 32-row atoms serve M=256 (two atoms for the two
+// 128-column halves); at M=128 the quarters holding columns [128,256) need the second
+// weight atom in the same columns as the first: those units stage a 128-row image
+// (atom 0 in quarters 0-1, atom 1 in quarters 2-3) and copy it unreplicated.  The odd
+// CTA could only hold a tile's rows 64-127 at M=128 with their scales moved to words
+// 0-1, which no copy can do, hence the M=256 form for longer singles.
+// Singles run in the same launch as the pairs and next to them (same item group, N
+// tiles interleaved), so they read the weight tiles the pairs just brought into L2.
+// The pair instruction issues about 1.5x the FLOPs per SM-cycle of the one-CTA M=128
+// form, and each SM moves 16 KB of weights per 128-deep k-block instead of 32 KB.
+// Both CTAs' TMA loads complete on the even CTA's stage barrier, and the MMA commits
+// free the stage in both.  A stage holds KB2 k-blocks (256 K): the issuing thread
+// waits, fences and commits once per eight MMAs, which keeps the pair's tensor pipe fed.
 constexpr int KB2 = 2, S2 = 3;              // k-blocks per stage, stages
 constexpr uint32_t BH_BYTES = B_BYTES / 2;  // a CTA's half of a k-block's weight tile
 constexpr uint32_t O2_A = 0;
@@ -666,24 +530,26 @@ constexpr uint32_t O2_MISC = O2_BAR + (2 * S2 + 2) * 8;
 constexpr uint32_t O2_AMAX = O2_MISC + 16;
 constexpr uint32_t O2_UNITQ = O2_AMAX + 2 * 128 * 4;
 constexpr uint32_t O2_UBAR = O2_UNITQ + kUnitQ * 32;
-constexpr uint32_t SMEM2_BYTES = O2_UBAR + 2 * kUnitQ * 8 + 1024;
-constexpr uint32_t TMEM_SF2 = 256;  // scale columns of stage s, k-block h: +32 s + 16 h
-static_assert(TMEM_SF2 + 32 * S2 <= TMEM_COLS, "TMEM columns");
+constexpr uint32_t O2_XBUF = O2_UBAR + 2 * kUnitQ * 8;  // [2 halves][32 columns][64 rows] fp32
+constexpr uint32_t XBUF_BYTES = 2 * 32 * 64 * 4;
+constexpr uint32_t SMEM2_BYTES = O2_XBUF + XBUF_BYTES + 1024;
+constexpr uint32_t TMEM_SF2 = 256;  // scale columns of stage s, k-block h: +16 (KB2 s + h)
+static_assert(TMEM_SF2 + 16 * KB2 * S2 <= TMEM_COLS, "TMEM columns");
+static_assert(SMEM2_BYTES <= 232448, "shared memory of the 2-SM kernel");
 
 struct Unit2 {
   int row0, nvalid;  // this CTA's tile, when active
   int we, ni, band;
   uint32_t tx;       // bytes one stage brings into both CTAs (expected on the even CTA)
-  bool ok, active, end;
+  bool ok, active, end, m128;
 };
 static_assert(sizeof(Unit2) <= 32, "unit ring slot");
 
-// Work unit -> the pair item's 2-SM unit in *out: returns 1; 0 for a unit of a single
-// tile (the one-CTA launch that follows takes those); -1 when the unit's entries do not
-// describe tiles inside the operands.  Both CTAs decode alike: `rank` only selects which
-// of the two tiles fills row0 / nvalid / active.
-__device__ __forceinline__ int get_pair2_unit(const GemmParams &P, int unit, int units2,
-                                              int rank, Unit2 *out) {
+// Work unit -> the item's 2-SM unit.  Both CTAs decode alike: `rank` only selects which
+// tile fills row0 / nvalid / active.  U.ok is false when the entries do not describe
+// tiles inside the operands (every role then skips the unit).
+__device__ __forceinline__ Unit2 get_2sm_unit(const GemmParams &P, int unit, int units2,
+                                              int rank) {
   const int32_t *tl = P.tiles;
   int u = unit;
   const bool second = unit < units2;
@@ -691,39 +557,39 @@ __device__ __forceinline__ int get_pair2_unit(const GemmParams &P, int unit, int
     tl = P.tiles2;
   else
     u -= units2;
+  Unit2 U = {};
   const int cap = second ? tl[0] : P.max_tiles;
   const int nitems = tl[4];
   const int32_t *items = tl + 8 + 8 * (size_t)cap;
-  const int g = u / P.n_tiles;
-  if (g >= nitems) return -1;
+  const int g = u / P.n_tiles;  // some item of the right group
+  if (g >= nitems) return U;
   const int gf = items[8 * g + 2], gc = items[8 * g + 3];
-  if (gf < 0 || gc < 1 || g < gf || g >= gf + gc || gf + gc > nitems) return -1;
+  // the item must lie inside the group it names (so local >= 0 below)
+  if (gf < 0 || gc < 1 || g < gf || g >= gf + gc || gf + gc > nitems) return U;
   const int local = u - P.n_tiles * gf;
-  const int ni = local / gc;
-  if (ni >= P.n_tiles) return -1;
+  U.ni = local / gc;
+  if (U.ni >= P.n_tiles) return U;
   const int32_t *it = items + 8 * (gf + local % gc);
-  if (it[4] == 0) return 0;
-  const int tile[2] = {it[0], it[1]};  // one expert's two tiles, one per CTA
-  Unit2 &U = *out;
-  U.ok = U.active = U.end = false;
-  U.row0 = U.nvalid = 0;
-  U.ni = ni;
-  if (tile[0] < 0 || tile[0] >= cap) return -1;
+  const bool pair = it[4] != 0;
+  const int tile[2] = {it[0], pair ? it[1] : -1};  // pair: one expert's two tiles
+  if (tile[0] < 0 || tile[0] >= cap || (pair && (tile[1] < 0 || tile[1] >= cap))) return U;
   const int32_t *e = tl + 8 + 8 * tile[0];
   U.we = second ? P.expert2 : (P.phys2log ? P.phys2log[e[1]] : e[1]);
   U.band = e[4];
-  if (U.we < 0 || U.we >= P.num_experts) return -1;
-  uint32_t tx = 0;
+  if (U.we < 0 || U.we >= P.num_experts) return U;
+  U.m128 = !pair && e[2] > 0 && e[2] <= 64;
+  uint32_t tx = 2 * KB2 * BH_BYTES;  // both halves of the weight tile
   for (int c = 0; c < 2; ++c) {
-    tx += KB2 * BH_BYTES;
     const int mi = tile[c];
     if (mi < 0) continue;
-    if (mi >= cap) return -1;
     const int32_t *t = tl + 8 + 8 * mi;
+    if (pair && t[1] != e[1]) return U;  // a pair shares one expert's weights
     const int row0 = t[0] + (second ? P.row_offset2 : 0), nv = t[2];
-    if (!tile_ok(P, row0, nv)) return -1;
+    if (!tile_ok(P, row0, nv)) return U;
     const int slices = nv == BM ? 0 : (nv + 31) / 32;
-    tx += KB2 * ((slices ? slices * (A_BYTES / 4) : A_BYTES) + SFA_BYTES + SFB_BYTES);
+    // an M=128 unit's weight scales come as a 128-row image (4 atoms per k-block)
+    tx += KB2 * ((slices ? slices * (A_BYTES / 4) : A_BYTES) + SFA_BYTES +
+                 (U.m128 ? 2 * SFB_BYTES : SFB_BYTES));
     if (c == rank) {
       U.row0 = row0;
       U.nvalid = nv;
@@ -732,15 +598,116 @@ __device__ __forceinline__ int get_pair2_unit(const GemmParams &P, int unit, int
   }
   U.tx = tx;
   U.ok = true;
-  return 1;
+  return U;
+}
+
+// Epilogue of an M=128 pair accumulator in the even CTA (the tile's rows 0-63): TMEM
+// lanes 0-63 hold output columns [0,128) of rows 0-63, lanes 64-127 columns
+// [128,256) of the same rows; each thread takes 64 of its lane's 128 columns.  For
+// GATEUP the lower lanes hold gate, the upper lanes up: the up values pass through
+// shared memory (xbuf, 32 columns at a time) to the gate thread of the same row, which
+// forms h = silu(g) * u, requantises it and stores it.  All kEpiThreads epilogue
+// threads call it.
+template <class Release>
+__device__ __forceinline__ void epilogue_m128(const GemmParams &P, int row0, int valid, int ni,
+                                              uint32_t t_row, int q, int half, int warp,
+                                              int lane, float *amax_x, float *xbuf,
+                                              Release release) {
+  const int m = 32 * (q & 1) + lane;  // row of the tile
+  const bool upper = q >= 2;          // columns [128, 256)
+  const int64_t r = (int64_t)row0 + m;
+  const bool store = m < valid && r < P.rows;
+  uint32_t v[64];
+  MOE_TMEM_LD_32x32b_X32(t_row + 64 * half, v);
+  MOE_TMEM_LD_32x32b_X32(t_row + 64 * half + 32, (v + 32));
+  tc_wait_ld();
+  tc_fence_before();
+  release();
+  if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int rd = 0; rd < 2; ++rd) {
+      if (upper) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) xbuf[(half * 32 + c) * 64 + m] = __uint_as_float(v[32 * rd + c]);
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      if (!upper) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float gf = __uint_as_float(v[32 * rd + c]);
+          const float uf = xbuf[(half * 32 + c) * 64 + m];
+          const float h = __fdividef(gf, 1.0f + __expf(-gf)) * uf;  // silu(g) * u
+          v[32 * rd + c] = __float_as_uint(h);
+          amax = fmaxf(amax, fabsf(h));
+        }
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+    }
+    // the 1x128 block of h spans both column halves
+    if (!upper) amax_x[half * 128 + m] = amax;
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+    if (!upper) amax = fmaxf(amax, amax_x[(half ^ 1) * 128 + m]);
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+    if (!upper && store) {
+      const int e = ue8m0_exp(amax);
+      const float inv = pow2i(-e);
+      uint8_t *dst = P.out + (size_t)r * P.I + (size_t)ni * 128 + 64 * half;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 w;
+        uint32_t *wp = &w.x;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int b = 16 * c + 4 * j;
+          wp[j] = e4m3x2(__fmul_rn(__uint_as_float(v[b]), inv),
+                         __fmul_rn(__uint_as_float(v[b + 1]), inv)) |
+                  (e4m3x2(__fmul_rn(__uint_as_float(v[b + 2]), inv),
+                          __fmul_rn(__uint_as_float(v[b + 3]), inv))
+                   << 16);
+        }
+        *reinterpret_cast<uint4 *>(dst + 16 * c) = w;
+      }
+      if (half == 0)
+        *reinterpret_cast<uint32_t *>(P.out_sf + sf_atom_off(r, ni, P.I / 128)) =
+            (uint32_t)(e + 127) * 0x01010101u;
+    }
+  } else {
+    if (store) {
+      uint8_t *dst =
+          P.out + ((size_t)r * P.n + (size_t)ni * 256 + (upper ? 128 : 0) + 64 * half) * 2;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint4 w;
+        w.x = f32_to_bf16_bits(__uint_as_float(v[8 * j + 0])) |
+              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 1])) << 16);
+        w.y = f32_to_bf16_bits(__uint_as_float(v[8 * j + 2])) |
+              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 3])) << 16);
+        w.z = f32_to_bf16_bits(__uint_as_float(v[8 * j + 4])) |
+              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 5])) << 16);
+        w.w = f32_to_bf16_bits(__uint_as_float(v[8 * j + 6])) |
+              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 7])) << 16);
+        *reinterpret_cast<uint4 *>(dst + 16 * j) = w;
+      }
+    }
+    if (P.signal) {
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      if (warp == 2 && lane == 0) {
+        for (int j = 0; j * P.bm_signal < BM; ++j)
+          if (j * P.bm_signal < valid && row0 + j * P.bm_signal < P.rows)
+            red_release_gpu_add(P.signal + (row0 + j * P.bm_signal) / P.bm_signal, 1);
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    grouped_gemm_pair2_kernel(const __grid_constant__ CUtensorMap tmA,
-                              const __grid_constant__ CUtensorMap tmA32,
-                              const __grid_constant__ CUtensorMap tmW,
-                              const __grid_constant__ CUtensorMap tmSFA,
-                              const __grid_constant__ CUtensorMap tmSFW, const GemmParams P) {
+    grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmA32,
+                            const __grid_constant__ CUtensorMap tmW,
+                            const __grid_constant__ CUtensorMap tmSFA,
+                            const __grid_constant__ CUtensorMap tmSFW, const GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -822,6 +789,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           continue;
         }
         const int we = U.we, ni = U.ni;
+        // a weight tile read by another unit of the expert (its other pairs or its
+        // single, scheduled beside this one) stays in L2
         const uint64_t pol_w = U.band > 2 ? pol_keep : pol_stream;
         const int a_slices = U.nvalid == BM ? 0 : (U.nvalid + 31) / 32;
         int wrow, nb0, nb1;
@@ -863,9 +832,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // scale atoms of consecutive k-blocks are adjacent: one box per stage each
             tma_load_2d_pair(s_base + O2_SFA + stage * KB2 * SFA_BYTES, &tmSFA, fb, 0,
                              sfa_atom + kb, pol_a);
-            const uint32_t ssfb = s_base + O2_SFB + stage * KB2 * SFB_BYTES;
-            tma_load_2d_pair(ssfb, &tmSFW, fb, 0, sfb_atom0 + kb, pol_w);
-            tma_load_2d_pair(ssfb + KB2 * 512, &tmSFW, fb, 0, sfb_atom1 + kb, pol_w);
+            if (U.m128) {
+              // the weight scale image of an M=128 unit: atom 0 in rows 0-63, atom 1 in
+              // rows 64-127, in the A slot's upper half (its rows 64-127 are never read);
+              // only the even CTA is active here, so its own barrier takes the bytes
+#pragma unroll
+              for (int h = 0; h < KB2; ++h) {
+                const uint32_t img = sa + h * A_BYTES + A_BYTES / 2;
+                const uint8_t *a0 = P.W_sf + (size_t)(sfb_atom0 + kb + h) * 512;
+                const uint8_t *a1 = P.W_sf + (size_t)(sfb_atom1 + kb + h) * 512;
+                bulk_load(img, a0, 512, bar_full + 8 * stage);
+                bulk_load(img + 512, a0, 512, bar_full + 8 * stage);
+                bulk_load(img + 1024, a1, 512, bar_full + 8 * stage);
+                bulk_load(img + 1536, a1, 512, bar_full + 8 * stage);
+              }
+            } else {
+              const uint32_t ssfb = s_base + O2_SFB + stage * KB2 * SFB_BYTES;
+              tma_load_2d_pair(ssfb, &tmSFW, fb, 0, sfb_atom0 + kb, pol_w);
+              tma_load_2d_pair(ssfb + KB2 * 512, &tmSFW, fb, 0, sfb_atom1 + kb, pol_w);
+            }
           }
           ++issued;
           if (++stage == S2) {
@@ -896,9 +881,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // N = 256, UE8M0 scales, M = 256 over the pair; bits 4-5 / 29-30 pick the scale byte
-      const uint32_t idesc_base = ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
-                                  ((uint32_t)((2 * BM) >> 4) << 24);
+      // N = 256, UE8M0 scales, M = 256 (or 128) over the pair; bits 4-5 / 29-30 pick
+      // the scale byte
+      const uint32_t idesc_n = ((uint32_t)(BN >> 3) << 17) | (1u << 23);
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -911,6 +896,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         release_unit(seq);
         if (U.end) break;
         if (!U.ok || rank != 0) continue;  // the odd CTA only follows the unit stream
+        const uint32_t idesc_base = idesc_n | ((uint32_t)((U.m128 ? BM : 2 * BM) >> 4) << 24);
         if (!mbar_wait_cluster(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
           fail(P.status, abort);
           break;
@@ -930,11 +916,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sb = s_base + O2_B + stage * KB2 * BH_BYTES;
 #pragma unroll
           for (int h = 0; h < KB2; ++h) {
-            const uint32_t t_sfa = tmem + TMEM_SF2 + 32 * stage + 16 * h;
+            const uint32_t t_sfa = tmem + TMEM_SF2 + 16 * (KB2 * stage + h);
             const uint32_t t_sfb = t_sfa + 4;
             tc_cp_pair_32x128b_x4(t_sfa, smem_desc(ssfa + 512 * h, 16, 128, 0));
-            tc_cp_pair_32x128b_x4(t_sfb, smem_desc(ssfb + 512 * h, 16, 128, 0));
-            tc_cp_pair_32x128b_x4(t_sfb + 4, smem_desc(ssfb + KB2 * 512 + 512 * h, 16, 128, 0));
+            if (U.m128) {
+              tc_cp_pair_128x128b(t_sfb, smem_desc(sa + h * A_BYTES + A_BYTES / 2, 16, 128, 0));
+            } else {
+              tc_cp_pair_32x128b_x4(t_sfb, smem_desc(ssfb + 512 * h, 16, 128, 0));
+              tc_cp_pair_32x128b_x4(t_sfb + 4, smem_desc(ssfb + KB2 * 512 + 512 * h, 16, 128, 0));
+            }
 #pragma unroll
             for (int j = 0; j < BK / 32; ++j) {
               const uint64_t ad = smem_desc(sa + h * A_BYTES + 32 * j, 16, 1024, 2);
@@ -961,6 +951,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row_local = 32 * q + lane;
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
     float *amax_x = reinterpret_cast<float *>(smem + O2_AMAX);
+    float *xbuf = reinterpret_cast<float *>(smem + O2_XBUF);
     const uint32_t lead_acc_empty = mapa_shared(bar_acc_empty, 0);
     auto release_acc = [&] {
       __syncwarp();
@@ -982,12 +973,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      if (U.active) {
-        epilogue_tile(P, U.row0, U.nvalid, U.ni, t_row, half, row_local, warp, lane, amax_x,
-                      release_acc);
-      } else {  // this CTA's rows of the pair MMA carry no tile
+      if (!U.active) {  // this CTA's rows of the pair MMA carry no tile
         tc_fence_before();
         release_acc();
+      } else if (U.m128) {
+        epilogue_m128(P, U.row0, U.nvalid, U.ni, t_row, q, half, warp, lane, amax_x, xbuf,
+                      release_acc);
+      } else {
+        epilogue_tile(P, U.row0, U.nvalid, U.ni, t_row, half, row_local, warp, lane, amax_x,
+                      release_acc);
       }
       acc_phase ^= 1;
     }
@@ -1007,11 +1001,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       return true;
     };
     bool ok = true;
-    for (int unit = first_unit; ok && unit < total; unit += ustride) {
-      Unit2 U = {};
-      const int n = get_pair2_unit(P, unit, units2, rank, &U);
-      if (n != 0) ok = push(U);  // -1: U.ok is false, and the producer records it
-    }
+    // U.ok false: every role skips the unit, and the producer records it
+    for (int unit = first_unit; ok && unit < total; unit += ustride)
+      ok = push(get_2sm_unit(P, unit, units2, rank));
     if (ok) {
       Unit2 end = {};
       end.end = true;
@@ -1135,9 +1127,11 @@ extern "C" int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf,
 extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   if (!a) return MOE_ERR_INVALID;
   if (a->op != MOE_GEMM_GATEUP_SWIGLU && a->op != MOE_GEMM_DOWN) return MOE_ERR_INVALID;
+  if (a->pair_tiles != 0 && a->pair_tiles != 1) return MOE_ERR_INVALID;
   if (a->n <= 0 || a->k <= 0 || a->rows <= 0 || a->max_tiles <= 0 || a->num_experts <= 0)
     return MOE_ERR_INVALID;
   if (a->n % 256 || a->k % 128 || a->rows % 128) return MOE_ERR_UNSUPPORTED;
+  if (a->pair_tiles && a->k % (KB2 * BK)) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)a->num_experts * a->n > INT32_MAX || a->rows > INT32_MAX) return MOE_ERR_UNSUPPORTED;
   if (!a->A || !a->A_sf || !a->W || !a->W_sf || !a->tiles || !a->out) return MOE_ERR_INVALID;
   if (a->op == MOE_GEMM_GATEUP_SWIGLU && (!a->out_sf || a->signal)) return MOE_ERR_INVALID;
@@ -1176,47 +1170,31 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.signal = a->signal;
   P.bm_signal = a->block_m_signal > 0 ? a->block_m_signal : BM;
   P.status = a->status;
-  P.singles = 0;
   static bool attr_set[kMaxDevices] = {};
-  static int max_clusters[kMaxDevices] = {}, max_clusters2[kMaxDevices] = {};
+  static int max_clusters[kMaxDevices] = {};
   const int dev = device_slot();
   if (dev < 0) return dev;
   if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_gemm_pair2_kernel,
+      e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
     if (e != cudaSuccess) return set_cuda_error(e);
     attr_set[dev] = true;
   }
   const int sms = a->num_sms > 0 ? a->num_sms : device_sm_count();
-  if (a->pair_tiles == 2) {
-    if (a->k % (KB2 * BK)) return MOE_ERR_UNSUPPORTED;
+  if (a->pair_tiles) {
     CUtensorMap mSFA, mSFW;
     if (!make_sf_map(&mSFA, a->A_sf, (uint64_t)(a->rows / 128) * (a->k / BK), KB2) ||
         !make_sf_map(&mSFW, a->W_sf, (uint64_t)a->num_experts * (a->n / 128) * (a->k / BK), KB2))
       return MOE_ERR_CUDA;
-    // the pairs on 2-SM MMAs, then the single tiles on one CTA each
-    int rc = launch_pairs(grouped_gemm_pair2_kernel, SMEM2_BYTES, sms, max_clusters2[dev],
-                          as_stream(stream), mA, mA32, mW, mSFA, mSFW, P);
-    if (rc) return rc;
-    P.singles = 1;
-    grouped_gemm_kernel<false><<<sms, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32,
-                                                                                    mW, P);
-    return check_launch();
-  }
-  if (a->pair_tiles) {
-    return launch_pairs(grouped_gemm_kernel<true>, SMEM_BYTES, sms, max_clusters[dev],
-                        as_stream(stream), mA, mA32, mW, P);
+    return launch_pairs(grouped_gemm_2sm_kernel, SMEM2_BYTES, sms, max_clusters[dev],
+                        as_stream(stream), mA, mA32, mW, mSFA, mSFW, P);
   }
   const int64_t max_units = a->tiles2 ? sms : a->max_tiles * (a->n / BN);
   const int grid = (int)(max_units < sms ? max_units : sms);
-  grouped_gemm_kernel<false><<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW,
-                                                                                    P);
+  grouped_gemm_kernel<<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW, P);
   return check_launch();
 }

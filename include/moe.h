@@ -48,10 +48,9 @@
  *   tile i at tiles[8 + 8*i ...]: {first row, physical expert, valid rows (1..128),
  *   first tile of this expert, number of tiles of this expert, 0, 0, 0};
  *   work item k at tiles[8 + 8*max_tiles + 8*k ...]: {tile 0, tile 1 or -1, first
- *   item of its group, items in its group, 1 if both tiles share one expert's
- *   weights, 0, 0, 0}.  An expert's tiles form pairs two by two; an odd last tile
- *   is a single, and singles form items two by two; items are listed so that a
- *   couple of singles follows the pairs of the expert that completes it.
+ *   item of its group, items in its group, 1 for a pair of one expert's tiles (0 for
+ *   a single tile), 0, 0, 0}.  An expert's tiles form pairs two by two, and an odd
+ *   last tile is a single; an expert's pairs and its single form one group.
  * Tiles of one expert are consecutive.  The grouped GEMM reads this list on the
  * device, so the host never needs the routing result.
  */
@@ -302,14 +301,13 @@ typedef struct moe_gemm_args {
   int32_t *signal;
   int block_m_signal;
   int num_sms;
-  int pair_tiles; /* 0: one CTA per M tile.
-                     1: 2-CTA clusters take an expert's M tiles two by two and share
-                        each weight tile (multicast), for experts with several M tiles.
-                     2: an expert's tile pairs run as 2-SM MMAs (M = 256 over the
-                        CTA pair, each SM holding half of the weight tile), then the
-                        single tiles run one per CTA in a second launch; needs
-                        k % 256 == 0 (else MOE_ERR_UNSUPPORTED).  Faster than 1 for
-                        experts with many M tiles and long K, slower for short K. */
+  int pair_tiles; /* 0: one CTA per M tile (128x256 MMAs).
+                     1: CTA pairs on one TPC share each weight tile, half of it in
+                        each SM: an expert's tile pairs run as M = 256 pair MMAs and its
+                        single tile, in the same launch, as an M = 128 pair MMA (up to 64
+                        valid rows) or an M = 256 one with the second half idle; needs
+                        k % 256 == 0 (else MOE_ERR_UNSUPPORTED).
+                     Other values: MOE_ERR_INVALID.  Both give the same bytes. */
   int32_t *status;
 } moe_gemm_args;
 
@@ -389,8 +387,10 @@ typedef struct moe_layer {
                                            moe_dispatch_max_tiles of the layer's dispatch
                                            (else MOE_ERR_INVALID before any launch) */
   int num_sms, combine_ctas;
-  int gemm_pairs; /* pair_tiles of both GEMMs.  0: 1 when B*K/N_phys >= 128, else 0;
-                     1: always 1; 2: always 2 (H and I multiples of 256); -1: always 0 */
+  int gemm_pairs; /* pair_tiles of both GEMMs.  0: 1 when B*K >= 128*N_phys and H and I
+                     are multiples of 256, else 0; 1: always 1 (MOE_ERR_UNSUPPORTED
+                     unless H and I are multiples of 256); -1: always 0; other values:
+                     MOE_ERR_INVALID */
   /* inputs and weights */
   void *x;                                         /* bf16 [B][H] */
   const float *W_router, *bias;                    /* [N][H], [N] or NULL */

@@ -92,21 +92,14 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 def cluster_items(ntiles):
     """Expected work items of a tile list for tile counts per expert (in expert order):
-    an expert's pairs [t, t+1, group first, group size, 1], then, when its odd last
-    tile completes a couple of singles, [earlier single, its single, k, 1, 0] (or
-    [its single, -1, k, 1, 0] for a lone last single)."""
-    items, first, sidx, prev = [], 0, 0, None
-    total_singles = sum(n % 2 for n in ntiles)
+    an expert's pairs [t, t+1, group first, group size, 1], then its odd last tile
+    [t, -1, group first, group size, 0], all in one group."""
+    items, first = [], 0
     for n in ntiles:
-        npair, f_item = n // 2, len(items)
-        for j in range(npair):
-            items.append([first + 2 * j, first + 2 * j + 1, f_item, npair, 1])
-        if n % 2:
-            mine = first + n - 1
-            if sidx % 2 == 1:
-                items.append([prev, mine, len(items), 1, 0])
-            elif sidx == total_singles - 1:
-                items.append([mine, -1, len(items), 1, 0])
-            prev, sidx = mine, sidx + 1
+        npair, gc, f_item = n // 2, n // 2 + n % 2, len(items)
+        for j in range(gc):
+            pair = j < npair
+            items.append([first + 2 * j, first + 2 * j + 1 if pair else -1, f_item, gc,
+                          1 if pair else 0])
         first += n
     return items

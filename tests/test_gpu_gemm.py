@@ -126,11 +126,17 @@ def cluster_tile_list(tiles_per_expert, nvalid_of) -> np.ndarray:
     return t
 
 
+# valid rows of tile j of an expert: singles of 108-128 rows (M=256 pair MMAs with the
+# odd CTA idle) or of 1-64 rows (M=128 pair MMAs), ragged pairs in both
+NVALID = {"long_singles": lambda j: 128 - 5 * j, "short_singles": lambda j: [64, 100, 37, 128, 1][j]}
+
+
+@pytest.mark.parametrize("pattern", sorted(NVALID))
 @pytest.mark.parametrize("op", [0, 1])
-def test_cluster_pair_gemm_equals_single_cta(dev, op):
-    """Two-CTA clusters (pairs sharing a weight tile, singles two by two) give the same
-    bytes as one CTA per tile, for experts with 1, 2, 3 and 5 M tiles (three singles:
-    the last cluster item has one idle CTA)."""
+def test_2sm_gemm_equals_single_cta(dev, op, pattern):
+    """The 2-SM kernel (an expert's tile pairs on M=256 pair MMAs, its odd last tile in
+    the same launch as an M=128 or M=256 pair MMA) gives the same bytes as one CTA per
+    tile, for experts with 1, 2, 3 and 5 M tiles."""
     tiles_per_expert = [1, 2, 3, 5, 2]
     E = len(tiles_per_expert)
     k, n = (512, 512) if op == 0 else (256, 768)
@@ -139,34 +145,43 @@ def test_cluster_pair_gemm_equals_single_cta(dev, op):
     q, sf = activations(rows, k, 7)
     W, Wsf = zip(*[inputs.make_fp8_matrix(n, k, (9, 55, e)) for e in range(E)])
     W, Wsf = np.stack(W), np.stack(Wsf)
-    t = cluster_tile_list(tiles_per_expert, lambda j: 128 - 5 * j)
+    t = cluster_tile_list(tiles_per_expert, NVALID[pattern])
     A = torch.from_numpy(q).to(dev)
     A_sf = torch.from_numpy(pack_sf_atoms(sf)).to(dev)
     Wd = torch.from_numpy(W).to(dev)
     Wa = api.pack_weight_scales(torch.from_numpy(Wsf).to(dev))
     tl = torch.from_numpy(t).to(dev)
     outs = []
-    for pairs in (0, 1, 2):
+    for pairs in (0, 1):
         st = api.new_status(dev)
         o = api.grouped_gemm_fp8(op, A, A_sf, Wd, Wa, tl, mt, status=st, pair_tiles=pairs)
         torch.cuda.synchronize()
         assert api.read_status(st) == 0
         outs.append(o)
     res = [o.view(torch.int16) if op == 1 else o[0] for o in outs]
-    for b in res[1:]:
-        for i0 in range(mt):                  # rows each tile stores
-            nvalid = t[8 + 8 * i0 + 2]
-            assert torch.equal(res[0][128 * i0: 128 * i0 + nvalid],
-                               b[128 * i0: 128 * i0 + nvalid]), i0
+    for i0 in range(mt):                      # rows each tile stores
+        nvalid = t[8 + 8 * i0 + 2]
+        assert torch.equal(res[0][128 * i0: 128 * i0 + nvalid],
+                           res[1][128 * i0: 128 * i0 + nvalid]), i0
+    if op == 0:                               # and the h scales of those rows
+        from support import unpack_sf_atoms
+        valid = np.zeros(rows, bool)
+        for i0 in range(mt):
+            valid[128 * i0: 128 * i0 + t[8 + 8 * i0 + 2]] = True
+        sfs = [unpack_sf_atoms(o[1].cpu().numpy(), rows, n // 256, check_rows=valid)
+               for o in outs]
+        assert np.array_equal(sfs[0][valid], sfs[1][valid])
 
 
 @pytest.mark.parametrize("k", [768, 4352])
-@pytest.mark.parametrize("pairs", [0, 1, 2])
-def test_weight_scale_bytes_per_block(dev, pairs, k):
+@pytest.mark.parametrize("pairs", [0, 1])
+@pytest.mark.parametrize("last", [128, 50])
+def test_weight_scale_bytes_per_block(dev, pairs, k, last):
     """Weight scale bytes drawn per 128x128 block over 21 binades, K of 6 and 34
     k-blocks: the down GEMM still equals the fp64 product of the dequantised operands
     in every scheduling mode (a scale atom read for the wrong block, k-block or row
-    half moves an output by a power of two)."""
+    half moves an output by a power of two), with full last tiles and with 50-row last
+    tiles (the 2-SM kernel's M=128 singles)."""
     tiles_per_expert = [2, 3, 1]
     E, n = len(tiles_per_expert), 512
     mt = sum(tiles_per_expert)
@@ -174,7 +189,15 @@ def test_weight_scale_bytes_per_block(dev, pairs, k):
     q, sf = activations(rows, k, 11)
     W = np.stack([inputs.make_fp8_matrix(n, k, (12, 3, e))[0] for e in range(E)])
     Wsf = np.random.default_rng(13).integers(117, 138, (E, n // 128, k // 128)).astype(np.uint8)
+    nv = {}
+    i = 0
+    for c in tiles_per_expert:
+        for j in range(c):
+            nv[i + j] = last if j == c - 1 else 128
+        i += c
     t = cluster_tile_list(tiles_per_expert, lambda j: 128)
+    for i0, v in nv.items():
+        t[8 + 8 * i0 + 2] = v
     st = api.new_status(dev)
     out = api.grouped_gemm_fp8(api.GEMM_DOWN, torch.from_numpy(q).to(dev),
                                torch.from_numpy(pack_sf_atoms(sf)).to(dev),
@@ -185,12 +208,14 @@ def test_weight_scale_bytes_per_block(dev, pairs, k):
     assert api.read_status(st) == 0
     got = oracle.bf16_to_f32(bits(out)).astype(np.float64)
     a = oracle.dequant_rows(q, sf)
-    r0 = 0
+    i = 0
     for e, c in enumerate(tiles_per_expert):
-        m = slice(r0, r0 + 128 * c)
-        ref = a[m] @ oracle.dequant_blocks(W[e], Wsf[e]).T
-        refb = oracle.bf16_to_f32(oracle.f32_to_bf16(ref.astype(np.float32))).astype(np.float64)
-        # bf16 rounding of the fp32 sum, plus fp32 accumulation error growing ~ sqrt(k)
-        tol = np.abs(refb) * 2.0 ** -7 + 2e-6 * np.sqrt(k / 768) * np.abs(ref).max()
-        assert np.all(np.abs(got[m] - refb) <= tol), e
-        r0 += 128 * c
+        wd = oracle.dequant_blocks(W[e], Wsf[e])
+        for j in range(c):
+            m = slice(128 * (i + j), 128 * (i + j) + nv[i + j])
+            ref = a[m] @ wd.T
+            refb = oracle.bf16_to_f32(oracle.f32_to_bf16(ref.astype(np.float32))).astype(np.float64)
+            # bf16 rounding of the fp32 sum, plus fp32 accumulation error growing ~ sqrt(k)
+            tol = np.abs(refb) * 2.0 ** -7 + 2e-6 * np.sqrt(k / 768) * np.abs(ref).max()
+            assert np.all(np.abs(got[m] - refb) <= tol), (e, j)
+        i += c
