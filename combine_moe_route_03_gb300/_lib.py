@@ -87,6 +87,7 @@ SIGNATURES = {
     "moe_dispatch_noalloc": (_c_int, [ctypes.POINTER(DispatchCfg)] + [_vp] * 15),
     "moe_grouped_gemm_fp8": (_c_int, [ctypes.POINTER(GemmArgs), _vp]),
     "moe_packed_scale_bytes": (_c_sz, [_c_int, _c_int, _c_int]),
+    "moe_scale_bytes": (_c_sz, [_c_i64, _c_int]),
     "moe_pack_weight_scales": (_c_int, [_c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "moe_combine": (_c_int, [ctypes.POINTER(CombineCfg), _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_read_status": (_c_int, [_vp, _vp]),

@@ -200,7 +200,7 @@ def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=N
     o = out if out is not None else {}
     if "A" not in o:
         o["A"] = torch.empty((rows, H * (2 if fmt == FMT_BF16 else 1)), dtype=torch.uint8, device=dev)
-        o["A_sf"] = torch.empty(rows * (H // 128) * 4, dtype=torch.uint8, device=dev)
+        o["A_sf"] = torch.empty(scale_bytes(rows, H), dtype=torch.uint8, device=dev)
         o["counts"] = torch.empty(cfg.N_phys, dtype=torch.int32, device=dev)
         o["row_of"] = torch.empty((B, cfg.K), dtype=torch.int32, device=dev)
         o["src_of"] = torch.empty(rows, dtype=torch.int32, device=dev)
@@ -209,7 +209,7 @@ def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=N
         if shared:
             srows = (B + 127) // 128 * 128
             o["As"] = torch.empty((srows, H), dtype=torch.uint8, device=dev)
-            o["As_sf"] = torch.empty(srows * (H // 128) * 4, dtype=torch.uint8, device=dev)
+            o["As_sf"] = torch.empty(scale_bytes(srows, H), dtype=torch.uint8, device=dev)
             o["shared_tiles"] = torch.empty(8 + 16 * (srows // 128), dtype=torch.int32, device=dev)
     st = status if status is not None else new_status(dev)
     check(load().moe_dispatch(ctypes.byref(dc), ptr(x), ptr(topk_idx), ptr(log2phys), ptr(rep),
@@ -219,6 +219,14 @@ def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=N
                               o["ws"].numel(), ptr(st), stream_ptr(stream)), "moe_dispatch")
     o.update(rows=rows, max_tiles=mt, status=st)
     return o
+
+
+def scale_bytes(rows: int, k: int) -> int:
+    """Bytes of the SF atoms of an activation tensor [rows][k] (moe_scale_bytes)."""
+    n = load().moe_scale_bytes(rows, k)
+    if n == 0:
+        raise ValueError(f"scale atoms need rows and k multiples of 128 (got {rows}, {k})")
+    return n
 
 
 def pack_weight_scales(W_sf: torch.Tensor, stream=None) -> torch.Tensor:
@@ -248,7 +256,7 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
         I = n // 2
         if out is None:
             out = torch.empty((rows, I), dtype=torch.uint8, device=dev)
-            out_sf = torch.empty(rows * (I // 128) * 4, dtype=torch.uint8, device=dev)
+            out_sf = torch.empty(scale_bytes(rows, I), dtype=torch.uint8, device=dev)
     elif out is None:
         out = torch.empty((rows, n), dtype=torch.bfloat16, device=dev)
     st = status if status is not None else new_status(dev)
@@ -340,9 +348,9 @@ class MoELayer:
         self.tiles = t(8 + 16 * self.max_tiles, dtype=torch.int32)
         self.shared_tiles = t(8 + 16 * (self.srows // 128), dtype=torch.int32) if cfg.shared else None
         self.A = t(rows, H)
-        self.A_sf = t(rows * (H // 128) * 4)
+        self.A_sf = t(scale_bytes(rows, H))
         self.H1 = t(rows, I)
-        self.H1_sf = t(rows * (I // 128) * 4)
+        self.H1_sf = t(scale_bytes(rows, I))
         self.Y = t(rows, H, dtype=torch.bfloat16)
         self.S = self.Y[self.rows:] if cfg.shared else None
         self.signal = t(rows // cfg.block_m_signal, dtype=torch.int32) if cfg.sbo else None

@@ -114,7 +114,6 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
     return MOE_ERR_INVALID;
   const int64_t srows = L->has_shared ? ((int64_t)rc.B + 127) / 128 * 128 : 0;
   const int64_t rows_all = L->rows + srows;
-  const size_t Hb = rc.H / 128, Ib = L->I / 128;
   mark(0);
   int rc_ = moe_route(&rc, L->x, L->W_router, L->bias, L->topk_idx, L->topk_w, L->expert_counts,
                       L->route_ws, L->route_ws_bytes, stream);
@@ -123,7 +122,7 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   uint8_t *A = static_cast<uint8_t *>(L->A), *A_sf = static_cast<uint8_t *>(L->A_sf);
   rc_ = moe_dispatch(&dc, L->x, L->topk_idx, L->log2phys, L->rep, A, A_sf, L->counts, L->row_of,
                      nullptr, L->tiles, L->has_shared ? A + L->rows * rc.H : nullptr,
-                     L->has_shared ? A_sf + L->rows * Hb * 4 : nullptr,
+                     L->has_shared ? A_sf + (size_t)L->rows * sf_groups(rc.H) * 4 : nullptr,
                      L->has_shared ? L->shared_tiles : nullptr, L->dispatch_ws,
                      L->dispatch_ws_bytes, L->status, stream);
   if (rc_) return rc_;
@@ -172,7 +171,6 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   cc.K = rc.K;
   const void *S = L->has_shared ? static_cast<uint8_t *>(L->Y) + (size_t)L->rows * rc.H * 2
                                 : nullptr;
-  (void)Ib;
   if (L->sbo) {
     if (!L->signal || !L->stream2 || L->stream2 == stream || L->block_m_signal <= 0 ||
         128 % L->block_m_signal)

@@ -100,6 +100,16 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// ------------------------------------------------------------ SF atoms
+// Scale atoms: one 512-byte atom per (128-row block, group of four 128-column blocks);
+// the byte of row r (0..127) for column block 4g + j sits at 16*(r%32) + 4*(r/32) + j.
+// Kg = column-block groups per row.
+__host__ __device__ __forceinline__ int sf_groups(int k) { return (k / 128 + 3) / 4; }
+__device__ __forceinline__ size_t sf_byte_off(int64_t r, int kb, int Kg) {
+  return ((size_t)(r >> 7) * Kg + (kb >> 2)) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5) +
+         (kb & 3);
+}
+
 // ------------------------------------------------------------- PTX: memory
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

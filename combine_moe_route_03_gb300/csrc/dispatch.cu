@@ -306,12 +306,6 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
   }
 }
 
-// Byte offset of row r's scale word for 128-column block kb in an SF-atom array
-// of Kb blocks per row.
-__device__ __forceinline__ size_t sf_atom_offset(int64_t r, int kb, int Kb) {
-  return ((size_t)(r >> 7) * Kb + kb) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5);
-}
-
 // One warp per task = (token, run of `cpt` chunks of kCols columns): each lane
 // quantises kCols/32 values (8 or 16), 128/(kCols/32) lanes share one 128-column
 // block's amax, and each lane stores 8 or 16 bytes into each of the K copies.  The
@@ -354,7 +348,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
   for (int k = 0; k < 16; ++k) rows[k] = __shfl_sync(0xffffffffu, my_row, k);
 
   const uint16_t *xr = x + (size_t)t * H;
-  const int Hb = H / 128;
+  const int Kg = sf_groups(H);
   for (int c = c0; c < c1; ++c) {
     const int h = c * kCols + kPer * lane;
     const bool act = h < H;
@@ -394,7 +388,7 @@ __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
       for (int i = 0; i < kPer / 4; ++i)
         q[i] = e4m3x2(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv)) |
                (e4m3x2(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv)) << 16);
-      const uint32_t sfw = (uint32_t)(e + 127) * 0x01010101u;
+      const uint8_t sfb = (uint8_t)(e + 127);
       const int kb = h >> 7;
       auto put = [&](uint8_t *dst) {
         if constexpr (kPer == 8)
@@ -408,12 +402,12 @@ __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
           if (k >= K || rows[k] < 0) continue;
           put(A + (size_t)rows[k] * H + h);
           if ((lane & (kBlk - 1)) == 0)
-            *reinterpret_cast<uint32_t *>(A_sf + sf_atom_offset(rows[k], kb, Hb)) = sfw;
+            A_sf[sf_byte_off(rows[k], kb, Kg)] = sfb;
         }
         if (As) {
           put(As + (size_t)t * H + h);
           if ((lane & (kBlk - 1)) == 0)
-            *reinterpret_cast<uint32_t *>(As_sf + sf_atom_offset(t, kb, Hb)) = sfw;
+            As_sf[sf_byte_off(t, kb, Kg)] = sfb;
         }
       }
     }

@@ -53,11 +53,15 @@ constexpr uint32_t OFF_UNITQ = OFF_AMAX + 2 * 128 * 4;  // [kUnitQ] decoded unit
 constexpr uint32_t OFF_UBAR = OFF_UNITQ + kUnitQ * 32;  // [kUnitQ] full, [kUnitQ] empty
 constexpr uint32_t SMEM_BYTES = OFF_UBAR + 2 * kUnitQ * 8 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_SF = 256;  // scale columns start here, 16 per stage
+// Scale columns start here: kSfSets rotating sets of 16 columns (A atom at +0, B atoms
+// at +4 and +8), one set per group of four k-blocks; a set is rewritten 4 * kSfSets
+// k-blocks after its last use.
+constexpr uint32_t TMEM_SF = 256;
+constexpr int kSfSets = 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct GemmParams {
-  int op, n, k, Kb, n_tiles, I;
+  int op, n, k, Kb, Kg, n_tiles, I;
   int64_t rows;
   const uint8_t *A_sf, *W_sf;
   const int32_t *phys2log, *tiles, *tiles2;
@@ -79,6 +83,7 @@ struct Unit {
 };
 
 static_assert(sizeof(Unit) <= 32, "unit ring slot");
+static_assert(TMEM_SF + 16 * kSfSets <= TMEM_COLS, "TMEM columns");
 
 __device__ __forceinline__ bool tile_ok(const GemmParams &P, int row0, int nvalid) {
   return row0 >= 0 && (int64_t)row0 + 128 <= P.rows && row0 % 128 == 0 && nvalid > 0 &&
@@ -120,9 +125,6 @@ __device__ __forceinline__ Unit get_unit(const GemmParams &P, int unit, int unit
   return r;
 }
 
-__device__ __forceinline__ size_t sf_atom_off(int64_t r, int kb, int Kb) {
-  return ((size_t)(r >> 7) * Kb + kb) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5);
-}
 
 __device__ __forceinline__ void fail(int32_t *status, volatile int *abort) {
   *abort = 1;
@@ -181,9 +183,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &P, int row0, int
         }
         *reinterpret_cast<uint4 *>(dst + 16 * c) = w;
       }
-      if (half == 0)
-        *reinterpret_cast<uint32_t *>(P.out_sf + sf_atom_off(r, ni, P.I / 128)) =
-            (uint32_t)(e + 127) * 0x01010101u;
+      if (half == 0) P.out_sf[sf_byte_off(r, ni, sf_groups(P.I))] = (uint8_t)(e + 127);
     }
   } else {
     // output columns [128*half, +128)
@@ -311,7 +311,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint64_t pol_w = U.band > 1 ? pol_keep : pol_stream;
         const int a_slices = U.nvalid == BM ? 0 : (U.nvalid + 31) / 32;  // 0: one full box
         const uint32_t a_bytes = a_slices ? a_slices * (A_BYTES / 4) : A_BYTES;
-        const uint32_t tx = a_bytes + SFA_BYTES + B_BYTES + SFB_BYTES;
+        // a group's scale atoms travel with its first k-block
+        const uint32_t tx = a_bytes + B_BYTES, tx_sf = SFA_BYTES + SFB_BYTES;
         int wrow0, wrow1, nb0, nb1;
         if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
           wrow0 = we * P.n + ni * 128;
@@ -324,9 +325,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           nb0 = 2 * ni;
           nb1 = 2 * ni + 1;
         }
-        const uint8_t *sfa = P.A_sf + (size_t)(row0 >> 7) * P.Kb * 512;
-        const uint8_t *sfb0 = P.W_sf + ((size_t)we * (P.n / 128) + nb0) * P.Kb * 512;
-        const uint8_t *sfb1 = P.W_sf + ((size_t)we * (P.n / 128) + nb1) * P.Kb * 512;
+        const uint8_t *sfa = P.A_sf + (size_t)(row0 >> 7) * P.Kg * 512;
+        const uint8_t *sfb0 = P.W_sf + ((size_t)we * (P.n / 128) + nb0) * P.Kg * 512;
+        const uint8_t *sfb1 = P.W_sf + ((size_t)we * (P.n / 128) + nb1) * P.Kg * 512;
         for (int kb = 0; kb < P.Kb; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort, kWaitLimitNs)) {
             fail(P.status, abort);
@@ -334,7 +335,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           const uint32_t full = bar_full + 8 * stage;
-          mbar_arrive_expect_tx(full, tx);
+          const bool sf = (kb & 3) == 0;
+          mbar_arrive_expect_tx(full, sf ? tx + tx_sf : tx);
           const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
           const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
           const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
@@ -344,11 +346,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           else
             for (int j = 0; j < a_slices; ++j)
               tma_load_2d(sa + j * (A_BYTES / 4), &tmA32, full, kb * BK, row0 + 32 * j, pol_a);
-          bulk_load(ssfa, sfa + (size_t)kb * 512, 512, full);
           tma_load_2d(sb, &tmW, full, kb * BK, wrow0, pol_w);
           tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
-          bulk_load(ssfb, sfb0 + (size_t)kb * 512, 512, full);
-          bulk_load(ssfb + 512, sfb1 + (size_t)kb * 512, 512, full);
+          if (sf) {
+            bulk_load(ssfa, sfa + (size_t)(kb >> 2) * 512, 512, full);
+            bulk_load(ssfb, sfb0 + (size_t)(kb >> 2) * 512, 512, full);
+            bulk_load(ssfb + 512, sfb1 + (size_t)(kb >> 2) * 512, 512, full);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       // kind::mxf8f6f4 instruction descriptor: E4M3 x E4M3, K-major A and B,
-      // N = 256, UE8M0 scales, M = 128; bits 4-5 / 29-30 select the scale byte.
+      // N = 256, UE8M0 scales, M = 128; bits 4-5 / 29-30 select the B / A scale byte.
       const uint32_t idesc_base = ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
                                   ((uint32_t)(BM >> 4) << 24);
       int stage = 0;
@@ -401,18 +405,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
           const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
-          const uint32_t t_sfa = tmem + TMEM_SF + 16 * stage;
+          const uint32_t t_sfa = tmem + TMEM_SF + 16 * ((kb >> 2) % kSfSets);
           const uint32_t t_sfb = t_sfa + 4;
-          const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
-          const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
-          tc_cp_32x128b_x4(t_sfa, smem_desc(ssfa, 16, 128, 0));
-          tc_cp_32x128b_x4(t_sfb, smem_desc(ssfb, 16, 128, 0));
-          tc_cp_32x128b_x4(t_sfb + 4, smem_desc(ssfb + 512, 16, 128, 0));
+          if ((kb & 3) == 0) {  // the group's scale atoms, once per four k-blocks
+            const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
+            const uint32_t ssfb = s_base + OFF_SFB + stage * SFB_BYTES;
+            tc_cp_32x128b_x4(t_sfa, smem_desc(ssfa, 16, 128, 0));
+            tc_cp_32x128b_x4(t_sfb, smem_desc(ssfb, 16, 128, 0));
+            tc_cp_32x128b_x4(t_sfb + 4, smem_desc(ssfb + 512, 16, 128, 0));
+          }
+          // k-block kb's scales are byte kb % 4 of each atom word, for all four
+          // 32-wide MMAs of the block
+          const uint32_t idesc = idesc_base | ((uint32_t)(kb & 3) << 29) | ((uint32_t)(kb & 3) << 4);
 #pragma unroll
           for (int j = 0; j < BK / 32; ++j) {
             const uint64_t ad = smem_desc(sa + 32 * j, 16, 1024, 2);
             const uint64_t bd = smem_desc(sb + 32 * j, 16, 1024, 2);
-            const uint32_t idesc = idesc_base | ((uint32_t)j << 29) | ((uint32_t)j << 4);
             tc_mma_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | j) != 0);
           }
           tc_commit(bar_empty + 8 * stage);
@@ -524,8 +532,8 @@ constexpr uint32_t BH_BYTES = B_BYTES / 2;  // a CTA's half of a k-block's weigh
 constexpr uint32_t O2_A = 0;
 constexpr uint32_t O2_B = O2_A + S2 * KB2 * A_BYTES;
 constexpr uint32_t O2_SFA = O2_B + S2 * KB2 * BH_BYTES;
-constexpr uint32_t O2_SFB = O2_SFA + S2 * KB2 * SFA_BYTES;
-constexpr uint32_t O2_BAR = O2_SFB + S2 * KB2 * SFB_BYTES;  // full, empty [S2]; acc full, empty
+constexpr uint32_t O2_SFB = O2_SFA + S2 * SFA_BYTES;  // a group's atoms, in its first stage
+constexpr uint32_t O2_BAR = O2_SFB + S2 * SFB_BYTES;  // full, empty [S2]; acc full, empty
 constexpr uint32_t O2_MISC = O2_BAR + (2 * S2 + 2) * 8;
 constexpr uint32_t O2_AMAX = O2_MISC + 16;
 constexpr uint32_t O2_UNITQ = O2_AMAX + 2 * 128 * 4;
@@ -533,14 +541,16 @@ constexpr uint32_t O2_UBAR = O2_UNITQ + kUnitQ * 32;
 constexpr uint32_t O2_XBUF = O2_UBAR + 2 * kUnitQ * 8;  // [2 halves][32 columns][64 rows] fp32
 constexpr uint32_t XBUF_BYTES = 2 * 32 * 64 * 4;
 constexpr uint32_t SMEM2_BYTES = O2_XBUF + XBUF_BYTES + 1024;
-constexpr uint32_t TMEM_SF2 = 256;  // scale columns of stage s, k-block h: +16 (KB2 s + h)
-static_assert(TMEM_SF2 + 16 * KB2 * S2 <= TMEM_COLS, "TMEM columns");
+constexpr uint32_t TMEM_SF2 = 256;  // kSfSets rotating scale sets of 16 columns, as above
+static_assert(TMEM_SF2 + 16 * kSfSets <= TMEM_COLS, "TMEM columns");
+static_assert(KB2 == 1 || KB2 == 2 || KB2 == 4, "a scale group (4 k-blocks) starts a stage");
 static_assert(SMEM2_BYTES <= 232448, "shared memory of the 2-SM kernel");
 
 struct Unit2 {
   int row0, nvalid;  // this CTA's tile, when active
   int we, ni, band;
   uint32_t tx;       // bytes one stage brings into both CTAs (expected on the even CTA)
+  uint32_t tx_sf;    // + the scale atoms, in a stage that starts a group of 4 k-blocks
   bool ok, active, end, m128;
 };
 static_assert(sizeof(Unit2) <= 32, "unit ring slot");
@@ -578,7 +588,7 @@ __device__ __forceinline__ Unit2 get_2sm_unit(const GemmParams &P, int unit, int
   U.band = e[4];
   if (U.we < 0 || U.we >= P.num_experts) return U;
   U.m128 = !pair && e[2] > 0 && e[2] <= 64;
-  uint32_t tx = 2 * KB2 * BH_BYTES;  // both halves of the weight tile
+  uint32_t tx = 2 * KB2 * BH_BYTES, tx_sf = 0;  // both halves of the weight tile
   for (int c = 0; c < 2; ++c) {
     const int mi = tile[c];
     if (mi < 0) continue;
@@ -587,9 +597,9 @@ __device__ __forceinline__ Unit2 get_2sm_unit(const GemmParams &P, int unit, int
     const int row0 = t[0] + (second ? P.row_offset2 : 0), nv = t[2];
     if (!tile_ok(P, row0, nv)) return U;
     const int slices = nv == BM ? 0 : (nv + 31) / 32;
-    // an M=128 unit's weight scales come as a 128-row image (4 atoms per k-block)
-    tx += KB2 * ((slices ? slices * (A_BYTES / 4) : A_BYTES) + SFA_BYTES +
-                 (U.m128 ? 2 * SFB_BYTES : SFB_BYTES));
+    tx += KB2 * (slices ? slices * (A_BYTES / 4) : A_BYTES);
+    // an M=128 unit's weight scales come as a 128-row image (4 atoms per group)
+    tx_sf += SFA_BYTES + (U.m128 ? 2 * SFB_BYTES : SFB_BYTES);
     if (c == rank) {
       U.row0 = row0;
       U.nvalid = nv;
@@ -597,6 +607,7 @@ __device__ __forceinline__ Unit2 get_2sm_unit(const GemmParams &P, int unit, int
     }
   }
   U.tx = tx;
+  U.tx_sf = tx_sf;
   U.ok = true;
   return U;
 }
@@ -668,9 +679,7 @@ __device__ __forceinline__ void epilogue_m128(const GemmParams &P, int row0, int
         }
         *reinterpret_cast<uint4 *>(dst + 16 * c) = w;
       }
-      if (half == 0)
-        *reinterpret_cast<uint32_t *>(P.out_sf + sf_atom_off(r, ni, P.I / 128)) =
-            (uint32_t)(e + 127) * 0x01010101u;
+      if (half == 0) P.out_sf[sf_byte_off(r, ni, sf_groups(P.I))] = (uint8_t)(e + 127);
     }
   } else {
     if (store) {
@@ -803,16 +812,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           nb0 = 2 * ni;
           nb1 = 2 * ni + 1;
         }
-        const int sfa_atom = (U.row0 >> 7) * P.Kb;
-        const int sfb_atom0 = (we * (P.n / 128) + nb0) * P.Kb;
-        const int sfb_atom1 = (we * (P.n / 128) + nb1) * P.Kb;
+        const int sfa_atom = (U.row0 >> 7) * P.Kg;
+        const int sfb_atom0 = (we * (P.n / 128) + nb0) * P.Kg;
+        const int sfb_atom1 = (we * (P.n / 128) + nb1) * P.Kg;
         for (int kb = 0; kb < P.Kb; kb += KB2) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort, kWaitLimitNs)) {
             fail(P.status, abort);
             ok = false;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, U.tx);
+          const bool sf = (kb & 3) == 0;  // the stage starts a group of 4 k-blocks
+          if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * stage, sf ? U.tx + U.tx_sf : U.tx);
           const uint32_t fb = lead_full + 8 * stage;
           const uint32_t sb = s_base + O2_B + stage * KB2 * BH_BYTES;
 #pragma unroll
@@ -829,27 +839,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                   tma_load_2d_pair(sa + h * A_BYTES + j * (A_BYTES / 4), &tmA32, fb, (kb + h) * BK,
                                    U.row0 + 32 * j, pol_a);
             }
-            // scale atoms of consecutive k-blocks are adjacent: one box per stage each
-            tma_load_2d_pair(s_base + O2_SFA + stage * KB2 * SFA_BYTES, &tmSFA, fb, 0,
-                             sfa_atom + kb, pol_a);
-            if (U.m128) {
-              // the weight scale image of an M=128 unit: atom 0 in rows 0-63, atom 1 in
-              // rows 64-127, in the A slot's upper half (its rows 64-127 are never read);
-              // only the even CTA is active here, so its own barrier takes the bytes
-#pragma unroll
-              for (int h = 0; h < KB2; ++h) {
-                const uint32_t img = sa + h * A_BYTES + A_BYTES / 2;
-                const uint8_t *a0 = P.W_sf + (size_t)(sfb_atom0 + kb + h) * 512;
-                const uint8_t *a1 = P.W_sf + (size_t)(sfb_atom1 + kb + h) * 512;
+            if (sf) {
+              const int g = kb >> 2;
+              tma_load_2d_pair(s_base + O2_SFA + stage * SFA_BYTES, &tmSFA, fb, 0, sfa_atom + g,
+                               pol_a);
+              if (U.m128) {
+                // the weight scale image of an M=128 unit: atom 0 in rows 0-63, atom 1 in
+                // rows 64-127, in the A slot's upper half (its rows 64-127 are never
+                // read); only the even CTA is active here, so its own barrier takes them
+                const uint32_t img = sa + A_BYTES / 2;
+                const uint8_t *a0 = P.W_sf + (size_t)(sfb_atom0 + g) * 512;
+                const uint8_t *a1 = P.W_sf + (size_t)(sfb_atom1 + g) * 512;
                 bulk_load(img, a0, 512, bar_full + 8 * stage);
                 bulk_load(img + 512, a0, 512, bar_full + 8 * stage);
                 bulk_load(img + 1024, a1, 512, bar_full + 8 * stage);
                 bulk_load(img + 1536, a1, 512, bar_full + 8 * stage);
+              } else {
+                const uint32_t ssfb = s_base + O2_SFB + stage * SFB_BYTES;
+                tma_load_2d_pair(ssfb, &tmSFW, fb, 0, sfb_atom0 + g, pol_w);
+                tma_load_2d_pair(ssfb + 512, &tmSFW, fb, 0, sfb_atom1 + g, pol_w);
               }
-            } else {
-              const uint32_t ssfb = s_base + O2_SFB + stage * KB2 * SFB_BYTES;
-              tma_load_2d_pair(ssfb, &tmSFW, fb, 0, sfb_atom0 + kb, pol_w);
-              tma_load_2d_pair(ssfb + KB2 * 512, &tmSFW, fb, 0, sfb_atom1 + kb, pol_w);
             }
           }
           ++issued;
@@ -910,26 +919,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           // a stage's scale columns are rewritten S2 stages later, after its refill
-          const uint32_t ssfa = s_base + O2_SFA + stage * KB2 * SFA_BYTES;
-          const uint32_t ssfb = s_base + O2_SFB + stage * KB2 * SFB_BYTES;
+          const uint32_t ssfa = s_base + O2_SFA + stage * SFA_BYTES;
+          const uint32_t ssfb = s_base + O2_SFB + stage * SFB_BYTES;
           const uint32_t sa = s_base + O2_A + stage * KB2 * A_BYTES;
           const uint32_t sb = s_base + O2_B + stage * KB2 * BH_BYTES;
 #pragma unroll
           for (int h = 0; h < KB2; ++h) {
-            const uint32_t t_sfa = tmem + TMEM_SF2 + 16 * (KB2 * stage + h);
+            const int kbh = kb + h;
+            const uint32_t t_sfa = tmem + TMEM_SF2 + 16 * ((kbh >> 2) % kSfSets);
             const uint32_t t_sfb = t_sfa + 4;
-            tc_cp_pair_32x128b_x4(t_sfa, smem_desc(ssfa + 512 * h, 16, 128, 0));
-            if (U.m128) {
-              tc_cp_pair_128x128b(t_sfb, smem_desc(sa + h * A_BYTES + A_BYTES / 2, 16, 128, 0));
-            } else {
-              tc_cp_pair_32x128b_x4(t_sfb, smem_desc(ssfb + 512 * h, 16, 128, 0));
-              tc_cp_pair_32x128b_x4(t_sfb + 4, smem_desc(ssfb + KB2 * 512 + 512 * h, 16, 128, 0));
+            if ((kbh & 3) == 0) {  // the group's scale atoms, once per four k-blocks
+              tc_cp_pair_32x128b_x4(t_sfa, smem_desc(ssfa, 16, 128, 0));
+              if (U.m128) {
+                tc_cp_pair_128x128b(t_sfb, smem_desc(sa + h * A_BYTES + A_BYTES / 2, 16, 128, 0));
+              } else {
+                tc_cp_pair_32x128b_x4(t_sfb, smem_desc(ssfb, 16, 128, 0));
+                tc_cp_pair_32x128b_x4(t_sfb + 4, smem_desc(ssfb + 512, 16, 128, 0));
+              }
             }
+            // k-block kbh's scales are byte kbh % 4 of each atom word
+            const uint32_t idesc =
+                idesc_base | ((uint32_t)(kbh & 3) << 29) | ((uint32_t)(kbh & 3) << 4);
 #pragma unroll
             for (int j = 0; j < BK / 32; ++j) {
               const uint64_t ad = smem_desc(sa + h * A_BYTES + 32 * j, 16, 1024, 2);
               const uint64_t bd = smem_desc(sb + h * BH_BYTES + 32 * j, 16, 1024, 2);
-              const uint32_t idesc = idesc_base | ((uint32_t)j << 29) | ((uint32_t)j << 4);
               tc_mma_pair_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | h | j) != 0);
             }
           }
@@ -1018,12 +1032,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
+// Weight scale bytes [blocks][Kb] -> atoms [blocks][Kg][512]: every word of a group's
+// atom holds the group's four k-block bytes (0 past the last k-block).
 __global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ atoms,
-                                   size_t n_atoms) {
+                                   size_t n_atoms, int Kb, int Kg) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;  // one 16-byte piece
   if (i >= n_atoms * 32) return;
-  const uint32_t b = (uint32_t)sf[i >> 5] * 0x01010101u;
-  reinterpret_cast<uint4 *>(atoms)[i] = make_uint4(b, b, b, b);
+  const size_t a = i >> 5;
+  const int g = (int)(a % Kg);
+  const uint8_t *src = sf + (a / Kg) * Kb + 4 * g;
+  uint32_t w = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (4 * g + j < Kb) w |= (uint32_t)src[j] << (8 * j);
+  reinterpret_cast<uint4 *>(atoms)[i] = make_uint4(w, w, w, w);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1110,7 +1132,12 @@ using namespace moe;
 
 extern "C" size_t moe_packed_scale_bytes(int E, int n, int k) {
   if (E <= 0 || n <= 0 || k <= 0 || n % 128 || k % 128) return 0;
-  return (size_t)E * (n / 128) * (k / 128) * 512;
+  return (size_t)E * (n / 128) * sf_groups(k) * 512;
+}
+
+extern "C" size_t moe_scale_bytes(int64_t rows, int k) {
+  if (rows <= 0 || k <= 0 || rows % 128 || k % 128) return 0;
+  return (size_t)(rows / 128) * sf_groups(k) * 512;
 }
 
 extern "C" int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf,
@@ -1120,7 +1147,7 @@ extern "C" int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf,
   const size_t n_atoms = bytes / 512;
   const size_t pieces = n_atoms * 32;
   pack_scales_kernel<<<(unsigned)((pieces + 255) / 256), 256, 0, as_stream(stream)>>>(
-      W_sf, static_cast<uint8_t *>(W_sf_packed), n_atoms);
+      W_sf, static_cast<uint8_t *>(W_sf_packed), n_atoms, k / 128, sf_groups(k));
   return check_launch();
 }
 
@@ -1159,6 +1186,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.n = a->n;
   P.k = a->k;
   P.Kb = a->k / BK;
+  P.Kg = sf_groups(a->k);
   P.n_tiles = a->n / BN;
   P.I = a->n / 2;
   P.A_sf = static_cast<const uint8_t *>(a->A_sf);
@@ -1187,8 +1215,9 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   const int sms = a->num_sms > 0 ? a->num_sms : device_sm_count();
   if (a->pair_tiles) {
     CUtensorMap mSFA, mSFW;
-    if (!make_sf_map(&mSFA, a->A_sf, (uint64_t)(a->rows / 128) * (a->k / BK), KB2) ||
-        !make_sf_map(&mSFW, a->W_sf, (uint64_t)a->num_experts * (a->n / 128) * (a->k / BK), KB2))
+    const uint64_t kg = (uint64_t)sf_groups(a->k);
+    if (!make_sf_map(&mSFA, a->A_sf, (uint64_t)(a->rows / 128) * kg, 1) ||
+        !make_sf_map(&mSFW, a->W_sf, (uint64_t)a->num_experts * (a->n / 128) * kg, 1))
       return MOE_ERR_CUDA;
     return launch_pairs(grouped_gemm_2sm_kernel, SMEM2_BYTES, sms, max_clusters[dev],
                         as_stream(stream), mA, mA32, mW, mSFA, mSFW, P);

@@ -34,12 +34,13 @@
  *
  * Packed scale layout ("SF atoms").  Every FP8 operand of the grouped GEMM
  * carries its 1x128 (activation) or 128x128 (weight) block scales as 512-byte
- * atoms, one per (128-row block, 128-column block).  Inside an atom, the scale of
- * row r (0..127 within the block) sits at bytes 16*(r%32) + 4*(r/32) + {0,1,2,3}
- * (the byte repeated four times, once per 32-column sub-block).  An activation
- * tensor of `rows` rows and `k` columns has atoms
- * [rows/128][k/128][512]; a weight tensor of E experts x n rows x k columns has
- * atoms [E][n/128][k/128][512] (all 512 bytes of a weight atom are equal).
+ * atoms, one per (128-row block, group of four 128-column blocks).  Inside an atom,
+ * the scale of row r (0..127 within the block) for column block 4g + j (j = 0..3)
+ * sits at byte 16*(r%32) + 4*(r/32) + j; bytes for blocks past the last column block
+ * are unused.  With Kg = ceil(k/512) groups, an activation tensor of `rows` rows and
+ * `k` columns has atoms [rows/128][Kg][512] (moe_scale_bytes(rows, k) bytes); a
+ * weight tensor of E experts x n rows x k columns has atoms [E][n/128][Kg][512]
+ * (moe_packed_scale_bytes; all 32 rows' words of a weight atom are equal).
  *
  * Tile list.  moe_dispatch describes the rows it wrote as 128-row "M tiles" in
  * an int32 array `tiles` of 8 + 16*max_tiles entries:
@@ -264,7 +265,7 @@ int moe_dispatch_noalloc(const moe_dispatch_cfg *cfg, const void *x, const int32
  *   block and w = e4m3(W)*2^(sfW-127) per 128x128 block, fp32 accumulation.
  *   GATEUP_SWIGLU: W [E][n][k] with n = 2I, rows [0,I) gate and [I,2I) up;
  *     h = silu(g) * u in fp32, quantised per 1x128 block exactly as dispatch
- *     quantises x; out = e4m3 [rows][I], out_sf = SF atoms [rows/128][I/128].
+ *     quantises x; out = e4m3 [rows][I], out_sf = SF atoms [rows/128][ceil(I/512)][512].
  *   DOWN: W [E][n][k] with n = H, k = I; out = bf16 [rows][n] (round to nearest
  *     even).  signal (nullable): after the tile (rows R..R+127, any 256 output
  *     columns) is stored, signal[(R + j) / block_m_signal] += 1 (release, gpu
@@ -316,10 +317,13 @@ int moe_grouped_gemm_fp8(const moe_gemm_args *args, void *stream);
 /*
  * Weight scales (UE8M0 bytes W_sf [E][n/128][k/128], one per 128x128 block as in the
  * "1d2d" scaling of the "Single Batch Overlap (SBO)" PR, §3) -> SF atoms
- * [E][n/128][k/128][512] (moe_packed_scale_bytes bytes).  One-time setup, off the
- * hot path.
+ * [E][n/128][ceil(k/512)][512] (moe_packed_scale_bytes bytes).  One-time setup, off
+ * the hot path.
  */
 size_t moe_packed_scale_bytes(int E, int n, int k);
+/* Bytes of the SF atoms of an activation tensor of `rows` rows and k columns
+   (rows and k multiples of 128; 0 otherwise): rows/128 * ceil(k/512) * 512. */
+size_t moe_scale_bytes(int64_t rows, int k);
 int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf, void *W_sf_packed,
                            void *stream);
 

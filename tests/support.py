@@ -12,17 +12,15 @@ from combine_moe_route_03_gb300 import configs, inputs
 REL, ABS = 2e-2, 1e-3
 
 
-def unpack_sf_atoms(atoms: np.ndarray, rows: int, kb: int, check_rows=None) -> np.ndarray:
-    """SF atoms [rows/128][kb][512] -> UE8M0 bytes [rows][kb].
-
-    For the rows listed in ``check_rows`` (default: all) it also checks that each
-    scale byte is repeated over its four 32-column sub-blocks."""
-    a = np.asarray(atoms, dtype=np.uint8).reshape(rows // 128, kb, 32, 4, 4)  # r%32, r/32, copy
-    # a[mb, b, r%32, r/32, c] -> row = mb*128 + (r/32)*32 + r%32
-    full = a.transpose(0, 3, 2, 1, 4).reshape(rows, kb, 4)
-    chk = full if check_rows is None else full[check_rows]
-    assert np.all(chk == chk[..., :1]), "scale byte not repeated over its four 32-column sub-blocks"
-    return full[..., 0].copy()
+def unpack_sf_atoms(atoms: np.ndarray, rows: int, kb: int) -> np.ndarray:
+    """SF atoms [rows/128][ceil(kb/4)][512] -> UE8M0 bytes [rows][kb] (the layout of
+    include/moe.h: byte j of the word at 16*(r%32) + 4*(r/32) of group g holds row r's
+    scale for column block 4g + j)."""
+    kg = (kb + 3) // 4
+    a = np.asarray(atoms, dtype=np.uint8).reshape(rows // 128, kg, 32, 4, 4)  # r%32, r/32, j
+    # a[mb, g, r%32, r/32, j] -> row = mb*128 + (r/32)*32 + r%32, block = 4g + j
+    full = a.transpose(0, 3, 2, 1, 4).reshape(rows, kg * 4)
+    return full[:, :kb].copy()
 
 
 def within_tol(got: np.ndarray, ref: np.ndarray, rel=REL, abs_=ABS) -> tuple[bool, float, float]:

@@ -11,10 +11,14 @@ pytestmark = pytest.mark.gpu
 
 
 def pack_sf_atoms(sf: np.ndarray) -> np.ndarray:
-    """UE8M0 bytes [rows][kb] -> SF atoms [rows/128][kb][512] (layout of include/moe.h)."""
+    """UE8M0 bytes [rows][kb] -> SF atoms [rows/128][ceil(kb/4)][512] (layout of
+    include/moe.h; bytes past the last column block are 0)."""
     rows, kb = sf.shape
-    a = sf.reshape(rows // 128, 4, 32, kb).transpose(0, 3, 2, 1)       # mb, kb, r%32, r/32
-    return np.repeat(a[..., None], 4, axis=-1).reshape(-1).copy()
+    kg = (kb + 3) // 4
+    p = np.zeros((rows, 4 * kg), np.uint8)
+    p[:, :kb] = sf
+    a = p.reshape(rows // 128, 4, 32, kg, 4).transpose(0, 3, 2, 1, 4)  # mb, g, r%32, r/32, j
+    return a.reshape(-1).copy()
 
 
 def dense_tiles(rows: int, experts_of_tiles=None) -> np.ndarray:
@@ -103,9 +107,15 @@ def support_unpack(atoms, rows, kb):
     return unpack_sf_atoms(atoms, rows, kb)
 
 
-def test_pack_unpack_sf_atoms_inverse():
-    sf = np.random.default_rng(0).integers(0, 255, (384, 5)).astype(np.uint8)
-    assert np.array_equal(support_unpack(pack_sf_atoms(sf), 384, 5), sf)
+@pytest.mark.parametrize("kb", [1, 4, 5, 56])
+def test_pack_unpack_sf_atoms_inverse(kb):
+    sf = np.random.default_rng(0).integers(0, 255, (384, kb)).astype(np.uint8)
+    atoms = pack_sf_atoms(sf)
+    assert atoms.size == 384 // 128 * ((kb + 3) // 4) * 512
+    assert np.array_equal(support_unpack(atoms, 384, kb), sf)
+    # row 130, block 5: atom (1, 1), word 16*(2 % 32) + 4*(2 // 32), byte 1
+    if kb > 5:
+        assert atoms[(1 * ((kb + 3) // 4) + 1) * 512 + 32 + 1] == sf[130, 5]
 
 
 def cluster_tile_list(tiles_per_expert, nvalid_of) -> np.ndarray:
@@ -168,8 +178,7 @@ def test_2sm_gemm_equals_single_cta(dev, op, pattern):
         valid = np.zeros(rows, bool)
         for i0 in range(mt):
             valid[128 * i0: 128 * i0 + t[8 + 8 * i0 + 2]] = True
-        sfs = [unpack_sf_atoms(o[1].cpu().numpy(), rows, n // 256, check_rows=valid)
-               for o in outs]
+        sfs = [unpack_sf_atoms(o[1].cpu().numpy(), rows, n // 256) for o in outs]
         assert np.array_equal(sfs[0][valid], sfs[1][valid])
 
 

@@ -153,7 +153,10 @@ def test_host_argument_checks_return_before_launch(L):
     assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
     cc = _lib.CombineCfg(4, 100, 2, None, 0, 64, 0, 0, 0)          # H % 128 != 0
     assert L.moe_combine(ctypes.byref(cc), *([None] * 7)) == -2
-    assert L.moe_packed_scale_bytes(2, 256, 384) == 2 * 2 * 3 * 512
+    assert L.moe_packed_scale_bytes(2, 256, 384) == 2 * 2 * 1 * 512   # 3 blocks: one group
+    assert L.moe_packed_scale_bytes(2, 256, 640) == 2 * 2 * 2 * 512   # 5 blocks: two groups
+    assert L.moe_scale_bytes(384, 7168) == 3 * 14 * 512
+    assert L.moe_scale_bytes(100, 7168) == 0 and L.moe_scale_bytes(128, 100) == 0
     h = ctypes.c_void_p()
     lay = _lib.Layer()
     assert L.moe_layer_graph_create(None, None, None, None, ctypes.byref(h)) == -1

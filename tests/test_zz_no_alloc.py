@@ -1,8 +1,9 @@
 """moe_dispatch_noalloc, the dispatch entry point for callers that cannot allocate
 device memory (a host framework owning all device memory, a path that must not
 make the device synchronise, a plugin host that forbids allocation), against
-moe_dispatch.  Collected last on purpose: it shares one library-wide scratch
-array, so it is run after (and also works without) every other test."""
+moe_dispatch and against the oracle's dispatch.  Collected last on purpose: it shares
+one library-wide scratch array, so it is run after (and also works without) every
+other test."""
 import ctypes
 
 import numpy as np
@@ -11,7 +12,7 @@ import torch
 
 import oracle
 from combine_moe_route_03_gb300 import _lib, api, configs
-from support import bf16_dev, host_workload, to_dev
+from support import bf16_dev, host_workload, to_dev, unpack_sf_atoms
 
 pytestmark = pytest.mark.gpu
 
@@ -22,10 +23,10 @@ def _outputs(cfg, B, dev):
     srows = (B + 127) // 128 * 128
     e = lambda *s, dt=torch.uint8: torch.full(s, 0x5A, dtype=dt, device=dev) if dt == torch.uint8 \
         else torch.full(s, -7, dtype=dt, device=dev)  # noqa: E731
-    return dict(A=e(rows, cfg.H), A_sf=e(rows * (cfg.H // 128) * 4),
+    return dict(A=e(rows, cfg.H), A_sf=e(api.scale_bytes(rows, cfg.H)),
                 counts=e(cfg.N_phys, dt=torch.int32), row_of=e(B, cfg.K, dt=torch.int32),
                 src_of=e(rows, dt=torch.int32), tiles=e(8 + 16 * mt, dt=torch.int32),
-                As=e(srows, cfg.H), As_sf=e(srows * (cfg.H // 128) * 4),
+                As=e(srows, cfg.H), As_sf=e(api.scale_bytes(srows, cfg.H)),
                 shared_tiles=e(8 + 16 * (srows // 128), dt=torch.int32),
                 status=torch.zeros(1, dtype=torch.int32, device=dev))
 
@@ -51,9 +52,10 @@ def _valid_equal(cfg, a, b):
     rows = ro[ro >= 0].long()
     assert torch.equal(a["A"][rows], b["A"][rows])
     kb = cfg.H // 128
-    sfa = a["A_sf"].view(-1, kb, 32, 4, 4).permute(0, 3, 2, 1, 4).reshape(-1, kb, 4)
-    sfb = b["A_sf"].view(-1, kb, 32, 4, 4).permute(0, 3, 2, 1, 4).reshape(-1, kb, 4)
-    assert torch.equal(sfa[rows], sfb[rows])
+    sfa = unpack_sf_atoms(a["A_sf"].cpu().numpy(), a["A"].shape[0], kb)
+    sfb = unpack_sf_atoms(b["A_sf"].cpu().numpy(), b["A"].shape[0], kb)
+    r = rows.cpu().numpy()
+    assert np.array_equal(sfa[r], sfb[r])
     B = a["row_of"].shape[0]
     assert torch.equal(a["As"][:B], b["As"][:B])
 
@@ -75,6 +77,22 @@ def test_noalloc_matches_dispatch_on_two_calls_in_a_row(dev, names):
         _call("moe_dispatch_noalloc", cfg, xd, idd, l2d, repd, got)
         torch.cuda.synchronize()
         _valid_equal(cfg, ref, got)
+        _oracle_equal(cfg, x, idx, l2p, rep, got)
+
+
+def _oracle_equal(cfg, x, idx, l2p, rep, got):
+    """The allocation-free call's output against the oracle's dispatch, bit for bit."""
+    o = oracle.dispatch(x, idx, cfg, log2phys=l2p, rep=rep)
+    assert np.array_equal(got["counts"].cpu().numpy(), o["cnt"])
+    ro = got["row_of"].cpu().numpy()
+    assert np.array_equal(ro, o["row_of"])
+    rows = got["A"].shape[0]
+    assert np.array_equal(got["src_of"].cpu().numpy(), o["src_of"][:rows])
+    v = ro[ro >= 0]
+    assert np.array_equal(got["A"].cpu().numpy()[v], o["A"][v])
+    sf = unpack_sf_atoms(got["A_sf"].cpu().numpy(), rows, cfg.H // 128)
+    assert np.array_equal(sf[v], o["sf"][v])
+    assert got["status"].item() == (1 if o["dropped"] else 0)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(dev):
