@@ -51,7 +51,10 @@ constexpr uint32_t OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
 constexpr uint32_t OFF_AMAX = OFF_MISC + 16;  // [2][128] partial row amax of the epilogue
 constexpr uint32_t OFF_UNITQ = OFF_AMAX + 2 * 128 * 4;  // [kUnitQ] decoded units
 constexpr uint32_t OFF_UBAR = OFF_UNITQ + kUnitQ * 32;  // [kUnitQ] full, [kUnitQ] empty
-constexpr uint32_t SMEM_BYTES = OFF_UBAR + 2 * kUnitQ * 8 + 1024;  // + alignment slack
+constexpr uint32_t STAGE_BYTES = 2048;                  // per epilogue warp, see store_bf16_rows
+constexpr uint32_t OFF_STAGE = OFF_UBAR + 2 * kUnitQ * 8;
+constexpr uint32_t SMEM_BYTES = OFF_STAGE + (kEpiThreads / 32) * STAGE_BYTES + 1024;  // + slack
+static_assert(SMEM_BYTES <= 232448, "shared memory of the one-CTA kernel");
 constexpr uint32_t TMEM_COLS = 512;
 // Scale columns start here: kSfSets rotating sets of 16 columns (A atom at +0, B atoms
 // at +4 and +8), one set per group of four k-blocks; a set is rewritten 4 * kSfSets
@@ -131,6 +134,64 @@ __device__ __forceinline__ void fail(int32_t *status, volatile int *abort) {
   status_or(status, MOE_STATUS_TIMEOUT);
 }
 
+// 32 rows (one per lane, row `lane` at out_row0 + lane) x 64 bytes of this warp, stored
+// so that each instruction writes 8 rows x 64 contiguous bytes: every lane puts its
+// row's four 16-byte pieces into the warp's 2 KB staging slot (XOR-swizzled by row, so
+// neither the writes nor the reads conflict on banks), then reads back piece lane%4 of
+// row 8i + lane/4.  Rows at or past nrows are not stored.
+__device__ __forceinline__ void store_rows_64B(uint8_t *stage, const uint4 *w, uint8_t *out_row0,
+                                               size_t pitch, int nrows, int lane) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+    *reinterpret_cast<uint4 *>(stage + 64 * lane + 16 * (p ^ ((lane >> 1) & 3))) = w[p];
+  __syncwarp();
+  const int p = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = 8 * i + (lane >> 2);
+    const uint4 x = *reinterpret_cast<const uint4 *>(stage + 64 * row + 16 * (p ^ ((row >> 1) & 3)));
+    if (row < nrows) *reinterpret_cast<uint4 *>(out_row0 + (size_t)row * pitch + 16 * p) = x;
+  }
+  __syncwarp();
+}
+
+// store_rows_64B of 32 fp32 values per row, rounded to bf16.
+__device__ __forceinline__ void store_bf16_rows(uint8_t *stage, const uint32_t *v,
+                                                uint8_t *out_row0, size_t pitch, int nrows,
+                                                int lane) {
+  uint4 w[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    w[p].x = f32_to_bf16_bits(__uint_as_float(v[8 * p + 0])) |
+             (f32_to_bf16_bits(__uint_as_float(v[8 * p + 1])) << 16);
+    w[p].y = f32_to_bf16_bits(__uint_as_float(v[8 * p + 2])) |
+             (f32_to_bf16_bits(__uint_as_float(v[8 * p + 3])) << 16);
+    w[p].z = f32_to_bf16_bits(__uint_as_float(v[8 * p + 4])) |
+             (f32_to_bf16_bits(__uint_as_float(v[8 * p + 5])) << 16);
+    w[p].w = f32_to_bf16_bits(__uint_as_float(v[8 * p + 6])) |
+             (f32_to_bf16_bits(__uint_as_float(v[8 * p + 7])) << 16);
+  }
+  store_rows_64B(stage, w, out_row0, pitch, nrows, lane);
+}
+
+// 64 fp32 values of a row times 2^-e, as 64 e4m3 codes (round to nearest even,
+// saturating) in four 16-byte pieces.
+__device__ __forceinline__ void quantize_64(const uint32_t *v, float inv, uint4 *w) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t *wp = &w[c].x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int b = 16 * c + 4 * j;
+      wp[j] = e4m3x2(__fmul_rn(__uint_as_float(v[b]), inv),
+                     __fmul_rn(__uint_as_float(v[b + 1]), inv)) |
+              (e4m3x2(__fmul_rn(__uint_as_float(v[b + 2]), inv),
+                      __fmul_rn(__uint_as_float(v[b + 3]), inv))
+               << 16);
+    }
+  }
+}
+
 // Epilogue of one 128-row accumulator for this thread's half-row: TMEM ->
 // registers, release() (the MMAs may overwrite the accumulator from then on), then
 // SwiGLU + 1x128 requantisation (GATEUP) or bf16 rounding (DOWN), global stores and
@@ -138,7 +199,8 @@ __device__ __forceinline__ void fail(int32_t *status, volatile int *abort) {
 template <class Release>
 __device__ __forceinline__ void epilogue_tile(const GemmParams &P, int row0, int valid, int ni,
                                               uint32_t t_row, int half, int row_local, int warp,
-                                              int lane, float *amax_x, Release release) {
+                                              int lane, float *amax_x, uint8_t *stage,
+                                              Release release) {
   const int64_t r = (int64_t)row0 + row_local;
   const bool store = row_local < valid && r < P.rows;
   if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
@@ -164,27 +226,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &P, int row0, int
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     amax = fmaxf(amax, amax_x[(half ^ 1) * 128 + row_local]);
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-    if (store) {
-      const int e = ue8m0_exp(amax);
-      const float inv = pow2i(-e);
-      uint8_t *dst = P.out + (size_t)r * P.I + (size_t)ni * 128 + 64 * half;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint4 w;
-        uint32_t *wp = &w.x;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int b = 16 * c + 4 * j;
-          wp[j] = e4m3x2(__fmul_rn(__uint_as_float(g[b]), inv),
-                         __fmul_rn(__uint_as_float(g[b + 1]), inv)) |
-                  (e4m3x2(__fmul_rn(__uint_as_float(g[b + 2]), inv),
-                          __fmul_rn(__uint_as_float(g[b + 3]), inv))
-                   << 16);
-        }
-        *reinterpret_cast<uint4 *>(dst + 16 * c) = w;
-      }
-      if (half == 0) P.out_sf[sf_byte_off(r, ni, sf_groups(P.I))] = (uint8_t)(e + 127);
-    }
+    const int e = ue8m0_exp(amax);
+    uint4 w[4];
+    quantize_64(g, pow2i(-e), w);
+    if (store && half == 0) P.out_sf[sf_byte_off(r, ni, sf_groups(P.I))] = (uint8_t)(e + 127);
+    const int64_t wrow0 = (int64_t)row0 + (row_local - lane);
+    const int nrows = (int)min((int64_t)min(valid - (row_local - lane), 32), P.rows - wrow0);
+    if (nrows > 0)
+      store_rows_64B(stage, w, P.out + (size_t)wrow0 * P.I + (size_t)ni * 128 + 64 * half,
+                     (size_t)P.I, nrows, lane);
   } else {
     // output columns [128*half, +128)
     uint32_t v[128];
@@ -193,21 +243,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &P, int row0, int
     tc_wait_ld();
     tc_fence_before();
     release();
-    if (store) {
-      uint8_t *dst = P.out + ((size_t)r * P.n + (size_t)ni * 256 + 128 * half) * 2;
+    // this warp's 32 rows (row_local - lane onwards), 32 columns at a time
+    const int64_t wrow0 = (int64_t)row0 + (row_local - lane);
+    const int nrows = (int)min((int64_t)min(valid - (row_local - lane), 32), P.rows - wrow0);
+    if (nrows > 0) {
+      uint8_t *dst = P.out + ((size_t)wrow0 * P.n + (size_t)ni * 256 + 128 * half) * 2;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        uint4 w;
-        w.x = f32_to_bf16_bits(__uint_as_float(v[8 * j + 0])) |
-              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 1])) << 16);
-        w.y = f32_to_bf16_bits(__uint_as_float(v[8 * j + 2])) |
-              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 3])) << 16);
-        w.z = f32_to_bf16_bits(__uint_as_float(v[8 * j + 4])) |
-              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 5])) << 16);
-        w.w = f32_to_bf16_bits(__uint_as_float(v[8 * j + 6])) |
-              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 7])) << 16);
-        *reinterpret_cast<uint4 *>(dst + 16 * j) = w;
-      }
+      for (int c = 0; c < 4; ++c)
+        store_bf16_rows(stage, v + 32 * c, dst + 64 * c, (size_t)P.n * 2, nrows, lane);
     }
     if (P.signal) {
       __threadfence();
@@ -445,6 +488,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row_local = 32 * q + lane;
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
     float *amax_x = reinterpret_cast<float *>(smem + OFF_AMAX);  // [half][row]
+    uint8_t *stage = smem + OFF_STAGE + (warp - 2) * STAGE_BYTES;
     uint32_t acc_phase = 0;
     for (int seq = 0;; ++seq) {
       Unit U;
@@ -462,7 +506,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_after();
       epilogue_tile(P, U.row0, U.nvalid, U.ni, t_row, half, row_local, warp, lane, amax_x,
-                    [&] { mbar_arrive(bar_acc_empty); });
+                    stage, [&] { mbar_arrive(bar_acc_empty); });
       acc_phase ^= 1;
     }
   } else if (lane == 0) {
@@ -540,6 +584,7 @@ constexpr uint32_t O2_UNITQ = O2_AMAX + 2 * 128 * 4;
 constexpr uint32_t O2_UBAR = O2_UNITQ + kUnitQ * 32;
 constexpr uint32_t O2_XBUF = O2_UBAR + 2 * kUnitQ * 8;  // [2 halves][32 columns][64 rows] fp32
 constexpr uint32_t XBUF_BYTES = 2 * 32 * 64 * 4;
+static_assert(XBUF_BYTES >= (kEpiThreads / 32) * STAGE_BYTES, "DOWN staging slots in xbuf");
 constexpr uint32_t SMEM2_BYTES = O2_XBUF + XBUF_BYTES + 1024;
 constexpr uint32_t TMEM_SF2 = 256;  // kSfSets rotating scale sets of 16 columns, as above
 static_assert(TMEM_SF2 + 16 * kSfSets <= TMEM_COLS, "TMEM columns");
@@ -623,7 +668,7 @@ template <class Release>
 __device__ __forceinline__ void epilogue_m128(const GemmParams &P, int row0, int valid, int ni,
                                               uint32_t t_row, int q, int half, int warp,
                                               int lane, float *amax_x, float *xbuf,
-                                              Release release) {
+                                              uint8_t *stage, Release release) {
   const int m = 32 * (q & 1) + lane;  // row of the tile
   const bool upper = q >= 2;          // columns [128, 256)
   const int64_t r = (int64_t)row0 + m;
@@ -635,6 +680,9 @@ __device__ __forceinline__ void epilogue_m128(const GemmParams &P, int row0, int
   tc_fence_before();
   release();
   if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
+    // xbuf also holds the warps' staging slots: every warp is done with the previous
+    // unit's stores before any up value lands in it
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     float amax = 0.0f;
 #pragma unroll
     for (int rd = 0; rd < 2; ++rd) {
@@ -660,44 +708,26 @@ __device__ __forceinline__ void epilogue_m128(const GemmParams &P, int row0, int
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
     if (!upper) amax = fmaxf(amax, amax_x[(half ^ 1) * 128 + m]);
     asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-    if (!upper && store) {
+    if (!upper) {  // warp-uniform: the gate lanes hold h
       const int e = ue8m0_exp(amax);
-      const float inv = pow2i(-e);
-      uint8_t *dst = P.out + (size_t)r * P.I + (size_t)ni * 128 + 64 * half;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint4 w;
-        uint32_t *wp = &w.x;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int b = 16 * c + 4 * j;
-          wp[j] = e4m3x2(__fmul_rn(__uint_as_float(v[b]), inv),
-                         __fmul_rn(__uint_as_float(v[b + 1]), inv)) |
-                  (e4m3x2(__fmul_rn(__uint_as_float(v[b + 2]), inv),
-                          __fmul_rn(__uint_as_float(v[b + 3]), inv))
-                   << 16);
-        }
-        *reinterpret_cast<uint4 *>(dst + 16 * c) = w;
-      }
-      if (half == 0) P.out_sf[sf_byte_off(r, ni, sf_groups(P.I))] = (uint8_t)(e + 127);
+      uint4 w[4];
+      quantize_64(v, pow2i(-e), w);
+      if (store && half == 0) P.out_sf[sf_byte_off(r, ni, sf_groups(P.I))] = (uint8_t)(e + 127);
+      const int64_t wrow0 = (int64_t)row0 + (m - lane);
+      const int nrows = (int)min((int64_t)min(valid - (m - lane), 32), P.rows - wrow0);
+      if (nrows > 0)
+        store_rows_64B(stage, w, P.out + (size_t)wrow0 * P.I + (size_t)ni * 128 + 64 * half,
+                       (size_t)P.I, nrows, lane);
     }
   } else {
-    if (store) {
+    const int64_t wrow0 = (int64_t)row0 + (m - lane);
+    const int nrows = (int)min((int64_t)min(valid - (m - lane), 32), P.rows - wrow0);
+    if (nrows > 0) {
       uint8_t *dst =
-          P.out + ((size_t)r * P.n + (size_t)ni * 256 + (upper ? 128 : 0) + 64 * half) * 2;
+          P.out + ((size_t)wrow0 * P.n + (size_t)ni * 256 + (upper ? 128 : 0) + 64 * half) * 2;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint4 w;
-        w.x = f32_to_bf16_bits(__uint_as_float(v[8 * j + 0])) |
-              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 1])) << 16);
-        w.y = f32_to_bf16_bits(__uint_as_float(v[8 * j + 2])) |
-              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 3])) << 16);
-        w.z = f32_to_bf16_bits(__uint_as_float(v[8 * j + 4])) |
-              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 5])) << 16);
-        w.w = f32_to_bf16_bits(__uint_as_float(v[8 * j + 6])) |
-              (f32_to_bf16_bits(__uint_as_float(v[8 * j + 7])) << 16);
-        *reinterpret_cast<uint4 *>(dst + 16 * j) = w;
-      }
+      for (int c = 0; c < 2; ++c)
+        store_bf16_rows(stage, v + 32 * c, dst + 64 * c, (size_t)P.n * 2, nrows, lane);
     }
     if (P.signal) {
       __threadfence();
@@ -966,6 +996,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
     float *amax_x = reinterpret_cast<float *>(smem + O2_AMAX);
     float *xbuf = reinterpret_cast<float *>(smem + O2_XBUF);
+    // the DOWN epilogue's staging slots share xbuf (the GATEUP M=128 exchange buffer)
+    uint8_t *stage = smem + O2_XBUF + (warp - 2) * STAGE_BYTES;
     const uint32_t lead_acc_empty = mapa_shared(bar_acc_empty, 0);
     auto release_acc = [&] {
       __syncwarp();
@@ -992,10 +1024,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         release_acc();
       } else if (U.m128) {
         epilogue_m128(P, U.row0, U.nvalid, U.ni, t_row, q, half, warp, lane, amax_x, xbuf,
-                      release_acc);
+                      stage, release_acc);
       } else {
         epilogue_tile(P, U.row0, U.nvalid, U.ni, t_row, half, row_local, warp, lane, amax_x,
-                      release_acc);
+                      stage, release_acc);
       }
       acc_phase ^= 1;
     }
