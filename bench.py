@@ -322,13 +322,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill",
-                    choices=sorted(configs.NAMED) + sorted(configs.PROFILE))
+                    choices=sorted(configs.NAMED) + sorted(configs.PROFILE) +
+                    sorted(configs.VARIANTS))
     ap.add_argument("--cpu-tokens", type=int, default=12,
                     help="tokens of the CPU-oracle baseline sample (0 = skip)")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    cfg = {**configs.NAMED, **configs.PROFILE}[args.workload]
+    cfg = {**configs.NAMED, **configs.PROFILE, **configs.VARIANTS}[args.workload]
     if args.impl == "reference":
         return run_reference(args, cfg)
 

@@ -303,7 +303,7 @@ class MoELayer:
     """
 
     def __init__(self, cfg: MoEConfig, W_router: torch.Tensor, bias: torch.Tensor | None,
-                 weights: dict, eplb_map=None, num_sms_: int = 0, combine_ctas: int = 16,
+                 weights: dict, eplb_map=None, num_sms_: int = 0, combine_ctas: int = 0,
                  timeout_ns: int = 1_000_000_000, device="cuda", gemm_pairs: int = 0):
         self.cfg = cfg
         dev = torch.device(device)
@@ -365,8 +365,7 @@ class MoELayer:
         lay.N_phys, lay.layout, lay.cap, lay.I = cfg.N_phys, cfg.layout, cfg.cap, I
         lay.has_shared, lay.sbo, lay.block_m_signal = int(cfg.shared), int(cfg.sbo), cfg.block_m_signal
         lay.rows, lay.max_tiles, lay.timeout_ns = self.rows, self.max_tiles, timeout_ns
-        sms = num_sms_ or num_sms()
-        lay.num_sms = sms - combine_ctas if cfg.sbo else sms
+        lay.num_sms = num_sms_ or num_sms()
         lay.combine_ctas = combine_ctas
         lay.gemm_pairs = gemm_pairs
         lay.eplb_max_rep = 0 if self.log2phys is None else self.log2phys.shape[1]

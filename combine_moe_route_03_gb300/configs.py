@@ -104,3 +104,9 @@ DECODE_N64 = MoEConfig("decode_n64", B=128, layout=MASKED, cap=128, bias_init="n
 PREFILL_N64 = MoEConfig("prefill_n64", B=2048, layout=CONTIG, router_init="uniform", **_DSV3_64)
 PROFILE = {c.name: c for c in (DECODE_N64, PREFILL_N64)}
 ALL.update(PROFILE)
+
+# The SBO workload run sequentially (down GEMM on every SM, then the combine): the
+# comparison arm of single-batch overlap.
+SBO_SEQ = SBO.with_(name="sbo_seq", sbo=False)
+VARIANTS = {SBO_SEQ.name: SBO_SEQ}
+ALL.update(VARIANTS)

@@ -2,6 +2,7 @@
 // builder, and the whole-layer chain.
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <vector>
 
 #include "common.cuh"
@@ -72,10 +73,29 @@ extern "C" int eplb_build_map(const int64_t *counts_host, int N_log, int N_phys,
 
 namespace {
 
-cudaEvent_t layer_event(int i) {
-  static cudaEvent_t ev[2] = {nullptr, nullptr};
-  if (!ev[i]) cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
-  return ev[i];
+std::mutex g_order_mutex;
+cudaEvent_t g_order_ev[kMaxDevices][2] = {};
+
+// Makes `waiter` wait for the work enqueued so far on `signaler`, through one of the
+// library's two events of the current device (created on first use).  Record and wait
+// happen under one lock, so callers on other threads cannot slip their own record in
+// between.  Only enqueues (also under stream capture, where it forks or joins streams).
+int order_streams(cudaStream_t signaler, cudaStream_t waiter, int which) {
+  const int dev = device_slot();
+  if (dev < 0) return dev;
+  std::lock_guard<std::mutex> lock(g_order_mutex);
+  cudaEvent_t &ev = g_order_ev[dev][which];
+  cudaError_t e = cudaSuccess;
+  if (!ev) {
+    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      ev = nullptr;
+      return set_cuda_error(e);
+    }
+  }
+  e = cudaEventRecord(ev, signaler);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(waiter, ev, 0);
+  return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
 }
 
 }  // namespace
@@ -97,6 +117,9 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   };
   if (L->has_shared && !L->shared_tiles) return MOE_ERR_INVALID;
   if (L->gemm_pairs < -1 || L->gemm_pairs > 1) return MOE_ERR_INVALID;
+  const int sms = L->num_sms > 0 ? L->num_sms : device_sm_count();
+  const int sbo_ctas = L->combine_ctas > 0 ? L->combine_ctas : 32;  // SBO consumer CTAs
+  if (L->sbo && sbo_ctas >= sms) return MOE_ERR_INVALID;
   if (L->gemm_pairs == 1 && (rc.H % 256 || L->I % 256)) return MOE_ERR_UNSUPPORTED;
   moe_dispatch_cfg dc;
   dc.B = rc.B;
@@ -147,7 +170,7 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   }
   g.out = L->H1;
   g.out_sf = L->H1_sf;
-  g.num_sms = L->num_sms;
+  g.num_sms = sms;
   g.status = L->status;
   // 2-SM GEMMs when experts average at least one full M tile (and both GEMMs' K allow
   // 256-deep stages); one CTA per tile otherwise (decode: HBM-bound on the weights)
@@ -177,25 +200,23 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
       return MOE_ERR_INVALID;
     const size_t nsig = (size_t)(rows_all / L->block_m_signal);
     cudaError_t e = cudaMemsetAsync(L->signal, 0, nsig * sizeof(int32_t), st);
-    if (e == cudaSuccess) e = cudaEventRecord(layer_event(0), st);
-    cudaStream_t st2 = as_stream(L->stream2);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st2, layer_event(0), 0);
     if (e != cudaSuccess) return set_cuda_error(e);
+    cudaStream_t st2 = as_stream(L->stream2);
+    if ((rc_ = order_streams(st, st2, 0))) return rc_;
     g.signal = L->signal;
     g.block_m_signal = L->block_m_signal;
+    g.num_sms = sms - sbo_ctas;  // the consumer's CTAs take SMs of their own
     if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
     mark(4);
     cc.signal = L->signal;
     cc.threshold = rc.H / 256;
     cc.block_m_signal = L->block_m_signal;
     cc.timeout_ns = L->timeout_ns > 0 ? L->timeout_ns : 1000000000ll;
-    cc.num_ctas = L->combine_ctas;
+    cc.num_ctas = sbo_ctas;
     cc.shared_row0 = L->rows;
     if ((rc_ = moe_combine(&cc, L->Y, L->row_of, L->topk_w, S, L->out, L->status, L->stream2)))
       return rc_;
-    e = cudaEventRecord(layer_event(1), st2);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, layer_event(1), 0);
-    if (e != cudaSuccess) return set_cuda_error(e);
+    if ((rc_ = order_streams(st2, st, 1))) return rc_;
     mark(5);
     return MOE_OK;
   }

@@ -9,9 +9,9 @@
 //
 // Single-batch overlap ("Single Batch Overlap (SBO)" PR, §2): with a signal
 // array, a row is read only after the down GEMM has published all of its output
-// tiles (acquire load of the row block's counter reaching the threshold).  Polls
-// are bounded by a wall-clock limit; a row that never becomes ready is skipped
-// and MOE_STATUS_TIMEOUT is raised.
+// tiles (acquire load of the row block's counter reaching the threshold).  The
+// consumer's wait is bounded by one wall-clock limit for the whole launch; rows that
+// are not ready by then are skipped and MOE_STATUS_TIMEOUT is raised.
 #include "common.cuh"
 
 namespace moe {
@@ -26,8 +26,7 @@ template <int KM>  // K <= KM
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     const uint16_t *__restrict__ Y, const int32_t *__restrict__ row_of,
     const float *__restrict__ topk_w, const uint16_t *__restrict__ S, uint16_t *__restrict__ out,
-    int B, int H, int K, int cpt, const int32_t *signal, int threshold, int bm,
-    int64_t timeout_ns, int64_t shared_row0, int32_t *status) {
+    int B, int H, int K, int cpt) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = gridDim.x * kCombineWarps;
   const int nch = (H + 255) / 256;
@@ -42,28 +41,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     if (lane < K) {
       my_r = row_of[(size_t)t * K + lane];
       my_w = topk_w[(size_t)t * K + lane];
-    } else if (lane == K && S) {
-      my_r = 0;  // this lane waits for the shared expert's row of token t
     }
-    if (signal && my_r >= 0 && lane <= K) {
-      {
-        const int64_t sr = lane < K ? (int64_t)my_r : shared_row0 + t;
-        const int32_t *sp = signal + sr / bm;
-        if (ld_acquire_gpu(sp) < threshold) {
-          const uint64_t t0 = globaltimer();
-          while (ld_acquire_gpu(sp) < threshold) {
-            if (globaltimer() - t0 > (uint64_t)timeout_ns) {
-              status_or(status, MOE_STATUS_TIMEOUT);
-              my_r = -1;
-              break;
-            }
-            __nanosleep(128);
-          }
-        }
-      }
-    }
-    __syncwarp();
-    const bool use_s = S && (K >= 32 || __shfl_sync(0xffffffffu, my_r, K) >= 0);
+    const bool use_s = S != nullptr;
     int r[KM];
     float w[KM];
 #pragma unroll
@@ -116,6 +95,131 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
   }
 }
 
+// Sum of one token's K rows (and its shared row) over 256-column chunks [c0, c1), in
+// the rank order k = 0..K-1 (the arithmetic of combine_kernel, bit for bit).
+// Sum of one token's K rows (and its shared row) over 256-column chunks [c0, c1), in
+// the rank order k = 0..K-1 (the arithmetic of combine_kernel, bit for bit), with all
+// K + 1 loads of a chunk in flight.  r[k] < 0: rank k left out.
+template <int KM>
+__device__ __forceinline__ void reduce_token(const uint16_t *__restrict__ Y,
+                                             const uint16_t *__restrict__ S,
+                                             uint16_t *__restrict__ out, int t, int H, int K,
+                                             int c0, int c1, const int *r, const float *w,
+                                             bool use_s, int lane) {
+  for (int c = c0; c < c1; ++c) {
+    const int h = c * 256 + 8 * lane;
+    if (h >= H) continue;
+    uint4 y[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k)
+      y[k] = (k < K && r[k] >= 0)
+                 ? __ldcg(reinterpret_cast<const uint4 *>(Y + (size_t)r[k] * H + h))
+                 : make_uint4(0, 0, 0, 0);
+    const uint4 sv =
+        use_s ? __ldcs(reinterpret_cast<const uint4 *>(S + (size_t)t * H + h)) : make_uint4(0, 0, 0, 0);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+      if (k >= K || r[k] < 0) continue;
+      const uint32_t v[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fmaf_rn(w[k], __uint_as_float(v[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = __fmaf_rn(w[k], __uint_as_float(v[i] & 0xffff0000u), acc[2 * i + 1]);
+      }
+    }
+    if (use_s) {
+      const uint32_t v[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fadd_rn(acc[2 * i], __uint_as_float(v[i] << 16));
+        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __uint_as_float(v[i] & 0xffff0000u));
+      }
+    }
+    uint4 o;
+    o.x = f32_to_bf16_bits(acc[0]) | (f32_to_bf16_bits(acc[1]) << 16);
+    o.y = f32_to_bf16_bits(acc[2]) | (f32_to_bf16_bits(acc[3]) << 16);
+    o.z = f32_to_bf16_bits(acc[4]) | (f32_to_bf16_bits(acc[5]) << 16);
+    o.w = f32_to_bf16_bits(acc[6]) | (f32_to_bf16_bits(acc[7]) << 16);
+    __stcs(reinterpret_cast<uint4 *>(out + (size_t)t * H + h), o);
+  }
+}
+
+// The SBO consumer ("Single Batch Overlap (SBO)" PR, §2), launched beside the down GEMM.
+// A token is ready once the row blocks of all its K rows (and of its shared row) have
+// reached the threshold; a token's rows come from K experts spread over the GEMM's whole
+// schedule, so tokens become ready in no useful order.  Each warp therefore owns a set
+// of tasks (token, run of cpt 256-column chunks; tasks w, w + warps, ..., 64 at a time)
+// and sweeps them without blocking, reducing a task as soon as its token is ready; it
+// sleeps briefly only after a sweep that found nothing.  It runs on SMs of its own (the
+// producing GEMM's grid leaves them free), so it never holds resources that a GEMM CTA
+// it waits for would need.  One wall-clock limit bounds the whole launch: past it
+// MOE_STATUS_TIMEOUT is raised and the remaining tasks are reduced without the rows still
+// unpublished.
+template <int KM>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_sbo_kernel(
+    const uint16_t *__restrict__ Y, const int32_t *__restrict__ row_of,
+    const float *__restrict__ topk_w, const uint16_t *__restrict__ S, uint16_t *__restrict__ out,
+    int B, int H, int K, int cpt, const int32_t *signal, int threshold, int bm,
+    int64_t timeout_ns, int64_t shared_row0, int32_t *status) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  const int nw = gridDim.x * kCombineWarps;
+  const int nch = (H + 255) / 256;
+  const int tpt = (nch + cpt - 1) / cpt;  // tasks per token
+  const long ntasks = (long)B * tpt;
+  const long mine = gw < ntasks ? (ntasks - 1 - gw) / nw + 1 : 0;
+  const uint64_t t0 = globaltimer();
+  bool late = false;  // past the wall-clock limit
+  for (long base = 0; base < mine; base += 64) {
+    const int n = (int)min(64L, mine - base);
+    uint64_t pending = n == 64 ? ~0ull : ((1ull << n) - 1);
+    while (pending) {
+      bool progress = false;
+      for (uint64_t m = pending; m; m &= m - 1) {
+        const int i = __ffsll((long long)m) - 1;
+        const long task = gw + (base + i) * nw;
+        const int t = (int)(task / tpt);
+        const int c0 = (int)(task % tpt) * cpt;
+        int my_r = -1;
+        float my_w = 0.0f;
+        int64_t sr = -1;
+        if (lane < K) {
+          my_r = row_of[(size_t)t * K + lane];
+          my_w = topk_w[(size_t)t * K + lane];
+          sr = my_r;
+        } else if (lane == K && S) {
+          sr = shared_row0 + t;
+        }
+        const bool ok = sr < 0 || ld_acquire_gpu(signal + sr / bm) >= threshold;
+        if (!__all_sync(0xffffffffu, ok) && !late) continue;
+        if (!ok) my_r = -1;  // past the limit: the row is left out
+        const bool use_s = S && __shfl_sync(0xffffffffu, ok ? 1 : 0, K) != 0;
+        int r[KM];
+        float w[KM];
+#pragma unroll
+        for (int k = 0; k < KM; ++k) {
+          r[k] = __shfl_sync(0xffffffffu, my_r, k);
+          w[k] = __shfl_sync(0xffffffffu, my_w, k);
+        }
+        reduce_token<KM>(Y, S, out, t, H, K, c0, min(nch, c0 + cpt), r, w, use_s, lane);
+        pending &= ~(1ull << i);
+        progress = true;
+      }
+      if (pending && !progress) {
+        if (!late && globaltimer() - t0 > (uint64_t)timeout_ns) {
+          late = true;
+          if (lane == 0) status_or(status, MOE_STATUS_TIMEOUT);
+        } else {
+          __nanosleep(256);
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -139,10 +243,27 @@ extern "C" int moe_combine(const moe_combine_cfg *c, const void *Y, const int32_
   const long tasks = (long)c->B * ((nch + cpt - 1) / cpt);
   long grid = (tasks + kCombineWarps - 1) / kCombineWarps;
   if (c->num_ctas > 0 && c->num_ctas < grid) grid = c->num_ctas;
-#define MOE_COMBINE_ARGS                                                                   \
+  if (c->signal) {  // the SBO consumer: tasks in the order their tokens become ready
+    long g = c->num_ctas > 0 ? c->num_ctas : device_sm_count();
+    // about two tasks per consumer warp, at least two chunks per task
+    const long w = g * kCombineWarps;
+    long sc = ((long)c->B * nch + 2 * w - 1) / (2 * w);
+    sc = sc < 2 ? 2 : (sc > nch ? nch : sc);
+    cpt = sc;
+#define MOE_SBO_ARGS                                                                       \
   static_cast<const uint16_t *>(Y), row_of, topk_w, static_cast<const uint16_t *>(shared),   \
       static_cast<uint16_t *>(out), c->B, c->H, c->K, (int)cpt, c->signal, c->threshold,     \
-      c->block_m_signal > 0 ? c->block_m_signal : 1, c->timeout_ns, c->shared_row0, status
+      c->block_m_signal, c->timeout_ns, c->shared_row0, status
+    if (c->K <= 8)
+      combine_sbo_kernel<8><<<(unsigned)g, kCombineWarps * 32, 0, as_stream(stream)>>>(MOE_SBO_ARGS);
+    else
+      combine_sbo_kernel<16><<<(unsigned)g, kCombineWarps * 32, 0, as_stream(stream)>>>(MOE_SBO_ARGS);
+#undef MOE_SBO_ARGS
+    return check_launch();
+  }
+#define MOE_COMBINE_ARGS                                                                   \
+  static_cast<const uint16_t *>(Y), row_of, topk_w, static_cast<const uint16_t *>(shared),   \
+      static_cast<uint16_t *>(out), c->B, c->H, c->K, (int)cpt
   if (c->K <= 8)
     combine_kernel<8><<<(unsigned)grid, kCombineWarps * 32, 0, as_stream(stream)>>>(MOE_COMBINE_ARGS);
   else

@@ -390,7 +390,10 @@ typedef struct moe_layer {
   int64_t rows, max_tiles, timeout_ns; /* rows, max_tiles: at least moe_dispatch_rows and
                                            moe_dispatch_max_tiles of the layer's dispatch
                                            (else MOE_ERR_INVALID before any launch) */
-  int num_sms, combine_ctas;
+  int num_sms;      /* CTAs of the persistent GEMM grids (0: every SM) */
+  int combine_ctas; /* sbo: CTAs of the combine consumer, taken from num_sms for the down
+                       GEMM while they run beside it (0: 32; at least one SM must stay
+                       for the GEMM, else MOE_ERR_INVALID) */
   int gemm_pairs; /* pair_tiles of both GEMMs.  0: 1 when B*K >= 128*N_phys and H and I
                      are multiples of 256, else 0; 1: always 1 (MOE_ERR_UNSUPPORTED
                      unless H and I are multiples of 256); -1: always 0; other values:
