@@ -11,13 +11,14 @@
 //                        and reorder partial sums).  Small grids.
 //   route_logits_wide_kernel  the same arithmetic for wide grids: x widened to fp32
 //                        once per CTA, larger per-thread tiles.
-//   route_logits_slice_kernel  256 experts, large batches: a warp owns a slice of
-//                        tokens against all experts, one CTA per SM; each step's W
-//                        and x operands are loaded into registers one step ahead
-//                        (the 8 warps of an SM leave register room, and a load
-//                        right before its FMAs stalled the warp).
+//   route_logits_pair_kernel  256 experts, large batches: a warp owns a slice of
+//                        tokens against all experts, one CTA of 8 warps per SM; packed
+//                        fp32 fmas (__ffma2_rn) advance two tokens' logits per
+//                        instruction, each in its own sequential k order; each step's
+//                        W and x operands are loaded into registers one step ahead.
 //   route_select_kernel  one warp per token: scores, group scores, top-K with the
 //                        (score desc, index asc) order, weights, expert counts.
+#include <algorithm>
 #include <cfloat>
 
 #include "common.cuh"
@@ -256,25 +257,34 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_wide_kernel(
   }
 }
 
-// Token-sliced variant for wide batches: one CTA of NW warps per SM, and each warp owns
+// Token-sliced kernel for wide batches: one CTA of NW warps per SM, and each warp owns
 // TT consecutive tokens (TT = B / (NW * SMs), rounded up) against all 32 * TE experts:
 // lane l takes experts l, l + 32, ...  Per 4-deep k step a lane loads its TE rows of W
-// (distinct addresses) and each token row of fp32-widened x as a warp-wide broadcast
-// (half the shared-memory cost of a distinct load), then does 4 * TT * TE fused
-// multiply-adds; the token slicing keeps every SM equally loaded (a fixed 2-D tiling of
-// 2^21 logits over 152 SMs leaves a sixth of them idle).  Same sequential k order per
-// logit.
+// (distinct addresses) and its tokens' x as warp-wide broadcast loads (half the
+// shared-memory cost of a distinct load); the token slicing keeps every SM equally
+// loaded (a fixed 2-D tiling of 2^21 logits over 152 SMs leaves a sixth of them idle).
+// The token-sliced kernel on packed fp32 fused multiply-adds: __ffma2_rn performs two
+// independent binary32 fmas (round to nearest even) in one instruction, so each one
+// advances two tokens' logits of one expert, each chain still in the sequential k order
+// (bit for bit the scalar kernel's results) while the multiply-add instructions halve.
+// A warp's TT tokens form TT/2 pairs plus, for odd TT, one token on scalar fmas.  The
+// widening pass writes each warp's x as its pairs, {x_2p(k), x_2p+1(k)} for k = 0, 1,
+// ..., then its odd token, so a broadcast 16-byte load yields two k steps of a pair (or
+// four of the odd token); W is staged and read as in the scalar kernel.  With 8 warps
+// the four SM sub-partitions carry equal work.
 template <int TT, int TE, int S, int BK, int NW>
-__global__ void __launch_bounds__(NW * 32, 1) route_logits_slice_kernel(
+__global__ void __launch_bounds__(NW * 32, 1) route_logits_pair_kernel(
     const uint16_t *__restrict__ x, const float *__restrict__ W, float *__restrict__ logits,
     int B, int H) {
+  constexpr int TP = TT / 2, TS = TT % 2;
   constexpr int BT = NW * TT, NE = 32 * TE, NT = NW * 32;
-  constexpr int LDH = BK + 8, LDF = BK + 4;
+  constexpr int LDH = BK + 8, LDF = BK + 4, LDP = 2 * BK + 4;
+  constexpr int XW = TP * LDP + TS * LDF;  // one warp's widened x, floats
   constexpr int XST = BT * LDH, WST = NE * LDF;
   extern __shared__ __align__(16) uint8_t route_smem[];
   float *ws = reinterpret_cast<float *>(route_smem);           // [S][NE][LDF]
-  float *xf = ws + S * WST;                                    // [BT][LDF]
-  uint16_t *xs = reinterpret_cast<uint16_t *>(xf + BT * LDF);  // [S][BT][LDH]
+  float *xp = ws + S * WST;                                    // [NW][XW]
+  uint16_t *xs = reinterpret_cast<uint16_t *>(xp + NW * XW);   // [S][BT][LDH]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = blockIdx.x * BT;
   const int nchunks = H / BK;
@@ -299,12 +309,19 @@ __global__ void __launch_bounds__(NW * 32, 1) route_logits_slice_kernel(
                    : "memory");
     }
   };
+  auto widen8 = [](uint32_t u, float &lo, float &hi) {  // bf16 -> fp32 is exact
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xffff0000u);
+  };
 
-  float acc[TT][TE];
+  float2 acc[TP > 0 ? TP : 1][TE];
+  float acc1[TE];
 #pragma unroll
-  for (int i = 0; i < TT; ++i)
+  for (int j = 0; j < TE; ++j) {
 #pragma unroll
-    for (int j = 0; j < TE; ++j) acc[i][j] = 0.0f;
+    for (int p = 0; p < TP; ++p) acc[p][j] = make_float2(0.0f, 0.0f);
+    acc1[j] = 0.0f;
+  }
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) {
     if (s < nchunks) load(s, s);
@@ -313,63 +330,102 @@ __global__ void __launch_bounds__(NW * 32, 1) route_logits_slice_kernel(
   for (int c = 0; c < nchunks; ++c) {
     asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");
     __syncthreads();
-    {  // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 word
+    {  // widen x: per warp its token pairs (interleaved), then its odd token
       const uint16_t *xb = xs + (c % S) * XST;
-      for (int i = tid; i < BT * BK / 8; i += NT) {
-        const int t = i / (BK / 8), k = (i % (BK / 8)) * 8;
-        const uint4 v = *reinterpret_cast<const uint4 *>(xb + t * LDH + k);
-        float4 *d = reinterpret_cast<float4 *>(xf + t * LDF + k);
-        d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
-                           __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-        d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
-                           __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+      constexpr int R = TP + TS;  // rows per warp
+      for (int i = tid; i < NW * R * (BK / 8); i += NT) {
+        const int w = i / (R * (BK / 8)), rr = (i / (BK / 8)) % R, k = (i % (BK / 8)) * 8;
+        const int tw = w * TT + 2 * rr;  // first token of the row in the CTA
+        const uint4 a = *reinterpret_cast<const uint4 *>(xb + tw * LDH + k);
+        const uint32_t ua[4] = {a.x, a.y, a.z, a.w};
+        if (rr < TP) {
+          const uint4 b = *reinterpret_cast<const uint4 *>(xb + (tw + 1) * LDH + k);
+          const uint32_t ub[4] = {b.x, b.y, b.z, b.w};
+          float4 *d = reinterpret_cast<float4 *>(xp + w * XW + rr * LDP + 2 * k);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float a0, a1, b0, b1;
+            widen8(ua[q], a0, a1);
+            widen8(ub[q], b0, b1);
+            d[q] = make_float4(a0, b0, a1, b1);
+          }
+        } else {
+          float4 *d = reinterpret_cast<float4 *>(xp + w * XW + TP * LDP + k);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            float a0, a1, a2, a3;
+            widen8(ua[2 * q], a0, a1);
+            widen8(ua[2 * q + 1], a2, a3);
+            d[q] = make_float4(a0, a1, a2, a3);
+          }
+        }
       }
     }
     if (c + S - 1 < nchunks) load(c + S - 1, (c + S - 1) % S);
     asm volatile("cp.async.commit_group;" ::: "memory");
     __syncthreads();
     const float *wb = ws + (c % S) * WST + lane * LDF;
-    const float *xw = xf + warp * TT * LDF;
-    // operands of step k4 + 4 are loaded while step k4's FMAs run
-    float4 wn[TE], xn[TT];
+    const float *xw = xp + warp * XW;
+    // operands of step k4 + 4 are loaded while step k4's fmas run
+    float4 wn[TE], xn[TP > 0 ? TP : 1][2], x1n;
+    auto fetch = [&](int k4) {
 #pragma unroll
-    for (int j = 0; j < TE; ++j) wn[j] = *reinterpret_cast<const float4 *>(wb + 32 * j * LDF);
+      for (int j = 0; j < TE; ++j) wn[j] = *reinterpret_cast<const float4 *>(wb + 32 * j * LDF + k4);
 #pragma unroll
-    for (int i = 0; i < TT; ++i) xn[i] = *reinterpret_cast<const float4 *>(xw + i * LDF);
+      for (int p = 0; p < TP; ++p)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          xn[p][h] = *reinterpret_cast<const float4 *>(xw + p * LDP + 2 * k4 + 4 * h);
+      if (TS) x1n = *reinterpret_cast<const float4 *>(xw + TP * LDP + k4);
+    };
+    fetch(0);
 #pragma unroll
     for (int k4 = 0; k4 < BK; k4 += 4) {
-      float4 wv[TE], xc[TT];
+      float4 wv[TE], xc[TP > 0 ? TP : 1][2], x1;
 #pragma unroll
       for (int j = 0; j < TE; ++j) wv[j] = wn[j];
 #pragma unroll
-      for (int i = 0; i < TT; ++i) xc[i] = xn[i];
-      if (k4 + 4 < BK) {
-#pragma unroll
-        for (int j = 0; j < TE; ++j)
-          wn[j] = *reinterpret_cast<const float4 *>(wb + 32 * j * LDF + k4 + 4);
-#pragma unroll
-        for (int i = 0; i < TT; ++i) xn[i] = *reinterpret_cast<const float4 *>(xw + i * LDF + k4 + 4);
+      for (int p = 0; p < TP; ++p) {
+        xc[p][0] = xn[p][0];
+        xc[p][1] = xn[p][1];
       }
+      x1 = x1n;
+      if (k4 + 4 < BK) fetch(k4 + 4);
+      // k order strictly sequential per logit
 #pragma unroll
-      for (int i = 0; i < TT; ++i) {
-        const float4 xv = xc[i];  // broadcast
-        // k order is strictly sequential for every output
+      for (int p = 0; p < TP; ++p) {
+        const float2 x0 = make_float2(xc[p][0].x, xc[p][0].y);
+        const float2 xk1 = make_float2(xc[p][0].z, xc[p][0].w);
+        const float2 x2 = make_float2(xc[p][1].x, xc[p][1].y);
+        const float2 x3 = make_float2(xc[p][1].z, xc[p][1].w);
 #pragma unroll
         for (int j = 0; j < TE; ++j) {
-          acc[i][j] = __fmaf_rn(xv.x, wv[j].x, acc[i][j]);
-          acc[i][j] = __fmaf_rn(xv.y, wv[j].y, acc[i][j]);
-          acc[i][j] = __fmaf_rn(xv.z, wv[j].z, acc[i][j]);
-          acc[i][j] = __fmaf_rn(xv.w, wv[j].w, acc[i][j]);
+          acc[p][j] = __ffma2_rn(x0, make_float2(wv[j].x, wv[j].x), acc[p][j]);
+          acc[p][j] = __ffma2_rn(xk1, make_float2(wv[j].y, wv[j].y), acc[p][j]);
+          acc[p][j] = __ffma2_rn(x2, make_float2(wv[j].z, wv[j].z), acc[p][j]);
+          acc[p][j] = __ffma2_rn(x3, make_float2(wv[j].w, wv[j].w), acc[p][j]);
+        }
+      }
+      if (TS) {
+#pragma unroll
+        for (int j = 0; j < TE; ++j) {
+          acc1[j] = __fmaf_rn(x1.x, wv[j].x, acc1[j]);
+          acc1[j] = __fmaf_rn(x1.y, wv[j].y, acc1[j]);
+          acc1[j] = __fmaf_rn(x1.z, wv[j].z, acc1[j]);
+          acc1[j] = __fmaf_rn(x1.w, wv[j].w, acc1[j]);
         }
       }
     }
   }
+  const int tw = t0 + warp * TT;
 #pragma unroll
-  for (int i = 0; i < TT; ++i) {
-    const int t = t0 + warp * TT + i;
-    if (t >= B) continue;
+  for (int j = 0; j < TE; ++j) {
 #pragma unroll
-    for (int j = 0; j < TE; ++j) logits[(size_t)t * NE + 32 * j + lane] = acc[i][j];
+    for (int p = 0; p < TP; ++p) {
+      if (tw + 2 * p < B) logits[(size_t)(tw + 2 * p) * NE + 32 * j + lane] = acc[p][j].x;
+      if (tw + 2 * p + 1 < B) logits[(size_t)(tw + 2 * p + 1) * NE + 32 * j + lane] = acc[p][j].y;
+    }
+    if (TS && tw + TT - 1 < B) logits[(size_t)(tw + TT - 1) * NE + 32 * j + lane] = acc1[j];
   }
 }
 
@@ -705,22 +761,22 @@ int launch_logits_wide(const uint16_t *x, const float *W, float *lg, int B, int 
 }
 
 template <int TT, int TE, int S, int BK, int NW>
-int launch_logits_slice(const uint16_t *x, const float *W, float *lg, int B, int H,
-                        cudaStream_t st) {
+int launch_logits_pair(const uint16_t *x, const float *W, float *lg, int B, int H,
+                       cudaStream_t st) {
   constexpr int BT = NW * TT;
   constexpr size_t smem = (size_t)S * (BT * (BK + 8) * 2 + 32 * TE * (BK + 4) * 4) +
-                          (size_t)BT * (BK + 4) * 4;
+                          (size_t)NW * ((TT / 2) * (2 * BK + 4) + (TT % 2) * (BK + 4)) * 4;
   static bool attr[kMaxDevices] = {};
   const int dev = device_slot();
   if (dev < 0) return dev;
   if (!attr[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(route_logits_slice_kernel<TT, TE, S, BK, NW>,
+    cudaError_t e = cudaFuncSetAttribute(route_logits_pair_kernel<TT, TE, S, BK, NW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return set_cuda_error(e);
   }
   attr[dev] = true;
-  route_logits_slice_kernel<TT, TE, S, BK, NW><<<(B + BT - 1) / BT, NW * 32, smem, st>>>(x, W, lg,
-                                                                                    B, H);
+  route_logits_pair_kernel<TT, TE, S, BK, NW><<<(B + BT - 1) / BT, NW * 32, smem, st>>>(x, W, lg,
+                                                                                   B, H);
   return check_launch();
 }
 
@@ -772,16 +828,37 @@ extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W
     return (long)((N + 16 * te - 1) / (16 * te)) * ((B + 8 * tt - 1) / (8 * tt));
   };
   const uint16_t *xb = static_cast<const uint16_t *>(x);
-  // 256 experts and 6-8 tokens per warp at 8 warps per SM: the token-sliced kernel.
-  // Other wide grids: fp32-widened x and the largest per-thread tile that still leaves
-  // every SM one and a half CTAs; small grids: the bf16 kernel below.
-  const long tt8 = (B + 8 * sms - 1) / (8 * sms);
-  if (N == 256 && tt8 == 6)
-    rc = launch_logits_slice<6, 8, 3, 32, 8>(xb, W, lg, B, H, st);
-  else if (N == 256 && tt8 == 7)
-    rc = launch_logits_slice<7, 8, 3, 32, 8>(xb, W, lg, B, H, st);
-  else if (N == 256 && tt8 == 8)
-    rc = launch_logits_slice<8, 8, 3, 32, 8>(xb, W, lg, B, H, st);
+  // 256 experts and 3-8 tokens per warp in one wave of CTAs of 7 or 8 warps: the
+  // token-sliced kernel on packed fmas, with the tile whose 4-deep step costs least:
+  // the larger of the SM's shared-memory wavefronts (per warp 32 for W, about TT for x)
+  // and the busiest sub-partition's fma cycles (ceil(NW/4) warps x TT x 32).  Other wide
+  // grids: fp32-widened x and the largest per-thread tile that still leaves every SM
+  // one and a half CTAs; small grids: the bf16 kernel below.
+  int best_tt = 0, best_nw = 0;
+  long best_cost = 0;
+  if (N == 256)
+    for (int nw = 7; nw <= 8; ++nw)
+      for (int tt = 3; tt <= 8; ++tt) {
+        // the instantiated tiles: 7 warps for 3-6 tokens (shared-memory-bound steps),
+        // 8 warps for 7-8 (fma-bound, so all four sub-partitions get two warps)
+        if ((nw == 7) != (tt <= 6) || (long)nw * tt * sms < B) continue;
+        const long cost = std::max((long)nw * (32 + tt), (long)((nw + 3) / 4) * tt * 32);
+        if (!best_tt || cost < best_cost) {
+          best_tt = tt;
+          best_nw = nw;
+          best_cost = cost;
+        }
+      }
+  if (best_tt && (long)B * 4 >= 3L * 3 * 7 * sms) {  // at least ~3 tokens per warp
+    switch (best_nw * 16 + best_tt) {
+#define MOE_PAIR_CASE(TT, NW) \
+  case NW * 16 + TT: rc = launch_logits_pair<TT, 8, 3, 32, NW>(xb, W, lg, B, H, st); break;
+      MOE_PAIR_CASE(3, 7) MOE_PAIR_CASE(4, 7) MOE_PAIR_CASE(5, 7) MOE_PAIR_CASE(6, 7)
+      MOE_PAIR_CASE(7, 8) MOE_PAIR_CASE(8, 8)
+#undef MOE_PAIR_CASE
+      default: rc = MOE_ERR_UNSUPPORTED;
+    }
+  }
   else if (2 * ctas(8, 8) >= 3 * sms)
     rc = launch_logits_wide<8, 8, 3, 32>(xb, W, lg, B, H, N, st);
   else if (2 * ctas(4, 8) >= 3 * sms)

@@ -72,11 +72,12 @@ def test_route_logits_kernel_shapes(dev, B, N, H):
     assert np.array_equal(r["counts"].cpu().numpy(), oracle.expert_counts(idx, N))
 
 @pytest.mark.parametrize("name,B", [("prefill", 0), ("skew", 0), ("prefill", 6100),
-                                    ("prefill", 9700)])
+                                    ("prefill", 9700), ("prefill", 3000), ("prefill", 5000)])
 def test_route_full_size_sampled(dev, name, B):
     """Full B: routing of a sample of tokens bit-exact, counts consistent at any size.
-    The prefill batch sizes 6100 and 9700 take the token-sliced logits kernel with
-    6 and 8 tokens per warp (8192 takes 7), with ragged last slices."""
+    The batch sizes take the token-sliced logits kernel with 3 (3000), 4 (4096), 5
+    (5000), 6 (6100), 7 (8192) and 8 (9700) tokens per warp (odd counts: token pairs
+    plus one token on scalar fmas), with ragged last slices."""
     cfg, x, W, bias = host_workload(name)
     if B:
         cfg = cfg.with_(B=B)
