@@ -78,11 +78,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_kernel(const uint1
     }
   };
 
-  float acc[TT][TE];
+  // token pairs (2p, 2p+1) on packed fmas, acc[p][j] = their logits; an odd last
+  // token on scalar fmas (acc1)
+  constexpr int TP = TT / 2, TS = TT % 2;
+  float2 acc[TP > 0 ? TP : 1][TE];
+  float acc1[TE];
 #pragma unroll
-  for (int i = 0; i < TT; ++i)
+  for (int j = 0; j < TE; ++j) {
 #pragma unroll
-    for (int j = 0; j < TE; ++j) acc[i][j] = 0.0f;
+    for (int p = 0; p < TP; ++p) acc[p][j] = make_float2(0.0f, 0.0f);
+    acc1[j] = 0.0f;
+  }
 
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) {
@@ -120,13 +126,25 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_kernel(const uint1
       if (k4 + 4 < kRouteBK) fetch(k4 + 4);
       // k order is strictly sequential for every output
 #pragma unroll
-      for (int i = 0; i < TT; ++i)
+      for (int j = 0; j < TE; ++j)
+        if (TS) {
+          acc1[j] = __fmaf_rn(xv[TT - 1].x, wv[j].x, acc1[j]);
+          acc1[j] = __fmaf_rn(xv[TT - 1].y, wv[j].y, acc1[j]);
+          acc1[j] = __fmaf_rn(xv[TT - 1].z, wv[j].z, acc1[j]);
+          acc1[j] = __fmaf_rn(xv[TT - 1].w, wv[j].w, acc1[j]);
+        }
+#pragma unroll
+      for (int p = 0; p < TP; ++p)
 #pragma unroll
         for (int j = 0; j < TE; ++j) {
-          acc[i][j] = __fmaf_rn(xv[i].x, wv[j].x, acc[i][j]);
-          acc[i][j] = __fmaf_rn(xv[i].y, wv[j].y, acc[i][j]);
-          acc[i][j] = __fmaf_rn(xv[i].z, wv[j].z, acc[i][j]);
-          acc[i][j] = __fmaf_rn(xv[i].w, wv[j].w, acc[i][j]);
+          acc[p][j] = __ffma2_rn(make_float2(xv[2 * p].x, xv[2 * p + 1].x),
+                                 make_float2(wv[j].x, wv[j].x), acc[p][j]);
+          acc[p][j] = __ffma2_rn(make_float2(xv[2 * p].y, xv[2 * p + 1].y),
+                                 make_float2(wv[j].y, wv[j].y), acc[p][j]);
+          acc[p][j] = __ffma2_rn(make_float2(xv[2 * p].z, xv[2 * p + 1].z),
+                                 make_float2(wv[j].z, wv[j].z), acc[p][j]);
+          acc[p][j] = __ffma2_rn(make_float2(xv[2 * p].w, xv[2 * p + 1].w),
+                                 make_float2(wv[j].w, wv[j].w), acc[p][j]);
         }
     }
   }
@@ -137,7 +155,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_kernel(const uint1
 #pragma unroll
     for (int j = 0; j < TE; ++j) {
       const int e = e0 + we * 8 * TE + el + 8 * j;
-      if (e < N) logits[(size_t)t * N + e] = acc[i][j];
+      if (e < N)
+        logits[(size_t)t * N + e] =
+            (TS && i == TT - 1) ? acc1[j] : ((i & 1) ? acc[i / 2][j].y : acc[i / 2][j].x);
     }
   }
 }
@@ -194,11 +214,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_wide_kernel(
     }
   };
 
-  float acc[TT][TE];
+  static_assert(TT % 2 == 0, "tokens per thread come in pairs");
+  float2 acc[TT / 2][TE];  // packed fmas over token pairs, as in route_logits_kernel
 #pragma unroll
-  for (int i = 0; i < TT; ++i)
+  for (int p = 0; p < TT / 2; ++p)
 #pragma unroll
-    for (int j = 0; j < TE; ++j) acc[i][j] = 0.0f;
+    for (int j = 0; j < TE; ++j) acc[p][j] = make_float2(0.0f, 0.0f);
 
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) {
@@ -235,13 +256,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_wide_kernel(
         wv[j] = *reinterpret_cast<const float4 *>(wb + (we * 8 * TE + el + 8 * j) * LDF + k4);
       // k order is strictly sequential for every output
 #pragma unroll
-      for (int i = 0; i < TT; ++i)
+      for (int p = 0; p < TT / 2; ++p)
 #pragma unroll
         for (int j = 0; j < TE; ++j) {
-          acc[i][j] = __fmaf_rn(xv[i].x, wv[j].x, acc[i][j]);
-          acc[i][j] = __fmaf_rn(xv[i].y, wv[j].y, acc[i][j]);
-          acc[i][j] = __fmaf_rn(xv[i].z, wv[j].z, acc[i][j]);
-          acc[i][j] = __fmaf_rn(xv[i].w, wv[j].w, acc[i][j]);
+          acc[p][j] = __ffma2_rn(make_float2(xv[2 * p].x, xv[2 * p + 1].x),
+                                 make_float2(wv[j].x, wv[j].x), acc[p][j]);
+          acc[p][j] = __ffma2_rn(make_float2(xv[2 * p].y, xv[2 * p + 1].y),
+                                 make_float2(wv[j].y, wv[j].y), acc[p][j]);
+          acc[p][j] = __ffma2_rn(make_float2(xv[2 * p].z, xv[2 * p + 1].z),
+                                 make_float2(wv[j].z, wv[j].z), acc[p][j]);
+          acc[p][j] = __ffma2_rn(make_float2(xv[2 * p].w, xv[2 * p + 1].w),
+                                 make_float2(wv[j].w, wv[j].w), acc[p][j]);
         }
     }
   }
@@ -252,7 +277,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_wide_kernel(
 #pragma unroll
     for (int j = 0; j < TE; ++j) {
       const int e = e0 + we * 8 * TE + el + 8 * j;
-      if (e < N) logits[(size_t)t * N + e] = acc[i][j];
+      if (e < N) logits[(size_t)t * N + e] = (i & 1) ? acc[i / 2][j].y : acc[i / 2][j].x;
     }
   }
 }
