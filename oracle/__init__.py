@@ -57,6 +57,10 @@ def lib():
         L.oracle_f32_to_bf16.restype = ctypes.c_uint16
         L.oracle_quantize_rows.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, _u8p, _u8p]
         L.oracle_quantize_rows.restype = None
+        L.oracle_quantize_rows_f32.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, _u8p, _f32p]
+        L.oracle_quantize_rows_f32.restype = None
+        L.oracle_scale_f32.argtypes = [ctypes.c_float]
+        L.oracle_scale_f32.restype = ctypes.c_float
         L.oracle_route.argtypes = [_u16p, _f32p, ctypes.c_void_p] + [ctypes.c_int] * 7 + [
             ctypes.c_float, ctypes.c_void_p, ctypes.c_int, _i32p, _f32p, ctypes.c_void_p,
             ctypes.c_int]
@@ -141,6 +145,20 @@ def quantize_rows(v: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     sf = np.empty((rows, n // 128), np.uint8)
     lib().oracle_quantize_rows(v, rows, n, q, sf)
     return q, sf
+
+
+def quantize_rows_f32(v: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """1x128-block e4m3 quantisation with binary32 scales amax/448 -> (codes, scales)."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    rows, n = v.shape
+    q = np.empty((rows, n), np.uint8)
+    s = np.empty((rows, n // 128), np.float32)
+    lib().oracle_quantize_rows_f32(v, rows, n, q, s)
+    return q, s
+
+
+def scale_f32(amax: float) -> float:
+    return lib().oracle_scale_f32(amax)
 
 
 def f32_to_bf16(v: np.ndarray) -> np.ndarray:
@@ -232,4 +250,5 @@ def combine(Y: np.ndarray, row_of: np.ndarray, w: np.ndarray, S=None) -> np.ndar
     return out
 
 
-from .ffn import dequant_blocks, dequant_rows, expert_ffn, layer_tokens  # noqa: E402,F401
+from .ffn import (dequant_blocks, dequant_rows, dequant_rows_f32, expert_ffn,  # noqa: E402,F401
+                  layer_tokens)

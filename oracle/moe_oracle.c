@@ -220,6 +220,36 @@ void oracle_quantize_rows(const float *v, int rows, int n, uint8_t *q, uint8_t *
         oracle_quantize_row(v + (size_t)r * n, n, q + (size_t)r * n, sf_byte + (size_t)r * (n / 128));
 }
 
+/*
+ * The same 1x128 quantisation with binary32 scales instead of powers of two (the
+ * "1d2d" scaling of the "Single Batch Overlap (SBO)" PR, §3, with its scales kept as
+ * floats): s_b = amax_b / 448, one binary32 division rounded to nearest even (1 when it
+ * is 0: an all-zero block, or an amax so small that the quotient underflows), and
+ * q = e4m3(v / s_b), one binary32 division per value followed by the e4m3 rounding
+ * above.  The largest |v| of a block lands at (or rounds to) 448.
+ */
+float oracle_scale_f32(float amax)
+{
+    float s = amax / 448.0f;
+    return s == 0.0f ? 1.0f : s;
+}
+
+void oracle_quantize_rows_f32(const float *v, int rows, int n, uint8_t *q, float *s)
+{
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < n / 128; ++b) {
+            const float *x = v + (size_t)r * n + b * 128;
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i)
+                if (fabsf(x[i]) > amax)
+                    amax = fabsf(x[i]);
+            float sb = oracle_scale_f32(amax);
+            for (int i = 0; i < 128; ++i)
+                q[(size_t)r * n + b * 128 + i] = oracle_e4m3_encode(x[i] / sb);
+            s[(size_t)r * (n / 128) + b] = sb;
+        }
+}
+
 /* ---------------------------------------------------------------- routing */
 
 /* "a ranks before b": larger score first, equal scores -> lower index first. */

@@ -156,6 +156,69 @@ def test_quantize_row_round_trip_and_bound():
     assert np.array_equal(q2, codes) and np.all(sf2 == 124)
 
 
+def test_quantize_f32_scale_is_amax_over_448_and_codes_follow():
+    """Binary32 scales: s = fp32(amax / 448) exactly as NumPy's float32 division gives
+    it, q = e4m3 of NumPy's float32 quotient x / s (the encoder pinned above), a zero
+    block gets s = 1 and zero codes, and each block's largest |x| lands on code 448."""
+    rng = np.random.default_rng(8)
+    v = (rng.standard_normal((32, 512)) * 2.0 ** rng.integers(-30, 30, (32, 1))).astype(np.float32)
+    v[3, 128:256] = 0.0
+    q, s = oracle.quantize_rows_f32(v)
+    blocks = v.reshape(32, 4, 128)
+    amax = np.abs(blocks).max(-1)
+    want = np.where(amax == 0, np.float32(1), amax / np.float32(448)).astype(np.float32)
+    assert want.dtype == np.float32 and np.array_equal(s, want)
+    quot = (blocks / s[:, :, None]).astype(np.float32)       # float32 division, RNE
+    assert np.array_equal(q.reshape(32, 4, 128), oracle.e4m3_encode_array(quot))
+    assert np.all(q[3, 128:256] == 0) and s[3, 1] == 1.0
+    table = oracle.e4m3_table()
+    top = np.take_along_axis(q.reshape(32, 4, 128), np.abs(blocks).argmax(-1)[..., None], -1)
+    assert np.all((np.abs(table[top]) == 448.0)[amax > 0])
+
+
+def test_quantize_f32_round_trip_bound_and_power_of_two_case():
+    """e4m3 RNE keeps |q s - x| within 2^-4 |x| (normal range) or 2^-10 s (subnormal
+    codes); when every block's amax is 448 * 2^e the binary32 scale is exactly 2^e and
+    the codes equal the power-of-two path's."""
+    rng = np.random.default_rng(9)
+    v = (rng.standard_normal((16, 384)) * 2.0 ** rng.integers(-10, 10, (16, 1))).astype(np.float32)
+    q, s = oracle.quantize_rows_f32(v)
+    deq = oracle.dequant_rows_f32(q, s).reshape(16, 3, 128)
+    x = v.reshape(16, 3, 128).astype(np.float64)
+    assert np.all(np.abs(deq - x) <= np.maximum(np.abs(x) * 2.0 ** -4,
+                                                2.0 ** -10 * s[:, :, None].astype(np.float64)))
+    table = oracle.e4m3_table()
+    codes = rng.integers(0, 0x7E, (8, 256)).astype(np.uint8)
+    codes[:, ::128] = 0x7E                                    # 448 in every block
+    exact = (table[codes] * 2.0 ** -3).astype(np.float32)
+    q2, s2 = oracle.quantize_rows_f32(exact)
+    q3, sf3 = oracle.quantize_rows(exact)
+    assert np.all(s2 == 2.0 ** -3) and np.array_equal(q2, codes) and np.array_equal(q2, q3)
+
+
+def test_ffn_f32_scales_reduce_to_power_of_two_path():
+    """With inputs whose 1x128 blocks have amax = 448 * 2^e, the binary32-scale FFN
+    sees the same a as the power-of-two FFN; the two paths then differ only through h's
+    scales (amax/448 against the next power of two), so y agrees within the e4m3 step of
+    h and exactly wherever h's block amax is itself 448 * 2^e."""
+    rng = np.random.default_rng(16)
+    W13, W13_sf, W2, W2_sf = _tiny_expert(rng, H=256, I=256)
+    table = oracle.e4m3_table()
+    codes = rng.integers(0, 0x7E, (6, 256)).astype(np.uint8)
+    codes[:, ::128] = 0x7E
+    x = (table[codes] * 2.0 ** 2).astype(np.float32)
+    q0, sf0 = oracle.quantize_rows(x)
+    q1, s1 = oracle.quantize_rows_f32(x)
+    assert np.array_equal(q0, q1) and np.all(s1 == 4.0)
+    y0 = oracle.bf16_to_f32(oracle.expert_ffn(q0, sf0, W13, W13_sf, W2, W2_sf)).astype(np.float64)
+    y1, hq, hs, h = oracle.expert_ffn(q1, s1, W13, W13_sf, W2, W2_sf, want_h=True, scale_fmt=1)
+    y1 = oracle.bf16_to_f32(y1).astype(np.float64)
+    assert np.abs(y1 - y0).max() <= 2.0 ** -3 * np.abs(y0).max()
+    # h requantised with binary32 scales: the definition applied to the fp32 h
+    hq2, hs2 = oracle.quantize_rows_f32(h.astype(np.float32))
+    assert np.array_equal(hq, hq2) and np.array_equal(hs, hs2)
+
+
 # -------------------------------------------------------------------------- logits
 def _tiny_cfg(**kw):
     base = dict(name="t", B=1, H=128, N=8, K=2, I=128)
@@ -522,7 +585,14 @@ def test_golden_decode_dispatch_volume():
     cfg = configs.DECODE
     b = vals["b"]
     assert (b, vals["K"], vals["H"]) == (cfg.B, cfg.K, cfg.H)
-    # the e4m3 row copies the oracle's dispatch writes for this workload
-    rows_bytes = cfg.B * cfg.K * cfg.H * 1
-    assert abs(rows_bytes / 1e6 - vals["MB"]) < 0.05
+    # the e4m3 row bytes the oracle's dispatch writes for the decode workload
+    from support import host_workload
+    cfg, x, W, bias = host_workload("decode")
+    idx, _ = oracle.route(x, W, bias, cfg)
+    d = oracle.dispatch(x, idx, cfg)
+    rows = int((d["row_of"] >= 0).sum())
+    assert rows == cfg.B * cfg.K                     # nothing dropped at capacity 128
+    code_bytes = rows * cfg.H * vals["s"]
+    assert np.count_nonzero(d["A"][d["row_of"][d["row_of"] >= 0]]) > 0.9 * code_bytes
+    assert abs(code_bytes / 1e6 - vals["MB"]) < 0.05
     assert abs(vals["MB"] * 1e-3 / (vals["budget_us"] * 1e-6) - vals["GBps"]) / vals["GBps"] < 0.05
