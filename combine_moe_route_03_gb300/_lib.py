@@ -19,7 +19,8 @@ MOE_OK = 0
 ERRORS = {-1: "MOE_ERR_INVALID", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA"}
 STATUS_CAPACITY, STATUS_TIMEOUT, STATUS_BAD_INDEX = 1, 2, 4
 GEMM_GATEUP_SWIGLU, GEMM_DOWN = 0, 1
-FMT_FP8, FMT_BF16 = 0, 1
+FMT_FP8, FMT_BF16, FMT_FP8_F32 = 0, 1, 2
+SCALE_UE8M0, SCALE_F32 = 0, 1   # moe_gemm_args.scale_fmt / moe_layer.scale_fmt
 
 _c_int, _c_i64, _c_sz, _vp, _f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 
@@ -47,7 +48,8 @@ class GemmArgs(ctypes.Structure):
                 ("W", _vp), ("W_sf", _vp), ("phys2log", _vp), ("tiles", _vp), ("tiles2", _vp),
                 ("row_offset2", _c_i64), ("expert2", _c_int), ("out", _vp),
                 ("out_sf", _vp), ("signal", _vp), ("block_m_signal", _c_int),
-                ("num_sms", _c_int), ("pair_tiles", _c_int), ("status", _vp)]
+                ("num_sms", _c_int), ("pair_tiles", _c_int), ("scale_fmt", _c_int),
+                ("status", _vp)]
 
 
 class CombineCfg(ctypes.Structure):
@@ -68,7 +70,7 @@ class Layer(ctypes.Structure):
             "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",
             "dispatch_ws")] + [("route_ws_bytes", _c_sz), ("dispatch_ws_bytes", _c_sz),
                                ("status", _vp), ("stream2", _vp), ("events", _vp),
-                               ("eplb_max_rep", _c_int)]
+                               ("eplb_max_rep", _c_int), ("scale_fmt", _c_int)]
 
 LAYER_EVENTS = 6
 STAGES = ("route", "dispatch", "gateup", "down", "combine")
@@ -87,8 +89,9 @@ SIGNATURES = {
     "moe_dispatch_noalloc": (_c_int, [ctypes.POINTER(DispatchCfg)] + [_vp] * 15),
     "moe_grouped_gemm_fp8": (_c_int, [ctypes.POINTER(GemmArgs), _vp]),
     "moe_packed_scale_bytes": (_c_sz, [_c_int, _c_int, _c_int]),
-    "moe_scale_bytes": (_c_sz, [_c_i64, _c_int]),
+    "moe_scale_bytes": (_c_sz, [_c_i64, _c_int, _c_int]),
     "moe_pack_weight_scales": (_c_int, [_c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_weight_scales_f32": (_c_int, [_c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "moe_combine": (_c_int, [ctypes.POINTER(CombineCfg), _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_read_status": (_c_int, [_vp, _vp]),
     "moe_last_cuda_error": (_c_int, []),

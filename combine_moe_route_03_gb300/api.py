@@ -11,13 +11,15 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import (FMT_BF16, FMT_FP8, GEMM_DOWN, GEMM_GATEUP_SWIGLU, CombineCfg, DispatchCfg,
-                   EplbCfg, GemmArgs, Layer, RouteCfg, check, load, ptr, stream_ptr)
+from ._lib import (FMT_BF16, FMT_FP8, FMT_FP8_F32, GEMM_DOWN, GEMM_GATEUP_SWIGLU, SCALE_F32,
+                   SCALE_UE8M0, CombineCfg, DispatchCfg, EplbCfg, GemmArgs, Layer, RouteCfg, check,
+                   load, ptr, stream_ptr)
 from .configs import MASKED, MoEConfig
 
 __all__ = ["route", "eplb_build_map", "eplb_plan", "check_eplb_map", "EplbRecorder", "dispatch", "dispatch_sizes", "pack_weight_scales",
            "grouped_gemm_fp8", "combine", "read_status", "new_status", "MoELayer",
-           "FMT_FP8", "FMT_BF16", "GEMM_GATEUP_SWIGLU", "GEMM_DOWN", "num_sms"]
+           "FMT_FP8", "FMT_BF16", "FMT_FP8_F32", "SCALE_UE8M0", "SCALE_F32", "GEMM_GATEUP_SWIGLU",
+           "GEMM_DOWN", "num_sms", "scale_bytes", "weight_scales_f32"]
 
 
 def num_sms() -> int:
@@ -200,7 +202,7 @@ def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=N
     o = out if out is not None else {}
     if "A" not in o:
         o["A"] = torch.empty((rows, H * (2 if fmt == FMT_BF16 else 1)), dtype=torch.uint8, device=dev)
-        o["A_sf"] = torch.empty(scale_bytes(rows, H), dtype=torch.uint8, device=dev)
+        o["A_sf"] = torch.empty(scale_bytes(rows, H, fmt), dtype=torch.uint8, device=dev)
         o["counts"] = torch.empty(cfg.N_phys, dtype=torch.int32, device=dev)
         o["row_of"] = torch.empty((B, cfg.K), dtype=torch.int32, device=dev)
         o["src_of"] = torch.empty(rows, dtype=torch.int32, device=dev)
@@ -209,7 +211,7 @@ def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=N
         if shared:
             srows = (B + 127) // 128 * 128
             o["As"] = torch.empty((srows, H), dtype=torch.uint8, device=dev)
-            o["As_sf"] = torch.empty(scale_bytes(srows, H), dtype=torch.uint8, device=dev)
+            o["As_sf"] = torch.empty(scale_bytes(srows, H, fmt), dtype=torch.uint8, device=dev)
             o["shared_tiles"] = torch.empty(8 + 16 * (srows // 128), dtype=torch.int32, device=dev)
     st = status if status is not None else new_status(dev)
     check(load().moe_dispatch(ctypes.byref(dc), ptr(x), ptr(topk_idx), ptr(log2phys), ptr(rep),
@@ -221,12 +223,23 @@ def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=N
     return o
 
 
-def scale_bytes(rows: int, k: int) -> int:
-    """Bytes of the SF atoms of an activation tensor [rows][k] (moe_scale_bytes)."""
-    n = load().moe_scale_bytes(rows, k)
+def scale_bytes(rows: int, k: int, fmt: int = 0) -> int:
+    """Bytes of the scales of an activation tensor [rows][k] in format fmt (FMT_FP8: SF
+    atoms; FMT_FP8_F32: float [rows][k/128]) (moe_scale_bytes)."""
+    n = load().moe_scale_bytes(rows, k, FMT_FP8_F32 if fmt == FMT_FP8_F32 else FMT_FP8)
     if n == 0:
         raise ValueError(f"scale atoms need rows and k multiples of 128 (got {rows}, {k})")
     return n
+
+
+def weight_scales_f32(W_sf: torch.Tensor, stream=None) -> torch.Tensor:
+    """UE8M0 bytes [E][n/128][k/128] (device) -> float 2^(byte-127), same shape (the
+    weight scales of the binary32-scale mode)."""
+    E, nb, kb = W_sf.shape
+    out = torch.empty((E, nb, kb), dtype=torch.float32, device=W_sf.device)
+    check(load().moe_weight_scales_f32(E, nb * 128, kb * 128, ptr(W_sf), ptr(out),
+                                       stream_ptr(stream)), "moe_weight_scales_f32")
+    return out
 
 
 def pack_weight_scales(W_sf: torch.Tensor, stream=None) -> torch.Tensor:
@@ -247,8 +260,9 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
                      block_m_signal: int = 64, num_sms_: int = 0,
                      status: torch.Tensor | None = None, stream=None,
                      tiles2: torch.Tensor | None = None, row_offset2: int = 0, expert2: int = 0,
-                     pair_tiles: int = 0):
-    """moe_grouped_gemm_fp8.  W e4m3 [E][n][k]; A e4m3 [rows][k]."""
+                     pair_tiles: int = 0, scale_fmt: int = SCALE_UE8M0):
+    """moe_grouped_gemm_fp8.  W e4m3 [E][n][k]; A e4m3 [rows][k]; scale_fmt SCALE_F32:
+    A_sf float [rows][k/128] and W_sf_atoms the float [E][n/128][k/128] scales."""
     E, n, k = W.shape
     rows = A.shape[0]
     dev = A.device
@@ -256,13 +270,15 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
         I = n // 2
         if out is None:
             out = torch.empty((rows, I), dtype=torch.uint8, device=dev)
-            out_sf = torch.empty(scale_bytes(rows, I), dtype=torch.uint8, device=dev)
+            out_sf = torch.empty(scale_bytes(rows, I, FMT_FP8_F32 if scale_fmt else FMT_FP8),
+                                 dtype=torch.uint8, device=dev)
     elif out is None:
         out = torch.empty((rows, n), dtype=torch.bfloat16, device=dev)
     st = status if status is not None else new_status(dev)
     g = GemmArgs(op, n, k, rows, max_tiles, E, ptr(A), ptr(A_sf), ptr(W), ptr(W_sf_atoms),
                  ptr(phys2log), ptr(tiles), ptr(tiles2), row_offset2, expert2, ptr(out),
-                 ptr(out_sf), ptr(signal), block_m_signal, num_sms_, pair_tiles, ptr(st))
+                 ptr(out_sf), ptr(signal), block_m_signal, num_sms_, pair_tiles, scale_fmt,
+                 ptr(st))
     check(load().moe_grouped_gemm_fp8(ctypes.byref(g), stream_ptr(stream)), "moe_grouped_gemm_fp8")
     return (out, out_sf) if op == GEMM_GATEUP_SWIGLU else out
 
@@ -327,8 +343,13 @@ class MoELayer:
         else:
             self.W13, self.W2 = weights["W13"], weights["W2"]
             W13_sf, W2_sf = weights["W13_sf"], weights["W2_sf"]
-        self.W13_sf = pack_weight_scales(W13_sf)
-        self.W2_sf = pack_weight_scales(W2_sf)
+        if cfg.scale_fmt:       # binary32 scales, read per k-block by the epilogue
+            self.W13_sf = weight_scales_f32(W13_sf)
+            self.W2_sf = weight_scales_f32(W2_sf)
+        else:                   # SF atoms for the tensor core's block scaling
+            self.W13_sf = pack_weight_scales(W13_sf)
+            self.W2_sf = pack_weight_scales(W2_sf)
+        afmt = FMT_FP8_F32 if cfg.scale_fmt else FMT_FP8
         self.log2phys = self.rep = self.phys2log = None
         if eplb_map is not None:
             check_eplb_map(eplb_map, cfg.N, cfg.N_phys)
@@ -348,9 +369,9 @@ class MoELayer:
         self.tiles = t(8 + 16 * self.max_tiles, dtype=torch.int32)
         self.shared_tiles = t(8 + 16 * (self.srows // 128), dtype=torch.int32) if cfg.shared else None
         self.A = t(rows, H)
-        self.A_sf = t(scale_bytes(rows, H))
+        self.A_sf = t(scale_bytes(rows, H, afmt))
         self.H1 = t(rows, I)
-        self.H1_sf = t(scale_bytes(rows, I))
+        self.H1_sf = t(scale_bytes(rows, I, afmt))
         self.Y = t(rows, H, dtype=torch.bfloat16)
         self.S = self.Y[self.rows:] if cfg.shared else None
         self.signal = t(rows // cfg.block_m_signal, dtype=torch.int32) if cfg.sbo else None
@@ -369,6 +390,7 @@ class MoELayer:
         lay.combine_ctas = combine_ctas
         lay.gemm_pairs = gemm_pairs
         lay.eplb_max_rep = 0 if self.log2phys is None else self.log2phys.shape[1]
+        lay.scale_fmt = cfg.scale_fmt
         names = ["x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
                  "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",
                  "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",

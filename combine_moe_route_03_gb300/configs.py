@@ -56,6 +56,7 @@ class MoEConfig:
     zipf_s: float = 1.2
     zipf_tau: float = 0.05
     seed: int = 0
+    scale_fmt: int = 0     # 0: UE8M0 power-of-two scales; 1: binary32 scales amax/448
 
     @property
     def N_phys(self) -> int:
@@ -108,5 +109,8 @@ ALL.update(PROFILE)
 # The SBO workload run sequentially (down GEMM on every SM, then the combine): the
 # comparison arm of single-batch overlap.
 SBO_SEQ = SBO.with_(name="sbo_seq", sbo=False)
-VARIANTS = {SBO_SEQ.name: SBO_SEQ}
+# The decode layer with binary32 activation scales (1d2d with float scales, promoted per
+# k-block in software) instead of power-of-two ones.
+DECODE_F32 = DECODE.with_(name="decode_f32", scale_fmt=1)
+VARIANTS = {c.name: c for c in (SBO_SEQ, DECODE_F32)}
 ALL.update(VARIANTS)

@@ -121,6 +121,8 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   const int sbo_ctas = L->combine_ctas > 0 ? L->combine_ctas : 32;  // SBO consumer CTAs
   if (L->sbo && sbo_ctas >= sms) return MOE_ERR_INVALID;
   if (L->gemm_pairs == 1 && (rc.H % 256 || L->I % 256)) return MOE_ERR_UNSUPPORTED;
+  if (L->scale_fmt != 0 && L->scale_fmt != 1) return MOE_ERR_INVALID;
+  if (L->scale_fmt == 1 && L->gemm_pairs == 1) return MOE_ERR_UNSUPPORTED;
   moe_dispatch_cfg dc;
   dc.B = rc.B;
   dc.H = rc.H;
@@ -129,7 +131,7 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   dc.N_phys = L->N_phys;
   dc.layout = L->layout;
   dc.cap = L->cap;
-  dc.fmt = MOE_FMT_FP8;
+  dc.fmt = L->scale_fmt ? MOE_FMT_FP8_F32 : MOE_FMT_FP8;
   dc.max_rep = L->eplb_max_rep;
   // the row buffers and the tile list must hold what dispatch writes (before any launch)
   const int64_t need_rows = moe_dispatch_rows(&dc);
@@ -145,7 +147,9 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   uint8_t *A = static_cast<uint8_t *>(L->A), *A_sf = static_cast<uint8_t *>(L->A_sf);
   rc_ = moe_dispatch(&dc, L->x, L->topk_idx, L->log2phys, L->rep, A, A_sf, L->counts, L->row_of,
                      nullptr, L->tiles, L->has_shared ? A + L->rows * rc.H : nullptr,
-                     L->has_shared ? A_sf + (size_t)L->rows * sf_groups(rc.H) * 4 : nullptr,
+                     L->has_shared ? A_sf + (L->scale_fmt ? (size_t)L->rows * (rc.H / 128) * 4
+                                                          : (size_t)L->rows * sf_groups(rc.H) * 4)
+                                   : nullptr,
                      L->has_shared ? L->shared_tiles : nullptr, L->dispatch_ws,
                      L->dispatch_ws_bytes, L->status, stream);
   if (rc_) return rc_;
@@ -174,9 +178,11 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   g.status = L->status;
   // 2-SM GEMMs when experts average at least one full M tile (and both GEMMs' K allow
   // 256-deep stages); one CTA per tile otherwise (decode: HBM-bound on the weights)
-  g.pair_tiles = L->gemm_pairs == 1 ||
-                 (L->gemm_pairs == 0 && (int64_t)rc.B * rc.K >= 128LL * L->N_phys &&
-                  rc.H % 256 == 0 && L->I % 256 == 0);
+  g.pair_tiles = !L->scale_fmt &&
+                 (L->gemm_pairs == 1 ||
+                  (L->gemm_pairs == 0 && (int64_t)rc.B * rc.K >= 128LL * L->N_phys &&
+                   rc.H % 256 == 0 && L->I % 256 == 0));
+  g.scale_fmt = L->scale_fmt;
   if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
   mark(3);
   g.op = MOE_GEMM_DOWN;

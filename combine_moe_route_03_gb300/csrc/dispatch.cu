@@ -310,12 +310,13 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
 // quantises kCols/32 values (8 or 16), 128/(kCols/32) lanes share one 128-column
 // block's amax, and each lane stores 8 or 16 bytes into each of the K copies.  The
 // task holding a token's first chunk also writes row_of / src_of.
-template <bool kFp8, int kCols>
+template <int kFmt, int kCols>
 __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
     const uint16_t *__restrict__ x, int B, int H, int K, int N_phys, int layout, int cap,
     int cpt, DispatchWs ws, uint8_t *__restrict__ A, uint8_t *__restrict__ A_sf,
     int32_t *__restrict__ row_of, int32_t *__restrict__ src_of, uint8_t *__restrict__ As,
     uint8_t *__restrict__ As_sf) {
+  constexpr bool kFp8 = kFmt != MOE_FMT_BF16;
   static_assert(kCols == 256 || (kFp8 && kCols == 512), "chunk width");
   constexpr int kPer = kCols / 32;    // columns per lane
   constexpr int kBlk = 128 / kPer;    // lanes per 128-column scale block
@@ -381,14 +382,25 @@ __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
 #pragma unroll
       for (int off = kBlk / 2; off > 0; off >>= 1)  // the lanes of one 128-column block
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const int e = ue8m0_exp(amax);
-      const float inv = pow2i(-e);
       uint32_t q[kPer / 4];
+      uint8_t sfb = 0;
+      float sf32 = 1.0f;
+      if constexpr (kFmt == MOE_FMT_FP8) {  // power-of-two scale: an exact multiply
+        const int e = ue8m0_exp(amax);
+        const float inv = pow2i(-e);
 #pragma unroll
-      for (int i = 0; i < kPer / 4; ++i)
-        q[i] = e4m3x2(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv)) |
-               (e4m3x2(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv)) << 16);
-      const uint8_t sfb = (uint8_t)(e + 127);
+        for (int i = 0; i < kPer / 4; ++i)
+          q[i] = e4m3x2(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv)) |
+                 (e4m3x2(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv)) << 16);
+        sfb = (uint8_t)(e + 127);
+      } else {  // binary32 scale amax / 448 (1 when it is 0), IEEE divisions
+        sf32 = __fdiv_rn(amax, 448.0f);
+        if (sf32 == 0.0f) sf32 = 1.0f;
+#pragma unroll
+        for (int i = 0; i < kPer / 4; ++i)
+          q[i] = e4m3x2(__fdiv_rn(f[4 * i], sf32), __fdiv_rn(f[4 * i + 1], sf32)) |
+                 (e4m3x2(__fdiv_rn(f[4 * i + 2], sf32), __fdiv_rn(f[4 * i + 3], sf32)) << 16);
+      }
       const int kb = h >> 7;
       auto put = [&](uint8_t *dst) {
         if constexpr (kPer == 8)
@@ -401,13 +413,21 @@ __global__ void __launch_bounds__(kScatterWarps * 32) dispatch_scatter_kernel(
         for (int k = 0; k < 16; ++k) {
           if (k >= K || rows[k] < 0) continue;
           put(A + (size_t)rows[k] * H + h);
-          if ((lane & (kBlk - 1)) == 0)
-            A_sf[sf_byte_off(rows[k], kb, Kg)] = sfb;
+          if ((lane & (kBlk - 1)) == 0) {
+            if constexpr (kFmt == MOE_FMT_FP8)
+              A_sf[sf_byte_off(rows[k], kb, Kg)] = sfb;
+            else
+              reinterpret_cast<float *>(A_sf)[(size_t)rows[k] * (H / 128) + kb] = sf32;
+          }
         }
         if (As) {
           put(As + (size_t)t * H + h);
-          if ((lane & (kBlk - 1)) == 0)
-            As_sf[sf_byte_off(t, kb, Kg)] = sfb;
+          if ((lane & (kBlk - 1)) == 0) {
+            if constexpr (kFmt == MOE_FMT_FP8)
+              As_sf[sf_byte_off(t, kb, Kg)] = sfb;
+            else
+              reinterpret_cast<float *>(As_sf)[(size_t)t * (H / 128) + kb] = sf32;
+          }
         }
       }
     }
@@ -456,24 +476,27 @@ int launch_scatter(const moe_dispatch_cfg *c, int B, int K, int Np, const void *
                    const DispatchWs &ws, void *A, void *A_sf, int32_t *row_of, int32_t *src_of,
                    void *As, void *As_sf, cudaStream_t st) {
   const uint16_t *xb = static_cast<const uint16_t *>(x);
-  const bool fp8 = c->fmt == MOE_FMT_FP8;
+  const bool fp8 = c->fmt != MOE_FMT_BF16;
   const int cols = fp8 && c->H % 512 == 0 ? 512 : 256;
   const int cpt = scatter_cpt(B, c->H, cols);
   const long tasks = (long)B * (((c->H + cols - 1) / cols + cpt - 1) / cpt);
   const unsigned grid = (unsigned)((tasks + kScatterWarps - 1) / kScatterWarps);
-  uint8_t *a = static_cast<uint8_t *>(A);
+  uint8_t *a = static_cast<uint8_t *>(A), *asf = static_cast<uint8_t *>(A_sf);
+  uint8_t *as = static_cast<uint8_t *>(As), *assf = static_cast<uint8_t *>(As_sf);
+#define MOE_SCATTER(FMT, COLS)                                                         \
+  dispatch_scatter_kernel<FMT, COLS><<<grid, kScatterWarps * 32, 0, st>>>(               \
+      xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, a, asf, row_of, src_of, as, assf)
   if (!fp8)
-    dispatch_scatter_kernel<false, 256><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, a, nullptr, row_of, src_of, nullptr,
-        nullptr);
+    MOE_SCATTER(MOE_FMT_BF16, 256);
+  else if (c->fmt == MOE_FMT_FP8 && cols == 512)
+    MOE_SCATTER(MOE_FMT_FP8, 512);
+  else if (c->fmt == MOE_FMT_FP8)
+    MOE_SCATTER(MOE_FMT_FP8, 256);
   else if (cols == 512)
-    dispatch_scatter_kernel<true, 512><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, a, static_cast<uint8_t *>(A_sf), row_of,
-        src_of, static_cast<uint8_t *>(As), static_cast<uint8_t *>(As_sf));
+    MOE_SCATTER(MOE_FMT_FP8_F32, 512);
   else
-    dispatch_scatter_kernel<true, 256><<<grid, kScatterWarps * 32, 0, st>>>(
-        xb, B, c->H, K, Np, c->layout, c->cap, cpt, ws, a, static_cast<uint8_t *>(A_sf), row_of,
-        src_of, static_cast<uint8_t *>(As), static_cast<uint8_t *>(As_sf));
+    MOE_SCATTER(MOE_FMT_FP8_F32, 256);
+#undef MOE_SCATTER
   return check_launch();
 }
 
@@ -488,7 +511,8 @@ static int dispatch_check(const moe_dispatch_cfg *c) {
     return MOE_ERR_INVALID;
   if (c->H % 128 || c->K > 16 || c->N_phys > kScanThreads) return MOE_ERR_UNSUPPORTED;
   if (c->layout != MOE_LAYOUT_CONTIG && c->layout != MOE_LAYOUT_MASKED) return MOE_ERR_INVALID;
-  if (c->fmt != MOE_FMT_FP8 && c->fmt != MOE_FMT_BF16) return MOE_ERR_INVALID;
+  if (c->fmt != MOE_FMT_FP8 && c->fmt != MOE_FMT_BF16 && c->fmt != MOE_FMT_FP8_F32)
+    return MOE_ERR_INVALID;
   if (c->layout == MOE_LAYOUT_MASKED && (c->cap <= 0 || c->cap % 128)) return MOE_ERR_UNSUPPORTED;
   if (c->max_rep < 0 || c->max_rep > 64) return MOE_ERR_INVALID;
   return MOE_OK;
@@ -531,9 +555,9 @@ extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int3
     return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
   }
   if (!x || !topk_idx || !A || !row_of || !workspace) return MOE_ERR_INVALID;
-  if (c->fmt == MOE_FMT_FP8 && !A_sf) return MOE_ERR_INVALID;
+  if (c->fmt != MOE_FMT_BF16 && !A_sf) return MOE_ERR_INVALID;
   if ((log2phys == nullptr) != (rep == nullptr)) return MOE_ERR_INVALID;
-  if (A_shared && (c->fmt != MOE_FMT_FP8 || !A_shared_sf)) return MOE_ERR_INVALID;
+  if (A_shared && (c->fmt == MOE_FMT_BF16 || !A_shared_sf)) return MOE_ERR_INVALID;
   if (workspace_bytes < moe_dispatch_workspace_size(c)) return MOE_ERR_INVALID;
   if ((uintptr_t)x % 16 || (uintptr_t)A % 16 || (A_sf && (uintptr_t)A_sf % 16) ||
       (A_shared && (uintptr_t)A_shared % 16))
@@ -599,9 +623,9 @@ extern "C" int moe_dispatch_noalloc(const moe_dispatch_cfg *c, const void *x,
     return e == cudaSuccess ? MOE_OK : set_cuda_error(e);
   }
   if (!x || !topk_idx || !A || !row_of) return MOE_ERR_INVALID;
-  if (c->fmt == MOE_FMT_FP8 && !A_sf) return MOE_ERR_INVALID;
+  if (c->fmt != MOE_FMT_BF16 && !A_sf) return MOE_ERR_INVALID;
   if ((log2phys == nullptr) != (rep == nullptr)) return MOE_ERR_INVALID;
-  if (A_shared && (c->fmt != MOE_FMT_FP8 || !A_shared_sf)) return MOE_ERR_INVALID;
+  if (A_shared && (c->fmt == MOE_FMT_BF16 || !A_shared_sf)) return MOE_ERR_INVALID;
   if ((uintptr_t)x % 16 || (uintptr_t)A % 16 || (A_sf && (uintptr_t)A_sf % 16) ||
       (A_shared && (uintptr_t)A_shared % 16))
     return MOE_ERR_INVALID;

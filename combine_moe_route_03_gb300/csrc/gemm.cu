@@ -47,7 +47,9 @@ constexpr uint32_t OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_BYTES;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
 constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-constexpr uint32_t OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
+// full, empty [STAGES]; accumulator full, empty; binary32-scale mode: partial full [2],
+// partial empty [2]
+constexpr uint32_t OFF_MISC = OFF_BAR + (2 * STAGES + 6) * 8;
 constexpr uint32_t OFF_AMAX = OFF_MISC + 16;  // [2][128] partial row amax of the epilogue
 constexpr uint32_t OFF_UNITQ = OFF_AMAX + 2 * 128 * 4;  // [kUnitQ] decoded units
 constexpr uint32_t OFF_UBAR = OFF_UNITQ + kUnitQ * 32;  // [kUnitQ] full, [kUnitQ] empty
@@ -73,6 +75,7 @@ struct GemmParams {
   int32_t *signal;
   int bm_signal;
   int32_t *status;
+  int scale_fmt;  // 0: UE8M0 SF atoms; 1: binary32 scales, promoted per k-block
 };
 
 struct Unit {
@@ -155,21 +158,20 @@ __device__ __forceinline__ void store_rows_64B(uint8_t *stage, const uint4 *w, u
   __syncwarp();
 }
 
-// store_rows_64B of 32 fp32 values per row, rounded to bf16.
-__device__ __forceinline__ void store_bf16_rows(uint8_t *stage, const uint32_t *v,
-                                                uint8_t *out_row0, size_t pitch, int nrows,
-                                                int lane) {
+// store_rows_64B of 32 fp32 values per row (float, or their bits as uint32_t), rounded
+// to bf16.
+__device__ __forceinline__ float as_f32(uint32_t b) { return __uint_as_float(b); }
+__device__ __forceinline__ float as_f32(float f) { return f; }
+template <class T>
+__device__ __forceinline__ void store_bf16_rows(uint8_t *stage, const T *v, uint8_t *out_row0,
+                                                size_t pitch, int nrows, int lane) {
   uint4 w[4];
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
-    w[p].x = f32_to_bf16_bits(__uint_as_float(v[8 * p + 0])) |
-             (f32_to_bf16_bits(__uint_as_float(v[8 * p + 1])) << 16);
-    w[p].y = f32_to_bf16_bits(__uint_as_float(v[8 * p + 2])) |
-             (f32_to_bf16_bits(__uint_as_float(v[8 * p + 3])) << 16);
-    w[p].z = f32_to_bf16_bits(__uint_as_float(v[8 * p + 4])) |
-             (f32_to_bf16_bits(__uint_as_float(v[8 * p + 5])) << 16);
-    w[p].w = f32_to_bf16_bits(__uint_as_float(v[8 * p + 6])) |
-             (f32_to_bf16_bits(__uint_as_float(v[8 * p + 7])) << 16);
+    w[p].x = f32_to_bf16_bits(as_f32(v[8 * p + 0])) | (f32_to_bf16_bits(as_f32(v[8 * p + 1])) << 16);
+    w[p].y = f32_to_bf16_bits(as_f32(v[8 * p + 2])) | (f32_to_bf16_bits(as_f32(v[8 * p + 3])) << 16);
+    w[p].z = f32_to_bf16_bits(as_f32(v[8 * p + 4])) | (f32_to_bf16_bits(as_f32(v[8 * p + 5])) << 16);
+    w[p].w = f32_to_bf16_bits(as_f32(v[8 * p + 6])) | (f32_to_bf16_bits(as_f32(v[8 * p + 7])) << 16);
   }
   store_rows_64B(stage, w, out_row0, pitch, nrows, lane);
 }
@@ -264,9 +266,122 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &P, int row0, int
   }
 }
 
+// Binary32-scale mode ("Single Batch Overlap (SBO)" PR, §3: the 1d2d scaling with float
+// scales, promoted in software): the tensor core computes each 128-deep k-block's
+// partial product unscaled (kind::f8f6f4) into one of two TMEM buffers (k-block g of
+// the CTA into buffer g % 2), and the epilogue warps fold it into 128 fp32 accumulators
+// per thread, acc += (s_a[row][kb] * s_w[block][kb]) * partial, one fma per value with
+// the k-blocks in order; then SwiGLU with binary32-scale requantisation of h (s = amax /
+// 448, code = e4m3(h / s)) or bf16 rounding, as epilogue_tile.  Returns false when a
+// wait gave up.  All kEpiThreads epilogue threads call it.
+__device__ __forceinline__ bool epilogue_f32(const GemmParams &P, const Unit &U, uint32_t tmem,
+                                             int q, int half, int row_local, int warp, int lane,
+                                             float *amax_x, uint8_t *stage, uint32_t bar_pfull,
+                                             uint32_t bar_pempty, uint32_t &g,
+                                             volatile int *abort) {
+  const bool gateup = P.op == MOE_GEMM_GATEUP_SWIGLU;
+  const int64_t r = (int64_t)U.row0 + row_local;  // < P.rows: tile_ok holds for the unit
+  const bool store = row_local < U.nvalid;
+  const float *sa = reinterpret_cast<const float *>(P.A_sf) + (size_t)r * P.Kb;
+  const int nb0 = gateup ? U.ni : 2 * U.ni + half, nb1 = gateup ? P.I / 128 + U.ni : nb0;
+  const float *sw = reinterpret_cast<const float *>(P.W_sf);
+  const float *sw0 = sw + ((size_t)U.we * (P.n / 128) + nb0) * P.Kb;
+  const float *sw1 = sw + ((size_t)U.we * (P.n / 128) + nb1) * P.Kb;
+  // this thread's columns: gate [64h, +64) and up [128 + 64h, +64), or [128h, +128)
+  const int c0 = gateup ? 64 * half : 128 * half, c1 = gateup ? 128 + 64 * half : c0 + 64;
+  const uint32_t t_lane = tmem + ((uint32_t)(32 * q) << 16);
+  float acc[128];
+#pragma unroll
+  for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+  // a warp whose 32 rows hold no data (most of a decode tile) only frees the buffers
+  const bool busy = row_local - lane < U.nvalid;
+  float sa_next = sa[0], w0_next = sw0[0], w1_next = sw1[0];
+  for (int kb = 0; kb < P.Kb; ++kb) {
+    const int b = g & 1;
+    if (!mbar_wait(bar_pfull + 8 * b, (g >> 1) & 1, abort, kWaitLimitNs)) return false;
+    tc_fence_after();
+    if (busy) {
+      const float s0 = __fmul_rn(sa_next, w0_next), s1 = __fmul_rn(sa_next, w1_next);
+      if (kb + 1 < P.Kb) {  // the next k-block's scales load while this one folds
+        sa_next = sa[kb + 1];
+        w0_next = sw0[kb + 1];
+        w1_next = sw1[kb + 1];
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {  // gate (or first 64) columns, then up (or next 64)
+        uint32_t v[64];
+        const uint32_t col = t_lane + 256 * b + (hh ? c1 : c0);
+        MOE_TMEM_LD_32x32b_X32(col, v);
+        MOE_TMEM_LD_32x32b_X32(col + 32, (v + 32));
+        tc_wait_ld();
+        const float sc = hh ? s1 : s0;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          acc[64 * hh + i] = __fmaf_rn(sc, __uint_as_float(v[i]), acc[64 * hh + i]);
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(bar_pempty + 8 * b);
+    ++g;
+  }
+  const int64_t wrow0 = (int64_t)U.row0 + (row_local - lane);
+  const int nrows = (int)min((int64_t)min(U.nvalid - (row_local - lane), 32), P.rows - wrow0);
+  if (gateup) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float v = __fdividef(acc[i], 1.0f + __expf(-acc[i])) * acc[64 + i];  // silu(g) u
+      acc[i] = v;
+      amax = fmaxf(amax, fabsf(v));
+    }
+    amax_x[half * 128 + row_local] = amax;  // the 1x128 block of h spans both halves
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+    amax = fmaxf(amax, amax_x[(half ^ 1) * 128 + row_local]);
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+    float sh = __fdiv_rn(amax, 448.0f);
+    if (sh == 0.0f) sh = 1.0f;
+    uint4 w[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t *wp = &w[c].x;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = 16 * c + 4 * j;
+        wp[j] = e4m3x2(__fdiv_rn(acc[i], sh), __fdiv_rn(acc[i + 1], sh)) |
+                (e4m3x2(__fdiv_rn(acc[i + 2], sh), __fdiv_rn(acc[i + 3], sh)) << 16);
+      }
+    }
+    if (store && half == 0)
+      reinterpret_cast<float *>(P.out_sf)[(size_t)r * (P.I / 128) + U.ni] = sh;
+    if (nrows > 0)
+      store_rows_64B(stage, w, P.out + (size_t)wrow0 * P.I + (size_t)U.ni * 128 + 64 * half,
+                     (size_t)P.I, nrows, lane);
+  } else {
+    if (nrows > 0) {
+      uint8_t *dst = P.out + ((size_t)wrow0 * P.n + (size_t)U.ni * 256 + 128 * half) * 2;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        store_bf16_rows(stage, acc + 32 * c, dst + 64 * c, (size_t)P.n * 2, nrows, lane);
+    }
+    if (P.signal) {
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      if (warp == 2 && lane == 0) {
+        for (int j = 0; j * P.bm_signal < BM; ++j)
+          if (j * P.bm_signal < U.nvalid && U.row0 + j * P.bm_signal < P.rows)
+            red_release_gpu_add(P.signal + (U.row0 + j * P.bm_signal) / P.bm_signal, 1);
+      }
+    }
+  }
+  return true;
+}
+
 // tmA loads full 128-row A tiles; tmA32 loads 32-row slices, used for tiles with
 // fewer valid rows so rows that hold no data are never fetched (the MMA then reads
 // stale shared memory for them, which only feeds accumulator rows never stored).
+// kF32: binary32-scale mode (see epilogue_f32); otherwise UE8M0 block scaling in the
+// tensor core.
+template <bool kF32>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA32,
@@ -280,6 +395,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t bar_empty = bar_full + 8 * STAGES;           // [STAGES]
   const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
+  const uint32_t bar_pfull = bar_acc_empty + 8;               // [2], binary32-scale mode
+  const uint32_t bar_pempty = bar_pfull + 16;                 // [2]
   const uint32_t bar_unit_full = s_base + OFF_UBAR;          // [kUnitQ]
   const uint32_t bar_unit_empty = bar_unit_full + 8 * kUnitQ; // [kUnitQ]
   Unit *unit_q = reinterpret_cast<Unit *>(smem + OFF_UNITQ);
@@ -293,6 +410,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, kEpiThreads);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_pfull + 8 * b, 1);
+      mbar_init(bar_pempty + 8 * b, kEpiThreads);
+    }
     for (int q = 0; q < kUnitQ; ++q) {
       mbar_init(bar_unit_full + 8 * q, 1);
       mbar_init(bar_unit_empty + 8 * q, 2 + kEpiThreads / 32);  // producer, MMA, epilogue warps
@@ -378,7 +499,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           const uint32_t full = bar_full + 8 * stage;
-          const bool sf = (kb & 3) == 0;
+          const bool sf = !kF32 && (kb & 3) == 0;  // binary32 scales are not staged
           mbar_arrive_expect_tx(full, sf ? tx + tx_sf : tx);
           const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
           const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
@@ -423,7 +544,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t idesc_base = ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
                                   ((uint32_t)(BM >> 4) << 24);
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0, acc_phase = 0, pg = 0;
       bool ok = true;
       for (int seq = 0; ok; ++seq) {
         Unit U;
@@ -434,6 +555,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         release_unit(seq);
         if (U.end) break;
         if (!U.ok) continue;
+        if constexpr (kF32) {
+          // each k-block's unscaled partial into TMEM buffer g % 2, once the epilogue has
+          // folded the k-block two before out of it
+          const uint32_t idesc_f8 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+          for (int kb = 0; kb < P.Kb; ++kb) {
+            const int b = pg & 1;
+            if (!mbar_wait(bar_full + 8 * stage, phase, abort, kWaitLimitNs) ||
+                !mbar_wait(bar_pempty + 8 * b, ((pg >> 1) & 1) ^ 1, abort, kWaitLimitNs)) {
+              fail(P.status, abort);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
+            const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
+#pragma unroll
+            for (int j = 0; j < BK / 32; ++j)
+              tc_mma_f8(tmem + 256 * b, smem_desc(sa + 32 * j, 16, 1024, 2),
+                        smem_desc(sb + 32 * j, 16, 1024, 2), idesc_f8, j != 0);
+            tc_commit(bar_empty + 8 * stage);
+            tc_commit(bar_pfull + 8 * b);
+            ++pg;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          continue;
+        }
         if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
           fail(P.status, abort);
           break;
@@ -489,7 +639,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
     float *amax_x = reinterpret_cast<float *>(smem + OFF_AMAX);  // [half][row]
     uint8_t *stage = smem + OFF_STAGE + (warp - 2) * STAGE_BYTES;
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0, pg = 0;
     for (int seq = 0;; ++seq) {
       Unit U;
       if (!take_unit(seq, U)) {
@@ -500,6 +650,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (lane == 0) release_unit(seq);
       if (U.end) break;
       if (!U.ok) continue;
+      if constexpr (kF32) {
+        if (!epilogue_f32(P, U, tmem, q, half, row_local, warp, lane, amax_x, stage, bar_pfull,
+                          bar_pempty, pg, abort)) {
+          fail(P.status, abort);
+          break;
+        }
+        continue;
+      }
       if (!mbar_wait(bar_acc_full, acc_phase, abort, kWaitLimitNs)) {
         fail(P.status, abort);
         break;
@@ -1167,8 +1325,10 @@ extern "C" size_t moe_packed_scale_bytes(int E, int n, int k) {
   return (size_t)E * (n / 128) * sf_groups(k) * 512;
 }
 
-extern "C" size_t moe_scale_bytes(int64_t rows, int k) {
+extern "C" size_t moe_scale_bytes(int64_t rows, int k, int fmt) {
   if (rows <= 0 || k <= 0 || rows % 128 || k % 128) return 0;
+  if (fmt == MOE_FMT_FP8_F32) return (size_t)rows * (k / 128) * 4;
+  if (fmt != MOE_FMT_FP8) return 0;
   return (size_t)(rows / 128) * sf_groups(k) * 512;
 }
 
@@ -1183,10 +1343,28 @@ extern "C" int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf,
   return check_launch();
 }
 
+__global__ void weight_scales_f32_kernel(const uint8_t *__restrict__ sf, float *__restrict__ out,
+                                         size_t n) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = pow2i((int)sf[i] - 127);
+}
+
+extern "C" int moe_weight_scales_f32(int E, int n, int k, const uint8_t *W_sf, float *W_sf_f32,
+                                     void *stream) {
+  if (E <= 0 || n <= 0 || k <= 0 || n % 128 || k % 128 || !W_sf || !W_sf_f32)
+    return MOE_ERR_INVALID;
+  const size_t cnt = (size_t)E * (n / 128) * (k / 128);
+  weight_scales_f32_kernel<<<(unsigned)((cnt + 255) / 256), 256, 0, as_stream(stream)>>>(
+      W_sf, W_sf_f32, cnt);
+  return check_launch();
+}
+
 extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   if (!a) return MOE_ERR_INVALID;
   if (a->op != MOE_GEMM_GATEUP_SWIGLU && a->op != MOE_GEMM_DOWN) return MOE_ERR_INVALID;
   if (a->pair_tiles != 0 && a->pair_tiles != 1) return MOE_ERR_INVALID;
+  if (a->scale_fmt != 0 && a->scale_fmt != 1) return MOE_ERR_INVALID;
+  if (a->scale_fmt == 1 && a->pair_tiles) return MOE_ERR_UNSUPPORTED;
   if (a->n <= 0 || a->k <= 0 || a->rows <= 0 || a->max_tiles <= 0 || a->num_experts <= 0)
     return MOE_ERR_INVALID;
   if (a->n % 256 || a->k % 128 || a->rows % 128) return MOE_ERR_UNSUPPORTED;
@@ -1230,14 +1408,18 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.signal = a->signal;
   P.bm_signal = a->block_m_signal > 0 ? a->block_m_signal : BM;
   P.status = a->status;
+  P.scale_fmt = a->scale_fmt;
   static bool attr_set[kMaxDevices] = {};
   static int max_clusters[kMaxDevices] = {};
   const int dev = device_slot();
   if (dev < 0) return dev;
   if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
@@ -1256,6 +1438,9 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   }
   const int64_t max_units = a->tiles2 ? sms : a->max_tiles * (a->n / BN);
   const int grid = (int)(max_units < sms ? max_units : sms);
-  grouped_gemm_kernel<<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW, P);
+  if (a->scale_fmt)
+    grouped_gemm_kernel<true><<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW, P);
+  else
+    grouped_gemm_kernel<false><<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW, P);
   return check_launch();
 }

@@ -80,6 +80,7 @@ extern "C" {
 #define MOE_LAYOUT_MASKED 1
 #define MOE_FMT_FP8 0
 #define MOE_FMT_BF16 1
+#define MOE_FMT_FP8_F32 2 /* e4m3 with binary32 scales amax/448 per 1x128 block */
 #define MOE_GEMM_GATEUP_SWIGLU 0
 #define MOE_GEMM_DOWN 1
 
@@ -189,6 +190,10 @@ int moe_eplb_plan(const moe_eplb_cfg *cfg, const int64_t *load, int32_t *phys2lo
  *     e = smallest integer with amax <= 448*2^e (amax == 0 -> 0, clamped to
  *     [-127,127]), code = e4m3_rne_satfinite(x * 2^-e) — and copied to its K
  *     rows of A [rows][H]; the exponents go to A_sf as SF atoms.
+ *   FP8_F32: the same rows with binary32 scales ("Single Batch Overlap (SBO)" PR,
+ *     §3, 1d2d scaling with float scales): s = amax / 448 per 1x128 block (one IEEE
+ *     division; 1 when it is 0), code = e4m3_rne_satfinite(x / s) (IEEE division);
+ *     A_sf is float [rows][H/128] (A_shared_sf likewise).
  *   BF16: rows are copied unchanged (A is bf16 [rows][H], A_sf unused).
  *   log2phys [N_log][max_rep] / rep [N_log] (nullable, EPLB) map logical to
  *     physical experts: token t of e goes to log2phys[e][t % rep[e]], and a
@@ -309,6 +314,15 @@ typedef struct moe_gemm_args {
                         valid rows) or an M = 256 one with the second half idle; needs
                         k % 256 == 0 (else MOE_ERR_UNSUPPORTED).
                      Other values: MOE_ERR_INVALID.  Both give the same bytes. */
+  int scale_fmt;  /* 0: UE8M0 scales as SF atoms, applied by the tensor core (block
+                     scaling).  1: binary32 scales (1d2d with float scales, "Single Batch
+                     Overlap (SBO)" PR, §3): A_sf float [rows][k/128], W_sf float
+                     [E][n/128][k/128] (moe_weight_scales_f32), out_sf (GATEUP) float
+                     [rows][I/128] with h's scales amax/448 and codes e4m3(h / s); each
+                     128-deep k-block's product is formed unscaled and promoted by
+                     acc += (s_a * s_w) * partial in fp32, k-blocks in order.  Needs
+                     pair_tiles == 0 (else MOE_ERR_UNSUPPORTED).  Other values:
+                     MOE_ERR_INVALID. */
   int32_t *status;
 } moe_gemm_args;
 
@@ -321,9 +335,14 @@ int moe_grouped_gemm_fp8(const moe_gemm_args *args, void *stream);
  * the hot path.
  */
 size_t moe_packed_scale_bytes(int E, int n, int k);
-/* Bytes of the SF atoms of an activation tensor of `rows` rows and k columns
-   (rows and k multiples of 128; 0 otherwise): rows/128 * ceil(k/512) * 512. */
-size_t moe_scale_bytes(int64_t rows, int k);
+/* Weight scales for scale_fmt 1: UE8M0 bytes W_sf [E][n/128][k/128] -> float
+   2^(byte - 127), same shape (exact).  One-time setup, off the hot path. */
+int moe_weight_scales_f32(int E, int n, int k, const uint8_t *W_sf, float *W_sf_f32,
+                          void *stream);
+/* Bytes of the scales of an activation tensor of `rows` rows and k columns (rows and k
+   multiples of 128; 0 otherwise) in format fmt: MOE_FMT_FP8, SF atoms, rows/128 *
+   ceil(k/512) * 512; MOE_FMT_FP8_F32, float [rows][k/128], rows * k/128 * 4. */
+size_t moe_scale_bytes(int64_t rows, int k, int fmt);
 int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf, void *W_sf_packed,
                            void *stream);
 
@@ -419,6 +438,10 @@ typedef struct moe_layer {
      caller can time each stage of the chain. */
   void *const *events;
   int eplb_max_rep; /* columns of log2phys (0: 2) */
+  int scale_fmt;    /* 0: UE8M0 scales (W13_sf / W2_sf as SF atoms, A_sf / H1_sf as SF
+                       atoms); 1: binary32 scales (W13_sf / W2_sf float [E][n/128][k/128],
+                       A_sf / H1_sf float [rows][k/128]; both GEMMs on one CTA per tile,
+                       so gemm_pairs 1 is MOE_ERR_UNSUPPORTED) */
 } moe_layer;
 
 #define MOE_LAYER_EVENTS 6

@@ -147,16 +147,26 @@ def test_host_argument_checks_return_before_launch(L):
     assert L.moe_dispatch_rows(ctypes.byref(dc)) == 0
     dc = _lib.DispatchCfg(4, 128, 2, 8, 8, 1, 100, 0)             # cap % 128 != 0
     assert L.moe_dispatch(ctypes.byref(dc), *([None] * 14), 0, None, None) == -2
-    g = _lib.GemmArgs(0, 300, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, None)
+    g = _lib.GemmArgs(0, 300, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, 0,
+                      None)
     assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -2
-    g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, None)
+    g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, 0,
+                      None)
+    assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
+    g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 1, 1,
+                      None)                                     # binary32 scales: one CTA only
+    assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -2
+    g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, 2,
+                      None)                                     # no such scale format
     assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
     cc = _lib.CombineCfg(4, 100, 2, None, 0, 64, 0, 0, 0)          # H % 128 != 0
     assert L.moe_combine(ctypes.byref(cc), *([None] * 7)) == -2
     assert L.moe_packed_scale_bytes(2, 256, 384) == 2 * 2 * 1 * 512   # 3 blocks: one group
     assert L.moe_packed_scale_bytes(2, 256, 640) == 2 * 2 * 2 * 512   # 5 blocks: two groups
-    assert L.moe_scale_bytes(384, 7168) == 3 * 14 * 512
-    assert L.moe_scale_bytes(100, 7168) == 0 and L.moe_scale_bytes(128, 100) == 0
+    assert L.moe_scale_bytes(384, 7168, 0) == 3 * 14 * 512
+    assert L.moe_scale_bytes(384, 7168, 2) == 384 * 56 * 4           # binary32 scales
+    assert L.moe_scale_bytes(100, 7168, 0) == 0 and L.moe_scale_bytes(128, 100, 0) == 0
+    assert L.moe_scale_bytes(128, 128, 1) == 0                         # bf16 rows: none
     h = ctypes.c_void_p()
     lay = _lib.Layer()
     assert L.moe_layer_graph_create(None, None, None, None, ctypes.byref(h)) == -1
