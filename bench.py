@@ -12,8 +12,10 @@ host-buffer call (each step's x copied in from pinned host memory and its output
 back, the copies of neighbouring steps overlapping the layer on a copy stream; all copies
 inside the timed region).  Prints one JSON line (rank 0): the rates, the dominant
 kernel against its roofline (`roofline`), every stage against the measured and nominal
-peaks (`stages`), the step's expert balance, clocks, and the oracle's rate on a sample of
-the same workload (`cpu_baseline`).  Under
+peaks (`stages`), the step's expert balance, clocks, the oracle's rate on a sample of
+the same workload (`cpu_baseline`) and, at one GPU, the other workloads timed the same
+way after it (`workloads`: decode, SBO with and without the overlap, decode with
+binary32 scales, skew with and without EPLB, tiny).  Under
 torchrun each rank runs its own independent batch (weak scaling, no collective on the
 data path).
 """
@@ -260,6 +262,124 @@ def run_config(cfg, world):
                    f"steps (no flush)")}
 
 
+def measure(lay, st, K, warmup, dist=None, dev=None, sampler=None):
+    """The timed region: one CUDA graph of K layer passes (the decode serving form:
+    launches replayed, no host work per step), replayed once between CUDA events after
+    `warmup` passes.  Every EVERY-th pass records its stage events as graph nodes; their
+    averages give the per-kernel durations (an event node costs a few microseconds, so
+    not every pass has them).  Returns (max over ranks of the total ms, stage ms)."""
+    EVERY = 8
+    sampled = list(range(0, K, EVERY))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(_lib.LAYER_EVENTS)]
+           for _ in sampled]
+    for row in evs:                      # torch creates the CUDA event on first record
+        for e in row:
+            e.record(st)
+    torch.cuda.synchronize()
+    steps_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(steps_graph, stream=st):
+        for i in range(K):
+            lay.forward(stream=st, events=evs[i // EVERY] if i % EVERY == 0 else None)
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.2)
+    for _ in range(warmup):                         # the GPU idled while the sampler started
+        lay.forward(stream=st)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):                     # replay() launches on the current stream
+        t0.record(st)
+        steps_graph.replay()
+        t1.record(st)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
+    stage_ms = {s: float(np.mean([row[j].elapsed_time(row[j + 1]) for row in evs]))
+                for j, s in enumerate(STAGES)}
+    return ms_total, stage_ms
+
+
+def roofline(cfg, work, stage_ms, pk, mhz, sms):
+    """The dominant stage against its roofline: the tensor peak for a GEMM at (or within
+    a quarter of) the ridge, HBM otherwise, FFMA units for the router."""
+    # e4m3 = 2x bf16 (the nominal dense ratio 4.5 / 2.25 PFLOP/s); the burst figure, as
+    # each GEMM launch is timed alone (well under a second), the sustained one beside it
+    fp8_peak, fp8_peak_sus = 2.0 * pk["bf16"], 2.0 * pk["bf16_sus"]
+    dom = max((s for s in STAGES if work[s]["bytes"]), key=lambda s: stage_ms[s])
+    w = work[dom]
+    dur = stage_ms[dom] * 1e-3
+    t_hbm = w["bytes"] / (pk["hbm"] * 1e9)
+    t_tc = w["flops"] / (fp8_peak * 1e12) if dom != "route" else 0.0
+    if dom == "route":
+        roof = {"bound": "alu", "achieved": w["flops"] / dur / 1e12, "unit": "TFLOP/s",
+                "peak": sms * 128 * 2 * (mhz or 1900.0) * 1e6 / 1e12}  # FFMA units x clock
+    elif t_tc >= 0.75 * t_hbm:
+        roof = {"bound": "tensor", "achieved": w["flops"] / dur / 1e12, "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac_of_sustained": w["flops"] / dur / 1e12 / fp8_peak_sus}
+    else:
+        roof = {"bound": "hbm", "achieved": w["bytes"] / dur / 1e9, "peak": pk["hbm"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{pk['src']} ({'burst bf16 x2 for e4m3' if roof['bound'] == 'tensor' else 'hbm_gbs' if roof['bound'] == 'hbm' else 'FFMA units x clock'})"
+    return roof
+
+
+# Workloads timed after the headline one in the same run (at one GPU): the other named
+# configurations, the SBO workload run sequentially and the decode layer with binary32
+# scales; passes per workload.
+EXTRAS = (("decode", 100), ("sbo", 100), ("sbo_seq", 100), ("decode_f32", 100),
+          ("skew", 20), ("skew_eplb", 20), ("tiny", 100))
+
+
+def run_extra(name, steps, base_cfg, wdev, dev, pk, mhz, sms, rank):
+    """Times one more workload on the same box (its own inputs; the expert weights of
+    the headline workload when the shapes and seed agree).  -> summary dict."""
+    cfg = {**configs.NAMED, **configs.PROFILE, **configs.VARIANTS}[name]
+    cfg = cfg.with_(seed=cfg.seed + rank)
+    x = inputs.make_x(cfg)
+    W, bias = inputs.make_router(cfg)
+    same = (cfg.N, cfg.H, cfg.I, cfg.seed, cfg.shared) == (base_cfg.N, base_cfg.H, base_cfg.I,
+                                                           base_cfg.seed, base_cfg.shared)
+    wd = wdev if same else load_workload(cfg, dev)[5]
+    Wd = torch.from_numpy(W).to(dev)
+    bd = None if bias is None else torch.from_numpy(bias).to(dev)
+    xd = torch.from_numpy(x).view(torch.bfloat16).to(dev)
+    emap = None
+    if cfg.N_phys != cfg.N:
+        r = api.route(cfg, xd, Wd, bd)
+        emap = api.eplb_build_map(r["counts"].cpu().numpy(), cfg.N, cfg.N_phys)
+    lay = api.MoELayer(cfg, Wd, bd, wd, eplb_map=emap, device=dev)
+    lay.x.copy_(xd)
+    st = torch.cuda.Stream(device=dev)
+    st.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        lay.forward(stream=st)
+    torch.cuda.synchronize()
+    status = api.read_status(lay.status)
+    ms_total, stage_ms = measure(lay, st, steps, 3)
+    counts = lay.counts.cpu().numpy()
+    work = stage_work(cfg, counts) if emap is None else physical_work(cfg, counts, emap[2])
+    roof = roofline(cfg, work, stage_ms, pk, mhz, sms)
+    out = {"workload": describe(cfg), "ms_per_step": round(ms_total / steps, 5),
+           "tokens_per_s": round(cfg.B / (ms_total / steps * 1e-3), 1), "steps": steps,
+           "status": status,
+           "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+           "dominant": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()
+                        if k in ("kernel", "bound", "achieved", "peak", "unit", "frac")}}
+    if name.startswith("skew"):
+        out["expert_balance"] = expert_balance(counts)
+    del lay
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args, cfg):
     """--impl reference: the CPU oracle on the host cores, one sampled token per step.
 
@@ -327,6 +447,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=12,
                     help="tokens of the CPU-oracle baseline sample (0 = skip)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time only the chosen workload (not the others beside it)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = {**configs.NAMED, **configs.PROFILE, **configs.VARIANTS}[args.workload]
@@ -353,7 +475,6 @@ def main():
     lay = api.MoELayer(cfg, torch.from_numpy(W).to(dev),
                        None if bias is None else torch.from_numpy(bias).to(dev), wdev,
                        eplb_map=emap, device=dev)
-    del wdev                                          # the layer holds its own copy
     torch.cuda.empty_cache()
     lay.x.copy_(torch.from_numpy(x).view(torch.bfloat16).to(dev))
     st = torch.cuda.Stream(device=dev)              # graphs capture on a created stream
@@ -364,47 +485,12 @@ def main():
     if api.read_status(lay.status) != 0:
         raise RuntimeError(f"device status {api.read_status(lay.status)}")
 
-    # The timed region is one CUDA graph of K layer passes (the decode serving form:
-    # launches replayed, no host work per step).  Every EVERY-th pass records its
-    # stage events as graph nodes; their averages give the per-kernel durations of the
-    # roofline (an event node costs a few microseconds, so not every pass has them).
-    K = args.steps
-    EVERY = 8
-    sampled = list(range(0, K, EVERY))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(_lib.LAYER_EVENTS)]
-           for _ in sampled]
-    for row in evs:                      # torch creates the CUDA event on first record
-        for e in row:
-            e.record(st)
-    torch.cuda.synchronize()
-    steps_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(steps_graph, stream=st):
-        for i in range(K):
-            lay.forward(stream=st, events=evs[i // EVERY] if i % EVERY == 0 else None)
-    torch.cuda.synchronize()
     sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.2)
-    for _ in range(args.warmup):                    # the GPU idled while the sampler started
-        lay.forward(stream=st)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(st):                     # replay() launches on the current stream
-        t0.record(st)
-        steps_graph.replay()
-        t1.record(st)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
+    ms_total, stage_ms = measure(lay, st, args.steps, args.warmup, dist, dev, sampler)
     clocks = sampler.stop()
-    ms_total = max_over_ranks(t0.elapsed_time(t1), dist, dev)
+    K = args.steps
     ms_step = ms_total / K
     value = whole_job_rate(world, cfg.B, ms_step)
-    stage_ms = {s: float(np.mean([row[j].elapsed_time(row[j + 1]) for row in evs]))
-                for j, s in enumerate(STAGES)}
 
     # end to end through the library's pipelined host-buffer call: K steps, each copying
     # its batch in from pinned host memory and its output back, the copies of
@@ -436,34 +522,11 @@ def main():
     work = (stage_work(cfg, counts) if emap is None
             else physical_work(cfg, counts, emap[2]))
     pk = peaks()
-    # e4m3 = 2x bf16 (the nominal dense ratio 4.5 / 2.25 PFLOP/s); the burst figure, as
-    # each GEMM launch is timed alone (well under a second), the sustained one beside it
     fp8_peak = 2.0 * pk["bf16"]
-    fp8_peak_sus = 2.0 * pk["bf16_sus"]
-    dom = max((s for s in STAGES if work[s]["bytes"]), key=lambda s: stage_ms[s])
-    w = work[dom]
-    dur = stage_ms[dom] * 1e-3
-    t_hbm = w["bytes"] / (pk["hbm"] * 1e9)
-    t_tc = w["flops"] / (fp8_peak * 1e12) if dom not in ("route",) else 0.0
     sms = _lib.load().moe_num_sms()
-    if dom == "route":
-        roof = {"bound": "alu", "achieved": w["flops"] / dur / 1e12, "unit": "TFLOP/s"}
-    elif t_tc >= 0.75 * t_hbm:
-        # at (or within a quarter of) the ridge, the GEMM is held to the tensor peak
-        roof = {"bound": "tensor", "achieved": w["flops"] / dur / 1e12, "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac_of_sustained": w["flops"] / dur / 1e12 / fp8_peak_sus}
-    else:
-        roof = {"bound": "hbm", "achieved": w["bytes"] / dur / 1e9, "peak": pk["hbm"],
-                "unit": "GB/s"}
-    if roof["bound"] == "alu":
-        # fp32 FFMA: SMs x 128 lanes x 2 flop x median SM clock under load
-        mhz = clocks.get("sm_mhz") or 1900.0
-        roof["peak"] = sms * 128 * 2 * mhz * 1e6 / 1e12
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    tr = recorded_traffic(cfg.name, dom) if dom in ("gateup", "down") else None
-    roof["traffic"] = tr
-    roof["kernel"] = dom
-    roof["peak_source"] = f"{pk['src']} ({'burst bf16 x2 for e4m3' if roof['bound'] == 'tensor' else 'hbm_gbs' if roof['bound'] == 'hbm' else 'FFMA units x clock'})"
+    roof = roofline(cfg, work, stage_ms, pk, clocks.get("sm_mhz"), sms)
+    dom = roof["kernel"]
+    roof["traffic"] = recorded_traffic(cfg.name, dom) if dom in ("gateup", "down") else None
     per_stage = stage_summary(work, stage_ms, pk["hbm"], fp8_peak)
 
     # route (logits, select), dispatch (count + scan fused into one launch for a
@@ -485,6 +548,14 @@ def main():
                                 "kind": "oracle",
                                 "sample": f"{len(tok)} sampled tokens of {cfg.name} through the "
                                           f"whole layer ({dt:.1f} s)"}
+    if world == 1 and not args.no_extras:
+        # the other workloads, timed on the same box after the headline one (reported
+        # beside it; they do not enter value, ms_per_step or roofline)
+        del lay
+        torch.cuda.empty_cache()
+        line["workloads"] = {
+            name: run_extra(name, n, cfg, wdev, dev, pk, clocks.get("sm_mhz"), sms, rank)
+            for name, n in EXTRAS if name != args.workload}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
