@@ -14,8 +14,9 @@ inside the timed region).  Prints one JSON line (rank 0): the rates, the dominan
 kernel against its roofline (`roofline`), every stage against the measured and nominal
 peaks (`stages`), the step's expert balance, clocks, the oracle's rate on a sample of
 the same workload (`cpu_baseline`) and, at one GPU, the other workloads timed the same
-way after it (`workloads`: decode, SBO with and without the overlap, decode with
-binary32 scales, skew with and without EPLB, tiny).  Under
+way after it (`workloads`: prefill, decode and skew with the combine fused into the down
+GEMM, decode, SBO with and without the overlap, decode with binary32 scales, skew with
+and without EPLB, tiny).  Under
 torchrun each rank runs its own independent batch (weak scaling, no collective on the
 data path).
 """
@@ -110,7 +111,7 @@ def stage_work(cfg, counts: np.ndarray) -> dict:
     w13 = 2 * I * H + (2 * I // 128) * Hb          # codes + one UE8M0 byte per block
     w2 = H * I + Hb * Ib
     sh = 1 if cfg.shared else 0
-    return {
+    work = {
         "route": dict(bytes=B * H * 2 + N * H * 4 + B * K * 8, flops=2 * B * H * N, bound="alu"),
         "dispatch": dict(bytes=B * H * 2 + R * (H + Hb + 8) + sh * B * (H + Hb), flops=0,
                          bound="hbm"),
@@ -121,6 +122,10 @@ def stage_work(cfg, counts: np.ndarray) -> dict:
                      flops=2 * (R + sh * B) * I * H, bound="hbm"),
         "combine": dict(bytes=R * H * 2 + sh * B * H * 2 + R * 8 + B * H * 2, flops=0, bound="hbm"),
     }
+    if cfg.fuse_combine:    # the down GEMM does the combine's work too
+        work["down"]["bytes"] += work["combine"]["bytes"]
+        work["combine"] = dict(bytes=0, flops=0, bound="hbm")
+    return work
 
 
 # Nominal GB300 figures, the secondary denominators (the measured ones are primary):
@@ -331,10 +336,12 @@ def roofline(cfg, work, stage_ms, pk, mhz, sms):
 
 
 # Workloads timed after the headline one in the same run (at one GPU): the other named
-# configurations, the SBO workload run sequentially and the decode layer with binary32
-# scales; passes per workload.
-EXTRAS = (("decode", 100), ("sbo", 100), ("sbo_seq", 100), ("decode_f32", 100),
-          ("skew", 20), ("skew_eplb", 20), ("tiny", 100))
+# configurations, the combine fused into the down GEMM (prefill, decode, skew), the SBO
+# workload run sequentially and the decode layer with binary32 scales; passes per
+# workload.
+EXTRAS = (("prefill_fc", 20), ("decode", 100), ("decode_fc", 100), ("sbo", 100),
+          ("sbo_seq", 100), ("decode_f32", 100), ("skew", 20), ("skew_fc", 20),
+          ("skew_eplb", 20), ("tiny", 100))
 
 
 def run_extra(name, steps, base_cfg, wdev, dev, pk, mhz, sms, rank):

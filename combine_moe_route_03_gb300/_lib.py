@@ -42,6 +42,12 @@ class EplbCfg(ctypes.Structure):
                 ("n_nodes", _c_int), ("n_gpus", _c_int), ("max_rep", _c_int)]
 
 
+class FusedCombine(ctypes.Structure):
+    _fields_ = [("B", _c_int), ("K", _c_int), ("row_of", _vp), ("topk_w", _vp),
+                ("src_of", _vp), ("src_rows", _c_i64), ("pending", _vp),
+                ("shared_row0", _c_i64), ("out", _vp)]
+
+
 class GemmArgs(ctypes.Structure):
     _fields_ = [("op", _c_int), ("n", _c_int), ("k", _c_int), ("rows", _c_i64),
                 ("max_tiles", _c_i64), ("num_experts", _c_int), ("A", _vp), ("A_sf", _vp),
@@ -49,7 +55,7 @@ class GemmArgs(ctypes.Structure):
                 ("row_offset2", _c_i64), ("expert2", _c_int), ("out", _vp),
                 ("out_sf", _vp), ("signal", _vp), ("block_m_signal", _c_int),
                 ("num_sms", _c_int), ("pair_tiles", _c_int), ("scale_fmt", _c_int),
-                ("status", _vp)]
+                ("status", _vp), ("combine", ctypes.POINTER(FusedCombine))]
 
 
 class CombineCfg(ctypes.Structure):
@@ -70,7 +76,8 @@ class Layer(ctypes.Structure):
             "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",
             "dispatch_ws")] + [("route_ws_bytes", _c_sz), ("dispatch_ws_bytes", _c_sz),
                                ("status", _vp), ("stream2", _vp), ("events", _vp),
-                               ("eplb_max_rep", _c_int), ("scale_fmt", _c_int)]
+                               ("eplb_max_rep", _c_int), ("scale_fmt", _c_int),
+                               ("fuse_combine", _c_int), ("src_of", _vp), ("pending", _vp)]
 
 LAYER_EVENTS = 6
 STAGES = ("route", "dispatch", "gateup", "down", "combine")
@@ -92,6 +99,7 @@ SIGNATURES = {
     "moe_scale_bytes": (_c_sz, [_c_i64, _c_int, _c_int]),
     "moe_pack_weight_scales": (_c_int, [_c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "moe_weight_scales_f32": (_c_int, [_c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_fused_combine_prep": (_c_int, [ctypes.POINTER(FusedCombine), _c_int, _vp]),
     "moe_combine": (_c_int, [ctypes.POINTER(CombineCfg), _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_read_status": (_c_int, [_vp, _vp]),
     "moe_last_cuda_error": (_c_int, []),

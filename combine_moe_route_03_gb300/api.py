@@ -12,8 +12,8 @@ import torch
 
 from . import _lib
 from ._lib import (FMT_BF16, FMT_FP8, FMT_FP8_F32, GEMM_DOWN, GEMM_GATEUP_SWIGLU, SCALE_F32,
-                   SCALE_UE8M0, CombineCfg, DispatchCfg, EplbCfg, GemmArgs, Layer, RouteCfg, check,
-                   load, ptr, stream_ptr)
+                   SCALE_UE8M0, CombineCfg, DispatchCfg, EplbCfg, FusedCombine, GemmArgs, Layer,
+                   RouteCfg, check, load, ptr, stream_ptr)
 from .configs import MASKED, MoEConfig
 
 __all__ = ["route", "eplb_build_map", "eplb_plan", "check_eplb_map", "EplbRecorder", "dispatch", "dispatch_sizes", "pack_weight_scales",
@@ -260,9 +260,11 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
                      block_m_signal: int = 64, num_sms_: int = 0,
                      status: torch.Tensor | None = None, stream=None,
                      tiles2: torch.Tensor | None = None, row_offset2: int = 0, expert2: int = 0,
-                     pair_tiles: int = 0, scale_fmt: int = SCALE_UE8M0):
+                     pair_tiles: int = 0, scale_fmt: int = SCALE_UE8M0,
+                     combine: dict | None = None):
     """moe_grouped_gemm_fp8.  W e4m3 [E][n][k]; A e4m3 [rows][k]; scale_fmt SCALE_F32:
-    A_sf float [rows][k/128] and W_sf_atoms the float [E][n/128][k/128] scales."""
+    A_sf float [rows][k/128] and W_sf_atoms the float [E][n/128][k/128] scales.
+    combine (DOWN): the fused combine's tensors, as fused_combine_prep takes them."""
     E, n, k = W.shape
     rows = A.shape[0]
     dev = A.device
@@ -279,8 +281,32 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
                  ptr(phys2log), ptr(tiles), ptr(tiles2), row_offset2, expert2, ptr(out),
                  ptr(out_sf), ptr(signal), block_m_signal, num_sms_, pair_tiles, scale_fmt,
                  ptr(st))
+    if combine is not None:
+        fc = _fused_combine_args(**combine)
+        g.combine = ctypes.pointer(fc)
     check(load().moe_grouped_gemm_fp8(ctypes.byref(g), stream_ptr(stream)), "moe_grouped_gemm_fp8")
     return (out, out_sf) if op == GEMM_GATEUP_SWIGLU else out
+
+
+def _fused_combine_args(row_of, topk_w, src_of, pending, out, shared_row0: int = -1):
+    _expect(row_of, "row_of", (torch.int32,), (None, None))
+    B, K = row_of.shape
+    _expect(topk_w, "topk_w", (torch.float32,), (B, K))
+    _expect(src_of, "src_of", (torch.int32,), (None,))
+    _expect(out, "out", _BF16, (B, None))
+    _expect(pending, "pending", (torch.int32,), (B, out.shape[1] // 128))
+    return FusedCombine(B, K, ptr(row_of), ptr(topk_w), ptr(src_of), src_of.numel(),
+                        ptr(pending), shared_row0, ptr(out))
+
+
+def fused_combine_prep(row_of: torch.Tensor, topk_w: torch.Tensor, src_of: torch.Tensor,
+                       pending: torch.Tensor, out: torch.Tensor, shared_row0: int = -1,
+                       stream=None) -> None:
+    """moe_fused_combine_prep: the pending counts of a fused-combine DOWN GEMM (and
+    zeros in out for tokens without rows).  out bf16 [B][H], pending int32 [B][H/128]."""
+    fc = _fused_combine_args(row_of, topk_w, src_of, pending, out, shared_row0)
+    check(load().moe_fused_combine_prep(ctypes.byref(fc), out.shape[1], stream_ptr(stream)),
+          "moe_fused_combine_prep")
 
 
 def combine(Y: torch.Tensor, row_of: torch.Tensor, topk_w: torch.Tensor,
@@ -375,6 +401,8 @@ class MoELayer:
         self.Y = t(rows, H, dtype=torch.bfloat16)
         self.S = self.Y[self.rows:] if cfg.shared else None
         self.signal = t(rows // cfg.block_m_signal, dtype=torch.int32) if cfg.sbo else None
+        self.src_of = t(self.rows, dtype=torch.int32) if cfg.fuse_combine else None
+        self.pending = t(B, H // 128, dtype=torch.int32) if cfg.fuse_combine else None
         self.out = t(B, H, dtype=torch.bfloat16)
         rcfg = _route_cfg(cfg)
         self.route_ws = t(max(1, L.moe_route_workspace_size(ctypes.byref(rcfg))))
@@ -391,10 +419,11 @@ class MoELayer:
         lay.gemm_pairs = gemm_pairs
         lay.eplb_max_rep = 0 if self.log2phys is None else self.log2phys.shape[1]
         lay.scale_fmt = cfg.scale_fmt
+        lay.fuse_combine = int(cfg.fuse_combine)
         names = ["x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
                  "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",
                  "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",
-                 "dispatch_ws", "status"]
+                 "dispatch_ws", "status", "src_of", "pending"]
         for n in names:
             setattr(lay, n, ptr(getattr(self, n)))
         lay.route_ws_bytes = self.route_ws.numel()

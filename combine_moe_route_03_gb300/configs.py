@@ -57,6 +57,7 @@ class MoEConfig:
     zipf_tau: float = 0.05
     seed: int = 0
     scale_fmt: int = 0     # 0: UE8M0 power-of-two scales; 1: binary32 scales amax/448
+    fuse_combine: bool = False  # the down GEMM reduces Y into out (no combine launch)
 
     @property
     def N_phys(self) -> int:
@@ -112,5 +113,10 @@ SBO_SEQ = SBO.with_(name="sbo_seq", sbo=False)
 # The decode layer with binary32 activation scales (1d2d with float scales, promoted per
 # k-block in software) instead of power-of-two ones.
 DECODE_F32 = DECODE.with_(name="decode_f32", scale_fmt=1)
-VARIANTS = {c.name: c for c in (SBO_SEQ, DECODE_F32)}
+# The combine fused into the down GEMM (each (token, 128 columns) reduced by the warp
+# that stores its last row) instead of a separate pass over Y.
+PREFILL_FC = PREFILL.with_(name="prefill_fc", fuse_combine=True)
+SKEW_FC = SKEW.with_(name="skew_fc", fuse_combine=True)
+DECODE_FC = DECODE.with_(name="decode_fc", fuse_combine=True)
+VARIANTS = {c.name: c for c in (SBO_SEQ, DECODE_F32, PREFILL_FC, SKEW_FC, DECODE_FC)}
 ALL.update(VARIANTS)

@@ -123,6 +123,8 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   if (L->gemm_pairs == 1 && (rc.H % 256 || L->I % 256)) return MOE_ERR_UNSUPPORTED;
   if (L->scale_fmt != 0 && L->scale_fmt != 1) return MOE_ERR_INVALID;
   if (L->scale_fmt == 1 && L->gemm_pairs == 1) return MOE_ERR_UNSUPPORTED;
+  if (L->fuse_combine != 0 && L->fuse_combine != 1) return MOE_ERR_INVALID;
+  if (L->fuse_combine && (L->sbo || !L->src_of || !L->pending)) return MOE_ERR_INVALID;
   moe_dispatch_cfg dc;
   dc.B = rc.B;
   dc.H = rc.H;
@@ -146,13 +148,28 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   mark(1);
   uint8_t *A = static_cast<uint8_t *>(L->A), *A_sf = static_cast<uint8_t *>(L->A_sf);
   rc_ = moe_dispatch(&dc, L->x, L->topk_idx, L->log2phys, L->rep, A, A_sf, L->counts, L->row_of,
-                     nullptr, L->tiles, L->has_shared ? A + L->rows * rc.H : nullptr,
+                     L->fuse_combine ? L->src_of : nullptr, L->tiles,
+                     L->has_shared ? A + L->rows * rc.H : nullptr,
                      L->has_shared ? A_sf + (L->scale_fmt ? (size_t)L->rows * (rc.H / 128) * 4
                                                           : (size_t)L->rows * sf_groups(rc.H) * 4)
                                    : nullptr,
                      L->has_shared ? L->shared_tiles : nullptr, L->dispatch_ws,
                      L->dispatch_ws_bytes, L->status, stream);
   if (rc_) return rc_;
+  // the fused combine's counts, from the row_of just written
+  moe_fused_combine fc{};
+  if (L->fuse_combine) {
+    fc.B = rc.B;
+    fc.K = rc.K;
+    fc.row_of = L->row_of;
+    fc.topk_w = L->topk_w;
+    fc.src_of = L->src_of;
+    fc.src_rows = L->rows;
+    fc.pending = L->pending;
+    fc.shared_row0 = L->has_shared ? L->rows : -1;
+    fc.out = L->out;
+    if ((rc_ = moe_fused_combine_prep(&fc, rc.H, stream))) return rc_;
+  }
   mark(2);
   moe_gemm_args g{};
   g.op = MOE_GEMM_GATEUP_SWIGLU;
@@ -223,6 +240,13 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
     if ((rc_ = moe_combine(&cc, L->Y, L->row_of, L->topk_w, S, L->out, L->status, L->stream2)))
       return rc_;
     if ((rc_ = order_streams(st2, st, 1))) return rc_;
+    mark(5);
+    return MOE_OK;
+  }
+  if (L->fuse_combine) {  // the down GEMM reduces Y into out as it stores it
+    g.combine = &fc;
+    if ((rc_ = moe_grouped_gemm_fp8(&g, stream))) return rc_;
+    mark(4);
     mark(5);
     return MOE_OK;
   }

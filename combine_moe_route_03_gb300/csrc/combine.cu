@@ -96,8 +96,6 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
 }
 
 // Sum of one token's K rows (and its shared row) over 256-column chunks [c0, c1), in
-// the rank order k = 0..K-1 (the arithmetic of combine_kernel, bit for bit).
-// Sum of one token's K rows (and its shared row) over 256-column chunks [c0, c1), in
 // the rank order k = 0..K-1 (the arithmetic of combine_kernel, bit for bit), with all
 // K + 1 loads of a chunk in flight.  r[k] < 0: rank k left out.
 template <int KM>
@@ -220,10 +218,40 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_sbo_kernel(
   }
 }
 
+// Setup of the fused combine of the down GEMM (the reduce done where the rows are
+// stored): pending[t][c] = 2 x (the ranks of t with a row + its shared row) for every
+// 128-column chunk c (a full-width store of a row counts 2, a half-width one 1), and
+// out[t] = 0 for a token with no row at all, which no store would ever complete
+// (combine_kernel's empty sum).  One warp per token.
+__global__ void __launch_bounds__(256) fused_combine_prep_kernel(
+    const int32_t *__restrict__ row_of, int32_t *__restrict__ pending, uint16_t *__restrict__ out,
+    int B, int K, int nch, int n, int shared) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= B) return;
+  const bool has = lane < K && row_of[(size_t)t * K + lane] >= 0;
+  const int cnt = __popc(__ballot_sync(0xffffffffu, has)) + (shared ? 1 : 0);
+  for (int c = lane; c < nch; c += 32) pending[(size_t)t * nch + c] = 2 * cnt;
+  if (cnt == 0)
+    for (int h = 8 * lane; h < n; h += 256)
+      *reinterpret_cast<uint4 *>(out + (size_t)t * n + h) = make_uint4(0, 0, 0, 0);
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
+
+extern "C" int moe_fused_combine_prep(const moe_fused_combine *fc, int n, void *stream) {
+  if (!fc || fc->B < 0 || fc->K < 1 || n <= 0) return MOE_ERR_INVALID;
+  if (fc->K > 16 || n % 256) return MOE_ERR_UNSUPPORTED;
+  if (fc->B == 0) return MOE_OK;
+  if (!fc->row_of || !fc->pending || !fc->out || (uintptr_t)fc->out % 16) return MOE_ERR_INVALID;
+  fused_combine_prep_kernel<<<(unsigned)((fc->B + 7) / 8), 256, 0, as_stream(stream)>>>(
+      fc->row_of, fc->pending, static_cast<uint16_t *>(fc->out), fc->B, fc->K, n / 128, n,
+      fc->shared_row0 >= 0 ? 1 : 0);
+  return check_launch();
+}
 
 extern "C" int moe_combine(const moe_combine_cfg *c, const void *Y, const int32_t *row_of,
                            const float *topk_w, const void *shared, void *out, int32_t *status,

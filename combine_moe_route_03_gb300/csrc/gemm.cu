@@ -76,7 +76,15 @@ struct GemmParams {
   int bm_signal;
   int32_t *status;
   int scale_fmt;  // 0: UE8M0 SF atoms; 1: binary32 scales, promoted per k-block
+  // fused combine (DOWN; fc_B > 0 turns it on): see fused_combine_rows
+  int fc_B, fc_K, fc_nch;
+  const int32_t *fc_row_of, *fc_src_of;
+  const float *fc_w;
+  int32_t *fc_pending;
+  int64_t fc_src_rows, fc_shared_row0;
+  uint16_t *fc_out;
 };
+constexpr int kFusedKMax = 16;
 
 struct Unit {
   int row0;    // first A / out row of this CTA's tile
@@ -194,6 +202,101 @@ __device__ __forceinline__ void quantize_64(const uint32_t *v, float inv, uint4 
   }
 }
 
+// Fused combine ("DeepEP 完全拆解", §为什么 combine 比 dispatch 慢: the reduce of the
+// expert outputs, here done by the kernel that makes them).  This warp has stored rows
+// [wrow0, wrow0 + nrows) of Y in the 128-column chunk `chunk`: all 128 columns (weight
+// 2) or 64 of them (weight 1, the split of the M=128 pair epilogue).  Each lane counts
+// its row off the pending count of (its row's token, chunk), after a gpu-scope fence of
+// its own stores; a lane whose subtraction empties the count holds the token's last
+// missing piece, so every row of that chunk is in memory, and the warp reduces those
+// chunks, two at a time (a half-warp each, 8 columns per lane), reading the rows
+// through L2: fmas into fp32 in the rank order k = 0..K-1, then the shared row, then
+// bf16 -- the arithmetic of moe_combine, bit for bit.  Nothing waits.
+__device__ __forceinline__ void fused_combine_rows(const GemmParams &P, int64_t wrow0, int nrows,
+                                                   int chunk, int weight, int lane) {
+  __threadfence();
+  __syncwarp();
+  int t = -1;
+  bool last = false;
+  if (lane < nrows) {
+    const int64_t row = wrow0 + lane;
+    if (P.fc_shared_row0 >= 0 && row >= P.fc_shared_row0)
+      t = row - P.fc_shared_row0 < P.fc_B ? (int)(row - P.fc_shared_row0) : -1;
+    else if (row < P.fc_src_rows)
+      t = P.fc_src_of[row];
+    if (t >= 0 && t < P.fc_B)
+      last = atomicSub(P.fc_pending + (size_t)t * P.fc_nch + chunk, weight) == weight;
+  }
+  unsigned m = __ballot_sync(0xffffffffu, last);
+  if (m == 0) return;
+  __threadfence();  // the token's other rows were fenced before they were counted
+  const int hl = lane & 15;
+  const int col = 128 * chunk + 8 * hl;
+  const uint16_t *Y = reinterpret_cast<const uint16_t *>(P.out);
+  while (m) {
+    const int la = __ffs(m) - 1;
+    m &= m - 1;
+    int lb = la;
+    if (m) {
+      lb = __ffs(m) - 1;
+      m &= m - 1;
+    }
+    const int ta = __shfl_sync(0xffffffffu, t, la), tb = __shfl_sync(0xffffffffu, t, lb);
+    const int tt = lane < 16 ? ta : (lb != la ? tb : -1);
+    int my_r = -1;
+    float my_w = 0.0f;
+    if (tt >= 0 && hl < P.fc_K) {
+      my_r = P.fc_row_of[(size_t)tt * P.fc_K + hl];
+      my_w = P.fc_w[(size_t)tt * P.fc_K + hl];
+    }
+    int r[kFusedKMax];
+    float w[kFusedKMax];
+    uint4 y[kFusedKMax];
+#pragma unroll
+    for (int k = 0; k < kFusedKMax; ++k) {
+      r[k] = __shfl_sync(0xffffffffu, my_r, k, 16);
+      w[k] = __shfl_sync(0xffffffffu, my_w, k, 16);
+      if (k >= P.fc_K || (uint64_t)r[k] >= (uint64_t)P.rows) r[k] = -1;
+    }
+    if (tt < 0) continue;
+#pragma unroll
+    for (int k = 0; k < kFusedKMax; ++k)
+      y[k] = r[k] >= 0 ? __ldcg(reinterpret_cast<const uint4 *>(Y + (size_t)r[k] * P.n + col))
+                       : make_uint4(0, 0, 0, 0);
+    const bool use_s = P.fc_shared_row0 >= 0;
+    const uint4 sv =
+        use_s ? __ldcg(reinterpret_cast<const uint4 *>(Y + (size_t)(P.fc_shared_row0 + tt) * P.n + col))
+              : make_uint4(0, 0, 0, 0);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kFusedKMax; ++k) {
+      if (r[k] < 0) continue;
+      const uint32_t u[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fmaf_rn(w[k], __uint_as_float(u[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = __fmaf_rn(w[k], __uint_as_float(u[i] & 0xffff0000u), acc[2 * i + 1]);
+      }
+    }
+    if (use_s) {
+      const uint32_t u[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fadd_rn(acc[2 * i], __uint_as_float(u[i] << 16));
+        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __uint_as_float(u[i] & 0xffff0000u));
+      }
+    }
+    uint4 o;
+    o.x = f32_to_bf16_bits(acc[0]) | (f32_to_bf16_bits(acc[1]) << 16);
+    o.y = f32_to_bf16_bits(acc[2]) | (f32_to_bf16_bits(acc[3]) << 16);
+    o.z = f32_to_bf16_bits(acc[4]) | (f32_to_bf16_bits(acc[5]) << 16);
+    o.w = f32_to_bf16_bits(acc[6]) | (f32_to_bf16_bits(acc[7]) << 16);
+    __stcs(reinterpret_cast<uint4 *>(P.fc_out + (size_t)tt * P.n + col), o);
+  }
+}
+
 // Epilogue of one 128-row accumulator for this thread's half-row: TMEM ->
 // registers, release() (the MMAs may overwrite the accumulator from then on), then
 // SwiGLU + 1x128 requantisation (GATEUP) or bf16 rounding (DOWN), global stores and
@@ -254,6 +357,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &P, int row0, int
       for (int c = 0; c < 4; ++c)
         store_bf16_rows(stage, v + 32 * c, dst + 64 * c, (size_t)P.n * 2, nrows, lane);
     }
+    if (P.fc_B > 0) fused_combine_rows(P, wrow0, nrows, 2 * ni + half, 2, lane);
     if (P.signal) {
       __threadfence();
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
@@ -363,6 +467,7 @@ __device__ __forceinline__ bool epilogue_f32(const GemmParams &P, const Unit &U,
       for (int c = 0; c < 4; ++c)
         store_bf16_rows(stage, acc + 32 * c, dst + 64 * c, (size_t)P.n * 2, nrows, lane);
     }
+    if (P.fc_B > 0) fused_combine_rows(P, wrow0, nrows, 2 * U.ni + half, 2, lane);
     if (P.signal) {
       __threadfence();
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
@@ -716,8 +821,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // accumulator lanes it computes from its own TMEM lanes: a row's scale at its lane,
 // word (row % 64) / 32 of the A scale columns (M=128; row / 32 at M=256), and output
 // column c's weight scale at lane 32 * quarter + c % 32, word (c % 128) / 32 of the
-// B scale columns.  So the replicated 32-row atoms serve M=256 (two atoms for the two
-// 128-column halves); at M=128 the quarters holding columns [128,256) need the second
+// B scale columns.  So an atom copied with .32x128b.warpx4 (the same 32 lanes in all four
+// quarters) serves M=256 (two atoms for the two 128-column halves); at M=128 the quarters holding columns [128,256) need the second
 // weight atom in the same columns as the first: those units stage a 128-row image
 // (atom 0 in quarters 0-1, atom 1 in quarters 2-3) and copy it unreplicated.  The odd
 // CTA could only hold a tile's rows 64-127 at M=128 with their scales moved to words
@@ -887,6 +992,7 @@ __device__ __forceinline__ void epilogue_m128(const GemmParams &P, int row0, int
       for (int c = 0; c < 2; ++c)
         store_bf16_rows(stage, v + 32 * c, dst + 64 * c, (size_t)P.n * 2, nrows, lane);
     }
+    if (P.fc_B > 0) fused_combine_rows(P, wrow0, nrows, 2 * ni + (upper ? 1 : 0), 1, lane);
     if (P.signal) {
       __threadfence();
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
@@ -1373,6 +1479,14 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   if (!a->A || !a->A_sf || !a->W || !a->W_sf || !a->tiles || !a->out) return MOE_ERR_INVALID;
   if (a->op == MOE_GEMM_GATEUP_SWIGLU && (!a->out_sf || a->signal)) return MOE_ERR_INVALID;
   if (a->signal && (a->block_m_signal <= 0 || BM % a->block_m_signal)) return MOE_ERR_INVALID;
+  if (const moe_fused_combine *fc = a->combine) {
+    if (a->op != MOE_GEMM_DOWN || a->signal || fc->B <= 0 || fc->K < 1 ||
+        fc->K > kFusedKMax || !fc->row_of || !fc->topk_w || !fc->pending || !fc->out ||
+        (uintptr_t)fc->out % 16 || fc->src_rows < 0 || (fc->src_rows > 0 && !fc->src_of) ||
+        fc->shared_row0 < -1 ||
+        (fc->shared_row0 >= 0 && fc->shared_row0 + fc->B > a->rows))
+      return MOE_ERR_INVALID;
+  }
   const void *ptrs[] = {a->A, a->A_sf, a->W, a->W_sf, a->out, a->out_sf};
   for (const void *p : ptrs)
     if ((uintptr_t)p % 16) return MOE_ERR_INVALID;
@@ -1409,6 +1523,19 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.bm_signal = a->block_m_signal > 0 ? a->block_m_signal : BM;
   P.status = a->status;
   P.scale_fmt = a->scale_fmt;
+  P.fc_B = 0;
+  if (const moe_fused_combine *fc = a->combine) {
+    P.fc_B = fc->B;
+    P.fc_K = fc->K;
+    P.fc_nch = a->n / 128;
+    P.fc_row_of = fc->row_of;
+    P.fc_src_of = fc->src_of;
+    P.fc_w = fc->topk_w;
+    P.fc_pending = fc->pending;
+    P.fc_src_rows = fc->src_rows;
+    P.fc_shared_row0 = fc->shared_row0;
+    P.fc_out = static_cast<uint16_t *>(fc->out);
+  }
   static bool attr_set[kMaxDevices] = {};
   static int max_clusters[kMaxDevices] = {};
   const int dev = device_slot();

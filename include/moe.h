@@ -262,6 +262,43 @@ int moe_dispatch_noalloc(const moe_dispatch_cfg *cfg, const void *x, const int32
 
 /* ------------------------------------------------------------ grouped GEMM */
 /*
+ * Fused combine for the DOWN GEMM: the expert outputs are reduced back to token order
+ * inside the GEMM that makes them ("DeepEP 完全拆解", §为什么 combine 比 dispatch 慢:
+ * combine moves and reduces; here the reduce rides in the producing kernel instead of
+ * a separate pass over Y).  The result is that of moe_combine, bit for bit: the sum
+ * of a token's rows is still formed by one warp in the rank order k = 0..K-1, in fp32,
+ * then the shared row added, then rounded to bf16.  What changes is who forms it and
+ * when: every warp of the GEMM that stores rows of Y counts them off per (token,
+ * 128-column chunk) (an atomic subtraction on `pending`, after a gpu-scope fence of its
+ * stores), and the warp that brings a chunk's count to zero -- it stored the token's
+ * last row of that chunk -- reduces the chunk right away, reading the other rows
+ * through L2.  No warp waits for another.
+ *   row_of, topk_w [B][K]: as for moe_combine (row_of < 0: rank left out).
+ *   src_of [src_rows]: token of each routed row of Y (moe_dispatch's src_of).
+ *   pending int32 [B][n/128]: initialised by moe_fused_combine_prep before each GEMM.
+ *   shared_row0: row of Y holding token 0's shared-expert row (token t at
+ *     shared_row0 + t), or -1 without a shared expert.
+ *   out bf16 [B][n].
+ * Limits: 1 <= K <= 16.
+ */
+typedef struct moe_fused_combine {
+  int B, K;
+  const int32_t *row_of;
+  const float *topk_w;
+  const int32_t *src_of;
+  int64_t src_rows;
+  int32_t *pending;
+  int64_t shared_row0;
+  void *out;
+} moe_fused_combine;
+
+/* Sets pending[t][c] for the fused combine of an n-column DOWN GEMM (twice the rows the
+   token has in Y: its ranks with row_of >= 0, plus its shared row) and writes zeros to
+   out[t] for a token that has no row at all (moe_combine's result for it).  Enqueued on
+   `stream` after the dispatch that wrote row_of and before the GEMM. */
+int moe_fused_combine_prep(const moe_fused_combine *fc, int n, void *stream);
+
+/*
  * Grouped FP8 GEMM over the M tiles of a tile list (DeepGEMM's contiguous and
  * masked grouped GEMMs, "Large-scale EP ...", §DeepEP; FP8 1x128 x 128x128
  * "1d2d" scaling, "Single Batch Overlap (SBO)" PR, §3), on tcgen05 tensor
@@ -324,6 +361,9 @@ typedef struct moe_gemm_args {
                      pair_tiles == 0 (else MOE_ERR_UNSUPPORTED).  Other values:
                      MOE_ERR_INVALID. */
   int32_t *status;
+  const moe_fused_combine *combine; /* nullable; DOWN only, and not with signal (else
+                                       MOE_ERR_INVALID): reduce Y into combine->out as
+                                       the rows are stored (see moe_fused_combine) */
 } moe_gemm_args;
 
 int moe_grouped_gemm_fp8(const moe_gemm_args *args, void *stream);
@@ -442,6 +482,11 @@ typedef struct moe_layer {
                        atoms); 1: binary32 scales (W13_sf / W2_sf float [E][n/128][k/128],
                        A_sf / H1_sf float [rows][k/128]; both GEMMs on one CTA per tile,
                        so gemm_pairs 1 is MOE_ERR_UNSUPPORTED) */
+  int fuse_combine; /* 1: the down GEMM reduces Y into out itself (moe_fused_combine; the
+                       same bytes as the separate combine); needs src_of and pending, and
+                       sbo == 0 (else MOE_ERR_INVALID) */
+  int32_t *src_of;  /* fuse_combine: int32 [rows], the token of each routed row */
+  int32_t *pending; /* fuse_combine: int32 [B][H/128] */
 } moe_layer;
 
 #define MOE_LAYER_EVENTS 6

@@ -42,7 +42,8 @@ def test_header_compiles_as_plain_c(tmp_path):
 
 STRUCTS = {"RouteCfg": "moe_route_cfg", "DispatchCfg": "moe_dispatch_cfg",
            "EplbCfg": "moe_eplb_cfg", "GemmArgs": "moe_gemm_args",
-           "CombineCfg": "moe_combine_cfg", "Layer": "moe_layer"}
+           "CombineCfg": "moe_combine_cfg", "Layer": "moe_layer",
+           "FusedCombine": "moe_fused_combine"}
 
 
 def test_binding_structs_match_the_c_layout(tmp_path):
@@ -159,6 +160,29 @@ def test_host_argument_checks_return_before_launch(L):
     g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *([None] * 7), 0, 0, None, None, None, 64, 0, 0, 2,
                       None)                                     # no such scale format
     assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
+    p = [ctypes.c_void_p(16)] * 4
+    fc = _lib.FusedCombine(4, 2, 16, 16, 16, 128, 16, -1, 16)
+    g = _lib.GemmArgs(0, 256, 128, 128, 1, 1, *p, None, 16, None, 0, 0, 16, 16, None, 64, 0, 0,
+                      0, None, ctypes.pointer(fc))                # fused combine on gate/up
+    assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
+    for bad in (_lib.FusedCombine(4, 17, 16, 16, 16, 128, 16, -1, 16),     # K > 16
+                _lib.FusedCombine(4, 2, 16, 16, 16, 128, 16, -1, 8),       # out unaligned
+                _lib.FusedCombine(4, 2, 16, 16, None, 128, 16, -1, 16),    # no src_of
+                _lib.FusedCombine(4, 2, 16, 16, 16, 128, 16, 126, 16)):    # shared rows past rows
+        g = _lib.GemmArgs(1, 256, 128, 128, 1, 1, *p, None, 16, None, 0, 0, 16, None, None, 64,
+                          0, 0, 0, None, ctypes.pointer(bad))
+        assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
+    g = _lib.GemmArgs(1, 256, 128, 128, 1, 1, *p, None, 16, None, 0, 0, 16, None, 16, 64, 0, 0,
+                      0, None, ctypes.pointer(fc))                # with SBO signals
+    assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
+    assert L.moe_fused_combine_prep(None, 256, None) == -1
+    assert L.moe_fused_combine_prep(ctypes.byref(_lib.FusedCombine(4, 0, 16, 16, 16, 128, 16,
+                                                                   -1, 16)), 256, None) == -1
+    assert L.moe_fused_combine_prep(ctypes.byref(_lib.FusedCombine(4, 17, 16, 16, 16, 128, 16,
+                                                                   -1, 16)), 256, None) == -2
+    assert L.moe_fused_combine_prep(ctypes.byref(fc), 384, None) == -2      # n % 256
+    assert L.moe_fused_combine_prep(ctypes.byref(_lib.FusedCombine(0, 2, None, None, None, 0,
+                                                                   None, -1, None)), 256, None) == 0
     cc = _lib.CombineCfg(4, 100, 2, None, 0, 64, 0, 0, 0)          # H % 128 != 0
     assert L.moe_combine(ctypes.byref(cc), *([None] * 7)) == -2
     assert L.moe_packed_scale_bytes(2, 256, 384) == 2 * 2 * 1 * 512   # 3 blocks: one group
