@@ -858,7 +858,9 @@ extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W
   // the larger of the SM's shared-memory wavefronts (per warp 32 for W, about TT for x)
   // and the busiest sub-partition's fma cycles (ceil(NW/4) warps x TT x 32).  Other wide
   // grids: fp32-widened x and the largest per-thread tile that still leaves every SM
-  // one and a half CTAs; small grids: the bf16 kernel below.
+  // one and a half CTAs; small grids: the bf16 kernel below.  The token-sliced kernel
+  // stages 64-deep chunks in two buffers (a chunk's fmas outlast the next chunk's load),
+  // which halves its barriers and widening passes against 32-deep ones.
   int best_tt = 0, best_nw = 0;
   long best_cost = 0;
   if (N == 256)
@@ -874,10 +876,10 @@ extern "C" int moe_route(const moe_route_cfg *cfg, const void *x, const float *W
           best_cost = cost;
         }
       }
-  if (best_tt && (long)B * 4 >= 3L * 3 * 7 * sms) {  // at least ~3 tokens per warp
+  if (best_tt && H % 64 == 0 && (long)B * 4 >= 3L * 3 * 7 * sms) {  // ~3 tokens per warp
     switch (best_nw * 16 + best_tt) {
 #define MOE_PAIR_CASE(TT, NW) \
-  case NW * 16 + TT: rc = launch_logits_pair<TT, 8, 3, 32, NW>(xb, W, lg, B, H, st); break;
+  case NW * 16 + TT: rc = launch_logits_pair<TT, 8, 2, 64, NW>(xb, W, lg, B, H, st); break;
       MOE_PAIR_CASE(3, 7) MOE_PAIR_CASE(4, 7) MOE_PAIR_CASE(5, 7) MOE_PAIR_CASE(6, 7)
       MOE_PAIR_CASE(7, 8) MOE_PAIR_CASE(8, 8)
 #undef MOE_PAIR_CASE
