@@ -163,9 +163,9 @@ __device__ __forceinline__ int block_scan(int32_t *buf, int v) {
   return v + prefix;
 }
 
-// Work items of the 2-SM GEMM, in schedule order: an expert's tile pairs (one weight
-// tile shared by both SMs of a pair), then its odd last tile alone, all in one group,
-// so the single runs beside the pairs that read the same weight tiles.  Item k =
+// Work items of the 2-SM GEMM: an expert's tile pairs (one weight tile shared by both
+// SMs of a pair), then its odd last tile alone, all in one group, so the single runs
+// beside the pairs that read the same weight tiles (the groups' order: see the scan).  Item k =
 // {tile 0, tile 1 or -1, first item of its group, items in its group, 1 for a pair,
 // 0, 0, 0}; a group's units are N-tile-major.
 __device__ __forceinline__ void write_items(int32_t *items, int first, int nt, int item_first) {
@@ -224,17 +224,49 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     nt = (valid + 127) / 128;
   }
   const int first = block_scan(scan, nt) - nt;
-  const int np = nt / 2, ns = nt % 2;
-  const int pairs_incl = block_scan(scan, np);
-  const int singles_incl = block_scan(scan, ns);
-  const int item_first = block_scan(scan, np + ns) - (np + ns);
+  const int np = nt / 2, ns = nt % 2, gcnt = np + ns;
+  // Order of the item groups (the 2-SM GEMM's schedule): an expert with several items
+  // reads each weight tile from HBM once for all of them (the rest come from L2), one
+  // with a single item reads a weight tile from HBM per unit.  Spreading the multi-item
+  // experts evenly between the single-item ones, in expert order within each kind, keeps
+  // the HBM demand of the CTAs running side by side even.  Multi-item expert i of nm
+  // goes before single-item expert floor((2i + 1) * n1 / (2 nm)) of n1; experts without
+  // items take no place.  One scan gives both ranks (counts <= kScanThreads, 11 bits
+  // apart), a second one each position's first item.
+  const int multi = (p < N_phys && gcnt >= 2) ? 1 : 0;
+  const int single = (p < N_phys && gcnt == 1) ? 1 : 0;
+  const int kinds_incl = block_scan(scan, multi | (single << 11));
+  const int multi_rank = (kinds_incl & 2047) - multi;
+  const int single_rank = (kinds_incl >> 11) - single;
+  __shared__ int32_t kinds[2];
+  __shared__ int32_t by_pos[kScanThreads];
+  if (p == kScanThreads - 1) {
+    kinds[0] = kinds_incl & 2047;
+    kinds[1] = kinds_incl >> 11;
+  }
+  by_pos[p] = 0;
+  const int singles = __syncthreads_count(ns);  // also orders the writes above
+  const int nm = kinds[0], n1 = kinds[1];
+  int pos = -1;
+  if (multi) {  // (products < 2^22: ranks and counts are at most kScanThreads)
+    pos = (2 * multi_rank + 1) * n1 / (2 * nm) + multi_rank;
+  } else if (single) {  // after the multi-item experts whose slot is at most single_rank
+    const int q = n1 > 0 ? (2 * nm * (single_rank + 1) - 1) / n1 : 0;
+    pos = single_rank + min(nm, (q + 1) / 2);
+  }
+  if (pos >= 0) by_pos[pos] = gcnt;
+  __syncthreads();
+  const int at_pos = p < nm + n1 ? by_pos[p] : 0;
+  const int pos_incl = block_scan(scan, at_pos);  // items up to position p
+  by_pos[p] = pos_incl - at_pos;
   if (p == kScanThreads - 1) {
     totals[0] = first + nt;
-    totals[1] = pairs_incl;
-    totals[2] = singles_incl;
-    totals[3] = item_first + np + ns;
+    totals[1] = pos_incl - singles;  // pairs: items that are not singles
+    totals[2] = singles;
+    totals[3] = pos_incl;
   }
   __syncthreads();
+  const int item_first = pos >= 0 ? by_pos[pos] : 0;
   const int64_t max_tiles = rows_alloc / 128;
   if (p < N_phys) {
     const int seg = layout == MOE_LAYOUT_CONTIG ? first * 128 : p * cap;

@@ -88,6 +88,33 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def dispatch_items(ntiles):
+    """cluster_items in the group order moe_dispatch writes: the experts with two or
+    more items spread evenly between those with one (multi-item expert i of nm, in
+    expert order, goes before single-item expert floor((2i + 1) n1 / (2 nm)) of n1)."""
+    first = np.concatenate([[0], np.cumsum(ntiles)]).astype(int)
+    groups = {}
+    for e, n in enumerate(ntiles):
+        npair, gc = n // 2, n // 2 + n % 2
+        groups[e] = [[first[e] + 2 * j, first[e] + 2 * j + 1 if j < npair else -1, j < npair]
+                     for j in range(gc)]
+    multi = [e for e in range(len(ntiles)) if len(groups[e]) >= 2]
+    single = [e for e in range(len(ntiles)) if len(groups[e]) == 1]
+    nm, n1 = len(multi), len(single)
+    order, i = [], 0
+    for s, e in enumerate(single):
+        while i < nm and (2 * i + 1) * n1 // (2 * nm) <= s:
+            order.append(multi[i])
+            i += 1
+        order.append(e)
+    order += multi[i:]
+    items = []
+    for e in order:
+        f_item, gc = len(items), len(groups[e])
+        items += [[t0, t1, f_item, gc, 1 if pair else 0] for t0, t1, pair in groups[e]]
+    return items
+
+
 def cluster_items(ntiles):
     """Expected work items of a tile list for tile counts per expert (in expert order):
     an expert's pairs [t, t+1, group first, group size, 1], then its odd last tile

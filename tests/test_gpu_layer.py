@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from combine_moe_route_03_gb300 import api, configs, inputs
-from support import (bf16_dev, bits, cluster_items, device_weights, getter, host_experts,
+from support import (bf16_dev, bits, device_weights, dispatch_items, getter, host_experts,
                      host_workload, shared_of, to_dev, unpack_sf_atoms, within_tol)
 
 pytestmark = pytest.mark.gpu
@@ -115,7 +115,7 @@ def check_dispatch(cfg, x, idx, d, ref, fmt=api.FMT_FP8):
     assert nt == int(((cnt + 127) // 128).sum())
     ntp = (cnt + 127) // 128
     assert list(t[2:5]) == [int((ntp // 2).sum()), int((ntp % 2).sum()),
-                            len(cluster_items(list(ntp)))]
+                            len(dispatch_items(list(ntp)))]
     tl = t[8: 8 + 8 * nt].reshape(nt, 8)
     i = 0
     for p in range(cfg.N_phys):
@@ -124,7 +124,7 @@ def check_dispatch(cfg, x, idx, d, ref, fmt=api.FMT_FP8):
             assert list(tl[i]) == [base + 128 * j, p, min(128, cnt[p] - 128 * j),
                                    i - j, ntp[p], 0, 0, 0]
             i += 1
-    items = cluster_items(list(ntp))
+    items = dispatch_items(list(ntp))
     mt = d["max_tiles"]
     got = t[8 + 8 * mt: 8 + 8 * mt + 8 * len(items)].reshape(-1, 8)
     assert [list(r[:5]) for r in got] == items
