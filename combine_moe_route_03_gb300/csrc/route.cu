@@ -292,11 +292,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_logits_wide_kernel(
 // independent binary32 fmas (round to nearest even) in one instruction, so each one
 // advances two tokens' logits of one expert, each chain still in the sequential k order
 // (bit for bit the scalar kernel's results) while the multiply-add instructions halve.
-// A warp's TT tokens form TT/2 pairs plus, for odd TT, one token on scalar fmas.  The
-// widening pass writes each warp's x as its pairs, {x_2p(k), x_2p+1(k)} for k = 0, 1,
-// ..., then its odd token, so a broadcast 16-byte load yields two k steps of a pair (or
-// four of the odd token); W is staged and read as in the scalar kernel.  With 8 warps
-// the four SM sub-partitions carry equal work.
+// A warp's TT tokens form TT/2 pairs plus, for odd TT, one token on scalar fmas.  Each
+// warp widens its own tokens' x of a chunk as its pairs, {x_2p(k), x_2p+1(k)} for k = 0,
+// 1, ..., then its odd token, so a broadcast 16-byte load yields two k steps of a pair
+// (or four of the odd token), and only a warp sync separates that pass from the fmas:
+// one CTA barrier per chunk (chunk landed; the ring slot of chunk c-1 free).  W is
+// staged and read as in the scalar kernel.  With 8 warps the four SM sub-partitions
+// carry equal work.
 template <int TT, int TE, int S, int BK, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) route_logits_pair_kernel(
     const uint16_t *__restrict__ x, const float *__restrict__ W, float *__restrict__ logits,
@@ -355,11 +357,12 @@ __global__ void __launch_bounds__(NW * 32, 1) route_logits_pair_kernel(
   for (int c = 0; c < nchunks; ++c) {
     asm volatile("cp.async.wait_group %0;" ::"n"(S - 2) : "memory");
     __syncthreads();
-    {  // widen x: per warp its token pairs (interleaved), then its odd token
+    {  // widen x: each warp its own token pairs (interleaved), then its odd token
       const uint16_t *xb = xs + (c % S) * XST;
       constexpr int R = TP + TS;  // rows per warp
-      for (int i = tid; i < NW * R * (BK / 8); i += NT) {
-        const int w = i / (R * (BK / 8)), rr = (i / (BK / 8)) % R, k = (i % (BK / 8)) * 8;
+      const int w = warp;
+      for (int i = lane; i < R * (BK / 8); i += 32) {
+        const int rr = i / (BK / 8), k = (i % (BK / 8)) * 8;
         const int tw = w * TT + 2 * rr;  // first token of the row in the CTA
         const uint4 a = *reinterpret_cast<const uint4 *>(xb + tw * LDH + k);
         const uint32_t ua[4] = {a.x, a.y, a.z, a.w};
@@ -386,9 +389,9 @@ __global__ void __launch_bounds__(NW * 32, 1) route_logits_pair_kernel(
         }
       }
     }
+    __syncwarp();  // only this warp reads its widened rows
     if (c + S - 1 < nchunks) load(c + S - 1, (c + S - 1) % S);
     asm volatile("cp.async.commit_group;" ::: "memory");
-    __syncthreads();
     const float *wb = ws + (c % S) * WST + lane * LDF;
     const float *xw = xp + warp * XW;
     // operands of step k4 + 4 are loaded while step k4's fmas run
