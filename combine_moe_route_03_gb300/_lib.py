@@ -77,7 +77,8 @@ class Layer(ctypes.Structure):
             "dispatch_ws")] + [("route_ws_bytes", _c_sz), ("dispatch_ws_bytes", _c_sz),
                                ("status", _vp), ("stream2", _vp), ("events", _vp),
                                ("eplb_max_rep", _c_int), ("scale_fmt", _c_int),
-                               ("fuse_combine", _c_int), ("src_of", _vp), ("pending", _vp)]
+                               ("fuse_combine", _c_int), ("src_of", _vp), ("pending", _vp),
+                               ("W2_sf_t224", _vp)]
 
 LAYER_EVENTS = 6
 STAGES = ("route", "dispatch", "gateup", "down", "combine")
@@ -99,6 +100,8 @@ SIGNATURES = {
     "moe_scale_bytes": (_c_sz, [_c_i64, _c_int, _c_int]),
     "moe_pack_weight_scales": (_c_int, [_c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "moe_weight_scales_f32": (_c_int, [_c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_tiled_scale_bytes": (_c_sz, [_c_int, _c_int, _c_int, _c_int]),
+    "moe_pack_weight_scales_tiled": (_c_int, [_c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "moe_fused_combine_prep": (_c_int, [ctypes.POINTER(FusedCombine), _c_int, _vp]),
     "moe_combine": (_c_int, [ctypes.POINTER(CombineCfg), _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_read_status": (_c_int, [_vp, _vp]),

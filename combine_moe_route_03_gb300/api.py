@@ -253,6 +253,21 @@ def pack_weight_scales(W_sf: torch.Tensor, stream=None) -> torch.Tensor:
     return out
 
 
+def pack_weight_scales_tiled(W_sf: torch.Tensor, tile_n: int = 224, stream=None) -> torch.Tensor:
+    """UE8M0 bytes [E][n/128][k/128] (device) -> two 128-row images per tile_n-row weight
+    tile and group of four k-blocks, [E][n/tile_n][ceil(k/512)][2][512] (the DOWN GEMM's
+    scales with pair_tiles 2, tile_n 224)."""
+    E, nb, kb = W_sf.shape
+    L = load()
+    nbytes = L.moe_tiled_scale_bytes(E, nb * 128, kb * 128, tile_n)
+    if nbytes == 0:
+        raise ValueError(f"no {tile_n}-row tiles for n={nb * 128}")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=W_sf.device)
+    check(L.moe_pack_weight_scales_tiled(E, nb * 128, kb * 128, tile_n, ptr(W_sf), ptr(out),
+                                         stream_ptr(stream)), "moe_pack_weight_scales_tiled")
+    return out
+
+
 def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tensor,
                      W_sf_atoms: torch.Tensor, tiles: torch.Tensor, max_tiles: int,
                      out: torch.Tensor | None = None, out_sf: torch.Tensor | None = None,
@@ -346,7 +361,8 @@ class MoELayer:
 
     def __init__(self, cfg: MoEConfig, W_router: torch.Tensor, bias: torch.Tensor | None,
                  weights: dict, eplb_map=None, num_sms_: int = 0, combine_ctas: int = 0,
-                 timeout_ns: int = 1_000_000_000, device="cuda", gemm_pairs: int = 0):
+                 timeout_ns: int = 1_000_000_000, device="cuda", gemm_pairs: int = 0,
+                 down224: bool = False):
         self.cfg = cfg
         dev = torch.device(device)
         B, H, I, K = cfg.B, cfg.H, cfg.I, cfg.K
@@ -375,6 +391,9 @@ class MoELayer:
         else:                   # SF atoms for the tensor core's block scaling
             self.W13_sf = pack_weight_scales(W13_sf)
             self.W2_sf = pack_weight_scales(W2_sf)
+        # the down GEMM's scales for 224-column tiles (CTA pairs, two accumulators)
+        self.W2_sf_t224 = (pack_weight_scales_tiled(W2_sf, 224)
+                           if down224 and not cfg.scale_fmt and H % 224 == 0 else None)
         afmt = FMT_FP8_F32 if cfg.scale_fmt else FMT_FP8
         self.log2phys = self.rep = self.phys2log = None
         if eplb_map is not None:
@@ -423,7 +442,7 @@ class MoELayer:
         names = ["x", "W_router", "bias", "log2phys", "rep", "phys2log", "W13", "W13_sf", "W2",
                  "W2_sf", "topk_idx", "topk_w", "expert_counts", "counts", "row_of", "tiles",
                  "shared_tiles", "signal", "A", "A_sf", "H1", "H1_sf", "Y", "out", "route_ws",
-                 "dispatch_ws", "status", "src_of", "pending"]
+                 "dispatch_ws", "status", "src_of", "pending", "W2_sf_t224"]
         for n in names:
             setattr(lay, n, ptr(getattr(self, n)))
         lay.route_ws_bytes = self.route_ws.numel()

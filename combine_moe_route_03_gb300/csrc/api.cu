@@ -209,6 +209,11 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   g.A_sf = L->H1_sf;
   g.W = L->W2;
   g.W_sf = L->W2_sf;
+  // CTA pairs on 224-column tiles with two accumulators, when the layer has the scales
+  if (g.pair_tiles && L->W2_sf_t224 && !L->fuse_combine && !L->sbo && rc.H % 224 == 0) {
+    g.pair_tiles = 2;
+    g.W_sf = L->W2_sf_t224;
+  }
   g.out = L->Y;
   g.out_sf = nullptr;
   moe_combine_cfg cc{};

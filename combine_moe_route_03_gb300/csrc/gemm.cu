@@ -840,8 +840,8 @@ constexpr uint32_t O2_A = 0;
 constexpr uint32_t O2_B = O2_A + S2 * KB2 * A_BYTES;
 constexpr uint32_t O2_SFA = O2_B + S2 * KB2 * BH_BYTES;
 constexpr uint32_t O2_SFB = O2_SFA + S2 * SFA_BYTES;  // a group's atoms, in its first stage
-constexpr uint32_t O2_BAR = O2_SFB + S2 * SFB_BYTES;  // full, empty [S2]; acc full, empty
-constexpr uint32_t O2_MISC = O2_BAR + (2 * S2 + 2) * 8;
+constexpr uint32_t O2_BAR = O2_SFB + S2 * SFB_BYTES;  // full, empty [S2]; acc full, empty [2]
+constexpr uint32_t O2_MISC = O2_BAR + (2 * S2 + 4) * 8;
 constexpr uint32_t O2_AMAX = O2_MISC + 16;
 constexpr uint32_t O2_UNITQ = O2_AMAX + 2 * 128 * 4;
 constexpr uint32_t O2_UBAR = O2_UNITQ + kUnitQ * 32;
@@ -851,6 +851,12 @@ static_assert(XBUF_BYTES >= (kEpiThreads / 32) * STAGE_BYTES, "DOWN staging slot
 constexpr uint32_t SMEM2_BYTES = O2_XBUF + XBUF_BYTES + 1024;
 constexpr uint32_t TMEM_SF2 = 256;  // kSfSets rotating scale sets of 16 columns, as above
 static_assert(TMEM_SF2 + 16 * kSfSets <= TMEM_COLS, "TMEM columns");
+// The DOWN GEMM on 224-column tiles (H = 7168 = 32 x 224): two 224-column accumulators
+// and the scale sets fill TMEM exactly, so the MMAs of a unit run while the epilogue
+// drains the previous unit's accumulator.
+constexpr int BN224 = 224;
+constexpr uint32_t TMEM_SF224 = 2 * BN224;
+static_assert(TMEM_SF224 + 16 * kSfSets <= TMEM_COLS, "TMEM columns (224-column tiles)");
 static_assert(KB2 == 1 || KB2 == 2 || KB2 == 4, "a scale group (4 k-blocks) starts a stage");
 static_assert(SMEM2_BYTES <= 232448, "shared memory of the 2-SM kernel");
 
@@ -865,7 +871,9 @@ static_assert(sizeof(Unit2) <= 32, "unit ring slot");
 
 // Work unit -> the item's 2-SM unit.  Both CTAs decode alike: `rank` only selects which
 // tile fills row0 / nvalid / active.  U.ok is false when the entries do not describe
-// tiles inside the operands (every role then skips the unit).
+// tiles inside the operands (every role then skips the unit).  kW224: 224-column DOWN
+// tiles (112 weight rows per CTA), every single tile at M=256.
+template <bool kW224>
 __device__ __forceinline__ Unit2 get_2sm_unit(const GemmParams &P, int unit, int units2,
                                               int rank) {
   const int32_t *tl = P.tiles;
@@ -895,8 +903,9 @@ __device__ __forceinline__ Unit2 get_2sm_unit(const GemmParams &P, int unit, int
   U.we = second ? P.expert2 : (P.phys2log ? P.phys2log[e[1]] : e[1]);
   U.band = e[4];
   if (U.we < 0 || U.we >= P.num_experts) return U;
-  U.m128 = !pair && e[2] > 0 && e[2] <= 64;
-  uint32_t tx = 2 * KB2 * BH_BYTES, tx_sf = 0;  // both halves of the weight tile
+  U.m128 = !kW224 && !pair && e[2] > 0 && e[2] <= 64;
+  // both halves of the weight tile
+  uint32_t tx = 2 * KB2 * (kW224 ? (uint32_t)(BN224 / 2) * BK : BH_BYTES), tx_sf = 0;
   for (int c = 0; c < 2; ++c) {
     const int mi = tile[c];
     if (mi < 0) continue;
@@ -1005,6 +1014,34 @@ __device__ __forceinline__ void epilogue_m128(const GemmParams &P, int row0, int
   }
 }
 
+// Epilogue of a 224-column DOWN accumulator: this thread's lane row, columns [0,128)
+// (half 0) or [128,224) (half 1); TMEM -> registers, release(), bf16 rounding and
+// stores as in epilogue_tile.
+template <class Release>
+__device__ __forceinline__ void epilogue_down224(const GemmParams &P, int row0, int valid, int ni,
+                                                 uint32_t t_row, int half, int row_local,
+                                                 int lane, uint8_t *stage, Release release) {
+  uint32_t v[128];
+  const int pieces = half ? (BN224 - 128) / 32 : 4;  // 32-column pieces of this thread
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    if (c < pieces) MOE_TMEM_LD_32x32b_X32(t_row + 128 * half + 32 * c, (v + 32 * c));
+  tc_wait_ld();
+  tc_fence_before();
+  release();
+  const int64_t wrow0 = (int64_t)row0 + (row_local - lane);
+  const int nrows = (int)min((int64_t)min(valid - (row_local - lane), 32), P.rows - wrow0);
+  if (nrows > 0) {
+    uint8_t *dst = P.out + ((size_t)wrow0 * P.n + (size_t)ni * BN224 + 128 * half) * 2;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (c < pieces)
+        store_bf16_rows(stage, v + 32 * c, dst + 64 * c, (size_t)P.n * 2, nrows, lane);
+  }
+}
+
+// kW224: the DOWN GEMM on 224-column tiles with two accumulators (see BN224).
+template <bool kW224>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmA32,
@@ -1018,8 +1055,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t s_base = smem_u32(smem);
   const uint32_t bar_full = s_base + O2_BAR;          // [S2], used in the even CTA
   const uint32_t bar_empty = bar_full + 8 * S2;       // [S2]
-  const uint32_t bar_acc_full = bar_empty + 8 * S2;
-  const uint32_t bar_acc_empty = bar_acc_full + 8;    // used in the even CTA
+  const uint32_t bar_acc_full = bar_empty + 8 * S2;  // [2] (one buffer unless kW224)
+  const uint32_t bar_acc_empty = bar_acc_full + 16;  // [2], used in the even CTA
   const uint32_t bar_unit_full = s_base + O2_UBAR;
   const uint32_t bar_unit_empty = bar_unit_full + 8 * kUnitQ;
   Unit2 *unit_q = reinterpret_cast<Unit2 *>(smem + O2_UNITQ);
@@ -1034,8 +1071,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, 2 * (kEpiThreads / 32));  // epilogue warps of both CTAs
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_acc_full + 8 * b, 1);
+      mbar_init(bar_acc_empty + 8 * b, 2 * (kEpiThreads / 32));  // epilogue warps, both CTAs
+    }
     for (int q = 0; q < kUnitQ; ++q) {
       mbar_init(bar_unit_full + 8 * q, 1);
       mbar_init(bar_unit_empty + 8 * q, 2 + kEpiThreads / 32);
@@ -1101,14 +1140,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           wrow = we * P.n + (rank ? P.I : 0) + ni * 128;  // gate half / up half
           nb0 = ni;
           nb1 = P.I / 128 + ni;
+        } else if (kW224) {
+          wrow = we * P.n + ni * BN224 + (BN224 / 2) * rank;
+          nb0 = nb1 = 0;
         } else {
           wrow = we * P.n + ni * 256 + 128 * rank;
           nb0 = 2 * ni;
           nb1 = 2 * ni + 1;
         }
         const int sfa_atom = (U.row0 >> 7) * P.Kg;
-        const int sfb_atom0 = (we * (P.n / 128) + nb0) * P.Kg;
-        const int sfb_atom1 = (we * (P.n / 128) + nb1) * P.Kg;
+        // atom of group g: 128-row atoms [E][n/128][Kg], or for 224-column tiles the
+        // tile's two images [E][n/224][Kg][2]
+        const int sfb_tile = (we * P.n_tiles + ni) * P.Kg * 2;
+        const int sfb_atom0 = kW224 ? sfb_tile : (we * (P.n / 128) + nb0) * P.Kg;
+        const int sfb_atom1 = kW224 ? sfb_tile + 1 : (we * (P.n / 128) + nb1) * P.Kg;
+        const int sfb_step = kW224 ? 2 : 1;
         for (int kb = 0; kb < P.Kb; kb += KB2) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort, kWaitLimitNs)) {
             fail(P.status, abort);
@@ -1150,8 +1196,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 bulk_load(img + 1536, a1, 512, bar_full + 8 * stage);
               } else {
                 const uint32_t ssfb = s_base + O2_SFB + stage * SFB_BYTES;
-                tma_load_2d_pair(ssfb, &tmSFW, fb, 0, sfb_atom0 + g, pol_w);
-                tma_load_2d_pair(ssfb + 512, &tmSFW, fb, 0, sfb_atom1 + g, pol_w);
+                tma_load_2d_pair(ssfb, &tmSFW, fb, 0, sfb_atom0 + sfb_step * g, pol_w);
+                tma_load_2d_pair(ssfb + 512, &tmSFW, fb, 0, sfb_atom1 + sfb_step * g, pol_w);
               }
             }
           }
@@ -1186,9 +1232,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       // N = 256, UE8M0 scales, M = 256 (or 128) over the pair; bits 4-5 / 29-30 pick
       // the scale byte
-      const uint32_t idesc_n = ((uint32_t)(BN >> 3) << 17) | (1u << 23);
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      const uint32_t idesc_n = ((uint32_t)((kW224 ? BN224 : BN) >> 3) << 17) | (1u << 23);
+      const uint32_t tmem_sf = kW224 ? TMEM_SF224 : TMEM_SF2;
+      int stage = 0, nacc = 0;  // nacc: units accumulated so far (buffer nacc % 2 if kW224)
+      uint32_t phase = 0;
       bool ok = true;
       for (int seq = 0; ok; ++seq) {
         Unit2 U;
@@ -1200,7 +1247,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (U.end) break;
         if (!U.ok || rank != 0) continue;  // the odd CTA only follows the unit stream
         const uint32_t idesc_base = idesc_n | ((uint32_t)((U.m128 ? BM : 2 * BM) >> 4) << 24);
-        if (!mbar_wait_cluster(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
+        const int buf = kW224 ? nacc & 1 : 0;
+        const uint32_t acc_phase = (uint32_t)(kW224 ? nacc >> 1 : nacc) & 1u;
+        const uint32_t acc = tmem + (kW224 ? (uint32_t)(BN224 * buf) : 0u);
+        if (!mbar_wait_cluster(bar_acc_empty + 8 * buf, acc_phase ^ 1, abort, kWaitLimitNs)) {
           fail(P.status, abort);
           break;
         }
@@ -1220,7 +1270,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int h = 0; h < KB2; ++h) {
             const int kbh = kb + h;
-            const uint32_t t_sfa = tmem + TMEM_SF2 + 16 * ((kbh >> 2) % kSfSets);
+            const uint32_t t_sfa = tmem + tmem_sf + 16 * ((kbh >> 2) % kSfSets);
             const uint32_t t_sfb = t_sfa + 4;
             if ((kbh & 3) == 0) {  // the group's scale atoms, once per four k-blocks
               tc_cp_pair_32x128b_x4(t_sfa, smem_desc(ssfa, 16, 128, 0));
@@ -1238,7 +1288,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int j = 0; j < BK / 32; ++j) {
               const uint64_t ad = smem_desc(sa + h * A_BYTES + 32 * j, 16, 1024, 2);
               const uint64_t bd = smem_desc(sb + h * BH_BYTES + 32 * j, 16, 1024, 2);
-              tc_mma_pair_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | h | j) != 0);
+              tc_mma_pair_mxf8(acc, ad, bd, idesc, t_sfa, t_sfb, (kb | h | j) != 0);
             }
           }
           tc_commit_pair_mc(bar_empty + 8 * stage, kBoth);
@@ -1248,8 +1298,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit_pair_mc(bar_acc_full, kBoth);
-        acc_phase ^= 1;
+        tc_commit_pair_mc(bar_acc_full + 8 * buf, kBoth);
+        ++nacc;
       }
     }
   } else if (warp < 2 + kEpiThreads / 32) {
@@ -1263,11 +1313,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // the DOWN epilogue's staging slots share xbuf (the GATEUP M=128 exchange buffer)
     uint8_t *stage = smem + O2_XBUF + (warp - 2) * STAGE_BYTES;
     const uint32_t lead_acc_empty = mapa_shared(bar_acc_empty, 0);
+    int buf = 0, nacc = 0;  // as the MMA issuer: buffer nacc % 2 if kW224
     auto release_acc = [&] {
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(lead_acc_empty);
+      if (lane == 0) mbar_arrive_cluster(lead_acc_empty + 8 * buf);
     };
-    uint32_t acc_phase = 0;
     for (int seq = 0;; ++seq) {
       Unit2 U;
       if (!take(seq, U)) {
@@ -1278,22 +1328,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (lane == 0) release_unit(seq);
       if (U.end) break;
       if (!U.ok) continue;
-      if (!mbar_wait(bar_acc_full, acc_phase, abort, kWaitLimitNs)) {
+      buf = kW224 ? nacc & 1 : 0;
+      const uint32_t acc_phase = (uint32_t)(kW224 ? nacc >> 1 : nacc) & 1u;
+      ++nacc;
+      if (!mbar_wait(bar_acc_full + 8 * buf, acc_phase, abort, kWaitLimitNs)) {
         fail(P.status, abort);
         break;
       }
       tc_fence_after();
+      const uint32_t t_acc = t_row + (kW224 ? (uint32_t)(BN224 * buf) : 0u);
       if (!U.active) {  // this CTA's rows of the pair MMA carry no tile
         tc_fence_before();
         release_acc();
+      } else if (kW224) {
+        epilogue_down224(P, U.row0, U.nvalid, U.ni, t_acc, half, row_local, lane, stage,
+                         release_acc);
       } else if (U.m128) {
-        epilogue_m128(P, U.row0, U.nvalid, U.ni, t_row, q, half, warp, lane, amax_x, xbuf,
+        epilogue_m128(P, U.row0, U.nvalid, U.ni, t_acc, q, half, warp, lane, amax_x, xbuf,
                       stage, release_acc);
       } else {
-        epilogue_tile(P, U.row0, U.nvalid, U.ni, t_row, half, row_local, warp, lane, amax_x,
+        epilogue_tile(P, U.row0, U.nvalid, U.ni, t_acc, half, row_local, warp, lane, amax_x,
                       stage, release_acc);
       }
-      acc_phase ^= 1;
     }
   } else if (lane == 0) {
     // ------------------------------------------------------------ scheduler
@@ -1313,7 +1369,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool ok = true;
     // U.ok false: every role skips the unit, and the producer records it
     for (int unit = first_unit; ok && unit < total; unit += ustride)
-      ok = push(get_2sm_unit(P, unit, units2, rank));
+      ok = push(get_2sm_unit<kW224>(P, unit, units2, rank));
     if (ok) {
       Unit2 end = {};
       end.end = true;
@@ -1431,6 +1487,54 @@ extern "C" size_t moe_packed_scale_bytes(int E, int n, int k) {
   return (size_t)E * (n / 128) * sf_groups(k) * 512;
 }
 
+// Weight scale images of tile_n-row tiles (tile_n <= 256, a multiple of 16): per (expert,
+// tile, group of four k-blocks) two 128-row images, image h holding tile rows
+// [128h, 128h + 128) in the SF atom layout, each row with its own 128x128 block's scale
+// (rows past tile_n zero).  One 16-byte piece (four rows of one lane) per thread.
+__global__ void pack_scales_tiled_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ out,
+                                         size_t n_atoms, int n, int tile_n, int n_tiles, int Kb,
+                                         int Kg) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_atoms * 32) return;
+  const size_t a = i >> 5;
+  const int lane_row = (int)(i & 31), h = (int)(a & 1);
+  const int g = (int)((a >> 1) % Kg);
+  const size_t tile = (a >> 1) / Kg;
+  const size_t e = tile / n_tiles;
+  const int ni = (int)(tile % n_tiles);
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int tr = 128 * h + 32 * q + lane_row;
+    w[q] = 0;
+    if (tr < tile_n) {
+      const uint8_t *src = sf + (e * (n / 128) + (size_t)(ni * tile_n + tr) / 128) * Kb + 4 * g;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (4 * g + j < Kb) w[q] |= (uint32_t)src[j] << (8 * j);
+    }
+  }
+  reinterpret_cast<uint4 *>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+extern "C" size_t moe_tiled_scale_bytes(int E, int n, int k, int tile_n) {
+  if (E <= 0 || n <= 0 || k <= 0 || n % 128 || k % 128 || tile_n <= 128 || tile_n > 256 ||
+      tile_n % 16 || n % tile_n)
+    return 0;
+  return (size_t)E * (n / tile_n) * sf_groups(k) * 1024;
+}
+
+extern "C" int moe_pack_weight_scales_tiled(int E, int n, int k, int tile_n, const uint8_t *W_sf,
+                                            void *W_sf_tiled, void *stream) {
+  const size_t bytes = moe_tiled_scale_bytes(E, n, k, tile_n);
+  if (!bytes || !W_sf || !W_sf_tiled || (uintptr_t)W_sf_tiled % 16) return MOE_ERR_INVALID;
+  const size_t n_atoms = bytes / 512, pieces = n_atoms * 32;
+  pack_scales_tiled_kernel<<<(unsigned)((pieces + 255) / 256), 256, 0, as_stream(stream)>>>(
+      W_sf, static_cast<uint8_t *>(W_sf_tiled), n_atoms, n, tile_n, n / tile_n, k / 128,
+      sf_groups(k));
+  return check_launch();
+}
+
 extern "C" size_t moe_scale_bytes(int64_t rows, int k, int fmt) {
   if (rows <= 0 || k <= 0 || rows % 128 || k % 128) return 0;
   if (fmt == MOE_FMT_FP8_F32) return (size_t)rows * (k / 128) * 4;
@@ -1468,7 +1572,11 @@ extern "C" int moe_weight_scales_f32(int E, int n, int k, const uint8_t *W_sf, f
 extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   if (!a) return MOE_ERR_INVALID;
   if (a->op != MOE_GEMM_GATEUP_SWIGLU && a->op != MOE_GEMM_DOWN) return MOE_ERR_INVALID;
-  if (a->pair_tiles != 0 && a->pair_tiles != 1) return MOE_ERR_INVALID;
+  if (a->pair_tiles < 0 || a->pair_tiles > 2) return MOE_ERR_INVALID;
+  if (a->pair_tiles == 2) {  // 224-column DOWN tiles with two accumulators
+    if (a->op != MOE_GEMM_DOWN || a->signal || a->combine) return MOE_ERR_INVALID;
+    if (a->n % BN224) return MOE_ERR_UNSUPPORTED;
+  }
   if (a->scale_fmt != 0 && a->scale_fmt != 1) return MOE_ERR_INVALID;
   if (a->scale_fmt == 1 && a->pair_tiles) return MOE_ERR_UNSUPPORTED;
   if (a->n <= 0 || a->k <= 0 || a->rows <= 0 || a->max_tiles <= 0 || a->num_experts <= 0)
@@ -1493,7 +1601,8 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   CUtensorMap mA, mA32, mW;
   if (!make_map(&mA, a->A, (uint64_t)a->rows, (uint64_t)a->k) ||
       !make_map(&mA32, a->A, (uint64_t)a->rows, (uint64_t)a->k, 32) ||
-      !make_map(&mW, a->W, (uint64_t)a->num_experts * a->n, (uint64_t)a->k))
+      !make_map(&mW, a->W, (uint64_t)a->num_experts * a->n, (uint64_t)a->k,
+                a->pair_tiles == 2 ? BN224 / 2 : 128))
     return MOE_ERR_CUDA;
   if (a->tiles2 && (a->expert2 < 0 || a->expert2 >= a->num_experts || a->row_offset2 < 0 ||
                     a->row_offset2 % 128 || a->row_offset2 >= a->rows))
@@ -1511,7 +1620,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.k = a->k;
   P.Kb = a->k / BK;
   P.Kg = sf_groups(a->k);
-  P.n_tiles = a->n / BN;
+  P.n_tiles = a->n / (a->pair_tiles == 2 ? BN224 : BN);
   P.I = a->n / 2;
   P.A_sf = static_cast<const uint8_t *>(a->A_sf);
   P.W_sf = static_cast<const uint8_t *>(a->W_sf);
@@ -1537,7 +1646,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
     P.fc_out = static_cast<uint16_t *>(fc->out);
   }
   static bool attr_set[kMaxDevices] = {};
-  static int max_clusters[kMaxDevices] = {};
+  static int max_clusters[kMaxDevices] = {}, max_clusters224[kMaxDevices] = {};
   const int dev = device_slot();
   if (dev < 0) return dev;
   if (!attr_set[dev]) {
@@ -1548,7 +1657,10 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
       e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel,
+      e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
     if (e != cudaSuccess) return set_cuda_error(e);
     attr_set[dev] = true;
@@ -1557,10 +1669,17 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   if (a->pair_tiles) {
     CUtensorMap mSFA, mSFW;
     const uint64_t kg = (uint64_t)sf_groups(a->k);
+    // weight scales: 128-row atoms, or two images per 224-column tile
+    const uint64_t w_atoms = a->pair_tiles == 2
+                                 ? (uint64_t)a->num_experts * (a->n / BN224) * kg * 2
+                                 : (uint64_t)a->num_experts * (a->n / 128) * kg;
     if (!make_sf_map(&mSFA, a->A_sf, (uint64_t)(a->rows / 128) * kg, 1) ||
-        !make_sf_map(&mSFW, a->W_sf, (uint64_t)a->num_experts * (a->n / 128) * kg, 1))
+        !make_sf_map(&mSFW, a->W_sf, w_atoms, 1))
       return MOE_ERR_CUDA;
-    return launch_pairs(grouped_gemm_2sm_kernel, SMEM2_BYTES, sms, max_clusters[dev],
+    if (a->pair_tiles == 2)
+      return launch_pairs(grouped_gemm_2sm_kernel<true>, SMEM2_BYTES, sms, max_clusters224[dev],
+                          as_stream(stream), mA, mA32, mW, mSFA, mSFW, P);
+    return launch_pairs(grouped_gemm_2sm_kernel<false>, SMEM2_BYTES, sms, max_clusters[dev],
                         as_stream(stream), mA, mA32, mW, mSFA, mSFW, P);
   }
   const int64_t max_units = a->tiles2 ? sms : a->max_tiles * (a->n / BN);

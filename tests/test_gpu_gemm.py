@@ -182,8 +182,57 @@ def test_2sm_gemm_equals_single_cta(dev, op, pattern):
         assert np.array_equal(sfs[0][valid], sfs[1][valid])
 
 
+@pytest.mark.parametrize("pattern", sorted(NVALID))
+@pytest.mark.parametrize("k", [512, 2048])
+def test_down_224_column_tiles_equal_single_cta(dev, k, pattern):
+    """The DOWN GEMM on 224-column tiles with two accumulators (pair_tiles 2, every tile
+    at M=256, weight scales as tile-aligned images) gives the bytes of one CTA per tile
+    on 256-column tiles, for experts with 1, 2, 3 and 5 M tiles."""
+    tiles_per_expert = [1, 2, 3, 5, 2]
+    E, n = len(tiles_per_expert), 1792           # 8 tiles of 224, 7 of 256
+    mt = sum(tiles_per_expert)
+    q, sf = activations(128 * mt, k, 17)
+    W = np.stack([inputs.make_fp8_matrix(n, k, (19, 5, e))[0] for e in range(E)])
+    Wsf = np.random.default_rng(23).integers(117, 138, (E, n // 128, k // 128)).astype(np.uint8)
+    t = cluster_tile_list(tiles_per_expert, NVALID[pattern])
+    A, A_sf = torch.from_numpy(q).to(dev), torch.from_numpy(pack_sf_atoms(sf)).to(dev)
+    Wd, Wsf_d = torch.from_numpy(W).to(dev), torch.from_numpy(Wsf).to(dev)
+    tl = torch.from_numpy(t).to(dev)
+    outs = []
+    for pairs, scales in ((0, api.pack_weight_scales(Wsf_d)),
+                          (2, api.pack_weight_scales_tiled(Wsf_d, 224))):
+        st = api.new_status(dev)
+        outs.append(api.grouped_gemm_fp8(api.GEMM_DOWN, A, A_sf, Wd, scales, tl, mt, status=st,
+                                         pair_tiles=pairs))
+        torch.cuda.synchronize()
+        assert api.read_status(st) == 0
+    for i0 in range(mt):
+        nvalid = t[8 + 8 * i0 + 2]
+        assert torch.equal(outs[0][128 * i0: 128 * i0 + nvalid].view(torch.int16),
+                           outs[1][128 * i0: 128 * i0 + nvalid].view(torch.int16)), i0
+
+
+def test_tiled_weight_scale_images(dev):
+    """moe_pack_weight_scales_tiled: image h of tile j holds, for tile row 128h + r, the
+    scale of W row 224j + 128h + r (zero past the tile), in the SF atom layout."""
+    E, n, k = 2, 1792, 640
+    Wsf = np.random.default_rng(29).integers(0, 255, (E, n // 128, k // 128)).astype(np.uint8)
+    img = api.pack_weight_scales_tiled(torch.from_numpy(Wsf).to(dev), 224).cpu().numpy()
+    kg = (k // 128 + 3) // 4
+    nt = n // 224
+    img = img.reshape(E, nt, kg, 2, 512)
+    from support import unpack_sf_atoms
+    for e in range(E):
+        for j in range(nt):
+            got = np.concatenate([unpack_sf_atoms(img[e, j, :, h].reshape(-1), 128, k // 128)
+                                  for h in range(2)])          # [256][kb]
+            rows = 224 * j + np.arange(224)
+            assert np.array_equal(got[:224], Wsf[e, rows // 128])
+            assert not got[224:].any()
+
+
 @pytest.mark.parametrize("k", [768, 4352])
-@pytest.mark.parametrize("pairs", [0, 1])
+@pytest.mark.parametrize("pairs", [0, 1, 2])
 @pytest.mark.parametrize("last", [128, 50])
 def test_weight_scale_bytes_per_block(dev, pairs, k, last):
     """Weight scale bytes drawn per 128x128 block over 21 binades, K of 6 and 34
@@ -192,7 +241,7 @@ def test_weight_scale_bytes_per_block(dev, pairs, k, last):
     half moves an output by a power of two), with full last tiles and with 50-row last
     tiles (the 2-SM kernel's M=128 singles)."""
     tiles_per_expert = [2, 3, 1]
-    E, n = len(tiles_per_expert), 512
+    E, n = len(tiles_per_expert), 1792 if pairs == 2 else 512
     mt = sum(tiles_per_expert)
     rows = 128 * mt
     q, sf = activations(rows, k, 11)
@@ -211,7 +260,8 @@ def test_weight_scale_bytes_per_block(dev, pairs, k, last):
     out = api.grouped_gemm_fp8(api.GEMM_DOWN, torch.from_numpy(q).to(dev),
                                torch.from_numpy(pack_sf_atoms(sf)).to(dev),
                                torch.from_numpy(W).to(dev),
-                               api.pack_weight_scales(torch.from_numpy(Wsf).to(dev)),
+                               (api.pack_weight_scales_tiled if pairs == 2 else
+                                api.pack_weight_scales)(torch.from_numpy(Wsf).to(dev)),
                                torch.from_numpy(t).to(dev), mt, status=st, pair_tiles=pairs)
     torch.cuda.synchronize()
     assert api.read_status(st) == 0
