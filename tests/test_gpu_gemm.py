@@ -278,3 +278,32 @@ def test_weight_scale_bytes_per_block(dev, pairs, k, last):
             tol = np.abs(refb) * 2.0 ** -7 + 2e-6 * np.sqrt(k / 768) * np.abs(ref).max()
             assert np.all(np.abs(got[m] - refb) <= tol), (e, j)
         i += c
+
+
+def test_layer_down_224_column_tiles(dev):
+    """A layer on CTA pairs (B*K >= 128 N) whose hidden size is a multiple of 224: the
+    down GEMM on 224-column tiles gives the layer the same bytes as on 256-column tiles,
+    and the oracle's output for sampled tokens."""
+    from combine_moe_route_03_gb300 import configs
+    from support import bf16_dev, getter, shared_of, to_dev, within_tol
+    cfg = configs.MoEConfig("mid224", B=2300, H=1792, N=32, K=4, I=512, n_group=4, topk_group=2,
+                            score_fn=configs.SIGMOID, renorm=1, route_scale=2.5, shared=True,
+                            bias_init="normal")
+    x = inputs.make_x(cfg)
+    W, bias = inputs.make_router(cfg)
+    ex = inputs.make_all_experts(cfg)
+    s = inputs.make_shared_expert(cfg)
+    ex.update(W13s=s[0], W13s_sf=s[1], W2s=s[2], W2s_sf=s[3])
+    wdev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in ex.items()}
+    outs = []
+    for d224 in (False, True):
+        lay = api.MoELayer(cfg, to_dev(W, dev), to_dev(bias, dev), wdev, device=dev, down224=d224)
+        assert (lay.W2_sf_t224 is not None) == d224
+        outs.append(bits(lay.forward(bf16_dev(x, dev))))
+        torch.cuda.synchronize()
+        assert api.read_status(lay.status) == 0
+    assert np.array_equal(outs[0], outs[1])
+    tok = np.array([0, 1, 777, 1500, cfg.B - 1])
+    ref = oracle.layer_tokens(cfg, x, W, bias, getter(ex), shared_of(ex), tokens=tok)
+    ok, err, bound = within_tol(oracle.bf16_to_f32(outs[1][tok]), oracle.bf16_to_f32(ref["out"]))
+    assert ok, (err, bound)
