@@ -168,17 +168,18 @@ __device__ __forceinline__ int block_scan(int32_t *buf, int v) {
 // beside the pairs that read the same weight tiles (the groups' order: see the scan).  Item k =
 // {tile 0, tile 1 or -1, first item of its group, items in its group, 1 for a pair,
 // 0, 0, 0}; a group's units are N-tile-major.
+// An 8-int tile-list entry as two 16-byte stores (the list is 16-byte aligned).
+__device__ __forceinline__ void put8(int32_t *dst, int a, int b, int c, int d, int e) {
+  reinterpret_cast<int4 *>(dst)[0] = make_int4(a, b, c, d);
+  reinterpret_cast<int4 *>(dst)[1] = make_int4(e, 0, 0, 0);
+}
+
 __device__ __forceinline__ void write_items(int32_t *items, int first, int nt, int item_first) {
   const int np = nt / 2, gc = np + nt % 2;
   for (int j = 0; j < gc; ++j) {
-    int32_t *it = items + 8 * (size_t)(item_first + j);
     const bool pair = j < np;
-    it[0] = first + 2 * j;
-    it[1] = pair ? first + 2 * j + 1 : -1;
-    it[2] = item_first;
-    it[3] = gc;
-    it[4] = pair ? 1 : 0;
-    it[5] = it[6] = it[7] = 0;
+    put8(items + 8 * (size_t)(item_first + j), first + 2 * j, pair ? first + 2 * j + 1 : -1,
+         item_first, gc, pair ? 1 : 0);
   }
 }
 
@@ -271,15 +272,9 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
   if (p < N_phys) {
     const int seg = layout == MOE_LAYOUT_CONTIG ? first * 128 : p * cap;
     ws.seg[p] = seg;
-    for (int i = 0; i < nt; ++i) {
-      int32_t *tl = tiles + 8 + 8 * (size_t)(first + i);
-      tl[0] = seg + 128 * i;
-      tl[1] = p;
-      tl[2] = min(128, valid - 128 * i);
-      tl[3] = first;
-      tl[4] = nt;
-      tl[5] = tl[6] = tl[7] = 0;
-    }
+    for (int i = 0; i < nt; ++i)
+      put8(tiles + 8 + 8 * (size_t)(first + i), seg + 128 * i, p, min(128, valid - 128 * i),
+           first, nt);
     write_items(tiles + 8 + 8 * max_tiles, first, nt, item_first);
     pad_seg[p] = seg;  // rows [valid, end) of this expert's segment that no token fills
     pad_from[p] = valid;
@@ -317,24 +312,12 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     // items: snt / 2 pairs, then the odd last tile alone, all in one group
     const int snp = snt / 2, sgc = snp + snt % 2;
     for (int j = p; j < sgc; j += kScanThreads) {
-      int32_t *it = shared_tiles + 8 + 8 * (size_t)snt + 8 * (size_t)j;
       const bool pair = j < snp;
-      it[0] = 2 * j;
-      it[1] = pair ? 2 * j + 1 : -1;
-      it[2] = 0;
-      it[3] = sgc;
-      it[4] = pair ? 1 : 0;
-      it[5] = it[6] = it[7] = 0;
+      put8(shared_tiles + 8 + 8 * (size_t)snt + 8 * (size_t)j, 2 * j, pair ? 2 * j + 1 : -1, 0,
+           sgc, pair ? 1 : 0);
     }
-    for (int i = p; i < snt; i += kScanThreads) {
-      int32_t *tl = shared_tiles + 8 + 8 * (size_t)i;
-      tl[0] = 128 * i;
-      tl[1] = 0;
-      tl[2] = min(128, B - 128 * i);
-      tl[3] = 0;
-      tl[4] = snt;
-      tl[5] = tl[6] = tl[7] = 0;
-    }
+    for (int i = p; i < snt; i += kScanThreads)
+      put8(shared_tiles + 8 + 8 * (size_t)i, 128 * i, 0, min(128, B - 128 * i), 0, snt);
   }
 }
 
@@ -592,7 +575,8 @@ extern "C" int moe_dispatch(const moe_dispatch_cfg *c, const void *x, const int3
   if (A_shared && (c->fmt == MOE_FMT_BF16 || !A_shared_sf)) return MOE_ERR_INVALID;
   if (workspace_bytes < moe_dispatch_workspace_size(c)) return MOE_ERR_INVALID;
   if ((uintptr_t)x % 16 || (uintptr_t)A % 16 || (A_sf && (uintptr_t)A_sf % 16) ||
-      (A_shared && (uintptr_t)A_shared % 16))
+      (A_shared && (uintptr_t)A_shared % 16) || (uintptr_t)tiles % 16 ||
+      (shared_tiles && (uintptr_t)shared_tiles % 16))
     return MOE_ERR_INVALID;
   const int nchunks = (B + kChunk - 1) / kChunk;
   DispatchWs ws = carve(workspace, B, K, Np);
@@ -659,7 +643,8 @@ extern "C" int moe_dispatch_noalloc(const moe_dispatch_cfg *c, const void *x,
   if ((log2phys == nullptr) != (rep == nullptr)) return MOE_ERR_INVALID;
   if (A_shared && (c->fmt == MOE_FMT_BF16 || !A_shared_sf)) return MOE_ERR_INVALID;
   if ((uintptr_t)x % 16 || (uintptr_t)A % 16 || (A_sf && (uintptr_t)A_sf % 16) ||
-      (A_shared && (uintptr_t)A_shared % 16))
+      (A_shared && (uintptr_t)A_shared % 16) || (uintptr_t)tiles % 16 ||
+      (shared_tiles && (uintptr_t)shared_tiles % 16))
     return MOE_ERR_INVALID;
   void *scratch = nullptr;
   if ((rc = scratch_address(&scratch))) return rc;

@@ -211,7 +211,8 @@ int moe_eplb_plan(const moe_eplb_cfg *cfg, const int64_t *load, int32_t *phys2lo
  *     (one expert, id 0) for a shared expert.
  *   status: device int32, MOE_STATUS_* bits OR-ed in.
  * Limits: H % 128 == 0, K <= 16, N_phys <= 1024, rows as returned by
- * moe_dispatch_rows().
+ * moe_dispatch_rows(); x, A, A_sf, A_shared, tiles and shared_tiles 16-byte aligned
+ * (else MOE_ERR_INVALID).
  */
 typedef struct moe_dispatch_cfg {
   int B, H, K;
