@@ -75,13 +75,25 @@ __device__ __forceinline__ void count_chunk(int chunk, const int32_t *__restrict
   const int per = (npairs + kCountWarps - 1) / kCountWarps;
   const int w_begin = warp * per, w_end = min(npairs, w_begin + per);
   const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = w_begin; base < w_end; base += 32) {
+  // the warp's expert ids, loaded together (up to 4 per lane) before the ranking rounds
+  constexpr int kPre = 4;
+  int pre[kPre];
+#pragma unroll
+  for (int r = 0; r < kPre; ++r) {
+    const int i = w_begin + 32 * r + lane;
+    pre[r] = i < w_end ? topk_idx[(size_t)t_begin * K + i] : 0;
+  }
+  for (int base = w_begin, round = 0; base < w_end; base += 32, ++round) {
     const int i = base + lane;
     const bool valid = i < w_end;
     int p = -1;
     if (valid) {
       const int t = t_begin + i / K;
-      const int e = topk_idx[(size_t)t_begin * K + i];
+      int e = 0;
+#pragma unroll
+      for (int r = 0; r < kPre; ++r)
+        if (round == r) e = pre[r];
+      if (round >= kPre) e = topk_idx[(size_t)t_begin * K + i];
       if (e < 0 || e >= N_log) {
         status_or(status, MOE_STATUS_BAD_INDEX);
       } else if (log2phys) {
