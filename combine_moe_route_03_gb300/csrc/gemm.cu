@@ -788,7 +788,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       return true;
     };
     bool ok = true;
-    for (int unit = blockIdx.x; ok && unit < total; unit += gridDim.x) ok = push(get_unit(P, unit, units2));
+    // Equal rounds: the units are spread over just enough CTAs that every CTA runs the
+    // same number of them (the rest run none), so the last round keeps as many CTAs
+    // streaming weights as the others (an HBM-bound launch otherwise ends on a partial
+    // round that cannot fill the memory system).
+    const int rounds = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int ctas = rounds > 0 ? (total + rounds - 1) / rounds : 0;
+    for (int unit = blockIdx.x; ok && unit < total && (int)blockIdx.x < ctas; unit += ctas)
+      ok = push(get_unit(P, unit, units2));
     if (ok) {
       Unit end = {};
       end.end = true;
