@@ -1374,8 +1374,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       return true;
     };
     bool ok = true;
-    // U.ok false: every role skips the unit, and the producer records it
-    for (int unit = first_unit; ok && unit < total; unit += ustride)
+    // U.ok false: every role skips the unit, and the producer records it.  Equal rounds
+    // over just enough CTA pairs, as in the one-CTA kernel.
+    const int rounds = (total + ustride - 1) / ustride;
+    const int pairs = rounds > 0 ? (total + rounds - 1) / rounds : 0;
+    for (int unit = first_unit; ok && unit < total && first_unit < pairs; unit += pairs)
       ok = push(get_2sm_unit<kW224>(P, unit, units2, rank));
     if (ok) {
       Unit2 end = {};
