@@ -12,9 +12,12 @@
 // fp32 accumulator stays in tensor memory for the whole K loop.
 //
 // Two kernels over the same tile list, both persistent with 11 warps per CTA:
-//   grouped_gemm_kernel (one CTA per M tile, 128x256 MMAs) and grouped_gemm_2sm_kernel
+//   grouped_gemm_kernel (one CTA per M tile, 128x256 MMAs; with binary32 scales the
+//   k-blocks' partial products are promoted in the epilogue) and grouped_gemm_2sm_kernel
 //   (CTA pairs on one TPC: an expert's tile pairs as M=256 cta_group::2 MMAs, its odd
-//   last tile as an M=128 or M=256 pair MMA in the same launch).
+//   last tile as an M=128 or M=256 pair MMA in the same launch; for DOWN optionally on
+//   224-column tiles with two accumulators).  The DOWN epilogue can also reduce the
+//   stored rows into token order (the fused combine).
 //   warp 0  TMA producer: A tile 128x128 e4m3, B tile 256x128 e4m3 (two 128-row
 //           boxes: gate and up halves for GATEUP, two output blocks for DOWN),
 //           and the matching scale atoms, a ring of stages.
