@@ -12,6 +12,10 @@
 // tiles (acquire load of the row block's counter reaching the threshold).  The
 // consumer's wait is bounded by one wall-clock limit for the whole launch; rows that
 // are not ready by then are skipped and MOE_STATUS_TIMEOUT is raised.
+//
+// The combine can also run inside the down GEMM (moe_gemm_args.combine); the setup it
+// needs, each (token, 128-column chunk)'s count of rows still to arrive, is written by
+// moe_fused_combine_prep here.
 #include "common.cuh"
 
 namespace moe {
