@@ -472,10 +472,11 @@ typedef struct moe_layer {
   int combine_ctas; /* sbo: CTAs of the combine consumer, taken from num_sms for the down
                        GEMM while they run beside it (0: 32; at least one SM must stay
                        for the GEMM, else MOE_ERR_INVALID) */
-  int gemm_pairs; /* pair_tiles of both GEMMs.  0: 1 when B*K >= 128*N_phys and H and I
-                     are multiples of 256, else 0; 1: always 1 (MOE_ERR_UNSUPPORTED
-                     unless H and I are multiples of 256); -1: always 0; other values:
-                     MOE_ERR_INVALID */
+  int gemm_pairs; /* CTA pairs (pair_tiles 1) for the GEMMs.  0: the gate/up GEMM on
+                     pairs when B*K >= 256*N_phys (two M tiles per expert on average) and
+                     H and I are multiples of 256, the down GEMM on one CTA per tile; 1:
+                     both GEMMs on pairs (MOE_ERR_UNSUPPORTED unless H and I are multiples
+                     of 256); -1: both on one CTA per tile; other values: MOE_ERR_INVALID */
   /* inputs and weights */
   void *x;                                         /* bf16 [B][H] */
   const float *W_router, *bias;                    /* [N][H], [N] or NULL */
@@ -507,8 +508,9 @@ typedef struct moe_layer {
   int32_t *src_of;  /* fuse_combine: int32 [rows], the token of each routed row */
   int32_t *pending; /* fuse_combine: int32 [B][H/128] */
   const void *W2_sf_t224; /* nullable: W2's scales as moe_pack_weight_scales_tiled images
-                             (tile_n 224); with them a down GEMM on CTA pairs runs on
-                             224-column tiles (pair_tiles 2), unless fuse_combine */
+                             (tile_n 224); with them a down GEMM on CTA pairs (gemm_pairs
+                             1) runs on 224-column tiles (pair_tiles 2), unless
+                             fuse_combine or sbo */
 } moe_layer;
 
 #define MOE_LAYER_EVENTS 6

@@ -281,7 +281,7 @@ def test_weight_scale_bytes_per_block(dev, pairs, k, last):
 
 
 def test_layer_down_224_column_tiles(dev):
-    """A layer on CTA pairs (B*K >= 128 N) whose hidden size is a multiple of 224: the
+    """A layer on CTA pairs (gemm_pairs 1) whose hidden size is a multiple of 224: the
     down GEMM on 224-column tiles gives the layer the same bytes as on 256-column tiles,
     and the oracle's output for sampled tokens."""
     from combine_moe_route_03_gb300 import configs
@@ -297,7 +297,8 @@ def test_layer_down_224_column_tiles(dev):
     wdev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in ex.items()}
     outs = []
     for d224 in (False, True):
-        lay = api.MoELayer(cfg, to_dev(W, dev), to_dev(bias, dev), wdev, device=dev, down224=d224)
+        lay = api.MoELayer(cfg, to_dev(W, dev), to_dev(bias, dev), wdev, device=dev, down224=d224,
+                           gemm_pairs=1)
         assert (lay.W2_sf_t224 is not None) == d224
         outs.append(bits(lay.forward(bf16_dev(x, dev))))
         torch.cuda.synchronize()
