@@ -55,7 +55,8 @@ class GemmArgs(ctypes.Structure):
                 ("row_offset2", _c_i64), ("expert2", _c_int), ("out", _vp),
                 ("out_sf", _vp), ("signal", _vp), ("block_m_signal", _c_int),
                 ("num_sms", _c_int), ("pair_tiles", _c_int), ("scale_fmt", _c_int),
-                ("status", _vp), ("combine", ctypes.POINTER(FusedCombine))]
+                ("status", _vp), ("combine", ctypes.POINTER(FusedCombine)),
+                ("tile_n", _c_int)]
 
 
 class CombineCfg(ctypes.Structure):

@@ -256,7 +256,7 @@ def pack_weight_scales(W_sf: torch.Tensor, stream=None) -> torch.Tensor:
 def pack_weight_scales_tiled(W_sf: torch.Tensor, tile_n: int = 224, stream=None) -> torch.Tensor:
     """UE8M0 bytes [E][n/128][k/128] (device) -> two 128-row images per tile_n-row weight
     tile and group of four k-blocks, [E][n/tile_n][ceil(k/512)][2][512] (the DOWN GEMM's
-    scales with pair_tiles 2, tile_n 224)."""
+    scales with tile_n 224)."""
     E, nb, kb = W_sf.shape
     L = load()
     nbytes = L.moe_tiled_scale_bytes(E, nb * 128, kb * 128, tile_n)
@@ -276,10 +276,12 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
                      status: torch.Tensor | None = None, stream=None,
                      tiles2: torch.Tensor | None = None, row_offset2: int = 0, expert2: int = 0,
                      pair_tiles: int = 0, scale_fmt: int = SCALE_UE8M0,
-                     combine: dict | None = None):
+                     combine: dict | None = None, tile_n: int = 0):
     """moe_grouped_gemm_fp8.  W e4m3 [E][n][k]; A e4m3 [rows][k]; scale_fmt SCALE_F32:
     A_sf float [rows][k/128] and W_sf_atoms the float [E][n/128][k/128] scales.
-    combine (DOWN): the fused combine's tensors, as fused_combine_prep takes them."""
+    combine (DOWN): the fused combine's tensors, as fused_combine_prep takes them.
+    tile_n 224 (DOWN): 224-column tiles with two accumulators; W_sf_atoms then from
+    pack_weight_scales_tiled."""
     E, n, k = W.shape
     rows = A.shape[0]
     dev = A.device
@@ -296,6 +298,7 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
                  ptr(phys2log), ptr(tiles), ptr(tiles2), row_offset2, expert2, ptr(out),
                  ptr(out_sf), ptr(signal), block_m_signal, num_sms_, pair_tiles, scale_fmt,
                  ptr(st))
+    g.tile_n = tile_n
     if combine is not None:
         fc = _fused_combine_args(**combine)
         g.combine = ctypes.pointer(fc)

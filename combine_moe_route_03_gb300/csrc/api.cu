@@ -216,9 +216,9 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   g.W = L->W2;
   g.W_sf = L->W2_sf;
   g.pair_tiles = pairs_down ? 1 : 0;
-  // CTA pairs on 224-column tiles with two accumulators, when the layer has the scales
-  if (g.pair_tiles && L->W2_sf_t224 && !L->fuse_combine && !L->sbo && rc.H % 224 == 0) {
-    g.pair_tiles = 2;
+  // 224-column tiles with two accumulators, when the layer has their scales
+  if (L->W2_sf_t224 && !L->scale_fmt && !L->fuse_combine && !L->sbo && rc.H % 224 == 0) {
+    g.tile_n = 224;
     g.W_sf = L->W2_sf_t224;
   }
   g.out = L->Y;

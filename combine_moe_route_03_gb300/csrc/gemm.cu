@@ -484,12 +484,46 @@ __device__ __forceinline__ bool epilogue_f32(const GemmParams &P, const Unit &U,
   return true;
 }
 
+// The DOWN GEMM on 224-column tiles (H = 7168 = 32 x 224): two 224-column accumulators
+// and the scale sets fill TMEM exactly, so the MMAs of a unit run while the epilogue
+// drains the previous unit's accumulator.
+constexpr int BN224 = 224;
+constexpr uint32_t TMEM_SF224 = 2 * BN224;
+static_assert(TMEM_SF224 + 16 * kSfSets <= TMEM_COLS, "TMEM columns (224-column tiles)");
+
+// Epilogue of a 224-column DOWN accumulator: this thread's lane row, columns [0,128)
+// (half 0) or [128,224) (half 1); TMEM -> registers, release(), bf16 rounding and
+// stores as in epilogue_tile.
+template <class Release>
+__device__ __forceinline__ void epilogue_down224(const GemmParams &P, int row0, int valid, int ni,
+                                                 uint32_t t_row, int half, int row_local,
+                                                 int lane, uint8_t *stage, Release release) {
+  uint32_t v[128];
+  const int pieces = half ? (BN224 - 128) / 32 : 4;  // 32-column pieces of this thread
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    if (c < pieces) MOE_TMEM_LD_32x32b_X32(t_row + 128 * half + 32 * c, (v + 32 * c));
+  tc_wait_ld();
+  tc_fence_before();
+  release();
+  const int64_t wrow0 = (int64_t)row0 + (row_local - lane);
+  const int nrows = (int)min((int64_t)min(valid - (row_local - lane), 32), P.rows - wrow0);
+  if (nrows > 0) {
+    uint8_t *dst = P.out + ((size_t)wrow0 * P.n + (size_t)ni * BN224 + 128 * half) * 2;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (c < pieces)
+        store_bf16_rows(stage, v + 32 * c, dst + 64 * c, (size_t)P.n * 2, nrows, lane);
+  }
+}
+
 // tmA loads full 128-row A tiles; tmA32 loads 32-row slices, used for tiles with
 // fewer valid rows so rows that hold no data are never fetched (the MMA then reads
 // stale shared memory for them, which only feeds accumulator rows never stored).
 // kF32: binary32-scale mode (see epilogue_f32); otherwise UE8M0 block scaling in the
-// tensor core.
-template <bool kF32>
+// tensor core.  kW224: the DOWN GEMM on 224-column tiles with two accumulators (TMEM
+// columns [0,224) and [224,448), scale sets from 448; weight scales as tile images).
+template <bool kF32, bool kW224 = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmA32,
@@ -584,9 +618,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int a_slices = U.nvalid == BM ? 0 : (U.nvalid + 31) / 32;  // 0: one full box
         const uint32_t a_bytes = a_slices ? a_slices * (A_BYTES / 4) : A_BYTES;
         // a group's scale atoms travel with its first k-block
-        const uint32_t tx = a_bytes + B_BYTES, tx_sf = SFA_BYTES + SFB_BYTES;
+        const uint32_t tx = a_bytes + (kW224 ? (uint32_t)BN224 * BK : B_BYTES),
+                       tx_sf = SFA_BYTES + SFB_BYTES;
         int wrow0, wrow1, nb0, nb1;
-        if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
+        if (kW224) {  // one 224-row box; the tile's two scale images
+          wrow0 = wrow1 = we * P.n + ni * BN224;
+          nb0 = nb1 = 0;
+        } else if (P.op == MOE_GEMM_GATEUP_SWIGLU) {
           wrow0 = we * P.n + ni * 128;
           wrow1 = we * P.n + P.I + ni * 128;
           nb0 = ni;
@@ -598,8 +636,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           nb1 = 2 * ni + 1;
         }
         const uint8_t *sfa = P.A_sf + (size_t)(row0 >> 7) * P.Kg * 512;
-        const uint8_t *sfb0 = P.W_sf + ((size_t)we * (P.n / 128) + nb0) * P.Kg * 512;
-        const uint8_t *sfb1 = P.W_sf + ((size_t)we * (P.n / 128) + nb1) * P.Kg * 512;
+        // group g's atoms at sfb0 / sfb1 + g * sfb_step (images interleave per group)
+        const uint8_t *sfb0 =
+            kW224 ? P.W_sf + ((size_t)we * P.n_tiles + ni) * P.Kg * 1024
+                  : P.W_sf + ((size_t)we * (P.n / 128) + nb0) * P.Kg * 512;
+        const uint8_t *sfb1 =
+            kW224 ? sfb0 + 512 : P.W_sf + ((size_t)we * (P.n / 128) + nb1) * P.Kg * 512;
+        const size_t sfb_step = kW224 ? 1024 : 512;
         for (int kb = 0; kb < P.Kb; ++kb) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort, kWaitLimitNs)) {
             fail(P.status, abort);
@@ -619,11 +662,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int j = 0; j < a_slices; ++j)
               tma_load_2d(sa + j * (A_BYTES / 4), &tmA32, full, kb * BK, row0 + 32 * j, pol_a);
           tma_load_2d(sb, &tmW, full, kb * BK, wrow0, pol_w);
-          tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
+          if (!kW224) tma_load_2d(sb + B_BYTES / 2, &tmW, full, kb * BK, wrow1, pol_w);
           if (sf) {
             bulk_load(ssfa, sfa + (size_t)(kb >> 2) * 512, 512, full);
-            bulk_load(ssfb, sfb0 + (size_t)(kb >> 2) * 512, 512, full);
-            bulk_load(ssfb + 512, sfb1 + (size_t)(kb >> 2) * 512, 512, full);
+            bulk_load(ssfb, sfb0 + (size_t)(kb >> 2) * sfb_step, 512, full);
+            bulk_load(ssfb + 512, sfb1 + (size_t)(kb >> 2) * sfb_step, 512, full);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -649,10 +692,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       // kind::mxf8f6f4 instruction descriptor: E4M3 x E4M3, K-major A and B,
       // N = 256, UE8M0 scales, M = 128; bits 4-5 / 29-30 select the B / A scale byte.
-      const uint32_t idesc_base = ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+      const uint32_t idesc_base = ((uint32_t)((kW224 ? BN224 : BN) >> 3) << 17) | (1u << 23) |
                                   ((uint32_t)(BM >> 4) << 24);
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0, pg = 0;
+      const uint32_t tmem_sf = kW224 ? TMEM_SF224 : TMEM_SF;
+      int stage = 0, nacc = 0;  // units accumulated so far (buffer nacc % 2 if kW224)
+      uint32_t phase = 0, pg = 0;
       bool ok = true;
       for (int seq = 0; ok; ++seq) {
         Unit U;
@@ -692,7 +736,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           continue;
         }
-        if (!mbar_wait(bar_acc_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
+        // buffer 1 of kW224 uses the binary32 mode's (here idle) partial barriers
+        const int buf = kW224 ? nacc & 1 : 0;
+        const uint32_t acc_phase = (uint32_t)(kW224 ? nacc >> 1 : nacc) & 1u;
+        const uint32_t acc = tmem + (kW224 ? (uint32_t)(BN224 * buf) : 0u);
+        const uint32_t b_full = buf ? bar_pfull : bar_acc_full;
+        const uint32_t b_empty = buf ? bar_pempty : bar_acc_empty;
+        if (!mbar_wait(b_empty, acc_phase ^ 1, abort, kWaitLimitNs)) {
           fail(P.status, abort);
           break;
         }
@@ -706,7 +756,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t sa = s_base + OFF_A + stage * A_BYTES;
           const uint32_t sb = s_base + OFF_B + stage * B_BYTES;
-          const uint32_t t_sfa = tmem + TMEM_SF + 16 * ((kb >> 2) % kSfSets);
+          const uint32_t t_sfa = tmem + tmem_sf + 16 * ((kb >> 2) % kSfSets);
           const uint32_t t_sfb = t_sfa + 4;
           if ((kb & 3) == 0) {  // the group's scale atoms, once per four k-blocks
             const uint32_t ssfa = s_base + OFF_SFA + stage * SFA_BYTES;
@@ -722,7 +772,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int j = 0; j < BK / 32; ++j) {
             const uint64_t ad = smem_desc(sa + 32 * j, 16, 1024, 2);
             const uint64_t bd = smem_desc(sb + 32 * j, 16, 1024, 2);
-            tc_mma_mxf8(tmem, ad, bd, idesc, t_sfa, t_sfb, (kb | j) != 0);
+            tc_mma_mxf8(acc, ad, bd, idesc, t_sfa, t_sfb, (kb | j) != 0);
           }
           tc_commit(bar_empty + 8 * stage);
           if (++stage == STAGES) {
@@ -731,8 +781,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(bar_acc_full);
-        acc_phase ^= 1;
+        tc_commit(b_full);
+        ++nacc;
       }
     }
   } else if (warp < 2 + kEpiThreads / 32) {
@@ -747,7 +797,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t t_row = tmem + ((uint32_t)(32 * q) << 16);
     float *amax_x = reinterpret_cast<float *>(smem + OFF_AMAX);  // [half][row]
     uint8_t *stage = smem + OFF_STAGE + (warp - 2) * STAGE_BYTES;
-    uint32_t acc_phase = 0, pg = 0;
+    uint32_t pg = 0;
+    int nacc = 0;  // as the MMA issuer: buffer nacc % 2 if kW224
     for (int seq = 0;; ++seq) {
       Unit U;
       if (!take_unit(seq, U)) {
@@ -766,14 +817,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         continue;
       }
-      if (!mbar_wait(bar_acc_full, acc_phase, abort, kWaitLimitNs)) {
+      const int buf = kW224 ? nacc & 1 : 0;
+      const uint32_t acc_phase = (uint32_t)(kW224 ? nacc >> 1 : nacc) & 1u;
+      ++nacc;
+      const uint32_t b_full = buf ? bar_pfull : bar_acc_full;
+      const uint32_t b_empty = buf ? bar_pempty : bar_acc_empty;
+      if (!mbar_wait(b_full, acc_phase, abort, kWaitLimitNs)) {
         fail(P.status, abort);
         break;
       }
       tc_fence_after();
-      epilogue_tile(P, U.row0, U.nvalid, U.ni, t_row, half, row_local, warp, lane, amax_x,
-                    stage, [&] { mbar_arrive(bar_acc_empty); });
-      acc_phase ^= 1;
+      if constexpr (kW224)
+        epilogue_down224(P, U.row0, U.nvalid, U.ni, t_row + (uint32_t)(BN224 * buf), half,
+                         row_local, lane, stage, [&] { mbar_arrive(b_empty); });
+      else
+        epilogue_tile(P, U.row0, U.nvalid, U.ni, t_row, half, row_local, warp, lane, amax_x,
+                      stage, [&] { mbar_arrive(b_empty); });
     }
   } else if (lane == 0) {
     // ------------------------------------------------------------ scheduler
@@ -861,12 +920,6 @@ static_assert(XBUF_BYTES >= (kEpiThreads / 32) * STAGE_BYTES, "DOWN staging slot
 constexpr uint32_t SMEM2_BYTES = O2_XBUF + XBUF_BYTES + 1024;
 constexpr uint32_t TMEM_SF2 = 256;  // kSfSets rotating scale sets of 16 columns, as above
 static_assert(TMEM_SF2 + 16 * kSfSets <= TMEM_COLS, "TMEM columns");
-// The DOWN GEMM on 224-column tiles (H = 7168 = 32 x 224): two 224-column accumulators
-// and the scale sets fill TMEM exactly, so the MMAs of a unit run while the epilogue
-// drains the previous unit's accumulator.
-constexpr int BN224 = 224;
-constexpr uint32_t TMEM_SF224 = 2 * BN224;
-static_assert(TMEM_SF224 + 16 * kSfSets <= TMEM_COLS, "TMEM columns (224-column tiles)");
 static_assert(KB2 == 1 || KB2 == 2 || KB2 == 4, "a scale group (4 k-blocks) starts a stage");
 static_assert(SMEM2_BYTES <= 232448, "shared memory of the 2-SM kernel");
 
@@ -1021,32 +1074,6 @@ __device__ __forceinline__ void epilogue_m128(const GemmParams &P, int row0, int
             red_release_gpu_add(P.signal + (row0 + j * P.bm_signal) / P.bm_signal, 1);
       }
     }
-  }
-}
-
-// Epilogue of a 224-column DOWN accumulator: this thread's lane row, columns [0,128)
-// (half 0) or [128,224) (half 1); TMEM -> registers, release(), bf16 rounding and
-// stores as in epilogue_tile.
-template <class Release>
-__device__ __forceinline__ void epilogue_down224(const GemmParams &P, int row0, int valid, int ni,
-                                                 uint32_t t_row, int half, int row_local,
-                                                 int lane, uint8_t *stage, Release release) {
-  uint32_t v[128];
-  const int pieces = half ? (BN224 - 128) / 32 : 4;  // 32-column pieces of this thread
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    if (c < pieces) MOE_TMEM_LD_32x32b_X32(t_row + 128 * half + 32 * c, (v + 32 * c));
-  tc_wait_ld();
-  tc_fence_before();
-  release();
-  const int64_t wrow0 = (int64_t)row0 + (row_local - lane);
-  const int nrows = (int)min((int64_t)min(valid - (row_local - lane), 32), P.rows - wrow0);
-  if (nrows > 0) {
-    uint8_t *dst = P.out + ((size_t)wrow0 * P.n + (size_t)ni * BN224 + 128 * half) * 2;
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (c < pieces)
-        store_bf16_rows(stage, v + 32 * c, dst + 64 * c, (size_t)P.n * 2, nrows, lane);
   }
 }
 
@@ -1585,9 +1612,12 @@ extern "C" int moe_weight_scales_f32(int E, int n, int k, const uint8_t *W_sf, f
 extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   if (!a) return MOE_ERR_INVALID;
   if (a->op != MOE_GEMM_GATEUP_SWIGLU && a->op != MOE_GEMM_DOWN) return MOE_ERR_INVALID;
-  if (a->pair_tiles < 0 || a->pair_tiles > 2) return MOE_ERR_INVALID;
-  if (a->pair_tiles == 2) {  // 224-column DOWN tiles with two accumulators
-    if (a->op != MOE_GEMM_DOWN || a->signal || a->combine) return MOE_ERR_INVALID;
+  if (a->pair_tiles != 0 && a->pair_tiles != 1) return MOE_ERR_INVALID;
+  if (a->tile_n != 0 && a->tile_n != BN && a->tile_n != BN224) return MOE_ERR_INVALID;
+  const bool w224 = a->tile_n == BN224;  // 224-column DOWN tiles with two accumulators
+  if (w224) {
+    if (a->op != MOE_GEMM_DOWN || a->signal || a->combine || a->scale_fmt)
+      return MOE_ERR_INVALID;
     if (a->n % BN224) return MOE_ERR_UNSUPPORTED;
   }
   if (a->scale_fmt != 0 && a->scale_fmt != 1) return MOE_ERR_INVALID;
@@ -1615,7 +1645,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   if (!make_map(&mA, a->A, (uint64_t)a->rows, (uint64_t)a->k) ||
       !make_map(&mA32, a->A, (uint64_t)a->rows, (uint64_t)a->k, 32) ||
       !make_map(&mW, a->W, (uint64_t)a->num_experts * a->n, (uint64_t)a->k,
-                a->pair_tiles == 2 ? BN224 / 2 : 128))
+                w224 ? (a->pair_tiles ? BN224 / 2 : BN224) : 128))
     return MOE_ERR_CUDA;
   if (a->tiles2 && (a->expert2 < 0 || a->expert2 >= a->num_experts || a->row_offset2 < 0 ||
                     a->row_offset2 % 128 || a->row_offset2 >= a->rows))
@@ -1633,7 +1663,7 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   P.k = a->k;
   P.Kb = a->k / BK;
   P.Kg = sf_groups(a->k);
-  P.n_tiles = a->n / (a->pair_tiles == 2 ? BN224 : BN);
+  P.n_tiles = a->n / (w224 ? BN224 : BN);
   P.I = a->n / 2;
   P.A_sf = static_cast<const uint8_t *>(a->A_sf);
   P.W_sf = static_cast<const uint8_t *>(a->W_sf);
@@ -1670,6 +1700,9 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
       e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_kernel<false, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(grouped_gemm_2sm_kernel<false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
     if (e == cudaSuccess)
@@ -1683,13 +1716,13 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
     CUtensorMap mSFA, mSFW;
     const uint64_t kg = (uint64_t)sf_groups(a->k);
     // weight scales: 128-row atoms, or two images per 224-column tile
-    const uint64_t w_atoms = a->pair_tiles == 2
+    const uint64_t w_atoms = w224
                                  ? (uint64_t)a->num_experts * (a->n / BN224) * kg * 2
                                  : (uint64_t)a->num_experts * (a->n / 128) * kg;
     if (!make_sf_map(&mSFA, a->A_sf, (uint64_t)(a->rows / 128) * kg, 1) ||
         !make_sf_map(&mSFW, a->W_sf, w_atoms, 1))
       return MOE_ERR_CUDA;
-    if (a->pair_tiles == 2)
+    if (w224)
       return launch_pairs(grouped_gemm_2sm_kernel<true>, SMEM2_BYTES, sms, max_clusters224[dev],
                           as_stream(stream), mA, mA32, mW, mSFA, mSFW, P);
     return launch_pairs(grouped_gemm_2sm_kernel<false>, SMEM2_BYTES, sms, max_clusters[dev],
@@ -1699,6 +1732,9 @@ extern "C" int moe_grouped_gemm_fp8(const moe_gemm_args *a, void *stream) {
   const int grid = (int)(max_units < sms ? max_units : sms);
   if (a->scale_fmt)
     grouped_gemm_kernel<true><<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW, P);
+  else if (w224)
+    grouped_gemm_kernel<false, true>
+        <<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW, P);
   else
     grouped_gemm_kernel<false><<<grid, kGemmThreads, SMEM_BYTES, as_stream(stream)>>>(mA, mA32, mW, P);
   return check_launch();

@@ -355,12 +355,7 @@ typedef struct moe_gemm_args {
                         single tile, in the same launch, as an M = 128 pair MMA (up to 64
                         valid rows) or an M = 256 one with the second half idle; needs
                         k % 256 == 0 (else MOE_ERR_UNSUPPORTED).
-                     2: DOWN only (else MOE_ERR_INVALID, as with signal or combine): CTA
-                        pairs on 224-column output tiles (n % 224 == 0, else
-                        MOE_ERR_UNSUPPORTED), every tile at M = 256, two accumulators in
-                        TMEM so a unit's MMAs overlap the previous unit's epilogue; W_sf
-                        from moe_pack_weight_scales_tiled with tile_n 224.
-                     Other values: MOE_ERR_INVALID.  All give the same bytes. */
+                     Other values: MOE_ERR_INVALID.  Both give the same bytes. */
   int scale_fmt;  /* 0: UE8M0 scales as SF atoms, applied by the tensor core (block
                      scaling).  1: binary32 scales (1d2d with float scales, "Single Batch
                      Overlap (SBO)" PR, §3): A_sf float [rows][k/128], W_sf float
@@ -374,6 +369,12 @@ typedef struct moe_gemm_args {
   const moe_fused_combine *combine; /* nullable; DOWN only, and not with signal (else
                                        MOE_ERR_INVALID): reduce Y into combine->out as
                                        the rows are stored (see moe_fused_combine) */
+  int tile_n; /* output columns per tile: 0 or 256; or 224 (DOWN only, UE8M0 scales, no
+                 signal or combine, else MOE_ERR_INVALID; n % 224 == 0, else
+                 MOE_ERR_UNSUPPORTED): two 224-column accumulators in TMEM, so a unit's
+                 MMAs overlap the previous unit's epilogue, with W_sf from
+                 moe_pack_weight_scales_tiled (tile_n 224); with pair_tiles 1 every tile
+                 runs at M = 256.  The same bytes either way. */
 } moe_gemm_args;
 
 int moe_grouped_gemm_fp8(const moe_gemm_args *args, void *stream);
@@ -389,8 +390,7 @@ size_t moe_packed_scale_bytes(int E, int n, int k);
    n % tile_n == 0; 0 otherwise): per (expert, tile, group of four k-blocks) two 128-row
    images in the SF atom layout, image h holding the tile's rows [128h, 128h + 128), each
    row with its own 128x128 block's scale (rows past tile_n zero):
-   [E][n/tile_n][ceil(k/512)][2][512] bytes.  The DOWN GEMM with pair_tiles 2 reads them
-   (tile_n 224).  One-time setup, off the hot path. */
+   [E][n/tile_n][ceil(k/512)][2][512] bytes.  The DOWN GEMM with tile_n 224 reads them.  One-time setup, off the hot path. */
 size_t moe_tiled_scale_bytes(int E, int n, int k, int tile_n);
 int moe_pack_weight_scales_tiled(int E, int n, int k, int tile_n, const uint8_t *W_sf,
                                  void *W_sf_tiled, void *stream);
@@ -508,9 +508,8 @@ typedef struct moe_layer {
   int32_t *src_of;  /* fuse_combine: int32 [rows], the token of each routed row */
   int32_t *pending; /* fuse_combine: int32 [B][H/128] */
   const void *W2_sf_t224; /* nullable: W2's scales as moe_pack_weight_scales_tiled images
-                             (tile_n 224); with them a down GEMM on CTA pairs (gemm_pairs
-                             1) runs on 224-column tiles (pair_tiles 2), unless
-                             fuse_combine or sbo */
+                             (tile_n 224); with them the down GEMM runs on 224-column
+                             tiles (moe_gemm_args.tile_n 224), unless fuse_combine or sbo */
 } moe_layer;
 
 #define MOE_LAYER_EVENTS 6

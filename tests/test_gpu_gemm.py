@@ -185,9 +185,10 @@ def test_2sm_gemm_equals_single_cta(dev, op, pattern):
 @pytest.mark.parametrize("pattern", sorted(NVALID))
 @pytest.mark.parametrize("k", [512, 2048])
 def test_down_224_column_tiles_equal_single_cta(dev, k, pattern):
-    """The DOWN GEMM on 224-column tiles with two accumulators (pair_tiles 2, every tile
-    at M=256, weight scales as tile-aligned images) gives the bytes of one CTA per tile
-    on 256-column tiles, for experts with 1, 2, 3 and 5 M tiles."""
+    """The DOWN GEMM on 224-column tiles with two accumulators (tile_n 224, weight scales
+    as tile-aligned images), on one CTA per tile and on CTA pairs (every tile at M=256),
+    gives the bytes of one CTA per tile on 256-column tiles, for experts with 1, 2, 3
+    and 5 M tiles."""
     tiles_per_expert = [1, 2, 3, 5, 2]
     E, n = len(tiles_per_expert), 1792           # 8 tiles of 224, 7 of 256
     mt = sum(tiles_per_expert)
@@ -199,17 +200,19 @@ def test_down_224_column_tiles_equal_single_cta(dev, k, pattern):
     Wd, Wsf_d = torch.from_numpy(W).to(dev), torch.from_numpy(Wsf).to(dev)
     tl = torch.from_numpy(t).to(dev)
     outs = []
-    for pairs, scales in ((0, api.pack_weight_scales(Wsf_d)),
-                          (2, api.pack_weight_scales_tiled(Wsf_d, 224))):
+    tiled = api.pack_weight_scales_tiled(Wsf_d, 224)
+    for pairs, tile_n, scales in ((0, 0, api.pack_weight_scales(Wsf_d)), (1, 224, tiled),
+                                  (0, 224, tiled)):
         st = api.new_status(dev)
         outs.append(api.grouped_gemm_fp8(api.GEMM_DOWN, A, A_sf, Wd, scales, tl, mt, status=st,
-                                         pair_tiles=pairs))
+                                         pair_tiles=pairs, tile_n=tile_n))
         torch.cuda.synchronize()
         assert api.read_status(st) == 0
-    for i0 in range(mt):
-        nvalid = t[8 + 8 * i0 + 2]
-        assert torch.equal(outs[0][128 * i0: 128 * i0 + nvalid].view(torch.int16),
-                           outs[1][128 * i0: 128 * i0 + nvalid].view(torch.int16)), i0
+    for o in outs[1:]:
+        for i0 in range(mt):
+            nvalid = t[8 + 8 * i0 + 2]
+            assert torch.equal(outs[0][128 * i0: 128 * i0 + nvalid].view(torch.int16),
+                               o[128 * i0: 128 * i0 + nvalid].view(torch.int16)), i0
 
 
 def test_tiled_weight_scale_images(dev):
@@ -232,16 +235,17 @@ def test_tiled_weight_scale_images(dev):
 
 
 @pytest.mark.parametrize("k", [768, 4352])
-@pytest.mark.parametrize("pairs", [0, 1, 2])
+@pytest.mark.parametrize("mode", ["one_cta", "pairs", "pairs_224", "one_cta_224"])
 @pytest.mark.parametrize("last", [128, 50])
-def test_weight_scale_bytes_per_block(dev, pairs, k, last):
+def test_weight_scale_bytes_per_block(dev, mode, k, last):
     """Weight scale bytes drawn per 128x128 block over 21 binades, K of 6 and 34
     k-blocks: the down GEMM still equals the fp64 product of the dequantised operands
     in every scheduling mode (a scale atom read for the wrong block, k-block or row
     half moves an output by a power of two), with full last tiles and with 50-row last
     tiles (the 2-SM kernel's M=128 singles)."""
+    pairs, tile_n = int(mode.startswith("pairs")), 224 if mode.endswith("224") else 0
     tiles_per_expert = [2, 3, 1]
-    E, n = len(tiles_per_expert), 1792 if pairs == 2 else 512
+    E, n = len(tiles_per_expert), 1792 if tile_n else 512
     mt = sum(tiles_per_expert)
     rows = 128 * mt
     q, sf = activations(rows, k, 11)
@@ -260,9 +264,10 @@ def test_weight_scale_bytes_per_block(dev, pairs, k, last):
     out = api.grouped_gemm_fp8(api.GEMM_DOWN, torch.from_numpy(q).to(dev),
                                torch.from_numpy(pack_sf_atoms(sf)).to(dev),
                                torch.from_numpy(W).to(dev),
-                               (api.pack_weight_scales_tiled if pairs == 2 else
+                               (api.pack_weight_scales_tiled if tile_n else
                                 api.pack_weight_scales)(torch.from_numpy(Wsf).to(dev)),
-                               torch.from_numpy(t).to(dev), mt, status=st, pair_tiles=pairs)
+                               torch.from_numpy(t).to(dev), mt, status=st, pair_tiles=pairs,
+                               tile_n=tile_n)
     torch.cuda.synchronize()
     assert api.read_status(st) == 0
     got = oracle.bf16_to_f32(bits(out)).astype(np.float64)
@@ -281,7 +286,7 @@ def test_weight_scale_bytes_per_block(dev, pairs, k, last):
 
 
 def test_layer_down_224_column_tiles(dev):
-    """A layer on CTA pairs (gemm_pairs 1) whose hidden size is a multiple of 224: the
+    """A layer whose hidden size is a multiple of 224 (CTA pairs, then one CTA per tile): the
     down GEMM on 224-column tiles gives the layer the same bytes as on 256-column tiles,
     and the oracle's output for sampled tokens."""
     from combine_moe_route_03_gb300 import configs
@@ -296,14 +301,14 @@ def test_layer_down_224_column_tiles(dev):
     ex.update(W13s=s[0], W13s_sf=s[1], W2s=s[2], W2s_sf=s[3])
     wdev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in ex.items()}
     outs = []
-    for d224 in (False, True):
+    for d224, pairs in ((False, 1), (True, 1), (True, 0)):
         lay = api.MoELayer(cfg, to_dev(W, dev), to_dev(bias, dev), wdev, device=dev, down224=d224,
-                           gemm_pairs=1)
+                           gemm_pairs=pairs)
         assert (lay.W2_sf_t224 is not None) == d224
         outs.append(bits(lay.forward(bf16_dev(x, dev))))
         torch.cuda.synchronize()
         assert api.read_status(lay.status) == 0
-    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
     tok = np.array([0, 1, 777, 1500, cfg.B - 1])
     ref = oracle.layer_tokens(cfg, x, W, bias, getter(ex), shared_of(ex), tokens=tok)
     ok, err, bound = within_tol(oracle.bf16_to_f32(outs[1][tok]), oracle.bf16_to_f32(ref["out"]))

@@ -175,6 +175,18 @@ def test_host_argument_checks_return_before_launch(L):
     g = _lib.GemmArgs(1, 256, 128, 128, 1, 1, *p, None, 16, None, 0, 0, 16, None, 16, 64, 0, 0,
                       0, None, ctypes.pointer(fc))                # with SBO signals
     assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
+    for op, tile_n in ((1, 100), (0, 224)):                      # no such width; gate/up
+        g = _lib.GemmArgs(op, 1792, 256, 128, 1, 1, *p, None, 16, None, 0, 0, 16, 16, None, 64,
+                          0, 0, 0, None, None, tile_n)
+        assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
+    g = _lib.GemmArgs(1, 1536, 256, 128, 1, 1, *p, None, 16, None, 0, 0, 16, None, None, 64, 0,
+                      0, 0, None, None, 224)                   # n % 224 != 0
+    assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -2
+    g = _lib.GemmArgs(1, 1792, 256, 128, 1, 1, *p, None, 16, None, 0, 0, 16, None, None, 64, 0,
+                      2, 0, None, None, 0)                     # pair_tiles 2 is no mode
+    assert L.moe_grouped_gemm_fp8(ctypes.byref(g), None) == -1
+    assert L.moe_tiled_scale_bytes(2, 1792, 640, 224) == 2 * 8 * 2 * 1024
+    assert L.moe_tiled_scale_bytes(2, 1792, 640, 100) == 0 and L.moe_tiled_scale_bytes(2, 1536, 640, 224) == 0
     assert L.moe_fused_combine_prep(None, 256, None) == -1
     assert L.moe_fused_combine_prep(ctypes.byref(_lib.FusedCombine(4, 0, 16, 16, 16, 128, 16,
                                                                    -1, 16)), 256, None) == -1
