@@ -238,26 +238,29 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
   }
   const int first = block_scan(scan, nt) - nt;
   const int np = nt / 2, ns = nt % 2, gcnt = np + ns;
-  // Order of the item groups (the 2-SM GEMM's schedule): an expert with several items
+  // Order of the experts' tiles and item groups (both GEMMs' schedules: the one-CTA
+  // kernel walks the tiles, the 2-SM kernel the items): an expert with several items
   // reads each weight tile from HBM once for all of them (the rest come from L2), one
   // with a single item reads a weight tile from HBM per unit.  Spreading the multi-item
   // experts evenly between the single-item ones, in expert order within each kind, keeps
   // the HBM demand of the CTAs running side by side even.  Multi-item expert i of nm
   // goes before single-item expert floor((2i + 1) * n1 / (2 nm)) of n1; experts without
-  // items take no place.  One scan gives both ranks (counts <= kScanThreads, 11 bits
-  // apart), a second one each position's first item.
+  // tiles take no place.  The rows stay in expert order (segments as `first`).  One scan
+  // gives both ranks (counts <= kScanThreads, 11 bits apart), two more each position's
+  // first item and first tile.
   const int multi = (p < N_phys && gcnt >= 2) ? 1 : 0;
   const int single = (p < N_phys && gcnt == 1) ? 1 : 0;
   const int kinds_incl = block_scan(scan, multi | (single << 11));
   const int multi_rank = (kinds_incl & 2047) - multi;
   const int single_rank = (kinds_incl >> 11) - single;
   __shared__ int32_t kinds[2];
-  __shared__ int32_t by_pos[kScanThreads];
+  __shared__ int32_t by_pos[kScanThreads], by_pos_nt[kScanThreads];
   if (p == kScanThreads - 1) {
     kinds[0] = kinds_incl & 2047;
     kinds[1] = kinds_incl >> 11;
   }
   by_pos[p] = 0;
+  by_pos_nt[p] = 0;
   const int singles = __syncthreads_count(ns);  // also orders the writes above
   const int nm = kinds[0], n1 = kinds[1];
   int pos = -1;
@@ -267,11 +270,17 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
     const int q = n1 > 0 ? (2 * nm * (single_rank + 1) - 1) / n1 : 0;
     pos = single_rank + min(nm, (q + 1) / 2);
   }
-  if (pos >= 0) by_pos[pos] = gcnt;
+  if (pos >= 0) {
+    by_pos[pos] = gcnt;
+    by_pos_nt[pos] = nt;
+  }
   __syncthreads();
   const int at_pos = p < nm + n1 ? by_pos[p] : 0;
-  const int pos_incl = block_scan(scan, at_pos);  // items up to position p
+  const int at_pos_nt = p < nm + n1 ? by_pos_nt[p] : 0;
+  const int pos_incl = block_scan(scan, at_pos);         // items up to position p
+  const int pos_nt_incl = block_scan(scan, at_pos_nt);   // tiles up to position p
   by_pos[p] = pos_incl - at_pos;
+  by_pos_nt[p] = pos_nt_incl - at_pos_nt;
   if (p == kScanThreads - 1) {
     totals[0] = first + nt;
     totals[1] = pos_incl - singles;  // pairs: items that are not singles
@@ -280,14 +289,15 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(
   }
   __syncthreads();
   const int item_first = pos >= 0 ? by_pos[pos] : 0;
+  const int tile_first = pos >= 0 ? by_pos_nt[pos] : 0;
   const int64_t max_tiles = rows_alloc / 128;
   if (p < N_phys) {
     const int seg = layout == MOE_LAYOUT_CONTIG ? first * 128 : p * cap;
     ws.seg[p] = seg;
     for (int i = 0; i < nt; ++i)
-      put8(tiles + 8 + 8 * (size_t)(first + i), seg + 128 * i, p, min(128, valid - 128 * i),
-           first, nt);
-    write_items(tiles + 8 + 8 * max_tiles, first, nt, item_first);
+      put8(tiles + 8 + 8 * (size_t)(tile_first + i), seg + 128 * i, p,
+           min(128, valid - 128 * i), tile_first, nt);
+    write_items(tiles + 8 + 8 * max_tiles, tile_first, nt, item_first);
     pad_seg[p] = seg;  // rows [valid, end) of this expert's segment that no token fills
     pad_from[p] = valid;
     pad_to[p] = layout == MOE_LAYOUT_CONTIG ? nt * 128 : cap;

@@ -51,12 +51,13 @@
  *   work item k at tiles[8 + 8*max_tiles + 8*k ...]: {tile 0, tile 1 or -1, first
  *   item of its group, items in its group, 1 for a pair of one expert's tiles (0 for
  *   a single tile), 0, 0, 0}.  An expert's tiles form pairs two by two, and an odd
- *   last tile is a single; an expert's pairs and its single form one group.  Groups
- *   run in this order: the experts with two or more items spread evenly between the
- *   experts with one (multi-item expert i of nm, in expert order, before single-item
- *   expert floor((2i + 1) * n1 / (2 nm)) of n1), so CTAs running side by side mix
- *   weight tiles read once for several units with tiles read for one.
- * Tiles of one expert are consecutive.  The grouped GEMM reads this list on the
+ *   last tile is a single; an expert's pairs and its single form one group.
+ * Tiles of one expert are consecutive, and the experts' tiles and groups come in this
+ *   order: the experts with two or more items spread evenly between the experts with
+ *   one (multi-item expert i of nm, in expert order, before single-item expert
+ *   floor((2i + 1) * n1 / (2 nm)) of n1), so CTAs running side by side mix weight tiles
+ *   read once for several units with tiles read for one.  The rows themselves stay in
+ *   expert order.  The grouped GEMM reads this list on the
  * device, so the host never needs the routing result.
  */
 #ifndef LIBMOE_MOE_H

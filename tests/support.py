@@ -88,18 +88,14 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def dispatch_items(ntiles):
-    """cluster_items in the group order moe_dispatch writes: the experts with two or
-    more items spread evenly between those with one (multi-item expert i of nm, in
-    expert order, goes before single-item expert floor((2i + 1) n1 / (2 nm)) of n1)."""
-    first = np.concatenate([[0], np.cumsum(ntiles)]).astype(int)
-    groups = {}
-    for e, n in enumerate(ntiles):
-        npair, gc = n // 2, n // 2 + n % 2
-        groups[e] = [[first[e] + 2 * j, first[e] + 2 * j + 1 if j < npair else -1, j < npair]
-                     for j in range(gc)]
-    multi = [e for e in range(len(ntiles)) if len(groups[e]) >= 2]
-    single = [e for e in range(len(ntiles)) if len(groups[e]) == 1]
+def dispatch_order(ntiles):
+    """The order of the experts' tiles and item groups in moe_dispatch's tile list: the
+    experts with two or more items (three or more tiles) spread evenly between those
+    with one (multi-item expert i of nm, in expert order, goes before single-item expert
+    floor((2i + 1) n1 / (2 nm)) of n1); experts without tiles take no place."""
+    gcs = [n // 2 + n % 2 for n in ntiles]
+    multi = [e for e, g in enumerate(gcs) if g >= 2]
+    single = [e for e, g in enumerate(gcs) if g == 1]
     nm, n1 = len(multi), len(single)
     order, i = [], 0
     for s, e in enumerate(single):
@@ -107,11 +103,28 @@ def dispatch_items(ntiles):
             order.append(multi[i])
             i += 1
         order.append(e)
-    order += multi[i:]
+    return order + multi[i:]
+
+
+def dispatch_tile_first(ntiles):
+    """Each expert's first tile index in the dispatch order (0 for experts without)."""
+    first, t = [0] * len(ntiles), 0
+    for e in dispatch_order(ntiles):
+        first[e], t = t, t + ntiles[e]
+    return first
+
+
+def dispatch_items(ntiles):
+    """cluster_items in the group order moe_dispatch writes (dispatch_order), the tiles
+    numbered in that order too."""
+    first = dispatch_tile_first(ntiles)
     items = []
-    for e in order:
-        f_item, gc = len(items), len(groups[e])
-        items += [[t0, t1, f_item, gc, 1 if pair else 0] for t0, t1, pair in groups[e]]
+    for e in dispatch_order(ntiles):
+        n = ntiles[e]
+        npair, gc = n // 2, n // 2 + n % 2
+        f_item = len(items)
+        items += [[first[e] + 2 * j, first[e] + 2 * j + 1 if j < npair else -1, f_item, gc,
+                   1 if j < npair else 0] for j in range(gc)]
     return items
 
 

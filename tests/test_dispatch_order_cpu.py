@@ -4,21 +4,31 @@ the experts with several items spread evenly between those with one."""
 import numpy as np
 import pytest
 
-from support import cluster_items, dispatch_items
+from support import cluster_items, dispatch_items, dispatch_order, dispatch_tile_first
 
 
 @pytest.mark.parametrize("seed", range(8))
 def test_dispatch_items_is_a_regrouping_of_the_expert_order(seed):
+    """Every tile in exactly one item, each expert's tiles consecutive from its first
+    tile, its group its pairs then its single, groups in the dispatch order."""
     rng = np.random.default_rng(seed)
     nt = list(rng.choice([0, 1, 1, 1, 2, 3, 4, 7], size=int(rng.integers(1, 300))))
-    got, ref = dispatch_items(nt), cluster_items(nt)
-    assert sorted(map(tuple, (it[:2] + it[4:] for it in got))) == \
-        sorted(map(tuple, (it[:2] + it[4:] for it in ref)))
+    got = dispatch_items(nt)
+    assert len(got) == len(cluster_items(nt))
+    tiles = sorted(t for it in got for t in it[:2] if t >= 0)
+    assert tiles == list(range(sum(nt)))
+    first, order = dispatch_tile_first(nt), dispatch_order(nt)
+    assert sorted(order) == [e for e, n in enumerate(nt) if n > 0]
     k = 0
-    while k < len(got):                     # groups: consecutive, sizes and firsts agree
-        f, gc = got[k][2], got[k][3]
-        assert f == k and all(got[k + j][2:4] == [f, gc] for j in range(gc))
+    for e in order:                         # groups: consecutive, sizes and firsts agree
+        gc = nt[e] // 2 + nt[e] % 2
+        assert all(got[k + j][2:4] == [k, gc] for j in range(gc))
+        for j in range(gc):
+            pair = j < nt[e] // 2
+            assert got[k + j][:2] == [first[e] + 2 * j, first[e] + 2 * j + 1 if pair else -1]
+            assert got[k + j][4] == int(pair)
         k += gc
+    assert k == len(got)
 
 
 def test_multi_item_experts_are_spread_evenly():
@@ -34,5 +44,6 @@ def test_multi_item_experts_are_spread_evenly():
 
 
 def test_all_one_kind():
+    """With one kind of expert only, the order is the expert order (cluster_items)."""
     for nt in ([1] * 7, [3] * 7, [2, 0, 2], []):
-        assert sorted(map(tuple, dispatch_items(nt))) == sorted(map(tuple, cluster_items(nt)))
+        assert dispatch_items(nt) == cluster_items(nt)

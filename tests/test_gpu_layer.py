@@ -5,7 +5,8 @@ import torch
 
 import oracle
 from combine_moe_route_03_gb300 import api, configs, inputs
-from support import (bf16_dev, bits, device_weights, dispatch_items, getter, host_experts,
+from support import (bf16_dev, bits, device_weights, dispatch_items, dispatch_tile_first,
+                     getter, host_experts,
                      host_workload, shared_of, to_dev, unpack_sf_atoms, within_tol)
 
 pytestmark = pytest.mark.gpu
@@ -117,13 +118,12 @@ def check_dispatch(cfg, x, idx, d, ref, fmt=api.FMT_FP8):
     assert list(t[2:5]) == [int((ntp // 2).sum()), int((ntp % 2).sum()),
                             len(dispatch_items(list(ntp)))]
     tl = t[8: 8 + 8 * nt].reshape(nt, 8)
-    i = 0
+    first = dispatch_tile_first(list(ntp))     # tiles in the dispatch order, rows not
     for p in range(cfg.N_phys):
         base = ref["seg_start"][p] if cfg.layout == configs.CONTIG else p * cfg.cap
         for j in range(ntp[p]):
-            assert list(tl[i]) == [base + 128 * j, p, min(128, cnt[p] - 128 * j),
-                                   i - j, ntp[p], 0, 0, 0]
-            i += 1
+            assert list(tl[first[p] + j]) == [base + 128 * j, p, min(128, cnt[p] - 128 * j),
+                                              first[p], ntp[p], 0, 0, 0]
     items = dispatch_items(list(ntp))
     mt = d["max_tiles"]
     got = t[8 + 8 * mt: 8 + 8 * mt + 8 * len(items)].reshape(-1, 8)
