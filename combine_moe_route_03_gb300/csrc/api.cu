@@ -184,7 +184,7 @@ extern "C" int moe_layer_forward(const moe_layer *L, void *stream) {
   g.W_sf = L->W13_sf;
   g.phys2log = L->phys2log;
   g.tiles = L->tiles;
-  if (L->has_shared) {
+  if (L->has_shared && srows > 0) {  // (an empty batch has no shared rows)
     g.tiles2 = L->shared_tiles;
     g.row_offset2 = L->rows;
     g.expert2 = rc.N;

@@ -192,6 +192,20 @@ def test_empty_batch(dev):
     assert d["tiles"][0].item() == 0 and int(d["counts"].sum()) == 0
 
 
+@pytest.mark.parametrize("name", ["small_contig", "small_masked", "small_sbo"])
+def test_empty_batch_layer(dev, name):
+    """B = 0 through the whole layer: every stage returns at once or runs with no work,
+    the status stays clean, and the output has no rows."""
+    cfg, _, W, bias = host_workload(name)
+    cfg = cfg.with_(B=0)
+    lay = api.MoELayer(cfg, to_dev(W), to_dev(bias), device_weights(host_experts(name)))
+    out = lay.forward(torch.empty((0, cfg.H), dtype=torch.bfloat16, device=dev))
+    torch.cuda.synchronize()
+    assert api.read_status(lay.status) == 0
+    assert tuple(out.shape) == (0, cfg.H)
+    assert int(lay.counts.sum()) == 0 and lay.tiles[0].item() == 0
+
+
 @pytest.mark.parametrize("B", [1, 37, 300])
 def test_route_at_the_largest_expert_count(dev, B):
     """512 experts in 8 groups of 64, top-3 groups, K = 16 (the largest K), sigmoid +
