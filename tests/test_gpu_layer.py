@@ -50,13 +50,16 @@ def test_route_bit_exact_other_group_shapes(dev, N, G, TG, K):
 
 
 @pytest.mark.parametrize("B,N,H", [(10000, 256, 256), (4000, 512, 256), (1000, 256, 256),
-                                   (700, 512, 192), (300, 256, 160), (77, 64, 160)])
+                                   (700, 512, 192), (300, 256, 160), (77, 64, 160),
+                                   (201, 256, 384), (129, 40, 256)])
 def test_route_logits_kernel_shapes(dev, B, N, H):
     """The logits kernel is chosen from B, N and H.  On 152 SMs these shapes take, in
     order: the fp32-widened 8x8 tile past the token-sliced range (256 experts) and at
     512 experts, the 2x2 tile with 64-wide chunks (H a multiple of 128, and of 64 only),
-    and the 32-wide-chunk kernel (H a multiple of 32 only) for a wide and a ragged
-    batch.  All logits, ids and weights bit-exact."""
+    the 32-wide-chunk kernel (H a multiple of 32 only) for a wide and a ragged batch,
+    and the two-token tile of decode-size batches for an odd batch (its last token pair
+    half empty) and an expert count that leaves a ragged expert tile.  All logits, ids
+    and weights bit-exact."""
     kw = (dict(n_group=8, topk_group=3, K=16) if N == 512 else
           dict(n_group=8, topk_group=4, K=8) if N == 256 else dict(n_group=4, topk_group=2, K=6))
     cfg = configs.MoEConfig("shape", B=B, H=H, N=N, I=128, score_fn=configs.SIGMOID, renorm=1,
