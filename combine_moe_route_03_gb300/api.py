@@ -26,6 +26,22 @@ def num_sms() -> int:
     return load().moe_num_sms()
 
 
+def _ordered(stream, *temps) -> int:
+    """The handle of the stream a call runs on.  A ``stream`` other than the caller's
+    current stream first waits for the current one, where the call's inputs and the
+    buffers this module allocates for it were made (torch's caching allocator ties a
+    fresh buffer to the current stream); ``temps`` -- buffers freed when the call
+    returns -- are kept from reuse until ``stream`` is done with them."""
+    if stream is not None:
+        cur = torch.cuda.current_stream(stream.device)
+        if stream != cur:
+            stream.wait_stream(cur)
+            for t in temps:
+                if t is not None:
+                    t.record_stream(stream)
+    return stream_ptr(stream)
+
+
 def new_status(device="cuda") -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device=device)
 
@@ -72,7 +88,7 @@ def route(cfg: MoEConfig, x: torch.Tensor, W: torch.Tensor, bias: torch.Tensor |
     ws = torch.empty(max(1, L.moe_route_workspace_size(ctypes.byref(rc))), dtype=torch.uint8,
                      device=dev)
     check(L.moe_route(ctypes.byref(rc), ptr(x), ptr(W), ptr(bias), ptr(idx), ptr(w), ptr(cnt),
-                      ptr(ws), ws.numel(), stream_ptr(stream)), "moe_route")
+                      ptr(ws), ws.numel(), _ordered(stream)), "moe_route")
     return dict(topk_idx=idx, topk_w=w, counts=cnt, logits=ws)
 
 
@@ -218,7 +234,7 @@ def dispatch(cfg: MoEConfig, x: torch.Tensor, topk_idx: torch.Tensor, log2phys=N
                               ptr(o["A"]), ptr(o["A_sf"]), ptr(o["counts"]), ptr(o["row_of"]),
                               ptr(o.get("src_of")), ptr(o["tiles"]), ptr(o.get("As")),
                               ptr(o.get("As_sf")), ptr(o.get("shared_tiles")), ptr(o["ws"]),
-                              o["ws"].numel(), ptr(st), stream_ptr(stream)), "moe_dispatch")
+                              o["ws"].numel(), ptr(st), _ordered(stream)), "moe_dispatch")
     o.update(rows=rows, max_tiles=mt, status=st)
     return o
 
@@ -238,7 +254,7 @@ def weight_scales_f32(W_sf: torch.Tensor, stream=None) -> torch.Tensor:
     E, nb, kb = W_sf.shape
     out = torch.empty((E, nb, kb), dtype=torch.float32, device=W_sf.device)
     check(load().moe_weight_scales_f32(E, nb * 128, kb * 128, ptr(W_sf), ptr(out),
-                                       stream_ptr(stream)), "moe_weight_scales_f32")
+                                       _ordered(stream)), "moe_weight_scales_f32")
     return out
 
 
@@ -249,7 +265,7 @@ def pack_weight_scales(W_sf: torch.Tensor, stream=None) -> torch.Tensor:
     nbytes = L.moe_packed_scale_bytes(E, nb * 128, kb * 128)
     out = torch.empty(nbytes, dtype=torch.uint8, device=W_sf.device)
     check(L.moe_pack_weight_scales(E, nb * 128, kb * 128, ptr(W_sf), ptr(out),
-                                   stream_ptr(stream)), "moe_pack_weight_scales")
+                                   _ordered(stream)), "moe_pack_weight_scales")
     return out
 
 
@@ -264,7 +280,7 @@ def pack_weight_scales_tiled(W_sf: torch.Tensor, tile_n: int = 224, stream=None)
         raise ValueError(f"no {tile_n}-row tiles for n={nb * 128}")
     out = torch.empty(nbytes, dtype=torch.uint8, device=W_sf.device)
     check(L.moe_pack_weight_scales_tiled(E, nb * 128, kb * 128, tile_n, ptr(W_sf), ptr(out),
-                                         stream_ptr(stream)), "moe_pack_weight_scales_tiled")
+                                         _ordered(stream)), "moe_pack_weight_scales_tiled")
     return out
 
 
@@ -302,7 +318,8 @@ def grouped_gemm_fp8(op: int, A: torch.Tensor, A_sf: torch.Tensor, W: torch.Tens
     if combine is not None:
         fc = _fused_combine_args(**combine)
         g.combine = ctypes.pointer(fc)
-    check(load().moe_grouped_gemm_fp8(ctypes.byref(g), stream_ptr(stream)), "moe_grouped_gemm_fp8")
+    check(load().moe_grouped_gemm_fp8(ctypes.byref(g), _ordered(stream, st)),
+          "moe_grouped_gemm_fp8")
     return (out, out_sf) if op == GEMM_GATEUP_SWIGLU else out
 
 
@@ -323,7 +340,7 @@ def fused_combine_prep(row_of: torch.Tensor, topk_w: torch.Tensor, src_of: torch
     """moe_fused_combine_prep: the pending counts of a fused-combine DOWN GEMM (and
     zeros in out for tokens without rows).  out bf16 [B][H], pending int32 [B][H/128]."""
     fc = _fused_combine_args(row_of, topk_w, src_of, pending, out, shared_row0)
-    check(load().moe_fused_combine_prep(ctypes.byref(fc), out.shape[1], stream_ptr(stream)),
+    check(load().moe_fused_combine_prep(ctypes.byref(fc), out.shape[1], _ordered(stream)),
           "moe_fused_combine_prep")
 
 
@@ -348,7 +365,7 @@ def combine(Y: torch.Tensor, row_of: torch.Tensor, topk_w: torch.Tensor,
                     shared_row0)
     st = status if status is not None else new_status(Y.device)
     check(load().moe_combine(ctypes.byref(cc), ptr(Y), ptr(row_of), ptr(topk_w), ptr(shared),
-                             ptr(out), ptr(st), stream_ptr(stream)), "moe_combine")
+                             ptr(out), ptr(st), _ordered(stream, st)), "moe_combine")
     return out
 
 
@@ -470,12 +487,20 @@ class MoELayer:
         self.phys2log.copy_(torch.from_numpy(p2l))
 
     def forward(self, x: torch.Tensor | None = None, stream=None, events=None) -> torch.Tensor:
-        """Runs the layer on self.x (copied from ``x`` first when given).
+        """Runs the layer on self.x (copied from ``x`` first when given) on ``stream``
+        (default: the current stream).  The copy is ordered after the caller's current
+        stream and runs on ``stream``, ahead of the layer.
 
         ``events``: optional list of moe_layer.events torch.cuda.Event recorded at the
         stage boundaries."""
         if x is not None:
-            self.x.copy_(x)
+            cur = torch.cuda.current_stream(self.x.device)
+            s = stream if stream is not None else cur
+            if s != cur:
+                s.wait_stream(cur)      # x was produced on the caller's stream
+                x.record_stream(s)
+            with torch.cuda.stream(s):
+                self.x.copy_(x)
         keep = None
         if events is not None:
             keep = (ctypes.c_void_p * _lib.LAYER_EVENTS)(*[e.cuda_event for e in events])

@@ -3,7 +3,8 @@ oracle: routing of every token bit for bit; every row of several whole experts (
 hottest, one whose odd last tile holds at most 64 rows, one whose odd last tile holds
 more, the one with the fewest rows) and of the shared expert over at least 256 tokens,
 each against the oracle's FFN on the oracle's own dispatched rows; and the layer output
-of 64 tokens.  The oracle's FFN is fp64 NumPy and costs about a second per expert
+of 64 tokens; then the same layer twice more, every byte of Y and of the output equal to
+the first run's.  The oracle's FFN is fp64 NumPy and costs about a second per expert
 (dequantising its weights), so the 64 tokens are chosen to share experts."""
 import numpy as np
 import pytest
@@ -70,9 +71,11 @@ def test_full_layer_experts_and_tokens(dev, dsv3_dev, name):
         emap = oracle.eplb_build_map(oracle.expert_counts(idx, cfg.N), cfg.N, cfg.N_phys)
         l2p, rep, p2l = emap
     lay = api.MoELayer(cfg, to_dev(W), to_dev(bias), wdev, eplb_map=emap)
-    out = bits(lay.forward(bf16_dev(x)))
+    out_dev = lay.forward(bf16_dev(x)).clone()
     torch.cuda.synchronize()
     assert api.read_status(lay.status) == 0
+    out = bits(out_dev)
+    Y_dev = lay.Y.clone()
 
     # routing and dispatch, every token
     assert np.array_equal(lay.topk_idx.cpu().numpy(), idx)
@@ -112,3 +115,11 @@ def test_full_layer_experts_and_tokens(dev, dsv3_dev, name):
     ok, err, bound = within_tol(oracle.bf16_to_f32(out[tok]), oracle.bf16_to_f32(ref["out"]))
     assert ok, (name, "out", err, bound)
     assert np.isfinite(oracle.bf16_to_f32(out)).all()
+
+    # the launch configuration the bench times, run again: every row of Y and every
+    # output byte repeat (a race between CTAs, warps or the streams would show here)
+    for _ in range(2):
+        again = lay.forward()
+        torch.cuda.synchronize()
+        assert api.read_status(lay.status) == 0
+        assert torch.equal(again, out_dev) and torch.equal(lay.Y, Y_dev)

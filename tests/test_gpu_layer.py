@@ -356,6 +356,31 @@ def test_layer_graph_replay_matches_eager(dev, name):
     g.close()
 
 
+def test_two_layers_on_two_streams(dev):
+    """Two layers enqueued on two streams at once, three times over, give the bytes each
+    gives alone: the library keeps no device state shared between calls (tensor maps
+    travel as launch parameters, every scratch buffer is the caller's), and the input
+    copy of ``forward(x, stream=s)`` is ordered on ``s``."""
+    lays, alone = [], {}
+    for name in ("small_contig", "small_masked"):
+        cfg, x, W, bias = host_workload(name)
+        lay = api.MoELayer(cfg, to_dev(W, dev), to_dev(bias, dev),
+                           device_weights(host_experts(name), dev), device=dev)
+        xd = bf16_dev(x, dev)
+        alone[name] = lay.forward(xd).clone()
+        lays.append((name, lay, xd))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(dev) for _ in lays]
+    for rep in range(3):
+        for (name, lay, xd), s in zip(lays, streams):
+            lay.x.zero_()              # on the current stream: s orders its copy after it
+            lay.forward(xd, stream=s)
+        torch.cuda.synchronize()
+        for name, lay, _ in lays:
+            assert api.read_status(lay.status) == 0
+            assert torch.equal(lay.out, alone[name]), (name, rep)
+
+
 def test_layer_host_graph_matches_forward_host(dev):
     """A graph that includes the pinned host copies gives forward_host's bytes."""
     cfg, x, W, bias = host_workload("small_masked")
