@@ -6,6 +6,7 @@ on tiny inputs, an invariant, or a value printed by the pages.
 """
 import itertools
 import math
+import os
 from fractions import Fraction
 
 import numpy as np
@@ -88,6 +89,31 @@ def test_e4m3_encode_matches_torch_rne_in_range():
     got = oracle.e4m3_encode_array(v)
     ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(got, ref)
+
+
+def test_e4m3_encode_every_fp32_pattern():
+    """All 2^32 binary32 bit patterns: below 448 in magnitude the code is torch's
+    round-to-nearest-even cast to float8_e4m3fn; from 448 up, infinities included, it
+    saturates to the largest finite code of the same sign; NaN keeps its sign on the NaN
+    code.  (Chunks on a thread pool: the oracle's C loop runs without the GIL.)"""
+    from concurrent.futures import ThreadPoolExecutor
+    step = 1 << 22
+    base = np.arange(step, dtype=np.uint32)
+
+    def chunk(lo):
+        u = base + np.uint32(lo)
+        v = u.view(np.float32)
+        got = oracle.e4m3_encode_array(v)
+        ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        big = ~(np.abs(v) < 448)                    # |v| >= 448, infinities, NaN
+        sat = (((u >> 24).astype(np.uint8) & 0x80) |
+               np.where(np.isnan(v), 0x7F, 0x7E).astype(np.uint8))
+        return np.array_equal(got, np.where(big, sat, ref))
+
+    with ThreadPoolExecutor(min(8, os.cpu_count() or 1)) as ex:
+        bad = [lo for lo, ok in zip(range(0, 1 << 32, step),
+                                    ex.map(chunk, range(0, 1 << 32, step))) if not ok]
+    assert not bad, [hex(b) for b in bad[:4]]
 
 
 def test_e4m3_encode_brute_force_nearest_ties_even():
