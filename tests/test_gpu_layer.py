@@ -152,6 +152,52 @@ def test_dispatch_bit_exact(dev, name):
         assert np.array_equal(got_sf[: cfg.B], sf)
 
 
+def _every_finite_bf16(seed: int) -> np.ndarray:
+    """All 65280 finite bf16 patterns twice, as [128][1024]: first sorted by magnitude
+    (a 128-column block holds neighbouring magnitudes, so its scale spreads them over
+    the e4m3 range: subnormal codes, saturation at 448, scales clamped at 2^-127), then
+    shuffled (tiny values beside huge ones flush to zero); zeros pad the last row."""
+    b = np.arange(1 << 16, dtype=np.uint32)
+    fin = b[np.isfinite((b << 16).view(np.float32))]
+    mag = np.abs((fin << 16).view(np.float32))
+    v = np.concatenate([fin[np.argsort(mag, kind="stable")],
+                        np.random.default_rng(seed).permutation(fin)]).astype(np.uint16)
+    return np.concatenate([v, np.zeros(128 * 1024 - v.size, np.uint16)]).reshape(128, 1024)
+
+
+@pytest.mark.parametrize("fmt", [api.FMT_FP8, api.FMT_FP8_F32])
+def test_dispatch_quantises_every_finite_bf16(dev, fmt):
+    """Every finite bf16 value through the dispatch's quantiser, with power-of-two and
+    with binary32 scales: the routed copies' codes and scales and the shared expert's
+    token-order rows equal the oracle's bit for bit."""
+    cfg = configs.MoEConfig("bf16_all", B=128, H=1024, N=8, K=2, I=128, shared=True)
+    x = _every_finite_bf16(12)
+    t = np.arange(cfg.B)
+    idx = np.stack([t % 8, (t + 3) % 8], 1).astype(np.int32)
+    d = api.dispatch(cfg, bf16_dev(x), to_dev(idx), fmt=fmt, shared=True)
+    torch.cuda.synchronize()
+    assert api.read_status(d["status"]) == 0
+    xf = oracle.bf16_to_f32(x)
+    if fmt == api.FMT_FP8:
+        check_dispatch(cfg, x, idx, d, oracle.dispatch(x, idx, cfg))
+        q, sf = oracle.quantize_rows(xf)
+        got_sf = unpack_sf_atoms(d["As_sf"].cpu().numpy(), d["As"].shape[0], cfg.H // 128)
+        assert np.array_equal(d["As"].cpu().numpy()[: cfg.B], q)
+        assert np.array_equal(got_sf[: cfg.B], sf)
+        assert (q[:64] != 0).mean() > 0.9 and sf.min() == 0     # codes used, 2^-127 reached
+    else:
+        q, s = oracle.quantize_rows_f32(xf)
+        ro = d["row_of"].cpu().numpy()
+        tt, kk = np.nonzero(ro >= 0)
+        A = d["A"].cpu().numpy()
+        sfa = d["A_sf"].cpu().numpy().view(np.float32).reshape(d["A"].shape[0], cfg.H // 128)
+        assert np.array_equal(A[ro[tt, kk]], q[tt])
+        assert np.array_equal(sfa[ro[tt, kk]].view(np.uint32), s[tt].view(np.uint32))
+        As = d["As"].cpu().numpy()[: cfg.B]
+        Ssf = d["As_sf"].cpu().numpy().view(np.float32).reshape(-1, cfg.H // 128)[: cfg.B]
+        assert np.array_equal(As, q) and np.array_equal(Ssf.view(np.uint32), s.view(np.uint32))
+
+
 @pytest.mark.parametrize("name", ["prefill", "skew"])
 def test_dispatch_full_size(dev, name):
     """Full-size dispatch on the oracle's full routing (the oracle routes all B tokens)."""
