@@ -34,6 +34,48 @@ def test_route_bit_exact(dev, name):
     assert np.array_equal(r["counts"].cpu().numpy(), oracle.expert_counts(idx, cfg.N))
 
 
+def _tie_workload(cfg, seed):
+    """Router inputs full of exact ties: W repeats 16 distinct rows (every group holds the
+    same logits), bias repeats three levels, and the batch mixes zero tokens (every logit
+    0), tokens scaled by 2^12 (sigmoid saturates to exactly 0 or 1 for most experts) and
+    plain normal tokens."""
+    rng = np.random.default_rng(seed)
+    base = (rng.standard_normal((16, cfg.H)) / np.sqrt(cfg.H)).astype(np.float32)
+    W = base[np.arange(cfg.N) % 16]
+    bias = (0.01 * (np.arange(cfg.N) % 3)).astype(np.float32)
+    xf = rng.standard_normal((cfg.B, cfg.H)).astype(np.float32)
+    xf[0::3] = 0.0
+    xf[1::3] *= 4096.0
+    x = (xf.view(np.uint32) >> 16).astype(np.uint16)      # truncate to bf16
+    return x, W, bias
+
+
+@pytest.mark.parametrize("grouped", [True, False])
+def test_route_ties_and_saturated_scores(dev, grouped):
+    """Exact ties everywhere (equal logits across experts and groups, equal biased
+    scores, sigmoid saturated to 0 or 1): the GPU's ids, weights, counts and logits equal
+    the oracle's bit for bit, so both break every tie to the lower index alike."""
+    if grouped:
+        cfg = configs.MoEConfig("ties", B=96, H=256, N=256, K=8, I=128, n_group=8,
+                                topk_group=4, score_fn=configs.SIGMOID, renorm=1,
+                                route_scale=2.5)
+    else:
+        cfg = configs.MoEConfig("ties_softmax", B=96, H=256, N=32, K=4, I=128)
+    x, W, bias = _tie_workload(cfg, 21)
+    if not grouped:
+        bias = None
+    r = api.route(cfg, bf16_dev(x), to_dev(W), to_dev(bias))
+    torch.cuda.synchronize()
+    idx, w, lg = oracle.route(x, W, bias, cfg, want_logits=True)
+    got_lg = r["logits"][: cfg.B * cfg.N * 4].view(torch.float32).cpu().numpy().reshape(cfg.B, cfg.N)
+    assert np.array_equal(got_lg.view(np.uint32), lg.view(np.uint32))
+    assert np.array_equal(r["topk_idx"].cpu().numpy(), idx)
+    assert np.array_equal(r["topk_w"].cpu().numpy().view(np.uint32), w.view(np.uint32))
+    assert np.array_equal(r["counts"].cpu().numpy(), oracle.expert_counts(idx, cfg.N))
+    assert (idx[0] == np.sort(idx[0])).all() or grouped       # all-zero token: lowest ids
+    assert len(np.unique(idx, axis=0)) < cfg.B                # ties really repeat choices
+
+
 @pytest.mark.parametrize("N,G,TG,K", [(24, 8, 3, 4), (48, 6, 2, 5), (64, 1, 1, 6)])
 def test_route_bit_exact_other_group_shapes(dev, N, G, TG, K):
     """Group shapes that do not fill whole lanes (the generic selection path)."""
