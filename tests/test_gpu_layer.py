@@ -368,6 +368,39 @@ def test_combine_bit_exact(dev, name):
     assert np.array_equal(bits(out), out_ref)
 
 
+@pytest.mark.parametrize("K", [8, 16])
+def test_combine_bit_exact_at_the_extremes(dev, K):
+    """Rows drawn from every finite bf16 pattern (subnormals to 3.39e38), weights from
+    fp32 subnormals to 1, a shared row, some ranks dropped: sums that underflow into
+    fp32 subnormals (no flush to zero), overflow to infinity, or round to bf16's largest
+    finite value or past it -- the GPU's bytes equal the oracle's."""
+    rng = np.random.default_rng(31 + K)
+    B, H, rows = 96, 512, 700
+    b = np.arange(1 << 16, dtype=np.uint32)
+    fin = b[np.isfinite((b << 16).view(np.float32))].astype(np.uint16)
+    Y = rng.choice(fin, (rows, H))
+    Y[:100] = (Y[:100] & 0x007F) | 0x7F00               # positive, exponent 2^127: sums overflow
+    Y[100:200] &= 0x807F                                # subnormal rows (exponent 0)
+    S = rng.choice(fin, (B, H))
+    S[: B // 4] = 0
+    w = rng.uniform(0, 1, (B, K)).astype(np.float32)
+    w[:, 0] = 2.0 ** rng.integers(-149, 0, B)           # down to the smallest subnormal
+    w[B // 2:, -1] = 1.0
+    row_of = rng.integers(0, rows, (B, K)).astype(np.int32)
+    row_of[B // 4: B // 2, :K // 2] = rng.integers(0, 100, (B // 4, K // 2))    # huge rows
+    row_of[B // 2: 3 * B // 4] = rng.integers(100, 200, (B // 4, K))          # subnormal
+    row_of[::7, 1] = -1                                 # dropped ranks
+    for shared in (S, None):
+        ref = oracle.combine(Y, row_of, w, shared)
+        out = api.combine(bf16_dev(Y), to_dev(row_of), to_dev(w),
+                          shared=None if shared is None else bf16_dev(shared))
+        assert np.array_equal(bits(out), ref)
+    f = oracle.bf16_to_f32(ref)                         # the cases occur (no shared row)
+    sub = (ref & 0x7F80) == 0
+    assert np.isinf(f).any() and not np.isnan(f).any()
+    assert sub.sum() > 1000 and ((ref[sub] & 0x7F) != 0).sum() > 1000
+
+
 def test_bf16_round_trip_is_exact(dev):
     cfg = configs.SMALL_CONTIG.with_(K=1)
     x = inputs.make_x(cfg)
