@@ -301,7 +301,11 @@ typedef struct moe_fused_combine {
 /* Sets pending[t][c] for the fused combine of an n-column DOWN GEMM (twice the rows the
    token has in Y: its ranks with row_of >= 0, plus its shared row) and writes zeros to
    out[t] for a token that has no row at all (moe_combine's result for it).  Enqueued on
-   `stream` after the dispatch that wrote row_of and before the GEMM. */
+   `stream` after the dispatch that wrote row_of and before the GEMM.  Reads row_of and
+   shared_row0 of fc (shared_row0 < 0: no shared row); B = 0 enqueues nothing.  Errors,
+   before any launch: fc NULL, B < 0, K < 1, n <= 0, or (B > 0) row_of, pending or out
+   NULL or out not 16-byte aligned: MOE_ERR_INVALID; K > 16 or n not a multiple of 256:
+   MOE_ERR_UNSUPPORTED. */
 int moe_fused_combine_prep(const moe_fused_combine *fc, int n, void *stream);
 
 /*
@@ -383,8 +387,8 @@ int moe_grouped_gemm_fp8(const moe_gemm_args *args, void *stream);
 /*
  * Weight scales (UE8M0 bytes W_sf [E][n/128][k/128], one per 128x128 block as in the
  * "1d2d" scaling of the "Single Batch Overlap (SBO)" PR, §3) -> SF atoms
- * [E][n/128][ceil(k/512)][512] (moe_packed_scale_bytes bytes).  One-time setup, off
- * the hot path.
+ * [E][n/128][ceil(k/512)][512] (moe_packed_scale_bytes bytes; 0 when E, n or k is not
+ * positive or n or k not a multiple of 128).  One-time setup, off the hot path.
  */
 size_t moe_packed_scale_bytes(int E, int n, int k);
 /* Weight scales of tile_n-row weight tiles (128 < tile_n <= 256, tile_n % 16 == 0,
@@ -393,16 +397,22 @@ size_t moe_packed_scale_bytes(int E, int n, int k);
    row with its own 128x128 block's scale (rows past tile_n zero):
    [E][n/tile_n][ceil(k/512)][2][512] bytes.  The DOWN GEMM with tile_n 224 reads them.  One-time setup, off the hot path. */
 size_t moe_tiled_scale_bytes(int E, int n, int k, int tile_n);
+/* Errors, before any launch: a shape moe_tiled_scale_bytes rejects (0 bytes), W_sf or
+   W_sf_tiled NULL, or W_sf_tiled not 16-byte aligned: MOE_ERR_INVALID. */
 int moe_pack_weight_scales_tiled(int E, int n, int k, int tile_n, const uint8_t *W_sf,
                                  void *W_sf_tiled, void *stream);
 /* Weight scales for scale_fmt 1: UE8M0 bytes W_sf [E][n/128][k/128] -> float
-   2^(byte - 127), same shape (exact).  One-time setup, off the hot path. */
+   2^(byte - 127), same shape (exact).  One-time setup, off the hot path.  E, n or k
+   not positive, n or k not a multiple of 128, or a NULL pointer: MOE_ERR_INVALID. */
 int moe_weight_scales_f32(int E, int n, int k, const uint8_t *W_sf, float *W_sf_f32,
                           void *stream);
 /* Bytes of the scales of an activation tensor of `rows` rows and k columns (rows and k
    multiples of 128; 0 otherwise) in format fmt: MOE_FMT_FP8, SF atoms, rows/128 *
    ceil(k/512) * 512; MOE_FMT_FP8_F32, float [rows][k/128], rows * k/128 * 4. */
 size_t moe_scale_bytes(int64_t rows, int k, int fmt);
+/* W_sf -> SF atoms (above).  Errors, before any launch: a shape moe_packed_scale_bytes
+   rejects (0 bytes), W_sf or W_sf_packed NULL, or W_sf_packed not 16-byte aligned:
+   MOE_ERR_INVALID. */
 int moe_pack_weight_scales(int E, int n, int k, const uint8_t *W_sf, void *W_sf_packed,
                            void *stream);
 
