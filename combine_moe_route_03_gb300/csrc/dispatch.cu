@@ -14,7 +14,9 @@
 //                           (t,k) (EPLB map applied), its rank among the chunk's
 //                           rows of that expert in (t,k) order, chunk histogram.
 //   dispatch_scan_kernel    one CTA: chunk bases per expert, expert counts,
-//                           segment starts, capacity check, M-tile list.
+//                           segment starts, capacity check, M-tile list and work
+//                           items (experts with several items spread evenly between
+//                           those with one).  A batch of one chunk counts here too.
 //   dispatch_scatter_kernel warps over (token, column chunk): quantise each piece of
 //                           a row once, write its K copies and their scales,
 //                           row_of / src_of.
